@@ -1,0 +1,352 @@
+"""Benchmark: GDN chunk forward throughput on B4 H16 T4096 K=V=128 bf16.
+
+One step = one chunked forward (cumulative gate, UT transform, state
+recurrence, output: gdn_chunk_fwd) over one batch of the synthetic BSND
+workload ``gdn_bsnd_bf16`` (B=4, T=4096, H=16, K=V=128, chunk 64, scalar
+gate, scale K^-1/2). Inputs are resident in HBM before the timed region and
+rotate over 4 copies (4 x 65.5 MB, above the 129 MB L2) so that no step reads
+its inputs from L2. N > 1 (torchrun) runs one independent replica per GPU:
+heads are independent, there is no collective on the data path (weak scaling).
+
+``--impl reference`` times the CPU oracle (fp64 token recurrence, all host
+cores) on a bounded sample of the same workload and prints the same line.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "GDN chunk fwd tokens/s & TFLOP/s (B4 H16 T4096 K=V=128 bf16), % roofline"
+WORKLOAD = dict(workload="gdn_bsnd_bf16", B=4, T=4096, H=16, K=128, V=128, chunk=64,
+                layout="BSND", gate="scalar per head", dtype_in="bf16", state="fp32")
+# algorithmic work per (token, head): flops of the chunk algorithm (KK^T, QK^T and w:
+# 3*2C^2K; u and A_qk v_new: 2*2C^2V; w h, kg^T v_new, q h: 3*2CKV, per 64 tokens)
+FLOP_PER_TOKEN_HEAD = 180224
+# bytes per (token, head): q, k, v, o bf16 (4 x 256) + g fp32 (4) + beta bf16 (2)
+BYTES_PER_TOKEN_HEAD = 1030
+STATE_BYTES = 128 * 128 * 4  # final state per head, fp32
+ROTATE = 4
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as fh:
+            d = json.load(fh)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
+    except Exception:
+        return 6800.0, 1900.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.t0 = self.t1 = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def mark(self, which):
+        setattr(self, which, time.time())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out = ""
+        rows = []
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 10:
+                continue
+            try:
+                ts = time.mktime(time.strptime(parts[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
+            except Exception:
+                ts = None
+            rows.append((ts, parts))
+        inside = [p for ts, p in rows if ts is not None and self.t0 is not None
+                  and self.t0 - 1 <= ts <= self.t1 + 1]
+        use = inside or [p for _, p in rows]
+        sm = [float(p[2]) for p in use if p[2].replace(".", "").isdigit()]
+        mx = [float(p[3]) for p in use if p[3].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for p in use for i in range(4) if "Active" in p[6 + i]
+                          and "Not" not in p[6 + i]})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(use), "samples_in_timed_region": len(inside)}
+
+
+def _dist():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def oracle_sample(inp, heads, n_threads=None):
+    """Run the CPU oracle on the listed (b, h) pairs; returns seconds."""
+    from oracle import recurrence as R
+    t0 = time.perf_counter()
+    for b, h in heads:
+        sl = lambda x: x[b:b + 1, :, h:h + 1]  # noqa: E731
+        R.forward(sl(inp.q), sl(inp.k), sl(inp.v), sl(inp.g), sl(inp.beta), n_threads=n_threads)
+    return time.perf_counter() - t0
+
+
+def oracle_batch(inp, n_threads):
+    """The oracle on the whole workload at once (threads over all heads); seconds."""
+    from oracle import recurrence as R
+    t0 = time.perf_counter()
+    R.forward(inp.q, inp.k, inp.v, inp.g, inp.beta, n_threads=n_threads)
+    return time.perf_counter() - t0
+
+
+def run_reference(args):
+    world, rank, _ = _dist()
+    if rank != 0:
+        return 0
+    from gated_delta_rule_28_gb300 import workloads
+    from oracle import recurrence as R
+    inp = workloads.make(2)
+    cores = os.cpu_count() or 1
+    R.build()
+    # each step: 8 of the 64 (batch, head) pairs, all host cores
+    # (the oracle threads over heads: 8 heads x 4096 tokens per step)
+    sub = workloads.Inputs(**{**inp.__dict__})
+    pairs = [(b, h) for b in range(4) for h in range(16)]
+    per_step = 8
+    threads = min(cores, per_step)
+
+    def step(i):
+        sel = [pairs[(i * per_step + j) % 64] for j in range(per_step)]
+        bsel = sorted({b for b, _ in sel})
+        t0 = time.perf_counter()
+        for b in bsel:
+            hs = [h for bb, h in sel if bb == b]
+            s = lambda x: np.ascontiguousarray(x[b:b + 1][:, :, hs])  # noqa: E731
+            R.forward(s(sub.q), s(sub.k), s(sub.v), s(sub.g), s(sub.beta), n_threads=threads)
+        return time.perf_counter() - t0
+
+    for i in range(args.warmup):
+        step(i)
+    t = sum(step(args.warmup + i) for i in range(args.steps))
+    token_heads = args.steps * per_step * 4096
+    value = token_heads / 16 / t  # full-forward tokens/s equivalent (16 heads per token)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * t / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": WORKLOAD,
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+                         "sample": f"{per_step} of 64 (batch, head) pairs x 4096 tokens per step"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args):
+    import torch
+    from gated_delta_rule_28_gb300 import binding as Bd, build as gbuild, workloads
+
+    world, rank, local = _dist()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    else:
+        torch.cuda.set_device(0)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    gbuild.build()
+    Bd.load()
+
+    inp = workloads.make(2)
+    Bsz, T, H, K, V = 4, 4096, 16, 128, 128
+    tokens = Bsz * T
+    t = lambda x, dt=torch.bfloat16: torch.from_numpy(np.ascontiguousarray(x)).to(dev, dt)  # noqa: E731
+    sets = []
+    for r in range(ROTATE):
+        sets.append(dict(q=t(inp.q), k=t(inp.k), v=t(inp.v), g=t(inp.g, torch.float32),
+                         beta=t(inp.beta), o=torch.empty((Bsz, T, H, V), device=dev, dtype=torch.bfloat16),
+                         ht=torch.empty((Bsz, H, K, V), device=dev, dtype=torch.float32)))
+    p = Bd.make_problem(Bsz, T, H, K, V, dtype=Bd.GDN_DTYPE_BF16)
+    nws = Bd.gdn_chunk_fwd_workspace(p)
+    ws = torch.empty(max(nws, 1), device=dev, dtype=torch.uint8)
+    stream = torch.cuda.Stream(device=dev)
+    sp = stream.cuda_stream
+
+    def launch(i):
+        s = sets[i % ROTATE]
+        Bd.gdn_chunk_fwd(p, s["q"], s["k"], s["v"], s["g"], s["beta"], None, s["o"], s["ht"],
+                         None, None, None, ws, nws, sp)
+
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            launch(i)
+    stream.synchronize()
+    Bd.gdn_device_status(sp)
+
+    sampler = ClockSampler(dev.index)
+    sampler.start()
+    time.sleep(0.5)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    sampler.mark("t0")
+    with torch.cuda.stream(stream):
+        start.record(stream)
+        for i in range(args.steps):
+            ev[i][0].record(stream)
+            launch(args.warmup + i)
+            ev[i][1].record(stream)
+        end.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    sampler.mark("t1")
+    clocks = sampler.stop()
+    Bd.gdn_device_status(sp)
+    elapsed = start.elapsed_time(end) / 1e3
+    kern = [a.elapsed_time(b) / 1e3 for a, b in ev]
+    if world > 1:
+        tt = torch.tensor([elapsed], device=dev)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        elapsed = float(tt.item())
+    value = world * tokens * args.steps / elapsed
+    kavg = sum(kern) / len(kern)
+
+    # end to end through the C ABI with host buffers: pinned inputs copied in,
+    # the output and final state copied out, every step
+    hq, hk, hv = (torch.from_numpy(x).to(torch.bfloat16).pin_memory() for x in (inp.q, inp.k, inp.v))
+    hg = torch.from_numpy(inp.g).pin_memory()
+    hb = torch.from_numpy(inp.beta).to(torch.bfloat16).pin_memory()
+    ho = torch.empty((Bsz, T, H, V), dtype=torch.bfloat16).pin_memory()
+    hht = torch.empty((Bsz, H, K, V), dtype=torch.float32).pin_memory()
+    s0 = sets[0]
+    h2d = sum(x.numel() * x.element_size() for x in (hq, hk, hv, hg, hb))
+    d2h = ho.numel() * ho.element_size() + hht.numel() * hht.element_size()
+
+    def e2e_step():
+        for src, dst in ((hq, "q"), (hk, "k"), (hv, "v"), (hg, "g"), (hb, "beta")):
+            s0[dst].copy_(src, non_blocking=True)
+        Bd.gdn_chunk_fwd(p, s0["q"], s0["k"], s0["v"], s0["g"], s0["beta"], None, s0["o"],
+                         s0["ht"], None, None, None, ws, nws, sp)
+        ho.copy_(s0["o"], non_blocking=True)
+        hht.copy_(s0["ht"], non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(max(1, args.warmup)):
+            e2e_step()
+        stream.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_t = e0.elapsed_time(e1) / 1e3
+    if world > 1:
+        tt = torch.tensor([e2e_t], device=dev)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        e2e_t = float(tt.item())
+    e2e_value = world * tokens * args.steps / e2e_t
+
+    hbm, tc, src = _peaks()
+    alg_bytes = Bsz * T * H * BYTES_PER_TOKEN_HEAD + Bsz * H * STATE_BYTES
+    flops = Bsz * T * H * FLOP_PER_TOKEN_HEAD
+    achieved = alg_bytes / kavg / 1e9
+    traffic = None
+    tpath = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(tpath):
+        try:
+            traffic = json.load(open(tpath)).get("gdn_bsnd_bf16_fwd")
+        except Exception:
+            traffic = None
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        from oracle import recurrence as R
+        R.build()
+        cores = os.cpu_count() or 1
+        # bounded sample: 16 of the 64 (batch, head) pairs, threads over heads
+        sub = lambda x: np.ascontiguousarray(x[:, :, :4])  # noqa: E731
+        t0 = time.perf_counter()
+        R.forward(sub(inp.q), sub(inp.k), sub(inp.v), sub(inp.g), sub(inp.beta), n_threads=cores)
+        ct = time.perf_counter() - t0
+        cpu = {"value": (Bsz * T * 4) / 16 / ct, "unit": "tokens/s", "cores": min(cores, 16),
+               "kind": "oracle",
+               "sample": "16 of 64 (batch, head) pairs (all batches, heads 0-3) x 4096 tokens, "
+                         "fp64 token recurrence, tokens/s scaled to 16 heads"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * elapsed / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "config": {**WORKLOAD, "l2": f"inputs larger than L2: {ROTATE} rotating input sets"},
+            "tflops": flops / kavg / 1e12,
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                         "frac": achieved / hbm, "traffic": traffic, "peak_source": src,
+                         "kernel": "gdn_chunk_fwd", "alg_bytes_per_launch": alg_bytes,
+                         "kernel_ms": 1e3 * kavg,
+                         "tensor_frac": flops / kavg / 1e12 / tc},
+            "cpu_baseline": cpu,
+            "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h},
+            "clocks": clocks,
+            "gpu_launches": args.steps,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,136 @@
+"""Tensor-level entry points over the C ABI.
+
+These allocate outputs and workspace with PyTorch (device memory and the
+current stream are the only things PyTorch provides here), derive the packed
+metadata with ``gdn_prepare_varlen`` and call the library. Every arithmetic
+step runs in the library's CUDA kernels.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+from . import binding as B
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return B.GDN_DTYPE_BF16
+    if t.dtype == torch.float32:
+        return B.GDN_DTYPE_F32
+    raise TypeError(f"q/k/v must be bfloat16 or float32, got {t.dtype}")
+
+
+class Varlen:
+    """Validated packed-document metadata on the device (int32 offsets and chunk pairs)."""
+
+    def __init__(self, cu_seqlens, total_tokens: int, device):
+        cu = np.asarray(cu_seqlens.cpu() if isinstance(cu_seqlens, torch.Tensor) else cu_seqlens,
+                        dtype=np.int64)
+        idx, n = B.gdn_prepare_varlen(cu, total_tokens)
+        self.num_seqs = len(cu) - 1
+        self.num_chunks = n
+        self.cu = torch.from_numpy(cu.astype(np.int32)).to(device)
+        self.chunk_indices = torch.from_numpy(np.ascontiguousarray(idx)).to(device)
+        self.chunk_indices_host = idx
+
+
+def problem_for(q, v, g, *, scale=None, use_exp2=False, varlen: Varlen | None = None,
+                use_qk_l2norm=False, segment_len=0):
+    packed = varlen is not None
+    if packed:
+        if q.ndim != 3:
+            raise ValueError("packed inputs must be [T, H, K]")
+        Bsz, T, H, K = 1, q.shape[0], q.shape[1], q.shape[2]
+    else:
+        if q.ndim != 4:
+            raise ValueError("inputs must be [B, T, H, K]")
+        Bsz, T, H, K = q.shape
+    per_key = g.ndim == q.ndim
+    return B.make_problem(
+        Bsz, T, H, K, v.shape[-1], layout=B.GDN_LAYOUT_TND if packed else B.GDN_LAYOUT_BSND,
+        gate_kind=B.GDN_GATE_PER_KEY if per_key else B.GDN_GATE_SCALAR, dtype=_dtype_code(q),
+        use_exp2=use_exp2, scale=0.0 if scale is None else scale, use_qk_l2norm=use_qk_l2norm,
+        cu_seqlens=varlen.cu if packed else None, num_seqs=varlen.num_seqs if packed else 0,
+        chunk_indices=varlen.chunk_indices if packed else None,
+        num_chunks=varlen.num_chunks if packed else 0, segment_len=segment_len)
+
+
+def chunk_gated_delta_rule_fwd(q, k, v, g, beta, *, h0=None, scale=None, use_exp2=False,
+                               cu_seqlens=None, varlen=None, output_final_state=True,
+                               return_g_cumsum=False, return_A=False, return_h_chunks=False,
+                               use_qk_l2norm=False, segment_len=0, stream=None):
+    """Chunked forward; returns a dict with o and, as requested, ht, g_cumsum, A, h_chunks."""
+    if cu_seqlens is not None and varlen is None:
+        varlen = Varlen(cu_seqlens, q.shape[0], q.device)
+    p = problem_for(q, v, g, scale=scale, use_exp2=use_exp2, varlen=varlen,
+                    use_qk_l2norm=use_qk_l2norm, segment_len=segment_len)
+    dev = q.device
+    out = {"o": torch.empty_like(v)}
+    nstate = varlen.num_seqs if varlen is not None else p.B
+    if output_final_state:
+        out["ht"] = torch.empty((nstate, p.H, p.K, p.V), device=dev, dtype=torch.float32)
+    if return_g_cumsum:
+        out["g_cumsum"] = torch.empty_like(g, dtype=torch.float32)
+    if return_A:
+        out["A"] = torch.empty(q.shape[:-1] + (64,), device=dev, dtype=torch.float32)
+    if return_h_chunks:
+        if varlen is not None:
+            shape = (varlen.num_chunks, p.H, p.K, p.V)
+        else:
+            shape = (p.B, p.H, -(-p.T // 64), p.K, p.V)
+        out["h_chunks"] = torch.empty(shape, device=dev, dtype=torch.float32)
+    nws = B.gdn_chunk_fwd_workspace(p)
+    ws = torch.empty(nws, device=dev, dtype=torch.uint8) if nws else None
+    B.gdn_chunk_fwd(p, q, k, v, g, beta, h0, out["o"], out.get("ht"), out.get("g_cumsum"),
+                    out.get("A"), out.get("h_chunks"), ws, nws, stream)
+    return out
+
+
+def chunk_gated_delta_rule_bwd(q, k, v, g_cumsum, beta, A, dO, *, h0=None, dht=None, scale=None,
+                               use_exp2=False, cu_seqlens=None, varlen=None, stream=None):
+    """Chunked backward; returns dq, dk, dv, dbeta, dg (raw gate) and dh0."""
+    if cu_seqlens is not None and varlen is None:
+        varlen = Varlen(cu_seqlens, q.shape[0], q.device)
+    p = problem_for(q, v, g_cumsum, scale=scale, use_exp2=use_exp2, varlen=varlen)
+    nstate = varlen.num_seqs if varlen is not None else p.B
+    out = dict(dq=torch.empty_like(q), dk=torch.empty_like(k), dv=torch.empty_like(v),
+               dbeta=torch.empty_like(beta), dg=torch.empty_like(g_cumsum),
+               dh0=torch.empty((nstate, p.H, p.K, p.V), device=q.device, dtype=torch.float32))
+    nws = B.gdn_chunk_bwd_workspace(p)
+    ws = torch.empty(nws, device=q.device, dtype=torch.uint8) if nws else None
+    B.gdn_chunk_bwd(p, q, k, v, g_cumsum, beta, A, dO, h0, dht, out["dq"], out["dk"], out["dv"],
+                    out["dg"], out["dbeta"], out["dh0"], ws, nws, stream)
+    return out
+
+
+def segment_summary(k, v, g, beta, segment_len, *, use_exp2=False, stream=None):
+    """(S_ext [B,H,nseg,K,V], M [B,H,nseg,K,K]) for every segment of ``segment_len`` tokens."""
+    p = problem_for(k, v, g, use_exp2=use_exp2)
+    nseg = -(-p.T // segment_len)
+    S = torch.empty((p.B, p.H, nseg, p.K, p.V), device=k.device, dtype=torch.float32)
+    M = torch.empty((p.B, p.H, nseg, p.K, p.K), device=k.device, dtype=torch.float32)
+    B.kda_segment_summary(p, k, v, g, beta, segment_len, S, M, None, 0, stream)
+    return S, M
+
+
+def segment_merge(S_ext, M, h0=None, stream=None):
+    """(S_init [B,H,nseg,K,V], ht [B,H,K,V]): ordered composition of the summaries."""
+    Bsz, H, nseg, K, V = S_ext.shape
+    p = B.make_problem(Bsz, nseg * 64, H, K, V, dtype=B.GDN_DTYPE_F32)
+    S_init = torch.empty_like(S_ext)
+    ht = torch.empty((Bsz, H, K, V), device=S_ext.device, dtype=torch.float32)
+    B.kda_segment_merge(p, S_ext, M, nseg, h0, S_init, ht, stream)
+    return S_init, ht
+
+
+def split_forward(q, k, v, g, beta, segment_len, *, h0=None, scale=None, use_exp2=False,
+                  return_h_chunks=False, stream=None):
+    """Long-sequence forward split across SMs: summaries, merge, corrected run."""
+    S, M = segment_summary(k, v, g, beta, segment_len, use_exp2=use_exp2, stream=stream)
+    S_init, _ = segment_merge(S, M, h0, stream=stream)
+    out = chunk_gated_delta_rule_fwd(q, k, v, g, beta, h0=S_init, scale=scale, use_exp2=use_exp2,
+                                     segment_len=segment_len, return_h_chunks=return_h_chunks,
+                                     stream=stream)
+    out.update(S_ext=S, M=M, S_init=S_init)
+    return out

@@ -1,0 +1,740 @@
+// fp32 SIMT backward of the chunked gated delta rule (sm_103a).
+//
+// Three stages, as the pages' backward is staged (KDA adapter backward on the
+// hyper-parallel "Diff Coverage" page: bwd_prepare -> bwd_dhu -> bwd_finalize;
+// the GDN adapter's chunk_gated_delta_rule_bwd consumes q, k, v, g_cumsum,
+// beta, A and dO):
+//  1. entry state h_c of every chunk, recomputed by the forward chunk kernel
+//     from the saved g_cumsum and A (launched by the API, not here);
+//  2. dhu: the reverse state recurrence, per (run, head, 32 state columns),
+//        dv_new_c = kgl_c dh_{c+1} + scale A_qk^T dO_c
+//        dh_c     = Diag(base^G_last) dh_{c+1} + scale Qg^T dO_c - w_c^T dv_new_c
+//     (the reverse loop of state_summary.py kda_state_grad_ext_kernel), with
+//     w_c^T dv_new = Kg^T beta (X^T dv_new); it stores dh_{c+1} per chunk and
+//     dv_new, and returns dh_0;
+//  3. local: per (chunk, head), with the whole value width, the adjoint of the
+//     chunk's UT transform, gates and Gram matrices, giving dq, dk, dv, dbeta
+//     and dg (reverse in-chunk cumulative sum: the gradient of the raw gate).
+#include "common.cuh"
+#include "kernels.h"
+
+namespace gdn {
+namespace {
+
+constexpr int NTH = 256;
+constexpr int KP = GDN_DK + 1;
+constexpr int CP = GDN_CHUNK + 1;
+
+// ---------------------------------------------------------------------------
+// run / chunk bookkeeping shared by both kernels
+struct Run {
+  int64_t r0, r1, chunk_base;
+  int state_idx, b;
+  bool ok;
+};
+
+__device__ Run run_of(const BwdArgs &a, int z) {
+  Run r{};
+  r.ok = true;
+  if (a.cu) {
+    r.r0 = a.cu[z];
+    r.r1 = a.cu[z + 1];
+    r.ok = r.r0 >= 0 && r.r1 > r.r0 && r.r1 <= a.T;
+    r.chunk_base = 0;
+    if (r.ok) {
+      for (int m = 0; m < z; ++m) r.chunk_base += (a.cu[m + 1] - a.cu[m] + GDN_CHUNK - 1) / GDN_CHUNK;
+      r.ok = r.chunk_base + (r.r1 - r.r0 + GDN_CHUNK - 1) / GDN_CHUNK <= a.num_chunks;
+    }
+    r.state_idx = z;
+    r.b = 0;
+  } else {
+    r.b = z;
+    r.r0 = (int64_t)z * a.T;
+    r.r1 = r.r0 + a.T;
+    r.chunk_base = 0;
+    r.state_idx = z;
+  }
+  return r;
+}
+
+__device__ __forceinline__ int64_t chunk_slot(const BwdArgs &a, const Run &r, int64_t ci, int h) {
+  const int NT = (a.T + GDN_CHUNK - 1) / GDN_CHUNK;
+  return a.cu ? (r.chunk_base + ci) * a.H + h : ((int64_t)r.b * a.H + h) * NT + ci;
+}
+
+// ---------------------------------------------------------------------------
+// dhu: reverse state recurrence
+constexpr int DBV = 32;
+constexpr int DVP = DBV + 1;
+
+template <bool PER_KEY>
+constexpr size_t dhu_smem_floats() {
+  return 3 * 64 * KP + (PER_KEY ? 64 * KP : 64) + 2 * 64 * CP + 128 * DVP + 3 * 64 * DVP + 64 + 128;
+}
+
+template <typename T, bool PER_KEY>
+__global__ void __launch_bounds__(NTH) dhu_kernel(BwdArgs a) {
+  extern __shared__ float smem[];
+  float *sKl = smem;                        // K (.) base^(G_last - G)
+  float *sQg = sKl + 64 * KP;               // scale Q (.) base^G
+  float *sKg = sQg + 64 * KP;               // K (.) base^G
+  float *sG = sKg + 64 * KP;                // cumulative gate
+  float *sX = sG + (PER_KEY ? 64 * KP : 64);
+  float *sAqk = sX + 64 * CP;
+  float *sDH = sAqk + 64 * CP;              // [128][DVP]
+  float *sDO = sDH + 128 * DVP;             // [64][DVP]
+  float *sDD = sDO + 64 * DVP;              // dv_new slice
+  float *sDY = sDD + 64 * DVP;              // -beta X^T dv_new
+  float *sBeta = sDY + 64 * DVP;
+  float *sEL = sBeta + 64;
+
+  const int tid = threadIdx.x, H = a.H, h = blockIdx.y, z = blockIdx.z;
+  const int col0 = blockIdx.x * DBV;
+  const bool e2 = a.use_exp2 != 0;
+  const T *q = static_cast<const T *>(a.q);
+  const T *k = static_cast<const T *>(a.k);
+  const T *beta = static_cast<const T *>(a.beta);
+  const T *dO = static_cast<const T *>(a.dO);
+  const Run run = run_of(a, z);
+  if (!run.ok) {
+    if (tid == 0) raise_device_flag(a.dev_flag, kDevCheck);
+    return;
+  }
+  const int64_t KV = (int64_t)GDN_DK * GDN_DV;
+  for (int idx = tid; idx < 128 * DBV; idx += NTH) {
+    const int d = idx / DBV, c = idx % DBV;
+    sDH[d * DVP + c] = a.dht ? a.dht[((int64_t)run.state_idx * H + h) * KV + d * GDN_DV + col0 + c] : 0.f;
+  }
+  __syncthreads();
+  const int64_t nchunks = (run.r1 - run.r0 + GDN_CHUNK - 1) / GDN_CHUNK;
+  for (int64_t ci = nchunks - 1; ci >= 0; --ci) {
+    const int64_t c0 = run.r0 + ci * GDN_CHUNK;
+    const int n = (int)min((int64_t)GDN_CHUNK, run.r1 - c0);
+    {  // gradient of this chunk's exit state
+      float *dst = a.dh_chunks + chunk_slot(a, run, ci, h) * KV;
+      for (int idx = tid; idx < 128 * DBV; idx += NTH) {
+        const int d = idx / DBV, c = idx % DBV;
+        dst[d * GDN_DV + col0 + c] = sDH[d * DVP + c];
+      }
+    }
+    for (int idx = tid; idx < 64 * GDN_DK; idx += NTH) {
+      const int i = idx >> 7, d = idx & 127;
+      float kv = 0.f, qv = 0.f, gv = 0.f;
+      if (i < n) {
+        const int64_t off = ((c0 + i) * H + h) * GDN_DK + d;
+        kv = to_f32(k[off]);
+        qv = to_f32(q[off]);
+        if (PER_KEY) gv = a.g_cumsum[off];
+      }
+      sKl[i * KP + d] = kv;
+      sQg[i * KP + d] = qv;
+      if (PER_KEY) sG[i * KP + d] = gv;
+    }
+    for (int idx = tid; idx < 64 * DBV; idx += NTH) {
+      const int i = idx / DBV, c = idx % DBV;
+      sDO[i * DVP + c] = i < n ? to_f32(dO[((c0 + i) * H + h) * GDN_DV + col0 + c]) : 0.f;
+    }
+    for (int idx = tid; idx < 64 * 64; idx += NTH) {
+      const int i = idx >> 6, j = idx & 63;
+      sX[i * CP + j] = (i < n && j < n) ? a.A[((c0 + i) * H + h) * GDN_CHUNK + j] : (i == j ? 1.f : 0.f);
+    }
+    if (tid < 64) {
+      sBeta[tid] = tid < n ? to_f32(beta[(c0 + tid) * H + h]) : 0.f;
+      if (!PER_KEY) sG[tid] = a.g_cumsum[(c0 + min(tid, n - 1)) * H + h];
+    }
+    __syncthreads();
+    if (PER_KEY) {  // rows past the end hold the last valid cumulative gate
+      for (int idx = tid; idx < (64 - n) * GDN_DK; idx += NTH) {
+        const int i = n + idx / GDN_DK, d = idx % GDN_DK;
+        sG[i * KP + d] = sG[(n - 1) * KP + d];
+      }
+      __syncthreads();
+    }
+    // A_qk = lower-incl(Q K^T (.) Gamma)
+    {
+      int m0, n0;
+      tile_origin<64, 64, 4, 4>(tid, m0, n0);
+      float acc[4][4];
+      zero_acc(acc);
+      if (n0 <= m0 + 3) {
+        if (PER_KEY) {
+          for (int d = 0; d < GDN_DK; ++d) {
+#pragma unroll
+            for (int x = 0; x < 4; ++x)
+#pragma unroll
+              for (int y = 0; y < 4; ++y) {
+                if (n0 + y > m0 + x) continue;
+                acc[x][y] = fmaf(sQg[(m0 + x) * KP + d] * sKl[(n0 + y) * KP + d],
+                                 gate_pow(sG[(m0 + x) * KP + d] - sG[(n0 + y) * KP + d], e2), acc[x][y]);
+              }
+          }
+        } else {
+          auto fq = [&](int m, int kk) { return sQg[m * KP + kk]; };
+          auto fkt = [&](int kk, int nn) { return sKl[nn * KP + kk]; };
+          mm_acc<64, 64, GDN_DK, 4, 4>(fq, fkt, acc, tid);
+#pragma unroll
+          for (int x = 0; x < 4; ++x)
+#pragma unroll
+            for (int y = 0; y < 4; ++y) acc[x][y] *= gate_pow(sG[m0 + x] - sG[n0 + y], e2);
+        }
+      }
+#pragma unroll
+      for (int x = 0; x < 4; ++x)
+#pragma unroll
+        for (int y = 0; y < 4; ++y) sAqk[(m0 + x) * CP + n0 + y] = (n0 + y <= m0 + x) ? acc[x][y] : 0.f;
+    }
+    __syncthreads();
+    for (int idx = tid; idx < 64 * GDN_DK; idx += NTH) {
+      const int i = idx >> 7, d = idx & 127;
+      const float Gi = PER_KEY ? sG[i * KP + d] : sG[i];
+      const float Gl = PER_KEY ? sG[63 * KP + d] : sG[63];
+      const float kk = sKl[i * KP + d];
+      sKg[i * KP + d] = kk * gate_pow(Gi, e2);
+      sQg[i * KP + d] *= a.scale * gate_pow(Gi, e2);
+      sKl[i * KP + d] = kk * gate_pow(Gl - Gi, e2);
+    }
+    if (tid < GDN_DK) sEL[tid] = gate_pow(PER_KEY ? sG[63 * KP + tid] : sG[63], e2);
+    __syncthreads();
+    // dv_new = kgl dh + scale A_qk^T dO
+    {
+      float acc[2][4];
+      zero_acc(acc);
+      auto fa = [&](int m, int kk) { return sKl[m * KP + kk]; };
+      auto fb = [&](int kk, int nn) { return sDH[kk * DVP + nn]; };
+      mm_acc<64, DBV, GDN_DK, 2, 4>(fa, fb, acc, tid);
+      float acc2[2][4];
+      zero_acc(acc2);
+      auto fa2 = [&](int m, int kk) { return sAqk[kk * CP + m]; };
+      auto fb2 = [&](int kk, int nn) { return sDO[kk * DVP + nn]; };
+      mm_acc<64, DBV, GDN_CHUNK, 2, 4>(fa2, fb2, acc2, tid);
+      int m0, n0;
+      tile_origin<64, DBV, 2, 4>(tid, m0, n0);
+#pragma unroll
+      for (int x = 0; x < 2; ++x)
+#pragma unroll
+        for (int y = 0; y < 4; ++y) {
+          const float val = acc[x][y] + a.scale * acc2[x][y];
+          sDD[(m0 + x) * DVP + n0 + y] = val;
+          if (m0 + x < n) a.dvnew[((c0 + m0 + x) * H + h) * GDN_DV + col0 + n0 + y] = val;
+        }
+    }
+    __syncthreads();
+    // dY = -beta (X^T dv_new)
+    {
+      float acc[2][4];
+      zero_acc(acc);
+      auto fa = [&](int m, int kk) { return sX[kk * CP + m]; };
+      auto fb = [&](int kk, int nn) { return sDD[kk * DVP + nn]; };
+      mm_acc<64, DBV, GDN_CHUNK, 2, 4>(fa, fb, acc, tid);
+      int m0, n0;
+      tile_origin<64, DBV, 2, 4>(tid, m0, n0);
+#pragma unroll
+      for (int x = 0; x < 2; ++x)
+#pragma unroll
+        for (int y = 0; y < 4; ++y) sDY[(m0 + x) * DVP + n0 + y] = -sBeta[m0 + x] * acc[x][y];
+    }
+    __syncthreads();
+    // dh <- Diag(base^G_last) dh + Qg^T dO + Kg^T dY
+    {
+      float acc[4][4];
+      zero_acc(acc);
+      auto fa = [&](int m, int kk) { return sQg[kk * KP + m]; };
+      auto fb = [&](int kk, int nn) { return sDO[kk * DVP + nn]; };
+      mm_acc<128, DBV, GDN_CHUNK, 4, 4>(fa, fb, acc, tid);
+      auto fa2 = [&](int m, int kk) { return sKg[kk * KP + m]; };
+      auto fb2 = [&](int kk, int nn) { return sDY[kk * DVP + nn]; };
+      mm_acc<128, DBV, GDN_CHUNK, 4, 4>(fa2, fb2, acc, tid);
+      int m0, n0;
+      tile_origin<128, DBV, 4, 4>(tid, m0, n0);
+#pragma unroll
+      for (int x = 0; x < 4; ++x)
+#pragma unroll
+        for (int y = 0; y < 4; ++y) {
+          float &dh = sDH[(m0 + x) * DVP + n0 + y];
+          dh = fmaf(sEL[m0 + x], dh, acc[x][y]);
+        }
+    }
+    __syncthreads();
+  }
+  if (a.dh0) {
+    for (int idx = tid; idx < 128 * DBV; idx += NTH) {
+      const int d = idx / DBV, c = idx % DBV;
+      a.dh0[((int64_t)run.state_idx * H + h) * KV + d * GDN_DV + col0 + c] = sDH[d * DVP + c];
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// local gradients, one CTA per (chunk, head), the value width in 8 slices
+constexpr int LBV = 16;
+constexpr int LVP = LBV + 1;
+
+template <bool PER_KEY>
+constexpr size_t local_smem_floats() {
+  // K, Q, (G), X, P, Aqk, slice buffers, beta, dbeta, EL, dGLh, dGlast, dGrow
+  return 2 * 64 * KP + (PER_KEY ? 64 * KP : 64) + 3 * 64 * CP +
+         (2 * 128 * LVP + 6 * 64 * LVP) + 64 + 64 + 128 + 128 + 128 + 64;
+}
+
+template <typename T, bool PER_KEY>
+__global__ void __launch_bounds__(NTH, 1) local_kernel(BwdArgs a) {
+  extern __shared__ float smem[];
+  float *sK = smem;
+  float *sQ = sK + 64 * KP;
+  float *sG = sQ + 64 * KP;
+  float *sX = sG + (PER_KEY ? 64 * KP : 64);
+  float *sP = sX + 64 * CP;     // gated K K^T (strict lower), later dP (.) Gamma
+  float *sAqk = sP + 64 * CP;   // gated Q K^T (lower incl), later dA_qk (.) Gamma
+  float *sSl = sAqk + 64 * CP;  // slice region
+  float *sHs = sSl;                  // [128][LVP] h slice
+  float *sDHs = sHs + 128 * LVP;     // [128][LVP] dh_{c+1} slice
+  float *sVs = sDHs + 128 * LVP;     // [64][LVP]
+  float *sDOs = sVs + 64 * LVP;
+  float *sDDs = sDOs + 64 * LVP;     // dv_new slice
+  float *sZs = sDDs + 64 * LVP;      // beta (V - Kg h)
+  float *sDels = sZs + 64 * LVP;     // v_new slice
+  float *sDYs = sDels + 64 * LVP;    // -beta X^T dv_new
+  float *sBeta = sSl + 2 * 128 * LVP + 6 * 64 * LVP;
+  float *sDBeta = sBeta + 64;
+  float *sEL = sDBeta + 64;
+  float *sDGLh = sEL + 128;   // sum_c dh_{c+1} (.) h per key channel
+  float *sDGlast = sDGLh + 128;
+  float *sDGrow = sDGlast + 128;
+
+  const int tid = threadIdx.x, H = a.H, h = blockIdx.y;
+  const int64_t zc = blockIdx.x;
+  const bool e2 = a.use_exp2 != 0;
+  const float lnb = e2 ? 0.69314718055994530942f : 1.f;
+  const T *q = static_cast<const T *>(a.q);
+  const T *k = static_cast<const T *>(a.k);
+  const T *v = static_cast<const T *>(a.v);
+  const T *beta = static_cast<const T *>(a.beta);
+  const T *dO = static_cast<const T *>(a.dO);
+  T *dq = static_cast<T *>(a.dq);
+  T *dk = static_cast<T *>(a.dk);
+  T *dv = static_cast<T *>(a.dv);
+  T *dbeta = static_cast<T *>(a.dbeta);
+
+  // ---- locate the chunk --------------------------------------------------
+  int64_t c0, slot;
+  int n;
+  if (a.cu) {
+    const int seq = a.chunk_indices[2 * zc], cc = a.chunk_indices[2 * zc + 1];
+    bool ok = seq >= 0 && seq < a.num_seqs && cc >= 0;
+    if (ok) {
+      c0 = a.cu[seq] + (int64_t)cc * GDN_CHUNK;
+      ok = c0 < a.cu[seq + 1] && a.cu[seq + 1] <= a.T;
+      n = ok ? (int)min((int64_t)GDN_CHUNK, (int64_t)a.cu[seq + 1] - c0) : 0;
+    }
+    if (!ok) {
+      if (tid == 0) raise_device_flag(a.dev_flag, kDevCheck);
+      return;
+    }
+    slot = zc * H + h;
+  } else {
+    const int NT = (a.T + GDN_CHUNK - 1) / GDN_CHUNK;
+    const int b = (int)(zc / NT), cc = (int)(zc % NT);
+    c0 = (int64_t)b * a.T + (int64_t)cc * GDN_CHUNK;
+    n = min(GDN_CHUNK, a.T - cc * GDN_CHUNK);
+    slot = ((int64_t)b * H + h) * NT + cc;
+  }
+  const int64_t KV = (int64_t)GDN_DK * GDN_DV;
+  const float *hc = a.h_chunks + slot * KV;
+  const float *dhc = a.dh_chunks + slot * KV;
+
+  // ---- chunk operands ----------------------------------------------------
+  for (int idx = tid; idx < 64 * GDN_DK; idx += NTH) {
+    const int i = idx >> 7, d = idx & 127;
+    float kv = 0.f, qv = 0.f, gv = 0.f;
+    if (i < n) {
+      const int64_t off = ((c0 + i) * H + h) * GDN_DK + d;
+      kv = to_f32(k[off]);
+      qv = to_f32(q[off]);
+      if (PER_KEY) gv = a.g_cumsum[off];
+    }
+    sK[i * KP + d] = kv;
+    sQ[i * KP + d] = qv;
+    if (PER_KEY) sG[i * KP + d] = gv;
+  }
+  for (int idx = tid; idx < 64 * 64; idx += NTH) {
+    const int i = idx >> 6, j = idx & 63;
+    sX[i * CP + j] = (i < n && j < n) ? a.A[((c0 + i) * H + h) * GDN_CHUNK + j] : (i == j ? 1.f : 0.f);
+  }
+  if (tid < 64) {
+    sBeta[tid] = tid < n ? to_f32(beta[(c0 + tid) * H + h]) : 0.f;
+    sDBeta[tid] = 0.f;
+    sDGrow[tid] = 0.f;
+    if (!PER_KEY) sG[tid] = a.g_cumsum[(c0 + min(tid, n - 1)) * H + h];
+  }
+  if (tid < 128) {
+    sDGLh[tid] = 0.f;
+    sDGlast[tid] = 0.f;
+  }
+  __syncthreads();
+  if (PER_KEY) {
+    for (int idx = tid; idx < (64 - n) * GDN_DK; idx += NTH) {
+      const int i = n + idx / GDN_DK, d = idx % GDN_DK;
+      sG[i * KP + d] = sG[(n - 1) * KP + d];
+    }
+    __syncthreads();
+  }
+  auto Gv = [&](int i, int d) { return PER_KEY ? sG[i * KP + d] : sG[i]; };
+  if (tid < GDN_DK) sEL[tid] = gate_pow(Gv(63, tid), e2);
+
+  // ---- gated Gram matrices ------------------------------------------------
+  {
+    int m0, n0;
+    tile_origin<64, 64, 4, 4>(tid, m0, n0);
+    float accP[4][4], accQ[4][4];
+    zero_acc(accP);
+    zero_acc(accQ);
+    if (n0 <= m0 + 3) {
+      if (PER_KEY) {
+        for (int d = 0; d < GDN_DK; ++d) {
+#pragma unroll
+          for (int x = 0; x < 4; ++x)
+#pragma unroll
+            for (int y = 0; y < 4; ++y) {
+              if (n0 + y > m0 + x) continue;
+              const float gam = gate_pow(sG[(m0 + x) * KP + d] - sG[(n0 + y) * KP + d], e2);
+              const float kj = sK[(n0 + y) * KP + d];
+              accP[x][y] = fmaf(sK[(m0 + x) * KP + d] * kj, gam, accP[x][y]);
+              accQ[x][y] = fmaf(sQ[(m0 + x) * KP + d] * kj, gam, accQ[x][y]);
+            }
+        }
+      } else {
+        auto fk = [&](int m, int kk) { return sK[m * KP + kk]; };
+        auto fq = [&](int m, int kk) { return sQ[m * KP + kk]; };
+        auto fkt = [&](int kk, int nn) { return sK[nn * KP + kk]; };
+        mm_acc<64, 64, GDN_DK, 4, 4>(fk, fkt, accP, tid);
+        mm_acc<64, 64, GDN_DK, 4, 4>(fq, fkt, accQ, tid);
+#pragma unroll
+        for (int x = 0; x < 4; ++x)
+#pragma unroll
+          for (int y = 0; y < 4; ++y) {
+            const float gam = gate_pow(sG[m0 + x] - sG[n0 + y], e2);
+            accP[x][y] *= gam;
+            accQ[x][y] *= gam;
+          }
+      }
+    }
+#pragma unroll
+    for (int x = 0; x < 4; ++x)
+#pragma unroll
+      for (int y = 0; y < 4; ++y) {
+        const int i = m0 + x, j = n0 + y;
+        sP[i * CP + j] = j < i ? accP[x][y] : 0.f;
+        sAqk[i * CP + j] = j <= i ? accQ[x][y] : 0.f;
+      }
+  }
+  __syncthreads();
+
+  // ---- pass over value slices: accumulate the value contractions -----------
+  // register tiles: 64x64 (4x4 per thread) and 64x128 (4x8 per thread)
+  int pm0, pn0, gm0, gn0;
+  tile_origin<64, 64, 4, 4>(tid, pm0, pn0);
+  tile_origin<64, 128, 4, 8>(tid, gm0, gn0);
+  float aX[4][4], aQk[4][4], aQg[4][8], aKg[4][8], aKl[4][8];
+  zero_acc(aX);
+  zero_acc(aQk);
+  zero_acc(aQg);
+  zero_acc(aKg);
+  zero_acc(aKl);
+  for (int vs = 0; vs < GDN_DV; vs += LBV) {
+    for (int idx = tid; idx < 128 * LBV; idx += NTH) {
+      const int d = idx / LBV, c = idx % LBV;
+      sHs[d * LVP + c] = hc[d * GDN_DV + vs + c];
+      sDHs[d * LVP + c] = dhc[d * GDN_DV + vs + c];
+    }
+    for (int idx = tid; idx < 64 * LBV; idx += NTH) {
+      const int i = idx / LBV, c = idx % LBV;
+      float vv = 0.f, dov = 0.f, ddv = 0.f;
+      if (i < n) {
+        const int64_t off = ((c0 + i) * H + h) * GDN_DV + vs + c;
+        vv = to_f32(v[off]);
+        dov = to_f32(dO[off]);
+        ddv = a.dvnew[off];
+      }
+      sVs[i * LVP + c] = vv;
+      sDOs[i * LVP + c] = dov;
+      sDDs[i * LVP + c] = ddv;
+    }
+    __syncthreads();
+    // Z = beta (V - (K (.) base^G) h) ; also keep V - Y for dbeta
+    if (tid < 64 * LBV / 4) {
+      const int i = tid / (LBV / 4), c4 = (tid % (LBV / 4)) * 4;
+      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+      for (int d = 0; d < GDN_DK; ++d) {
+        const float kg = sK[i * KP + d] * gate_pow(Gv(i, d), e2);
+#pragma unroll
+        for (int y = 0; y < 4; ++y) acc[y] = fmaf(kg, sHs[d * LVP + c4 + y], acc[y]);
+      }
+#pragma unroll
+      for (int y = 0; y < 4; ++y) {
+        const float r = sVs[i * LVP + c4 + y] - acc[y];
+        sZs[i * LVP + c4 + y] = sBeta[i] * r;
+        sVs[i * LVP + c4 + y] = r;  // V - Y
+      }
+    }
+    __syncthreads();
+    // v_new = X Z ; dZ = X^T dv_new
+    if (tid < 64 * LBV / 4) {
+      const int i = tid / (LBV / 4), c4 = (tid % (LBV / 4)) * 4;
+      float acc[4] = {0.f, 0.f, 0.f, 0.f}, acc2[4] = {0.f, 0.f, 0.f, 0.f};
+      for (int j = 0; j < GDN_CHUNK; ++j) {
+        const float x = sX[i * CP + j], xt = sX[j * CP + i];
+#pragma unroll
+        for (int y = 0; y < 4; ++y) {
+          acc[y] = fmaf(x, sZs[j * LVP + c4 + y], acc[y]);
+          acc2[y] = fmaf(xt, sDDs[j * LVP + c4 + y], acc2[y]);
+        }
+      }
+      float db = 0.f;
+#pragma unroll
+      for (int y = 0; y < 4; ++y) {
+        sDels[i * LVP + c4 + y] = acc[y];
+        db = fmaf(acc2[y], sVs[i * LVP + c4 + y], db);
+        sDYs[i * LVP + c4 + y] = -sBeta[i] * acc2[y];
+        if (i < n) dv[((c0 + i) * H + h) * GDN_DV + vs + c4 + y] = from_f32<T>(sBeta[i] * acc2[y]);
+      }
+      atomicAdd(&sDBeta[i], db);
+    }
+    if (tid < GDN_DK) {
+      float acc = 0.f;
+      for (int c = 0; c < LBV; ++c) acc = fmaf(sDHs[tid * LVP + c], sHs[tid * LVP + c], acc);
+      sDGLh[tid] += acc;
+    }
+    __syncthreads();
+    // dX += dv_new Z^T ; dA_qk += scale dO v_new^T
+    {
+      auto fa = [&](int m, int kk) { return sDDs[m * LVP + kk]; };
+      auto fb = [&](int kk, int nn) { return sZs[nn * LVP + kk]; };
+      mm_acc<64, 64, LBV, 4, 4>(fa, fb, aX, tid);
+      auto fa2 = [&](int m, int kk) { return sDOs[m * LVP + kk]; };
+      auto fb2 = [&](int kk, int nn) { return sDels[nn * LVP + kk]; };
+      mm_acc<64, 64, LBV, 4, 4>(fa2, fb2, aQk, tid);
+    }
+    // dQg += dO h^T ; dKg += dY h^T ; dkgl += v_new dh^T
+    {
+      auto fo = [&](int m, int kk) { return sDOs[m * LVP + kk]; };
+      auto fy = [&](int m, int kk) { return sDYs[m * LVP + kk]; };
+      auto fd = [&](int m, int kk) { return sDels[m * LVP + kk]; };
+      auto fh = [&](int kk, int nn) { return sHs[nn * LVP + kk]; };
+      auto fdh = [&](int kk, int nn) { return sDHs[nn * LVP + kk]; };
+      mm_acc<64, 128, LBV, 4, 8>(fo, fh, aQg, tid);
+      mm_acc<64, 128, LBV, 4, 8>(fy, fh, aKg, tid);
+      mm_acc<64, 128, LBV, 4, 8>(fd, fdh, aKl, tid);
+    }
+    __syncthreads();
+  }
+
+  // ---- dL = -X^T dX X^T ; dbeta ; dP ------------------------------------------
+  float *sDX = sSl;              // [64][CP]
+  float *sT1 = sSl + 64 * CP;    // [64][CP]
+#pragma unroll
+  for (int x = 0; x < 4; ++x)
+#pragma unroll
+    for (int y = 0; y < 4; ++y) {
+      sDX[(pm0 + x) * CP + pn0 + y] = aX[x][y];
+      // dA_qk is used only on the causal part; fold the output scale in now
+      aQk[x][y] = (pn0 + y <= pm0 + x) ? a.scale * aQk[x][y] : 0.f;
+    }
+  __syncthreads();
+  {
+    float acc[4][4];
+    zero_acc(acc);
+    auto fa = [&](int m, int kk) { return sDX[m * CP + kk]; };
+    auto fb = [&](int kk, int nn) { return sX[nn * CP + kk]; };
+    mm_acc<64, 64, GDN_CHUNK, 4, 4>(fa, fb, acc, tid);  // dX X^T
+#pragma unroll
+    for (int x = 0; x < 4; ++x)
+#pragma unroll
+      for (int y = 0; y < 4; ++y) sT1[(pm0 + x) * CP + pn0 + y] = acc[x][y];
+  }
+  __syncthreads();
+  {
+    float acc[4][4];
+    zero_acc(acc);
+    auto fa = [&](int m, int kk) { return sX[kk * CP + m]; };
+    auto fb = [&](int kk, int nn) { return sT1[kk * CP + nn]; };
+    mm_acc<64, 64, GDN_CHUNK, 4, 4>(fa, fb, acc, tid);  // X^T (dX X^T)
+    float rows[4] = {0.f, 0.f, 0.f, 0.f};
+    float dPv[4][4];
+#pragma unroll
+    for (int x = 0; x < 4; ++x)
+#pragma unroll
+      for (int y = 0; y < 4; ++y) {
+        const int i = pm0 + x, j = pn0 + y;
+        const float dL = j < i ? -acc[x][y] : 0.f;
+        rows[x] = fmaf(dL, sP[i * CP + j], rows[x]);
+        dPv[x][y] = sBeta[i] * dL;
+      }
+#pragma unroll
+    for (int x = 0; x < 4; ++x) atomicAdd(&sDBeta[pm0 + x], rows[x]);
+    __syncthreads();  // every read of sP (the gated Gram) is done
+#pragma unroll
+    for (int x = 0; x < 4; ++x)
+#pragma unroll
+      for (int y = 0; y < 4; ++y) {
+        const int i = pm0 + x, j = pn0 + y;
+        float mP = dPv[x][y], mQ = aQk[x][y];
+        if (!PER_KEY) {
+          const float gam = j <= i ? gate_pow(sG[i] - sG[j], e2) : 0.f;
+          mP *= gam;
+          mQ *= gam;
+        }
+        sP[i * CP + j] = mP;
+        sAqk[i * CP + j] = mQ;
+      }
+  }
+  __syncthreads();
+
+  // ---- fold everything into dq, dk, dG ------------------------------------------
+  float rdq[4][8], rdk[4][8], rdG[4][8];
+  float colGl[8];
+#pragma unroll
+  for (int y = 0; y < 8; ++y) colGl[y] = 0.f;
+#pragma unroll
+  for (int x = 0; x < 4; ++x)
+#pragma unroll
+    for (int y = 0; y < 8; ++y) {
+      const int i = gm0 + x, d = gn0 + y;
+      const float G = Gv(i, d), eg = gate_pow(G, e2), egl = gate_pow(Gv(63, d) - G, e2);
+      const float kk = sK[i * KP + d], qq = sQ[i * KP + d];
+      const float dQg = a.scale * aQg[x][y];
+      rdq[x][y] = dQg * eg;
+      rdk[x][y] = aKg[x][y] * eg + aKl[x][y] * egl;
+      rdG[x][y] = lnb * (dQg * qq * eg + aKg[x][y] * kk * eg - aKl[x][y] * kk * egl);
+      colGl[y] = fmaf(aKl[x][y] * kk, egl, colGl[y]);
+    }
+#pragma unroll
+  for (int y = 0; y < 8; ++y) atomicAdd(&sDGlast[gn0 + y], colGl[y]);
+  // Gram adjoints, one at a time: (dP K), (dP^T K), (dAqk K), (dAqk^T Q), with Gamma
+  for (int which = 0; which < 4; ++which) {
+    const float *Mx = which < 2 ? sP : sAqk;
+    const bool tr = which == 1 || which == 3;  // use M^T
+    const float *Op = which == 3 ? sQ : sK;
+    float t[4][8];
+    zero_acc(t);
+    for (int j = 0; j < GDN_CHUNK; ++j) {
+#pragma unroll
+      for (int x = 0; x < 4; ++x) {
+        const int i = gm0 + x;
+        const float m = tr ? Mx[j * CP + i] : Mx[i * CP + j];
+        if (m == 0.f) continue;
+#pragma unroll
+        for (int y = 0; y < 8; ++y) {
+          const int d = gn0 + y;
+          float w = m * Op[j * KP + d];
+          if (PER_KEY)
+            w *= tr ? gate_pow(sG[j * KP + d] - sG[i * KP + d], e2)
+                    : gate_pow(sG[i * KP + d] - sG[j * KP + d], e2);
+          t[x][y] += w;
+        }
+      }
+    }
+#pragma unroll
+    for (int x = 0; x < 4; ++x)
+#pragma unroll
+      for (int y = 0; y < 8; ++y) {
+        const int i = gm0 + x, d = gn0 + y;
+        const float kk = sK[i * KP + d], qq = sQ[i * KP + d];
+        if (which == 0) {
+          rdk[x][y] += t[x][y];
+          rdG[x][y] += lnb * kk * t[x][y];
+        } else if (which == 1) {
+          rdk[x][y] += t[x][y];
+          rdG[x][y] -= lnb * kk * t[x][y];
+        } else if (which == 2) {
+          rdq[x][y] += t[x][y];
+          rdG[x][y] += lnb * qq * t[x][y];
+        } else {
+          rdk[x][y] += t[x][y];
+          rdG[x][y] -= lnb * kk * t[x][y];
+        }
+      }
+  }
+#pragma unroll
+  for (int x = 0; x < 4; ++x) {
+    const int i = gm0 + x;
+    if (i >= n) continue;
+#pragma unroll
+    for (int y = 0; y < 8; ++y) {
+      const int64_t off = ((c0 + i) * H + h) * GDN_DK + gn0 + y;
+      dq[off] = from_f32<T>(rdq[x][y]);
+      dk[off] = from_f32<T>(rdk[x][y]);
+    }
+  }
+  __syncthreads();  // sDGlast complete; sQ free for the gate gradient
+  // ---- gate gradient: add G_last terms, reverse cumulative sum ---------------
+  if (PER_KEY) {
+    float *sDG = sQ;
+#pragma unroll
+    for (int x = 0; x < 4; ++x)
+#pragma unroll
+      for (int y = 0; y < 8; ++y) sDG[(gm0 + x) * KP + gn0 + y] = rdG[x][y];
+    __syncthreads();
+    if (tid < GDN_DK) {
+      const int d = tid;
+      const float extra = lnb * (sDGlast[d] + sEL[d] * sDGLh[d]);
+      float run = 0.f;
+      for (int i = n - 1; i >= 0; --i) {
+        run += sDG[i * KP + d] + (i == n - 1 ? extra : 0.f);
+        a.dg[((c0 + i) * H + h) * GDN_DK + d] = run;
+      }
+    }
+  } else {
+#pragma unroll
+    for (int x = 0; x < 4; ++x) {
+      float s = 0.f;
+#pragma unroll
+      for (int y = 0; y < 8; ++y) s += rdG[x][y];
+      atomicAdd(&sDGrow[gm0 + x], s);
+    }
+    if (tid < GDN_DK) atomicAdd(&sDGrow[n - 1], lnb * (sDGlast[tid] + sEL[tid] * sDGLh[tid]));
+    __syncthreads();
+    if (tid == 0) {
+      float run = 0.f;
+      for (int i = n - 1; i >= 0; --i) {
+        run += sDGrow[i];
+        a.dg[(c0 + i) * H + h] = run;
+      }
+    }
+  }
+  if (tid < n) dbeta[(c0 + tid) * H + h] = from_f32<T>(sDBeta[tid]);
+}
+
+template <typename T, bool PK>
+cudaError_t dhu_one(const BwdArgs &a, cudaStream_t st) {
+  const size_t bytes = dhu_smem_floats<PK>() * sizeof(float);
+  cudaError_t e = cudaFuncSetAttribute(dhu_kernel<T, PK>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+  if (e != cudaSuccess) return e;
+  const int runs = a.cu ? a.num_seqs : a.B;
+  dhu_kernel<T, PK><<<dim3(GDN_DV / DBV, a.H, runs), NTH, bytes, st>>>(a);
+  return cudaGetLastError();
+}
+
+template <typename T, bool PK>
+cudaError_t local_one(const BwdArgs &a, cudaStream_t st) {
+  const size_t bytes = local_smem_floats<PK>() * sizeof(float);
+  cudaError_t e = cudaFuncSetAttribute(local_kernel<T, PK>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+  if (e != cudaSuccess) return e;
+  const int64_t nch = a.cu ? a.num_chunks : (int64_t)a.B * ((a.T + GDN_CHUNK - 1) / GDN_CHUNK);
+  if (nch == 0) return cudaSuccess;
+  local_kernel<T, PK><<<dim3((unsigned)nch, a.H), NTH, bytes, st>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_bwd_dhu(const BwdArgs &a, bool per_key, bool bf16, cudaStream_t st) {
+  if (bf16) return per_key ? dhu_one<__nv_bfloat16, true>(a, st) : dhu_one<__nv_bfloat16, false>(a, st);
+  return per_key ? dhu_one<float, true>(a, st) : dhu_one<float, false>(a, st);
+}
+
+cudaError_t launch_bwd_local(const BwdArgs &a, bool per_key, bool bf16, cudaStream_t st) {
+  if (bf16) return per_key ? local_one<__nv_bfloat16, true>(a, st) : local_one<__nv_bfloat16, false>(a, st);
+  return per_key ? local_one<float, true>(a, st) : local_one<float, false>(a, st);
+}
+
+}  // namespace gdn

@@ -1,0 +1,485 @@
+// C ABI of the chunked gated-delta-rule library: validation, workspace
+// layout and dispatch to the sm_103a kernels. See include/gdn.h for the
+// contract of every entry point.
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <string>
+
+#include "../../include/gdn.h"
+#include "common.cuh"
+#include "kernels.h"
+
+namespace {
+
+thread_local std::string g_last_error;
+
+// Device-side error word (see gdn_device_status); one per device that loads
+// the library, written by kernels with atomicMax.
+__device__ int g_dev_flag;
+
+gdn_status fail(gdn_status st, const char *fmt, ...) __attribute__((format(printf, 2, 3)));
+gdn_status fail(gdn_status st, const char *fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return st;
+}
+
+gdn_status ok() {
+  g_last_error.clear();
+  return GDN_OK;
+}
+
+gdn_status cuda_fail(cudaError_t e, const char *what) {
+  return fail(GDN_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// sm_103 check, cached per device ordinal.
+gdn_status check_device(int *dev_out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  static int cached[64];  // 0 unknown, 1 ok, 2 bad
+  if (dev < 64 && cached[dev] == 1) {
+    *dev_out = dev;
+    return GDN_OK;
+  }
+  int major = 0, minor = 0;
+  cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+  cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+  if (major != 10 || minor != 3) {
+    if (dev < 64) cached[dev] = 2;
+    return fail(GDN_ERR_UNSUPPORTED, "device %d is sm_%d%d; this library is built for sm_103a",
+                dev, major, minor);
+  }
+  if (dev < 64) cached[dev] = 1;
+  *dev_out = dev;
+  return GDN_OK;
+}
+
+int *device_flag_ptr() {
+  int *p = nullptr;
+  if (cudaGetSymbolAddress(reinterpret_cast<void **>(&p), g_dev_flag) != cudaSuccess) return nullptr;
+  return p;
+}
+
+int64_t div_up(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// Validation shared by the entry points (no device work).
+gdn_status check_problem(const gdn_problem *p, bool allow_segments) {
+  if (!p) return fail(GDN_ERR_INVALID_ARGUMENT, "problem is NULL");
+  if (p->layout != GDN_LAYOUT_BSND && p->layout != GDN_LAYOUT_TND)
+    return fail(GDN_ERR_INVALID_ARGUMENT, "layout must be BSND (0) or TND (1), got %d", p->layout);
+  if (p->gate_kind != GDN_GATE_SCALAR && p->gate_kind != GDN_GATE_PER_KEY)
+    return fail(GDN_ERR_INVALID_ARGUMENT, "gate_kind must be 0 or 1, got %d", p->gate_kind);
+  if (p->dtype != GDN_DTYPE_F32 && p->dtype != GDN_DTYPE_BF16)
+    return fail(GDN_ERR_INVALID_ARGUMENT, "dtype must be F32 (0) or BF16 (1), got %d", p->dtype);
+  if (p->use_exp2 != 0 && p->use_exp2 != 1)
+    return fail(GDN_ERR_INVALID_ARGUMENT, "use_exp2 must be 0 or 1");
+  if (p->use_qk_l2norm != 0 && p->use_qk_l2norm != 1)
+    return fail(GDN_ERR_INVALID_ARGUMENT, "use_qk_l2norm must be 0 or 1");
+  if (p->B < 1 || p->H < 1 || p->T < 0)
+    return fail(GDN_ERR_INVALID_ARGUMENT, "need B >= 1, H >= 1, T >= 0 (got B=%d H=%d T=%d)", p->B,
+                p->H, p->T);
+  if (p->K != GDN_DK || p->V != GDN_DV)
+    return fail(GDN_ERR_UNSUPPORTED, "K and V must be 128 (got K=%d V=%d)", p->K, p->V);
+  if (p->chunk_size != GDN_CHUNK)
+    return fail(GDN_ERR_UNSUPPORTED, "chunk_size must be 64, got %d", p->chunk_size);
+  if (!std::isfinite(p->scale))
+    return fail(GDN_ERR_INVALID_ARGUMENT, "scale must be finite");
+  if ((int64_t)p->B * p->T * p->H * GDN_DK >= (int64_t)1 << 40)
+    return fail(GDN_ERR_INVALID_ARGUMENT, "problem too large");
+  if (p->layout == GDN_LAYOUT_TND) {
+    if (p->B != 1)
+      return fail(GDN_ERR_INVALID_ARGUMENT, "packed TND layout requires physical batch size one (B=%d)", p->B);
+    if (!p->cu_seqlens || p->num_seqs < 1)
+      return fail(GDN_ERR_INVALID_ARGUMENT, "packed TND layout requires cu_seqlens and num_seqs >= 1");
+    if (!p->chunk_indices || p->num_chunks < p->num_seqs)
+      return fail(GDN_ERR_INVALID_ARGUMENT,
+                  "packed TND layout requires chunk_indices with num_chunks >= num_seqs");
+    if (p->T < p->num_seqs)
+      return fail(GDN_ERR_INVALID_ARGUMENT, "T=%d packed tokens cannot hold %d documents", p->T,
+                  p->num_seqs);
+    if (!aligned16(p->cu_seqlens) || !aligned16(p->chunk_indices))
+      return fail(GDN_ERR_INVALID_ARGUMENT, "cu_seqlens and chunk_indices must be 16-byte aligned");
+    if (p->segment_len != 0)
+      return fail(GDN_ERR_UNSUPPORTED, "segment_len applies to the BSND layout only");
+  } else if (p->cu_seqlens) {
+    return fail(GDN_ERR_INVALID_ARGUMENT, "cu_seqlens given with the BSND layout");
+  }
+  if (p->segment_len != 0) {
+    if (!allow_segments) return fail(GDN_ERR_UNSUPPORTED, "segment_len must be 0 here");
+    if (p->segment_len < 0 || p->segment_len % GDN_CHUNK != 0)
+      return fail(GDN_ERR_INVALID_ARGUMENT, "segment_len must be a positive multiple of 64, got %d",
+                  p->segment_len);
+  }
+  return GDN_OK;
+}
+
+#define REQUIRE_PTR(ptr, name)                                                         \
+  do {                                                                                 \
+    if (!(ptr)) return fail(GDN_ERR_INVALID_ARGUMENT, "%s must not be NULL", name);    \
+    if (!aligned16(ptr)) return fail(GDN_ERR_INVALID_ARGUMENT, "%s must be 16-byte aligned", name); \
+  } while (0)
+#define OPTIONAL_PTR(ptr, name)                                                        \
+  do {                                                                                 \
+    if ((ptr) && !aligned16(ptr))                                                      \
+      return fail(GDN_ERR_INVALID_ARGUMENT, "%s must be 16-byte aligned", name);       \
+  } while (0)
+
+float eff_scale(const gdn_problem *p) {
+  return p->scale == 0.f ? 1.0f / std::sqrt((float)p->K) : p->scale;
+}
+
+// bf16 inputs with one gate per head run on the tensor-core kernel; fp32
+// inputs, per-key gates and the in-kernel norm run on the fp32 SIMT kernel.
+bool use_tensor_cores(const gdn_problem *p) {
+  return p->dtype == GDN_DTYPE_BF16 && p->gate_kind == GDN_GATE_SCALAR && !p->use_qk_l2norm;
+}
+
+int64_t n_chunk_slots(const gdn_problem *p) {
+  return p->layout == GDN_LAYOUT_TND ? (int64_t)p->num_chunks : (int64_t)p->B * div_up(p->T, GDN_CHUNK);
+}
+
+size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+struct BwdWs {
+  size_t h_chunks, dh_chunks, dvnew, total;
+};
+
+BwdWs bwd_ws_layout(const gdn_problem *p) {
+  const size_t KV = (size_t)GDN_DK * GDN_DV * sizeof(float);
+  BwdWs w{};
+  const size_t slots = (size_t)n_chunk_slots(p) * p->H;
+  const size_t rows = (size_t)p->B * p->T;
+  w.h_chunks = 0;
+  w.dh_chunks = align256(slots * KV);
+  w.dvnew = w.dh_chunks + align256(slots * KV);
+  w.total = w.dvnew + align256(rows * p->H * GDN_DV * sizeof(float));
+  return w;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *gdn_last_error(void) { return g_last_error.c_str(); }
+
+gdn_status gdn_device_status(void *stream) {
+  int dev;
+  gdn_status st = check_device(&dev);
+  if (st != GDN_OK) return st;
+  int *flag = device_flag_ptr();
+  if (!flag) return fail(GDN_ERR_CUDA, "device flag unavailable");
+  int host = 0;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemcpyAsync(&host, flag, sizeof(int), cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(e, "reading the device flag");
+  if (host == gdn::kDevOk) return ok();
+  const int zero = 0;
+  e = cudaMemcpyAsync(flag, &zero, sizeof(int), cudaMemcpyHostToDevice, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(e, "clearing the device flag");
+  if (host == gdn::kDevTimeout) return fail(GDN_ERR_TIMEOUT, "a bounded device-side wait ran out");
+  return fail(GDN_ERR_DEVICE_CHECK, "a kernel found inconsistent device metadata (code %d)", host);
+}
+
+gdn_status gdn_prepare_varlen(const int32_t *cu, int32_t n_seq_plus_1, int64_t total_tokens,
+                              int32_t *chunk_indices, int32_t *num_chunks) {
+  if (!cu || !num_chunks) return fail(GDN_ERR_INVALID_ARGUMENT, "cu_seqlens and num_chunks must not be NULL");
+  if (n_seq_plus_1 < 2)
+    return fail(GDN_ERR_INVALID_ARGUMENT, "cu_seqlens needs at least two offsets, got %d", n_seq_plus_1);
+  if (cu[0] != 0)
+    return fail(GDN_ERR_INVALID_ARGUMENT, "cu_seqlens must start at zero, got %d", cu[0]);
+  if ((int64_t)cu[n_seq_plus_1 - 1] != total_tokens)
+    return fail(GDN_ERR_INVALID_ARGUMENT, "cu_seqlens must end at the packed token count %lld, got %d",
+                (long long)total_tokens, cu[n_seq_plus_1 - 1]);
+  int64_t count = 0;
+  for (int i = 0; i + 1 < n_seq_plus_1; ++i) {
+    if (cu[i] >= cu[i + 1])
+      return fail(GDN_ERR_INVALID_ARGUMENT,
+                  "cu_seqlens must strictly increase (offsets %d and %d at %d)", cu[i], cu[i + 1], i);
+    count += div_up(cu[i + 1] - cu[i], GDN_CHUNK);
+  }
+  if (count > INT32_MAX) return fail(GDN_ERR_INVALID_ARGUMENT, "too many chunks");
+  if (chunk_indices) {
+    if (*num_chunks < count)
+      return fail(GDN_ERR_INVALID_ARGUMENT, "chunk_indices capacity %d < %lld chunks", *num_chunks,
+                  (long long)count);
+    int64_t w = 0;
+    for (int i = 0; i + 1 < n_seq_plus_1; ++i)
+      for (int64_t c = 0; c < div_up(cu[i + 1] - cu[i], GDN_CHUNK); ++c) {
+        chunk_indices[2 * w] = i;
+        chunk_indices[2 * w + 1] = (int32_t)c;
+        ++w;
+      }
+  }
+  *num_chunks = (int32_t)count;
+  return ok();
+}
+
+gdn_status gdn_chunk_fwd_workspace(const gdn_problem *p, size_t *bytes) {
+  gdn_status st = check_problem(p, true);
+  if (st != GDN_OK) return st;
+  if (!bytes) return fail(GDN_ERR_INVALID_ARGUMENT, "bytes must not be NULL");
+  *bytes = 0;
+  return ok();
+}
+
+gdn_status gdn_chunk_fwd(const gdn_problem *p, const void *q, const void *k, const void *v,
+                         const float *g, const void *beta, const float *h0, void *o, float *ht,
+                         float *g_cumsum, float *A, float *h_chunks, void *ws, size_t ws_bytes,
+                         void *stream) {
+  gdn_status st = check_problem(p, true);
+  if (st != GDN_OK) return st;
+  REQUIRE_PTR(q, "q");
+  REQUIRE_PTR(k, "k");
+  REQUIRE_PTR(v, "v");
+  REQUIRE_PTR(g, "g");
+  REQUIRE_PTR(beta, "beta");
+  REQUIRE_PTR(o, "o");
+  OPTIONAL_PTR(h0, "h0");
+  OPTIONAL_PTR(ht, "ht");
+  OPTIONAL_PTR(g_cumsum, "g_cumsum");
+  OPTIONAL_PTR(A, "A");
+  OPTIONAL_PTR(h_chunks, "h_chunks");
+  (void)ws;
+  (void)ws_bytes;
+  if (p->segment_len > 0 && !h0)
+    return fail(GDN_ERR_INVALID_ARGUMENT, "segment_len > 0 needs h0 = S_init [B,H,nseg,K,V]");
+  int dev;
+  if ((st = check_device(&dev)) != GDN_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+  gdn::SimtFwdArgs a{};
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.g = g;
+  a.beta = beta;
+  a.h0 = h0;
+  a.o = o;
+  a.ht = ht;
+  a.g_cumsum = g_cumsum;
+  a.A = A;
+  a.h_chunks = h_chunks;
+  a.B = p->B;
+  a.T = p->T;
+  a.H = p->H;
+  a.scale = eff_scale(p);
+  a.use_exp2 = p->use_exp2;
+  a.l2norm = p->use_qk_l2norm;
+  a.cu = p->layout == GDN_LAYOUT_TND ? p->cu_seqlens : nullptr;
+  a.num_seqs = p->num_seqs;
+  a.num_chunks = p->num_chunks;
+  a.seg_len = p->segment_len;
+  a.nseg = p->segment_len > 0 ? (int)div_up(p->T, p->segment_len) : 0;
+  a.dev_flag = device_flag_ptr();
+  const int runs = a.cu ? p->num_seqs : (a.nseg > 0 ? p->B * a.nseg : p->B);
+  if (a.nseg > 0 && p->T == 0) return ok();
+  cudaError_t e;
+  if (use_tensor_cores(p)) {
+    e = gdn::launch_tc_fwd(a, dim3(GDN_DV / gdn::tc_fwd_bv(), p->H, runs), s);
+  } else {
+    const dim3 grid(GDN_DV / gdn::simt_fwd_bv(), p->H, runs);
+    e = gdn::launch_simt_fwd(a, p->gate_kind == GDN_GATE_PER_KEY, p->dtype == GDN_DTYPE_BF16, grid, s);
+  }
+  if (e != cudaSuccess) return cuda_fail(e, "chunk forward launch");
+  return ok();
+}
+
+gdn_status gdn_chunk_bwd_workspace(const gdn_problem *p, size_t *bytes) {
+  gdn_status st = check_problem(p, false);
+  if (st != GDN_OK) return st;
+  if (!bytes) return fail(GDN_ERR_INVALID_ARGUMENT, "bytes must not be NULL");
+  *bytes = bwd_ws_layout(p).total;
+  return ok();
+}
+
+gdn_status gdn_chunk_bwd(const gdn_problem *p, const void *q, const void *k, const void *v,
+                         const float *g_cumsum, const void *beta, const float *A, const void *dO,
+                         const float *h0, const float *dht, void *dq, void *dk, void *dv, float *dg,
+                         void *dbeta, float *dh0, void *ws, size_t ws_bytes, void *stream) {
+  gdn_status st = check_problem(p, false);
+  if (st != GDN_OK) return st;
+  if (p->use_qk_l2norm)
+    return fail(GDN_ERR_UNSUPPORTED, "the backward takes normalised q and k (use_qk_l2norm = 0)");
+  REQUIRE_PTR(q, "q");
+  REQUIRE_PTR(k, "k");
+  REQUIRE_PTR(v, "v");
+  REQUIRE_PTR(g_cumsum, "g_cumsum");
+  REQUIRE_PTR(beta, "beta");
+  REQUIRE_PTR(A, "A");
+  REQUIRE_PTR(dO, "dO");
+  REQUIRE_PTR(dq, "dq");
+  REQUIRE_PTR(dk, "dk");
+  REQUIRE_PTR(dv, "dv");
+  REQUIRE_PTR(dg, "dg");
+  REQUIRE_PTR(dbeta, "dbeta");
+  OPTIONAL_PTR(h0, "h0");
+  OPTIONAL_PTR(dht, "dht");
+  OPTIONAL_PTR(dh0, "dh0");
+  const BwdWs L = bwd_ws_layout(p);
+  if (L.total > 0 && (!ws || ws_bytes < L.total))
+    return fail(GDN_ERR_WORKSPACE, "backward workspace needs %zu bytes, got %zu", L.total,
+                ws ? ws_bytes : (size_t)0);
+  if (ws && !aligned16(ws)) return fail(GDN_ERR_INVALID_ARGUMENT, "ws must be 16-byte aligned");
+  int dev;
+  if ((st = check_device(&dev)) != GDN_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const bool pk = p->gate_kind == GDN_GATE_PER_KEY, bf = p->dtype == GDN_DTYPE_BF16;
+  char *w = static_cast<char *>(ws);
+  float *hch = reinterpret_cast<float *>(w + L.h_chunks);
+  float *dhch = reinterpret_cast<float *>(w + L.dh_chunks);
+  float *dvn = reinterpret_cast<float *>(w + L.dvnew);
+  const bool packed = p->layout == GDN_LAYOUT_TND;
+  const int runs = packed ? p->num_seqs : p->B;
+  int *flag = device_flag_ptr();
+
+  if (p->T == 0) {  // nothing but the state: dh0 = dht
+    if (dh0) {
+      const size_t bytes = (size_t)runs * p->H * GDN_DK * GDN_DV * sizeof(float);
+      cudaError_t e = dht ? cudaMemcpyAsync(dh0, dht, bytes, cudaMemcpyDeviceToDevice, s)
+                          : cudaMemsetAsync(dh0, 0, bytes, s);
+      if (e != cudaSuccess) return cuda_fail(e, "dh0 pass-through");
+    }
+    return ok();
+  }
+
+  // 1. entry state of every chunk, from the saved cumulative gate and A
+  gdn::SimtFwdArgs f{};
+  f.q = q;
+  f.k = k;
+  f.v = v;
+  f.g = g_cumsum;
+  f.beta = beta;
+  f.h0 = h0;
+  f.h_chunks = hch;
+  f.B = p->B;
+  f.T = p->T;
+  f.H = p->H;
+  f.scale = eff_scale(p);
+  f.use_exp2 = p->use_exp2;
+  f.cu = packed ? p->cu_seqlens : nullptr;
+  f.num_seqs = p->num_seqs;
+  f.num_chunks = p->num_chunks;
+  f.g_cum_in = g_cumsum;
+  f.A_in = A;
+  f.dev_flag = flag;
+  cudaError_t e = gdn::launch_simt_fwd(f, pk, bf, dim3(GDN_DV / gdn::simt_fwd_bv(), p->H, runs), s);
+  if (e != cudaSuccess) return cuda_fail(e, "backward state recompute launch");
+
+  gdn::BwdArgs b{};
+  b.q = q;
+  b.k = k;
+  b.v = v;
+  b.beta = beta;
+  b.dO = dO;
+  b.g_cumsum = g_cumsum;
+  b.A = A;
+  b.dht = dht;
+  b.dq = dq;
+  b.dk = dk;
+  b.dv = dv;
+  b.dbeta = dbeta;
+  b.dg = dg;
+  b.dh0 = dh0;
+  b.h_chunks = hch;
+  b.dh_chunks = dhch;
+  b.dvnew = dvn;
+  b.B = p->B;
+  b.T = p->T;
+  b.H = p->H;
+  b.scale = eff_scale(p);
+  b.use_exp2 = p->use_exp2;
+  b.cu = packed ? p->cu_seqlens : nullptr;
+  b.chunk_indices = packed ? p->chunk_indices : nullptr;
+  b.num_seqs = p->num_seqs;
+  b.num_chunks = p->num_chunks;
+  b.dev_flag = flag;
+  // 2. reverse state recurrence
+  if ((e = gdn::launch_bwd_dhu(b, pk, bf, s)) != cudaSuccess) return cuda_fail(e, "dhu launch");
+  // 3. local gradients
+  if ((e = gdn::launch_bwd_local(b, pk, bf, s)) != cudaSuccess) return cuda_fail(e, "local gradient launch");
+  return ok();
+}
+
+gdn_status kda_segment_summary(const gdn_problem *p, const void *k, const void *v, const float *g,
+                               const void *beta, int32_t segment_len, float *S_ext, float *M,
+                               void *ws, size_t ws_bytes, void *stream) {
+  gdn_status st = check_problem(p, true);
+  if (st != GDN_OK) return st;
+  (void)ws;
+  (void)ws_bytes;
+  if (p->layout != GDN_LAYOUT_BSND)
+    return fail(GDN_ERR_UNSUPPORTED, "segment summaries take the BSND layout");
+  if (segment_len <= 0 || segment_len % GDN_CHUNK != 0)
+    return fail(GDN_ERR_INVALID_ARGUMENT, "segment_len must be a positive multiple of 64, got %d",
+                segment_len);
+  REQUIRE_PTR(k, "k");
+  REQUIRE_PTR(v, "v");
+  REQUIRE_PTR(g, "g");
+  REQUIRE_PTR(beta, "beta");
+  REQUIRE_PTR(S_ext, "S_ext");
+  REQUIRE_PTR(M, "M");
+  int dev;
+  if ((st = check_device(&dev)) != GDN_OK) return st;
+  if (p->T == 0) return ok();
+  gdn::SimtFwdArgs a{};
+  a.q = k;  // unused in summary mode
+  a.k = k;
+  a.v = v;
+  a.g = g;
+  a.beta = beta;
+  a.S_ext = S_ext;
+  a.M = M;
+  a.B = p->B;
+  a.T = p->T;
+  a.H = p->H;
+  a.scale = 1.f;
+  a.use_exp2 = p->use_exp2;
+  a.l2norm = p->use_qk_l2norm;
+  a.seg_len = segment_len;
+  a.nseg = (int)div_up(p->T, segment_len);
+  a.summary = 1;
+  a.dev_flag = device_flag_ptr();
+  const dim3 grid((GDN_DV + GDN_DK) / gdn::simt_fwd_bv(), p->H, p->B * a.nseg);
+  cudaError_t e = gdn::launch_simt_fwd(a, p->gate_kind == GDN_GATE_PER_KEY,
+                                       p->dtype == GDN_DTYPE_BF16, grid,
+                                       static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "segment summary launch");
+  return ok();
+}
+
+gdn_status kda_segment_merge(const gdn_problem *p, const float *S_ext, const float *M,
+                             int32_t nseg, const float *h0, float *S_init, float *ht,
+                             void *stream) {
+  gdn_status st = check_problem(p, true);
+  if (st != GDN_OK) return st;
+  if (p->layout != GDN_LAYOUT_BSND)
+    return fail(GDN_ERR_UNSUPPORTED, "segment merge takes the BSND layout");
+  if (nseg < 1) return fail(GDN_ERR_INVALID_ARGUMENT, "nseg must be >= 1, got %d", nseg);
+  REQUIRE_PTR(S_ext, "S_ext");
+  REQUIRE_PTR(M, "M");
+  REQUIRE_PTR(S_init, "S_init");
+  OPTIONAL_PTR(h0, "h0");
+  OPTIONAL_PTR(ht, "ht");
+  int dev;
+  if ((st = check_device(&dev)) != GDN_OK) return st;
+  gdn::MergeArgs a{S_ext, M, h0, S_init, ht, p->B * p->H, nseg};
+  cudaError_t e = gdn::launch_merge(a, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "segment merge launch");
+  return ok();
+}
+
+}  // extern "C"

@@ -1,0 +1,71 @@
+// Internal launcher interface between the C ABI (gdn_api.cu) and the kernel
+// translation units. Not installed; not part of the public header.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace gdn {
+
+// Arguments of the fp32 SIMT chunk kernel (forward, correction run, segment
+// summary and the backward's state recompute share it).
+struct SimtFwdArgs {
+  const void *q, *k, *v;
+  const float *g;
+  const void *beta;
+  const float *h0;   // [N,H,K,V]; segment mode [B,H,nseg,K,V]
+  void *o;           // nullable
+  float *ht;         // nullable
+  float *g_cumsum;   // nullable
+  float *A;          // nullable, [rows,H,64]
+  float *h_chunks;   // nullable entry states
+  float *S_ext, *M;  // summary mode outputs
+  int B, T, H;
+  float scale;
+  int use_exp2, l2norm;
+  const int32_t *cu;  // packed offsets (device) or nullptr
+  int num_seqs;
+  int num_chunks;     // packed: chunk slots of h_chunks (bounds check)
+  int seg_len, nseg;  // segment runs when nseg > 0
+  int summary;        // 1: columns [0,V) from v with zero start, [V,V+K) transfer from I
+  const float *g_cum_in;  // nullable: read the cumulative gate instead of summing g
+  const float *A_in;      // nullable: read X = (I + L)^-1 instead of solving
+  int *dev_flag;
+};
+
+cudaError_t launch_simt_fwd(const SimtFwdArgs &a, bool per_key, bool bf16, dim3 grid,
+                            cudaStream_t st);
+int simt_fwd_bv();  // value columns per CTA
+
+// tcgen05 chunk forward: bf16 inputs, scalar gate, no in-kernel norm
+cudaError_t launch_tc_fwd(const SimtFwdArgs &a, dim3 grid, cudaStream_t st);
+int tc_fwd_bv();
+
+struct MergeArgs {
+  const float *S_ext, *M, *h0;
+  float *S_init, *ht;
+  int BH, nseg;
+};
+cudaError_t launch_merge(const MergeArgs &a, cudaStream_t st);
+
+// Backward: reverse state recurrence (dhu) and local gradients.
+struct BwdArgs {
+  const void *q, *k, *v, *beta, *dO;
+  const float *g_cumsum, *A, *dht;
+  void *dq, *dk, *dv, *dbeta;
+  float *dg, *dh0;
+  const float *h_chunks;  // workspace: entry state of every chunk
+  float *dh_chunks;       // workspace: gradient of every chunk's exit state
+  float *dvnew;           // workspace: [rows,H,V] gradient of v_new
+  int B, T, H;
+  float scale;
+  int use_exp2;
+  const int32_t *cu;
+  const int32_t *chunk_indices;
+  int num_seqs, num_chunks;
+  int *dev_flag;
+};
+cudaError_t launch_bwd_dhu(const BwdArgs &a, bool per_key, bool bf16, cudaStream_t st);
+cudaError_t launch_bwd_local(const BwdArgs &a, bool per_key, bool bf16, cudaStream_t st);
+
+}  // namespace gdn

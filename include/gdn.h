@@ -1,0 +1,204 @@
+/*
+ * gdn.h -- C ABI of the GB300 (sm_103a) chunked gated-delta-rule scan.
+ *
+ * The operation (benchmark spec of the gated delta rule, restated):
+ *   S_t = (I - beta_t k_t k_t^T) Diag(a_t) S_{t-1} + beta_t k_t v_t^T,
+ *   o_t = scale * S_t^T q_t,
+ *   a_t = exp(g_t) (use_exp2 = 0) or 2^(g_t) (use_exp2 = 1),
+ * with one log-gate per (token, head) (GDN, "gate_kind" SCALAR) or one per
+ * (token, head, key channel) (KDA, PER_KEY), computed in 64-token chunks:
+ * in-chunk cumulative log-gate, UT/WY transform A = (I + L)^-1, w, u, an fp32
+ * inter-chunk state recurrence and the intra-chunk output. The argument list
+ * follows the call contract of chunk_gated_delta_rule_fwd / _bwd in the GDN
+ * Ascend C adapter ("Diff Coverage" page of hyper-parallel, _AscendCGDN):
+ * q/k/v/g/beta, BSND or packed TND layout with cu_seqlens and chunk_indices,
+ * chunk 64, state [K, V] (state_v_first = False), optional initial and final
+ * state.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * Ownership: the caller allocates every input, output and workspace buffer.
+ *   The library never allocates or frees memory, never synchronises a
+ *   stream (gdn_device_status excepted) and launches only on `stream`.
+ * Pointers: "device" pointers are CUDA device (or managed) memory of the
+ *   current device; "host" pointers are ordinary host memory. Every device
+ *   pointer must be 16-byte aligned; row strides are implied by the shapes
+ *   (all tensors contiguous, row-major).
+ * Layouts: BSND = [B, T, H, D]; TND = packed [T, H, D] (B must be 1) with
+ *   document offsets. q, k are [.., H, K]; v, o, dO are [.., H, V]; beta is
+ *   [.., H]; g is [.., H] (SCALAR) or [.., H, K] (PER_KEY). States are fp32
+ *   [N, H, K, V] with N = B (BSND) or num_seqs (TND).
+ * Element types: q, k, v, beta, o, dq, dk, dv, dbeta use `dtype` (fp32 or
+ *   bf16); g, g_cumsum, A, states, dg are always fp32.
+ * Errors: every argument is validated before any launch. On failure the
+ *   call returns a nonzero gdn_status, launches nothing and leaves a message
+ *   for gdn_last_error(). A failed launch returns GDN_ERR_CUDA. Kernels that
+ *   detect an inconsistent input on the device (for example non-increasing
+ *   device cu_seqlens) skip the affected work and raise a device flag that
+ *   gdn_device_status() reports as GDN_ERR_DEVICE_CHECK.
+ */
+#ifndef GDN_H
+#define GDN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum gdn_status {
+    GDN_OK = 0,
+    GDN_ERR_INVALID_ARGUMENT = 1, /* contract violation (bad shape, null pointer, offsets) */
+    GDN_ERR_UNSUPPORTED = 2,      /* valid but not provided (K or V != 128, chunk != 64, no sm_103 device) */
+    GDN_ERR_WORKSPACE = 3,        /* workspace missing or smaller than the query returned */
+    GDN_ERR_CUDA = 4,             /* a CUDA runtime call or launch failed */
+    GDN_ERR_TIMEOUT = 5,          /* a bounded device-side wait ran out */
+    GDN_ERR_DEVICE_CHECK = 6      /* a kernel found inconsistent device-side metadata */
+} gdn_status;
+
+enum { GDN_LAYOUT_BSND = 0, GDN_LAYOUT_TND = 1 };
+enum { GDN_GATE_SCALAR = 0, GDN_GATE_PER_KEY = 1 };
+enum { GDN_DTYPE_F32 = 0, GDN_DTYPE_BF16 = 1 };
+
+/* Problem description shared by the entry points.
+ *   B, T, H, K, V : batch, tokens per batch row (TND: total packed tokens),
+ *                   heads, key width, value width. K = V = 128.
+ *   layout        : GDN_LAYOUT_BSND or GDN_LAYOUT_TND.
+ *   gate_kind     : GDN_GATE_SCALAR (GDN) or GDN_GATE_PER_KEY (KDA).
+ *   dtype         : element type of q, k, v, beta and the token outputs.
+ *   use_exp2      : 0 -> a = exp(g); 1 -> a = 2^g (the KDA stages use base 2).
+ *   scale         : output scale; 0 selects K^-1/2 (the adapters' default).
+ *   chunk_size    : must be 64 (the fused backends require chunk_size=64).
+ *   use_qk_l2norm : normalise q and k in-kernel, x / sqrt(sum x^2 + 1e-6).
+ *   cu_seqlens    : TND only: device int32 [num_seqs + 1] document offsets,
+ *                   validated beforehand with gdn_prepare_varlen.
+ *   num_seqs      : TND only: number of documents.
+ *   chunk_indices : TND only: device int32 [2 * num_chunks] (document, chunk)
+ *                   pairs produced by gdn_prepare_varlen.
+ *   num_chunks    : TND only: total chunks (sum of ceil(len / 64)).
+ *   segment_len   : BSND only, 0 or a multiple of 64. When nonzero,
+ *                   gdn_chunk_fwd treats every segment of segment_len tokens
+ *                   as an independent run whose entry state is read from
+ *                   h0 laid out [B, H, nseg, K, V] (the S_init produced by
+ *                   kda_segment_merge): the correction run of the segment
+ *                   split. ht then receives each batch row's final state.
+ */
+typedef struct gdn_problem {
+    int32_t B, T, H, K, V;
+    int32_t layout;
+    int32_t gate_kind;
+    int32_t dtype;
+    int32_t use_exp2;
+    float scale;
+    int32_t chunk_size;
+    int32_t use_qk_l2norm;
+    const int32_t *cu_seqlens;
+    int32_t num_seqs;
+    const int32_t *chunk_indices;
+    int32_t num_chunks;
+    int32_t segment_len;
+} gdn_problem;
+
+/* Thread-local text of the last failure in this thread ("" after success). */
+const char *gdn_last_error(void);
+
+/* Reads and clears the device-side error flag: synchronises `stream`.
+ * Returns GDN_OK, GDN_ERR_DEVICE_CHECK or GDN_ERR_TIMEOUT. */
+gdn_status gdn_device_status(void *stream);
+
+/* Packed-sequence metadata (host only, no device work).
+ * Defined by _packed_offsets / _packed_metadata of the Ascend C adapters
+ * ("Diff Coverage" page): offsets must have at least two entries, start at
+ * 0, end at total_tokens and strictly increase; else
+ * GDN_ERR_INVALID_ARGUMENT. chunk_indices receives, for every document n in
+ * order and every chunk c < ceil(len_n / 64), the pair (n, c).
+ *   cu_seqlens_host   : host int32 [n_seq_plus_1], read only.
+ *   chunk_indices_host: host int32 [2 * capacity] output, or NULL to only
+ *                       count; capacity is *num_chunks on entry when
+ *                       non-NULL (GDN_ERR_INVALID_ARGUMENT if too small).
+ *   num_chunks        : out, number of chunks. */
+gdn_status gdn_prepare_varlen(const int32_t *cu_seqlens_host, int32_t n_seq_plus_1,
+                              int64_t total_tokens, int32_t *chunk_indices_host,
+                              int32_t *num_chunks);
+
+/* Workspace bytes gdn_chunk_fwd needs for `p` (0 is a valid answer). */
+gdn_status gdn_chunk_fwd_workspace(const gdn_problem *p, size_t *bytes);
+
+/* Chunked forward (the GDN forward's ten-slot contract, slots that are
+ * enabled here: o, final_state, g_cumsum, A, h). All pointers device.
+ *   q, k, v, g, beta : inputs (read only).
+ *   h0       : nullable fp32 [N, H, K, V] initial state; with segment_len > 0
+ *              it is [B, H, nseg, K, V] (entry state of every segment).
+ *   o        : output, layout of v, element type `dtype`.
+ *   ht       : nullable fp32 [N, H, K, V] final state.
+ *   g_cumsum : nullable fp32, shape of g: in-chunk cumulative log-gate,
+ *              restarting at every chunk and document start.
+ *   A        : nullable fp32 [.., H, 64]: row i of the chunk's
+ *              (I + L)^-1, L = strictly-lower(diag(beta)(K K^T (.) Gamma));
+ *              beta is not folded in (the separate "beta_eff" slot).
+ *   h_chunks : nullable fp32 entry state of every chunk:
+ *              BSND [B, H, ceil(T/64), K, V]; TND [num_chunks, H, K, V] in
+ *              chunk_indices order.
+ *   ws, ws_bytes : workspace of at least gdn_chunk_fwd_workspace bytes.
+ *   stream   : cudaStream_t (NULL = legacy default stream). */
+gdn_status gdn_chunk_fwd(const gdn_problem *p, const void *q, const void *k, const void *v,
+                         const float *g, const void *beta, const float *h0, void *o, float *ht,
+                         float *g_cumsum, float *A, float *h_chunks, void *ws, size_t ws_bytes,
+                         void *stream);
+
+/* Workspace bytes gdn_chunk_bwd needs for `p`. */
+gdn_status gdn_chunk_bwd_workspace(const gdn_problem *p, size_t *bytes);
+
+/* Chunked backward (the GDN backward's contract: inputs q, k, v, the saved
+ * g_cumsum, beta and A, the output gradient and scale; first five result
+ * slots dq, dk, dv, dbeta, dg). All pointers device.
+ *   q, k, v, beta : forward inputs.
+ *   g_cumsum, A   : the forward's saved slots (fp32).
+ *   dO            : output gradient, layout of v.
+ *   h0            : nullable fp32 [N, H, K, V] initial state of the forward.
+ *   dht           : nullable fp32 [N, H, K, V] gradient of the final state.
+ *   dq, dk, dv, dbeta : outputs, element type `dtype`.
+ *   dg            : fp32, shape of g: gradient w.r.t. the raw per-token
+ *                   gate (not its cumulative sum).
+ *   dh0           : nullable fp32 [N, H, K, V] gradient of h0.
+ *   ws, ws_bytes  : workspace of at least gdn_chunk_bwd_workspace bytes.
+ * segment_len must be 0 and use_qk_l2norm must be 0 (the adapters apply
+ * the norm outside the native backward). */
+gdn_status gdn_chunk_bwd(const gdn_problem *p, const void *q, const void *k, const void *v,
+                         const float *g_cumsum, const void *beta, const float *A,
+                         const void *dO, const float *h0, const float *dht, void *dq, void *dk,
+                         void *dv, float *dg, void *dbeta, float *dh0, void *ws,
+                         size_t ws_bytes, void *stream);
+
+/* Affine segment summary (state_summary.py kda_split_state_summary_kernel,
+ * combined mode): for every batch row b, head h and segment s of
+ * segment_len tokens (BSND, segment_len a multiple of 64; the last segment
+ * may be shorter), the local state from a zero start and the transfer map
+ * from the identity, so that  S_exit = M S_entry + S_ext.  q is not needed.
+ *   k, v, g, beta : device inputs (g_cumsum is computed internally).
+ *   S_ext         : device fp32 [B, H, nseg, K, V].
+ *   M             : device fp32 [B, H, nseg, K, K].
+ * ws may be NULL (no workspace needed). */
+gdn_status kda_segment_summary(const gdn_problem *p, const void *k, const void *v,
+                               const float *g, const void *beta, int32_t segment_len,
+                               float *S_ext, float *M, void *ws, size_t ws_bytes, void *stream);
+
+/* Ordered merge of segment summaries (apply_kda_state_summary on the
+ * "Diff Coverage" page; _exclusive_prefix_compose in SANA's
+ * distributed_scan.py): S_init_0 = h0 (or 0), S_init_{s+1} = M_s S_init_s
+ * + S_ext_s, in fp32.
+ *   S_ext, M : device fp32 [B, H, nseg, K, V] and [B, H, nseg, K, K].
+ *   h0       : nullable device fp32 [B, H, K, V].
+ *   S_init   : device fp32 [B, H, nseg, K, V], entry state of every segment.
+ *   ht       : nullable device fp32 [B, H, K, V], the state after the last
+ *              segment. */
+gdn_status kda_segment_merge(const gdn_problem *p, const float *S_ext, const float *M,
+                             int32_t nseg, const float *h0, float *S_init, float *ht,
+                             void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GDN_H */
