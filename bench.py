@@ -103,6 +103,20 @@ class ClockSampler:
                 "samples": len(use), "samples_in_timed_region": len(inside)}
 
 
+def _recorded_traffic():
+    """DRAM bytes per launch from the committed ncu summary, only while the kernel source
+    is the one those counters were taken on (else None)."""
+    import hashlib
+    try:
+        rec = json.load(open(os.path.join(ROOT, "profiles", "traffic.json")))["gdn_bsnd_bf16_fwd"]
+        src = os.path.join(ROOT, "gated_delta_rule_28_gb300", "csrc", "fwd_tc.cu")
+        if hashlib.sha256(open(src, "rb").read()).hexdigest() == rec["kernel_source_sha256"]:
+            return rec["bytes_per_launch"]
+    except Exception:
+        pass
+    return None
+
+
 def _dist():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -170,6 +184,81 @@ def run_reference(args):
     }
     print(json.dumps(line), flush=True)
     return 0
+
+
+def _time_ms(fn, reps, warmup, stream):
+    """Mean device time of fn() over reps launches on `stream` (CUDA events)."""
+    import torch
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            fn()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(reps):
+            fn()
+        b.record(stream)
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / reps
+
+
+def secondary_rows(dev, hbm_peak):
+    """The other scope rows, each on its own workload at full size (device-generated
+    seeded inputs with the workloads' distributions; timing only, parity is in tests)."""
+    import torch
+    from gated_delta_rule_28_gb300 import api, binding as Bd
+    g = torch.Generator(device=dev)
+    g.manual_seed(1234)
+    stream = torch.cuda.Stream(device=dev)
+    out = {}
+
+    def unit(shape):
+        x = torch.randn(shape, device=dev, generator=g)
+        return (x / x.norm(dim=-1, keepdim=True)).to(torch.bfloat16)
+
+    def common(shape, gshape, gscale):
+        q, k = unit(shape), unit(shape)
+        v = torch.randn(shape, device=dev, generator=g).to(torch.bfloat16)
+        beta = torch.sigmoid(torch.randn(shape[:-1], device=dev, generator=g)).to(torch.bfloat16)
+        gg = -gscale * torch.nn.functional.softplus(torch.randn(gshape, device=dev, generator=g))
+        return q, k, v, gg, beta
+
+    with torch.cuda.stream(stream):
+        # packed documents: 32768 tokens, H=32, lengths U[37, 8192]
+        from gated_delta_rule_28_gb300 import workloads
+        lens = workloads.doc_lengths(np.random.default_rng(2), 32768)
+        cu = np.concatenate([[0], np.cumsum(lens)])
+        q, k, v, gg, beta = common((32768, 32, 128), (32768, 32), 0.1)
+        vl = api.Varlen(cu, 32768, dev)
+        ms = _time_ms(lambda: api.chunk_gated_delta_rule_fwd(q, k, v, gg, beta, varlen=vl,
+                                                             stream=stream.cuda_stream), 5, 2, stream)
+        byts = 32768 * 32 * BYTES_PER_TOKEN_HEAD + len(lens) * 32 * STATE_BYTES
+        out["packed_fwd"] = {"workload": "gdn_packed_bf16", "ms": ms, "tokens_per_s": 32768 / ms * 1e3,
+                             "hbm_frac": byts / (ms * 1e-3) / 1e9 / hbm_peak, "docs": int(len(lens))}
+        del q, k, v, gg, beta
+        # KDA long context: per-key base-2 gates, 16 segments of 4096 vs unsplit
+        q, k, v, gg, beta = common((1, 65536, 8, 128), (1, 65536, 8, 128), 0.05)
+        ms_split = _time_ms(lambda: api.split_forward(q, k, v, gg, beta, 4096, use_exp2=True,
+                                                      stream=stream.cuda_stream), 2, 1, stream)
+        ms_whole = _time_ms(lambda: api.chunk_gated_delta_rule_fwd(q, k, v, gg, beta, use_exp2=True,
+                                                                   stream=stream.cuda_stream), 1, 1, stream)
+        out["kda_split_fwd"] = {"workload": "kda_long_bf16", "ms_split": ms_split, "ms_unsplit": ms_whole,
+                                "tokens_per_s_split": 65536 / ms_split * 1e3}
+        del q, k, v, gg, beta
+        # training step: forward with saved slots + backward, B8 H16 T8192
+        q, k, v, gg, beta = common((8, 8192, 16, 128), (8, 8192, 16), 0.1)
+        h0 = 0.1 * torch.randn((8, 16, 128, 128), device=dev, generator=g)
+        dO = torch.randn((8, 8192, 16, 128), device=dev, generator=g).to(torch.bfloat16)
+        f = api.chunk_gated_delta_rule_fwd(q, k, v, gg, beta, h0=h0, return_g_cumsum=True,
+                                           return_A=True, stream=stream.cuda_stream)
+        ms_f = _time_ms(lambda: api.chunk_gated_delta_rule_fwd(q, k, v, gg, beta, h0=h0, return_g_cumsum=True,
+                                                               return_A=True, stream=stream.cuda_stream),
+                        2, 1, stream)
+        ms_b = _time_ms(lambda: api.chunk_gated_delta_rule_bwd(q, k, v, f["g_cumsum"], beta, f["A"], dO,
+                                                               h0=h0, stream=stream.cuda_stream), 2, 1, stream)
+        out["train_fwd_bwd"] = {"workload": "gdn_train_bf16", "ms_fwd": ms_f, "ms_bwd": ms_b,
+                                "tokens_per_s": 8 * 8192 / (ms_f + ms_b) * 1e3}
+    Bd.gdn_device_status(stream.cuda_stream)
+    return out
 
 
 def run_ours(args):
@@ -285,13 +374,7 @@ def run_ours(args):
     alg_bytes = Bsz * T * H * BYTES_PER_TOKEN_HEAD + Bsz * H * STATE_BYTES
     flops = Bsz * T * H * FLOP_PER_TOKEN_HEAD
     achieved = alg_bytes / kavg / 1e9
-    traffic = None
-    tpath = os.path.join(ROOT, "profiles", "traffic.json")
-    if os.path.exists(tpath):
-        try:
-            traffic = json.load(open(tpath)).get("gdn_bsnd_bf16_fwd")
-        except Exception:
-            traffic = None
+    traffic = _recorded_traffic()
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -327,6 +410,11 @@ def run_ours(args):
             "clocks": clocks,
             "gpu_launches": args.steps,
         }
+        if not args.no_rows and world == 1:
+            try:
+                line["rows"] = secondary_rows(dev, hbm)
+            except Exception as exc:  # reported, never hidden
+                line["rows"] = {"error": repr(exc)}
         print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()
@@ -340,6 +428,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-rows", action="store_true", help="skip the other scope rows' timings")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

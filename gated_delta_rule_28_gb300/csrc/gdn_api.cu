@@ -242,12 +242,14 @@ gdn_status gdn_chunk_fwd(const gdn_problem *p, const void *q, const void *k, con
                          void *stream) {
   gdn_status st = check_problem(p, true);
   if (st != GDN_OK) return st;
-  REQUIRE_PTR(q, "q");
-  REQUIRE_PTR(k, "k");
-  REQUIRE_PTR(v, "v");
-  REQUIRE_PTR(g, "g");
-  REQUIRE_PTR(beta, "beta");
-  REQUIRE_PTR(o, "o");
+  if (p->T > 0) {  // an empty sequence has no token tensors (they may be NULL)
+    REQUIRE_PTR(q, "q");
+    REQUIRE_PTR(k, "k");
+    REQUIRE_PTR(v, "v");
+    REQUIRE_PTR(g, "g");
+    REQUIRE_PTR(beta, "beta");
+    REQUIRE_PTR(o, "o");
+  }
   OPTIONAL_PTR(h0, "h0");
   OPTIONAL_PTR(ht, "ht");
   OPTIONAL_PTR(g_cumsum, "g_cumsum");
@@ -314,18 +316,20 @@ gdn_status gdn_chunk_bwd(const gdn_problem *p, const void *q, const void *k, con
   if (st != GDN_OK) return st;
   if (p->use_qk_l2norm)
     return fail(GDN_ERR_UNSUPPORTED, "the backward takes normalised q and k (use_qk_l2norm = 0)");
-  REQUIRE_PTR(q, "q");
-  REQUIRE_PTR(k, "k");
-  REQUIRE_PTR(v, "v");
-  REQUIRE_PTR(g_cumsum, "g_cumsum");
-  REQUIRE_PTR(beta, "beta");
-  REQUIRE_PTR(A, "A");
-  REQUIRE_PTR(dO, "dO");
-  REQUIRE_PTR(dq, "dq");
-  REQUIRE_PTR(dk, "dk");
-  REQUIRE_PTR(dv, "dv");
-  REQUIRE_PTR(dg, "dg");
-  REQUIRE_PTR(dbeta, "dbeta");
+  if (p->T > 0) {
+    REQUIRE_PTR(q, "q");
+    REQUIRE_PTR(k, "k");
+    REQUIRE_PTR(v, "v");
+    REQUIRE_PTR(g_cumsum, "g_cumsum");
+    REQUIRE_PTR(beta, "beta");
+    REQUIRE_PTR(A, "A");
+    REQUIRE_PTR(dO, "dO");
+    REQUIRE_PTR(dq, "dq");
+    REQUIRE_PTR(dk, "dk");
+    REQUIRE_PTR(dv, "dv");
+    REQUIRE_PTR(dg, "dg");
+    REQUIRE_PTR(dbeta, "dbeta");
+  }
   OPTIONAL_PTR(h0, "h0");
   OPTIONAL_PTR(dht, "dht");
   OPTIONAL_PTR(dh0, "dh0");
