@@ -30,8 +30,10 @@ GDN_DTYPE_F32, GDN_DTYPE_BF16 = 0, 1
 
 # every symbol the public header declares
 EXPORTS = ("gdn_last_error", "gdn_device_status", "gdn_prepare_varlen", "gdn_chunk_fwd_workspace",
-           "gdn_chunk_fwd", "gdn_chunk_bwd_workspace", "gdn_chunk_bwd", "kda_segment_summary",
-           "kda_segment_merge")
+           "gdn_chunk_fwd", "gdn_chunk_bwd_workspace", "gdn_chunk_bwd", "gdn_chunk_bwd_noalloc",
+           "kda_segment_summary", "kda_segment_merge")
+# bytes of the library's built-in scratch array used by gdn_chunk_bwd_noalloc
+GDN_NOALLOC_SCRATCH_BYTES = 64 * 1024 * 1024
 
 
 class GdnError(RuntimeError):
@@ -82,6 +84,7 @@ def load():
             lib.gdn_chunk_fwd.argtypes = [P] + [vp] * 11 + [vp, sz, vp]
             lib.gdn_chunk_bwd_workspace.argtypes = [P, ctypes.POINTER(sz)]
             lib.gdn_chunk_bwd.argtypes = [P] + [vp] * 15 + [vp, sz, vp]
+            lib.gdn_chunk_bwd_noalloc.argtypes = [P] + [vp] * 15 + [vp]
             lib.kda_segment_summary.argtypes = [P, vp, vp, vp, vp, ctypes.c_int32, vp, vp, vp, sz, vp]
             lib.kda_segment_merge.argtypes = [P, vp, vp, ctypes.c_int32, vp, vp, vp, vp]
             for name in EXPORTS[1:]:
@@ -183,6 +186,15 @@ def gdn_chunk_bwd(p: gdn_problem, q, k, v, g_cumsum, beta, A, dO, h0, dht, dq, d
                                 _ptr(beta), _ptr(A), _ptr(dO), _ptr(h0), _ptr(dht), _ptr(dq),
                                 _ptr(dk), _ptr(dv), _ptr(dg), _ptr(dbeta), _ptr(dh0), _ptr(ws),
                                 int(ws_bytes), _stream(stream)))
+
+
+def gdn_chunk_bwd_noalloc(p: gdn_problem, q, k, v, g_cumsum, beta, A, dO, h0, dht, dq, dk, dv, dg,
+                          dbeta, dh0, stream=None):
+    """Backward with the library's built-in scratch instead of a workspace (see gdn.h)."""
+    _check(load().gdn_chunk_bwd_noalloc(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(g_cumsum),
+                                        _ptr(beta), _ptr(A), _ptr(dO), _ptr(h0), _ptr(dht),
+                                        _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dg), _ptr(dbeta),
+                                        _ptr(dh0), _stream(stream)))
 
 
 def kda_segment_summary(p: gdn_problem, k, v, g, beta, segment_len, S_ext, M, ws=None, ws_bytes=0,

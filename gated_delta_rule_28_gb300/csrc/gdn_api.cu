@@ -487,3 +487,10 @@ gdn_status kda_segment_merge(const gdn_problem *p, const float *S_ext, const flo
 }
 
 }  // extern "C"
+
+namespace gdn {
+gdn_status set_error(gdn_status st, const char *msg) {
+  g_last_error = msg ? msg : "";
+  return st;
+}
+}  // namespace gdn

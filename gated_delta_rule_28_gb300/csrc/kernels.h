@@ -5,6 +5,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "../../include/gdn.h"
+
 namespace gdn {
 
 // Arguments of the fp32 SIMT chunk kernel (forward, correction run, segment
@@ -68,4 +70,9 @@ struct BwdArgs {
 cudaError_t launch_bwd_dhu(const BwdArgs &a, bool per_key, bool bf16, cudaStream_t st);
 cudaError_t launch_bwd_local(const BwdArgs &a, bool per_key, bool bf16, cudaStream_t st);
 
+}  // namespace gdn
+
+namespace gdn {
+// Records `msg` for gdn_last_error() in the calling thread and returns `st`.
+gdn_status set_error(gdn_status st, const char *msg);
 }  // namespace gdn

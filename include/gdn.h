@@ -171,6 +171,33 @@ gdn_status gdn_chunk_bwd(const gdn_problem *p, const void *q, const void *k, con
                          void *dv, float *dg, void *dbeta, float *dh0, void *ws,
                          size_t ws_bytes, void *stream);
 
+/* Backward without a caller workspace (the paper has no counterpart; this is
+ * a convenience of this library).
+ * For callers that cannot allocate device memory: runtimes that plan every
+ * device buffer at start-up and forbid allocation afterwards, and plugin
+ * hosts that hand a library only its input and output buffers. Arguments,
+ * outputs and numerics are those of gdn_chunk_bwd; the scratch lives in one
+ * array of GDN_NOALLOC_SCRATCH_BYTES (64 MiB) of device memory inside the
+ * library, which every GPU that loads the library holds until the process
+ * exits. Nothing here allocates or frees memory.
+ *   - Problems whose backward workspace (gdn_chunk_bwd_workspace) exceeds
+ *     GDN_NOALLOC_SCRATCH_BYTES are rejected with GDN_ERR_WORKSPACE and a
+ *     message giving both sizes, before any device work.
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture.
+ *   - Every call on a device shares the one array and it keeps the last
+ *     call's contents; the backward writes every scratch element it reads in
+ *     the same call, so no clearing is needed. Calls whose work overlaps on
+ *     the GPU (other streams, other host threads) race on the array: order
+ *     them, for example on one stream. */
+#define GDN_NOALLOC_SCRATCH_BYTES (64u * 1024u * 1024u)
+gdn_status gdn_chunk_bwd_noalloc(const gdn_problem *p, const void *q, const void *k,
+                                 const void *v, const float *g_cumsum, const void *beta,
+                                 const float *A, const void *dO, const float *h0,
+                                 const float *dht, void *dq, void *dk, void *dv, float *dg,
+                                 void *dbeta, float *dh0, void *stream);
+
 /* Affine segment summary (state_summary.py kda_split_state_summary_kernel,
  * combined mode): for every batch row b, head h and segment s of
  * segment_len tokens (BSND, segment_len a multiple of 64; the last segment
