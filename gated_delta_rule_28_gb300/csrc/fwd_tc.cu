@@ -1,27 +1,30 @@
 // Tensor-core (tcgen05) chunk forward for bf16 inputs, scalar gate (sm_103a).
 //
-// One CTA owns one independent run (batch row, packed document or segment)
-// of one head and 64 of the 128 state columns; the state slice h (128 x 64,
-// fp32) lives in registers (thread = key row, 32 columns), its bf16 copy in
-// shared memory is the operand of the state contraction. Per 64-token chunk
-// the CTA takes the chunk algorithm's steps (north star; GDN Ascend C adapter
-// forward; chunk_fwd_h / chunk_kda_fwd_finalize of the KDA adapter), with
-// every dense contraction on the tensor core (bf16 operands from shared
-// memory, fp32 accumulators in tensor memory) and M = 128 throughout:
+// One CTA (512 threads) owns one independent run (batch row, packed document
+// or segment) of one head and 64 of the 128 state columns. The state slice h
+// (128 x 64, fp32) lives in registers: thread = key row (its tensor-memory
+// lane) and 16 columns. Per 64-token chunk the CTA takes the steps of the
+// chunk algorithm (north star; GDN Ascend C adapter forward; chunk_fwd_h and
+// chunk_kda_fwd_finalize of the KDA adapter) with every dense contraction on
+// the tensor core (bf16 operands in shared memory, fp32 accumulators in
+// tensor memory, M = 128):
 //
-//   P1   S = [K; Q] K^T                          -> L = strictly-lower(beta S (.) Gamma),
-//                                                   A_qk = lower-incl(S_qk (.) Gamma)
-//   SIMT X = (I + L)^-1 (fp32, 16x16 blocks: diagonal blocks by forward
-//        substitution, then the off-diagonal block levels)
-//   P3a  [X; A_qk] X            -> A_qk X
-//   P3b  [X; A_qk X] [beta Kg | beta V]  -> [w | u ; A_qk w | A_qk u]   (Kg = K (.) e^G)
-//   P4   [-w; Qg - A_qk w] h   accumulated onto [u; A_qk u]  -> [v_new ; o / scale]
-//        (o = scale (Qg h + A_qk v_new) = scale ((Qg - A_qk w) h + A_qk u))
-//   P5   (K (.) e^(G_last - G))^T v_new          -> h <- e^(G_last) h + P5
+//   P1   S = [K; Q] K^T                   -> L = strictly-lower(beta S (.) Gamma),
+//                                            A_qk = lower-incl(S_qk (.) Gamma)
+//   X = (I + L)^-1: 16x16 diagonal blocks by fp32 forward substitution, the
+//        off-diagonal block levels with tf32 mma.sync
+//   P3a  [X; A_qk] X                      -> A_qk X
+//   P3b  [X; A_qk X] [beta e^G K | beta V] -> [w | u ; A_qk w | A_qk u]
+//   P4   [-w; e^G Q - A_qk w] h accumulated onto [u; A_qk u] -> [v_new ; o / scale]
+//   P5   (e^(G_last - G) K)^T v_new       -> h <- e^(G_last) h + P5
 //
-// Loads of chunk c+1 (cp.async, zero-filled past the run end) overlap the
-// work on chunk c. All mbarrier waits are bounded; a wait that runs out sets
-// the device flag and the CTA leaves after releasing its tensor memory.
+// Every operand tile is K-major with the 128-byte swizzle; the transposed
+// tiles (X^T, [beta e^G K | beta V]^T, (e^(G_last-G) K)^T, v_new^T, h^T) are
+// made with ldmatrix.trans / stmatrix, scaling per token on the way, and all
+// other operands are written with 16-byte stores. Loads of chunk c+1 (cp.async,
+// zero-filled past the run end) and its P1 overlap the work on chunk c. Every
+// mbarrier wait is bounded; a wait that runs out sets the device flag and the
+// CTA leaves after its MMAs have drained and its tensor memory is released.
 #include "common.cuh"
 #include "kernels.h"
 #include "tc.cuh"
@@ -30,57 +33,166 @@ namespace gdn {
 namespace {
 using namespace tc;
 
-constexpr int TBV = 64;    // state columns per CTA
-constexpr int TNT = 256;   // threads per CTA
-constexpr uint32_t TMEM_COLS = 256;
-constexpr uint32_t T_S = 0;   // 64 columns: S, then A_qk X, then P5
-constexpr uint32_t T_W = 64;  // 192 columns: P3b; P4 accumulates into [T_W+128, T_W+192)
+constexpr int TBV = 64;   // state columns per CTA
+constexpr int NTH = 512;  // threads per CTA
+constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t T_S0 = 0;    // 2 x 64 columns: S (per chunk parity), then A_qk X
+constexpr uint32_t T_W = 128;   // 192 columns: P3b; P4 accumulates into [T_W+128, T_W+192)
+constexpr uint32_t T_P5 = 320;  // 64 columns
 
-// shared memory map (bytes from a 1024-aligned base)
-constexpr int SZ_KQ = 2 * 128 * 128;  // two K-blocks of 128 rows ([K; Q]) x 128 B
-constexpr int SZ_V = 64 * TBV * 2;    // value slice, plain [token][column]
-constexpr int OFF_KQ = 0;             // 2 stages
-constexpr int OFF_V = OFF_KQ + 2 * SZ_KQ;
-constexpr int OFF_AOP = OFF_V + 2 * SZ_V;     // [X; A_qk | A_qk X]  128 x 64
-constexpr int OFF_AT = OFF_AOP + 16384;       // X^T                  64 x 64
-constexpr int OFF_B3 = OFF_AT + 8192;         // [beta Kg | beta V]^T 192 x 64
-constexpr int OFF_WQ = OFF_B3 + 24576;        // [-w; Qg - A_qk w]    2 x 128 x 64
-constexpr int OFF_KL = OFF_WQ + 32768;        // kgl^T                128 x 64
-constexpr int OFF_HT = OFF_KL + 16384;        // h^T                  2 x 64 x 64
-constexpr int OFF_VN = OFF_HT + 16384;        // v_new^T              64 x 64
+// shared memory map (bytes from a 1024-aligned base); every tile K-major, 128 B rows
+constexpr int SZ_KQ = 32768;                     // [K; Q]: 2 K-blocks x 128 rows
+constexpr int SZ_V = 8192;                       // V slice: 64 rows
+constexpr int OFF_KQ = 0;                        // 2 stages
+constexpr int OFF_V = OFF_KQ + 2 * SZ_KQ;        // 2 stages
+constexpr int OFF_AOP = OFF_V + 2 * SZ_V;        // [X; A_qk | A_qk X]     128 rows, K = 64
+constexpr int OFF_XT = OFF_AOP + 16384;          // X^T                    64 rows, K = 64
+constexpr int OFF_B3 = OFF_XT + 8192;            // [b e^G K | b V]^T      192 rows, K = 64
+constexpr int OFF_KL = OFF_B3 + 24576;           // (e^(Gl-G) K)^T         128 rows, K = 64
+constexpr int OFF_WQ = OFF_KL + 16384;           // [-w; q']               2 K-blocks x 128 rows
+constexpr int OFF_HT = OFF_WQ + 32768;           // h^T                    2 K-blocks x 64 rows
+constexpr int OFF_VN = OFF_HT + 16384;           // v_new^T                64 rows, K = 64
 constexpr int OFF_SMALL = OFF_VN + 8192;
-constexpr int SMEM_BYTES = OFF_SMALL + 2048 + 1024;
-// fp32 solve buffers alias [OFF_WQ, OFF_WQ + 49152) (free while solving)
-constexpr int LS = 65;
-constexpr int OFF_L = OFF_WQ;
-constexpr int OFF_X = OFF_L + 64 * LS * 4;
-constexpr int OFF_T = OFF_X + 64 * LS * 4;
-static_assert(OFF_T + 3 * 256 * 4 <= OFF_WQ + 49152, "solve buffers overflow");
+constexpr int SMALL_BYTES = 4096;
+constexpr int SMEM_BYTES = OFF_SMALL + SMALL_BYTES + 1024;
 static_assert(SMEM_BYTES <= 232448, "shared memory");
+// aliases: the solve's fp32 blocks live in WQ (free until WQ is formed); the
+// row-major staging of v_new and h (for their transposes) lives in B3 (free
+// after P3b)
+constexpr int OFF_LB = OFF_WQ;               // 10 lower 16x16 fp32 blocks of L
+constexpr int OFF_XB = OFF_WQ + 10 * 1024;   // 10 blocks of X
+constexpr int OFF_TB = OFF_WQ + 20 * 1024;   // 3 scratch blocks (one per level warp)
+static_assert(23 * 1024 <= 32768, "solve buffers");
+constexpr int OFF_STG = OFF_B3;              // staging: v_new 64 rows (8 KB), h 128 rows (16 KB)
+static_assert(16384 <= 24576, "staging");
 
 constexpr uint32_t WAIT_LIMIT = 1u << 22;
 
+// --- small helpers -----------------------------------------------------------------
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, uint32_t bytes) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(bytes)
                : "memory");
 }
+__device__ __forceinline__ void cp_async4(uint32_t dst, const void *src, uint32_t bytes) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src), "r"(bytes)
+               : "memory");
+}
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
 
-// base-e or base-2 decay factor of a (difference of) cumulative log-gate(s)
 __device__ __forceinline__ float gexp(float x, bool e2) { return e2 ? exp2f(x) : __expf(x); }
 
-__device__ __forceinline__ void st_bf16(uint8_t *base, uint32_t off, float x) {
-  *reinterpret_cast<__nv_bfloat16 *>(base + off) = __float2bfloat16_rn(x);
+__device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
+  const __nv_bfloat162 t = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<const uint32_t *>(&t);
 }
-__device__ __forceinline__ float ld_bf16(const uint8_t *base, uint32_t off) {
-  return __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(base + off));
+__device__ __forceinline__ float2 unpack_bf16(uint32_t u) {
+  return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&u));
+}
+__device__ __forceinline__ uint4 pack8(const float *f) {
+  uint4 u;
+  u.x = pack_bf16(f[0], f[1]);
+  u.y = pack_bf16(f[2], f[3]);
+  u.z = pack_bf16(f[4], f[5]);
+  u.w = pack_bf16(f[6], f[7]);
+  return u;
+}
+__device__ __forceinline__ void unpack8(uint4 u, float *f) {
+  const float2 a = unpack_bf16(u.x), b = unpack_bf16(u.y), c = unpack_bf16(u.z), d = unpack_bf16(u.w);
+  f[0] = a.x; f[1] = a.y; f[2] = b.x; f[3] = b.y; f[4] = c.x; f[5] = c.y; f[6] = d.x; f[7] = d.y;
+}
+// byte offset of 16-byte chunk c8 of row `row` in a 128-byte-row swizzled tile
+__device__ __forceinline__ uint32_t chunk_off(int row, int c8) {
+  return (uint32_t)((row >> 3) * 1024 + (row & 7) * 128 + (((c8 ^ row) & 7) << 4));
 }
 
-// X = (I + L)^-1 for a 64x64 strictly-lower L (stride LS), 256 threads.
-__device__ void solve64(const float *L, float *X, float *T, int tid) {
-  if (tid < 64) {  // diagonal 16x16 blocks, one column per thread
-    const int b = tid >> 4, c = tid & 15, base = b * 16;
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+__device__ __forceinline__ void stsm_x4(uint32_t addr, const uint32_t (&r)[4]) {
+  asm volatile("stmatrix.sync.aligned.m8n8.x4.shared.b16 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(r[0]),
+               "r"(r[1]), "r"(r[2]), "r"(r[3])
+               : "memory");
+}
+
+// Transposes one 16x16 bf16 block with one warp: source rows s0..s0+15 and
+// columns 8*c0 .. 8*c0+15 of a swizzled tile (`src` is the
+// address of the K-block holding those columns) become rows d0..d0+15 of the
+// destination, columns s0..s0+15 (inside the destination K-block given), each
+// element multiplied by fac[source row] when fac is given.
+struct TransJob {
+  uint32_t src;       // address of the source tile's K-block holding chunk c0
+  int s0, c0;         // first source row; first source chunk (even, within the K-block)
+  uint32_t dst;       // address of the destination tile's K-block holding column s0
+  int d0;             // first destination row
+};
+__device__ __forceinline__ void trans16(const TransJob &j, const float *fac, int lane) {
+  const int m = lane >> 3, r = lane & 7;
+  uint32_t x[4];
+  ldsm_x4_trans(j.src + chunk_off(j.s0 + r + 8 * (m & 1), j.c0 + (m >> 1)), x);
+  if (fac) {
+    // register i of this thread holds destination (row lane/4, columns 2(lane%4), +1) of
+    // matrix i, i.e. source rows s0 + 8*(i&1) + 2(lane%4) + {0, 1}
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int srow = j.s0 + 8 * (i & 1) + 2 * (lane & 3);
+      const float2 t = unpack_bf16(x[i]);
+      x[i] = pack_bf16(t.x * fac[srow], t.y * fac[srow + 1]);
+    }
+  }
+  stsm_x4(j.dst + chunk_off(j.d0 + r + 8 * (m >> 1), ((j.s0 & 63) >> 3) + (m & 1)), x);
+}
+
+// --- blocked 64x64 fp32 matrices for the solve ------------------------------------------
+__device__ __forceinline__ int blk(int bi, int bj) { return bi * (bi + 1) / 2 + bj; }
+__device__ __forceinline__ int bsw(int r, int c) { return r * 16 + (c ^ (((r >> 1) & 3) << 2)); }
+
+__device__ __forceinline__ uint32_t to_tf32(float x) {
+  uint32_t r;
+  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+  return r;
+}
+// acc (16x16 as two 16x8 tiles) += A (16x16) B (16x16), tf32 inputs, fp32 accumulate
+__device__ __forceinline__ void mm16_tf32(const float *A, const float *B, float (&acc)[2][4], int lane) {
+  const int g = lane >> 2, t = lane & 3;
+#pragma unroll
+  for (int kk = 0; kk < 16; kk += 8) {
+    const uint32_t a0 = to_tf32(A[bsw(g, kk + t)]), a1 = to_tf32(A[bsw(g + 8, kk + t)]);
+    const uint32_t a2 = to_tf32(A[bsw(g, kk + t + 4)]), a3 = to_tf32(A[bsw(g + 8, kk + t + 4)]);
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+      const uint32_t b0 = to_tf32(B[bsw(kk + t, nt * 8 + g)]);
+      const uint32_t b1 = to_tf32(B[bsw(kk + t + 4, nt * 8 + g)]);
+      asm volatile(
+          "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+          "{%0,%1,%2,%3};"
+          : "+f"(acc[nt][0]), "+f"(acc[nt][1]), "+f"(acc[nt][2]), "+f"(acc[nt][3])
+          : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+    }
+  }
+}
+__device__ __forceinline__ void acc_store(float *C, const float (&acc)[2][4], int lane, float sign) {
+  const int g = lane >> 2, t = lane & 3;
+#pragma unroll
+  for (int nt = 0; nt < 2; ++nt) {
+    C[bsw(g, nt * 8 + 2 * t)] = sign * acc[nt][0];
+    C[bsw(g, nt * 8 + 2 * t + 1)] = sign * acc[nt][1];
+    C[bsw(g + 8, nt * 8 + 2 * t)] = sign * acc[nt][2];
+    C[bsw(g + 8, nt * 8 + 2 * t + 1)] = sign * acc[nt][3];
+  }
+}
+
+// X = (I + L)^-1 from the lower 16x16 blocks of a strictly-lower L; all threads.
+__device__ void solve_blocks(const float *L, float *X, float *T, int tid) {
+  const int warp = tid >> 5, lane = tid & 31;
+  if (tid < 64) {  // diagonal blocks: one column per thread, fp32 forward substitution
+    const int b = tid >> 4, c = tid & 15;
+    const float *Lb = L + blk(b, b) * 256;
     float x[16];
 #pragma unroll
     for (int r = 0; r < 16; ++r) x[r] = (r == c) ? 1.f : 0.f;
@@ -88,64 +200,65 @@ __device__ void solve64(const float *L, float *X, float *T, int tid) {
     for (int r = 1; r < 16; ++r) {
       float acc = 0.f;
 #pragma unroll
-      for (int j = 0; j < r; ++j) acc = fmaf(L[(base + r) * LS + base + j], x[j], acc);
+      for (int j = 0; j < r; ++j) acc = fmaf(Lb[bsw(r, j)], x[j], acc);
       if (r > c) x[r] = -acc;
     }
+    float *Xb = X + blk(b, b) * 256;
 #pragma unroll
-    for (int r = 0; r < 16; ++r) X[(base + r) * LS + base + c] = x[r];
-  }
-  for (int e = tid; e < 64 * 64; e += TNT) {
-    const int i = e >> 6, j = e & 63;
-    if ((i >> 4) < (j >> 4)) X[i * LS + j] = 0.f;
+    for (int r = 0; r < 16; ++r) Xb[bsw(r, c)] = x[r];
   }
   __syncthreads();
-  for (int dist = 1; dist <= 3; ++dist) {
-    const int nblk = 4 - dist;
-    for (int e = tid; e < nblk * 256; e += TNT) {
-      const int bi = dist + e / 256, bj = bi - dist, r = (e & 255) >> 4, c = e & 15;
-      float acc = 0.f;
-      for (int kb = bj; kb < bi; ++kb)
-#pragma unroll
-        for (int kk = 0; kk < 16; ++kk)
-          acc = fmaf(L[(bi * 16 + r) * LS + kb * 16 + kk], X[(kb * 16 + kk) * LS + bj * 16 + c], acc);
-      T[e] = acc;
-    }
-    __syncthreads();
-    for (int e = tid; e < nblk * 256; e += TNT) {
-      const int bi = dist + e / 256, bj = bi - dist, r = (e & 255) >> 4, c = e & 15;
-      const int eb = e & ~255;
-      float acc = 0.f;
-#pragma unroll
-      for (int kk = 0; kk < 16; ++kk)
-        acc = fmaf(X[(bi * 16 + r) * LS + bi * 16 + kk], T[eb + kk * 16 + c], acc);
-      X[(bi * 16 + r) * LS + bj * 16 + c] = -acc;
+  for (int dist = 1; dist <= 3; ++dist) {  // X_ij = -X_ii sum_k L_ik X_kj, by block distance
+    if (warp < 4 - dist) {
+      const int bj = warp, bi = warp + dist;
+      float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+      for (int kb = bj; kb < bi; ++kb) mm16_tf32(L + blk(bi, kb) * 256, X + blk(kb, bj) * 256, acc, lane);
+      float *Tw = T + warp * 256;
+      acc_store(Tw, acc, lane, 1.f);
+      __syncwarp();
+      float acc2[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+      mm16_tf32(X + blk(bi, bi) * 256, Tw, acc2, lane);
+      acc_store(X + blk(bi, bj) * 256, acc2, lane, -1.f);
     }
     __syncthreads();
   }
 }
 
-__global__ void __launch_bounds__(TNT, 1) tc_fwd_kernel(SimtFwdArgs a) {
+struct TcState {
+  float G[2][64], eG[2][64], eGL[2][64], bEG[2][64];  // per chunk parity
+  float g[2][64];                                     // raw gate per load stage
+  float beta[2][64];
+  float EL[2];
+  uint64_t bar_s[2], bar_m;
+  uint32_t tmem;
+};
+static_assert(sizeof(TcState) <= SMALL_BYTES, "small state");
+
+__global__ void __launch_bounds__(NTH, 1) tc_fwd_kernel(SimtFwdArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                             ~static_cast<uintptr_t>(1023));
-  float *sG = reinterpret_cast<float *>(sm + OFF_SMALL);  // [2][64] raw g, then cumulative
-  float *sBeta = sG + 128;                                // [2][64]
-  uint64_t *bar = reinterpret_cast<uint64_t *>(sm + OFF_SMALL + 1024);
-  uint32_t *tbase_p = reinterpret_cast<uint32_t *>(sm + OFF_SMALL + 1040);
-  float *sL = reinterpret_cast<float *>(sm + OFF_L);
-  float *sX = reinterpret_cast<float *>(sm + OFF_X);
-  float *sT = reinterpret_cast<float *>(sm + OFF_T);
+  TcState &st = *reinterpret_cast<TcState *>(sm + OFF_SMALL);
+  float *LB = reinterpret_cast<float *>(sm + OFF_LB);
+  float *XB = reinterpret_cast<float *>(sm + OFF_XB);
+  float *TB = reinterpret_cast<float *>(sm + OFF_TB);
+  const uint32_t sb = smem_u32(sm);
 
-  const int tid = threadIdx.x, warp = tid >> 5;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int q4 = warp & 3;         // tensor-memory lane quarter of this warp
+  const int cg = warp >> 2;        // column group: 16 of 64 columns
+  const int row = q4 * 32 + lane;  // tensor-memory lane = matrix row
   const int H = a.H, h = blockIdx.y, z = blockIdx.z;
   const int col0 = blockIdx.x * TBV;
+  const bool e2 = a.use_exp2 != 0;
+  const float scale = a.scale;
   const __nv_bfloat16 *q = static_cast<const __nv_bfloat16 *>(a.q);
   const __nv_bfloat16 *k = static_cast<const __nv_bfloat16 *>(a.k);
   const __nv_bfloat16 *v = static_cast<const __nv_bfloat16 *>(a.v);
   const __nv_bfloat16 *beta = static_cast<const __nv_bfloat16 *>(a.beta);
   __nv_bfloat16 *o = static_cast<__nv_bfloat16 *>(a.o);
 
-  // ---- the run -------------------------------------------------------------
+  // ---- the run -------------------------------------------------------------------
   int64_t r0, r1, chunk_base = 0;
   int b = 0, s = 0, state_idx;
   const int NT = (a.T + GDN_CHUNK - 1) / GDN_CHUNK;
@@ -175,138 +288,75 @@ __global__ void __launch_bounds__(TNT, 1) tc_fwd_kernel(SimtFwdArgs a) {
     r1 = r0 + a.T;
     state_idx = b;
   }
-  const int64_t nchunks = (r1 - r0 + GDN_CHUNK - 1) / GDN_CHUNK;
+  const int64_t nch = (r1 - r0 + GDN_CHUNK - 1) / GDN_CHUNK;
+  auto chunk_rows = [&](int64_t c) { return (int)min((int64_t)GDN_CHUNK, r1 - (r0 + c * GDN_CHUNK)); };
 
-  // ---- tensor memory and barrier ---------------------------------------------
+  // ---- tensor memory, barriers -----------------------------------------------------
   if (warp == 0) {
-    tmem_alloc(tbase_p, TMEM_COLS);
+    tmem_alloc(&st.tmem, TMEM_COLS);
     tmem_relinquish();
   }
   if (tid == 0) {
-    mbar_init(bar, 1);
+    mbar_init(&st.bar_s[0], 1);
+    mbar_init(&st.bar_s[1], 1);
+    mbar_init(&st.bar_m, 1);
     mbar_fence_init();
   }
   fence_before_sync();
   __syncthreads();
   fence_after_sync();
-  const uint32_t tmem = *tbase_p;
-  const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-  const int row = tid & 127;   // TMEM lane / key row owned by this thread
-  const int half = tid >> 7;   // column half owned by this thread
-  uint32_t phase = 0;
+  const uint32_t tmem = st.tmem;
+  const uint32_t tl = tmem + ((uint32_t)(q4 * 32) << 16);  // this warp's lane quarter
+  uint32_t ph_s[2] = {0, 0}, ph_m = 0;
   bool bad = false;
-
-  // ---- initial state ------------------------------------------------------------
-  float hreg[32];
-  {
-    const float *src = nullptr;
-    if (a.h0) {
-      const int64_t slot = a.nseg > 0 ? (((int64_t)b * H + h) * a.nseg + s) : ((int64_t)state_idx * H + h);
-      src = a.h0 + slot * GDN_DK * GDN_DV + (int64_t)row * GDN_DV + col0 + half * 32;
-    }
-#pragma unroll
-    for (int j = 0; j < 32; ++j) hreg[j] = src ? src[j] : 0.f;
-  }
-
-  auto write_ht_bf16 = [&]() {
-#pragma unroll
-    for (int j = 0; j < 32; ++j) {
-      const int c = half * 32 + j;
-      st_bf16(sm, OFF_HT + (row >> 6) * 8192 + sw128_offset(c, row & 63), hreg[j]);
-    }
+  auto wait_bar = [&](uint64_t *bar, uint32_t &ph) {
+    if (!mbar_wait(bar, ph & 1, WAIT_LIMIT)) bad = true;
+    ++ph;
+    fence_after_sync();
   };
-  write_ht_bf16();
+  // one MMA group issued by thread 0 and waited for by every thread
+  auto mma_sync_wait = [&]() {
+    if (tid == 0) mma_commit(&st.bar_m);
+    wait_bar(&st.bar_m, ph_m);
+  };
 
-  auto issue_loads = [&](int64_t ci, int stage) {
-    const int64_t c0 = r0 + ci * GDN_CHUNK;
-    const int n = (int)min((int64_t)GDN_CHUNK, r1 - c0);
-    const uint32_t kq = smem_u32(sm + OFF_KQ + stage * SZ_KQ);
-    const uint32_t vb = smem_u32(sm + OFF_V + stage * SZ_V);
-    for (int x = tid; x < 2048 + 512; x += TNT) {
+  // ---- loads -----------------------------------------------------------------------
+  float beta_pend = 0.f;  // beta row of the most recently issued chunk (threads < 64)
+  auto issue_loads = [&](int64_t c) {
+    const int stage = (int)(c & 1);
+    const int64_t c0 = r0 + c * GDN_CHUNK;
+    const int n = chunk_rows(c);
+    const uint32_t kq = sb + OFF_KQ + stage * SZ_KQ;
+    const uint32_t vb = sb + OFF_V + stage * SZ_V;
+    for (int x = tid; x < 2048 + 512; x += NTH) {
       if (x < 2048) {
-        const int which = x >> 10, rem = x & 1023, r = rem >> 4, f16 = rem & 15;
+        const int which = x >> 10, r = (x >> 4) & 63, f16 = x & 15;
         const bool valid = r < n;
         const __nv_bfloat16 *src = (which ? q : k) + ((c0 + (valid ? r : 0)) * H + h) * GDN_DK + f16 * 8;
-        const int rr = r + which * 64, kb = f16 >> 3, c8 = f16 & 7;
-        const uint32_t dst = kq + kb * 16384 + (rr >> 3) * 1024 + (rr & 7) * 128 + ((c8 ^ (rr & 7)) << 4);
-        cp_async16(dst, src, valid ? 16u : 0u);
+        cp_async16(kq + (f16 >> 3) * 16384 + chunk_off(r + which * 64, f16 & 7), src, valid ? 16u : 0u);
       } else {
-        const int rem = x - 2048, r = rem >> 3, c8 = rem & 7;
+        const int r = (x - 2048) >> 3, c8 = x & 7;
         const bool valid = r < n;
         const __nv_bfloat16 *src = v + ((c0 + (valid ? r : 0)) * H + h) * GDN_DV + col0 + c8 * 8;
-        cp_async16(vb + r * 128 + c8 * 16, src, valid ? 16u : 0u);
+        cp_async16(vb + chunk_off(r, c8), src, valid ? 16u : 0u);
       }
+    }
+    if (tid < 64) {
+      const bool valid = tid < n;
+      const float *gsrc = a.g_cum_in ? a.g_cum_in : a.g;
+      cp_async4(smem_u32(&st.g[stage][tid]), gsrc + (c0 + (valid ? tid : 0)) * H + h, valid ? 4u : 0u);
+      beta_pend = valid ? __bfloat162float(beta[(c0 + tid) * H + h]) : 0.f;
     }
     cp_async_commit();
   };
-  // gate and beta of one chunk, one row per thread (tid < 64)
-  auto load_gb = [&](int64_t ci, float &gv, float &bv) {
-    const int64_t c0 = r0 + ci * GDN_CHUNK;
-    const int n = (int)min((int64_t)GDN_CHUNK, r1 - c0);
-    gv = 0.f;
-    bv = 0.f;
-    if (tid < n) {
-      gv = a.g[(c0 + tid) * H + h];
-      bv = __bfloat162float(beta[(c0 + tid) * H + h]);
-    }
-  };
-
-  auto mma_wait = [&]() {
-    if (!mbar_wait(bar, phase & 1, WAIT_LIMIT)) bad = true;
-    ++phase;
-    fence_after_sync();
-  };
-
-  if (nchunks > 0) {
-    issue_loads(0, 0);
-    float gv, bv;
-    load_gb(0, gv, bv);
-    if (tid < 64) {
-      sG[tid] = gv;
-      sBeta[tid] = bv;
-    }
-  }
-
-  const float scale = a.scale;
-  const bool e2 = a.use_exp2 != 0;
-  const bool lead = blockIdx.x == 0;
-  for (int64_t ci = 0; ci < nchunks && !bad; ++ci) {
-    const int stage = (int)(ci & 1);
-    const int64_t c0 = r0 + ci * GDN_CHUNK;
-    const int n = (int)min((int64_t)GDN_CHUNK, r1 - c0);
-    uint8_t *kq = sm + OFF_KQ + stage * SZ_KQ;
-    const uint8_t *vs = sm + OFF_V + stage * SZ_V;
-    float *G = sG + stage * 64;
-    float *Bt = sBeta + stage * 64;
-
-    // entry state of this chunk
-    if (a.h_chunks) {
-      const int64_t slot = a.cu ? (chunk_base + ci) * H + h : ((int64_t)b * H + h) * NT + chunk_base + ci;
-      float *dst = a.h_chunks + slot * GDN_DK * GDN_DV + (int64_t)row * GDN_DV + col0 + half * 32;
-#pragma unroll
-      for (int j = 0; j < 32; ++j) dst[j] = hreg[j];
-    }
-
-    cp_async_wait_all();
-    fence_proxy_async();
-    __syncthreads();
-    float g_next = 0.f, b_next = 0.f;
-    if (ci + 1 < nchunks) {
-      issue_loads(ci + 1, stage ^ 1);
-      load_gb(ci + 1, g_next, b_next);
-    }
-
-    // P1: S = [K; Q] K^T
-    if (tid == 0) {
-      fence_after_sync();
-      const uint32_t kqa = smem_u32(kq);
-      mma_tiles(tmem + T_S, kqa, 16384, kqa, 16384, 128, idesc_bf16(128, 64), false);
-      mma_commit(bar);
-    }
-    // cumulative gate (rows past the end carry g = 0, so G stays flat there)
-    if (warp == 0) {
-      const int lane = tid;
-      const float x0 = G[2 * lane], x1 = G[2 * lane + 1];
+  // cumulative gate and per-token factors of chunk c once its loads landed
+  auto chunk_factors = [&](int64_t c, float bval) {
+    const int par = (int)(c & 1);
+    const int n = chunk_rows(c);
+    if (a.g_cum_in) {  // saved cumulative gate; rows past the end repeat the last one
+      if (tid < 64) st.G[par][tid] = st.g[par][min(tid, n - 1)];
+    } else if (warp == 0) {
+      const float x0 = st.g[par][2 * lane], x1 = st.g[par][2 * lane + 1];
       const float pair = x0 + x1;
       float incl = pair;
 #pragma unroll
@@ -315,229 +365,295 @@ __global__ void __launch_bounds__(TNT, 1) tc_fwd_kernel(SimtFwdArgs a) {
         if (lane >= off) incl += y;
       }
       const float ex = incl - pair;
-      G[2 * lane] = ex + x0;
-      G[2 * lane + 1] = ex + pair;
+      st.G[par][2 * lane] = ex + x0;
+      st.G[par][2 * lane + 1] = ex + pair;
     }
+    if (tid < 64) st.beta[par][tid] = bval;
     __syncthreads();
-    if (lead && a.g_cumsum && tid < n) a.g_cumsum[(c0 + tid) * H + h] = G[tid];
-    const float Gl = G[63];
-    mma_wait();
+    if (tid < 64) {
+      const float G = st.G[par][tid], Gl = st.G[par][63];
+      st.eG[par][tid] = gexp(G, e2);
+      st.eGL[par][tid] = gexp(Gl - G, e2);
+      st.bEG[par][tid] = st.beta[par][tid] * gexp(G, e2);
+      if (tid == 0) st.EL[par] = gexp(Gl, e2);
+      if (a.g_cumsum && blockIdx.x == 0 && tid < n) a.g_cumsum[(r0 + c * GDN_CHUNK + tid) * H + h] = G;
+    }
+  };
+  auto issue_p1 = [&](int64_t c) {  // S = [K; Q] K^T
+    if (tid == 0) {
+      fence_after_sync();
+      const uint32_t kq = sb + OFF_KQ + (int)(c & 1) * SZ_KQ;
+      mma_tiles(tmem + T_S0 + 64 * (uint32_t)(c & 1), kq, 16384, kq, 16384, 128, idesc_bf16(128, 64), false);
+      mma_commit(&st.bar_s[c & 1]);
+    }
+  };
 
-    // gated Gram rows: L (fp32, for the solve) and A_qk (bf16 operand rows 64..127)
+  // ---- state ------------------------------------------------------------------------
+  float hreg[16];
+  {
+    const float *src = nullptr;
+    if (a.h0) {
+      const int64_t slot = a.nseg > 0 ? (((int64_t)b * H + h) * a.nseg + s) : ((int64_t)state_idx * H + h);
+      src = a.h0 + slot * GDN_DK * GDN_DV + (int64_t)row * GDN_DV + col0 + cg * 16;
+    }
+#pragma unroll
+    for (int j = 0; j < 16; ++j) hreg[j] = src ? src[j] : 0.f;
+  }
+  // h^T operand: h row-major through the staging tile, then 16x16 transposes
+  auto write_h_operand = [&]() {
+    uint8_t *stg = sm + OFF_STG;
+    *reinterpret_cast<uint4 *>(stg + chunk_off(row, cg * 2)) = pack8(hreg);
+    *reinterpret_cast<uint4 *>(stg + chunk_off(row, cg * 2 + 1)) = pack8(hreg + 8);
+    __syncthreads();
+    for (int jb = warp; jb < 32; jb += NTH / 32) {  // 8 key blocks x 4 column blocks
+      const int rb = jb >> 2, cb = jb & 3;
+      trans16(TransJob{sb + OFF_STG, rb * 16, cb * 2, sb + OFF_HT + (rb >> 2) * 8192, cb * 16}, nullptr, lane);
+    }
+  };
+
+  // ---- prologue -----------------------------------------------------------------------
+  if (nch > 0) {
+    issue_loads(0);
+    const float beta0 = beta_pend;
+    cp_async_wait<0>();
+    fence_proxy_async();
+    __syncthreads();
+    issue_p1(0);
+    chunk_factors(0, beta0);
+    if (nch > 1) issue_loads(1);
+  }
+  write_h_operand();
+  fence_proxy_async();
+  __syncthreads();
+
+  const bool lead = blockIdx.x == 0;
+  for (int64_t c = 0; c < nch && !bad; ++c) {
+    const int par = (int)(c & 1);
+    const int64_t c0 = r0 + c * GDN_CHUNK;
+    const int n = chunk_rows(c);
+    const uint32_t kq = sb + OFF_KQ + par * SZ_KQ;
+    const uint32_t vs = sb + OFF_V + par * SZ_V;
+    const float *G = st.G[par];
+
+    if (a.h_chunks) {  // entry state of chunk c
+      const int64_t slot = a.cu ? (chunk_base + c) * H + h : ((int64_t)b * H + h) * NT + chunk_base + c;
+      float4 *dst = reinterpret_cast<float4 *>(a.h_chunks + slot * GDN_DK * GDN_DV + (int64_t)row * GDN_DV +
+                                               col0 + cg * 16);
+#pragma unroll
+      for (int g4 = 0; g4 < 4; ++g4)
+        dst[g4] = make_float4(hreg[g4 * 4], hreg[g4 * 4 + 1], hreg[g4 * 4 + 2], hreg[g4 * 4 + 3]);
+    }
+
+    // ---- gated Gram rows: L (fp32 blocks) and A_qk (operand rows 64..127) --------------
+    wait_bar(&st.bar_s[par], ph_s[par]);
     {
-      float sv[32];
-      float t16[16];
-      tmem_ld16(tmem + lane_base + T_S + half * 32, t16);
-#pragma unroll
-      for (int j = 0; j < 16; ++j) sv[j] = t16[j];
-      tmem_ld16(tmem + lane_base + T_S + half * 32 + 16, t16);
-#pragma unroll
-      for (int j = 0; j < 16; ++j) sv[16 + j] = t16[j];
+      float sv[16];
+      tmem_ld16(tl + T_S0 + 64 * par + cg * 16, sv);
       tmem_ld_wait();
       if (row < 64) {
-        const int i = row;
-        const float bi = Bt[i], gi = G[i];
+        const int i = row, bi = i >> 4;
+        if (bi >= cg) {
+          const float bt = st.beta[par][i], gi = G[i];
+          float vals[16];
 #pragma unroll
-        for (int jj = 0; jj < 32; ++jj) {
-          const int j = half * 32 + jj;
-          sL[i * LS + j] = j < i ? bi * sv[jj] * gexp(gi - G[j], e2) : 0.f;
+          for (int jj = 0; jj < 16; ++jj) {
+            const int j = cg * 16 + jj;
+            vals[jj] = j < i ? bt * sv[jj] * gexp(gi - G[j], e2) : 0.f;
+          }
+          float *Lrow = LB + blk(bi, cg) * 256;
+#pragma unroll
+          for (int g4 = 0; g4 < 4; ++g4)
+            *reinterpret_cast<float4 *>(Lrow + bsw(i & 15, g4 * 4)) =
+                make_float4(vals[g4 * 4], vals[g4 * 4 + 1], vals[g4 * 4 + 2], vals[g4 * 4 + 3]);
         }
       } else {
         const int i = row - 64;
         const float gi = G[i];
+        float vals[16];
 #pragma unroll
-        for (int jj = 0; jj < 32; ++jj) {
-          const int j = half * 32 + jj;
-          st_bf16(sm, OFF_AOP + sw128_offset(64 + i, j), j <= i ? sv[jj] * gexp(gi - G[j], e2) : 0.f);
+        for (int jj = 0; jj < 16; ++jj) {
+          const int j = cg * 16 + jj;
+          vals[jj] = j <= i ? sv[jj] * gexp(gi - G[j], e2) : 0.f;
         }
+        *reinterpret_cast<uint4 *>(sm + OFF_AOP + chunk_off(row, cg * 2)) = pack8(vals);
+        *reinterpret_cast<uint4 *>(sm + OFF_AOP + chunk_off(row, cg * 2 + 1)) = pack8(vals + 8);
       }
     }
     fence_before_sync();
     __syncthreads();
-
-    solve64(sL, sX, sT, tid);
-
-    // X into the operand tiles (and the optional fp32 A slot)
-    for (int e = tid; e < 64 * 64; e += TNT) {
-      const int i = e >> 6, j = e & 63;
-      const float x = sX[i * LS + j];
-      st_bf16(sm, OFF_AOP + sw128_offset(i, j), x);
-      st_bf16(sm, OFF_AT + sw128_offset(j, i), x);
-      if (lead && a.A && i < n) a.A[((c0 + i) * H + h) * GDN_CHUNK + j] = x;
+    // ---- next chunk: loads landed -> its factors and P1 (overlaps this chunk) ------------
+    if (c + 1 < nch) {
+      const float bnext = beta_pend;
+      cp_async_wait<0>();
+      fence_proxy_async();
+      __syncthreads();
+      issue_p1(c + 1);
+      chunk_factors(c + 1, bnext);
     }
-    __syncthreads();  // solve buffers are dead from here
 
-    // [beta Kg | beta V]^T and kgl^T, 8 tokens per item (one 16-byte chunk)
-    for (int e = tid; e < (192 + 128) * 8; e += TNT) {
-      const int f = e >> 3, j0 = (e & 7) * 8;
-      alignas(16) __nv_bfloat16 pk[8];
-      if (f < 128) {
+    // ---- X = (I + L)^-1 ------------------------------------------------------------------
+    solve_blocks(LB, XB, TB, tid);
+    if (row < 64) {  // X into operand rows 0..63 (and the optional fp32 A slot)
+      const int i = row, bi = i >> 4;
+      float vals[16];
+      if (bi >= cg) {
+        const float *Xr = XB + blk(bi, cg) * 256;
 #pragma unroll
-        for (int t = 0; t < 8; ++t) {
-          const int j = j0 + t;
-          const float kv = ld_bf16(kq, (f >> 6) * 16384 + sw128_offset(j, f & 63));
-          pk[t] = __float2bfloat16_rn(Bt[j] * kv * gexp(G[j], e2));
+        for (int g4 = 0; g4 < 4; ++g4) {
+          const float4 t = *reinterpret_cast<const float4 *>(Xr + bsw(i & 15, g4 * 4));
+          vals[g4 * 4] = t.x;
+          vals[g4 * 4 + 1] = t.y;
+          vals[g4 * 4 + 2] = t.z;
+          vals[g4 * 4 + 3] = t.w;
         }
-        *reinterpret_cast<uint4 *>(sm + OFF_B3 + sw128_offset(f, j0)) = *reinterpret_cast<uint4 *>(pk);
-      } else if (f < 192) {
-        const int cc = f - 128;
-#pragma unroll
-        for (int t = 0; t < 8; ++t) {
-          const int j = j0 + t;
-          const float vv = ld_bf16(vs, j * 128 + cc * 2);
-          pk[t] = __float2bfloat16_rn(Bt[j] * vv);
-        }
-        *reinterpret_cast<uint4 *>(sm + OFF_B3 + sw128_offset(f, j0)) = *reinterpret_cast<uint4 *>(pk);
       } else {
-        const int d = f - 192;
 #pragma unroll
-        for (int t = 0; t < 8; ++t) {
-          const int j = j0 + t;
-          const float kv = ld_bf16(kq, (d >> 6) * 16384 + sw128_offset(j, d & 63));
-          pk[t] = __float2bfloat16_rn(kv * gexp(Gl - G[j], e2));
-        }
-        *reinterpret_cast<uint4 *>(sm + OFF_KL + sw128_offset(d, j0)) = *reinterpret_cast<uint4 *>(pk);
+        for (int jj = 0; jj < 16; ++jj) vals[jj] = 0.f;
+      }
+      *reinterpret_cast<uint4 *>(sm + OFF_AOP + chunk_off(i, cg * 2)) = pack8(vals);
+      *reinterpret_cast<uint4 *>(sm + OFF_AOP + chunk_off(i, cg * 2 + 1)) = pack8(vals + 8);
+      if (a.A && lead && i < n) {
+        float4 *Ad = reinterpret_cast<float4 *>(a.A + ((c0 + i) * H + h) * GDN_CHUNK + cg * 16);
+#pragma unroll
+        for (int g4 = 0; g4 < 4; ++g4)
+          Ad[g4] = make_float4(vals[g4 * 4], vals[g4 * 4 + 1], vals[g4 * 4 + 2], vals[g4 * 4 + 3]);
+      }
+    }
+    __syncthreads();
+    // ---- transposed operands: X^T; [b e^G K | b V]^T and (e^(Gl-G) K)^T ----------------------
+    for (int jb = warp; jb < 16 + 32 + 16; jb += NTH / 32) {
+      if (jb < 16) {  // X^T: 4 x 4 blocks of the 64x64 X
+        const int rb = jb >> 2, cb = jb & 3;
+        trans16(TransJob{sb + OFF_AOP, rb * 16, cb * 2, sb + OFF_XT, cb * 16}, nullptr, lane);
+      } else if (jb < 48) {  // K: 4 token blocks x 8 feature blocks -> B3 rows 0..127 and KL
+        const int t = jb - 16, rb = t >> 3, fb = t & 7;
+        const uint32_t src = kq + (fb >> 2) * 16384;
+        const int cc = (fb & 3) * 2;
+        trans16(TransJob{src, rb * 16, cc, sb + OFF_B3, fb * 16}, st.bEG[par], lane);
+        trans16(TransJob{src, rb * 16, cc, sb + OFF_KL, fb * 16}, st.eGL[par], lane);
+      } else {  // V: 4 token blocks x 4 column blocks -> B3 rows 128..191
+        const int t = jb - 48, rb = t >> 2, cb = t & 3;
+        trans16(TransJob{vs, rb * 16, cb * 2, sb + OFF_B3, 128 + cb * 16}, st.beta[par], lane);
       }
     }
     fence_proxy_async();
     __syncthreads();
 
-    // P3a: [X; A_qk] X  -> rows 64..127 hold A_qk X
+    // ---- P3a: [X; A_qk] X -> rows 64..127 hold A_qk X -------------------------------------
     if (tid == 0) {
       fence_after_sync();
-      mma_tiles(tmem + T_S, smem_u32(sm + OFF_AOP), 16384, smem_u32(sm + OFF_AT), 8192, 64,
-                idesc_bf16(128, 64), false);
-      mma_commit(bar);
+      mma_tiles(tmem + T_S0 + 64 * par, sb + OFF_AOP, 16384, sb + OFF_XT, 8192, 64, idesc_bf16(128, 64), false);
     }
-    mma_wait();
-    if ((warp & 3) >= 2) {  // lanes 64..127
-      float t16[16];
-      const int i = row - 64;
-#pragma unroll
-      for (int part = 0; part < 2; ++part) {
-        tmem_ld16(tmem + lane_base + T_S + half * 32 + part * 16, t16);
-        tmem_ld_wait();
-#pragma unroll
-        for (int jj = 0; jj < 16; ++jj)
-          st_bf16(sm, OFF_AOP + sw128_offset(64 + i, half * 32 + part * 16 + jj), t16[jj]);
-      }
+    mma_sync_wait();
+    if (row >= 64) {
+      float sv[16];
+      tmem_ld16(tl + T_S0 + 64 * par + cg * 16, sv);
+      tmem_ld_wait();
+      *reinterpret_cast<uint4 *>(sm + OFF_AOP + chunk_off(row, cg * 2)) = pack8(sv);
+      *reinterpret_cast<uint4 *>(sm + OFF_AOP + chunk_off(row, cg * 2 + 1)) = pack8(sv + 8);
     }
     fence_proxy_async();
     fence_before_sync();
     __syncthreads();
-
-    // P3b: [X; A_qk X] [beta Kg | beta V]
+    // ---- P3b: [X; A_qk X] [b e^G K | b V] ----------------------------------------------------
     if (tid == 0) {
       fence_after_sync();
-      mma_tiles(tmem + T_W, smem_u32(sm + OFF_AOP), 16384, smem_u32(sm + OFF_B3), 24576, 64,
-                idesc_bf16(128, 192), false);
-      mma_commit(bar);
+      mma_tiles(tmem + T_W, sb + OFF_AOP, 16384, sb + OFF_B3, 24576, 64, idesc_bf16(128, 192), false);
     }
-    mma_wait();
-    // operand of P4: rows 0..63 = -w, rows 64..127 = Qg - A_qk w
+    mma_sync_wait();
+    // ---- operand of P4: rows 0..63 = -w, rows 64..127 = e^G Q - A_qk w ----------------------
+#pragma unroll
+    for (int part = 0; part < 2; ++part) {
+      const int d0 = cg * 32 + part * 16;  // 16 key columns
+      float sv[16];
+      tmem_ld16(tl + T_W + d0, sv);
+      tmem_ld_wait();
+      const int kb = d0 >> 6, ch = (d0 & 63) >> 3;
+      float vals[16];
+      if (row < 64) {
+#pragma unroll
+        for (int t = 0; t < 16; ++t) vals[t] = -sv[t];
+      } else {
+        const float eg = st.eG[par][row - 64];
+        float qf[16];
+        const uint8_t *qrow = sm + OFF_KQ + par * SZ_KQ + kb * 16384;
+        unpack8(*reinterpret_cast<const uint4 *>(qrow + chunk_off(row, ch)), qf);
+        unpack8(*reinterpret_cast<const uint4 *>(qrow + chunk_off(row, ch + 1)), qf + 8);
+#pragma unroll
+        for (int t = 0; t < 16; ++t) vals[t] = fmaf(qf[t], eg, -sv[t]);
+      }
+      uint8_t *dst = sm + OFF_WQ + kb * 16384;
+      *reinterpret_cast<uint4 *>(dst + chunk_off(row, ch)) = pack8(vals);
+      *reinterpret_cast<uint4 *>(dst + chunk_off(row, ch + 1)) = pack8(vals + 8);
+    }
+    fence_proxy_async();
+    fence_before_sync();
+    __syncthreads();
+    // ---- P4: [v_new; o/scale] = [u; A_qk u] + [-w; q'] h ---------------------------------------
+    if (tid == 0) {
+      fence_after_sync();
+      mma_tiles(tmem + T_W + 128, sb + OFF_WQ, 16384, sb + OFF_HT, 8192, 128, idesc_bf16(128, 64), true);
+    }
+    mma_sync_wait();
     {
-      float t16[16];
+      float sv[16];
+      tmem_ld16(tl + T_W + 128 + cg * 16, sv);
+      tmem_ld_wait();
+      if (row < 64) {  // v_new row-major into the staging tile
+        *reinterpret_cast<uint4 *>(sm + OFF_STG + chunk_off(row, cg * 2)) = pack8(sv);
+        *reinterpret_cast<uint4 *>(sm + OFF_STG + chunk_off(row, cg * 2 + 1)) = pack8(sv + 8);
+      } else if (o && row - 64 < n) {
 #pragma unroll
-      for (int part = 0; part < 4; ++part) {
-        const int dcol = half * 64 + part * 16;
-        tmem_ld16(tmem + lane_base + T_W + dcol, t16);
-        tmem_ld_wait();
-        if (row < 64) {
-#pragma unroll
-          for (int jj = 0; jj < 16; ++jj) {
-            const int d = dcol + jj;
-            st_bf16(sm, OFF_WQ + (d >> 6) * 16384 + sw128_offset(row, d & 63), -t16[jj]);
-          }
-        } else {
-          const int i = row - 64;
-          const float eg = gexp(G[i], e2);
-#pragma unroll
-          for (int jj = 0; jj < 16; ++jj) {
-            const int d = dcol + jj;
-            const float qv = ld_bf16(kq, (d >> 6) * 16384 + sw128_offset(64 + i, d & 63));
-            st_bf16(sm, OFF_WQ + (d >> 6) * 16384 + sw128_offset(row, d & 63), qv * eg - t16[jj]);
-          }
-        }
+        for (int t = 0; t < 16; ++t) sv[t] *= scale;
+        uint4 *dst = reinterpret_cast<uint4 *>(o + ((c0 + row - 64) * H + h) * GDN_DV + col0 + cg * 16);
+        dst[0] = pack8(sv);
+        dst[1] = pack8(sv + 8);
       }
+    }
+    __syncthreads();
+    if (warp < 16) {  // v_new^T: 4 x 4 blocks
+      const int rb = warp >> 2, cb = warp & 3;
+      trans16(TransJob{sb + OFF_STG, rb * 16, cb * 2, sb + OFF_VN, cb * 16}, nullptr, lane);
     }
     fence_proxy_async();
     fence_before_sync();
     __syncthreads();
-
-    // P4: [v_new; o/scale] = [u; A_qk u] + [-w; q'] h
+    // ---- P5: (e^(Gl-G) K)^T v_new --------------------------------------------------------------
     if (tid == 0) {
       fence_after_sync();
-      mma_tiles(tmem + T_W + 128, smem_u32(sm + OFF_WQ), 16384, smem_u32(sm + OFF_HT), 8192, 128,
-                idesc_bf16(128, 64), true);
-      mma_commit(bar);
+      mma_tiles(tmem + T_P5, sb + OFF_KL, 16384, sb + OFF_VN, 8192, 64, idesc_bf16(128, 64), false);
     }
-    mma_wait();
+    mma_sync_wait();
     {
-      float t16[16];
+      float sv[16];
+      tmem_ld16(tl + T_P5 + cg * 16, sv);
+      tmem_ld_wait();
+      const float el = st.EL[par];
 #pragma unroll
-      for (int part = 0; part < 2; ++part) {
-        const int cb = half * 32 + part * 16;
-        tmem_ld16(tmem + lane_base + T_W + 128 + cb, t16);
-        tmem_ld_wait();
-        if (row < 64) {
-#pragma unroll
-          for (int jj = 0; jj < 16; ++jj) st_bf16(sm, OFF_VN + sw128_offset(cb + jj, row), t16[jj]);
-        } else if (row - 64 < n) {
-          alignas(16) __nv_bfloat16 pk[16];
-#pragma unroll
-          for (int jj = 0; jj < 16; ++jj) pk[jj] = __float2bfloat16_rn(scale * t16[jj]);
-          uint4 *dst = reinterpret_cast<uint4 *>(o + ((c0 + row - 64) * H + h) * GDN_DV + col0 + cb);
-          dst[0] = reinterpret_cast<uint4 *>(pk)[0];
-          dst[1] = reinterpret_cast<uint4 *>(pk)[1];
-        }
-      }
+      for (int t = 0; t < 16; ++t) hreg[t] = fmaf(el, hreg[t], sv[t]);
     }
-    fence_proxy_async();
     fence_before_sync();
-    __syncthreads();
-
-    // P5: kgl^T v_new
-    if (tid == 0) {
-      fence_after_sync();
-      mma_tiles(tmem + T_S, smem_u32(sm + OFF_KL), 16384, smem_u32(sm + OFF_VN), 8192, 64,
-                idesc_bf16(128, 64), false);
-      mma_commit(bar);
-    }
-    mma_wait();
-    {
-      const float el = gexp(Gl, e2);
-      float t16[16];
-#pragma unroll
-      for (int part = 0; part < 2; ++part) {
-        tmem_ld16(tmem + lane_base + T_S + half * 32 + part * 16, t16);
-        tmem_ld_wait();
-#pragma unroll
-        for (int jj = 0; jj < 16; ++jj) hreg[part * 16 + jj] = fmaf(el, hreg[part * 16 + jj], t16[jj]);
-      }
-    }
-    write_ht_bf16();
-    if (tid < 64) {
-      sG[(stage ^ 1) * 64 + tid] = g_next;
-      sBeta[(stage ^ 1) * 64 + tid] = b_next;
-    }
+    __syncthreads();  // the staging tile (v_new) has been consumed
+    write_h_operand();
+    // ---- loads of chunk c+2 into this chunk's stage ------------------------------------------
+    if (c + 2 < nch) issue_loads(c + 2);
     fence_proxy_async();
-    fence_before_sync();
     if (__syncthreads_or(bad)) bad = true;
   }
 
   if (bad) {
-    if (tid == 0) raise_device_flag(a.dev_flag, kDevTimeout);
-    cp_async_wait_all();
-    mbar_wait(bar, phase & 1, WAIT_LIMIT);  // let an MMA still in flight finish
-  } else {
-    float *dst = nullptr;
-    if (a.ht && (a.nseg == 0 || s == a.nseg - 1))
-      dst = a.ht + ((int64_t)state_idx * H + h) * GDN_DK * GDN_DV;
-    if (dst) {
-      float *p = dst + (int64_t)row * GDN_DV + col0 + half * 32;
-#pragma unroll
-      for (int j = 0; j < 32; ++j) p[j] = hreg[j];
+    if (tid == 0) {
+      raise_device_flag(a.dev_flag, kDevTimeout);
+      mma_commit(&st.bar_m);  // arrives once every MMA issued so far has finished
     }
+    cp_async_wait<0>();
+    mbar_wait(&st.bar_m, ph_m & 1, WAIT_LIMIT);
+  } else if (a.ht && (a.nseg == 0 || s == a.nseg - 1)) {
+    float4 *dst = reinterpret_cast<float4 *>(a.ht + ((int64_t)state_idx * H + h) * GDN_DK * GDN_DV +
+                                             (int64_t)row * GDN_DV + col0 + cg * 16);
+#pragma unroll
+    for (int g4 = 0; g4 < 4; ++g4)
+      dst[g4] = make_float4(hreg[g4 * 4], hreg[g4 * 4 + 1], hreg[g4 * 4 + 2], hreg[g4 * 4 + 3]);
   }
   fence_before_sync();
   __syncthreads();
@@ -552,7 +668,7 @@ cudaError_t launch_tc_fwd(const SimtFwdArgs &a, dim3 grid, cudaStream_t st) {
   cudaError_t e = cudaFuncSetAttribute(tc_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        SMEM_BYTES);
   if (e != cudaSuccess) return e;
-  tc_fwd_kernel<<<grid, TNT, SMEM_BYTES, st>>>(a);
+  tc_fwd_kernel<<<grid, NTH, SMEM_BYTES, st>>>(a);
   return cudaGetLastError();
 }
 

@@ -380,7 +380,9 @@ gdn_status gdn_chunk_bwd(const gdn_problem *p, const void *q, const void *k, con
   f.g_cum_in = g_cumsum;
   f.A_in = A;
   f.dev_flag = flag;
-  cudaError_t e = gdn::launch_simt_fwd(f, pk, bf, dim3(GDN_DV / gdn::simt_fwd_bv(), p->H, runs), s);
+  cudaError_t e = use_tensor_cores(p)
+                      ? gdn::launch_tc_fwd(f, dim3(GDN_DV / gdn::tc_fwd_bv(), p->H, runs), s)
+                      : gdn::launch_simt_fwd(f, pk, bf, dim3(GDN_DV / gdn::simt_fwd_bv(), p->H, runs), s);
   if (e != cudaSuccess) return cuda_fail(e, "backward state recompute launch");
 
   gdn::BwdArgs b{};
