@@ -69,7 +69,7 @@ constexpr int DVP = DBV + 1;
 
 template <bool PER_KEY>
 constexpr size_t dhu_smem_floats() {
-  return 3 * 64 * KP + (PER_KEY ? 64 * KP : 64) + 2 * 64 * CP + 128 * DVP + 3 * 64 * DVP + 64 + 128;
+  return 3 * 64 * KP + (PER_KEY ? 64 * KP : 3 * 64) + 2 * 64 * CP + 128 * DVP + 3 * 64 * DVP + 64 + 128;
 }
 
 template <typename T, bool PER_KEY>
@@ -78,8 +78,8 @@ __global__ void __launch_bounds__(NTH) dhu_kernel(BwdArgs a) {
   float *sKl = smem;                        // K (.) base^(G_last - G)
   float *sQg = sKl + 64 * KP;               // scale Q (.) base^G
   float *sKg = sQg + 64 * KP;               // K (.) base^G
-  float *sG = sKg + 64 * KP;                // cumulative gate
-  float *sX = sG + (PER_KEY ? 64 * KP : 64);
+  float *sG = sKg + 64 * KP;                // cumulative gate (scalar gate: + e^G, e^(Gl-G))
+  float *sX = sG + (PER_KEY ? 64 * KP : 3 * 64);
   float *sAqk = sX + 64 * CP;
   float *sDH = sAqk + 64 * CP;              // [128][DVP]
   float *sDO = sDH + 128 * DVP;             // [64][DVP]
@@ -183,15 +183,21 @@ __global__ void __launch_bounds__(NTH) dhu_kernel(BwdArgs a) {
 #pragma unroll
         for (int y = 0; y < 4; ++y) sAqk[(m0 + x) * CP + n0 + y] = (n0 + y <= m0 + x) ? acc[x][y] : 0.f;
     }
+    if (!PER_KEY && tid < 64) {  // per-token gate factors (scalar gate)
+      sG[64 + tid] = gate_pow(sG[tid], e2);
+      sG[128 + tid] = gate_pow(sG[63] - sG[tid], e2);
+    }
     __syncthreads();
     for (int idx = tid; idx < 64 * GDN_DK; idx += NTH) {
       const int i = idx >> 7, d = idx & 127;
       const float Gi = PER_KEY ? sG[i * KP + d] : sG[i];
       const float Gl = PER_KEY ? sG[63 * KP + d] : sG[63];
       const float kk = sKl[i * KP + d];
-      sKg[i * KP + d] = kk * gate_pow(Gi, e2);
-      sQg[i * KP + d] *= a.scale * gate_pow(Gi, e2);
-      sKl[i * KP + d] = kk * gate_pow(Gl - Gi, e2);
+      const float eg = PER_KEY ? gate_pow(Gi, e2) : sG[64 + i];
+      const float egl = PER_KEY ? gate_pow(Gl - Gi, e2) : sG[128 + i];
+      sKg[i * KP + d] = kk * eg;
+      sQg[i * KP + d] *= a.scale * eg;
+      sKl[i * KP + d] = kk * egl;
     }
     if (tid < GDN_DK) sEL[tid] = gate_pow(PER_KEY ? sG[63 * KP + tid] : sG[63], e2);
     __syncthreads();
@@ -272,7 +278,7 @@ constexpr int LVP = LBV + 1;
 template <bool PER_KEY>
 constexpr size_t local_smem_floats() {
   // K, Q, (G), X, P, Aqk, slice buffers, beta, dbeta, EL, dGLh, dGlast, dGrow
-  return 2 * 64 * KP + (PER_KEY ? 64 * KP : 64) + 3 * 64 * CP +
+  return 2 * 64 * KP + (PER_KEY ? 64 * KP : 3 * 64) + 3 * 64 * CP +
          (2 * 128 * LVP + 6 * 64 * LVP) + 64 + 64 + 128 + 128 + 128 + 64;
 }
 
@@ -281,8 +287,8 @@ __global__ void __launch_bounds__(NTH, 1) local_kernel(BwdArgs a) {
   extern __shared__ float smem[];
   float *sK = smem;
   float *sQ = sK + 64 * KP;
-  float *sG = sQ + 64 * KP;
-  float *sX = sG + (PER_KEY ? 64 * KP : 64);
+  float *sG = sQ + 64 * KP;  // cumulative gate (scalar gate: + e^G, e^(Gl-G))
+  float *sX = sG + (PER_KEY ? 64 * KP : 3 * 64);
   float *sP = sX + 64 * CP;     // gated K K^T (strict lower), later dP (.) Gamma
   float *sAqk = sP + 64 * CP;   // gated Q K^T (lower incl), later dA_qk (.) Gamma
   float *sSl = sAqk + 64 * CP;  // slice region
@@ -380,6 +386,16 @@ __global__ void __launch_bounds__(NTH, 1) local_kernel(BwdArgs a) {
   }
   auto Gv = [&](int i, int d) { return PER_KEY ? sG[i * KP + d] : sG[i]; };
   if (tid < GDN_DK) sEL[tid] = gate_pow(Gv(63, tid), e2);
+  if (!PER_KEY && tid >= 128 && tid < 192) {  // per-token gate factors (scalar gate)
+    const int i = tid - 128;
+    sG[64 + i] = gate_pow(sG[i], e2);
+    sG[128 + i] = gate_pow(sG[63] - sG[i], e2);
+  }
+  // e^G and e^(G_last - G) of token i, key channel d
+  auto EG = [&](int i, int d) { return PER_KEY ? gate_pow(sG[i * KP + d], e2) : sG[64 + i]; };
+  auto EGL = [&](int i, int d) {
+    return PER_KEY ? gate_pow(sG[63 * KP + d] - sG[i * KP + d], e2) : sG[128 + i];
+  };
 
   // ---- gated Gram matrices ------------------------------------------------
   {
@@ -465,7 +481,7 @@ __global__ void __launch_bounds__(NTH, 1) local_kernel(BwdArgs a) {
       const int i = tid / (LBV / 4), c4 = (tid % (LBV / 4)) * 4;
       float acc[4] = {0.f, 0.f, 0.f, 0.f};
       for (int d = 0; d < GDN_DK; ++d) {
-        const float kg = sK[i * KP + d] * gate_pow(Gv(i, d), e2);
+        const float kg = sK[i * KP + d] * EG(i, d);
 #pragma unroll
         for (int y = 0; y < 4; ++y) acc[y] = fmaf(kg, sHs[d * LVP + c4 + y], acc[y]);
       }
@@ -599,7 +615,7 @@ __global__ void __launch_bounds__(NTH, 1) local_kernel(BwdArgs a) {
 #pragma unroll
     for (int y = 0; y < 8; ++y) {
       const int i = gm0 + x, d = gn0 + y;
-      const float G = Gv(i, d), eg = gate_pow(G, e2), egl = gate_pow(Gv(63, d) - G, e2);
+      const float eg = EG(i, d), egl = EGL(i, d);
       const float kk = sK[i * KP + d], qq = sQ[i * KP + d];
       const float dQg = a.scale * aQg[x][y];
       rdq[x][y] = dQg * eg;

@@ -29,7 +29,7 @@ constexpr int VP = BV + 1;        // padded row stride of [*][32] tiles
 
 template <bool PER_KEY>
 constexpr size_t smem_floats() {
-  return 3 * 64 * KP + (PER_KEY ? 64 * KP : 64) + 2 * 64 * CP + 128 * VP + 3 * 64 * VP + 64 +
+  return 3 * 64 * KP + (PER_KEY ? 64 * KP : 3 * 64) + 2 * 64 * CP + 128 * VP + 3 * 64 * VP + 64 +
          128;
 }
 
@@ -39,8 +39,8 @@ __global__ void __launch_bounds__(NTH) simt_chunk_kernel(SimtFwdArgs a) {
   float *sK = smem;                                // K, later K (.) base^(G_last - G)
   float *sQ = sK + 64 * KP;                        // Q, later scale Q (.) base^G
   float *sKg = sQ + 64 * KP;                       // L during the solve, then K (.) base^G
-  float *sG = sKg + 64 * KP;                       // cumulative gate [64][KP] or [64]
-  float *sX = sG + (PER_KEY ? 64 * KP : 64);       // X = (I + L)^-1
+  float *sG = sKg + 64 * KP;                       // cumulative gate [64][KP], or [64] + e^G + e^(Gl-G)
+  float *sX = sG + (PER_KEY ? 64 * KP : 3 * 64);   // X = (I + L)^-1
   float *sAqk = sX + 64 * CP;                      // gated causal Q K^T
   float *sH = sAqk + 64 * CP;                      // state slice [128][VP]
   float *sV = sH + 128 * VP;                       // value slice
@@ -260,6 +260,11 @@ __global__ void __launch_bounds__(NTH) simt_chunk_kernel(SimtFwdArgs a) {
     }
     __syncthreads();
 
+    if (!PER_KEY && tid >= 64 && tid < 128) {  // per-token gate factors (scalar gate)
+      const int i = tid - 64;
+      sG[64 + i] = gate_pow(sG[i], e2);
+      sG[128 + i] = gate_pow(sG[63] - sG[i], e2);
+    }
     // ---- X = (I + L)^-1 by forward substitution, one column per thread ---
     if (a.A_in) {
       for (int idx = tid; idx < 64 * 64; idx += NTH) {
@@ -291,9 +296,11 @@ __global__ void __launch_bounds__(NTH) simt_chunk_kernel(SimtFwdArgs a) {
       const float Gi = PER_KEY ? sG[i * KP + d] : sG[i];
       const float Gl = PER_KEY ? sG[63 * KP + d] : sG[63];
       const float kk = sK[i * KP + d];
-      sKg[i * KP + d] = kk * gate_pow(Gi, e2);
-      sQ[i * KP + d] *= a.scale * gate_pow(Gi, e2);
-      sK[i * KP + d] = kk * gate_pow(Gl - Gi, e2);
+      const float eg = PER_KEY ? gate_pow(Gi, e2) : sG[64 + i];
+      const float egl = PER_KEY ? gate_pow(Gl - Gi, e2) : sG[128 + i];
+      sKg[i * KP + d] = kk * eg;
+      sQ[i * KP + d] *= a.scale * eg;
+      sK[i * KP + d] = kk * egl;
     }
     if (tid < GDN_DK) sEL[tid] = gate_pow(PER_KEY ? sG[63 * KP + tid] : sG[63], e2);
     __syncthreads();

@@ -53,7 +53,7 @@ constexpr int OFF_WQ = OFF_KL + 16384;           // [-w; q']               2 K-b
 constexpr int OFF_HT = OFF_WQ + 32768;           // h^T                    2 K-blocks x 64 rows
 constexpr int OFF_VN = OFF_HT + 16384;           // v_new^T                64 rows, K = 64
 constexpr int OFF_SMALL = OFF_VN + 8192;
-constexpr int SMALL_BYTES = 4096;
+constexpr int SMALL_BYTES = 17408;
 constexpr int SMEM_BYTES = OFF_SMALL + SMALL_BYTES + 1024;
 static_assert(SMEM_BYTES <= 232448, "shared memory");
 // aliases: the solve's fp32 blocks live in WQ (free until WQ is formed); the
@@ -61,8 +61,8 @@ static_assert(SMEM_BYTES <= 232448, "shared memory");
 // after P3b)
 constexpr int OFF_LB = OFF_WQ;               // 10 lower 16x16 fp32 blocks of L
 constexpr int OFF_XB = OFF_WQ + 10 * 1024;   // 10 blocks of X
-constexpr int OFF_TB = OFF_WQ + 20 * 1024;   // 3 scratch blocks (one per level warp)
-static_assert(23 * 1024 <= 32768, "solve buffers");
+constexpr int OFF_TB = OFF_WQ + 20 * 1024;   // 4 scratch blocks (one per solve warp)
+static_assert(24 * 1024 <= 32768, "solve buffers");
 constexpr int OFF_STG = OFF_B3;              // staging: v_new 64 rows (8 KB), h 128 rows (16 KB)
 static_assert(16384 <= 24576, "staging");
 
@@ -73,17 +73,15 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, uint32
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(bytes)
                : "memory");
 }
-__device__ __forceinline__ void cp_async4(uint32_t dst, const void *src, uint32_t bytes) {
-  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src), "r"(bytes)
-               : "memory");
-}
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 template <int N>
 __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
-__device__ __forceinline__ float gexp(float x, bool e2) { return e2 ? exp2f(x) : __expf(x); }
+// decay factor base^x: base 2 (E2) or e, chosen at compile time
+template <bool E2>
+__device__ __forceinline__ float gexp(float x) { return E2 ? exp2f(x) : __expf(x); }
 
 __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
   const __nv_bfloat162 t = __floats2bfloat162_rn(a, b);
@@ -187,7 +185,10 @@ __device__ __forceinline__ void acc_store(float *C, const float (&acc)[2][4], in
   }
 }
 
-// X = (I + L)^-1 from the lower 16x16 blocks of a strictly-lower L; all threads.
+__device__ __forceinline__ void solve_group_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+// X = (I + L)^-1 from the lower 16x16 blocks of a strictly-lower L; called by
+// warps 0..3 only (named barrier 1).
 __device__ void solve_blocks(const float *L, float *X, float *T, int tid) {
   const int warp = tid >> 5, lane = tid & 31;
   if (tid < 64) {  // diagonal blocks: one column per thread, fp32 forward substitution
@@ -207,26 +208,48 @@ __device__ void solve_blocks(const float *L, float *X, float *T, int tid) {
 #pragma unroll
     for (int r = 0; r < 16; ++r) Xb[bsw(r, c)] = x[r];
   }
-  __syncthreads();
-  for (int dist = 1; dist <= 3; ++dist) {  // X_ij = -X_ii sum_k L_ik X_kj, by block distance
-    if (warp < 4 - dist) {
-      const int bj = warp, bi = warp + dist;
-      float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-      for (int kb = bj; kb < bi; ++kb) mm16_tf32(L + blk(bi, kb) * 256, X + blk(kb, bj) * 256, acc, lane);
-      float *Tw = T + warp * 256;
-      acc_store(Tw, acc, lane, 1.f);
-      __syncwarp();
-      float acc2[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-      mm16_tf32(X + blk(bi, bi) * 256, Tw, acc2, lane);
-      acc_store(X + blk(bi, bj) * 256, acc2, lane, -1.f);
-    }
-    __syncthreads();
+  solve_group_sync();
+  // 32x32 halves: X_10 = -X_11 L_10 X_00 and X_32 = -X_33 L_32 X_22 (warps 0, 1)
+  if (warp < 2) {
+    const int b0 = 2 * warp, b1 = b0 + 1;
+    float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+    mm16_tf32(L + blk(b1, b0) * 256, X + blk(b0, b0) * 256, acc, lane);
+    float *Tw = T + warp * 256;
+    acc_store(Tw, acc, lane, 1.f);
+    __syncwarp();
+    float acc2[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+    mm16_tf32(X + blk(b1, b1) * 256, Tw, acc2, lane);
+    acc_store(X + blk(b1, b0) * 256, acc2, lane, -1.f);
   }
+  solve_group_sync();
+  // lower-left 32x32: Tb = L_bt X_top, then X_bt = -X_bot Tb (one 16x16 block per warp)
+  {
+    const int r = 2 + (warp >> 1), cc = warp & 1;  // block (r, cc), r in {2,3}, cc in {0,1}
+    float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+    for (int kb = cc; kb < 2; ++kb) mm16_tf32(L + blk(r, kb) * 256, X + blk(kb, cc) * 256, acc, lane);
+    acc_store(T + warp * 256, acc, lane, 1.f);  // T block (r, cc), in warp order
+  }
+  solve_group_sync();
+  {
+    const int r = 2 + (warp >> 1), cc = warp & 1;
+    float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+    for (int kb = 2; kb <= r; ++kb)  // X_bot rows r, columns kb; T rows kb (warp 2*(kb-2)+cc)
+      mm16_tf32(X + blk(r, kb) * 256, T + (2 * (kb - 2) + cc) * 256, acc, lane);
+    acc_store(X + blk(r, cc) * 256, acc, lane, -1.f);
+  }
+  solve_group_sync();
 }
 
 struct TcState {
   float G[2][64], eG[2][64], eGL[2][64], bEG[2][64];  // per chunk parity
+  // e^(G_i - G_r(i)) with r(i) the first row of i's 16-row block, and
+  // e^(G_16b - G_j) for j < 16b: the Gram gate of an off-diagonal block is their
+  // product (both factors <= 1, no overflow for any gate strength)
+  float eA[2][64], eB[2][4][64];
+  // gate of the four diagonal 16x16 blocks: base^(G_{16b+r} - G_{16b+j}) for j <= r, else 0
+  alignas(16) float gd[2][4][16][20];  // rows padded to 20: conflict-free float4 reads
   float g[2][64];                                     // raw gate per load stage
+  float braw[2][64];                                  // raw beta per load stage
   float beta[2][64];
   float EL[2];
   uint64_t bar_s[2], bar_m;
@@ -234,6 +257,7 @@ struct TcState {
 };
 static_assert(sizeof(TcState) <= SMALL_BYTES, "small state");
 
+template <bool E2>
 __global__ void __launch_bounds__(NTH, 1) tc_fwd_kernel(SimtFwdArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -250,7 +274,6 @@ __global__ void __launch_bounds__(NTH, 1) tc_fwd_kernel(SimtFwdArgs a) {
   const int row = q4 * 32 + lane;  // tensor-memory lane = matrix row
   const int H = a.H, h = blockIdx.y, z = blockIdx.z;
   const int col0 = blockIdx.x * TBV;
-  const bool e2 = a.use_exp2 != 0;
   const float scale = a.scale;
   const __nv_bfloat16 *q = static_cast<const __nv_bfloat16 *>(a.q);
   const __nv_bfloat16 *k = static_cast<const __nv_bfloat16 *>(a.k);
@@ -307,7 +330,7 @@ __global__ void __launch_bounds__(NTH, 1) tc_fwd_kernel(SimtFwdArgs a) {
   fence_after_sync();
   const uint32_t tmem = st.tmem;
   const uint32_t tl = tmem + ((uint32_t)(q4 * 32) << 16);  // this warp's lane quarter
-  uint32_t ph_s[2] = {0, 0}, ph_m = 0;
+  uint32_t ph_s0 = 0, ph_s1 = 0, ph_m = 0;
   bool bad = false;
   auto wait_bar = [&](uint64_t *bar, uint32_t &ph) {
     if (!mbar_wait(bar, ph & 1, WAIT_LIMIT)) bad = true;
@@ -321,13 +344,13 @@ __global__ void __launch_bounds__(NTH, 1) tc_fwd_kernel(SimtFwdArgs a) {
   };
 
   // ---- loads -----------------------------------------------------------------------
-  float beta_pend = 0.f;  // beta row of the most recently issued chunk (threads < 64)
   auto issue_loads = [&](int64_t c) {
     const int stage = (int)(c & 1);
     const int64_t c0 = r0 + c * GDN_CHUNK;
     const int n = chunk_rows(c);
     const uint32_t kq = sb + OFF_KQ + stage * SZ_KQ;
     const uint32_t vb = sb + OFF_V + stage * SZ_V;
+#pragma unroll
     for (int x = tid; x < 2048 + 512; x += NTH) {
       if (x < 2048) {
         const int which = x >> 10, r = (x >> 4) & 63, f16 = x & 15;
@@ -341,21 +364,39 @@ __global__ void __launch_bounds__(NTH, 1) tc_fwd_kernel(SimtFwdArgs a) {
         cp_async16(vb + chunk_off(r, c8), src, valid ? 16u : 0u);
       }
     }
-    if (tid < 64) {
-      const bool valid = tid < n;
-      const float *gsrc = a.g_cum_in ? a.g_cum_in : a.g;
-      cp_async4(smem_u32(&st.g[stage][tid]), gsrc + (c0 + (valid ? tid : 0)) * H + h, valid ? 4u : 0u);
-      beta_pend = valid ? __bfloat162float(beta[(c0 + tid) * H + h]) : 0.f;
-    }
     cp_async_commit();
   };
+  // gate and beta rows of chunk c (threads < 64; zero past the run end), loaded
+  // into registers well before they are stored for chunk_factors
+  const float *gsrc = a.g_cum_in ? a.g_cum_in : a.g;
+  auto load_gb = [&](int64_t c) -> float2 {
+    float2 gb = make_float2(0.f, 0.f);
+    if (tid < 64 && c < nch) {
+      const int64_t c0 = r0 + c * GDN_CHUNK;
+      if (tid < chunk_rows(c)) {
+        gb.x = gsrc[(c0 + tid) * H + h];
+        gb.y = __bfloat162float(beta[(c0 + tid) * H + h]);
+      }
+    }
+    return gb;
+  };
+  auto store_gb = [&](int64_t c, float2 gb) {
+    if (tid < 64) {
+      st.g[c & 1][tid] = gb.x;
+      st.braw[c & 1][tid] = gb.y;
+    }
+  };
   // cumulative gate and per-token factors of chunk c once its loads landed
-  auto chunk_factors = [&](int64_t c, float bval) {
+  // Run by warps 4..15 only (named barrier 2), so that warps 0..3 can go on with
+  // the solve; the results are read after the next CTA-wide barrier.
+  auto chunk_factors = [&](int64_t c) {
+    if (warp < 4) return;
     const int par = (int)(c & 1);
     const int n = chunk_rows(c);
+    const int t = tid - 128;  // 0..383
     if (a.g_cum_in) {  // saved cumulative gate; rows past the end repeat the last one
-      if (tid < 64) st.G[par][tid] = st.g[par][min(tid, n - 1)];
-    } else if (warp == 0) {
+      if (t < 64) st.G[par][t] = st.g[par][min(t, n - 1)];
+    } else if (warp == 4) {
       const float x0 = st.g[par][2 * lane], x1 = st.g[par][2 * lane + 1];
       const float pair = x0 + x1;
       float incl = pair;
@@ -368,15 +409,23 @@ __global__ void __launch_bounds__(NTH, 1) tc_fwd_kernel(SimtFwdArgs a) {
       st.G[par][2 * lane] = ex + x0;
       st.G[par][2 * lane + 1] = ex + pair;
     }
-    if (tid < 64) st.beta[par][tid] = bval;
-    __syncthreads();
-    if (tid < 64) {
-      const float G = st.G[par][tid], Gl = st.G[par][63];
-      st.eG[par][tid] = gexp(G, e2);
-      st.eGL[par][tid] = gexp(Gl - G, e2);
-      st.bEG[par][tid] = st.beta[par][tid] * gexp(G, e2);
-      if (tid == 0) st.EL[par] = gexp(Gl, e2);
-      if (a.g_cumsum && blockIdx.x == 0 && tid < n) a.g_cumsum[(r0 + c * GDN_CHUNK + tid) * H + h] = G;
+    if (t < 64) st.beta[par][t] = st.braw[par][t];
+    asm volatile("bar.sync 2, 384;" ::: "memory");
+    if (t < 64) {
+      const float G = st.G[par][t], Gl = st.G[par][63];
+      st.eG[par][t] = gexp<E2>(G);
+      st.eGL[par][t] = gexp<E2>(Gl - G);
+      st.bEG[par][t] = st.beta[par][t] * gexp<E2>(G);
+      st.eA[par][t] = gexp<E2>(G - st.G[par][t & ~15]);
+#pragma unroll
+      for (int bb = 1; bb < 4; ++bb)
+        st.eB[par][bb][t] = t < 16 * bb ? gexp<E2>(st.G[par][16 * bb] - G) : 0.f;
+      if (t == 0) st.EL[par] = gexp<E2>(Gl);
+      if (a.g_cumsum && blockIdx.x == 0 && t < n) a.g_cumsum[(r0 + c * GDN_CHUNK + t) * H + h] = G;
+    }
+    for (int e = t; e < 4 * 256; e += NTH - 128) {  // diagonal-block gates
+      const int bb = e >> 8, r = (e >> 4) & 15, j = e & 15;
+      st.gd[par][bb][r][j] = j <= r ? gexp<E2>(st.G[par][16 * bb + r] - st.G[par][16 * bb + j]) : 0.f;
     }
   };
   auto issue_p1 = [&](int64_t c) {  // S = [K; Q] K^T
@@ -414,12 +463,13 @@ __global__ void __launch_bounds__(NTH, 1) tc_fwd_kernel(SimtFwdArgs a) {
   // ---- prologue -----------------------------------------------------------------------
   if (nch > 0) {
     issue_loads(0);
-    const float beta0 = beta_pend;
+    store_gb(0, load_gb(0));
+    store_gb(1, load_gb(1));
     cp_async_wait<0>();
     fence_proxy_async();
     __syncthreads();
     issue_p1(0);
-    chunk_factors(0, beta0);
+    chunk_factors(0);
     if (nch > 1) issue_loads(1);
   }
   write_h_operand();
@@ -434,6 +484,7 @@ __global__ void __launch_bounds__(NTH, 1) tc_fwd_kernel(SimtFwdArgs a) {
     const uint32_t kq = sb + OFF_KQ + par * SZ_KQ;
     const uint32_t vs = sb + OFF_V + par * SZ_V;
     const float *G = st.G[par];
+    const float2 gb_pf = load_gb(c + 2);  // gate and beta rows of chunk c+2, stored at the end
 
     if (a.h_chunks) {  // entry state of chunk c
       const int64_t slot = a.cu ? (chunk_base + c) * H + h : ((int64_t)b * H + h) * NT + chunk_base + c;
@@ -445,7 +496,7 @@ __global__ void __launch_bounds__(NTH, 1) tc_fwd_kernel(SimtFwdArgs a) {
     }
 
     // ---- gated Gram rows: L (fp32 blocks) and A_qk (operand rows 64..127) --------------
-    wait_bar(&st.bar_s[par], ph_s[par]);
+    if (par) wait_bar(&st.bar_s[1], ph_s1); else wait_bar(&st.bar_s[0], ph_s0);
     {
       float sv[16];
       tmem_ld16(tl + T_S0 + 64 * par + cg * 16, sv);
@@ -455,10 +506,18 @@ __global__ void __launch_bounds__(NTH, 1) tc_fwd_kernel(SimtFwdArgs a) {
         if (bi >= cg) {
           const float bt = st.beta[par][i], gi = G[i];
           float vals[16];
+          if (cg < bi) {  // off-diagonal block: factorised gate
+            const float fa = bt * st.eA[par][i];
+            const float *fb = st.eB[par][bi] + cg * 16;
 #pragma unroll
-          for (int jj = 0; jj < 16; ++jj) {
-            const int j = cg * 16 + jj;
-            vals[jj] = j < i ? bt * sv[jj] * gexp(gi - G[j], e2) : 0.f;
+            for (int jj = 0; jj < 16; ++jj) vals[jj] = fa * sv[jj] * fb[jj];
+          } else {  // diagonal block: tabulated gate, strictly lower part
+            float gdr[16];
+#pragma unroll
+            for (int k4 = 0; k4 < 4; ++k4)
+              *reinterpret_cast<float4 *>(gdr + 4 * k4) = reinterpret_cast<const float4 *>(st.gd[par][bi][i & 15])[k4];
+#pragma unroll
+            for (int jj = 0; jj < 16; ++jj) vals[jj] = jj < (i & 15) ? bt * sv[jj] * gdr[jj] : 0.f;
           }
           float *Lrow = LB + blk(bi, cg) * 256;
 #pragma unroll
@@ -467,13 +526,24 @@ __global__ void __launch_bounds__(NTH, 1) tc_fwd_kernel(SimtFwdArgs a) {
                 make_float4(vals[g4 * 4], vals[g4 * 4 + 1], vals[g4 * 4 + 2], vals[g4 * 4 + 3]);
         }
       } else {
-        const int i = row - 64;
+        const int i = row - 64, bi = i >> 4;
         const float gi = G[i];
         float vals[16];
+        if (cg < bi) {
+          const float fa = st.eA[par][i];
+          const float *fb = st.eB[par][bi] + cg * 16;
 #pragma unroll
-        for (int jj = 0; jj < 16; ++jj) {
-          const int j = cg * 16 + jj;
-          vals[jj] = j <= i ? sv[jj] * gexp(gi - G[j], e2) : 0.f;
+          for (int jj = 0; jj < 16; ++jj) vals[jj] = fa * sv[jj] * fb[jj];
+        } else if (cg == bi) {  // diagonal block: tabulated gate (zero above the diagonal)
+          float gdr[16];
+#pragma unroll
+          for (int k4 = 0; k4 < 4; ++k4)
+            *reinterpret_cast<float4 *>(gdr + 4 * k4) = reinterpret_cast<const float4 *>(st.gd[par][bi][i & 15])[k4];
+#pragma unroll
+          for (int jj = 0; jj < 16; ++jj) vals[jj] = sv[jj] * gdr[jj];
+        } else {
+#pragma unroll
+          for (int jj = 0; jj < 16; ++jj) vals[jj] = 0.f;
         }
         *reinterpret_cast<uint4 *>(sm + OFF_AOP + chunk_off(row, cg * 2)) = pack8(vals);
         *reinterpret_cast<uint4 *>(sm + OFF_AOP + chunk_off(row, cg * 2 + 1)) = pack8(vals + 8);
@@ -483,16 +553,31 @@ __global__ void __launch_bounds__(NTH, 1) tc_fwd_kernel(SimtFwdArgs a) {
     __syncthreads();
     // ---- next chunk: loads landed -> its factors and P1 (overlaps this chunk) ------------
     if (c + 1 < nch) {
-      const float bnext = beta_pend;
       cp_async_wait<0>();
       fence_proxy_async();
       __syncthreads();
       issue_p1(c + 1);
-      chunk_factors(c + 1, bnext);
+      chunk_factors(c + 1);
     }
 
-    // ---- X = (I + L)^-1 ------------------------------------------------------------------
-    solve_blocks(LB, XB, TB, tid);
+    // ---- X = (I + L)^-1 on warps 0..3; K and V transposes on warps 4..15 meanwhile -------
+    if (warp < 4) {
+      solve_blocks(LB, XB, TB, tid);
+    } else {
+      for (int jb = warp - 4; jb < 32 + 16; jb += NTH / 32 - 4) {
+        if (jb < 32) {  // K: 4 token blocks x 8 feature blocks -> B3 rows 0..127 and KL
+          const int rb = jb >> 3, fb = jb & 7;
+          const uint32_t src = kq + (fb >> 2) * 16384;
+          const int cc = (fb & 3) * 2;
+          trans16(TransJob{src, rb * 16, cc, sb + OFF_B3, fb * 16}, st.bEG[par], lane);
+          trans16(TransJob{src, rb * 16, cc, sb + OFF_KL, fb * 16}, st.eGL[par], lane);
+        } else {  // V: 4 token blocks x 4 column blocks -> B3 rows 128..191
+          const int t = jb - 32, rb = t >> 2, cb = t & 3;
+          trans16(TransJob{vs, rb * 16, cb * 2, sb + OFF_B3, 128 + cb * 16}, st.beta[par], lane);
+        }
+      }
+    }
+    __syncthreads();
     if (row < 64) {  // X into operand rows 0..63 (and the optional fp32 A slot)
       const int i = row, bi = i >> 4;
       float vals[16];
@@ -520,21 +605,9 @@ __global__ void __launch_bounds__(NTH, 1) tc_fwd_kernel(SimtFwdArgs a) {
       }
     }
     __syncthreads();
-    // ---- transposed operands: X^T; [b e^G K | b V]^T and (e^(Gl-G) K)^T ----------------------
-    for (int jb = warp; jb < 16 + 32 + 16; jb += NTH / 32) {
-      if (jb < 16) {  // X^T: 4 x 4 blocks of the 64x64 X
-        const int rb = jb >> 2, cb = jb & 3;
-        trans16(TransJob{sb + OFF_AOP, rb * 16, cb * 2, sb + OFF_XT, cb * 16}, nullptr, lane);
-      } else if (jb < 48) {  // K: 4 token blocks x 8 feature blocks -> B3 rows 0..127 and KL
-        const int t = jb - 16, rb = t >> 3, fb = t & 7;
-        const uint32_t src = kq + (fb >> 2) * 16384;
-        const int cc = (fb & 3) * 2;
-        trans16(TransJob{src, rb * 16, cc, sb + OFF_B3, fb * 16}, st.bEG[par], lane);
-        trans16(TransJob{src, rb * 16, cc, sb + OFF_KL, fb * 16}, st.eGL[par], lane);
-      } else {  // V: 4 token blocks x 4 column blocks -> B3 rows 128..191
-        const int t = jb - 48, rb = t >> 2, cb = t & 3;
-        trans16(TransJob{vs, rb * 16, cb * 2, sb + OFF_B3, 128 + cb * 16}, st.beta[par], lane);
-      }
+    if (warp < 16) {  // X^T: 4 x 4 blocks of the 64x64 X
+      const int rb = warp >> 2, cb = warp & 3;
+      trans16(TransJob{sb + OFF_AOP, rb * 16, cb * 2, sb + OFF_XT, cb * 16}, nullptr, lane);
     }
     fence_proxy_async();
     __syncthreads();
@@ -589,6 +662,7 @@ __global__ void __launch_bounds__(NTH, 1) tc_fwd_kernel(SimtFwdArgs a) {
     fence_proxy_async();
     fence_before_sync();
     __syncthreads();
+    if (c + 2 < nch) issue_loads(c + 2);  // chunk c's stage is free from here
     // ---- P4: [v_new; o/scale] = [u; A_qk u] + [-w; q'] h ---------------------------------------
     if (tid == 0) {
       fence_after_sync();
@@ -635,8 +709,7 @@ __global__ void __launch_bounds__(NTH, 1) tc_fwd_kernel(SimtFwdArgs a) {
     fence_before_sync();
     __syncthreads();  // the staging tile (v_new) has been consumed
     write_h_operand();
-    // ---- loads of chunk c+2 into this chunk's stage ------------------------------------------
-    if (c + 2 < nch) issue_loads(c + 2);
+    store_gb(c + 2, gb_pf);
     fence_proxy_async();
     if (__syncthreads_or(bad)) bad = true;
   }
@@ -665,10 +738,10 @@ __global__ void __launch_bounds__(NTH, 1) tc_fwd_kernel(SimtFwdArgs a) {
 int tc_fwd_bv() { return TBV; }
 
 cudaError_t launch_tc_fwd(const SimtFwdArgs &a, dim3 grid, cudaStream_t st) {
-  cudaError_t e = cudaFuncSetAttribute(tc_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       SMEM_BYTES);
+  auto kern = a.use_exp2 ? tc_fwd_kernel<true> : tc_fwd_kernel<false>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
   if (e != cudaSuccess) return e;
-  tc_fwd_kernel<<<grid, NTH, SMEM_BYTES, st>>>(a);
+  kern<<<grid, NTH, SMEM_BYTES, st>>>(a);
   return cudaGetLastError();
 }
 

@@ -134,14 +134,19 @@ __device__ __forceinline__ void mma_commit(uint64_t *bar) {
 
 // D[M x N] (+)= A[M x K] B[N x K]^T for K a multiple of 64: A and B are
 // consecutive 64-wide K-blocks of swizzled tiles (a_kb / b_kb bytes apart).
+// The descriptor of every K step is the first one plus the step's byte offset
+// in the 14-bit start-address field (addresses stay below 256 KB, so the add
+// never carries out of the field).
 __device__ __forceinline__ void mma_tiles(uint32_t d_tmem, uint32_t a_saddr, uint32_t a_kb,
                                           uint32_t b_saddr, uint32_t b_kb, int K, uint32_t idesc,
                                           bool accumulate) {
+  const uint64_t a0 = sdesc_sw128(a_saddr), b0 = sdesc_sw128(b_saddr);
+#pragma unroll
   for (int kb = 0; kb < K / 64; ++kb) {
 #pragma unroll
     for (int s = 0; s < 4; ++s) {
-      const uint64_t ad = sdesc_sw128(a_saddr + kb * a_kb + s * 32);
-      const uint64_t bd = sdesc_sw128(b_saddr + kb * b_kb + s * 32);
+      const uint64_t ad = a0 + ((uint64_t)(kb * a_kb + s * 32) >> 4);
+      const uint64_t bd = b0 + ((uint64_t)(kb * b_kb + s * 32) >> 4);
       mma_bf16(d_tmem, ad, bd, idesc, (accumulate || kb > 0 || s > 0) ? 1u : 0u);
     }
   }
