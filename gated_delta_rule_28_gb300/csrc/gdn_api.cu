@@ -152,8 +152,35 @@ int64_t n_chunk_slots(const gdn_problem *p) {
 
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
+// bf16 X = (I + L)^-1 of every chunk and head (tensor-core path only)
+size_t x_ws_bytes(const gdn_problem *p) {
+  if (!use_tensor_cores(p)) return 0;
+  return align256((size_t)n_chunk_slots(p) * p->H * GDN_CHUNK * GDN_CHUNK * 2);
+}
+
+gdn::UtArgs ut_args(const gdn_problem *p, const void *k, const float *g, const float *g_cum_in,
+                    const void *beta, void *xw, float *A, float *g_cumsum, int *flag) {
+  gdn::UtArgs u{};
+  u.k = k;
+  u.g = g;
+  u.g_cum_in = g_cum_in;
+  u.beta = beta;
+  u.xw = static_cast<__nv_bfloat16 *>(xw);
+  u.A = A;
+  u.g_cumsum = g_cumsum;
+  u.T = p->T;
+  u.H = p->H;
+  u.use_exp2 = p->use_exp2;
+  const bool packed = p->layout == GDN_LAYOUT_TND;
+  u.cu = packed ? p->cu_seqlens : nullptr;
+  u.chunk_indices = packed ? p->chunk_indices : nullptr;
+  u.num_seqs = p->num_seqs;
+  u.dev_flag = flag;
+  return u;
+}
+
 struct BwdWs {
-  size_t h_chunks, dh_chunks, dvnew, total;
+  size_t h_chunks, dh_chunks, dvnew, xw, total;
 };
 
 BwdWs bwd_ws_layout(const gdn_problem *p) {
@@ -164,7 +191,8 @@ BwdWs bwd_ws_layout(const gdn_problem *p) {
   w.h_chunks = 0;
   w.dh_chunks = align256(slots * KV);
   w.dvnew = w.dh_chunks + align256(slots * KV);
-  w.total = w.dvnew + align256(rows * p->H * GDN_DV * sizeof(float));
+  w.xw = w.dvnew + align256(rows * p->H * GDN_DV * sizeof(float));
+  w.total = w.xw + x_ws_bytes(p);
   return w;
 }
 
@@ -232,7 +260,7 @@ gdn_status gdn_chunk_fwd_workspace(const gdn_problem *p, size_t *bytes) {
   gdn_status st = check_problem(p, true);
   if (st != GDN_OK) return st;
   if (!bytes) return fail(GDN_ERR_INVALID_ARGUMENT, "bytes must not be NULL");
-  *bytes = 0;
+  *bytes = x_ws_bytes(p);
   return ok();
 }
 
@@ -255,8 +283,11 @@ gdn_status gdn_chunk_fwd(const gdn_problem *p, const void *q, const void *k, con
   OPTIONAL_PTR(g_cumsum, "g_cumsum");
   OPTIONAL_PTR(A, "A");
   OPTIONAL_PTR(h_chunks, "h_chunks");
-  (void)ws;
-  (void)ws_bytes;
+  const size_t need = x_ws_bytes(p);
+  if (need > 0 && (!ws || ws_bytes < need))
+    return fail(GDN_ERR_WORKSPACE, "forward workspace needs %zu bytes, got %zu", need,
+                ws ? ws_bytes : (size_t)0);
+  if (ws && !aligned16(ws)) return fail(GDN_ERR_INVALID_ARGUMENT, "ws must be 16-byte aligned");
   if (p->segment_len > 0 && !h0)
     return fail(GDN_ERR_INVALID_ARGUMENT, "segment_len > 0 needs h0 = S_init [B,H,nseg,K,V]");
   int dev;
@@ -291,7 +322,10 @@ gdn_status gdn_chunk_fwd(const gdn_problem *p, const void *q, const void *k, con
   if (a.nseg > 0 && p->T == 0) return ok();
   cudaError_t e;
   if (use_tensor_cores(p)) {
-    e = gdn::launch_tc_fwd(a, dim3(GDN_DV / gdn::tc_fwd_bv(), p->H, runs), s);
+    const gdn::UtArgs u = ut_args(p, k, g, nullptr, beta, ws, A, g_cumsum, a.dev_flag);
+    if ((e = gdn::launch_ut(u, (int)n_chunk_slots(p), s)) != cudaSuccess) return cuda_fail(e, "UT transform launch");
+    a.xw = static_cast<const __nv_bfloat16 *>(ws);
+    e = gdn::launch_tc_fwd_ws(a, dim3(GDN_DV / gdn::tc_fwd_ws_bv(), p->H, runs), s);
   } else {
     const dim3 grid(GDN_DV / gdn::simt_fwd_bv(), p->H, runs);
     e = gdn::launch_simt_fwd(a, p->gate_kind == GDN_GATE_PER_KEY, p->dtype == GDN_DTYPE_BF16, grid, s);
@@ -346,6 +380,7 @@ gdn_status gdn_chunk_bwd(const gdn_problem *p, const void *q, const void *k, con
   float *hch = reinterpret_cast<float *>(w + L.h_chunks);
   float *dhch = reinterpret_cast<float *>(w + L.dh_chunks);
   float *dvn = reinterpret_cast<float *>(w + L.dvnew);
+  void *xw = w + L.xw;
   const bool packed = p->layout == GDN_LAYOUT_TND;
   const int runs = packed ? p->num_seqs : p->B;
   int *flag = device_flag_ptr();
@@ -380,9 +415,15 @@ gdn_status gdn_chunk_bwd(const gdn_problem *p, const void *q, const void *k, con
   f.g_cum_in = g_cumsum;
   f.A_in = A;
   f.dev_flag = flag;
-  cudaError_t e = use_tensor_cores(p)
-                      ? gdn::launch_tc_fwd(f, dim3(GDN_DV / gdn::tc_fwd_bv(), p->H, runs), s)
-                      : gdn::launch_simt_fwd(f, pk, bf, dim3(GDN_DV / gdn::simt_fwd_bv(), p->H, runs), s);
+  cudaError_t e;
+  if (use_tensor_cores(p)) {  // X recomputed from the saved cumulative gate (same values as A)
+    const gdn::UtArgs u = ut_args(p, k, nullptr, g_cumsum, beta, xw, nullptr, nullptr, flag);
+    if ((e = gdn::launch_ut(u, (int)n_chunk_slots(p), s)) != cudaSuccess) return cuda_fail(e, "UT transform launch");
+    f.xw = static_cast<const __nv_bfloat16 *>(xw);
+    e = gdn::launch_tc_fwd_ws(f, dim3(GDN_DV / gdn::tc_fwd_ws_bv(), p->H, runs), s);
+  } else {
+    e = gdn::launch_simt_fwd(f, pk, bf, dim3(GDN_DV / gdn::simt_fwd_bv(), p->H, runs), s);
+  }
   if (e != cudaSuccess) return cuda_fail(e, "backward state recompute launch");
 
   gdn::BwdArgs b{};

@@ -2,6 +2,7 @@
 // translation units. Not installed; not part of the public header.
 #pragma once
 
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -32,6 +33,7 @@ struct SimtFwdArgs {
   int summary;        // 1: columns [0,V) from v with zero start, [V,V+K) transfer from I
   const float *g_cum_in;  // nullable: read the cumulative gate instead of summing g
   const float *A_in;      // nullable: read X = (I + L)^-1 instead of solving
+  const __nv_bfloat16 *xw;  // tensor-core path: X of every chunk, [slots, H, 64, 64] bf16
   int *dev_flag;
 };
 
@@ -42,6 +44,29 @@ int simt_fwd_bv();  // value columns per CTA
 // tcgen05 chunk forward: bf16 inputs, scalar gate, no in-kernel norm
 cudaError_t launch_tc_fwd(const SimtFwdArgs &a, dim3 grid, cudaStream_t st);
 int tc_fwd_bv();
+
+// UT transform of every chunk (bf16 keys, scalar gate): X = (I + L)^-1 in bf16
+// into xw [slots, H, 64, 64]; optionally the fp32 X (A) and the cumulative gate.
+struct UtArgs {
+  const void *k;
+  const float *g;         // raw gate, or
+  const float *g_cum_in;  // the saved cumulative gate (nullable)
+  const void *beta;
+  __nv_bfloat16 *xw;
+  float *A;         // nullable, [rows, H, 64]
+  float *g_cumsum;  // nullable
+  int T, H;
+  int use_exp2;
+  const int32_t *cu, *chunk_indices;  // packed documents, or nullptr
+  int num_seqs;
+  int *dev_flag;
+};
+cudaError_t launch_ut(const UtArgs &a, int slots, cudaStream_t st);
+
+// tcgen05 chunk forward with the state recurrence overlapped with the next
+// chunk's preparation; reads X from a.xw (launch_ut first)
+cudaError_t launch_tc_fwd_ws(const SimtFwdArgs &a, dim3 grid, cudaStream_t st);
+int tc_fwd_ws_bv();
 
 struct MergeArgs {
   const float *S_ext, *M, *h0;

@@ -1,0 +1,161 @@
+// UT transform of every 64-token chunk, for all chunks and heads at once
+// (bf16 keys, scalar gate, sm_103a).
+//
+// Per chunk (north star: "the UT/WY transform A = (I + strictly-lower(diag(beta)
+// K K^T (.) gate-decay))^-1 diag(beta)"; GDN Ascend C adapter forward, steps
+// chunk_local_cumsum / chunk_scaled_dot_kkt / solve_tril):
+//   G = cumsum(g) inside the chunk
+//   L = strictly-lower(diag(beta) (K K^T (.) Gamma)),  Gamma_ij = base^(G_i - G_j)
+//   X = (I + L)^-1
+// X has no dependence on the state, so it is computed here for every chunk
+// in parallel (one CTA of 4 warps per chunk and head; K K^T on bf16 mma.sync,
+// the solve in fp32 shared memory) and written in bf16 for the tensor-core
+// state kernel, which then only multiplies by it. The fp32 X (the A output
+// of the forward) and the cumulative gate are written here when asked for.
+#include "common.cuh"
+#include "kernels.h"
+#include "tc.cuh"
+#include "tile_ops.cuh"
+
+namespace gdn {
+namespace {
+using namespace tc;
+using namespace tile;
+
+__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+template <bool E2>
+__global__ void __launch_bounds__(128) ut_kernel(UtArgs a) {
+  __shared__ __align__(1024) uint8_t ktile[16384];  // K: 2 K-blocks of 64 rows x 128 B, swizzled
+  __shared__ __align__(16) float LB[10 * 256], XB[10 * 256], TB[4 * 256];
+  __shared__ float sg[64], sG[64], sbeta[64];
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int slot = blockIdx.x, h = blockIdx.y, H = a.H;
+  int64_t r0, r1;
+  if (a.cu) {
+    const int seq = a.chunk_indices[2 * slot], cc = a.chunk_indices[2 * slot + 1];
+    bool ok = seq >= 0 && seq < a.num_seqs && cc >= 0;
+    if (ok) {
+      r0 = (int64_t)a.cu[seq] + (int64_t)cc * GDN_CHUNK;
+      r1 = a.cu[seq + 1];
+      ok = r0 >= 0 && r0 < r1 && r1 <= a.T;
+    }
+    if (!ok) {
+      if (tid == 0) raise_device_flag(a.dev_flag, kDevCheck);
+      return;
+    }
+  } else {
+    const int NT = (a.T + GDN_CHUNK - 1) / GDN_CHUNK;
+    const int b = slot / NT, c = slot % NT;
+    r0 = (int64_t)b * a.T + (int64_t)c * GDN_CHUNK;
+    r1 = (int64_t)b * a.T + a.T;
+  }
+  const int n = (int)min((int64_t)GDN_CHUNK, r1 - r0);
+  const __nv_bfloat16 *k = static_cast<const __nv_bfloat16 *>(a.k);
+  const __nv_bfloat16 *beta = static_cast<const __nv_bfloat16 *>(a.beta);
+
+  // keys of the chunk, zero past its end
+  const uint32_t kt = smem_u32(ktile);
+#pragma unroll
+  for (int x = tid; x < 1024; x += 128) {
+    const int r = x >> 4, f16 = x & 15;
+    const bool valid = r < n;
+    const __nv_bfloat16 *src = k + ((r0 + (valid ? r : 0)) * H + h) * GDN_DK + f16 * 8;
+    cp_async16(kt + (f16 >> 3) * 8192 + chunk_off(r, f16 & 7), src, valid ? 16u : 0u);
+  }
+  cp_async_commit();
+  // gate and beta; rows past the end: no gate increment, beta 0
+  const float *gsrc = a.g_cum_in ? a.g_cum_in : a.g;
+  if (tid < 64) {
+    sg[tid] = tid < n ? gsrc[(r0 + tid) * H + h] : 0.f;
+    sbeta[tid] = tid < n ? __bfloat162float(beta[(r0 + tid) * H + h]) : 0.f;
+  }
+  __syncthreads();
+  if (a.g_cum_in) {
+    if (tid < 64) sG[tid] = sg[min(tid, n - 1)];
+  } else if (warp == 0) {
+    const float x0 = sg[2 * lane], x1 = sg[2 * lane + 1], pair = x0 + x1;
+    float incl = pair;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const float y = __shfl_up_sync(0xffffffffu, incl, off);
+      if (lane >= off) incl += y;
+    }
+    const float ex = incl - pair;
+    sG[2 * lane] = ex + x0;
+    sG[2 * lane + 1] = ex + pair;
+  }
+  cp_async_wait<0>();
+  __syncthreads();
+
+  // L blocks (bi, bj), bj <= bi, in blk() order; warp w takes blocks w, w+4, w+8
+  for (int bidx = warp; bidx < 10; bidx += 4) {
+    const int bi = bidx < 1 ? 0 : bidx < 3 ? 1 : bidx < 6 ? 2 : 3;
+    const int bj = bidx - bi * (bi + 1) / 2;
+    float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks) {  // 16 features per step
+      const int c8 = (2 * ks + (lane >> 4)) & 7;
+      const uint32_t kb = kt + (ks >> 2) * 8192;
+      uint32_t af[4], bf[4];
+      ldsm_x4(kb + chunk_off(16 * bi + (lane & 15), c8), af);
+      ldsm_x4(kb + chunk_off(16 * bj + (lane & 15), c8), bf);
+      mma_bf16_16816(acc[0], af, bf[0], bf[2]);
+      mma_bf16_16816(acc[1], af, bf[1], bf[3]);
+    }
+    const int g = lane >> 2, t = lane & 3;
+    float *Lb = LB + blk(bi, bj) * 256;
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int r = g + 8 * (e >> 1), c = nt * 8 + 2 * t + (e & 1);
+        const int i = 16 * bi + r, j = 16 * bj + c;
+        Lb[bsw(r, c)] = i > j ? sbeta[i] * acc[nt][e] * gexp<E2>(sG[i] - sG[j]) : 0.f;
+      }
+  }
+  __syncthreads();
+  solve_blocks(LB, XB, TB, tid);
+
+  // X rows: thread -> row tid/2, columns 32 (tid&1) .. +32
+  {
+    const int row = tid >> 1, half = tid & 1, bi = row >> 4;
+    float vals[32];
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      const int cb = 2 * half + q;
+#pragma unroll
+      for (int cc = 0; cc < 16; ++cc) vals[16 * q + cc] = cb <= bi ? XB[blk(bi, cb) * 256 + bsw(row & 15, cc)] : 0.f;
+    }
+    uint4 *dst = reinterpret_cast<uint4 *>(a.xw + (((int64_t)slot * H + h) * GDN_CHUNK + row) * GDN_CHUNK + 32 * half);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) dst[q] = pack8(vals + 8 * q);
+    if (a.A && row < n) {
+      float4 *Ad = reinterpret_cast<float4 *>(a.A + ((r0 + row) * H + h) * GDN_CHUNK + 32 * half);
+#pragma unroll
+      for (int q = 0; q < 8; ++q) Ad[q] = make_float4(vals[4 * q], vals[4 * q + 1], vals[4 * q + 2], vals[4 * q + 3]);
+    }
+  }
+  if (a.g_cumsum && !a.g_cum_in && tid < n) a.g_cumsum[(r0 + tid) * H + h] = sG[tid];
+}
+
+}  // namespace
+
+cudaError_t launch_ut(const UtArgs &a, int slots, cudaStream_t st) {
+  if (slots <= 0) return cudaSuccess;
+  const dim3 grid(slots, a.H);
+  if (a.use_exp2)
+    ut_kernel<true><<<grid, 128, 0, st>>>(a);
+  else
+    ut_kernel<false><<<grid, 128, 0, st>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace gdn

@@ -174,7 +174,9 @@ def test_device_metadata_check_flags_bad_offsets():
     p = B.make_problem(1, 300, 2, layout=B.GDN_LAYOUT_TND, cu_seqlens=cu_bad, num_seqs=3,
                        chunk_indices=idx, num_chunks=5)
     o = torch.zeros_like(d["v"])
-    B.gdn_chunk_fwd(p, d["q"], d["k"], d["v"], d["g"], d["beta"], None, o)
+    nws = B.gdn_chunk_fwd_workspace(p)
+    ws = torch.empty(max(nws, 1), device="cuda", dtype=torch.uint8)
+    B.gdn_chunk_fwd(p, d["q"], d["k"], d["v"], d["g"], d["beta"], None, o, ws=ws, ws_bytes=nws)
     with pytest.raises(B.GdnError) as e:
         B.gdn_device_status()
     assert e.value.status == B.GDN_ERR_DEVICE_CHECK
