@@ -62,11 +62,13 @@ static_assert(OFF_AQ >= 8192, "rows 0..63 of the A_qk operand precede its buffer
 
 constexpr uint32_t WAIT_LIMIT = 1u << 22;
 
+// gate factor table of a chunk (from the UT transform kernel), per chunk parity:
+// G, base^G, base^(G_last - G), beta base^G, beta
+enum { F_G = 0, F_EG = 1, F_EGL = 2, F_BEG = 3, F_BETA = 4 };
 struct WsState {
-  float G[2][64], eG[2][64], eGL[2][64], bEG[2][64], beta[2][64];  // per chunk parity
-  float graw[2][64], braw[2][64];
-  float EL[2];
-  uint64_t bar_p1, bar_p3, bar_p4, bar_p5, bar_d0, bar_d1;
+  alignas(16) float tab[2][5][64];  // refilled with chunk c+2 while the chain runs chunk c
+  float EL[2];                      // base^(G_last) per chunk parity, for the chain
+  uint64_t bar_p1, bar_p3, bar_p4, bar_p5, bar_po, bar_d0, bar_d1;
   uint32_t tmem;
 };
 static_assert(sizeof(WsState) <= SMALL_BYTES, "small state");
@@ -100,7 +102,6 @@ __global__ void __launch_bounds__(NTH, 1) tc_fwd_ws_kernel(SimtFwdArgs a) {
   const __nv_bfloat16 *q = static_cast<const __nv_bfloat16 *>(a.q);
   const __nv_bfloat16 *k = static_cast<const __nv_bfloat16 *>(a.k);
   const __nv_bfloat16 *v = static_cast<const __nv_bfloat16 *>(a.v);
-  const __nv_bfloat16 *beta = static_cast<const __nv_bfloat16 *>(a.beta);
   const __nv_bfloat16 *xw = a.xw;
   __nv_bfloat16 *o = static_cast<__nv_bfloat16 *>(a.o);
 
@@ -152,6 +153,7 @@ __global__ void __launch_bounds__(NTH, 1) tc_fwd_ws_kernel(SimtFwdArgs a) {
     mbar_init(&st.bar_p3, 1);
     mbar_init(&st.bar_p4, 1);
     mbar_init(&st.bar_p5, 1);
+    mbar_init(&st.bar_po, 1);
     mbar_init(&st.bar_d0, 1);
     mbar_init(&st.bar_d1, 1);
     mbar_fence_init();
@@ -169,11 +171,12 @@ __global__ void __launch_bounds__(NTH, 1) tc_fwd_ws_kernel(SimtFwdArgs a) {
 
   // ---- producer: loads -----------------------------------------------------------------
   const int ptid = tid - 256;  // 0..255 on producer threads
-  auto issue_kqx = [&](int64_t c) {  // K, Q and X of chunk c into stage c&1
+  auto issue_kqx = [&](int64_t c) {  // K, Q, X and the gate factors of chunk c into stage c&1
     const uint32_t stg = sb + OFF_ST + (int)(c & 1) * SZ_STAGE;
     const int64_t c0 = r0 + c * GDN_CHUNK;
     const int n = chunk_rows(c);
-    const __nv_bfloat16 *xs = xw + ((xbase + c) * H + h) * (GDN_CHUNK * GDN_CHUNK);
+    const int64_t xs = (xbase + c) * H + h;
+    const __nv_bfloat16 *xsrc = xw + xs * (GDN_CHUNK * GDN_CHUNK);
 #pragma unroll
     for (int x = ptid; x < 2048 + 512; x += 256) {
       if (x < 2048) {
@@ -183,9 +186,11 @@ __global__ void __launch_bounds__(NTH, 1) tc_fwd_ws_kernel(SimtFwdArgs a) {
         cp_async16(stg + (f16 >> 3) * 16384 + chunk_off(r + which * 64, f16 & 7), src, valid ? 16u : 0u);
       } else {
         const int r = (x - 2048) >> 3, c8 = x & 7;
-        cp_async16(stg + ST_X + chunk_off(r, c8), xs + r * GDN_CHUNK + c8 * 8, 16u);
+        cp_async16(stg + ST_X + chunk_off(r, c8), xsrc + r * GDN_CHUNK + c8 * 8, 16u);
       }
     }
+    if (ptid < 80)
+      cp_async16(smem_u32(&st.tab[c & 1][0][0]) + ptid * 16, a.ftab + xs * 5 * GDN_CHUNK + ptid * 4, 16u);
   };
   auto issue_v = [&](int64_t c) {  // the CTA's 64 columns of V of chunk c
     const int64_t c0 = r0 + c * GDN_CHUNK;
@@ -198,78 +203,48 @@ __global__ void __launch_bounds__(NTH, 1) tc_fwd_ws_kernel(SimtFwdArgs a) {
       cp_async16(sb + OFF_V + chunk_off(r, c8), src, valid ? 16u : 0u);
     }
   };
-  const float *gsrc = a.g_cum_in ? a.g_cum_in : a.g;
-  auto load_gb = [&](int64_t c) -> float2 {  // threads ptid < 64; zero past the run end
-    float2 gb = make_float2(0.f, 0.f);
-    if (producer && ptid < 64 && c < nch && ptid < chunk_rows(c)) {
-      const int64_t c0 = r0 + c * GDN_CHUNK;
-      gb.x = gsrc[(c0 + ptid) * H + h];
-      gb.y = __bfloat162float(beta[(c0 + ptid) * H + h]);
-    }
-    return gb;
-  };
 
   // ---- producer: one chunk -------------------------------------------------------------
-  float2 gb_cur = make_float2(0.f, 0.f);
   auto produce = [&](int64_t pc, int64_t c_chain) {
     const int ps = (int)(pc & 1);
     const uint32_t stg = sb + OFF_ST + ps * SZ_STAGE;
-    const int n = chunk_rows(pc);
+    const float(&tab)[5][64] = st.tab[ps];
     // stage of chunk pc+1 (it held chunk pc-1, finished in the previous round)
     if (pc + 1 < nch) issue_kqx(pc + 1);
     cp_async_commit();
-    const float2 gb_next = load_gb(pc + 1);
-    if (ptid < 64) {
-      st.graw[ps][ptid] = gb_cur.x;
-      st.braw[ps][ptid] = gb_cur.y;
-    }
-    cp_async_wait<1>();  // K, Q, X and V of chunk pc have landed
+    cp_async_wait<1>();  // K, Q, X, factors and V of chunk pc have landed
     fence_proxy_async();
     prod_sync();
     if (ptid == 0) {  // P1: S = [K; Q] K^T
+      st.EL[ps] = tab[F_EG][63];
       fence_after_sync();
       mma_tiles(tmem + T_S + 64 * ps, stg, 16384, stg, 16384, 128, idesc_bf16(128, 64), false);
       mma_commit(&st.bar_p1);
     }
-    // cumulative gate and per-token factors
-    if (a.g_cum_in) {
-      if (ptid < 64) st.G[ps][ptid] = st.graw[ps][min(ptid, n - 1)];
-    } else if (warp == 8) {
-      const float x0 = st.graw[ps][2 * lane], x1 = st.graw[ps][2 * lane + 1];
-      const float pair = x0 + x1;
-      float incl = pair;
+    // transposes, loads first: K -> B3 rows 0..127 (b e^G) and KL (e^(Gl-G)); V -> B3 rows 128..191 (b)
+    {
+      const int pw = warp - 8;
+      uint32_t xk[4][4], xv[2][4];
 #pragma unroll
-      for (int off = 1; off < 32; off <<= 1) {
-        const float y = __shfl_up_sync(0xffffffffu, incl, off);
-        if (lane >= off) incl += y;
+      for (int i = 0; i < 4; ++i) {
+        const int jb = pw + 8 * i, rb = jb >> 3, fb = jb & 7;
+        trans16_load(stg + (fb >> 2) * 16384, rb * 16, (fb & 3) * 2, lane, xk[i]);
       }
-      const float ex = incl - pair;
-      st.G[ps][2 * lane] = ex + x0;
-      st.G[ps][2 * lane + 1] = ex + pair;
-    }
-    prod_sync();
-    if (ptid < 64) {
-      const float G = st.G[ps][ptid], Gl = st.G[ps][63], bt = st.braw[ps][ptid];
-      const float eg = gexp<E2>(G);
-      st.beta[ps][ptid] = bt;
-      st.eG[ps][ptid] = eg;
-      st.eGL[ps][ptid] = gexp<E2>(Gl - G);
-      st.bEG[ps][ptid] = bt * eg;
-      if (ptid == 0) st.EL[ps] = gexp<E2>(Gl);
-    }
-    prod_sync();
-    // transposes: K -> B3 rows 0..127 (b e^G) and KL (e^(Gl-G)); V -> B3 rows 128..191 (b)
-    const int pw = warp - 8;
-    for (int jb = pw; jb < 32 + 16; jb += 8) {
-      if (jb < 32) {
-        const int rb = jb >> 3, fb = jb & 7;
-        const uint32_t src = stg + (fb >> 2) * 16384;
-        const int cc = (fb & 3) * 2;
-        trans16(TransJob{src, rb * 16, cc, sb + OFF_B3, fb * 16}, st.bEG[ps], lane);
-        trans16(TransJob{src, rb * 16, cc, sb + OFF_KL + ps * 16384, fb * 16}, st.eGL[ps], lane);
-      } else {
-        const int t = jb - 32, rb = t >> 2, cb = t & 3;
-        trans16(TransJob{sb + OFF_V, rb * 16, cb * 2, sb + OFF_B3, 128 + cb * 16}, st.beta[ps], lane);
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        const int t = pw + 8 * i, rb = t >> 2, cb = t & 3;
+        trans16_load(sb + OFF_V, rb * 16, cb * 2, lane, xv[i]);
+      }
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        const int t = pw + 8 * i, rb = t >> 2, cb = t & 3;
+        trans16_store(sb + OFF_B3, 128 + cb * 16, rb * 16, xv[i], tab[F_BETA], lane);
+      }
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int jb = pw + 8 * i, rb = jb >> 3, fb = jb & 7;
+        trans16_store(sb + OFF_B3, fb * 16, rb * 16, xk[i], tab[F_BEG], lane);
+        trans16_store(sb + OFF_KL + ps * 16384, fb * 16, rb * 16, xk[i], tab[F_EGL], lane);
       }
     }
     prod_sync();  // V consumed: load the next chunk's
@@ -283,11 +258,11 @@ __global__ void __launch_bounds__(NTH, 1) tc_fwd_ws_kernel(SimtFwdArgs a) {
       tmem_ld16(tl + T_S + 64 * ps + 32 * hc, *reinterpret_cast<float(*)[16]>(sv));
       tmem_ld16(tl + T_S + 64 * ps + 32 * hc + 16, *reinterpret_cast<float(*)[16]>(sv + 16));
       tmem_ld_wait();
-      const float Gt = st.G[ps][t];
+      const float Gt = tab[F_G][t];
 #pragma unroll
       for (int j = 0; j < 32; ++j) {
         const int sj = 32 * hc + j;
-        sv[j] = sj <= t ? sv[j] * gexp<E2>(Gt - st.G[ps][sj]) : 0.f;
+        sv[j] = sj <= t ? sv[j] * gexp<E2>(Gt - tab[F_G][sj]) : 0.f;
       }
       uint8_t *dst = sm + OFF_AQ + ps * 8192;
 #pragma unroll
@@ -303,36 +278,35 @@ __global__ void __launch_bounds__(NTH, 1) tc_fwd_ws_kernel(SimtFwdArgs a) {
       mma_tiles(tmem + T_U + 64 * ps, stg + ST_X, 8192, sb + OFF_B3 + 16384, 24576, 64, idesc_bf16(128, 64), false);
       mma_commit(&st.bar_p3);
     }
+    // operand of P4: rows 64..127 = e^G Q once the chain's P4 has read the previous one,
+    // rows 0..63 = w once P3b is done (keys 64*hc .. +64 per thread)
+    uint8_t *wq = sm + OFF_WQ + hc * 16384;
+    if (c_chain >= 0) wait_par(&st.bar_p4, c_chain);
+    if (q4 >= 2) {
+      const float eg = tab[F_EG][row - 64];
+      const uint8_t *qrow = sm + OFF_ST + ps * SZ_STAGE + hc * 16384;
+#pragma unroll
+      for (int c8 = 0; c8 < 8; ++c8) {
+        float f[8];
+        unpack8(*reinterpret_cast<const uint4 *>(qrow + chunk_off(row, c8)), f);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) f[e] *= eg;
+        *reinterpret_cast<uint4 *>(wq + chunk_off(row, c8)) = pack8(f);
+      }
+    }
     wait_par(&st.bar_p3, pc);
-    if (c_chain >= 0) wait_par(&st.bar_p4, c_chain);  // the chain's P4 has read the operand
-    // operand of P4: rows 0..63 = w, rows 64..127 = e^G Q (keys 64*hc .. +64 per thread)
-    {
-      uint8_t *dst = sm + OFF_WQ + hc * 16384;
-      if (q4 < 2) {
+    if (q4 < 2) {
 #pragma unroll
-        for (int part = 0; part < 4; ++part) {
-          float sv[16];
-          tmem_ld16(tl + T_WW + 64 * hc + 16 * part, sv);
-          tmem_ld_wait();
-          *reinterpret_cast<uint4 *>(dst + chunk_off(row, 2 * part)) = pack8(sv);
-          *reinterpret_cast<uint4 *>(dst + chunk_off(row, 2 * part + 1)) = pack8(sv + 8);
-        }
-      } else {
-        const float eg = st.eG[ps][row - 64];
-        const uint8_t *qrow = sm + OFF_ST + ps * SZ_STAGE + hc * 16384;
-#pragma unroll
-        for (int c8 = 0; c8 < 8; ++c8) {
-          float f[8];
-          unpack8(*reinterpret_cast<const uint4 *>(qrow + chunk_off(row, c8)), f);
-#pragma unroll
-          for (int e = 0; e < 8; ++e) f[e] *= eg;
-          *reinterpret_cast<uint4 *>(dst + chunk_off(row, c8)) = pack8(f);
-        }
+      for (int part = 0; part < 4; ++part) {
+        float sv[16];
+        tmem_ld16(tl + T_WW + 64 * hc + 16 * part, sv);
+        tmem_ld_wait();
+        *reinterpret_cast<uint4 *>(wq + chunk_off(row, 2 * part)) = pack8(sv);
+        *reinterpret_cast<uint4 *>(wq + chunk_off(row, 2 * part + 1)) = pack8(sv + 8);
       }
     }
     fence_proxy_async();
     fence_before_sync();
-    gb_cur = gb_next;
   };
 
   // ---- chain: state and one chunk ----------------------------------------------------------
@@ -387,11 +361,12 @@ __global__ void __launch_bounds__(NTH, 1) tc_fwd_ws_kernel(SimtFwdArgs a) {
     fence_proxy_async();
     fence_before_sync();
     chain_sync();
-    if (tid == 0) {  // P5 and the intra-chunk output term
+    if (tid == 0) {  // P5, then the intra-chunk output term
       fence_after_sync();
       mma_tiles(tmem + T_P5, sb + OFF_KL + par * 16384, 16384, sb + OFF_VN, 8192, 64, idesc_bf16(128, 64), false);
-      mma_tiles(tmem + T_D4, sb + OFF_AQ + par * 8192 - 8192, 16384, sb + OFF_VN, 8192, 64, idesc_bf16(128, 64), true);
       mma_commit(&st.bar_p5);
+      mma_tiles(tmem + T_D4, sb + OFF_AQ + par * 8192 - 8192, 16384, sb + OFF_VN, 8192, 64, idesc_bf16(128, 64), true);
+      mma_commit(&st.bar_po);
     }
     wait_par(&st.bar_p5, c);
     {
@@ -411,6 +386,7 @@ __global__ void __launch_bounds__(NTH, 1) tc_fwd_ws_kernel(SimtFwdArgs a) {
         }
       }
       if (q4 >= 2) {  // o = scale (q' h + A_qk v_new); the whole warp loads (collective)
+        wait_par(&st.bar_po, c);
         const bool st_row = o && row - 64 < n;
         uint4 *dst = reinterpret_cast<uint4 *>(o + ((c0 + (st_row ? row - 64 : 0)) * H + h) * GDN_DV + col0 + 32 * hc);
 #pragma unroll
@@ -437,7 +413,6 @@ __global__ void __launch_bounds__(NTH, 1) tc_fwd_ws_kernel(SimtFwdArgs a) {
     cp_async_commit();
     issue_v(0);
     cp_async_commit();
-    gb_cur = load_gb(0);
   }
   if (!producer) {
     write_ht();

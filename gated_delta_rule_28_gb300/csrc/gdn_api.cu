@@ -152,10 +152,14 @@ int64_t n_chunk_slots(const gdn_problem *p) {
 
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
-// bf16 X = (I + L)^-1 of every chunk and head (tensor-core path only)
+// bf16 X = (I + L)^-1 of every chunk and head, then the chunks' gate factor
+// tables (tensor-core path only)
+size_t x_part_bytes(const gdn_problem *p) {
+  return align256((size_t)n_chunk_slots(p) * p->H * GDN_CHUNK * GDN_CHUNK * 2);
+}
 size_t x_ws_bytes(const gdn_problem *p) {
   if (!use_tensor_cores(p)) return 0;
-  return align256((size_t)n_chunk_slots(p) * p->H * GDN_CHUNK * GDN_CHUNK * 2);
+  return x_part_bytes(p) + align256((size_t)n_chunk_slots(p) * p->H * 5 * GDN_CHUNK * sizeof(float));
 }
 
 gdn::UtArgs ut_args(const gdn_problem *p, const void *k, const float *g, const float *g_cum_in,
@@ -166,6 +170,7 @@ gdn::UtArgs ut_args(const gdn_problem *p, const void *k, const float *g, const f
   u.g_cum_in = g_cum_in;
   u.beta = beta;
   u.xw = static_cast<__nv_bfloat16 *>(xw);
+  u.ftab = reinterpret_cast<float *>(static_cast<char *>(xw) + x_part_bytes(p));
   u.A = A;
   u.g_cumsum = g_cumsum;
   u.T = p->T;
@@ -324,7 +329,8 @@ gdn_status gdn_chunk_fwd(const gdn_problem *p, const void *q, const void *k, con
   if (use_tensor_cores(p)) {
     const gdn::UtArgs u = ut_args(p, k, g, nullptr, beta, ws, A, g_cumsum, a.dev_flag);
     if ((e = gdn::launch_ut(u, (int)n_chunk_slots(p), s)) != cudaSuccess) return cuda_fail(e, "UT transform launch");
-    a.xw = static_cast<const __nv_bfloat16 *>(ws);
+    a.xw = u.xw;
+    a.ftab = u.ftab;
     e = gdn::launch_tc_fwd_ws(a, dim3(GDN_DV / gdn::tc_fwd_ws_bv(), p->H, runs), s);
   } else {
     const dim3 grid(GDN_DV / gdn::simt_fwd_bv(), p->H, runs);
@@ -419,7 +425,8 @@ gdn_status gdn_chunk_bwd(const gdn_problem *p, const void *q, const void *k, con
   if (use_tensor_cores(p)) {  // X recomputed from the saved cumulative gate (same values as A)
     const gdn::UtArgs u = ut_args(p, k, nullptr, g_cumsum, beta, xw, nullptr, nullptr, flag);
     if ((e = gdn::launch_ut(u, (int)n_chunk_slots(p), s)) != cudaSuccess) return cuda_fail(e, "UT transform launch");
-    f.xw = static_cast<const __nv_bfloat16 *>(xw);
+    f.xw = u.xw;
+    f.ftab = u.ftab;
     e = gdn::launch_tc_fwd_ws(f, dim3(GDN_DV / gdn::tc_fwd_ws_bv(), p->H, runs), s);
   } else {
     e = gdn::launch_simt_fwd(f, pk, bf, dim3(GDN_DV / gdn::simt_fwd_bv(), p->H, runs), s);

@@ -34,6 +34,7 @@ struct SimtFwdArgs {
   const float *g_cum_in;  // nullable: read the cumulative gate instead of summing g
   const float *A_in;      // nullable: read X = (I + L)^-1 instead of solving
   const __nv_bfloat16 *xw;  // tensor-core path: X of every chunk, [slots, H, 64, 64] bf16
+  const float *ftab;        // tensor-core path: gate factor table of every chunk, [slots, H, 5, 64]
   int *dev_flag;
 };
 
@@ -53,6 +54,7 @@ struct UtArgs {
   const float *g_cum_in;  // the saved cumulative gate (nullable)
   const void *beta;
   __nv_bfloat16 *xw;
+  float *ftab;      // per chunk and head: G, base^G, base^(G_last-G), beta base^G, beta (5 x 64)
   float *A;         // nullable, [rows, H, 64]
   float *g_cumsum;  // nullable
   int T, H;

@@ -77,21 +77,36 @@ struct TransJob {
   uint32_t dst;       // address of the destination tile's K-block holding column s0
   int d0;             // first destination row
 };
-__device__ __forceinline__ void trans16(const TransJob &j, const float *fac, int lane) {
+// The two halves of a transpose, so that a warp can issue the shared-memory
+// loads of several blocks before their stores: load the 16x16 block at source
+// rows s0.. and chunks c0, c0+1 of `src`; store it (scaled by fac[source row]
+// when fac is given) as rows d0..d0+15 of `dst`, columns s0..s0+15.
+__device__ __forceinline__ void trans16_load(uint32_t src, int s0, int c0, int lane, uint32_t (&x)[4]) {
   const int m = lane >> 3, r = lane & 7;
-  uint32_t x[4];
-  ldsm_x4_trans(j.src + chunk_off(j.s0 + r + 8 * (m & 1), j.c0 + (m >> 1)), x);
-  if (fac) {
-    // register i of this thread holds destination (row lane/4, columns 2(lane%4), +1) of
-    // matrix i, i.e. source rows s0 + 8*(i&1) + 2(lane%4) + {0, 1}
+  ldsm_x4_trans(src + chunk_off(s0 + r + 8 * (m & 1), c0 + (m >> 1)), x);
+}
+__device__ __forceinline__ void trans16_store(uint32_t dst, int d0, int s0, const uint32_t (&x)[4],
+                                              const float *fac, int lane) {
+  const int m = lane >> 3, r = lane & 7;
+  uint32_t y[4];
+  // register i of this thread holds destination (row lane/4, columns 2(lane%4), +1) of
+  // matrix i, i.e. source rows s0 + 8*(i&1) + 2(lane%4) + {0, 1}
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int srow = j.s0 + 8 * (i & 1) + 2 * (lane & 3);
+  for (int i = 0; i < 4; ++i) {
+    if (fac) {
+      const int srow = s0 + 8 * (i & 1) + 2 * (lane & 3);
       const float2 t = unpack_bf16(x[i]);
-      x[i] = pack_bf16(t.x * fac[srow], t.y * fac[srow + 1]);
+      y[i] = pack_bf16(t.x * fac[srow], t.y * fac[srow + 1]);
+    } else {
+      y[i] = x[i];
     }
   }
-  stsm_x4(j.dst + chunk_off(j.d0 + r + 8 * (m >> 1), ((j.s0 & 63) >> 3) + (m & 1)), x);
+  stsm_x4(dst + chunk_off(d0 + r + 8 * (m >> 1), ((s0 & 63) >> 3) + (m & 1)), y);
+}
+__device__ __forceinline__ void trans16(const TransJob &j, const float *fac, int lane) {
+  uint32_t x[4];
+  trans16_load(j.src, j.s0, j.c0, lane, x);
+  trans16_store(j.dst, j.d0, j.s0, x, fac, lane);
 }
 
 // --- blocked 64x64 fp32 matrices for the solve ------------------------------------------

@@ -10,8 +10,10 @@
 // X has no dependence on the state, so it is computed here for every chunk
 // in parallel (one CTA of 4 warps per chunk and head; K K^T on bf16 mma.sync,
 // the solve in fp32 shared memory) and written in bf16 for the tensor-core
-// state kernel, which then only multiplies by it. The fp32 X (the A output
-// of the forward) and the cumulative gate are written here when asked for.
+// state kernel, which then only multiplies by it, with a table of the chunk's
+// per-token gate factors (G, base^G, base^(G_last - G), beta base^G, beta).
+// The fp32 X (the A output of the forward) and the cumulative gate are
+// written here when asked for.
 #include "common.cuh"
 #include "kernels.h"
 #include "tc.cuh"
@@ -144,6 +146,15 @@ __global__ void __launch_bounds__(128) ut_kernel(UtArgs a) {
     }
   }
   if (a.g_cumsum && !a.g_cum_in && tid < n) a.g_cumsum[(r0 + tid) * H + h] = sG[tid];
+  if (tid < 64) {  // per-token gate factors for the state kernel
+    float *tab = a.ftab + ((int64_t)slot * H + h) * 5 * GDN_CHUNK;
+    const float G = sG[tid], eg = gexp<E2>(G), bt = sbeta[tid];
+    tab[tid] = G;
+    tab[64 + tid] = eg;
+    tab[128 + tid] = gexp<E2>(sG[63] - G);
+    tab[192 + tid] = bt * eg;
+    tab[256 + tid] = bt;
+  }
 }
 
 }  // namespace
