@@ -1,0 +1,456 @@
+// Tensor-core (tcgen05) reverse state recurrence of the backward (dhu) for bf16
+// inputs, scalar gate (sm_103a), overlapped with the preparation of the
+// previous chunk.
+//
+// For every run and head, from the last chunk to the first (the reverse loop of
+// the hyper-parallel "Diff Coverage" page's kda_state_grad_ext_kernel; KDA
+// adapter backward, stage bwd_dhu), with dh the gradient of the chunk's exit
+// state:
+//
+//   dv_new = kgl dh + scale A_qk^T dO                 kgl = K (.) base^(G_last - G)
+//   dh    <- base^(G_last) dh + scale (Q (.) base^G)^T dO - w^T dv_new
+//                                                      w   = X diag(beta base^G) K
+//
+// One CTA (512 threads) owns one run of one head and 64 of the 128 value
+// columns; dh lives in fp32 registers of the chain warps 0..7, which run
+//   D1   [kgl; -] dh^T-operand  accumulated onto  scale A_qk^T dO   -> dv_new
+//   D2   -w^T dv_new            accumulated onto  scale Qg^T dO     -> dh update
+// while the producer warps 8..15 prepare the previous chunk: A_qk^T (from
+// [Q; K] Q^T and the gate), the three h-independent products scale A_qk^T dO,
+// scale Qg^T dO and w^T (= (beta base^G K)^T X^T), and the operands kgl and
+// w^T. X and the per-token gate factors come from the UT transform kernel.
+// It writes dh of every chunk (the exit-state gradient) and dv_new in fp32
+// for the local-gradient kernel, and dh of the first chunk's entry as dh0.
+// Every mbarrier wait is bounded; a wait that runs out sets the device flag
+// and the CTA drains its MMAs, frees its tensor memory and leaves.
+#include "common.cuh"
+#include "kernels.h"
+#include "tc.cuh"
+#include "tile_ops.cuh"
+
+namespace gdn {
+namespace {
+using namespace tc;
+using namespace tile;
+
+constexpr int TBV = 64;   // value columns per CTA
+constexpr int NTH = 512;  // 256 chain + 256 producer threads
+constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t T_S = 0;     // 2 x 64: [Q; K] Q^T per parity (rows 64..127 = K Q^T)
+constexpr uint32_t T_I1 = 128;  // 2 x 64: rows 0..63 = scale A_qk^T dO, then dv_new
+constexpr uint32_t T_I2 = 256;  // 2 x 64: scale Qg^T dO, then the dh increment
+constexpr uint32_t T_WT = 384;  // 64: w^T (keys x tokens)
+
+// shared memory (bytes from a 1024-aligned base); K-major tiles, 128 B rows
+constexpr int SZ_STAGE = 32768;               // [Q; K]: 2 K-blocks x 128 rows
+constexpr int OFF_ST = 0;                     // 2 stages
+constexpr int OFF_X0 = OFF_ST + 2 * SZ_STAGE; // X of even-order chunks (64 rows)
+constexpr int OFF_X1 = OFF_X0 + 8192;
+constexpr int OFF_DO = OFF_X1 + 8192;         // dO slice, natural (64 rows, one buffer)
+constexpr int OFF_DOT = OFF_DO + 8192;        // dO^T (64 value rows)
+constexpr int OFF_AQT = OFF_DOT + 8192;       // A_qk^T rows 0..63 (rows 64..127 of the operand: QGT)
+constexpr int OFF_QGT = OFF_AQT + 8192;       // (scale base^G Q)^T   128 rows
+constexpr int OFF_B3K = OFF_QGT + 16384;      // (beta base^G K)^T    128 rows
+constexpr int OFF_KGL = OFF_B3K + 16384;      // kgl, 2 K-blocks of 64 rows
+constexpr int OFF_WT = OFF_KGL + 16384;       // w^T, 128 rows
+constexpr int OFF_DHT = OFF_WT + 16384;       // dh^T, 2 K-blocks x 64 rows
+constexpr int OFF_DVT = OFF_DHT + 16384;      // dv_new^T, 64 rows
+constexpr int OFF_SMALL = OFF_DVT + 8192;
+constexpr int SMALL_BYTES = 4096;
+constexpr int SMEM_BYTES = OFF_SMALL + SMALL_BYTES + 1024;
+static_assert(SMEM_BYTES <= 232448, "shared memory");
+
+constexpr uint32_t WAIT_LIMIT = 1u << 22;
+
+enum { F_G = 0, F_EG = 1, F_EGL = 2, F_BEG = 3, F_BETA = 4 };
+struct BwState {
+  alignas(16) float tab[2][5][64];  // gate factor table per order parity
+  float seg[2][64];                 // scale base^G
+  float EL[2];
+  uint64_t bar_p1, bar_p3, bar_d1, bar_d2, bar_x0, bar_x1;
+  uint32_t tmem;
+};
+static_assert(sizeof(BwState) <= SMALL_BYTES, "small state");
+
+__device__ __forceinline__ void chain_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+__device__ __forceinline__ void prod_sync() { asm volatile("bar.sync 2, 256;" ::: "memory"); }
+__device__ __forceinline__ void sts_u16(uint32_t addr, uint16_t v) {
+  asm volatile("st.shared.u16 [%0], %1;" ::"r"(addr), "h"(v) : "memory");
+}
+__device__ __forceinline__ uint16_t bf16_bits(float x) {
+  const __nv_bfloat16 b = __float2bfloat16_rn(x);
+  return *reinterpret_cast<const uint16_t *>(&b);
+}
+
+template <bool E2>
+__global__ void __launch_bounds__(NTH, 1) tc_dhu_kernel(BwdArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                            ~static_cast<uintptr_t>(1023));
+  BwState &st = *reinterpret_cast<BwState *>(sm + OFF_SMALL);
+  const uint32_t sb = smem_u32(sm);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const bool producer = warp >= 8;
+  const int q4 = warp & 3, hc = (warp >> 2) & 1, row = q4 * 32 + lane;
+  const int H = a.H, h = blockIdx.y, z = blockIdx.z;
+  const int col0 = blockIdx.x * TBV;
+  const float scale = a.scale;
+  const __nv_bfloat16 *q = static_cast<const __nv_bfloat16 *>(a.q);
+  const __nv_bfloat16 *k = static_cast<const __nv_bfloat16 *>(a.k);
+  const __nv_bfloat16 *dO = static_cast<const __nv_bfloat16 *>(a.dO);
+
+  // ---- the run: chunk slots as the forward (X workspace: xbase + c; states: slot()) ----
+  int64_t r0, r1, chunk_base = 0, xbase;
+  int b = 0;
+  const int NT = (a.T + GDN_CHUNK - 1) / GDN_CHUNK;
+  if (a.cu) {
+    r0 = a.cu[z];
+    r1 = a.cu[z + 1];
+    bool ok = r0 >= 0 && r1 > r0 && r1 <= a.T;
+    if (ok) {
+      for (int m = 0; m < z; ++m) chunk_base += (a.cu[m + 1] - a.cu[m] + GDN_CHUNK - 1) / GDN_CHUNK;
+      ok = chunk_base + (r1 - r0 + GDN_CHUNK - 1) / GDN_CHUNK <= a.num_chunks;
+    }
+    if (!ok) {
+      if (tid == 0) raise_device_flag(a.dev_flag, kDevCheck);
+      return;
+    }
+    xbase = chunk_base;
+  } else {
+    b = z;
+    r0 = (int64_t)b * a.T;
+    r1 = r0 + a.T;
+    xbase = (int64_t)b * NT;
+  }
+  const int state_idx = z;
+  const int64_t nch = (r1 - r0 + GDN_CHUNK - 1) / GDN_CHUNK;
+  auto chunk_rows = [&](int64_t c) { return (int)min((int64_t)GDN_CHUNK, r1 - (r0 + c * GDN_CHUNK)); };
+  auto state_slot = [&](int64_t c) -> int64_t {
+    return a.cu ? (chunk_base + c) * H + h : ((int64_t)b * H + h) * NT + c;
+  };
+  // order index m = nch - 1 - c: the reverse loop visits m = 0, 1, ...
+  auto chunk_of = [&](int64_t m) { return nch - 1 - m; };
+
+  // ---- tensor memory, barriers -------------------------------------------------------
+  if (warp == 0) {
+    tmem_alloc(&st.tmem, TMEM_COLS);
+    tmem_relinquish();
+  }
+  if (tid == 0) {
+    mbar_init(&st.bar_p1, 1);
+    mbar_init(&st.bar_p3, 1);
+    mbar_init(&st.bar_d1, 1);
+    mbar_init(&st.bar_d2, 1);
+    mbar_init(&st.bar_x0, 1);
+    mbar_init(&st.bar_x1, 1);
+    mbar_fence_init();
+  }
+  fence_before_sync();
+  __syncthreads();
+  fence_after_sync();
+  const uint32_t tmem = st.tmem;
+  const uint32_t tl = tmem + ((uint32_t)(q4 * 32) << 16);
+  bool bad = false;
+  auto wait_par = [&](uint64_t *bar, int64_t phase) {
+    if (!mbar_wait(bar, (uint32_t)(phase & 1), WAIT_LIMIT)) bad = true;
+    fence_after_sync();
+  };
+
+  // ---- producer: loads -----------------------------------------------------------------
+  const int ptid = tid - 256;
+  // copies are issued by producer warps 9..15 only: the MMA-issuing thread (ptid 0,
+  // warp 8) keeps no copies of its own in flight
+  const int ltid = ptid - 32;  // 0..223 on the copying warps
+  auto issue_qkx = [&](int64_t m) {  // Q, K, X and the gate table of order index m
+    const int64_t c = chunk_of(m);
+    const uint32_t stg = sb + OFF_ST + (int)(m & 1) * SZ_STAGE;
+    const uint32_t xt = sb + ((m & 1) ? OFF_X1 : OFF_X0);
+    const int64_t c0 = r0 + c * GDN_CHUNK;
+    const int n = chunk_rows(c);
+    const int64_t xs = (xbase + c) * H + h;
+    const __nv_bfloat16 *xsrc = a.xw + xs * (GDN_CHUNK * GDN_CHUNK);
+#pragma unroll
+    for (int x = ltid; x >= 0 && x < 2048 + 512; x += 224) {
+      if (x < 2048) {
+        const int which = x >> 10, r = (x >> 4) & 63, f16 = x & 15;  // which 0: Q rows 0..63, 1: K rows 64..127
+        const bool valid = r < n;
+        const __nv_bfloat16 *src = (which ? k : q) + ((c0 + (valid ? r : 0)) * H + h) * GDN_DK + f16 * 8;
+        cp_async16(stg + (f16 >> 3) * 16384 + chunk_off(r + which * 64, f16 & 7), src, valid ? 16u : 0u);
+      } else {
+        const int r = (x - 2048) >> 3, c8 = x & 7;
+        cp_async16(xt + chunk_off(r, c8), xsrc + r * GDN_CHUNK + c8 * 8, 16u);
+      }
+    }
+    if (ltid >= 0 && ltid < 80)
+      cp_async16(smem_u32(&st.tab[m & 1][0][0]) + ltid * 16, a.ftab + xs * 5 * GDN_CHUNK + ltid * 4, 16u);
+  };
+  auto issue_do = [&](int64_t m) {  // the CTA's 64 columns of dO
+    const int64_t c = chunk_of(m);
+    const int64_t c0 = r0 + c * GDN_CHUNK;
+    const int n = chunk_rows(c);
+#pragma unroll
+    for (int x = ltid; x >= 0 && x < 512; x += 224) {
+      const int r = x >> 3, c8 = x & 7;
+      const bool valid = r < n;
+      const __nv_bfloat16 *src = dO + ((c0 + (valid ? r : 0)) * H + h) * GDN_DV + col0 + c8 * 8;
+      cp_async16(sb + OFF_DO + chunk_off(r, c8), src, valid ? 16u : 0u);
+    }
+  };
+
+  // ---- producer: one chunk (order index pm) ------------------------------------------------
+  auto produce = [&](int64_t pm, int64_t m_chain) {
+    const int ps = (int)(pm & 1);
+    const uint32_t stg = sb + OFF_ST + ps * SZ_STAGE;
+    const float(&tab)[5][64] = st.tab[ps];
+    if (pm + 1 < nch) issue_qkx(pm + 1);
+    cp_async_commit();
+    cp_async_wait<1>();  // Q, K, X, factors and dO of this chunk have landed
+    fence_proxy_async();
+    prod_sync();
+    if (ptid == 0) {  // P1: [Q; K] Q^T (rows 64..127 = K Q^T)
+      st.EL[ps] = tab[F_EG][63];
+      fence_after_sync();
+      mma_tiles(tmem + T_S + 64 * ps, stg, 16384, stg, 16384, 128, idesc_bf16(128, 64), false);
+      mma_commit(&st.bar_p1);
+    }
+    __syncwarp();
+    if (ptid < 64) st.seg[ps][ptid] = scale * tab[F_EG][ptid];
+    prod_sync();
+    // transposes: K (rows 64..127) -> (beta base^G K)^T; Q -> (scale base^G Q)^T; dO -> dO^T
+    {
+      const int pw = warp - 8;
+      uint32_t xk[4][4], xq[4][4], xd[2][4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int jb = pw + 8 * i, rb = jb >> 3, fb = jb & 7;
+        trans16_load(stg + (fb >> 2) * 16384, 64 + rb * 16, (fb & 3) * 2, lane, xk[i]);
+        trans16_load(stg + (fb >> 2) * 16384, rb * 16, (fb & 3) * 2, lane, xq[i]);
+      }
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        const int t = pw + 8 * i, rb = t >> 2, cb = t & 3;
+        trans16_load(sb + OFF_DO, rb * 16, cb * 2, lane, xd[i]);
+      }
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        const int t = pw + 8 * i, rb = t >> 2, cb = t & 3;
+        trans16_store(sb + OFF_DOT, cb * 16, rb * 16, xd[i], nullptr, lane);
+      }
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int jb = pw + 8 * i, rb = jb >> 3, fb = jb & 7;
+        // destination columns are token indices: the source row offset of K (64) is dropped
+        trans16_store(sb + OFF_B3K, fb * 16, rb * 16, xk[i], tab[F_BEG], lane);
+        trans16_store(sb + OFF_QGT, fb * 16, rb * 16, xq[i], st.seg[ps], lane);
+      }
+    }
+    prod_sync();  // dO consumed: load the next chunk's
+    if (pm + 1 < nch) issue_do(pm + 1);
+    cp_async_commit();
+    // gating of K Q^T (rows 64..127 of S): A_qk^T[s][t] = scale (k_s . q_t) base^(G_t - G_s), t >= s
+    wait_par(&st.bar_p1, pm);
+    if (q4 >= 2) {
+      const int s = row - 64;
+      float sv[32];
+      tmem_ld16(tl + T_S + 64 * ps + 32 * hc, *reinterpret_cast<float(*)[16]>(sv));
+      tmem_ld16(tl + T_S + 64 * ps + 32 * hc + 16, *reinterpret_cast<float(*)[16]>(sv + 16));
+      tmem_ld_wait();
+      const float Gs = tab[F_G][s];
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        const int t = 32 * hc + j;
+        sv[j] = t >= s ? scale * sv[j] * gexp<E2>(tab[F_G][t] - Gs) : 0.f;
+      }
+      uint8_t *dst = sm + OFF_AQT;
+#pragma unroll
+      for (int q8 = 0; q8 < 4; ++q8)
+        *reinterpret_cast<uint4 *>(dst + chunk_off(s, 4 * hc + q8)) = pack8(sv + 8 * q8);
+    }
+    fence_proxy_async();
+    fence_before_sync();
+    prod_sync();
+    if (ptid == 0) {  // the h-independent products
+      fence_after_sync();
+      const uint32_t xt = sb + (ps ? OFF_X1 : OFF_X0);
+      // scale A_qk^T dO  (rows 64..127 of the operand are not used)
+      mma_tiles(tmem + T_I1 + 64 * ps, sb + OFF_AQT, 8192, sb + OFF_DOT, 8192, 64, idesc_bf16(128, 64), false);
+      // scale Qg^T dO
+      mma_tiles(tmem + T_I2 + 64 * ps, sb + OFF_QGT, 16384, sb + OFF_DOT, 8192, 64, idesc_bf16(128, 64), false);
+      // w^T = (beta base^G K)^T X^T
+      mma_tiles(tmem + T_WT, sb + OFF_B3K, 16384, xt, 8192, 64, idesc_bf16(128, 64), false);
+      mma_commit(&st.bar_p3);
+    }
+    __syncwarp();
+    // kgl rows (K rows scaled by base^(G_last - G)) once the chain's D1 has read the previous ones
+    if (m_chain >= 0) wait_par(&st.bar_d1, m_chain);
+    if (q4 >= 2) {
+      const int t = row - 64;
+      const float egl = tab[F_EGL][t];
+      const uint8_t *krow = sm + OFF_ST + ps * SZ_STAGE + hc * 16384;
+      uint8_t *dst = sm + OFF_KGL + hc * 8192;
+#pragma unroll
+      for (int c8 = 0; c8 < 8; ++c8) {
+        float f[8];
+        unpack8(*reinterpret_cast<const uint4 *>(krow + chunk_off(row, c8)), f);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) f[e] *= egl;
+        *reinterpret_cast<uint4 *>(dst + chunk_off(t, c8)) = pack8(f);
+      }
+    }
+    // w^T rows (keys) once the products are done and the chain's D2 has read the previous ones
+    wait_par(&st.bar_p3, pm);
+    if (m_chain >= 0) wait_par(&st.bar_d2, m_chain);
+    {
+      uint8_t *dst = sm + OFF_WT;
+#pragma unroll
+      for (int part = 0; part < 2; ++part) {
+        float sv[16];
+        tmem_ld16(tl + T_WT + 32 * hc + 16 * part, sv);
+        tmem_ld_wait();
+        *reinterpret_cast<uint4 *>(dst + chunk_off(row, 4 * hc + 2 * part)) = pack8(sv);
+        *reinterpret_cast<uint4 *>(dst + chunk_off(row, 4 * hc + 2 * part + 1)) = pack8(sv + 8);
+      }
+    }
+    fence_proxy_async();
+    fence_before_sync();
+  };
+
+  // ---- chain ----------------------------------------------------------------------------
+  float dh[32];
+  if (!producer) {
+    const float *src = a.dht ? a.dht + ((int64_t)state_idx * H + h) * GDN_DK * GDN_DV + (int64_t)row * GDN_DV +
+                                   col0 + 32 * hc
+                             : nullptr;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) dh[j] = src ? src[j] : 0.f;
+  }
+  auto write_dht = [&]() {  // dh^T (B operand of D1): key `row`, columns 32*hc .. +32
+    const uint32_t hbase = sb + OFF_DHT + (row >> 6) * 8192 + (row & 7) * 2;
+    const int kc = (row & 63) >> 3;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) sts_u16(hbase + chunk_off(32 * hc + j, kc), bf16_bits(dh[j]));
+  };
+  auto chain = [&](int64_t m) {
+    const int cs = (int)(m & 1);
+    const int64_t c = chunk_of(m);
+    const int64_t c0 = r0 + c * GDN_CHUNK;
+    const int n = chunk_rows(c);
+    {  // gradient of this chunk's exit state
+      float4 *dst = reinterpret_cast<float4 *>(a.dh_chunks + state_slot(c) * GDN_DK * GDN_DV +
+                                               (int64_t)row * GDN_DV + col0 + 32 * hc);
+#pragma unroll
+      for (int g4 = 0; g4 < 8; ++g4) dst[g4] = make_float4(dh[4 * g4], dh[4 * g4 + 1], dh[4 * g4 + 2], dh[4 * g4 + 3]);
+    }
+    if (tid == 0) {  // D1: dv_new = kgl dh + scale A_qk^T dO
+      fence_after_sync();
+      mma_tiles(tmem + T_I1 + 64 * cs, sb + OFF_KGL, 8192, sb + OFF_DHT, 8192, 128, idesc_bf16(128, 64), true);
+      mma_commit(&st.bar_d1);
+    }
+    __syncwarp();
+    wait_par(&st.bar_d1, m);
+    if (q4 < 2) {  // dv_new rows: fp32 to the workspace, bf16 into dv_new^T
+      const uint32_t base = sb + OFF_DVT + (row & 7) * 2;
+      const bool valid = row < n;
+      float4 *gdst = reinterpret_cast<float4 *>(a.dvnew + ((c0 + (valid ? row : 0)) * H + h) * GDN_DV + col0 + 32 * hc);
+#pragma unroll
+      for (int part = 0; part < 2; ++part) {
+        float dv[16];
+        tmem_ld16(tl + T_I1 + 64 * cs + 32 * hc + 16 * part, dv);
+        tmem_ld_wait();
+        if (valid) {
+#pragma unroll
+          for (int g4 = 0; g4 < 4; ++g4)
+            gdst[4 * part + g4] = make_float4(dv[4 * g4], dv[4 * g4 + 1], dv[4 * g4 + 2], dv[4 * g4 + 3]);
+        }
+#pragma unroll
+        for (int j = 0; j < 16; ++j) sts_u16(base + chunk_off(32 * hc + 16 * part + j, row >> 3), bf16_bits(dv[j]));
+      }
+    }
+    fence_proxy_async();
+    fence_before_sync();
+    chain_sync();
+    if (tid == 0) {  // D2: dh increment = scale Qg^T dO - w^T dv_new
+      fence_after_sync();
+      mma_tiles(tmem + T_I2 + 64 * cs, sb + OFF_WT, 16384, sb + OFF_DVT, 8192, 64, idesc_bf16(128, 64, true), true);
+      mma_commit(&st.bar_d2);
+    }
+    __syncwarp();
+    wait_par(&st.bar_d2, m);
+    {
+      const float el = st.EL[cs];
+      const uint32_t hbase = sb + OFF_DHT + (row >> 6) * 8192 + (row & 7) * 2;
+      const int kc = (row & 63) >> 3;
+#pragma unroll
+      for (int part = 0; part < 2; ++part) {
+        float inc[16];
+        tmem_ld16(tl + T_I2 + 64 * cs + 32 * hc + 16 * part, inc);
+        tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          float &d = dh[16 * part + j];
+          d = fmaf(el, d, inc[j]);
+          sts_u16(hbase + chunk_off(32 * hc + 16 * part + j, kc), bf16_bits(d));
+        }
+      }
+    }
+    fence_proxy_async();
+    fence_before_sync();
+  };
+
+  // ---- prologue and rounds ------------------------------------------------------------------
+  if (producer && nch > 0) {
+    issue_qkx(0);
+    cp_async_commit();
+    issue_do(0);
+    cp_async_commit();
+  }
+  if (!producer) {
+    write_dht();
+    fence_proxy_async();
+  }
+  __syncthreads();
+  // round m: the chain runs order index m while the producer prepares m+1
+  for (int64_t m = -1; m < nch; ++m) {
+    if (producer) {
+      if (m + 1 < nch) produce(m + 1, m);
+    } else if (m >= 0) {
+      chain(m);
+    }
+    if (__syncthreads_or(bad)) {
+      bad = true;
+      break;
+    }
+  }
+
+  if (bad) {
+    if (tid == 0) {
+      raise_device_flag(a.dev_flag, kDevTimeout);
+      mma_commit(&st.bar_x0);  // arrives once every MMA this thread issued has finished
+    }
+    if (tid == 256) mma_commit(&st.bar_x1);
+    if (tid == 0) mbar_wait(&st.bar_x0, 0, WAIT_LIMIT);
+    if (tid == 256) mbar_wait(&st.bar_x1, 0, WAIT_LIMIT);
+    cp_async_wait<0>();
+  } else if (!producer && a.dh0) {
+    float4 *dst = reinterpret_cast<float4 *>(a.dh0 + ((int64_t)state_idx * H + h) * GDN_DK * GDN_DV +
+                                             (int64_t)row * GDN_DV + col0 + 32 * hc);
+#pragma unroll
+    for (int g4 = 0; g4 < 8; ++g4) dst[g4] = make_float4(dh[4 * g4], dh[4 * g4 + 1], dh[4 * g4 + 2], dh[4 * g4 + 3]);
+  }
+  fence_before_sync();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tmem, TMEM_COLS);
+}
+
+}  // namespace
+
+cudaError_t launch_tc_dhu(const BwdArgs &a, int runs, cudaStream_t st) {
+  auto kern = a.use_exp2 ? tc_dhu_kernel<true> : tc_dhu_kernel<false>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  kern<<<dim3(GDN_DV / TBV, a.H, runs), NTH, SMEM_BYTES, st>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace gdn

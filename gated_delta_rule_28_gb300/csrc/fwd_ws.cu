@@ -42,23 +42,25 @@ constexpr uint32_t T_U = 256;   // 2 x 64: P3b rows 0..63 = u, per chunk parity
 constexpr uint32_t T_D4 = 384;  // 64: P4 rows 0..63 = w h, rows 64..127 = q' h (+ A_qk v_new)
 constexpr uint32_t T_P5 = 448;  // 64: P5
 
-// shared memory map (bytes from a 1024-aligned base); every tile K-major, 128 B rows
-constexpr int SZ_STAGE = 40960;            // [K; Q] (2 K-blocks x 128 rows) + X (64 rows)
-constexpr int ST_X = 32768;                // X inside a stage; the 8 KB after it are the
-                                           // (unused) rows 64..127 of the P3b operand
-constexpr int OFF_ST = 0;                  // 2 stages
+// shared memory map (bytes from a 1024-aligned base); every tile K-major, 128 B rows.
+// The P3b operand is a 128-row tile whose rows 64..127 are not used: each X tile
+// is placed in front of a buffer that no copy writes while P3b runs (B3, KL),
+// and the A_qk tiles behind v_new^T for the same reason.
+constexpr int SZ_STAGE = 32768;                // [K; Q]: 2 K-blocks x 128 rows
+constexpr int OFF_ST = 0;                      // 2 stages
 constexpr int OFF_V = OFF_ST + 2 * SZ_STAGE;   // V slice, 64 rows (one buffer)
-constexpr int OFF_B3 = OFF_V + 8192;           // [b e^G K | b V]^T       192 rows
-constexpr int OFF_KL = OFF_B3 + 24576;         // (e^(Gl-G) K)^T           2 x 128 rows
-constexpr int OFF_WQ = OFF_KL + 2 * 16384;     // [w; e^G Q]               2 K-blocks x 128 rows
-constexpr int OFF_AQ = OFF_WQ + 32768;         // A_qk                     2 x 64 rows
-constexpr int OFF_HT = OFF_AQ + 2 * 8192;      // h^T                      2 K-blocks x 64 rows
-constexpr int OFF_VN = OFF_HT + 16384;         // v_new^T                  64 rows
-constexpr int OFF_SMALL = OFF_VN + 8192;
+constexpr int OFF_X0 = OFF_V + 8192;           // X of even chunks              64 rows
+constexpr int OFF_B3 = OFF_X0 + 8192;          // [b e^G K | b V]^T            192 rows
+constexpr int OFF_X1 = OFF_B3 + 24576;         // X of odd chunks               64 rows
+constexpr int OFF_KL = OFF_X1 + 8192;          // (e^(Gl-G) K)^T                2 x 128 rows
+constexpr int OFF_WQ = OFF_KL + 2 * 16384;     // [w; e^G Q]                    2 K-blocks x 128 rows
+constexpr int OFF_HT = OFF_WQ + 32768;         // h^T                           2 K-blocks x 64 rows
+constexpr int OFF_VN = OFF_HT + 16384;         // v_new^T                       64 rows
+constexpr int OFF_AQ = OFF_VN + 8192;          // A_qk                          2 x 64 rows
+constexpr int OFF_SMALL = OFF_AQ + 2 * 8192;
 constexpr int SMALL_BYTES = 4096;
 constexpr int SMEM_BYTES = OFF_SMALL + SMALL_BYTES + 1024;
 static_assert(SMEM_BYTES <= 232448, "shared memory");
-static_assert(OFF_AQ >= 8192, "rows 0..63 of the A_qk operand precede its buffer");
 
 constexpr uint32_t WAIT_LIMIT = 1u << 22;
 
@@ -170,15 +172,19 @@ __global__ void __launch_bounds__(NTH, 1) tc_fwd_ws_kernel(SimtFwdArgs a) {
   };
 
   // ---- producer: loads -----------------------------------------------------------------
-  const int ptid = tid - 256;  // 0..255 on producer threads
-  auto issue_kqx = [&](int64_t c) {  // K, Q, X and the gate factors of chunk c into stage c&1
+  const int ptid = tid - 256;
+  // copies are issued by producer warps 9..15 only: the MMA-issuing thread (ptid 0,
+  // warp 8) keeps no copies of its own in flight
+  const int ltid = ptid - 32;  // 0..223 on the copying warps
+  auto issue_kqx = [&](int64_t c) {  // K, Q, X and the gate factors of chunk c (buffers of parity c&1)
     const uint32_t stg = sb + OFF_ST + (int)(c & 1) * SZ_STAGE;
+    const uint32_t xt = sb + ((c & 1) ? OFF_X1 : OFF_X0);
     const int64_t c0 = r0 + c * GDN_CHUNK;
     const int n = chunk_rows(c);
     const int64_t xs = (xbase + c) * H + h;
     const __nv_bfloat16 *xsrc = xw + xs * (GDN_CHUNK * GDN_CHUNK);
 #pragma unroll
-    for (int x = ptid; x < 2048 + 512; x += 256) {
+    for (int x = ltid; x >= 0 && x < 2048 + 512; x += 224) {
       if (x < 2048) {
         const int which = x >> 10, r = (x >> 4) & 63, f16 = x & 15;
         const bool valid = r < n;
@@ -186,17 +192,17 @@ __global__ void __launch_bounds__(NTH, 1) tc_fwd_ws_kernel(SimtFwdArgs a) {
         cp_async16(stg + (f16 >> 3) * 16384 + chunk_off(r + which * 64, f16 & 7), src, valid ? 16u : 0u);
       } else {
         const int r = (x - 2048) >> 3, c8 = x & 7;
-        cp_async16(stg + ST_X + chunk_off(r, c8), xsrc + r * GDN_CHUNK + c8 * 8, 16u);
+        cp_async16(xt + chunk_off(r, c8), xsrc + r * GDN_CHUNK + c8 * 8, 16u);
       }
     }
-    if (ptid < 80)
-      cp_async16(smem_u32(&st.tab[c & 1][0][0]) + ptid * 16, a.ftab + xs * 5 * GDN_CHUNK + ptid * 4, 16u);
+    if (ltid >= 0 && ltid < 80)
+      cp_async16(smem_u32(&st.tab[c & 1][0][0]) + ltid * 16, a.ftab + xs * 5 * GDN_CHUNK + ltid * 4, 16u);
   };
   auto issue_v = [&](int64_t c) {  // the CTA's 64 columns of V of chunk c
     const int64_t c0 = r0 + c * GDN_CHUNK;
     const int n = chunk_rows(c);
 #pragma unroll
-    for (int x = ptid; x < 512; x += 256) {
+    for (int x = ltid; x >= 0 && x < 512; x += 224) {
       const int r = x >> 3, c8 = x & 7;
       const bool valid = r < n;
       const __nv_bfloat16 *src = v + ((c0 + (valid ? r : 0)) * H + h) * GDN_DV + col0 + c8 * 8;
@@ -221,6 +227,7 @@ __global__ void __launch_bounds__(NTH, 1) tc_fwd_ws_kernel(SimtFwdArgs a) {
       mma_tiles(tmem + T_S + 64 * ps, stg, 16384, stg, 16384, 128, idesc_bf16(128, 64), false);
       mma_commit(&st.bar_p1);
     }
+    __syncwarp();  // the issuing warp reconverges before any of its lanes polls a barrier
     // transposes, loads first: K -> B3 rows 0..127 (b e^G) and KL (e^(Gl-G)); V -> B3 rows 128..191 (b)
     {
       const int pw = warp - 8;
@@ -274,10 +281,12 @@ __global__ void __launch_bounds__(NTH, 1) tc_fwd_ws_kernel(SimtFwdArgs a) {
     prod_sync();
     if (ptid == 0) {  // P3b: w and u
       fence_after_sync();
-      mma_tiles(tmem + T_WW, stg + ST_X, 8192, sb + OFF_B3, 24576, 64, idesc_bf16(128, 128), false);
-      mma_tiles(tmem + T_U + 64 * ps, stg + ST_X, 8192, sb + OFF_B3 + 16384, 24576, 64, idesc_bf16(128, 64), false);
+      const uint32_t xt = sb + (ps ? OFF_X1 : OFF_X0);
+      mma_tiles(tmem + T_WW, xt, 8192, sb + OFF_B3, 24576, 64, idesc_bf16(128, 128), false);
+      mma_tiles(tmem + T_U + 64 * ps, xt, 8192, sb + OFF_B3 + 16384, 24576, 64, idesc_bf16(128, 64), false);
       mma_commit(&st.bar_p3);
     }
+    __syncwarp();  // the issuing warp reconverges before any of its lanes polls a barrier
     // operand of P4: rows 64..127 = e^G Q once the chain's P4 has read the previous one,
     // rows 0..63 = w once P3b is done (keys 64*hc .. +64 per thread)
     uint8_t *wq = sm + OFF_WQ + hc * 16384;
@@ -344,6 +353,7 @@ __global__ void __launch_bounds__(NTH, 1) tc_fwd_ws_kernel(SimtFwdArgs a) {
       mma_tiles(tmem + T_D4, sb + OFF_WQ, 16384, sb + OFF_HT, 8192, 128, idesc_bf16(128, 64), false);
       mma_commit(&st.bar_p4);
     }
+    __syncwarp();  // the issuing warp reconverges before any of its lanes polls a barrier
     wait_par(&st.bar_p4, c);
     if (q4 < 2) {  // v_new = u - w h  ->  v_new^T (column writes)
       const uint32_t base = sb + OFF_VN + (row & 7) * 2;
@@ -368,6 +378,7 @@ __global__ void __launch_bounds__(NTH, 1) tc_fwd_ws_kernel(SimtFwdArgs a) {
       mma_tiles(tmem + T_D4, sb + OFF_AQ + par * 8192 - 8192, 16384, sb + OFF_VN, 8192, 64, idesc_bf16(128, 64), true);
       mma_commit(&st.bar_po);
     }
+    __syncwarp();  // the issuing warp reconverges before any of its lanes polls a barrier
     wait_par(&st.bar_p5, c);
     {
       const float el = st.EL[par];

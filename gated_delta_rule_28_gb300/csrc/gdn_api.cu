@@ -462,7 +462,14 @@ gdn_status gdn_chunk_bwd(const gdn_problem *p, const void *q, const void *k, con
   b.num_chunks = p->num_chunks;
   b.dev_flag = flag;
   // 2. reverse state recurrence
-  if ((e = gdn::launch_bwd_dhu(b, pk, bf, s)) != cudaSuccess) return cuda_fail(e, "dhu launch");
+  if (use_tensor_cores(p)) {
+    b.xw = f.xw;
+    b.ftab = f.ftab;
+    e = gdn::launch_tc_dhu(b, runs, s);
+  } else {
+    e = gdn::launch_bwd_dhu(b, pk, bf, s);
+  }
+  if (e != cudaSuccess) return cuda_fail(e, "dhu launch");
   // 3. local gradients
   if ((e = gdn::launch_bwd_local(b, pk, bf, s)) != cudaSuccess) return cuda_fail(e, "local gradient launch");
   return ok();

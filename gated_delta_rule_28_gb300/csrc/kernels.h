@@ -42,10 +42,6 @@ cudaError_t launch_simt_fwd(const SimtFwdArgs &a, bool per_key, bool bf16, dim3 
                             cudaStream_t st);
 int simt_fwd_bv();  // value columns per CTA
 
-// tcgen05 chunk forward: bf16 inputs, scalar gate, no in-kernel norm
-cudaError_t launch_tc_fwd(const SimtFwdArgs &a, dim3 grid, cudaStream_t st);
-int tc_fwd_bv();
-
 // UT transform of every chunk (bf16 keys, scalar gate): X = (I + L)^-1 in bf16
 // into xw [slots, H, 64, 64]; optionally the fp32 X (A) and the cumulative gate.
 struct UtArgs {
@@ -86,6 +82,8 @@ struct BwdArgs {
   const float *h_chunks;  // workspace: entry state of every chunk
   float *dh_chunks;       // workspace: gradient of every chunk's exit state
   float *dvnew;           // workspace: [rows,H,V] gradient of v_new
+  const __nv_bfloat16 *xw;  // tensor-core path: X of every chunk (UT transform kernel)
+  const float *ftab;        // tensor-core path: gate factor table of every chunk
   int B, T, H;
   float scale;
   int use_exp2;
@@ -96,6 +94,8 @@ struct BwdArgs {
 };
 cudaError_t launch_bwd_dhu(const BwdArgs &a, bool per_key, bool bf16, cudaStream_t st);
 cudaError_t launch_bwd_local(const BwdArgs &a, bool per_key, bool bf16, cudaStream_t st);
+// tcgen05 reverse state recurrence (bf16, scalar gate); needs a.xw / a.ftab
+cudaError_t launch_tc_dhu(const BwdArgs &a, int runs, cudaStream_t st);
 
 }  // namespace gdn
 

@@ -8,12 +8,14 @@
 //   L = strictly-lower(diag(beta) (K K^T (.) Gamma)),  Gamma_ij = base^(G_i - G_j)
 //   X = (I + L)^-1
 // X has no dependence on the state, so it is computed here for every chunk
-// in parallel (one CTA of 4 warps per chunk and head; K K^T on bf16 mma.sync,
-// the solve in fp32 shared memory) and written in bf16 for the tensor-core
+// in parallel (persistent CTAs of 4 warps walking the (chunk, head) items; K K^T
+// on bf16 mma.sync, the solve in fp32 shared memory) and written in bf16 for the tensor-core
 // state kernel, which then only multiplies by it, with a table of the chunk's
 // per-token gate factors (G, base^G, base^(G_last - G), beta base^G, beta).
 // The fp32 X (the A output of the forward) and the cumulative gate are
 // written here when asked for.
+#include <algorithm>
+
 #include "common.cuh"
 #include "kernels.h"
 #include "tc.cuh"
@@ -32,140 +34,200 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
+// Persistent: each CTA walks the (chunk, head) items with a stride of the grid,
+// loading the next item's keys while it works on the current one.
 template <bool E2>
-__global__ void __launch_bounds__(128) ut_kernel(UtArgs a) {
-  __shared__ __align__(1024) uint8_t ktile[16384];  // K: 2 K-blocks of 64 rows x 128 B, swizzled
-  __shared__ __align__(16) float LB[10 * 256], XB[10 * 256], TB[4 * 256];
-  __shared__ float sg[64], sG[64], sbeta[64];
+__global__ void __launch_bounds__(128, 4) ut_kernel(UtArgs a, int64_t items) {
+  __shared__ __align__(1024) uint8_t kbuf[2][16384];  // keys (64 rows x 2 K-blocks, swizzled);
+                                                      // the current one then holds L's blocks
+  __shared__ __align__(16) float XB[10 * 256], TB[4 * 256];
+  __shared__ __align__(16) float sg[64];
+  __shared__ __align__(16) float sG[64];
+  __shared__ __align__(16) float sbeta[64];
 
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int slot = blockIdx.x, h = blockIdx.y, H = a.H;
-  int64_t r0, r1;
-  if (a.cu) {
-    const int seq = a.chunk_indices[2 * slot], cc = a.chunk_indices[2 * slot + 1];
-    bool ok = seq >= 0 && seq < a.num_seqs && cc >= 0;
-    if (ok) {
-      r0 = (int64_t)a.cu[seq] + (int64_t)cc * GDN_CHUNK;
-      r1 = a.cu[seq + 1];
-      ok = r0 >= 0 && r0 < r1 && r1 <= a.T;
-    }
-    if (!ok) {
-      if (tid == 0) raise_device_flag(a.dev_flag, kDevCheck);
-      return;
-    }
-  } else {
-    const int NT = (a.T + GDN_CHUNK - 1) / GDN_CHUNK;
-    const int b = slot / NT, c = slot % NT;
-    r0 = (int64_t)b * a.T + (int64_t)c * GDN_CHUNK;
-    r1 = (int64_t)b * a.T + a.T;
-  }
-  const int n = (int)min((int64_t)GDN_CHUNK, r1 - r0);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, H = a.H;
   const __nv_bfloat16 *k = static_cast<const __nv_bfloat16 *>(a.k);
   const __nv_bfloat16 *beta = static_cast<const __nv_bfloat16 *>(a.beta);
-
-  // keys of the chunk, zero past its end
-  const uint32_t kt = smem_u32(ktile);
-#pragma unroll
-  for (int x = tid; x < 1024; x += 128) {
-    const int r = x >> 4, f16 = x & 15;
-    const bool valid = r < n;
-    const __nv_bfloat16 *src = k + ((r0 + (valid ? r : 0)) * H + h) * GDN_DK + f16 * 8;
-    cp_async16(kt + (f16 >> 3) * 8192 + chunk_off(r, f16 & 7), src, valid ? 16u : 0u);
-  }
-  cp_async_commit();
-  // gate and beta; rows past the end: no gate increment, beta 0
   const float *gsrc = a.g_cum_in ? a.g_cum_in : a.g;
-  if (tid < 64) {
-    sg[tid] = tid < n ? gsrc[(r0 + tid) * H + h] : 0.f;
-    sbeta[tid] = tid < n ? __bfloat162float(beta[(r0 + tid) * H + h]) : 0.f;
-  }
-  __syncthreads();
-  if (a.g_cum_in) {
-    if (tid < 64) sG[tid] = sg[min(tid, n - 1)];
-  } else if (warp == 0) {
-    const float x0 = sg[2 * lane], x1 = sg[2 * lane + 1], pair = x0 + x1;
-    float incl = pair;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-      const float y = __shfl_up_sync(0xffffffffu, incl, off);
-      if (lane >= off) incl += y;
+  const int NT = (a.T + GDN_CHUNK - 1) / GDN_CHUNK;
+
+  // rows [r0, r0 + n) of item it = slot * H + h; false for a corrupt packed chunk index
+  auto locate = [&](int64_t it, int64_t &r0, int &n) -> bool {
+    const int64_t slot = it / H;
+    int64_t r1;
+    if (a.cu) {
+      const int seq = a.chunk_indices[2 * slot], cc = a.chunk_indices[2 * slot + 1];
+      if (!(seq >= 0 && seq < a.num_seqs && cc >= 0)) return false;
+      r0 = (int64_t)a.cu[seq] + (int64_t)cc * GDN_CHUNK;
+      r1 = a.cu[seq + 1];
+      if (!(r0 >= 0 && r0 < r1 && r1 <= a.T)) return false;
+    } else {
+      const int64_t b = slot / NT, c = slot % NT;
+      r0 = b * a.T + c * GDN_CHUNK;
+      r1 = b * a.T + a.T;
     }
-    const float ex = incl - pair;
-    sG[2 * lane] = ex + x0;
-    sG[2 * lane + 1] = ex + pair;
+    n = (int)min((int64_t)GDN_CHUNK, r1 - r0);
+    return true;
+  };
+  auto load_keys = [&](int64_t it, int buf) {  // zero past the chunk end
+    int64_t r0;
+    int n;
+    if (it < items && locate(it, r0, n)) {
+      const int h = (int)(it % H);
+      const uint32_t kt = smem_u32(kbuf[buf]);
+#pragma unroll
+      for (int x = tid; x < 1024; x += 128) {
+        const int r = x >> 4, f16 = x & 15;
+        const bool valid = r < n;
+        const __nv_bfloat16 *src = k + ((r0 + (valid ? r : 0)) * H + h) * GDN_DK + f16 * 8;
+        cp_async16(kt + (f16 >> 3) * 8192 + chunk_off(r, f16 & 7), src, valid ? 16u : 0u);
+      }
+    }
+    cp_async_commit();
+  };
+
+  int buf = 0;
+  load_keys(blockIdx.x, 0);
+  for (int64_t it = blockIdx.x; it < items; it += gridDim.x, buf ^= 1) {
+    int64_t r0 = 0;
+    int n = 0;
+    const bool ok = locate(it, r0, n);
+    const int h = (int)(it % H);
+    const int64_t slot = it / H;
+    if (tid < 64) {  // gate and beta; rows past the end: no gate increment, beta 0
+      sg[tid] = ok && tid < n ? gsrc[(r0 + tid) * H + h] : 0.f;
+      sbeta[tid] = ok && tid < n ? __bfloat162float(beta[(r0 + tid) * H + h]) : 0.f;
+    }
+    cp_async_wait<0>();
+    __syncthreads();
+    load_keys(it + gridDim.x, buf ^ 1);
+    if (!ok) {
+      if (tid == 0) raise_device_flag(a.dev_flag, kDevCheck);
+      continue;  // uniform: every thread saw the same chunk index
+    }
+    if (a.g_cum_in) {
+      if (tid < 64) sG[tid] = sg[min(tid, n - 1)];
+    } else if (warp == 0) {
+      const float x0 = sg[2 * lane], x1 = sg[2 * lane + 1], pair = x0 + x1;
+      float incl = pair;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const float y = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += y;
+      }
+      const float ex = incl - pair;
+      sG[2 * lane] = ex + x0;
+      sG[2 * lane + 1] = ex + pair;
+    }
+
+    // K K^T blocks (bi, bj), bj <= bi, in blk() order; warp w takes blocks w, w+4, w+8
+    const uint32_t kt = smem_u32(kbuf[buf]);
+    float acc[3][2][4];
+#pragma unroll
+    for (int u = 0; u < 3; ++u) {
+      const int bidx = warp + 4 * u;
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc[u][nt][e] = 0.f;
+      if (bidx >= 10) continue;
+      const int bi = bidx < 1 ? 0 : bidx < 3 ? 1 : bidx < 6 ? 2 : 3;
+      const int bj = bidx - bi * (bi + 1) / 2;
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks) {  // 16 features per step
+        const int c8 = (2 * ks + (lane >> 4)) & 7;
+        const uint32_t kb = kt + (ks >> 2) * 8192;
+        uint32_t af[4], bf[4];
+        ldsm_x4(kb + chunk_off(16 * bi + (lane & 15), c8), af);
+        ldsm_x4(kb + chunk_off(16 * bj + (lane & 15), c8), bf);
+        mma_bf16_16816(acc[u][0], af, bf[0], bf[2]);
+        mma_bf16_16816(acc[u][1], af, bf[1], bf[3]);
+      }
+    }
+    __syncthreads();  // every warp is done with the keys: their buffer now takes L
+    float *LB = reinterpret_cast<float *>(kbuf[buf]);
+#pragma unroll
+    for (int u = 0; u < 3; ++u) {
+      const int bidx = warp + 4 * u;
+      if (bidx >= 10) continue;
+      const int bi = bidx < 1 ? 0 : bidx < 3 ? 1 : bidx < 6 ? 2 : 3;
+      const int bj = bidx - bi * (bi + 1) / 2;
+      const int g = lane >> 2, t = lane & 3;
+      float *Lb = LB + blk(bi, bj) * 256;
+      // this thread's rows g, g+8 and columns nt*8 + 2t + {0, 1}
+      const float Gi[2] = {sG[16 * bi + g], sG[16 * bi + g + 8]};
+      const float bi_[2] = {sbeta[16 * bi + g], sbeta[16 * bi + g + 8]};
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt) {
+        const float2 Gj = *reinterpret_cast<const float2 *>(&sG[16 * bj + nt * 8 + 2 * t]);
+#pragma unroll
+        for (int hr = 0; hr < 2; ++hr) {
+          const int r = g + 8 * hr, c = nt * 8 + 2 * t;
+          const int i = 16 * bi + r, j = 16 * bj + c;
+          float2 val;
+          val.x = i > j ? bi_[hr] * acc[u][nt][2 * hr] * gexp<E2>(Gi[hr] - Gj.x) : 0.f;
+          val.y = i > j + 1 ? bi_[hr] * acc[u][nt][2 * hr + 1] * gexp<E2>(Gi[hr] - Gj.y) : 0.f;
+          *reinterpret_cast<float2 *>(&Lb[bsw(r, c)]) = val;  // c even: c, c+1 adjacent after the swizzle
+        }
+      }
+    }
+    __syncthreads();
+    solve_blocks(LB, XB, TB, tid);
+
+    // X rows: thread -> row tid/2, columns 32 (tid&1) .. +32
+    {
+      const int row = tid >> 1, half = tid & 1, bi = row >> 4;
+      float vals[32];
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        const int cb = 2 * half + q;
+#pragma unroll
+        for (int c4 = 0; c4 < 16; c4 += 4) {  // aligned groups of 4 stay contiguous under bsw
+          const float4 x = cb <= bi ? *reinterpret_cast<const float4 *>(&XB[blk(bi, cb) * 256 + bsw(row & 15, c4)])
+                                    : make_float4(0.f, 0.f, 0.f, 0.f);
+          vals[16 * q + c4] = x.x;
+          vals[16 * q + c4 + 1] = x.y;
+          vals[16 * q + c4 + 2] = x.z;
+          vals[16 * q + c4 + 3] = x.w;
+        }
+      }
+      uint4 *dst = reinterpret_cast<uint4 *>(a.xw + ((slot * H + h) * GDN_CHUNK + row) * GDN_CHUNK + 32 * half);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) dst[q] = pack8(vals + 8 * q);
+      if (a.A && row < n) {
+        float4 *Ad = reinterpret_cast<float4 *>(a.A + ((r0 + row) * H + h) * GDN_CHUNK + 32 * half);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) Ad[q] = make_float4(vals[4 * q], vals[4 * q + 1], vals[4 * q + 2], vals[4 * q + 3]);
+      }
+    }
+    if (a.g_cumsum && !a.g_cum_in && tid < n) a.g_cumsum[(r0 + tid) * H + h] = sG[tid];
+    if (tid < 64) {  // per-token gate factors for the state kernel
+      float *tab = a.ftab + (slot * H + h) * 5 * GDN_CHUNK;
+      const float G = sG[tid], eg = gexp<E2>(G), bt = sbeta[tid];
+      tab[tid] = G;
+      tab[64 + tid] = eg;
+      tab[128 + tid] = gexp<E2>(sG[63] - G);
+      tab[192 + tid] = bt * eg;
+      tab[256 + tid] = bt;
+    }
+    __syncthreads();  // sG, sbeta and the X blocks are rewritten by the next item
   }
   cp_async_wait<0>();
-  __syncthreads();
-
-  // L blocks (bi, bj), bj <= bi, in blk() order; warp w takes blocks w, w+4, w+8
-  for (int bidx = warp; bidx < 10; bidx += 4) {
-    const int bi = bidx < 1 ? 0 : bidx < 3 ? 1 : bidx < 6 ? 2 : 3;
-    const int bj = bidx - bi * (bi + 1) / 2;
-    float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-#pragma unroll
-    for (int ks = 0; ks < 8; ++ks) {  // 16 features per step
-      const int c8 = (2 * ks + (lane >> 4)) & 7;
-      const uint32_t kb = kt + (ks >> 2) * 8192;
-      uint32_t af[4], bf[4];
-      ldsm_x4(kb + chunk_off(16 * bi + (lane & 15), c8), af);
-      ldsm_x4(kb + chunk_off(16 * bj + (lane & 15), c8), bf);
-      mma_bf16_16816(acc[0], af, bf[0], bf[2]);
-      mma_bf16_16816(acc[1], af, bf[1], bf[3]);
-    }
-    const int g = lane >> 2, t = lane & 3;
-    float *Lb = LB + blk(bi, bj) * 256;
-#pragma unroll
-    for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int r = g + 8 * (e >> 1), c = nt * 8 + 2 * t + (e & 1);
-        const int i = 16 * bi + r, j = 16 * bj + c;
-        Lb[bsw(r, c)] = i > j ? sbeta[i] * acc[nt][e] * gexp<E2>(sG[i] - sG[j]) : 0.f;
-      }
-  }
-  __syncthreads();
-  solve_blocks(LB, XB, TB, tid);
-
-  // X rows: thread -> row tid/2, columns 32 (tid&1) .. +32
-  {
-    const int row = tid >> 1, half = tid & 1, bi = row >> 4;
-    float vals[32];
-#pragma unroll
-    for (int q = 0; q < 2; ++q) {
-      const int cb = 2 * half + q;
-#pragma unroll
-      for (int cc = 0; cc < 16; ++cc) vals[16 * q + cc] = cb <= bi ? XB[blk(bi, cb) * 256 + bsw(row & 15, cc)] : 0.f;
-    }
-    uint4 *dst = reinterpret_cast<uint4 *>(a.xw + (((int64_t)slot * H + h) * GDN_CHUNK + row) * GDN_CHUNK + 32 * half);
-#pragma unroll
-    for (int q = 0; q < 4; ++q) dst[q] = pack8(vals + 8 * q);
-    if (a.A && row < n) {
-      float4 *Ad = reinterpret_cast<float4 *>(a.A + ((r0 + row) * H + h) * GDN_CHUNK + 32 * half);
-#pragma unroll
-      for (int q = 0; q < 8; ++q) Ad[q] = make_float4(vals[4 * q], vals[4 * q + 1], vals[4 * q + 2], vals[4 * q + 3]);
-    }
-  }
-  if (a.g_cumsum && !a.g_cum_in && tid < n) a.g_cumsum[(r0 + tid) * H + h] = sG[tid];
-  if (tid < 64) {  // per-token gate factors for the state kernel
-    float *tab = a.ftab + ((int64_t)slot * H + h) * 5 * GDN_CHUNK;
-    const float G = sG[tid], eg = gexp<E2>(G), bt = sbeta[tid];
-    tab[tid] = G;
-    tab[64 + tid] = eg;
-    tab[128 + tid] = gexp<E2>(sG[63] - G);
-    tab[192 + tid] = bt * eg;
-    tab[256 + tid] = bt;
-  }
 }
 
 }  // namespace
 
 cudaError_t launch_ut(const UtArgs &a, int slots, cudaStream_t st) {
   if (slots <= 0) return cudaSuccess;
-  const dim3 grid(slots, a.H);
-  if (a.use_exp2)
-    ut_kernel<true><<<grid, 128, 0, st>>>(a);
-  else
-    ut_kernel<false><<<grid, 128, 0, st>>>(a);
+  const int64_t items = (int64_t)slots * a.H;
+  auto kern = a.use_exp2 ? ut_kernel<true> : ut_kernel<false>;
+  int dev = 0, sms = 0, per_sm = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 128, 0);
+  if (e != cudaSuccess) return e;
+  const int64_t grid = std::min<int64_t>(items, (int64_t)std::max(1, sms * std::max(1, per_sm)));
+  kern<<<(unsigned)grid, 128, 0, st>>>(a, items);
   return cudaGetLastError();
 }
 

@@ -78,3 +78,13 @@ def test_backward_training_workload_slice():
     from gated_delta_rule_28_gb300 import workloads
     inp = workloads.make(5, T=512)
     _compare(_run(inp), _oracle(inp), TOL["bf16"])
+
+
+@pytest.mark.parametrize("use_exp2", [False, True])
+def test_backward_bf16_final_state_gradient(use_exp2):
+    """Tensor-core path with an upstream final-state gradient, a ragged last chunk and both bases."""
+    from gated_delta_rule_28_gb300 import workloads
+    inp = workloads.make(5, B=2, T=130, H=2, with_h0=True, with_dO=True)
+    inp.use_exp2 = use_exp2
+    dht = np.random.default_rng(7).standard_normal((2, 2, 128, 128)).astype(np.float32)
+    _compare(_run(inp, dht), _oracle(inp, dht), TOL["bf16"])
