@@ -19,6 +19,7 @@
 // [Q; K] Q^T and the gate), the three h-independent products scale A_qk^T dO,
 // scale Qg^T dO and w^T (= (beta base^G K)^T X^T), and the operands kgl and
 // w^T. X and the per-token gate factors come from the UT transform kernel.
+// Loads are TMA copies completing on mbarriers.
 // It writes dh of every chunk (the exit-state gradient) and dv_new in fp32
 // for the local-gradient kernel, and dh of the first chunk's entry as dh0.
 // Every mbarrier wait is bounded; a wait that runs out sets the device flag
@@ -68,6 +69,7 @@ struct BwState {
   float seg[2][64];                 // scale base^G
   float EL[2];
   uint64_t bar_p1, bar_p3, bar_d1, bar_d2, bar_x0, bar_x1;
+  uint64_t bar_ld[2], bar_do;  // TMA loads: order parity (Q, K, X, factors) and dO
   uint32_t tmem;
 };
 static_assert(sizeof(BwState) <= SMALL_BYTES, "small state");
@@ -82,8 +84,13 @@ __device__ __forceinline__ uint16_t bf16_bits(float x) {
   return *reinterpret_cast<const uint16_t *>(&b);
 }
 
+// TMA maps: q, k, dO over [rows, H*128] and X over [slots*H*64, 64], 64 x 64 boxes
+struct BwdMaps {
+  TmaMap q, k, dO, x;
+};
+
 template <bool E2>
-__global__ void __launch_bounds__(NTH, 1) tc_dhu_kernel(BwdArgs a) {
+__global__ void __launch_bounds__(NTH, 1) tc_dhu_kernel(BwdArgs a, const __grid_constant__ BwdMaps maps) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                             ~static_cast<uintptr_t>(1023));
@@ -144,6 +151,9 @@ __global__ void __launch_bounds__(NTH, 1) tc_dhu_kernel(BwdArgs a) {
     mbar_init(&st.bar_d2, 1);
     mbar_init(&st.bar_x0, 1);
     mbar_init(&st.bar_x1, 1);
+    mbar_init(&st.bar_ld[0], 1);
+    mbar_init(&st.bar_ld[1], 1);
+    mbar_init(&st.bar_do, 1);
     mbar_fence_init();
   }
   fence_before_sync();
@@ -157,45 +167,35 @@ __global__ void __launch_bounds__(NTH, 1) tc_dhu_kernel(BwdArgs a) {
     fence_after_sync();
   };
 
-  // ---- producer: loads -----------------------------------------------------------------
+  // ---- producer: loads (TMA, issued by one thread: ptid 32, warp 9 lane 0) --------------
+  // Rows past the run end are loaded as they are (the next run's tokens, or zeros past
+  // the tensor); the gating and the factor scale (scale base^G) are zeroed there, and
+  // beta = 0 removes them from w.
   const int ptid = tid - 256;
-  // copies are issued by producer warps 9..15 only: the MMA-issuing thread (ptid 0,
-  // warp 8) keeps no copies of its own in flight
-  const int ltid = ptid - 32;  // 0..223 on the copying warps
+  const bool loader = ptid == 32;
+  int64_t last_ld[2] = {-1, -1}, last_do = -1;  // loader: newest order index per barrier
   auto issue_qkx = [&](int64_t m) {  // Q, K, X and the gate table of order index m
     const int64_t c = chunk_of(m);
-    const uint32_t stg = sb + OFF_ST + (int)(m & 1) * SZ_STAGE;
-    const uint32_t xt = sb + ((m & 1) ? OFF_X1 : OFF_X0);
-    const int64_t c0 = r0 + c * GDN_CHUNK;
-    const int n = chunk_rows(c);
+    const int s2 = (int)(m & 1);
+    const uint32_t stg = sb + OFF_ST + s2 * SZ_STAGE;
+    const uint32_t xt = sb + (s2 ? OFF_X1 : OFF_X0);
+    const int y = (int)(r0 + c * GDN_CHUNK);
     const int64_t xs = (xbase + c) * H + h;
-    const __nv_bfloat16 *xsrc = a.xw + xs * (GDN_CHUNK * GDN_CHUNK);
-#pragma unroll
-    for (int x = ltid; x >= 0 && x < 2048 + 512; x += 224) {
-      if (x < 2048) {
-        const int which = x >> 10, r = (x >> 4) & 63, f16 = x & 15;  // which 0: Q rows 0..63, 1: K rows 64..127
-        const bool valid = r < n;
-        const __nv_bfloat16 *src = (which ? k : q) + ((c0 + (valid ? r : 0)) * H + h) * GDN_DK + f16 * 8;
-        cp_async16(stg + (f16 >> 3) * 16384 + chunk_off(r + which * 64, f16 & 7), src, valid ? 16u : 0u);
-      } else {
-        const int r = (x - 2048) >> 3, c8 = x & 7;
-        cp_async16(xt + chunk_off(r, c8), xsrc + r * GDN_CHUNK + c8 * 8, 16u);
-      }
-    }
-    if (ltid >= 0 && ltid < 80)
-      cp_async16(smem_u32(&st.tab[m & 1][0][0]) + ltid * 16, a.ftab + xs * 5 * GDN_CHUNK + ltid * 4, 16u);
+    uint64_t *bar = &st.bar_ld[s2];
+    mbar_expect_tx(bar, 5 * 8192 + 5 * GDN_CHUNK * 4);
+    tma_load_2d(stg, &maps.q, h * GDN_DK, y, bar);  // rows 0..63: Q
+    tma_load_2d(stg + 16384, &maps.q, h * GDN_DK + 64, y, bar);
+    tma_load_2d(stg + 8192, &maps.k, h * GDN_DK, y, bar);  // rows 64..127: K
+    tma_load_2d(stg + 16384 + 8192, &maps.k, h * GDN_DK + 64, y, bar);
+    tma_load_2d(xt, &maps.x, 0, (int)(xs * GDN_CHUNK), bar);
+    bulk_load(smem_u32(&st.tab[s2][0][0]), a.ftab + xs * 5 * GDN_CHUNK, 5 * GDN_CHUNK * 4, bar);
+    last_ld[s2] = m;
   };
   auto issue_do = [&](int64_t m) {  // the CTA's 64 columns of dO
     const int64_t c = chunk_of(m);
-    const int64_t c0 = r0 + c * GDN_CHUNK;
-    const int n = chunk_rows(c);
-#pragma unroll
-    for (int x = ltid; x >= 0 && x < 512; x += 224) {
-      const int r = x >> 3, c8 = x & 7;
-      const bool valid = r < n;
-      const __nv_bfloat16 *src = dO + ((c0 + (valid ? r : 0)) * H + h) * GDN_DV + col0 + c8 * 8;
-      cp_async16(sb + OFF_DO + chunk_off(r, c8), src, valid ? 16u : 0u);
-    }
+    mbar_expect_tx(&st.bar_do, 8192);
+    tma_load_2d(sb + OFF_DO, &maps.dO, h * GDN_DV + col0, (int)(r0 + c * GDN_CHUNK), &st.bar_do);
+    last_do = m;
   };
 
   // ---- producer: one chunk (order index pm) ------------------------------------------------
@@ -203,11 +203,9 @@ __global__ void __launch_bounds__(NTH, 1) tc_dhu_kernel(BwdArgs a) {
     const int ps = (int)(pm & 1);
     const uint32_t stg = sb + OFF_ST + ps * SZ_STAGE;
     const float(&tab)[5][64] = st.tab[ps];
-    if (pm + 1 < nch) issue_qkx(pm + 1);
-    cp_async_commit();
-    cp_async_wait<1>();  // Q, K, X, factors and dO of this chunk have landed
-    fence_proxy_async();
-    prod_sync();
+    const int n = chunk_rows(chunk_of(pm));
+    if (loader && pm + 1 < nch) issue_qkx(pm + 1);
+    wait_par(&st.bar_ld[ps], pm >> 1);  // Q, K, X and factors of this chunk have landed
     if (ptid == 0) {  // P1: [Q; K] Q^T (rows 64..127 = K Q^T)
       st.EL[ps] = tab[F_EG][63];
       fence_after_sync();
@@ -215,7 +213,7 @@ __global__ void __launch_bounds__(NTH, 1) tc_dhu_kernel(BwdArgs a) {
       mma_commit(&st.bar_p1);
     }
     __syncwarp();
-    if (ptid < 64) st.seg[ps][ptid] = scale * tab[F_EG][ptid];
+    if (ptid < 64) st.seg[ps][ptid] = ptid < n ? scale * tab[F_EG][ptid] : 0.f;
     prod_sync();
     // transposes: K (rows 64..127) -> (beta base^G K)^T; Q -> (scale base^G Q)^T; dO -> dO^T
     {
@@ -228,6 +226,7 @@ __global__ void __launch_bounds__(NTH, 1) tc_dhu_kernel(BwdArgs a) {
         trans16_load(stg + (fb >> 2) * 16384, rb * 16, (fb & 3) * 2, lane, xq[i]);
       }
 #pragma unroll
+      wait_par(&st.bar_do, pm);  // dO of this chunk
       for (int i = 0; i < 2; ++i) {
         const int t = pw + 8 * i, rb = t >> 2, cb = t & 3;
         trans16_load(sb + OFF_DO, rb * 16, cb * 2, lane, xd[i]);
@@ -245,9 +244,7 @@ __global__ void __launch_bounds__(NTH, 1) tc_dhu_kernel(BwdArgs a) {
         trans16_store(sb + OFF_QGT, fb * 16, rb * 16, xq[i], st.seg[ps], lane);
       }
     }
-    prod_sync();  // dO consumed: load the next chunk's
-    if (pm + 1 < nch) issue_do(pm + 1);
-    cp_async_commit();
+    prod_sync();  // dO consumed (the next chunk's is loaded after the product issue)
     // gating of K Q^T (rows 64..127 of S): A_qk^T[s][t] = scale (k_s . q_t) base^(G_t - G_s), t >= s
     wait_par(&st.bar_p1, pm);
     if (q4 >= 2) {
@@ -260,7 +257,7 @@ __global__ void __launch_bounds__(NTH, 1) tc_dhu_kernel(BwdArgs a) {
 #pragma unroll
       for (int j = 0; j < 32; ++j) {
         const int t = 32 * hc + j;
-        sv[j] = t >= s ? scale * sv[j] * gexp<E2>(tab[F_G][t] - Gs) : 0.f;
+        sv[j] = t >= s && t < n ? scale * sv[j] * gexp<E2>(tab[F_G][t] - Gs) : 0.f;
       }
       uint8_t *dst = sm + OFF_AQT;
 #pragma unroll
@@ -282,6 +279,7 @@ __global__ void __launch_bounds__(NTH, 1) tc_dhu_kernel(BwdArgs a) {
       mma_commit(&st.bar_p3);
     }
     __syncwarp();
+    if (loader && pm + 1 < nch) issue_do(pm + 1);  // dO consumed by the transposes
     // kgl rows (K rows scaled by base^(G_last - G)) once the chain's D1 has read the previous ones
     if (m_chain >= 0) wait_par(&st.bar_d1, m_chain);
     if (q4 >= 2) {
@@ -399,11 +397,9 @@ __global__ void __launch_bounds__(NTH, 1) tc_dhu_kernel(BwdArgs a) {
   };
 
   // ---- prologue and rounds ------------------------------------------------------------------
-  if (producer && nch > 0) {
+  if (loader && nch > 0) {
     issue_qkx(0);
-    cp_async_commit();
     issue_do(0);
-    cp_async_commit();
   }
   if (!producer) {
     write_dht();
@@ -431,7 +427,11 @@ __global__ void __launch_bounds__(NTH, 1) tc_dhu_kernel(BwdArgs a) {
     if (tid == 256) mma_commit(&st.bar_x1);
     if (tid == 0) mbar_wait(&st.bar_x0, 0, WAIT_LIMIT);
     if (tid == 256) mbar_wait(&st.bar_x1, 0, WAIT_LIMIT);
-    cp_async_wait<0>();
+    if (loader) {  // copies still in flight land before the CTA leaves
+      for (int s2 = 0; s2 < 2; ++s2)
+        if (last_ld[s2] >= 0) mbar_wait(&st.bar_ld[s2], (uint32_t)((last_ld[s2] >> 1) & 1), WAIT_LIMIT);
+      if (last_do >= 0) mbar_wait(&st.bar_do, (uint32_t)(last_do & 1), WAIT_LIMIT);
+    }
   } else if (!producer && a.dh0) {
     float4 *dst = reinterpret_cast<float4 *>(a.dh0 + ((int64_t)state_idx * H + h) * GDN_DK * GDN_DV +
                                              (int64_t)row * GDN_DV + col0 + 32 * hc);
@@ -446,10 +446,19 @@ __global__ void __launch_bounds__(NTH, 1) tc_dhu_kernel(BwdArgs a) {
 }  // namespace
 
 cudaError_t launch_tc_dhu(const BwdArgs &a, int runs, cudaStream_t st) {
-  auto kern = a.use_exp2 ? tc_dhu_kernel<true> : tc_dhu_kernel<false>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+  const uint64_t rows = a.cu ? (uint64_t)a.T : (uint64_t)a.B * a.T;
+  const uint64_t slots = a.cu ? (uint64_t)a.num_chunks : (uint64_t)a.B * ((a.T + GDN_CHUNK - 1) / GDN_CHUNK);
+  const uint64_t pitch = (uint64_t)a.H * GDN_DK * 2;
+  BwdMaps maps;
+  cudaError_t e = make_tmap_bf16(&maps.q, a.q, (uint64_t)a.H * GDN_DK, rows, pitch);
+  if (e == cudaSuccess) e = make_tmap_bf16(&maps.k, a.k, (uint64_t)a.H * GDN_DK, rows, pitch);
+  if (e == cudaSuccess) e = make_tmap_bf16(&maps.dO, a.dO, (uint64_t)a.H * GDN_DV, rows, (uint64_t)a.H * GDN_DV * 2);
+  if (e == cudaSuccess) e = make_tmap_bf16(&maps.x, a.xw, GDN_CHUNK, slots * a.H * GDN_CHUNK, GDN_CHUNK * 2);
   if (e != cudaSuccess) return e;
-  kern<<<dim3(GDN_DV / TBV, a.H, runs), NTH, SMEM_BYTES, st>>>(a);
+  auto kern = a.use_exp2 ? tc_dhu_kernel<true> : tc_dhu_kernel<false>;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  kern<<<dim3(GDN_DV / TBV, a.H, runs), NTH, SMEM_BYTES, st>>>(a, maps);
   return cudaGetLastError();
 }
 

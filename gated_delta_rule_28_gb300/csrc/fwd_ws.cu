@@ -17,12 +17,16 @@
 //
 // The two warp groups meet once per chunk (a CTA barrier); inside a chunk the
 // producer waits for P4 of the chain before it overwrites the P4 operand.
+// Loads are TMA copies (tensor tiles with the 128-byte swizzle, and one bulk copy
+// of the chunk's gate factors) completing on mbarriers.
 // Operands are K-major tiles with the 128-byte swizzle; the state-side
 // transposes (v_new^T, h^T) are written column-wise straight from the tensor
 // memory loads, the key and value transposes of the producer with
 // ldmatrix.trans / stmatrix. Every mbarrier wait is bounded; a wait that runs
 // out sets the device flag and the CTA drains its MMAs, frees its tensor
 // memory and leaves.
+#include <string.h>
+
 #include "common.cuh"
 #include "kernels.h"
 #include "tc.cuh"
@@ -71,6 +75,7 @@ struct WsState {
   alignas(16) float tab[2][5][64];  // refilled with chunk c+2 while the chain runs chunk c
   float EL[2];                      // base^(G_last) per chunk parity, for the chain
   uint64_t bar_p1, bar_p3, bar_p4, bar_p5, bar_po, bar_d0, bar_d1;
+  uint64_t bar_ld[2], bar_v;  // TMA loads: stage parity (K, Q, X, factors) and V
   uint32_t tmem;
 };
 static_assert(sizeof(WsState) <= SMALL_BYTES, "small state");
@@ -85,8 +90,13 @@ __device__ __forceinline__ uint16_t bf16_bits(float x) {
   return *reinterpret_cast<const uint16_t *>(&b);
 }
 
+// TMA maps: q, k, v over [rows, H*128] and X over [slots*H*64, 64], 64 x 64 boxes
+struct FwdMaps {
+  TmaMap q, k, v, x;
+};
+
 template <bool E2>
-__global__ void __launch_bounds__(NTH, 1) tc_fwd_ws_kernel(SimtFwdArgs a) {
+__global__ void __launch_bounds__(NTH, 1) tc_fwd_ws_kernel(SimtFwdArgs a, const __grid_constant__ FwdMaps maps) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                             ~static_cast<uintptr_t>(1023));
@@ -158,6 +168,9 @@ __global__ void __launch_bounds__(NTH, 1) tc_fwd_ws_kernel(SimtFwdArgs a) {
     mbar_init(&st.bar_po, 1);
     mbar_init(&st.bar_d0, 1);
     mbar_init(&st.bar_d1, 1);
+    mbar_init(&st.bar_ld[0], 1);
+    mbar_init(&st.bar_ld[1], 1);
+    mbar_init(&st.bar_v, 1);
     mbar_fence_init();
   }
   fence_before_sync();
@@ -171,43 +184,32 @@ __global__ void __launch_bounds__(NTH, 1) tc_fwd_ws_kernel(SimtFwdArgs a) {
     fence_after_sync();
   };
 
-  // ---- producer: loads -----------------------------------------------------------------
+  // ---- producer: loads (TMA, issued by one thread: ptid 32, warp 9 lane 0) --------------
+  // Rows past the run end are loaded as they are (the next run's tokens, or zeros past
+  // the tensor): they only meet beta = 0, a causal mask, or rows of o that are not stored.
   const int ptid = tid - 256;
-  // copies are issued by producer warps 9..15 only: the MMA-issuing thread (ptid 0,
-  // warp 8) keeps no copies of its own in flight
-  const int ltid = ptid - 32;  // 0..223 on the copying warps
+  const bool loader = ptid == 32;
+  int64_t last_ld[2] = {-1, -1}, last_v = -1;  // loader: newest chunk per barrier
   auto issue_kqx = [&](int64_t c) {  // K, Q, X and the gate factors of chunk c (buffers of parity c&1)
-    const uint32_t stg = sb + OFF_ST + (int)(c & 1) * SZ_STAGE;
-    const uint32_t xt = sb + ((c & 1) ? OFF_X1 : OFF_X0);
-    const int64_t c0 = r0 + c * GDN_CHUNK;
-    const int n = chunk_rows(c);
+    const int s2 = (int)(c & 1);
+    const uint32_t stg = sb + OFF_ST + s2 * SZ_STAGE;
+    const uint32_t xt = sb + (s2 ? OFF_X1 : OFF_X0);
+    const int y = (int)(r0 + c * GDN_CHUNK);
     const int64_t xs = (xbase + c) * H + h;
-    const __nv_bfloat16 *xsrc = xw + xs * (GDN_CHUNK * GDN_CHUNK);
-#pragma unroll
-    for (int x = ltid; x >= 0 && x < 2048 + 512; x += 224) {
-      if (x < 2048) {
-        const int which = x >> 10, r = (x >> 4) & 63, f16 = x & 15;
-        const bool valid = r < n;
-        const __nv_bfloat16 *src = (which ? q : k) + ((c0 + (valid ? r : 0)) * H + h) * GDN_DK + f16 * 8;
-        cp_async16(stg + (f16 >> 3) * 16384 + chunk_off(r + which * 64, f16 & 7), src, valid ? 16u : 0u);
-      } else {
-        const int r = (x - 2048) >> 3, c8 = x & 7;
-        cp_async16(xt + chunk_off(r, c8), xsrc + r * GDN_CHUNK + c8 * 8, 16u);
-      }
-    }
-    if (ltid >= 0 && ltid < 80)
-      cp_async16(smem_u32(&st.tab[c & 1][0][0]) + ltid * 16, a.ftab + xs * 5 * GDN_CHUNK + ltid * 4, 16u);
+    uint64_t *bar = &st.bar_ld[s2];
+    mbar_expect_tx(bar, 5 * 8192 + 5 * GDN_CHUNK * 4);
+    tma_load_2d(stg, &maps.k, h * GDN_DK, y, bar);
+    tma_load_2d(stg + 16384, &maps.k, h * GDN_DK + 64, y, bar);
+    tma_load_2d(stg + 8192, &maps.q, h * GDN_DK, y, bar);
+    tma_load_2d(stg + 16384 + 8192, &maps.q, h * GDN_DK + 64, y, bar);
+    tma_load_2d(xt, &maps.x, 0, (int)(xs * GDN_CHUNK), bar);
+    bulk_load(smem_u32(&st.tab[s2][0][0]), a.ftab + xs * 5 * GDN_CHUNK, 5 * GDN_CHUNK * 4, bar);
+    last_ld[s2] = c;
   };
   auto issue_v = [&](int64_t c) {  // the CTA's 64 columns of V of chunk c
-    const int64_t c0 = r0 + c * GDN_CHUNK;
-    const int n = chunk_rows(c);
-#pragma unroll
-    for (int x = ltid; x >= 0 && x < 512; x += 224) {
-      const int r = x >> 3, c8 = x & 7;
-      const bool valid = r < n;
-      const __nv_bfloat16 *src = v + ((c0 + (valid ? r : 0)) * H + h) * GDN_DV + col0 + c8 * 8;
-      cp_async16(sb + OFF_V + chunk_off(r, c8), src, valid ? 16u : 0u);
-    }
+    mbar_expect_tx(&st.bar_v, 8192);
+    tma_load_2d(sb + OFF_V, &maps.v, h * GDN_DV + col0, (int)(r0 + c * GDN_CHUNK), &st.bar_v);
+    last_v = c;
   };
 
   // ---- producer: one chunk -------------------------------------------------------------
@@ -215,12 +217,9 @@ __global__ void __launch_bounds__(NTH, 1) tc_fwd_ws_kernel(SimtFwdArgs a) {
     const int ps = (int)(pc & 1);
     const uint32_t stg = sb + OFF_ST + ps * SZ_STAGE;
     const float(&tab)[5][64] = st.tab[ps];
-    // stage of chunk pc+1 (it held chunk pc-1, finished in the previous round)
-    if (pc + 1 < nch) issue_kqx(pc + 1);
-    cp_async_commit();
-    cp_async_wait<1>();  // K, Q, X, factors and V of chunk pc have landed
-    fence_proxy_async();
-    prod_sync();
+    // buffers of chunk pc+1 (they held chunk pc-1, finished in the previous round)
+    if (loader && pc + 1 < nch) issue_kqx(pc + 1);
+    wait_par(&st.bar_ld[ps], pc >> 1);  // K, Q, X and factors of chunk pc have landed
     if (ptid == 0) {  // P1: S = [K; Q] K^T
       st.EL[ps] = tab[F_EG][63];
       fence_after_sync();
@@ -238,6 +237,7 @@ __global__ void __launch_bounds__(NTH, 1) tc_fwd_ws_kernel(SimtFwdArgs a) {
         trans16_load(stg + (fb >> 2) * 16384, rb * 16, (fb & 3) * 2, lane, xk[i]);
       }
 #pragma unroll
+      wait_par(&st.bar_v, pc);  // V of chunk pc
       for (int i = 0; i < 2; ++i) {
         const int t = pw + 8 * i, rb = t >> 2, cb = t & 3;
         trans16_load(sb + OFF_V, rb * 16, cb * 2, lane, xv[i]);
@@ -254,9 +254,7 @@ __global__ void __launch_bounds__(NTH, 1) tc_fwd_ws_kernel(SimtFwdArgs a) {
         trans16_store(sb + OFF_KL + ps * 16384, fb * 16, rb * 16, xk[i], tab[F_EGL], lane);
       }
     }
-    prod_sync();  // V consumed: load the next chunk's
-    if (pc + 1 < nch) issue_v(pc + 1);
-    cp_async_commit();
+    prod_sync();  // V consumed (the next chunk's is loaded after the P3b issue)
     // gating of Q K^T (rows 64..127 of S) -> A_qk, lower triangle including the diagonal
     wait_par(&st.bar_p1, pc);
     if (q4 >= 2) {
@@ -287,6 +285,7 @@ __global__ void __launch_bounds__(NTH, 1) tc_fwd_ws_kernel(SimtFwdArgs a) {
       mma_commit(&st.bar_p3);
     }
     __syncwarp();  // the issuing warp reconverges before any of its lanes polls a barrier
+    if (loader && pc + 1 < nch) issue_v(pc + 1);  // V consumed by the transposes
     // operand of P4: rows 64..127 = e^G Q once the chain's P4 has read the previous one,
     // rows 0..63 = w once P3b is done (keys 64*hc .. +64 per thread)
     uint8_t *wq = sm + OFF_WQ + hc * 16384;
@@ -419,11 +418,9 @@ __global__ void __launch_bounds__(NTH, 1) tc_fwd_ws_kernel(SimtFwdArgs a) {
   };
 
   // ---- prologue --------------------------------------------------------------------------
-  if (producer && nch > 0) {
+  if (loader && nch > 0) {
     issue_kqx(0);
-    cp_async_commit();
     issue_v(0);
-    cp_async_commit();
   }
   if (!producer) {
     write_ht();
@@ -452,7 +449,11 @@ __global__ void __launch_bounds__(NTH, 1) tc_fwd_ws_kernel(SimtFwdArgs a) {
     if (tid == 256) mma_commit(&st.bar_d1);
     if (tid == 0) mbar_wait(&st.bar_d0, 0, WAIT_LIMIT);
     if (tid == 256) mbar_wait(&st.bar_d1, 0, WAIT_LIMIT);
-    cp_async_wait<0>();
+    if (loader) {  // copies still in flight land before the CTA leaves
+      for (int s2 = 0; s2 < 2; ++s2)
+        if (last_ld[s2] >= 0) mbar_wait(&st.bar_ld[s2], (uint32_t)((last_ld[s2] >> 1) & 1), WAIT_LIMIT);
+      if (last_v >= 0) mbar_wait(&st.bar_v, (uint32_t)(last_v & 1), WAIT_LIMIT);
+    }
   } else if (!producer && a.ht && (a.nseg == 0 || s == a.nseg - 1)) {
     float4 *dst = reinterpret_cast<float4 *>(a.ht + ((int64_t)state_idx * H + h) * GDN_DK * GDN_DV +
                                              (int64_t)row * GDN_DV + col0 + 32 * hc);
@@ -470,10 +471,23 @@ __global__ void __launch_bounds__(NTH, 1) tc_fwd_ws_kernel(SimtFwdArgs a) {
 int tc_fwd_ws_bv() { return TBV; }
 
 cudaError_t launch_tc_fwd_ws(const SimtFwdArgs &a, dim3 grid, cudaStream_t st) {
-  auto kern = a.use_exp2 ? tc_fwd_ws_kernel<true> : tc_fwd_ws_kernel<false>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+  const uint64_t rows = a.cu ? (uint64_t)a.T : (uint64_t)a.B * a.T;
+  const uint64_t slots = a.cu ? (uint64_t)a.num_chunks : (uint64_t)a.B * ((a.T + GDN_CHUNK - 1) / GDN_CHUNK);
+  const uint64_t pitch = (uint64_t)a.H * GDN_DK * 2;
+  FwdMaps maps;
+  memset(&maps, 0, sizeof(maps));
+  cudaError_t e = cudaSuccess;
+  if (rows > 0) {  // an empty sequence loads nothing (the kernel only writes ht = h0)
+    e = make_tmap_bf16(&maps.q, a.q, (uint64_t)a.H * GDN_DK, rows, pitch);
+    if (e == cudaSuccess) e = make_tmap_bf16(&maps.k, a.k, (uint64_t)a.H * GDN_DK, rows, pitch);
+    if (e == cudaSuccess) e = make_tmap_bf16(&maps.v, a.v, (uint64_t)a.H * GDN_DV, rows, (uint64_t)a.H * GDN_DV * 2);
+    if (e == cudaSuccess) e = make_tmap_bf16(&maps.x, a.xw, GDN_CHUNK, slots * a.H * GDN_CHUNK, GDN_CHUNK * 2);
+  }
   if (e != cudaSuccess) return e;
-  kern<<<grid, NTH, SMEM_BYTES, st>>>(a);
+  auto kern = a.use_exp2 ? tc_fwd_ws_kernel<true> : tc_fwd_ws_kernel<false>;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  kern<<<grid, NTH, SMEM_BYTES, st>>>(a, maps);
   return cudaGetLastError();
 }
 

@@ -10,6 +10,14 @@
 
 namespace gdn {
 
+// Opaque storage of a TMA tensor map (the driver's CUtensorMap: 128 bytes, 64-byte aligned).
+struct alignas(64) TmaMap {
+  unsigned char bytes[128];
+};
+// Map over a row-major bf16 matrix [rows][cols] (row pitch row_bytes) read in
+// 64 x 64 boxes with the 128-byte swizzle; zero fill outside the matrix.
+cudaError_t make_tmap_bf16(TmaMap *map, const void *base, uint64_t cols, uint64_t rows, uint64_t row_bytes);
+
 // Arguments of the fp32 SIMT chunk kernel (forward, correction run, segment
 // summary and the backward's state recompute share it).
 struct SimtFwdArgs {

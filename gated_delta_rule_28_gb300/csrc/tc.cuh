@@ -152,5 +152,28 @@ __device__ __forceinline__ void mma_tiles(uint32_t d_tmem, uint32_t a_saddr, uin
   }
 }
 
+// ---------------------------------------------------------------------------
+// TMA: tensor tiles and plain bulk copies into shared memory, completing on an
+// mbarrier that the issuing thread armed with the expected byte count
+__device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+               : "memory");
+}
+// box of a 2-D tensor map at element coordinates (x = innermost, y); x * 2 bytes
+// must be a multiple of 16 (every caller passes a multiple of 64 elements)
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const void *map, int x, int y, uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+          dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+// contiguous copy; both addresses 16-byte aligned, bytes a multiple of 16
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes, uint64_t *bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "l"(src), "r"(bytes), "r"(smem_u32(bar))
+               : "memory");
+}
+
 }  // namespace tc
 }  // namespace gdn
