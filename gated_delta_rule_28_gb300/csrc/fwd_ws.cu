@@ -7,7 +7,7 @@
 // (north star; GDN Ascend C adapter forward, chunk_fwd_h and the output step):
 //
 //   producer warps 8..15, chunk c+1 (no dependence on the state):
-//     P1   S = [K; Q] K^T                      -> A_qk = lower-incl(Q K^T (.) Gamma)
+//     P1   S = [Q; K] K^T                      -> A_qk = lower-incl(Q K^T (.) Gamma)
 //     P3b  X [b e^G K | b V]                   -> w = X diag(b e^G) K,  u = X diag(b) V
 //          operand [w; e^G Q] for P4
 //   chain warps 0..7, chunk c (the state h lives in their registers, fp32):
@@ -40,7 +40,7 @@ using namespace tile;
 constexpr int TBV = 64;   // state columns per CTA
 constexpr int NTH = 512;  // threads per CTA: 256 chain + 256 producer
 constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t T_S = 0;     // 2 x 64: P1 per chunk parity (rows 64..127 = Q K^T)
+constexpr uint32_t T_S = 0;     // 2 x 64: P1 per chunk parity (rows 0..63 = Q K^T)
 constexpr uint32_t T_WW = 128;  // 128: P3b rows 0..63 = w
 constexpr uint32_t T_U = 256;   // 2 x 64: P3b rows 0..63 = u, per chunk parity
 constexpr uint32_t T_D4 = 384;  // 64: P4 rows 0..63 = w h, rows 64..127 = q' h (+ A_qk v_new)
@@ -50,7 +50,7 @@ constexpr uint32_t T_P5 = 448;  // 64: P5
 // The P3b operand is a 128-row tile whose rows 64..127 are not used: each X tile
 // is placed in front of a buffer that no copy writes while P3b runs (B3, KL),
 // and the A_qk tiles behind v_new^T for the same reason.
-constexpr int SZ_STAGE = 32768;                // [K; Q]: 2 K-blocks x 128 rows
+constexpr int SZ_STAGE = 32768;                // [Q; K]: 2 K-blocks x 128 rows
 constexpr int OFF_ST = 0;                      // 2 stages
 constexpr int OFF_V = OFF_ST + 2 * SZ_STAGE;   // V slice, 64 rows (one buffer)
 constexpr int OFF_X0 = OFF_V + 8192;           // X of even chunks              64 rows
@@ -198,10 +198,10 @@ __global__ void __launch_bounds__(NTH, 1) tc_fwd_ws_kernel(SimtFwdArgs a, const 
     const int64_t xs = (xbase + c) * H + h;
     uint64_t *bar = &st.bar_ld[s2];
     mbar_expect_tx(bar, 5 * 8192 + 5 * GDN_CHUNK * 4);
-    tma_load_2d(stg, &maps.k, h * GDN_DK, y, bar);
-    tma_load_2d(stg + 16384, &maps.k, h * GDN_DK + 64, y, bar);
-    tma_load_2d(stg + 8192, &maps.q, h * GDN_DK, y, bar);
-    tma_load_2d(stg + 16384 + 8192, &maps.q, h * GDN_DK + 64, y, bar);
+    tma_load_2d(stg, &maps.q, h * GDN_DK, y, bar);  // rows 0..63: Q
+    tma_load_2d(stg + 16384, &maps.q, h * GDN_DK + 64, y, bar);
+    tma_load_2d(stg + 8192, &maps.k, h * GDN_DK, y, bar);  // rows 64..127: K
+    tma_load_2d(stg + 16384 + 8192, &maps.k, h * GDN_DK + 64, y, bar);
     tma_load_2d(xt, &maps.x, 0, (int)(xs * GDN_CHUNK), bar);
     bulk_load(smem_u32(&st.tab[s2][0][0]), a.ftab + xs * 5 * GDN_CHUNK, 5 * GDN_CHUNK * 4, bar);
     last_ld[s2] = c;
@@ -220,10 +220,10 @@ __global__ void __launch_bounds__(NTH, 1) tc_fwd_ws_kernel(SimtFwdArgs a, const 
     // buffers of chunk pc+1 (they held chunk pc-1, finished in the previous round)
     if (loader && pc + 1 < nch) issue_kqx(pc + 1);
     wait_par(&st.bar_ld[ps], pc >> 1);  // K, Q, X and factors of chunk pc have landed
-    if (ptid == 0) {  // P1: S = [K; Q] K^T
+    if (ptid == 0) {  // P1: S = [Q; K] K^T (rows 0..63 = Q K^T)
       st.EL[ps] = tab[F_EG][63];
       fence_after_sync();
-      mma_tiles(tmem + T_S + 64 * ps, stg, 16384, stg, 16384, 128, idesc_bf16(128, 64), false);
+      mma_tiles(tmem + T_S + 64 * ps, stg, 16384, stg + 8192, 16384, 128, idesc_bf16(128, 64), false);
       mma_commit(&st.bar_p1);
     }
     __syncwarp();  // the issuing warp reconverges before any of its lanes polls a barrier
@@ -234,10 +234,10 @@ __global__ void __launch_bounds__(NTH, 1) tc_fwd_ws_kernel(SimtFwdArgs a, const 
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const int jb = pw + 8 * i, rb = jb >> 3, fb = jb & 7;
-        trans16_load(stg + (fb >> 2) * 16384, rb * 16, (fb & 3) * 2, lane, xk[i]);
+        trans16_load(stg + (fb >> 2) * 16384, 64 + rb * 16, (fb & 3) * 2, lane, xk[i]);  // K rows
       }
-#pragma unroll
       wait_par(&st.bar_v, pc);  // V of chunk pc
+#pragma unroll
       for (int i = 0; i < 2; ++i) {
         const int t = pw + 8 * i, rb = t >> 2, cb = t & 3;
         trans16_load(sb + OFF_V, rb * 16, cb * 2, lane, xv[i]);
@@ -255,10 +255,10 @@ __global__ void __launch_bounds__(NTH, 1) tc_fwd_ws_kernel(SimtFwdArgs a, const 
       }
     }
     prod_sync();  // V consumed (the next chunk's is loaded after the P3b issue)
-    // gating of Q K^T (rows 64..127 of S) -> A_qk, lower triangle including the diagonal
+    // gating of Q K^T (rows 0..63 of S) -> A_qk, lower triangle including the diagonal
     wait_par(&st.bar_p1, pc);
-    if (q4 >= 2) {
-      const int t = row - 64;
+    if (q4 < 2) {
+      const int t = row;
       float sv[32];
       tmem_ld16(tl + T_S + 64 * ps + 32 * hc, *reinterpret_cast<float(*)[16]>(sv));
       tmem_ld16(tl + T_S + 64 * ps + 32 * hc + 16, *reinterpret_cast<float(*)[16]>(sv + 16));
@@ -292,11 +292,11 @@ __global__ void __launch_bounds__(NTH, 1) tc_fwd_ws_kernel(SimtFwdArgs a, const 
     if (c_chain >= 0) wait_par(&st.bar_p4, c_chain);
     if (q4 >= 2) {
       const float eg = tab[F_EG][row - 64];
-      const uint8_t *qrow = sm + OFF_ST + ps * SZ_STAGE + hc * 16384;
+      const uint8_t *qrow = sm + OFF_ST + ps * SZ_STAGE + hc * 16384;  // Q: stage rows 0..63
 #pragma unroll
       for (int c8 = 0; c8 < 8; ++c8) {
         float f[8];
-        unpack8(*reinterpret_cast<const uint4 *>(qrow + chunk_off(row, c8)), f);
+        unpack8(*reinterpret_cast<const uint4 *>(qrow + chunk_off(row - 64, c8)), f);
 #pragma unroll
         for (int e = 0; e < 8; ++e) f[e] *= eg;
         *reinterpret_cast<uint4 *>(wq + chunk_off(row, c8)) = pack8(f);
