@@ -57,15 +57,18 @@ constexpr int OFF_WT = OFF_KGL + 16384;       // w^T, 128 rows
 constexpr int OFF_DHT = OFF_WT + 16384;       // dh^T, 2 K-blocks x 64 rows
 constexpr int OFF_DVT = OFF_DHT + 16384;      // dv_new^T, 64 rows
 constexpr int OFF_SMALL = OFF_DVT + 8192;
-constexpr int SMALL_BYTES = 4096;
-constexpr int SMEM_BYTES = OFF_SMALL + SMALL_BYTES + 1024;
+constexpr int SMALL_BYTES = 6144;
+// gates of the four diagonal 16x16 blocks, gdn[b][x][y] = base^(G_{16b+x} - G_{16b+y}) for
+// x >= y (else 0) at b * GD_B + x * 16 + y; block stride 272 against bank conflicts
+constexpr int GD_B = 272;
+constexpr int OFF_GD = OFF_SMALL + SMALL_BYTES;
+constexpr int SMEM_BYTES = OFF_GD + 4 * GD_B * 4 + 1024;
 static_assert(SMEM_BYTES <= 232448, "shared memory");
 
 constexpr uint32_t WAIT_LIMIT = 1u << 22;
 
-enum { F_G = 0, F_EG = 1, F_EGL = 2, F_BEG = 3, F_BETA = 4 };
 struct BwState {
-  alignas(16) float tab[2][5][64];  // gate factor table per order parity
+  alignas(16) float tab[2][F_ROWS][64];  // gate factor table per order parity
   float seg[2][64];                 // scale base^G
   float EL[2];
   uint64_t bar_p1, bar_p3, bar_d1, bar_d2, bar_x0, bar_x1;
@@ -92,8 +95,9 @@ struct BwdMaps {
 template <bool E2>
 __global__ void __launch_bounds__(NTH, 1) tc_dhu_kernel(BwdArgs a, const __grid_constant__ BwdMaps maps) {
   extern __shared__ uint8_t smem_raw[];
-  uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                            ~static_cast<uintptr_t>(1023));
+  // 1024-aligned base by pointer arithmetic on the shared array, so that the compiler keeps
+  // the shared address space (shared-memory instructions, not generic ones)
+  uint8_t *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   BwState &st = *reinterpret_cast<BwState *>(sm + OFF_SMALL);
   const uint32_t sb = smem_u32(sm);
 
@@ -182,13 +186,13 @@ __global__ void __launch_bounds__(NTH, 1) tc_dhu_kernel(BwdArgs a, const __grid_
     const int y = (int)(r0 + c * GDN_CHUNK);
     const int64_t xs = (xbase + c) * H + h;
     uint64_t *bar = &st.bar_ld[s2];
-    mbar_expect_tx(bar, 5 * 8192 + 5 * GDN_CHUNK * 4);
+    mbar_expect_tx(bar, 5 * 8192 + F_ROWS * GDN_CHUNK * 4);
     tma_load_2d(stg, &maps.q, h * GDN_DK, y, bar);  // rows 0..63: Q
     tma_load_2d(stg + 16384, &maps.q, h * GDN_DK + 64, y, bar);
     tma_load_2d(stg + 8192, &maps.k, h * GDN_DK, y, bar);  // rows 64..127: K
     tma_load_2d(stg + 16384 + 8192, &maps.k, h * GDN_DK + 64, y, bar);
     tma_load_2d(xt, &maps.x, 0, (int)(xs * GDN_CHUNK), bar);
-    bulk_load(smem_u32(&st.tab[s2][0][0]), a.ftab + xs * 5 * GDN_CHUNK, 5 * GDN_CHUNK * 4, bar);
+    bulk_load(smem_u32(&st.tab[s2][0][0]), a.ftab + xs * F_ROWS * GDN_CHUNK, F_ROWS * GDN_CHUNK * 4, bar);
     last_ld[s2] = m;
   };
   auto issue_do = [&](int64_t m) {  // the CTA's 64 columns of dO
@@ -202,7 +206,7 @@ __global__ void __launch_bounds__(NTH, 1) tc_dhu_kernel(BwdArgs a, const __grid_
   auto produce = [&](int64_t pm, int64_t m_chain) {
     const int ps = (int)(pm & 1);
     const uint32_t stg = sb + OFF_ST + ps * SZ_STAGE;
-    const float(&tab)[5][64] = st.tab[ps];
+    const float(&tab)[F_ROWS][64] = st.tab[ps];
     const int n = chunk_rows(chunk_of(pm));
     if (loader && pm + 1 < nch) issue_qkx(pm + 1);
     wait_par(&st.bar_ld[ps], pm >> 1);  // Q, K, X and factors of this chunk have landed
@@ -215,6 +219,14 @@ __global__ void __launch_bounds__(NTH, 1) tc_dhu_kernel(BwdArgs a, const __grid_
     __syncwarp();
     if (ptid < 64) st.seg[ps][ptid] = ptid < n ? scale * tab[F_EG][ptid] : 0.f;
     prod_sync();
+    {  // diagonal-block gate table, spread over all producer threads (read after the next barrier)
+      float *gdn = reinterpret_cast<float *>(sm + OFF_GD);
+      for (int e = ptid; e < 1024; e += 256) {
+        const int b = e >> 8, x = (e >> 4) & 15, y = e & 15;
+        const float v = gexp<E2>(tab[F_G][16 * b + x] - tab[F_G][16 * b + y]);
+        gdn[b * GD_B + x * 16 + y] = x >= y ? v : 0.f;
+      }
+    }
     // transposes: K (rows 64..127) -> (beta base^G K)^T; Q -> (scale base^G Q)^T; dO -> dO^T
     {
       const int pw = warp - 8;
@@ -245,7 +257,20 @@ __global__ void __launch_bounds__(NTH, 1) tc_dhu_kernel(BwdArgs a, const __grid_
       }
     }
     prod_sync();  // dO consumed (the next chunk's is loaded after the product issue)
-    // gating of K Q^T (rows 64..127 of S): A_qk^T[s][t] = scale (k_s . q_t) base^(G_t - G_s), t >= s
+    // gating of K Q^T (rows 64..127 of S): A_qk^T[s][t] = scale (k_s . q_t) base^(G_t - G_s),
+    // s <= t < n; gate factors from tables as in the forward, formed while P1 may still run.
+    float gf[32];
+    if (q4 >= 2) {
+      const int s = row - 64, bs = s >> 4;
+      const float *gd = reinterpret_cast<const float *>(sm + OFF_GD) + bs * GD_B + (s & 15);
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        const int t = 32 * hc + j, bt = t >> 4;
+        const float off = tab[F_EA][t] * tab[F_EB1 + (bt > 0 ? bt - 1 : 0)][s], dg = gd[(t & 15) * 16];
+        const float f = bt > bs ? off : (bt == bs ? dg : 0.f);
+        gf[j] = t < n ? scale * f : 0.f;
+      }
+    }
     wait_par(&st.bar_p1, pm);
     if (q4 >= 2) {
       const int s = row - 64;
@@ -253,12 +278,8 @@ __global__ void __launch_bounds__(NTH, 1) tc_dhu_kernel(BwdArgs a, const __grid_
       tmem_ld16(tl + T_S + 64 * ps + 32 * hc, *reinterpret_cast<float(*)[16]>(sv));
       tmem_ld16(tl + T_S + 64 * ps + 32 * hc + 16, *reinterpret_cast<float(*)[16]>(sv + 16));
       tmem_ld_wait();
-      const float Gs = tab[F_G][s];
 #pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        const int t = 32 * hc + j;
-        sv[j] = t >= s && t < n ? scale * sv[j] * gexp<E2>(tab[F_G][t] - Gs) : 0.f;
-      }
+      for (int j = 0; j < 32; ++j) sv[j] *= gf[j];
       uint8_t *dst = sm + OFF_AQT;
 #pragma unroll
       for (int q8 = 0; q8 < 4; ++q8)

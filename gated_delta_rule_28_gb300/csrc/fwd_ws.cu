@@ -62,17 +62,19 @@ constexpr int OFF_HT = OFF_WQ + 32768;         // h^T                           
 constexpr int OFF_VN = OFF_HT + 16384;         // v_new^T                       64 rows
 constexpr int OFF_AQ = OFF_VN + 8192;          // A_qk                          2 x 64 rows
 constexpr int OFF_SMALL = OFF_AQ + 2 * 8192;
-constexpr int SMALL_BYTES = 4096;
-constexpr int SMEM_BYTES = OFF_SMALL + SMALL_BYTES + 1024;
+constexpr int SMALL_BYTES = 5120;
+// gates of the four diagonal 16x16 blocks, gdt[b][c][r] = base^(G_{16b+r} - G_{16b+c}) for
+// r >= c (else 0) at b * GD_B + c * 16 + r; the block stride 272 keeps the gating reads
+// (consecutive r across lanes) free of bank conflicts
+constexpr int GD_B = 272;
+constexpr int OFF_GD = OFF_SMALL + SMALL_BYTES;
+constexpr int SMEM_BYTES = OFF_GD + 4 * GD_B * 4 + 1024;
 static_assert(SMEM_BYTES <= 232448, "shared memory");
 
 constexpr uint32_t WAIT_LIMIT = 1u << 22;
 
-// gate factor table of a chunk (from the UT transform kernel), per chunk parity:
-// G, base^G, base^(G_last - G), beta base^G, beta
-enum { F_G = 0, F_EG = 1, F_EGL = 2, F_BEG = 3, F_BETA = 4 };
 struct WsState {
-  alignas(16) float tab[2][5][64];  // refilled with chunk c+2 while the chain runs chunk c
+  alignas(16) float tab[2][F_ROWS][64];  // refilled with chunk c+2 while the chain runs chunk c
   float EL[2];                      // base^(G_last) per chunk parity, for the chain
   uint64_t bar_p1, bar_p3, bar_p4, bar_p5, bar_po, bar_d0, bar_d1;
   uint64_t bar_ld[2], bar_v;  // TMA loads: stage parity (K, Q, X, factors) and V
@@ -98,8 +100,9 @@ struct FwdMaps {
 template <bool E2>
 __global__ void __launch_bounds__(NTH, 1) tc_fwd_ws_kernel(SimtFwdArgs a, const __grid_constant__ FwdMaps maps) {
   extern __shared__ uint8_t smem_raw[];
-  uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                            ~static_cast<uintptr_t>(1023));
+  // 1024-aligned base by pointer arithmetic on the shared array, so that the compiler keeps
+  // the shared address space (shared-memory instructions, not generic ones)
+  uint8_t *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   WsState &st = *reinterpret_cast<WsState *>(sm + OFF_SMALL);
   const uint32_t sb = smem_u32(sm);
 
@@ -197,13 +200,13 @@ __global__ void __launch_bounds__(NTH, 1) tc_fwd_ws_kernel(SimtFwdArgs a, const 
     const int y = (int)(r0 + c * GDN_CHUNK);
     const int64_t xs = (xbase + c) * H + h;
     uint64_t *bar = &st.bar_ld[s2];
-    mbar_expect_tx(bar, 5 * 8192 + 5 * GDN_CHUNK * 4);
+    mbar_expect_tx(bar, 5 * 8192 + F_ROWS * GDN_CHUNK * 4);
     tma_load_2d(stg, &maps.q, h * GDN_DK, y, bar);  // rows 0..63: Q
     tma_load_2d(stg + 16384, &maps.q, h * GDN_DK + 64, y, bar);
     tma_load_2d(stg + 8192, &maps.k, h * GDN_DK, y, bar);  // rows 64..127: K
     tma_load_2d(stg + 16384 + 8192, &maps.k, h * GDN_DK + 64, y, bar);
     tma_load_2d(xt, &maps.x, 0, (int)(xs * GDN_CHUNK), bar);
-    bulk_load(smem_u32(&st.tab[s2][0][0]), a.ftab + xs * 5 * GDN_CHUNK, 5 * GDN_CHUNK * 4, bar);
+    bulk_load(smem_u32(&st.tab[s2][0][0]), a.ftab + xs * F_ROWS * GDN_CHUNK, F_ROWS * GDN_CHUNK * 4, bar);
     last_ld[s2] = c;
   };
   auto issue_v = [&](int64_t c) {  // the CTA's 64 columns of V of chunk c
@@ -216,7 +219,7 @@ __global__ void __launch_bounds__(NTH, 1) tc_fwd_ws_kernel(SimtFwdArgs a, const 
   auto produce = [&](int64_t pc, int64_t c_chain) {
     const int ps = (int)(pc & 1);
     const uint32_t stg = sb + OFF_ST + ps * SZ_STAGE;
-    const float(&tab)[5][64] = st.tab[ps];
+    const float(&tab)[F_ROWS][64] = st.tab[ps];
     // buffers of chunk pc+1 (they held chunk pc-1, finished in the previous round)
     if (loader && pc + 1 < nch) issue_kqx(pc + 1);
     wait_par(&st.bar_ld[ps], pc >> 1);  // K, Q, X and factors of chunk pc have landed
@@ -227,6 +230,14 @@ __global__ void __launch_bounds__(NTH, 1) tc_fwd_ws_kernel(SimtFwdArgs a, const 
       mma_commit(&st.bar_p1);
     }
     __syncwarp();  // the issuing warp reconverges before any of its lanes polls a barrier
+    {  // diagonal-block gate table, spread over all producer threads (read after the next barrier)
+      float *gdt = reinterpret_cast<float *>(sm + OFF_GD);
+      for (int e = ptid; e < 1024; e += 256) {
+        const int b = e >> 8, c = (e >> 4) & 15, r = e & 15;
+        const float v = gexp<E2>(tab[F_G][16 * b + r] - tab[F_G][16 * b + c]);
+        gdt[b * GD_B + c * 16 + r] = r >= c ? v : 0.f;
+      }
+    }
     // transposes, loads first: K -> B3 rows 0..127 (b e^G) and KL (e^(Gl-G)); V -> B3 rows 128..191 (b)
     {
       const int pw = warp - 8;
@@ -255,7 +266,23 @@ __global__ void __launch_bounds__(NTH, 1) tc_fwd_ws_kernel(SimtFwdArgs a, const 
       }
     }
     prod_sync();  // V consumed (the next chunk's is loaded after the P3b issue)
-    // gating of Q K^T (rows 0..63 of S) -> A_qk, lower triangle including the diagonal
+    // gating of Q K^T (rows 0..63 of S) -> A_qk, lower triangle including the diagonal.
+    // Gate factors of this thread's 32 key tokens s, all read from tables (no exponential
+    // here): between 16-token blocks EA[t] EB_{b(t)}[s], inside the diagonal block the table
+    // above. They do not depend on S, so they are formed while P1 may still run.
+    float gf[32];
+    if (q4 < 2) {
+      const int t = row, bt = t >> 4;
+      const float ea = tab[F_EA][t];
+      const float *eb = tab[F_EB1 + (bt > 0 ? bt - 1 : 0)];
+      const float *gd = reinterpret_cast<const float *>(sm + OFF_GD) + bt * GD_B + (t & 15);
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        const int sj = 32 * hc + j, bs = sj >> 4;
+        const float off = ea * eb[sj], dg = gd[(sj & 15) * 16];
+        gf[j] = bs < bt ? off : (bs == bt ? dg : 0.f);
+      }
+    }
     wait_par(&st.bar_p1, pc);
     if (q4 < 2) {
       const int t = row;
@@ -263,12 +290,8 @@ __global__ void __launch_bounds__(NTH, 1) tc_fwd_ws_kernel(SimtFwdArgs a, const 
       tmem_ld16(tl + T_S + 64 * ps + 32 * hc, *reinterpret_cast<float(*)[16]>(sv));
       tmem_ld16(tl + T_S + 64 * ps + 32 * hc + 16, *reinterpret_cast<float(*)[16]>(sv + 16));
       tmem_ld_wait();
-      const float Gt = tab[F_G][t];
 #pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        const int sj = 32 * hc + j;
-        sv[j] = sj <= t ? sv[j] * gexp<E2>(Gt - tab[F_G][sj]) : 0.f;
-      }
+      for (int j = 0; j < 32; ++j) sv[j] *= gf[j];
       uint8_t *dst = sm + OFF_AQ + ps * 8192;
 #pragma unroll
       for (int q8 = 0; q8 < 4; ++q8)

@@ -18,6 +18,15 @@ struct alignas(64) TmaMap {
 // 64 x 64 boxes with the 128-byte swizzle; zero fill outside the matrix.
 cudaError_t make_tmap_bf16(TmaMap *map, const void *base, uint64_t cols, uint64_t rows, uint64_t row_bytes);
 
+// Rows of the per-chunk gate factor table written by the UT transform kernel
+// (64 floats each, one per token t of the chunk, b(t) = t / 16 its 16-token block):
+//   F_G    G_t (cumulative gate)            F_EG   base^G_t
+//   F_EGL  base^(G_last - G_t)              F_BEG  beta_t base^G_t        F_BETA beta_t
+//   F_EA   base^(G_t - G_{16 b(t)})         F_EB1 + b - 1  base^(G_{16 b} - G_t) for t < 16 b, else 0
+// so that for tokens t > s in different blocks base^(G_t - G_s) = EA[t] EB_{b(t)}[s], a
+// product of two factors that are both at most 1 for decaying gates.
+enum GateTabRow { F_G = 0, F_EG, F_EGL, F_BEG, F_BETA, F_EA, F_EB1, F_EB2, F_EB3, F_ROWS };
+
 // Arguments of the fp32 SIMT chunk kernel (forward, correction run, segment
 // summary and the backward's state recompute share it).
 struct SimtFwdArgs {
@@ -42,7 +51,7 @@ struct SimtFwdArgs {
   const float *g_cum_in;  // nullable: read the cumulative gate instead of summing g
   const float *A_in;      // nullable: read X = (I + L)^-1 instead of solving
   const __nv_bfloat16 *xw;  // tensor-core path: X of every chunk, [slots, H, 64, 64] bf16
-  const float *ftab;        // tensor-core path: gate factor table of every chunk, [slots, H, 5, 64]
+  const float *ftab;        // tensor-core path: gate factor table of every chunk, [slots, H, F_ROWS, 64]
   int *dev_flag;
 };
 
@@ -58,7 +67,7 @@ struct UtArgs {
   const float *g_cum_in;  // the saved cumulative gate (nullable)
   const void *beta;
   __nv_bfloat16 *xw;
-  float *ftab;      // per chunk and head: G, base^G, base^(G_last-G), beta base^G, beta (5 x 64)
+  float *ftab;      // per chunk and head: the gate factor table (F_ROWS x 64, GateTabRow)
   float *A;         // nullable, [rows, H, 64]
   float *g_cumsum;  // nullable
   int T, H;

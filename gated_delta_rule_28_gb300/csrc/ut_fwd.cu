@@ -11,7 +11,8 @@
 // in parallel (persistent CTAs of 4 warps walking the (chunk, head) items; K K^T
 // on bf16 mma.sync, the solve in fp32 shared memory) and written in bf16 for the tensor-core
 // state kernel, which then only multiplies by it, with a table of the chunk's
-// per-token gate factors (G, base^G, base^(G_last - G), beta base^G, beta).
+// per-token gate factors (GateTabRow: G, base^G, base^(G_last - G), beta base^G,
+// beta and the two factors of the gate between 16-token blocks).
 // The fp32 X (the A output of the forward) and the cumulative gate are
 // written here when asked for.
 #include <algorithm>
@@ -44,6 +45,7 @@ __global__ void __launch_bounds__(128, 4) ut_kernel(UtArgs a, int64_t items) {
   __shared__ __align__(16) float sg[64];
   __shared__ __align__(16) float sG[64];
   __shared__ __align__(16) float sbeta[64];
+  __shared__ __align__(16) float sEA[64], sEB[3][64];  // block-factorised gate (rows F_EA, F_EB1..)
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, H = a.H;
   const __nv_bfloat16 *k = static_cast<const __nv_bfloat16 *>(a.k);
@@ -144,7 +146,15 @@ __global__ void __launch_bounds__(128, 4) ut_kernel(UtArgs a, int64_t items) {
         mma_bf16_16816(acc[u][1], af, bf[1], bf[3]);
       }
     }
-    __syncthreads();  // every warp is done with the keys: their buffer now takes L
+    __syncthreads();  // the keys are consumed (their buffer now takes L); sG is complete
+    // base^(G_t - G_{16 b(t)}) and base^(G_{16 b} - G_s) for s < 16 b: for t > s in
+    // different blocks the gate is their product (each factor at most 1 for decaying gates)
+    if (tid < 64) sEA[tid] = gexp<E2>(sG[tid] - sG[tid & ~15]);
+    for (int e = tid; e < 192; e += 128) {
+      const int bb = 1 + (e >> 6), s2 = e & 63;
+      sEB[bb - 1][s2] = s2 < 16 * bb ? gexp<E2>(sG[16 * bb] - sG[s2]) : 0.f;
+    }
+    __syncthreads();
     float *LB = reinterpret_cast<float *>(kbuf[buf]);
 #pragma unroll
     for (int u = 0; u < 3; ++u) {
@@ -165,8 +175,15 @@ __global__ void __launch_bounds__(128, 4) ut_kernel(UtArgs a, int64_t items) {
           const int r = g + 8 * hr, c = nt * 8 + 2 * t;
           const int i = 16 * bi + r, j = 16 * bj + c;
           float2 val;
-          val.x = i > j ? bi_[hr] * acc[u][nt][2 * hr] * gexp<E2>(Gi[hr] - Gj.x) : 0.f;
-          val.y = i > j + 1 ? bi_[hr] * acc[u][nt][2 * hr + 1] * gexp<E2>(Gi[hr] - Gj.y) : 0.f;
+          if (bi > bj) {  // off-diagonal block: factorised gate, no exponential
+            const float fa = bi_[hr] * sEA[i];
+            const float2 eb = *reinterpret_cast<const float2 *>(&sEB[bi - 1][j]);
+            val.x = fa * acc[u][nt][2 * hr] * eb.x;
+            val.y = fa * acc[u][nt][2 * hr + 1] * eb.y;
+          } else {
+            val.x = i > j ? bi_[hr] * acc[u][nt][2 * hr] * gexp<E2>(Gi[hr] - Gj.x) : 0.f;
+            val.y = i > j + 1 ? bi_[hr] * acc[u][nt][2 * hr + 1] * gexp<E2>(Gi[hr] - Gj.y) : 0.f;
+          }
           *reinterpret_cast<float2 *>(&Lb[bsw(r, c)]) = val;  // c even: c, c+1 adjacent after the swizzle
         }
       }
@@ -201,14 +218,18 @@ __global__ void __launch_bounds__(128, 4) ut_kernel(UtArgs a, int64_t items) {
       }
     }
     if (a.g_cumsum && !a.g_cum_in && tid < n) a.g_cumsum[(r0 + tid) * H + h] = sG[tid];
-    if (tid < 64) {  // per-token gate factors for the state kernel
-      float *tab = a.ftab + (slot * H + h) * 5 * GDN_CHUNK;
+    if (tid < 64) {  // per-token gate factors for the state kernels (rows of GateTabRow)
+      float *tab = a.ftab + (slot * H + h) * F_ROWS * GDN_CHUNK;
       const float G = sG[tid], eg = gexp<E2>(G), bt = sbeta[tid];
-      tab[tid] = G;
-      tab[64 + tid] = eg;
-      tab[128 + tid] = gexp<E2>(sG[63] - G);
-      tab[192 + tid] = bt * eg;
-      tab[256 + tid] = bt;
+      tab[F_G * 64 + tid] = G;
+      tab[F_EG * 64 + tid] = eg;
+      tab[F_EGL * 64 + tid] = gexp<E2>(sG[63] - G);
+      tab[F_BEG * 64 + tid] = bt * eg;
+      tab[F_BETA * 64 + tid] = bt;
+      tab[F_EA * 64 + tid] = sEA[tid];
+      tab[F_EB1 * 64 + tid] = sEB[0][tid];
+      tab[F_EB2 * 64 + tid] = sEB[1][tid];
+      tab[F_EB3 * 64 + tid] = sEB[2][tid];
     }
     __syncthreads();  // sG, sbeta and the X blocks are rewritten by the next item
   }
