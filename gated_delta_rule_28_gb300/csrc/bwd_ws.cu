@@ -60,7 +60,7 @@ constexpr int OFF_SMALL = OFF_DVT + 8192;
 constexpr int SMALL_BYTES = 6144;
 // gates of the four diagonal 16x16 blocks, gdn[b][x][y] = base^(G_{16b+x} - G_{16b+y}) for
 // x >= y (else 0) at b * GD_B + x * 16 + y; block stride 272 against bank conflicts
-constexpr int GD_B = 272;
+constexpr int GD_B = GD_BLOCK;
 constexpr int OFF_GD = OFF_SMALL + SMALL_BYTES;
 constexpr int SMEM_BYTES = OFF_GD + 4 * GD_B * 4 + 1024;
 static_assert(SMEM_BYTES <= 232448, "shared memory");
@@ -192,7 +192,7 @@ __global__ void __launch_bounds__(NTH, 1) tc_dhu_kernel(BwdArgs a, const __grid_
     tma_load_2d(stg + 8192, &maps.k, h * GDN_DK, y, bar);  // rows 64..127: K
     tma_load_2d(stg + 16384 + 8192, &maps.k, h * GDN_DK + 64, y, bar);
     tma_load_2d(xt, &maps.x, 0, (int)(xs * GDN_CHUNK), bar);
-    bulk_load(smem_u32(&st.tab[s2][0][0]), a.ftab + xs * F_ROWS * GDN_CHUNK, F_ROWS * GDN_CHUNK * 4, bar);
+    bulk_load(smem_u32(&st.tab[s2][0][0]), a.ftab + xs * F_TAB, F_ROWS * GDN_CHUNK * 4, bar);
     last_ld[s2] = m;
   };
   auto issue_do = [&](int64_t m) {  // the CTA's 64 columns of dO

@@ -63,10 +63,9 @@ constexpr int OFF_VN = OFF_HT + 16384;         // v_new^T                       
 constexpr int OFF_AQ = OFF_VN + 8192;          // A_qk                          2 x 64 rows
 constexpr int OFF_SMALL = OFF_AQ + 2 * 8192;
 constexpr int SMALL_BYTES = 5120;
-// gates of the four diagonal 16x16 blocks, gdt[b][c][r] = base^(G_{16b+r} - G_{16b+c}) for
-// r >= c (else 0) at b * GD_B + c * 16 + r; the block stride 272 keeps the gating reads
-// (consecutive r across lanes) free of bank conflicts
-constexpr int GD_B = 272;
+// gates inside the four diagonal 16x16 blocks of one chunk (the F_GD part of its gate
+// table, one buffer: refilled for chunk c+1 once the gating of chunk c has read it)
+constexpr int GD_B = GD_BLOCK;
 constexpr int OFF_GD = OFF_SMALL + SMALL_BYTES;
 constexpr int SMEM_BYTES = OFF_GD + 4 * GD_B * 4 + 1024;
 static_assert(SMEM_BYTES <= 232448, "shared memory");
@@ -77,7 +76,7 @@ struct WsState {
   alignas(16) float tab[2][F_ROWS][64];  // refilled with chunk c+2 while the chain runs chunk c
   float EL[2];                      // base^(G_last) per chunk parity, for the chain
   uint64_t bar_p1, bar_p3, bar_p4, bar_p5, bar_po, bar_d0, bar_d1;
-  uint64_t bar_ld[2], bar_v;  // TMA loads: stage parity (K, Q, X, factors) and V
+  uint64_t bar_ld[2], bar_v, bar_gd;  // TMA loads: stage parity (K, Q, X, factors), V, diagonal gates
   uint32_t tmem;
 };
 static_assert(sizeof(WsState) <= SMALL_BYTES, "small state");
@@ -174,6 +173,7 @@ __global__ void __launch_bounds__(NTH, 1) tc_fwd_ws_kernel(SimtFwdArgs a, const 
     mbar_init(&st.bar_ld[0], 1);
     mbar_init(&st.bar_ld[1], 1);
     mbar_init(&st.bar_v, 1);
+    mbar_init(&st.bar_gd, 1);
     mbar_fence_init();
   }
   fence_before_sync();
@@ -206,8 +206,14 @@ __global__ void __launch_bounds__(NTH, 1) tc_fwd_ws_kernel(SimtFwdArgs a, const 
     tma_load_2d(stg + 8192, &maps.k, h * GDN_DK, y, bar);  // rows 64..127: K
     tma_load_2d(stg + 16384 + 8192, &maps.k, h * GDN_DK + 64, y, bar);
     tma_load_2d(xt, &maps.x, 0, (int)(xs * GDN_CHUNK), bar);
-    bulk_load(smem_u32(&st.tab[s2][0][0]), a.ftab + xs * F_ROWS * GDN_CHUNK, F_ROWS * GDN_CHUNK * 4, bar);
+    bulk_load(smem_u32(&st.tab[s2][0][0]), a.ftab + xs * F_TAB, F_ROWS * GDN_CHUNK * 4, bar);
     last_ld[s2] = c;
+  };
+  int64_t last_gd = -1;
+  auto issue_gd = [&](int64_t c) {  // gates inside the diagonal blocks of chunk c
+    mbar_expect_tx(&st.bar_gd, 4 * GD_B * 4);
+    bulk_load(sb + OFF_GD, a.ftab + ((xbase + c) * H + h) * F_TAB + F_GD, 4 * GD_B * 4, &st.bar_gd);
+    last_gd = c;
   };
   auto issue_v = [&](int64_t c) {  // the CTA's 64 columns of V of chunk c
     mbar_expect_tx(&st.bar_v, 8192);
@@ -230,14 +236,6 @@ __global__ void __launch_bounds__(NTH, 1) tc_fwd_ws_kernel(SimtFwdArgs a, const 
       mma_commit(&st.bar_p1);
     }
     __syncwarp();  // the issuing warp reconverges before any of its lanes polls a barrier
-    {  // diagonal-block gate table, spread over all producer threads (read after the next barrier)
-      float *gdt = reinterpret_cast<float *>(sm + OFF_GD);
-      for (int e = ptid; e < 1024; e += 256) {
-        const int b = e >> 8, c = (e >> 4) & 15, r = e & 15;
-        const float v = gexp<E2>(tab[F_G][16 * b + r] - tab[F_G][16 * b + c]);
-        gdt[b * GD_B + c * 16 + r] = r >= c ? v : 0.f;
-      }
-    }
     // transposes, loads first: K -> B3 rows 0..127 (b e^G) and KL (e^(Gl-G)); V -> B3 rows 128..191 (b)
     {
       const int pw = warp - 8;
@@ -268,8 +266,10 @@ __global__ void __launch_bounds__(NTH, 1) tc_fwd_ws_kernel(SimtFwdArgs a, const 
     prod_sync();  // V consumed (the next chunk's is loaded after the P3b issue)
     // gating of Q K^T (rows 0..63 of S) -> A_qk, lower triangle including the diagonal.
     // Gate factors of this thread's 32 key tokens s, all read from tables (no exponential
-    // here): between 16-token blocks EA[t] EB_{b(t)}[s], inside the diagonal block the table
-    // above. They do not depend on S, so they are formed while P1 may still run.
+    // here): between 16-token blocks EA[t] EB_{b(t)}[s], inside the diagonal block the UT
+    // kernel's table (in OFF_GD). They do not depend on S, so they are formed while P1 may
+    // still run.
+    wait_par(&st.bar_gd, pc);  // diagonal-block gates of chunk pc
     float gf[32];
     if (q4 < 2) {
       const int t = row, bt = t >> 4;
@@ -300,6 +300,7 @@ __global__ void __launch_bounds__(NTH, 1) tc_fwd_ws_kernel(SimtFwdArgs a, const 
     fence_proxy_async();
     fence_before_sync();
     prod_sync();
+    if (loader && pc + 1 < nch) issue_gd(pc + 1);  // the gating has read this chunk's
     if (ptid == 0) {  // P3b: w and u
       fence_after_sync();
       const uint32_t xt = sb + (ps ? OFF_X1 : OFF_X0);
@@ -444,6 +445,7 @@ __global__ void __launch_bounds__(NTH, 1) tc_fwd_ws_kernel(SimtFwdArgs a, const 
   if (loader && nch > 0) {
     issue_kqx(0);
     issue_v(0);
+    issue_gd(0);
   }
   if (!producer) {
     write_ht();
@@ -476,6 +478,7 @@ __global__ void __launch_bounds__(NTH, 1) tc_fwd_ws_kernel(SimtFwdArgs a, const 
       for (int s2 = 0; s2 < 2; ++s2)
         if (last_ld[s2] >= 0) mbar_wait(&st.bar_ld[s2], (uint32_t)((last_ld[s2] >> 1) & 1), WAIT_LIMIT);
       if (last_v >= 0) mbar_wait(&st.bar_v, (uint32_t)(last_v & 1), WAIT_LIMIT);
+      if (last_gd >= 0) mbar_wait(&st.bar_gd, (uint32_t)(last_gd & 1), WAIT_LIMIT);
     }
   } else if (!producer && a.ht && (a.nseg == 0 || s == a.nseg - 1)) {
     float4 *dst = reinterpret_cast<float4 *>(a.ht + ((int64_t)state_idx * H + h) * GDN_DK * GDN_DV +

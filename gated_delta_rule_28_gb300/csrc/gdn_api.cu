@@ -159,7 +159,7 @@ size_t x_part_bytes(const gdn_problem *p) {
 }
 size_t x_ws_bytes(const gdn_problem *p) {
   if (!use_tensor_cores(p)) return 0;
-  return x_part_bytes(p) + align256((size_t)n_chunk_slots(p) * p->H * gdn::F_ROWS * GDN_CHUNK * sizeof(float));
+  return x_part_bytes(p) + align256((size_t)n_chunk_slots(p) * p->H * gdn::F_TAB * sizeof(float));
 }
 
 gdn::UtArgs ut_args(const gdn_problem *p, const void *k, const float *g, const float *g_cum_in,

@@ -12,7 +12,8 @@
 // on bf16 mma.sync, the solve in fp32 shared memory) and written in bf16 for the tensor-core
 // state kernel, which then only multiplies by it, with a table of the chunk's
 // per-token gate factors (GateTabRow: G, base^G, base^(G_last - G), beta base^G,
-// beta and the two factors of the gate between 16-token blocks).
+// beta, the two factors of the gate between 16-token blocks, and the gates inside
+// the diagonal 16x16 blocks).
 // The fp32 X (the A output of the forward) and the cumulative gate are
 // written here when asked for.
 #include <algorithm>
@@ -46,6 +47,7 @@ __global__ void __launch_bounds__(128, 4) ut_kernel(UtArgs a, int64_t items) {
   __shared__ __align__(16) float sG[64];
   __shared__ __align__(16) float sbeta[64];
   __shared__ __align__(16) float sEA[64], sEB[3][64];  // block-factorised gate (rows F_EA, F_EB1..)
+  __shared__ __align__(16) float sGD[4 * GD_BLOCK];     // diagonal-block gates (layout of F_GD)
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, H = a.H;
   const __nv_bfloat16 *k = static_cast<const __nv_bfloat16 *>(a.k);
@@ -154,6 +156,10 @@ __global__ void __launch_bounds__(128, 4) ut_kernel(UtArgs a, int64_t items) {
       const int bb = 1 + (e >> 6), s2 = e & 63;
       sEB[bb - 1][s2] = s2 < 16 * bb ? gexp<E2>(sG[16 * bb] - sG[s2]) : 0.f;
     }
+    for (int e = tid; e < 4 * GD_BLOCK; e += 128) {  // gates inside the diagonal blocks
+      const int bb = e / GD_BLOCK, kk = e - GD_BLOCK * bb, c = kk >> 4, r = kk & 15;
+      sGD[e] = kk < 256 && r >= c ? gexp<E2>(sG[16 * bb + r] - sG[16 * bb + c]) : 0.f;
+    }
     __syncthreads();
     float *LB = reinterpret_cast<float *>(kbuf[buf]);
 #pragma unroll
@@ -165,11 +171,9 @@ __global__ void __launch_bounds__(128, 4) ut_kernel(UtArgs a, int64_t items) {
       const int g = lane >> 2, t = lane & 3;
       float *Lb = LB + blk(bi, bj) * 256;
       // this thread's rows g, g+8 and columns nt*8 + 2t + {0, 1}
-      const float Gi[2] = {sG[16 * bi + g], sG[16 * bi + g + 8]};
       const float bi_[2] = {sbeta[16 * bi + g], sbeta[16 * bi + g + 8]};
 #pragma unroll
       for (int nt = 0; nt < 2; ++nt) {
-        const float2 Gj = *reinterpret_cast<const float2 *>(&sG[16 * bj + nt * 8 + 2 * t]);
 #pragma unroll
         for (int hr = 0; hr < 2; ++hr) {
           const int r = g + 8 * hr, c = nt * 8 + 2 * t;
@@ -180,9 +184,10 @@ __global__ void __launch_bounds__(128, 4) ut_kernel(UtArgs a, int64_t items) {
             const float2 eb = *reinterpret_cast<const float2 *>(&sEB[bi - 1][j]);
             val.x = fa * acc[u][nt][2 * hr] * eb.x;
             val.y = fa * acc[u][nt][2 * hr + 1] * eb.y;
-          } else {
-            val.x = i > j ? bi_[hr] * acc[u][nt][2 * hr] * gexp<E2>(Gi[hr] - Gj.x) : 0.f;
-            val.y = i > j + 1 ? bi_[hr] * acc[u][nt][2 * hr + 1] * gexp<E2>(Gi[hr] - Gj.y) : 0.f;
+          } else {  // diagonal block: tabulated gate, strictly lower part
+            const float *gd = sGD + GD_BLOCK * bi + r;
+            val.x = i > j ? bi_[hr] * acc[u][nt][2 * hr] * gd[16 * c] : 0.f;
+            val.y = i > j + 1 ? bi_[hr] * acc[u][nt][2 * hr + 1] * gd[16 * (c + 1)] : 0.f;
           }
           *reinterpret_cast<float2 *>(&Lb[bsw(r, c)]) = val;  // c even: c, c+1 adjacent after the swizzle
         }
@@ -219,7 +224,7 @@ __global__ void __launch_bounds__(128, 4) ut_kernel(UtArgs a, int64_t items) {
     }
     if (a.g_cumsum && !a.g_cum_in && tid < n) a.g_cumsum[(r0 + tid) * H + h] = sG[tid];
     if (tid < 64) {  // per-token gate factors for the state kernels (rows of GateTabRow)
-      float *tab = a.ftab + (slot * H + h) * F_ROWS * GDN_CHUNK;
+      float *tab = a.ftab + (slot * H + h) * F_TAB;
       const float G = sG[tid], eg = gexp<E2>(G), bt = sbeta[tid];
       tab[F_G * 64 + tid] = G;
       tab[F_EG * 64 + tid] = eg;
@@ -231,6 +236,7 @@ __global__ void __launch_bounds__(128, 4) ut_kernel(UtArgs a, int64_t items) {
       tab[F_EB2 * 64 + tid] = sEB[1][tid];
       tab[F_EB3 * 64 + tid] = sEB[2][tid];
     }
+    for (int e = tid; e < 4 * GD_BLOCK; e += 128) a.ftab[(slot * H + h) * F_TAB + F_GD + e] = sGD[e];
     __syncthreads();  // sG, sbeta and the X blocks are rewritten by the next item
   }
   cp_async_wait<0>();
