@@ -17,8 +17,9 @@
 //   D2   -w^T dv_new            accumulated onto  scale Qg^T dO     -> dh update
 // while the producer warps 8..15 prepare the previous chunk: A_qk^T (from
 // [Q; K] Q^T and the gate), the three h-independent products scale A_qk^T dO,
-// scale Qg^T dO and w^T (= (beta base^G K)^T X^T), and the operands kgl and
-// w^T. X and the per-token gate factors come from the UT transform kernel.
+// scale Qg^T dO and w^T (= K^T (X diag(beta base^G))^T, the stage's K read as an
+// MN-major operand), and the operands kgl and w^T. X diag(beta base^G) and the
+// per-token gate factors come from the UT transform kernel.
 // Loads are TMA copies completing on mbarriers.
 // It writes dh of every chunk (the exit-state gradient) and dv_new in fp32
 // for the local-gradient kernel, and dh of the first chunk's entry as dh0.
@@ -45,14 +46,13 @@ constexpr uint32_t T_WT = 384;  // 64: w^T (keys x tokens)
 // shared memory (bytes from a 1024-aligned base); K-major tiles, 128 B rows
 constexpr int SZ_STAGE = 32768;               // [Q; K]: 2 K-blocks x 128 rows
 constexpr int OFF_ST = 0;                     // 2 stages
-constexpr int OFF_X0 = OFF_ST + 2 * SZ_STAGE; // X of even-order chunks (64 rows)
+constexpr int OFF_X0 = OFF_ST + 2 * SZ_STAGE; // X diag(beta base^G) of even-order chunks (64 rows)
 constexpr int OFF_X1 = OFF_X0 + 8192;
 constexpr int OFF_DO = OFF_X1 + 8192;         // dO slice, natural (64 rows, one buffer)
 constexpr int OFF_DOT = OFF_DO + 8192;        // dO^T (64 value rows)
 constexpr int OFF_AQT = OFF_DOT + 8192;       // A_qk^T rows 0..63 (rows 64..127 of the operand: QGT)
 constexpr int OFF_QGT = OFF_AQT + 8192;       // (scale base^G Q)^T   128 rows
-constexpr int OFF_B3K = OFF_QGT + 16384;      // (beta base^G K)^T    128 rows
-constexpr int OFF_KGL = OFF_B3K + 16384;      // kgl, 2 K-blocks of 64 rows
+constexpr int OFF_KGL = OFF_QGT + 16384;      // kgl, 2 K-blocks of 64 rows
 constexpr int OFF_WT = OFF_KGL + 16384;       // w^T, 128 rows
 constexpr int OFF_DHT = OFF_WT + 16384;       // dh^T, 2 K-blocks x 64 rows
 constexpr int OFF_DVT = OFF_DHT + 16384;      // dv_new^T, 64 rows
@@ -191,7 +191,7 @@ __global__ void __launch_bounds__(NTH, 1) tc_dhu_kernel(BwdArgs a, const __grid_
     tma_load_2d(stg + 16384, &maps.q, h * GDN_DK + 64, y, bar);
     tma_load_2d(stg + 8192, &maps.k, h * GDN_DK, y, bar);  // rows 64..127: K
     tma_load_2d(stg + 16384 + 8192, &maps.k, h * GDN_DK + 64, y, bar);
-    tma_load_2d(xt, &maps.x, 0, (int)(xs * GDN_CHUNK), bar);
+    tma_load_2d(xt, &maps.x, 0, (int)(xs * 2 * GDN_CHUNK + GDN_CHUNK), bar);  // X diag(b e^G)
     bulk_load(smem_u32(&st.tab[s2][0][0]), a.ftab + xs * F_TAB, F_ROWS * GDN_CHUNK * 4, bar);
     last_ld[s2] = m;
   };
@@ -227,18 +227,17 @@ __global__ void __launch_bounds__(NTH, 1) tc_dhu_kernel(BwdArgs a, const __grid_
         gdn[b * GD_B + x * 16 + y] = x >= y ? v : 0.f;
       }
     }
-    // transposes: K (rows 64..127) -> (beta base^G K)^T; Q -> (scale base^G Q)^T; dO -> dO^T
+    // transposes: Q -> (scale base^G Q)^T; dO -> dO^T
     {
       const int pw = warp - 8;
-      uint32_t xk[4][4], xq[4][4], xd[2][4];
+      uint32_t xq[4][4], xd[2][4];
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const int jb = pw + 8 * i, rb = jb >> 3, fb = jb & 7;
-        trans16_load(stg + (fb >> 2) * 16384, 64 + rb * 16, (fb & 3) * 2, lane, xk[i]);
         trans16_load(stg + (fb >> 2) * 16384, rb * 16, (fb & 3) * 2, lane, xq[i]);
       }
-#pragma unroll
       wait_par(&st.bar_do, pm);  // dO of this chunk
+#pragma unroll
       for (int i = 0; i < 2; ++i) {
         const int t = pw + 8 * i, rb = t >> 2, cb = t & 3;
         trans16_load(sb + OFF_DO, rb * 16, cb * 2, lane, xd[i]);
@@ -251,8 +250,6 @@ __global__ void __launch_bounds__(NTH, 1) tc_dhu_kernel(BwdArgs a, const __grid_
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const int jb = pw + 8 * i, rb = jb >> 3, fb = jb & 7;
-        // destination columns are token indices: the source row offset of K (64) is dropped
-        trans16_store(sb + OFF_B3K, fb * 16, rb * 16, xk[i], tab[F_BEG], lane);
         trans16_store(sb + OFF_QGT, fb * 16, rb * 16, xq[i], st.seg[ps], lane);
       }
     }
@@ -295,8 +292,8 @@ __global__ void __launch_bounds__(NTH, 1) tc_dhu_kernel(BwdArgs a, const __grid_
       mma_tiles(tmem + T_I1 + 64 * ps, sb + OFF_AQT, 8192, sb + OFF_DOT, 8192, 64, idesc_bf16(128, 64), false);
       // scale Qg^T dO
       mma_tiles(tmem + T_I2 + 64 * ps, sb + OFF_QGT, 16384, sb + OFF_DOT, 8192, 64, idesc_bf16(128, 64), false);
-      // w^T = (beta base^G K)^T X^T
-      mma_tiles(tmem + T_WT, sb + OFF_B3K, 16384, xt, 8192, 64, idesc_bf16(128, 64), false);
+      // w^T = K^T (X diag(beta base^G))^T: the stage's K rows read as an MN-major A
+      mma_ops(tmem + T_WT, mnmaj(stg + 8192, 16384), kmaj(xt, 0), 64, idesc_bf16(128, 64, false, true, false), false);
       mma_commit(&st.bar_p3);
     }
     __syncwarp();
@@ -474,7 +471,7 @@ cudaError_t launch_tc_dhu(const BwdArgs &a, int runs, cudaStream_t st) {
   cudaError_t e = make_tmap_bf16(&maps.q, a.q, (uint64_t)a.H * GDN_DK, rows, pitch);
   if (e == cudaSuccess) e = make_tmap_bf16(&maps.k, a.k, (uint64_t)a.H * GDN_DK, rows, pitch);
   if (e == cudaSuccess) e = make_tmap_bf16(&maps.dO, a.dO, (uint64_t)a.H * GDN_DV, rows, (uint64_t)a.H * GDN_DV * 2);
-  if (e == cudaSuccess) e = make_tmap_bf16(&maps.x, a.xw, GDN_CHUNK, slots * a.H * GDN_CHUNK, GDN_CHUNK * 2);
+  if (e == cudaSuccess) e = make_tmap_bf16(&maps.x, a.xw, GDN_CHUNK, slots * a.H * 2 * GDN_CHUNK, GDN_CHUNK * 2);
   if (e != cudaSuccess) return e;
   auto kern = a.use_exp2 ? tc_dhu_kernel<true> : tc_dhu_kernel<false>;
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);

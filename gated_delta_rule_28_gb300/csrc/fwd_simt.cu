@@ -3,7 +3,7 @@
 // One CTA owns one independent run (a batch row, a packed document or a
 // segment) of one head and one 32-column slice of the state, and walks the
 // run's 64-token chunks in order. Per chunk it takes the steps of the chunk
-// algorithm (north star; "state_summary.py" kda_split_state_summary_kernel
+// algorithm ("state_summary.py" kda_split_state_summary_kernel
 // loop body; chunk_fwd_h / chunk_kda_fwd_finalize stages of the KDA adapter):
 //   G   = in-chunk cumulative log-gate
 //   L   = strictly-lower(diag(beta) (K K^T (.) Gamma)),  X = (I + L)^-1

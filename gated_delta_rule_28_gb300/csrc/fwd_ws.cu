@@ -2,29 +2,28 @@
 // state recurrence overlapped with the preparation of the next chunk.
 //
 // One CTA (512 threads) owns one independent run (batch row, packed document
-// or segment) of one head and 64 of the 128 state columns; X = (I + L)^-1 of
-// every chunk comes precomputed in bf16 (UT transform kernel). Per chunk
-// (north star; GDN Ascend C adapter forward, chunk_fwd_h and the output step):
+// or segment) of one head and 64 of the 128 state columns; the UT transform
+// kernel supplies X = (I + L)^-1 of every chunk already scaled by its columns,
+// as the pair [X diag(b); X diag(b e^G)] in bf16. Per chunk (GDN Ascend C adapter
+// forward, chunk_fwd_h and the output step):
 //
 //   producer warps 8..15, chunk c+1 (no dependence on the state):
-//     P1   S = [Q; K] K^T                      -> A_qk = lower-incl(Q K^T (.) Gamma)
-//     P3b  X [b e^G K | b V]                   -> w = X diag(b e^G) K,  u = X diag(b) V
+//     P1   S = Q K^T                           -> A_qk = lower-incl(Q K^T (.) Gamma)
+//     P3   [X diag(b); X diag(b e^G)] [K | V]  -> w = X diag(b e^G) K,  u = X diag(b) V
 //          operand [w; e^G Q] for P4
 //   chain warps 0..7, chunk c (the state h lives in their registers, fp32):
 //     P4   [w; e^G Q] h                        -> v_new = u - w h,  q' h
-//     P5   (e^(G_last - G) K)^T v_new          -> h <- e^(G_last) h + P5
+//     P5   K^T (e^(G_last - G) v_new)          -> h <- e^(G_last) h + P5
 //     PO   A_qk v_new added onto q' h          -> o = scale (q' h + A_qk v_new)
 //
 // The two warp groups meet once per chunk (a CTA barrier); inside a chunk the
 // producer waits for P4 of the chain before it overwrites the P4 operand.
-// Loads are TMA copies (tensor tiles with the 128-byte swizzle, and one bulk copy
-// of the chunk's gate factors) completing on mbarriers.
-// Operands are K-major tiles with the 128-byte swizzle; the state-side
-// transposes (v_new^T, h^T) are written column-wise straight from the tensor
-// memory loads, the key and value transposes of the producer with
-// ldmatrix.trans / stmatrix. Every mbarrier wait is bounded; a wait that runs
-// out sets the device flag and the CTA drains its MMAs, frees its tensor
-// memory and leaves.
+// Loads are TMA copies (tensor tiles with the 128-byte swizzle, and bulk copies
+// of the chunk's gate factors) completing on mbarriers. No operand is
+// transposed: the token-major tiles (K, V, v_new, h by key) enter the MMAs as
+// MN-major operands, and every row the threads write is a run of 16-byte stores.
+// Every mbarrier wait is bounded; a wait that runs out sets the device flag and
+// the CTA drains its MMAs, frees its tensor memory and leaves.
 #include <string.h>
 
 #include "common.cuh"
@@ -41,28 +40,26 @@ constexpr int TBV = 64;   // state columns per CTA
 constexpr int NTH = 512;  // threads per CTA: 256 chain + 256 producer
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t T_S = 0;     // 2 x 64: P1 per chunk parity (rows 0..63 = Q K^T)
-constexpr uint32_t T_WW = 128;  // 128: P3b rows 0..63 = w
-constexpr uint32_t T_U = 256;   // 2 x 64: P3b rows 0..63 = u, per chunk parity
+constexpr uint32_t T_WW = 128;  // 128: P3w rows 64..127 = w
+constexpr uint32_t T_U = 256;   // 2 x 64: P3u rows 0..63 = u, per chunk parity
 constexpr uint32_t T_D4 = 384;  // 64: P4 rows 0..63 = w h, rows 64..127 = q' h (+ A_qk v_new)
 constexpr uint32_t T_P5 = 448;  // 64: P5
 
-// shared memory map (bytes from a 1024-aligned base); every tile K-major, 128 B rows.
-// The P3b operand is a 128-row tile whose rows 64..127 are not used: each X tile
-// is placed in front of a buffer that no copy writes while P3b runs (B3, KL),
-// and the A_qk tiles behind v_new^T for the same reason.
-constexpr int SZ_STAGE = 32768;                // [Q; K]: 2 K-blocks x 128 rows
-constexpr int OFF_ST = 0;                      // 2 stages
-constexpr int OFF_V = OFF_ST + 2 * SZ_STAGE;   // V slice, 64 rows (one buffer)
-constexpr int OFF_X0 = OFF_V + 8192;           // X of even chunks              64 rows
-constexpr int OFF_B3 = OFF_X0 + 8192;          // [b e^G K | b V]^T            192 rows
-constexpr int OFF_X1 = OFF_B3 + 24576;         // X of odd chunks               64 rows
-constexpr int OFF_KL = OFF_X1 + 8192;          // (e^(Gl-G) K)^T                2 x 128 rows
-constexpr int OFF_WQ = OFF_KL + 2 * 16384;     // [w; e^G Q]                    2 K-blocks x 128 rows
-constexpr int OFF_HT = OFF_WQ + 32768;         // h^T                           2 K-blocks x 64 rows
-constexpr int OFF_VN = OFF_HT + 16384;         // v_new^T                       64 rows
-constexpr int OFF_AQ = OFF_VN + 8192;          // A_qk                          2 x 64 rows
+// shared memory map (bytes from a 1024-aligned base); tiles of 128-byte rows, swizzled.
+// Token-major tiles (Q, K, V as loaded, v_new, h) serve as K- or MN-major operands as they
+// are. P1 and PO use 128-row A operands whose rows 64..127 (P1) or 0..63 (PO) are not
+// needed: they read whatever follows (precedes) the tile, and land in unread rows of D.
+constexpr int OFF_Q = 0;                      // Q, per chunk parity: 2 K-blocks x 64 rows
+constexpr int OFF_K = OFF_Q + 2 * 16384;      // K, three chunks in flight: 2 K-blocks x 64 rows
+constexpr int OFF_XX = OFF_K + 3 * 16384;     // [X diag(b); X diag(b e^G)] per parity: 128 rows
+constexpr int OFF_V = OFF_XX + 2 * 16384;     // V slice per parity: 64 rows
+constexpr int OFF_WQ = OFF_V + 2 * 8192;      // [w; e^G Q]: 2 K-blocks x 128 rows
+constexpr int OFF_HT = OFF_WQ + 32768;        // h: 128 key rows (MN-major B of P4)
+constexpr int OFF_VN = OFF_HT + 16384;        // v_new: 64 token rows (MN-major B of PO)
+constexpr int OFF_VNL = OFF_VN + 8192;        // e^(Gl - G) v_new (MN-major B of P5)
+constexpr int OFF_AQ = OFF_VNL + 8192;        // A_qk per parity: 64 rows (PO's rows 0..63: the 8 KB before)
 constexpr int OFF_SMALL = OFF_AQ + 2 * 8192;
-constexpr int SMALL_BYTES = 5120;
+constexpr int SMALL_BYTES = 6144;
 // gates inside the four diagonal 16x16 blocks of one chunk (the F_GD part of its gate
 // table, one buffer: refilled for chunk c+1 once the gating of chunk c has read it)
 constexpr int GD_B = GD_BLOCK;
@@ -74,24 +71,18 @@ constexpr uint32_t WAIT_LIMIT = 1u << 22;
 
 struct WsState {
   alignas(16) float tab[2][F_ROWS][64];  // refilled with chunk c+2 while the chain runs chunk c
+  float EGL[2][64];                 // base^(G_last - G) per chunk parity, for the chain
   float EL[2];                      // base^(G_last) per chunk parity, for the chain
   uint64_t bar_p1, bar_p3, bar_p4, bar_p5, bar_po, bar_d0, bar_d1;
-  uint64_t bar_ld[2], bar_v, bar_gd;  // TMA loads: stage parity (K, Q, X, factors), V, diagonal gates
+  uint64_t bar_ld[2], bar_gd;  // TMA loads: chunk parity (Q, K, X's, V, factors), diagonal gates
   uint32_t tmem;
 };
 static_assert(sizeof(WsState) <= SMALL_BYTES, "small state");
 
 __device__ __forceinline__ void chain_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
-__device__ __forceinline__ void prod_sync() { asm volatile("bar.sync 2, 256;" ::: "memory"); }
-__device__ __forceinline__ void sts_u16(uint32_t addr, uint16_t v) {
-  asm volatile("st.shared.u16 [%0], %1;" ::"r"(addr), "h"(v) : "memory");
-}
-__device__ __forceinline__ uint16_t bf16_bits(float x) {
-  const __nv_bfloat16 b = __float2bfloat16_rn(x);
-  return *reinterpret_cast<const uint16_t *>(&b);
-}
+__device__ __forceinline__ void gate_sync() { asm volatile("bar.sync 2, 128;" ::: "memory"); }
 
-// TMA maps: q, k, v over [rows, H*128] and X over [slots*H*64, 64], 64 x 64 boxes
+// TMA maps: q, k, v over [rows, H*128]; the X pair over [slots*H*128, 64]; 64 x 64 boxes
 struct FwdMaps {
   TmaMap q, k, v, x;
 };
@@ -113,10 +104,6 @@ __global__ void __launch_bounds__(NTH, 1) tc_fwd_ws_kernel(SimtFwdArgs a, const 
   const int H = a.H, h = blockIdx.y, z = blockIdx.z;
   const int col0 = blockIdx.x * TBV;
   const float scale = a.scale;
-  const __nv_bfloat16 *q = static_cast<const __nv_bfloat16 *>(a.q);
-  const __nv_bfloat16 *k = static_cast<const __nv_bfloat16 *>(a.k);
-  const __nv_bfloat16 *v = static_cast<const __nv_bfloat16 *>(a.v);
-  const __nv_bfloat16 *xw = a.xw;
   __nv_bfloat16 *o = static_cast<__nv_bfloat16 *>(a.o);
 
   // ---- the run -------------------------------------------------------------------
@@ -172,7 +159,6 @@ __global__ void __launch_bounds__(NTH, 1) tc_fwd_ws_kernel(SimtFwdArgs a, const 
     mbar_init(&st.bar_d1, 1);
     mbar_init(&st.bar_ld[0], 1);
     mbar_init(&st.bar_ld[1], 1);
-    mbar_init(&st.bar_v, 1);
     mbar_init(&st.bar_gd, 1);
     mbar_fence_init();
   }
@@ -186,26 +172,32 @@ __global__ void __launch_bounds__(NTH, 1) tc_fwd_ws_kernel(SimtFwdArgs a, const 
     if (!mbar_wait(bar, (uint32_t)(phase & 1), WAIT_LIMIT)) bad = true;
     fence_after_sync();
   };
+  auto q_at = [&](int64_t c) { return sb + OFF_Q + (uint32_t)(c & 1) * 16384u; };
+  auto k_at = [&](int64_t c) { return sb + OFF_K + (uint32_t)(c % 3) * 16384u; };
+  auto xx_at = [&](int64_t c) { return sb + OFF_XX + (uint32_t)(c & 1) * 16384u; };
+  auto v_at = [&](int64_t c) { return sb + OFF_V + (uint32_t)(c & 1) * 8192u; };
 
   // ---- producer: loads (TMA, issued by one thread: ptid 32, warp 9 lane 0) --------------
   // Rows past the run end are loaded as they are (the next run's tokens, or zeros past
-  // the tensor): they only meet beta = 0, a causal mask, or rows of o that are not stored.
+  // the tensor): they only meet beta = 0 (zero columns of both X's), a causal mask, or rows
+  // of o that are not stored.
   const int ptid = tid - 256;
   const bool loader = ptid == 32;
-  int64_t last_ld[2] = {-1, -1}, last_v = -1;  // loader: newest chunk per barrier
-  auto issue_kqx = [&](int64_t c) {  // K, Q, X and the gate factors of chunk c (buffers of parity c&1)
+  const bool issuer = ptid == 64;  // producer MMAs: warp 10 lane 0
+  int64_t last_ld[2] = {-1, -1};   // loader: newest chunk per barrier
+  auto issue_loads = [&](int64_t c) {  // Q, K, the X pair, V and the gate factors of chunk c
     const int s2 = (int)(c & 1);
-    const uint32_t stg = sb + OFF_ST + s2 * SZ_STAGE;
-    const uint32_t xt = sb + (s2 ? OFF_X1 : OFF_X0);
     const int y = (int)(r0 + c * GDN_CHUNK);
     const int64_t xs = (xbase + c) * H + h;
     uint64_t *bar = &st.bar_ld[s2];
-    mbar_expect_tx(bar, 5 * 8192 + F_ROWS * GDN_CHUNK * 4);
-    tma_load_2d(stg, &maps.q, h * GDN_DK, y, bar);  // rows 0..63: Q
-    tma_load_2d(stg + 16384, &maps.q, h * GDN_DK + 64, y, bar);
-    tma_load_2d(stg + 8192, &maps.k, h * GDN_DK, y, bar);  // rows 64..127: K
-    tma_load_2d(stg + 16384 + 8192, &maps.k, h * GDN_DK + 64, y, bar);
-    tma_load_2d(xt, &maps.x, 0, (int)(xs * GDN_CHUNK), bar);
+    mbar_expect_tx(bar, 7 * 8192 + F_ROWS * GDN_CHUNK * 4);
+    tma_load_2d(q_at(c), &maps.q, h * GDN_DK, y, bar);
+    tma_load_2d(q_at(c) + 8192, &maps.q, h * GDN_DK + 64, y, bar);
+    tma_load_2d(k_at(c), &maps.k, h * GDN_DK, y, bar);
+    tma_load_2d(k_at(c) + 8192, &maps.k, h * GDN_DK + 64, y, bar);
+    tma_load_2d(xx_at(c), &maps.x, 0, (int)(xs * 2 * GDN_CHUNK), bar);
+    tma_load_2d(xx_at(c) + 8192, &maps.x, 0, (int)(xs * 2 * GDN_CHUNK + GDN_CHUNK), bar);
+    tma_load_2d(v_at(c), &maps.v, h * GDN_DV + col0, y, bar);
     bulk_load(smem_u32(&st.tab[s2][0][0]), a.ftab + xs * F_TAB, F_ROWS * GDN_CHUNK * 4, bar);
     last_ld[s2] = c;
   };
@@ -215,126 +207,92 @@ __global__ void __launch_bounds__(NTH, 1) tc_fwd_ws_kernel(SimtFwdArgs a, const 
     bulk_load(sb + OFF_GD, a.ftab + ((xbase + c) * H + h) * F_TAB + F_GD, 4 * GD_B * 4, &st.bar_gd);
     last_gd = c;
   };
-  auto issue_v = [&](int64_t c) {  // the CTA's 64 columns of V of chunk c
-    mbar_expect_tx(&st.bar_v, 8192);
-    tma_load_2d(sb + OFF_V, &maps.v, h * GDN_DV + col0, (int)(r0 + c * GDN_CHUNK), &st.bar_v);
-    last_v = c;
-  };
 
   // ---- producer: one chunk -------------------------------------------------------------
+  // warps 8, 9, 12, 13 (lane quarters 0, 1): gating of Q K^T, then the e^G Q rows of the P4
+  // operand; warps 10, 11, 14, 15 (quarters 2, 3): the w rows.
   auto produce = [&](int64_t pc, int64_t c_chain) {
     const int ps = (int)(pc & 1);
-    const uint32_t stg = sb + OFF_ST + ps * SZ_STAGE;
     const float(&tab)[F_ROWS][64] = st.tab[ps];
-    // buffers of chunk pc+1 (they held chunk pc-1, finished in the previous round)
-    if (loader && pc + 1 < nch) issue_kqx(pc + 1);
-    wait_par(&st.bar_ld[ps], pc >> 1);  // K, Q, X and factors of chunk pc have landed
-    if (ptid == 0) {  // P1: S = [Q; K] K^T (rows 0..63 = Q K^T)
-      st.EL[ps] = tab[F_EG][63];
-      fence_after_sync();
-      mma_tiles(tmem + T_S + 64 * ps, stg, 16384, stg + 8192, 16384, 128, idesc_bf16(128, 64), false);
+    // buffers of chunk pc+1 (they held chunk pc-1, and K chunk pc-2: finished)
+    if (loader && pc + 1 < nch) issue_loads(pc + 1);
+    wait_par(&st.bar_ld[ps], pc >> 1);  // Q, K, X's, V and factors of chunk pc have landed
+    if (issuer) {
+      // P1: S = Q K^T (A rows 64..127: the next 64 rows of shared memory, unread output rows)
+      mma_ops(tmem + T_S + 64 * ps, kmaj(q_at(pc), 8192), kmaj(k_at(pc), 8192), 128, idesc_bf16(128, 64), false);
       mma_commit(&st.bar_p1);
-    }
-    __syncwarp();  // the issuing warp reconverges before any of its lanes polls a barrier
-    // transposes, loads first: K -> B3 rows 0..127 (b e^G) and KL (e^(Gl-G)); V -> B3 rows 128..191 (b)
-    {
-      const int pw = warp - 8;
-      uint32_t xk[4][4], xv[2][4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int jb = pw + 8 * i, rb = jb >> 3, fb = jb & 7;
-        trans16_load(stg + (fb >> 2) * 16384, 64 + rb * 16, (fb & 3) * 2, lane, xk[i]);  // K rows
-      }
-      wait_par(&st.bar_v, pc);  // V of chunk pc
-#pragma unroll
-      for (int i = 0; i < 2; ++i) {
-        const int t = pw + 8 * i, rb = t >> 2, cb = t & 3;
-        trans16_load(sb + OFF_V, rb * 16, cb * 2, lane, xv[i]);
-      }
-#pragma unroll
-      for (int i = 0; i < 2; ++i) {
-        const int t = pw + 8 * i, rb = t >> 2, cb = t & 3;
-        trans16_store(sb + OFF_B3, 128 + cb * 16, rb * 16, xv[i], tab[F_BETA], lane);
-      }
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int jb = pw + 8 * i, rb = jb >> 3, fb = jb & 7;
-        trans16_store(sb + OFF_B3, fb * 16, rb * 16, xk[i], tab[F_BEG], lane);
-        trans16_store(sb + OFF_KL + ps * 16384, fb * 16, rb * 16, xk[i], tab[F_EGL], lane);
-      }
-    }
-    prod_sync();  // V consumed (the next chunk's is loaded after the P3b issue)
-    // gating of Q K^T (rows 0..63 of S) -> A_qk, lower triangle including the diagonal.
-    // Gate factors of this thread's 32 key tokens s, all read from tables (no exponential
-    // here): between 16-token blocks EA[t] EB_{b(t)}[s], inside the diagonal block the UT
-    // kernel's table (in OFF_GD). They do not depend on S, so they are formed while P1 may
-    // still run.
-    wait_par(&st.bar_gd, pc);  // diagonal-block gates of chunk pc
-    float gf[32];
-    if (q4 < 2) {
-      const int t = row, bt = t >> 4;
-      const float ea = tab[F_EA][t];
-      const float *eb = tab[F_EB1 + (bt > 0 ? bt - 1 : 0)];
-      const float *gd = reinterpret_cast<const float *>(sm + OFF_GD) + bt * GD_B + (t & 15);
-#pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        const int sj = 32 * hc + j, bs = sj >> 4;
-        const float off = ea * eb[sj], dg = gd[(sj & 15) * 16];
-        gf[j] = bs < bt ? off : (bs == bt ? dg : 0.f);
-      }
-    }
-    wait_par(&st.bar_p1, pc);
-    if (q4 < 2) {
-      const int t = row;
-      float sv[32];
-      tmem_ld16(tl + T_S + 64 * ps + 32 * hc, *reinterpret_cast<float(*)[16]>(sv));
-      tmem_ld16(tl + T_S + 64 * ps + 32 * hc + 16, *reinterpret_cast<float(*)[16]>(sv + 16));
-      tmem_ld_wait();
-#pragma unroll
-      for (int j = 0; j < 32; ++j) sv[j] *= gf[j];
-      uint8_t *dst = sm + OFF_AQ + ps * 8192;
-#pragma unroll
-      for (int q8 = 0; q8 < 4; ++q8)
-        *reinterpret_cast<uint4 *>(dst + chunk_off(t, 4 * hc + q8)) = pack8(sv + 8 * q8);
-    }
-    fence_proxy_async();
-    fence_before_sync();
-    prod_sync();
-    if (loader && pc + 1 < nch) issue_gd(pc + 1);  // the gating has read this chunk's
-    if (ptid == 0) {  // P3b: w and u
-      fence_after_sync();
-      const uint32_t xt = sb + (ps ? OFF_X1 : OFF_X0);
-      mma_tiles(tmem + T_WW, xt, 8192, sb + OFF_B3, 24576, 64, idesc_bf16(128, 128), false);
-      mma_tiles(tmem + T_U + 64 * ps, xt, 8192, sb + OFF_B3 + 16384, 24576, 64, idesc_bf16(128, 64), false);
+      // P3: [X diag(b); X diag(b e^G)] [K | V] -> rows 64..127 of the K product = w,
+      // rows 0..63 of the V product = u (K and V token-major, read as MN-major B)
+      mma_ops(tmem + T_WW, kmaj(xx_at(pc), 0), mnmaj(k_at(pc), 8192), 64, idesc_bf16(128, 128, false, false, true),
+              false);
+      mma_ops(tmem + T_U + 64 * ps, kmaj(xx_at(pc), 0), mnmaj(v_at(pc), 0), 64,
+              idesc_bf16(128, 64, false, false, true), false);
       mma_commit(&st.bar_p3);
     }
     __syncwarp();  // the issuing warp reconverges before any of its lanes polls a barrier
-    if (loader && pc + 1 < nch) issue_v(pc + 1);  // V consumed by the transposes
-    // operand of P4: rows 64..127 = e^G Q once the chain's P4 has read the previous one,
-    // rows 0..63 = w once P3b is done (keys 64*hc .. +64 per thread)
     uint8_t *wq = sm + OFF_WQ + hc * 16384;
-    if (c_chain >= 0) wait_par(&st.bar_p4, c_chain);
-    if (q4 >= 2) {
-      const float eg = tab[F_EG][row - 64];
-      const uint8_t *qrow = sm + OFF_ST + ps * SZ_STAGE + hc * 16384;  // Q: stage rows 0..63
+    if (q4 < 2) {
+      const int t = row;
+      if (ptid == 0) st.EL[ps] = tab[F_EG][63];
+      if (hc == 0) st.EGL[ps][t] = tab[F_EGL][t];
+      // gating of Q K^T (rows 0..63 of S) -> A_qk, lower triangle including the diagonal.
+      // Gate factors of this thread's 32 key tokens s, all read from tables (no exponential
+      // here): between 16-token blocks EA[t] EB_{b(t)}[s], inside the diagonal block the UT
+      // kernel's table (in OFF_GD). They do not depend on S, so they are formed while P1 may
+      // still run.
+      wait_par(&st.bar_gd, pc);  // diagonal-block gates of chunk pc
+      float gf[32];
+      {
+        const int bt = t >> 4;
+        const float ea = tab[F_EA][t];
+        const float *eb = tab[F_EB1 + (bt > 0 ? bt - 1 : 0)];
+        const float *gd = reinterpret_cast<const float *>(sm + OFF_GD) + bt * GD_B + (t & 15);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const int sj = 32 * hc + j, bs = sj >> 4;
+          const float off = ea * eb[sj], dg = gd[(sj & 15) * 16];
+          gf[j] = bs < bt ? off : (bs == bt ? dg : 0.f);
+        }
+      }
+      wait_par(&st.bar_p1, pc);
+      {
+        float sv[32];
+        tmem_ld16(tl + T_S + 64 * ps + 32 * hc, *reinterpret_cast<float(*)[16]>(sv));
+        tmem_ld16(tl + T_S + 64 * ps + 32 * hc + 16, *reinterpret_cast<float(*)[16]>(sv + 16));
+        tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 32; ++j) sv[j] *= gf[j];
+        uint8_t *dst = sm + OFF_AQ + ps * 8192;
+#pragma unroll
+        for (int q8 = 0; q8 < 4; ++q8)
+          *reinterpret_cast<uint4 *>(dst + chunk_off(t, 4 * hc + q8)) = pack8(sv + 8 * q8);
+      }
+      gate_sync();  // every gating thread has read the diagonal gates of chunk pc
+      if (loader && pc + 1 < nch) issue_gd(pc + 1);
+      // rows 64..127 of the P4 operand: e^G Q, once the chain's P4 has read the previous one
+      if (c_chain >= 0) wait_par(&st.bar_p4, c_chain);
+      const float eg = tab[F_EG][t];
+      const uint8_t *qrow = sm + OFF_Q + ps * 16384 + hc * 8192;  // Q, K-block hc
 #pragma unroll
       for (int c8 = 0; c8 < 8; ++c8) {
         float f[8];
-        unpack8(*reinterpret_cast<const uint4 *>(qrow + chunk_off(row - 64, c8)), f);
+        unpack8(*reinterpret_cast<const uint4 *>(qrow + chunk_off(t, c8)), f);
 #pragma unroll
         for (int e = 0; e < 8; ++e) f[e] *= eg;
-        *reinterpret_cast<uint4 *>(wq + chunk_off(row, c8)) = pack8(f);
+        *reinterpret_cast<uint4 *>(wq + chunk_off(64 + t, c8)) = pack8(f);
       }
-    }
-    wait_par(&st.bar_p3, pc);
-    if (q4 < 2) {
+    } else {
+      // rows 0..63 of the P4 operand: w (keys 64*hc .. +64 per thread), once P3 is done and
+      // the chain's P4 has read the previous w
+      if (c_chain >= 0) wait_par(&st.bar_p4, c_chain);
+      wait_par(&st.bar_p3, pc);
 #pragma unroll
       for (int part = 0; part < 4; ++part) {
         float sv[16];
         tmem_ld16(tl + T_WW + 64 * hc + 16 * part, sv);
         tmem_ld_wait();
-        *reinterpret_cast<uint4 *>(wq + chunk_off(row, 2 * part)) = pack8(sv);
-        *reinterpret_cast<uint4 *>(wq + chunk_off(row, 2 * part + 1)) = pack8(sv + 8);
+        *reinterpret_cast<uint4 *>(wq + chunk_off(row - 64, 2 * part)) = pack8(sv);
+        *reinterpret_cast<uint4 *>(wq + chunk_off(row - 64, 2 * part + 1)) = pack8(sv + 8);
       }
     }
     fence_proxy_async();
@@ -352,12 +310,12 @@ __global__ void __launch_bounds__(NTH, 1) tc_fwd_ws_kernel(SimtFwdArgs a, const 
 #pragma unroll
     for (int j = 0; j < 32; ++j) hreg[j] = src ? src[j] : 0.f;
   }
-  // h^T (B operand of P4): this thread's key `row`, columns 32*hc .. +32
+  // h in bf16 (MN-major B operand of P4): this thread's key `row`, columns 32*hc .. +32
   auto write_ht = [&]() {
-    const uint32_t hbase = sb + OFF_HT + (row >> 6) * 8192 + (row & 7) * 2;
-    const int kc = (row & 63) >> 3;
+    uint8_t *hrow = sm + OFF_HT;
 #pragma unroll
-    for (int j = 0; j < 32; ++j) sts_u16(hbase + chunk_off(32 * hc + j, kc), bf16_bits(hreg[j]));
+    for (int q8 = 0; q8 < 4; ++q8)
+      *reinterpret_cast<uint4 *>(hrow + chunk_off(row, 4 * hc + q8)) = pack8(hreg + 8 * q8);
   };
   auto chain = [&](int64_t c) {
     const int par = (int)(c & 1);
@@ -373,13 +331,14 @@ __global__ void __launch_bounds__(NTH, 1) tc_fwd_ws_kernel(SimtFwdArgs a, const 
     }
     if (tid == 0) {  // P4: [w; e^G Q] h
       fence_after_sync();
-      mma_tiles(tmem + T_D4, sb + OFF_WQ, 16384, sb + OFF_HT, 8192, 128, idesc_bf16(128, 64), false);
+      mma_ops(tmem + T_D4, kmaj(sb + OFF_WQ, 16384), mnmaj(sb + OFF_HT, 0), 128,
+              idesc_bf16(128, 64, false, false, true), false);
       mma_commit(&st.bar_p4);
     }
     __syncwarp();  // the issuing warp reconverges before any of its lanes polls a barrier
     wait_par(&st.bar_p4, c);
-    if (q4 < 2) {  // v_new = u - w h  ->  v_new^T (column writes)
-      const uint32_t base = sb + OFF_VN + (row & 7) * 2;
+    if (q4 < 2) {  // v_new = u - w h (token row), and e^(Gl - G) v_new
+      const float egl = st.EGL[par][row];
 #pragma unroll
       for (int part = 0; part < 2; ++part) {
         float wh[16], u[16];
@@ -387,38 +346,40 @@ __global__ void __launch_bounds__(NTH, 1) tc_fwd_ws_kernel(SimtFwdArgs a, const 
         tmem_ld16(tl + T_U + 64 * par + 32 * hc + 16 * part, u);
         tmem_ld_wait();
 #pragma unroll
-        for (int j = 0; j < 16; ++j)
-          sts_u16(base + chunk_off(32 * hc + 16 * part + j, row >> 3), bf16_bits(u[j] - wh[j]));
+        for (int j = 0; j < 16; ++j) u[j] -= wh[j];
+        *reinterpret_cast<uint4 *>(sm + OFF_VN + chunk_off(row, 4 * hc + 2 * part)) = pack8(u);
+        *reinterpret_cast<uint4 *>(sm + OFF_VN + chunk_off(row, 4 * hc + 2 * part + 1)) = pack8(u + 8);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) u[j] *= egl;
+        *reinterpret_cast<uint4 *>(sm + OFF_VNL + chunk_off(row, 4 * hc + 2 * part)) = pack8(u);
+        *reinterpret_cast<uint4 *>(sm + OFF_VNL + chunk_off(row, 4 * hc + 2 * part + 1)) = pack8(u + 8);
       }
     }
     fence_proxy_async();
     fence_before_sync();
     chain_sync();
-    if (tid == 0) {  // P5, then the intra-chunk output term
+    if (tid == 0) {  // P5: K^T (e^(Gl-G) v_new), K read as MN-major A; then the intra-chunk output term
       fence_after_sync();
-      mma_tiles(tmem + T_P5, sb + OFF_KL + par * 16384, 16384, sb + OFF_VN, 8192, 64, idesc_bf16(128, 64), false);
+      mma_ops(tmem + T_P5, mnmaj(k_at(c), 8192), mnmaj(sb + OFF_VNL, 0), 64, idesc_bf16(128, 64, false, true, true),
+              false);
       mma_commit(&st.bar_p5);
-      mma_tiles(tmem + T_D4, sb + OFF_AQ + par * 8192 - 8192, 16384, sb + OFF_VN, 8192, 64, idesc_bf16(128, 64), true);
+      mma_ops(tmem + T_D4, kmaj(sb + OFF_AQ + par * 8192 - 8192, 0), mnmaj(sb + OFF_VN, 0), 64,
+              idesc_bf16(128, 64, false, false, true), true);
       mma_commit(&st.bar_po);
     }
     __syncwarp();  // the issuing warp reconverges before any of its lanes polls a barrier
     wait_par(&st.bar_p5, c);
     {
       const float el = st.EL[par];
-      const uint32_t hbase = sb + OFF_HT + (row >> 6) * 8192 + (row & 7) * 2;
-      const int kc = (row & 63) >> 3;
 #pragma unroll
       for (int part = 0; part < 2; ++part) {
         float p5[16];
         tmem_ld16(tl + T_P5 + 32 * hc + 16 * part, p5);
         tmem_ld_wait();
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          float &hv = hreg[16 * part + j];
-          hv = fmaf(el, hv, p5[j]);
-          sts_u16(hbase + chunk_off(32 * hc + 16 * part + j, kc), bf16_bits(hv));
-        }
+        for (int j = 0; j < 16; ++j) hreg[16 * part + j] = fmaf(el, hreg[16 * part + j], p5[j]);
       }
+      write_ht();
       if (q4 >= 2) {  // o = scale (q' h + A_qk v_new); the whole warp loads (collective)
         wait_par(&st.bar_po, c);
         const bool st_row = o && row - 64 < n;
@@ -443,8 +404,7 @@ __global__ void __launch_bounds__(NTH, 1) tc_fwd_ws_kernel(SimtFwdArgs a, const 
 
   // ---- prologue --------------------------------------------------------------------------
   if (loader && nch > 0) {
-    issue_kqx(0);
-    issue_v(0);
+    issue_loads(0);
     issue_gd(0);
   }
   if (!producer) {
@@ -471,13 +431,12 @@ __global__ void __launch_bounds__(NTH, 1) tc_fwd_ws_kernel(SimtFwdArgs a, const 
       raise_device_flag(a.dev_flag, kDevTimeout);
       mma_commit(&st.bar_d0);  // arrives once every MMA this thread issued has finished
     }
-    if (tid == 256) mma_commit(&st.bar_d1);
+    if (issuer) mma_commit(&st.bar_d1);
     if (tid == 0) mbar_wait(&st.bar_d0, 0, WAIT_LIMIT);
-    if (tid == 256) mbar_wait(&st.bar_d1, 0, WAIT_LIMIT);
+    if (issuer) mbar_wait(&st.bar_d1, 0, WAIT_LIMIT);
     if (loader) {  // copies still in flight land before the CTA leaves
       for (int s2 = 0; s2 < 2; ++s2)
         if (last_ld[s2] >= 0) mbar_wait(&st.bar_ld[s2], (uint32_t)((last_ld[s2] >> 1) & 1), WAIT_LIMIT);
-      if (last_v >= 0) mbar_wait(&st.bar_v, (uint32_t)(last_v & 1), WAIT_LIMIT);
       if (last_gd >= 0) mbar_wait(&st.bar_gd, (uint32_t)(last_gd & 1), WAIT_LIMIT);
     }
   } else if (!producer && a.ht && (a.nseg == 0 || s == a.nseg - 1)) {
@@ -507,7 +466,7 @@ cudaError_t launch_tc_fwd_ws(const SimtFwdArgs &a, dim3 grid, cudaStream_t st) {
     e = make_tmap_bf16(&maps.q, a.q, (uint64_t)a.H * GDN_DK, rows, pitch);
     if (e == cudaSuccess) e = make_tmap_bf16(&maps.k, a.k, (uint64_t)a.H * GDN_DK, rows, pitch);
     if (e == cudaSuccess) e = make_tmap_bf16(&maps.v, a.v, (uint64_t)a.H * GDN_DV, rows, (uint64_t)a.H * GDN_DV * 2);
-    if (e == cudaSuccess) e = make_tmap_bf16(&maps.x, a.xw, GDN_CHUNK, slots * a.H * GDN_CHUNK, GDN_CHUNK * 2);
+    if (e == cudaSuccess) e = make_tmap_bf16(&maps.x, a.xw, GDN_CHUNK, slots * a.H * 2 * GDN_CHUNK, GDN_CHUNK * 2);
   }
   if (e != cudaSuccess) return e;
   auto kern = a.use_exp2 ? tc_fwd_ws_kernel<true> : tc_fwd_ws_kernel<false>;

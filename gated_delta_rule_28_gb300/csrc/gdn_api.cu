@@ -155,7 +155,7 @@ size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 // bf16 X = (I + L)^-1 of every chunk and head, then the chunks' gate factor
 // tables (tensor-core path only)
 size_t x_part_bytes(const gdn_problem *p) {
-  return align256((size_t)n_chunk_slots(p) * p->H * GDN_CHUNK * GDN_CHUNK * 2);
+  return align256((size_t)n_chunk_slots(p) * p->H * 2 * GDN_CHUNK * GDN_CHUNK * 2);
 }
 size_t x_ws_bytes(const gdn_problem *p) {
   if (!use_tensor_cores(p)) return 0;

@@ -56,7 +56,7 @@ struct SimtFwdArgs {
   int summary;        // 1: columns [0,V) from v with zero start, [V,V+K) transfer from I
   const float *g_cum_in;  // nullable: read the cumulative gate instead of summing g
   const float *A_in;      // nullable: read X = (I + L)^-1 instead of solving
-  const __nv_bfloat16 *xw;  // tensor-core path: X of every chunk, [slots, H, 64, 64] bf16
+  const __nv_bfloat16 *xw;  // tensor-core path: [X diag(b); X diag(b e^G)] of every chunk, [slots, H, 128, 64] bf16
   const float *ftab;        // tensor-core path: gate factor table of every chunk, [slots, H, F_TAB]
   int *dev_flag;
 };
@@ -66,7 +66,8 @@ cudaError_t launch_simt_fwd(const SimtFwdArgs &a, bool per_key, bool bf16, dim3 
 int simt_fwd_bv();  // value columns per CTA
 
 // UT transform of every chunk (bf16 keys, scalar gate): X = (I + L)^-1 in bf16
-// into xw [slots, H, 64, 64]; optionally the fp32 X (A) and the cumulative gate.
+// as the pair [X diag(beta); X diag(beta base^G)] into xw [slots, H, 128, 64];
+// optionally the fp32 X (A) and the cumulative gate.
 struct UtArgs {
   const void *k;
   const float *g;         // raw gate, or
@@ -105,7 +106,7 @@ struct BwdArgs {
   const float *h_chunks;  // workspace: entry state of every chunk
   float *dh_chunks;       // workspace: gradient of every chunk's exit state
   float *dvnew;           // workspace: [rows,H,V] gradient of v_new
-  const __nv_bfloat16 *xw;  // tensor-core path: X of every chunk (UT transform kernel)
+  const __nv_bfloat16 *xw;  // tensor-core path: the X pair of every chunk (UT transform kernel)
   const float *ftab;        // tensor-core path: gate factor table of every chunk
   int B, T, H;
   float scale;

@@ -2,12 +2,13 @@
 // with bounded waits, tensor-memory allocation and loads, and tcgen05.mma
 // with shared-memory operand descriptors.
 //
-// Operand layout used throughout: "K-major, 128-byte swizzle" bf16 tiles.
-// A tile holds R rows (the M or N index) of 64 bf16 along K (128 bytes per
-// row); rows come in 8-row, 1024-byte atoms; inside an atom the 16-byte
-// chunk index of an element is XORed with (row mod 8). Wider K is stored as
-// consecutive 64-wide K-blocks of R x 128 bytes. Tiles start on 1024-byte
-// boundaries.
+// Operand layout: bf16 tiles with the 128-byte swizzle. A tile holds rows of
+// 64 bf16 (128 bytes); rows come in 8-row, 1024-byte atoms; inside an atom the
+// 16-byte chunk index of an element is XORed with (row mod 8). Tiles start on
+// 1024-byte boundaries. K-major: a row is one M (or N) index, 64 along K; wider
+// K is stored as consecutive 64-wide K-blocks. MN-major: a row is one K index,
+// 64 along M (or N) -- the natural layout of a row-major matrix read
+// transposed, so that token-major tiles serve as either operand unchanged.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -110,10 +111,24 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr) {
   return d;
 }
 
-// instruction descriptor of kind::f16: bf16 x bf16 -> f32, both K-major
-__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool negate_a = false) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | ((negate_a ? 1u : 0u) << 13) |
-         ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+// shared-memory operand descriptor: MN-major, 128-byte swizzle. Each 128-byte row holds 64
+// consecutive M (or N) elements of one K index; 8-row atoms of 1024 bytes follow each other
+// along K; the next 64 elements along M (N) start `lbo` bytes further on.
+__device__ __forceinline__ uint64_t sdesc_sw128_mn(uint32_t saddr, uint32_t lbo) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);      // start address
+  d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;   // leading byte offset: next 64 along M / N
+  d |= (uint64_t)(1024u >> 4) << 32;             // stride byte offset: next 8 rows along K
+  d |= (uint64_t)1 << 46;                        // descriptor version
+  d |= (uint64_t)2 << 61;                        // 128-byte swizzle
+  return d;
+}
+
+// instruction descriptor of kind::f16: bf16 x bf16 -> f32; A and B K-major unless a_mn / b_mn
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool negate_a = false, bool a_mn = false,
+                                                  bool b_mn = false) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((negate_a ? 1u : 0u) << 13) | ((a_mn ? 1u : 0u) << 15) |
+         ((b_mn ? 1u : 0u) << 16) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
 __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
@@ -149,6 +164,30 @@ __device__ __forceinline__ void mma_tiles(uint32_t d_tmem, uint32_t a_saddr, uin
       const uint64_t bd = b0 + ((uint64_t)(kb * b_kb + s * 32) >> 4);
       mma_bf16(d_tmem, ad, bd, idesc, (accumulate || kb > 0 || s > 0) ? 1u : 0u);
     }
+  }
+}
+
+// One operand of mma_ops: a swizzled tile at `addr`. K-major: 64-wide K-blocks `step` bytes
+// apart (a 16-element K step moves 32 bytes inside the block). MN-major: K rows of 128 bytes
+// (a 16-element K step moves 2048 bytes), `step` = bytes to the next 64 along M / N.
+struct Opnd {
+  uint32_t addr, step;
+  bool mn;
+};
+__device__ __forceinline__ Opnd kmaj(uint32_t addr, uint32_t kb) { return Opnd{addr, kb, false}; }
+__device__ __forceinline__ Opnd mnmaj(uint32_t addr, uint32_t lbo) { return Opnd{addr, lbo, true}; }
+
+// D[M x N] (+)= A[M x K] B[N x K]^T for K a multiple of 16, either operand K- or MN-major
+// (the instruction descriptor must say which, idesc_bf16's a_mn / b_mn)
+__device__ __forceinline__ void mma_ops(uint32_t d_tmem, Opnd A, Opnd B, int K, uint32_t idesc,
+                                        bool accumulate) {
+  const uint64_t a0 = A.mn ? sdesc_sw128_mn(A.addr, A.step) : sdesc_sw128(A.addr);
+  const uint64_t b0 = B.mn ? sdesc_sw128_mn(B.addr, B.step) : sdesc_sw128(B.addr);
+#pragma unroll
+  for (int ks = 0; ks < K / 16; ++ks) {
+    const uint32_t ao = A.mn ? (uint32_t)ks * 2048u : (uint32_t)(ks >> 2) * A.step + (uint32_t)(ks & 3) * 32u;
+    const uint32_t bo = B.mn ? (uint32_t)ks * 2048u : (uint32_t)(ks >> 2) * B.step + (uint32_t)(ks & 3) * 32u;
+    mma_bf16(d_tmem, a0 + (ao >> 4), b0 + (bo >> 4), idesc, (accumulate || ks > 0) ? 1u : 0u);
   }
 }
 

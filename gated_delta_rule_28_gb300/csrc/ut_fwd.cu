@@ -1,8 +1,7 @@
 // UT transform of every 64-token chunk, for all chunks and heads at once
 // (bf16 keys, scalar gate, sm_103a).
 //
-// Per chunk (north star: "the UT/WY transform A = (I + strictly-lower(diag(beta)
-// K K^T (.) gate-decay))^-1 diag(beta)"; GDN Ascend C adapter forward, steps
+// Per chunk (the UT/WY transform; GDN Ascend C adapter forward, steps
 // chunk_local_cumsum / chunk_scaled_dot_kkt / solve_tril):
 //   G = cumsum(g) inside the chunk
 //   L = strictly-lower(diag(beta) (K K^T (.) Gamma)),  Gamma_ij = base^(G_i - G_j)
@@ -48,6 +47,7 @@ __global__ void __launch_bounds__(128, 4) ut_kernel(UtArgs a, int64_t items) {
   __shared__ __align__(16) float sbeta[64];
   __shared__ __align__(16) float sEA[64], sEB[3][64];  // block-factorised gate (rows F_EA, F_EB1..)
   __shared__ __align__(16) float sGD[4 * GD_BLOCK];     // diagonal-block gates (layout of F_GD)
+  __shared__ __align__(16) float sBEG[64];              // beta base^G (column factor of X diag(b e^G))
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, H = a.H;
   const __nv_bfloat16 *k = static_cast<const __nv_bfloat16 *>(a.k);
@@ -156,6 +156,7 @@ __global__ void __launch_bounds__(128, 4) ut_kernel(UtArgs a, int64_t items) {
       const int bb = 1 + (e >> 6), s2 = e & 63;
       sEB[bb - 1][s2] = s2 < 16 * bb ? gexp<E2>(sG[16 * bb] - sG[s2]) : 0.f;
     }
+    if (tid < 64) sBEG[tid] = sbeta[tid] * gexp<E2>(sG[tid]);
     for (int e = tid; e < 4 * GD_BLOCK; e += 128) {  // gates inside the diagonal blocks
       const int bb = e / GD_BLOCK, kk = e - GD_BLOCK * bb, c = kk >> 4, r = kk & 15;
       sGD[e] = kk < 256 && r >= c ? gexp<E2>(sG[16 * bb + r] - sG[16 * bb + c]) : 0.f;
@@ -213,14 +214,22 @@ __global__ void __launch_bounds__(128, 4) ut_kernel(UtArgs a, int64_t items) {
           vals[16 * q + c4 + 3] = x.w;
         }
       }
-      uint4 *dst = reinterpret_cast<uint4 *>(a.xw + ((slot * H + h) * GDN_CHUNK + row) * GDN_CHUNK + 32 * half);
-#pragma unroll
-      for (int q = 0; q < 4; ++q) dst[q] = pack8(vals + 8 * q);
       if (a.A && row < n) {
         float4 *Ad = reinterpret_cast<float4 *>(a.A + ((r0 + row) * H + h) * GDN_CHUNK + 32 * half);
 #pragma unroll
         for (int q = 0; q < 8; ++q) Ad[q] = make_float4(vals[4 * q], vals[4 * q + 1], vals[4 * q + 2], vals[4 * q + 3]);
       }
+      // the pair [X diag(beta); X diag(beta base^G)] in bf16, 128 rows per chunk and head
+      __nv_bfloat16 *xrow = a.xw + ((slot * H + h) * 2 * GDN_CHUNK + row) * GDN_CHUNK + 32 * half;
+      float sc[32];
+#pragma unroll
+      for (int j = 0; j < 32; ++j) sc[j] = vals[j] * sbeta[32 * half + j];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) reinterpret_cast<uint4 *>(xrow)[q] = pack8(sc + 8 * q);
+#pragma unroll
+      for (int j = 0; j < 32; ++j) sc[j] = vals[j] * sBEG[32 * half + j];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) reinterpret_cast<uint4 *>(xrow + GDN_CHUNK * GDN_CHUNK)[q] = pack8(sc + 8 * q);
     }
     if (a.g_cumsum && !a.g_cum_in && tid < n) a.g_cumsum[(r0 + tid) * H + h] = sG[tid];
     if (tid < 64) {  // per-token gate factors for the state kernels (rows of GateTabRow)

@@ -1,7 +1,7 @@
 /*
  * gdn.h -- C ABI of the GB300 (sm_103a) chunked gated-delta-rule scan.
  *
- * The operation (benchmark spec of the gated delta rule, restated):
+ * The operation (the gated delta rule, restated):
  *   S_t = (I - beta_t k_t k_t^T) Diag(a_t) S_{t-1} + beta_t k_t v_t^T,
  *   o_t = scale * S_t^T q_t,
  *   a_t = exp(g_t) (use_exp2 = 0) or 2^(g_t) (use_exp2 = 1),

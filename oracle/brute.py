@@ -9,7 +9,7 @@ sum of products
     A_s = (I - b_s k_s k_s^T) Diag(a_s),    B_j = b_j k_j v_j^T,
     o_t = scale S_t^T q_t,
 
-which is what the north-star recurrence S_t = e^{g_t}(I - b k k^T) S_{t-1}
+which is what the gated-delta-rule recurrence S_t = e^{g_t}(I - b k k^T) S_{t-1}
 + b k v^T unrolls to (decay first for a per-key gate; for a scalar gate the
 two orders coincide). With base-2 gates whose logs are integers and rational
 b, k, v, q, every quantity is an exact ``Fraction``, so the fp64 oracle can

@@ -9,8 +9,8 @@ It takes the steps the pages name, in their order, one chunk at a time:
      kda_split_state_summary_kernel argument list; the GDN adapter's forward
      returns it as the g_cumsum slot);
   2. L = strictly-lower(diag(beta) (K K^T (.) Gamma)), Gamma_ij = base^(G_i - G_j)
-     (per key channel for the per-key gate), and A = (I + L)^-1 (spec:
-     the UT/WY transform; the GDN forward's "A" slot holds this inverse and
+     (per key channel for the per-key gate), and A = (I + L)^-1 (the UT/WY
+     transform; the GDN forward's "A" slot holds this inverse and
      beta stays separate in the "beta_eff" slot);
   3. w = A diag(beta) (K (.) base^G),  u = A diag(beta) V;
   4. state recurrence over chunks: v_new = u - w h;

@@ -9,7 +9,7 @@
  *
  * What it computes (the plain definition, one token at a time, no chunks):
  *
- *   Recurrence (benchmark spec of the gated delta rule; for the
+ *   Recurrence (the gated delta rule; for the
  *   per-key gate, decay first, as the state-summary page applies the decay
  *   to the state before the rank-one correction -- "state_summary.py",
  *   kda_split_state_summary_kernel loop body):

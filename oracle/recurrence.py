@@ -6,8 +6,8 @@ document offsets ``cu``; states are [N, H, K, V].
 
 Definitions followed (restated in ``gdn_oracle.c``):
   * the recurrence S_t = (I - b_t k_t k_t^T) Diag(a_t) S_{t-1} + b_t k_t v_t^T,
-    o_t = scale S_t^T q_t, a_t = exp(g_t) or 2^(g_t) -- the north-star
-    statement of the gated delta rule, decay-first for the per-key gate as in
+    o_t = scale S_t^T q_t, a_t = exp(g_t) or 2^(g_t) -- the gated delta
+    rule, decay-first for the per-key gate as in
     "state_summary.py" kda_split_state_summary_kernel;
   * the segment summary (S_ext, M) and merge S_{s+1} = M_s S_s + S_ext_s of
     apply_kda_state_summary (coverage-diff page) and SANA's

@@ -5,7 +5,7 @@ import numpy as np
 
 from oracle import chunk_form as CF, recurrence as R
 
-# relative Frobenius bounds (the benchmark spec): bf16 inputs with fp32 accumulation,
+# relative Frobenius bounds: bf16 inputs with fp32 accumulation,
 # and fp32 inputs
 TOL = {"bf16": 1e-2, "f32": 1e-4}
 

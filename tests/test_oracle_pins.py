@@ -2,7 +2,7 @@
 
 * exact rational values of the unrolled-product form (live and stored in
   tests/golden/exact_tiny.json);
-* closed forms the recurrence must satisfy (spec: with g = 0, beta = 1
+* closed forms the recurrence must satisfy (with g = 0, beta = 1
   and unit k, the updated state satisfies S_t^T k_t = v_t exactly; beta = 0
   leaves pure decay; a = 0 leaves one rank-one write);
 * central finite differences for the reverse mode, and the adjoint identity
@@ -106,7 +106,7 @@ def test_planted_mistakes_are_caught():
 
 
 def test_closed_form_unit_key_full_write():
-    """g = 0, beta = 1, |k| = 1  =>  S_t^T k_t = v_t exactly (the benchmark spec)."""
+    """g = 0, beta = 1, |k| = 1  =>  S_t^T k_t = v_t exactly (the delta rule's full write)."""
     rng = np.random.default_rng(3)
     B, T, H, K, V = 1, 40, 2, 16, 8
     q, k, v, g, beta, h0 = _rand_case(rng, B, T, H, K, V)
