@@ -10,14 +10,15 @@
 //   producer warps 8..15, chunk c+1 (no dependence on the state):
 //     P1   S = Q K^T                           -> A_qk = lower-incl(Q K^T (.) Gamma)
 //     P3   [X diag(b); X diag(b e^G)] [K | V]  -> w = X diag(b e^G) K,  u = X diag(b) V
-//          operand [w; e^G Q] for P4
+//          w rows of the operand [w; Q] of P4 (Q is loaded into it)
 //   chain warps 0..7, chunk c (the state h lives in their registers, fp32):
-//     P4   [w; e^G Q] h                        -> v_new = u - w h,  q' h
+//     P4   [w; Q] h                            -> v_new = u - w h,  Q h
 //     P5   K^T (e^(G_last - G) v_new)          -> h <- e^(G_last) h + P5
-//     PO   A_qk v_new added onto q' h          -> o = scale (q' h + A_qk v_new)
+//     PO   A_qk v_new                          -> o = scale (e^G (Q h) + A_qk v_new)
 //
-// The two warp groups meet once per chunk (a CTA barrier); inside a chunk the
-// producer waits for P4 of the chain before it overwrites the P4 operand.
+// The two warp groups meet once per chunk (a CTA barrier); every buffer one group
+// writes while the other reads is double-buffered by chunk parity (K, read by P5 one
+// round later, by three).
 // Loads are TMA copies (tensor tiles with the 128-byte swizzle, and bulk copies
 // of the chunk's gate factors) completing on mbarriers. No operand is
 // transposed: the token-major tiles (K, V, v_new, h by key) enter the MMAs as
@@ -39,32 +40,33 @@ using namespace tile;
 constexpr int TBV = 64;   // state columns per CTA
 constexpr int NTH = 512;  // threads per CTA: 256 chain + 256 producer
 constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t T_S = 0;     // 2 x 64: P1 per chunk parity (rows 0..63 = Q K^T)
+constexpr uint32_t T_S = 0;     // 64: P1 (rows 0..63 = Q K^T)
+constexpr uint32_t T_PO = 64;   // 64: PO (rows 64..127 = A_qk v_new)
 constexpr uint32_t T_WW = 128;  // 128: P3w rows 64..127 = w
 constexpr uint32_t T_U = 256;   // 2 x 64: P3u rows 0..63 = u, per chunk parity
-constexpr uint32_t T_D4 = 384;  // 64: P4 rows 0..63 = w h, rows 64..127 = q' h (+ A_qk v_new)
+constexpr uint32_t T_D4 = 384;  // 64: P4 rows 0..63 = w h, rows 64..127 = Q h
 constexpr uint32_t T_P5 = 448;  // 64: P5
 
 // shared memory map (bytes from a 1024-aligned base); tiles of 128-byte rows, swizzled.
 // Token-major tiles (Q, K, V as loaded, v_new, h) serve as K- or MN-major operands as they
 // are. P1 and PO use 128-row A operands whose rows 64..127 (P1) or 0..63 (PO) are not
 // needed: they read whatever follows (precedes) the tile, and land in unread rows of D.
-constexpr int OFF_Q = 0;                      // Q, per chunk parity: 2 K-blocks x 64 rows
-constexpr int OFF_K = OFF_Q + 2 * 16384;      // K, three chunks in flight: 2 K-blocks x 64 rows
+constexpr int OFF_WQ = 0;                     // [w; Q] per chunk parity: 2 K-blocks x 128 rows
+constexpr int OFF_K = OFF_WQ + 2 * 32768;     // K, three chunks in flight: 2 K-blocks x 64 rows
 constexpr int OFF_XX = OFF_K + 3 * 16384;     // [X diag(b); X diag(b e^G)] per parity: 128 rows
 constexpr int OFF_V = OFF_XX + 2 * 16384;     // V slice per parity: 64 rows
-constexpr int OFF_WQ = OFF_V + 2 * 8192;      // [w; e^G Q]: 2 K-blocks x 128 rows
-constexpr int OFF_HT = OFF_WQ + 32768;        // h: 128 key rows (MN-major B of P4)
+constexpr int OFF_HT = OFF_V + 2 * 8192;      // h: 128 key rows (MN-major B of P4)
 constexpr int OFF_VN = OFF_HT + 16384;        // v_new: 64 token rows (MN-major B of PO)
 constexpr int OFF_VNL = OFF_VN + 8192;        // e^(Gl - G) v_new (MN-major B of P5)
 constexpr int OFF_AQ = OFF_VNL + 8192;        // A_qk per parity: 64 rows (PO's rows 0..63: the 8 KB before)
 constexpr int OFF_SMALL = OFF_AQ + 2 * 8192;
 constexpr int SMALL_BYTES = 6144;
-// gates inside the four diagonal 16x16 blocks of one chunk (the F_GD part of its gate
-// table, one buffer: refilled for chunk c+1 once the gating of chunk c has read it)
+// gates inside the four diagonal 16x16 blocks of a chunk (the F_GD part of its gate
+// table), per chunk parity
 constexpr int GD_B = GD_BLOCK;
+constexpr int GD_BYTES = 4 * GD_B * 4;
 constexpr int OFF_GD = OFF_SMALL + SMALL_BYTES;
-constexpr int SMEM_BYTES = OFF_GD + 4 * GD_B * 4 + 1024;
+constexpr int SMEM_BYTES = OFF_GD + 2 * GD_BYTES + 1024;
 static_assert(SMEM_BYTES <= 232448, "shared memory");
 
 constexpr uint32_t WAIT_LIMIT = 1u << 22;
@@ -72,15 +74,16 @@ constexpr uint32_t WAIT_LIMIT = 1u << 22;
 struct WsState {
   alignas(16) float tab[2][F_ROWS][64];  // refilled with chunk c+2 while the chain runs chunk c
   float EGL[2][64];                 // base^(G_last - G) per chunk parity, for the chain
+  float EG[2][64];                  // base^G per chunk parity, for the chain
   float EL[2];                      // base^(G_last) per chunk parity, for the chain
-  uint64_t bar_p1, bar_p3, bar_p4, bar_p5, bar_po, bar_d0, bar_d1;
-  uint64_t bar_ld[2], bar_gd;  // TMA loads: chunk parity (Q, K, X's, V, factors), diagonal gates
+  uint64_t bar_p1, bar_p3, bar_p4, bar_p5, bar_po, bar_d0, bar_d1, bar_d2;
+  uint64_t bar_ld[2];  // TMA loads per chunk parity: K, the X pair, V, gate factors
+  uint64_t bar_q[2];   // TMA loads per chunk parity: Q (issued once P4 has read the buffer)
   uint32_t tmem;
 };
 static_assert(sizeof(WsState) <= SMALL_BYTES, "small state");
 
 __device__ __forceinline__ void chain_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
-__device__ __forceinline__ void gate_sync() { asm volatile("bar.sync 2, 128;" ::: "memory"); }
 
 // TMA maps: q, k, v over [rows, H*128]; the X pair over [slots*H*128, 64]; 64 x 64 boxes
 struct FwdMaps {
@@ -157,14 +160,18 @@ __global__ void __launch_bounds__(NTH, 1) tc_fwd_ws_kernel(SimtFwdArgs a, const 
     mbar_init(&st.bar_po, 1);
     mbar_init(&st.bar_d0, 1);
     mbar_init(&st.bar_d1, 1);
+    mbar_init(&st.bar_d2, 1);
+    mbar_init(&st.bar_q[0], 1);
+    mbar_init(&st.bar_q[1], 1);
     mbar_init(&st.bar_ld[0], 1);
     mbar_init(&st.bar_ld[1], 1);
-    mbar_init(&st.bar_gd, 1);
     mbar_fence_init();
   }
   fence_before_sync();
   __syncthreads();
   fence_after_sync();
+  // the X pair and the gate tables come from the kernel launched before this one
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const uint32_t tmem = st.tmem;
   const uint32_t tl = tmem + ((uint32_t)(q4 * 32) << 16);  // this warp's lane quarter
   bool bad = false;
@@ -172,7 +179,7 @@ __global__ void __launch_bounds__(NTH, 1) tc_fwd_ws_kernel(SimtFwdArgs a, const 
     if (!mbar_wait(bar, (uint32_t)(phase & 1), WAIT_LIMIT)) bad = true;
     fence_after_sync();
   };
-  auto q_at = [&](int64_t c) { return sb + OFF_Q + (uint32_t)(c & 1) * 16384u; };
+  auto wq_at = [&](int64_t c) { return sb + OFF_WQ + (uint32_t)(c & 1) * 32768u; };
   auto k_at = [&](int64_t c) { return sb + OFF_K + (uint32_t)(c % 3) * 16384u; };
   auto xx_at = [&](int64_t c) { return sb + OFF_XX + (uint32_t)(c & 1) * 16384u; };
   auto v_at = [&](int64_t c) { return sb + OFF_V + (uint32_t)(c & 1) * 8192u; };
@@ -183,44 +190,45 @@ __global__ void __launch_bounds__(NTH, 1) tc_fwd_ws_kernel(SimtFwdArgs a, const 
   // of o that are not stored.
   const int ptid = tid - 256;
   const bool loader = ptid == 32;
-  const bool issuer = ptid == 64;  // producer MMAs: warp 10 lane 0
+  const bool issuer = ptid == 64;  // producer MMAs: P3 by warp 10 lane 0, P1 by warp 8 lane 0
   int64_t last_ld[2] = {-1, -1};   // loader: newest chunk per barrier
-  auto issue_loads = [&](int64_t c) {  // Q, K, the X pair, V and the gate factors of chunk c
+  auto issue_loads = [&](int64_t c) {  // K, the X pair, V and the gate factors of chunk c
     const int s2 = (int)(c & 1);
     const int y = (int)(r0 + c * GDN_CHUNK);
     const int64_t xs = (xbase + c) * H + h;
     uint64_t *bar = &st.bar_ld[s2];
-    mbar_expect_tx(bar, 7 * 8192 + F_ROWS * GDN_CHUNK * 4);
-    tma_load_2d(q_at(c), &maps.q, h * GDN_DK, y, bar);
-    tma_load_2d(q_at(c) + 8192, &maps.q, h * GDN_DK + 64, y, bar);
+    mbar_expect_tx(bar, 5 * 8192 + F_ROWS * GDN_CHUNK * 4 + GD_BYTES);
     tma_load_2d(k_at(c), &maps.k, h * GDN_DK, y, bar);
     tma_load_2d(k_at(c) + 8192, &maps.k, h * GDN_DK + 64, y, bar);
     tma_load_2d(xx_at(c), &maps.x, 0, (int)(xs * 2 * GDN_CHUNK), bar);
     tma_load_2d(xx_at(c) + 8192, &maps.x, 0, (int)(xs * 2 * GDN_CHUNK + GDN_CHUNK), bar);
     tma_load_2d(v_at(c), &maps.v, h * GDN_DV + col0, y, bar);
     bulk_load(smem_u32(&st.tab[s2][0][0]), a.ftab + xs * F_TAB, F_ROWS * GDN_CHUNK * 4, bar);
+    bulk_load(sb + OFF_GD + s2 * GD_BYTES, a.ftab + xs * F_TAB + F_GD, GD_BYTES, bar);
     last_ld[s2] = c;
   };
-  int64_t last_gd = -1;
-  auto issue_gd = [&](int64_t c) {  // gates inside the diagonal blocks of chunk c
-    mbar_expect_tx(&st.bar_gd, 4 * GD_B * 4);
-    bulk_load(sb + OFF_GD, a.ftab + ((xbase + c) * H + h) * F_TAB + F_GD, 4 * GD_B * 4, &st.bar_gd);
-    last_gd = c;
+  // Q of chunk c into rows 64..127 of [w; Q] of parity c&1, by the chain's thread 0 (the
+  // buffer held chunk c-2, whose P4 it waits for)
+  int64_t last_q[2] = {-1, -1};
+  auto issue_q = [&](int64_t c) {
+    const int s2 = (int)(c & 1);
+    const int y = (int)(r0 + c * GDN_CHUNK);
+    mbar_expect_tx(&st.bar_q[s2], 2 * 8192);
+    tma_load_2d(wq_at(c) + 8192, &maps.q, h * GDN_DK, y, &st.bar_q[s2]);
+    tma_load_2d(wq_at(c) + 16384 + 8192, &maps.q, h * GDN_DK + 64, y, &st.bar_q[s2]);
+    last_q[s2] = c;
   };
 
   // ---- producer: one chunk -------------------------------------------------------------
-  // warps 8, 9, 12, 13 (lane quarters 0, 1): gating of Q K^T, then the e^G Q rows of the P4
-  // operand; warps 10, 11, 14, 15 (quarters 2, 3): the w rows.
+  // warps 8, 9, 12, 13 (lane quarters 0, 1): gating of Q K^T; warps 10, 11, 14, 15
+  // (quarters 2, 3): the w rows of the P4 operand.
   auto produce = [&](int64_t pc, int64_t c_chain) {
     const int ps = (int)(pc & 1);
     const float(&tab)[F_ROWS][64] = st.tab[ps];
-    // buffers of chunk pc+1 (they held chunk pc-1, and K chunk pc-2: finished)
+    // buffers of chunk pc+1 (they held chunk pc-1, and K chunk pc-2: finished, P4 included)
     if (loader && pc + 1 < nch) issue_loads(pc + 1);
-    wait_par(&st.bar_ld[ps], pc >> 1);  // Q, K, X's, V and factors of chunk pc have landed
+    wait_par(&st.bar_ld[ps], pc >> 1);  // K, X's, V and factors of chunk pc have landed
     if (issuer) {
-      // P1: S = Q K^T (A rows 64..127: the next 64 rows of shared memory, unread output rows)
-      mma_ops(tmem + T_S + 64 * ps, kmaj(q_at(pc), 8192), kmaj(k_at(pc), 8192), 128, idesc_bf16(128, 64), false);
-      mma_commit(&st.bar_p1);
       // P3: [X diag(b); X diag(b e^G)] [K | V] -> rows 64..127 of the K product = w,
       // rows 0..63 of the V product = u (K and V token-major, read as MN-major B)
       mma_ops(tmem + T_WW, kmaj(xx_at(pc), 0), mnmaj(k_at(pc), 8192), 64, idesc_bf16(128, 128, false, false, true),
@@ -230,23 +238,32 @@ __global__ void __launch_bounds__(NTH, 1) tc_fwd_ws_kernel(SimtFwdArgs a, const 
       mma_commit(&st.bar_p3);
     }
     __syncwarp();  // the issuing warp reconverges before any of its lanes polls a barrier
-    uint8_t *wq = sm + OFF_WQ + hc * 16384;
     if (q4 < 2) {
       const int t = row;
       if (ptid == 0) st.EL[ps] = tab[F_EG][63];
-      if (hc == 0) st.EGL[ps][t] = tab[F_EGL][t];
+      if (hc == 0) {
+        st.EGL[ps][t] = tab[F_EGL][t];
+        st.EG[ps][t] = tab[F_EG][t];
+      }
       // gating of Q K^T (rows 0..63 of S) -> A_qk, lower triangle including the diagonal.
       // Gate factors of this thread's 32 key tokens s, all read from tables (no exponential
       // here): between 16-token blocks EA[t] EB_{b(t)}[s], inside the diagonal block the UT
       // kernel's table (in OFF_GD). They do not depend on S, so they are formed while P1 may
       // still run.
-      wait_par(&st.bar_gd, pc);  // diagonal-block gates of chunk pc
+      if (ptid == 0) {
+        // P1: S = Q K^T, once Q has landed (A rows 64..127: the next 64 rows of shared
+        // memory, unread output rows)
+        wait_par(&st.bar_q[ps], pc >> 1);
+        mma_ops(tmem + T_S, kmaj(wq_at(pc) + 8192, 16384), kmaj(k_at(pc), 8192), 128, idesc_bf16(128, 64), false);
+        mma_commit(&st.bar_p1);
+      }
+      __syncwarp();  // the issuing warp reconverges before any of its lanes polls a barrier
       float gf[32];
       {
         const int bt = t >> 4;
         const float ea = tab[F_EA][t];
         const float *eb = tab[F_EB1 + (bt > 0 ? bt - 1 : 0)];
-        const float *gd = reinterpret_cast<const float *>(sm + OFF_GD) + bt * GD_B + (t & 15);
+        const float *gd = reinterpret_cast<const float *>(sm + OFF_GD + ps * GD_BYTES) + bt * GD_B + (t & 15);
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
           const int sj = 32 * hc + j, bs = sj >> 4;
@@ -257,8 +274,8 @@ __global__ void __launch_bounds__(NTH, 1) tc_fwd_ws_kernel(SimtFwdArgs a, const 
       wait_par(&st.bar_p1, pc);
       {
         float sv[32];
-        tmem_ld16(tl + T_S + 64 * ps + 32 * hc, *reinterpret_cast<float(*)[16]>(sv));
-        tmem_ld16(tl + T_S + 64 * ps + 32 * hc + 16, *reinterpret_cast<float(*)[16]>(sv + 16));
+        tmem_ld16(tl + T_S + 32 * hc, *reinterpret_cast<float(*)[16]>(sv));
+        tmem_ld16(tl + T_S + 32 * hc + 16, *reinterpret_cast<float(*)[16]>(sv + 16));
         tmem_ld_wait();
 #pragma unroll
         for (int j = 0; j < 32; ++j) sv[j] *= gf[j];
@@ -267,24 +284,9 @@ __global__ void __launch_bounds__(NTH, 1) tc_fwd_ws_kernel(SimtFwdArgs a, const 
         for (int q8 = 0; q8 < 4; ++q8)
           *reinterpret_cast<uint4 *>(dst + chunk_off(t, 4 * hc + q8)) = pack8(sv + 8 * q8);
       }
-      gate_sync();  // every gating thread has read the diagonal gates of chunk pc
-      if (loader && pc + 1 < nch) issue_gd(pc + 1);
-      // rows 64..127 of the P4 operand: e^G Q, once the chain's P4 has read the previous one
-      if (c_chain >= 0) wait_par(&st.bar_p4, c_chain);
-      const float eg = tab[F_EG][t];
-      const uint8_t *qrow = sm + OFF_Q + ps * 16384 + hc * 8192;  // Q, K-block hc
-#pragma unroll
-      for (int c8 = 0; c8 < 8; ++c8) {
-        float f[8];
-        unpack8(*reinterpret_cast<const uint4 *>(qrow + chunk_off(t, c8)), f);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) f[e] *= eg;
-        *reinterpret_cast<uint4 *>(wq + chunk_off(64 + t, c8)) = pack8(f);
-      }
     } else {
-      // rows 0..63 of the P4 operand: w (keys 64*hc .. +64 per thread), once P3 is done and
-      // the chain's P4 has read the previous w
-      if (c_chain >= 0) wait_par(&st.bar_p4, c_chain);
+      // rows 0..63 of the P4 operand [w; Q] of chunk pc (keys 64*hc .. +64), once P3 is done
+      uint8_t *wq = sm + OFF_WQ + ps * 32768 + hc * 16384;
       wait_par(&st.bar_p3, pc);
 #pragma unroll
       for (int part = 0; part < 4; ++part) {
@@ -329,14 +331,15 @@ __global__ void __launch_bounds__(NTH, 1) tc_fwd_ws_kernel(SimtFwdArgs a, const 
       for (int g4 = 0; g4 < 8; ++g4)
         dst[g4] = make_float4(hreg[g4 * 4], hreg[g4 * 4 + 1], hreg[g4 * 4 + 2], hreg[g4 * 4 + 3]);
     }
-    if (tid == 0) {  // P4: [w; e^G Q] h
+    if (tid == 0) {  // P4: [w; Q] h
       fence_after_sync();
-      mma_ops(tmem + T_D4, kmaj(sb + OFF_WQ, 16384), mnmaj(sb + OFF_HT, 0), 128,
+      mma_ops(tmem + T_D4, kmaj(wq_at(c), 16384), mnmaj(sb + OFF_HT, 0), 128,
               idesc_bf16(128, 64, false, false, true), false);
       mma_commit(&st.bar_p4);
     }
     __syncwarp();  // the issuing warp reconverges before any of its lanes polls a barrier
     wait_par(&st.bar_p4, c);
+    if (tid == 0 && c + 2 < nch) issue_q(c + 2);  // P4 has read Q of chunk c
     if (q4 < 2) {  // v_new = u - w h (token row), and e^(Gl - G) v_new
       const float egl = st.EGL[par][row];
 #pragma unroll
@@ -363,8 +366,8 @@ __global__ void __launch_bounds__(NTH, 1) tc_fwd_ws_kernel(SimtFwdArgs a, const 
       mma_ops(tmem + T_P5, mnmaj(k_at(c), 8192), mnmaj(sb + OFF_VNL, 0), 64, idesc_bf16(128, 64, false, true, true),
               false);
       mma_commit(&st.bar_p5);
-      mma_ops(tmem + T_D4, kmaj(sb + OFF_AQ + par * 8192 - 8192, 0), mnmaj(sb + OFF_VN, 0), 64,
-              idesc_bf16(128, 64, false, false, true), true);
+      mma_ops(tmem + T_PO, kmaj(sb + OFF_AQ + par * 8192 - 8192, 0), mnmaj(sb + OFF_VN, 0), 64,
+              idesc_bf16(128, 64, false, false, true), false);
       mma_commit(&st.bar_po);
     }
     __syncwarp();  // the issuing warp reconverges before any of its lanes polls a barrier
@@ -380,17 +383,19 @@ __global__ void __launch_bounds__(NTH, 1) tc_fwd_ws_kernel(SimtFwdArgs a, const 
         for (int j = 0; j < 16; ++j) hreg[16 * part + j] = fmaf(el, hreg[16 * part + j], p5[j]);
       }
       write_ht();
-      if (q4 >= 2) {  // o = scale (q' h + A_qk v_new); the whole warp loads (collective)
+      if (q4 >= 2) {  // o = scale (base^G Q h + A_qk v_new); the whole warp loads (collective)
         wait_par(&st.bar_po, c);
+        const float eg = st.EG[par][row - 64];
         const bool st_row = o && row - 64 < n;
         uint4 *dst = reinterpret_cast<uint4 *>(o + ((c0 + (st_row ? row - 64 : 0)) * H + h) * GDN_DV + col0 + 32 * hc);
 #pragma unroll
         for (int part = 0; part < 2; ++part) {
-          float ov[16];
+          float ov[16], av[16];
           tmem_ld16(tl + T_D4 + 32 * hc + 16 * part, ov);
+          tmem_ld16(tl + T_PO + 32 * hc + 16 * part, av);
           tmem_ld_wait();
 #pragma unroll
-          for (int j = 0; j < 16; ++j) ov[j] *= scale;
+          for (int j = 0; j < 16; ++j) ov[j] = scale * fmaf(eg, ov[j], av[j]);
           if (st_row) {
             dst[2 * part] = pack8(ov);
             dst[2 * part + 1] = pack8(ov + 8);
@@ -403,9 +408,10 @@ __global__ void __launch_bounds__(NTH, 1) tc_fwd_ws_kernel(SimtFwdArgs a, const 
   };
 
   // ---- prologue --------------------------------------------------------------------------
-  if (loader && nch > 0) {
-    issue_loads(0);
-    issue_gd(0);
+  if (loader && nch > 0) issue_loads(0);
+  if (tid == 0) {
+    if (nch > 0) issue_q(0);
+    if (nch > 1) issue_q(1);
   }
   if (!producer) {
     write_ht();
@@ -432,12 +438,16 @@ __global__ void __launch_bounds__(NTH, 1) tc_fwd_ws_kernel(SimtFwdArgs a, const 
       mma_commit(&st.bar_d0);  // arrives once every MMA this thread issued has finished
     }
     if (issuer) mma_commit(&st.bar_d1);
+    if (ptid == 0) mma_commit(&st.bar_d2);
     if (tid == 0) mbar_wait(&st.bar_d0, 0, WAIT_LIMIT);
     if (issuer) mbar_wait(&st.bar_d1, 0, WAIT_LIMIT);
+    if (ptid == 0) mbar_wait(&st.bar_d2, 0, WAIT_LIMIT);
+    if (tid == 0)  // Q copies still in flight land before the CTA leaves
+      for (int s2 = 0; s2 < 2; ++s2)
+        if (last_q[s2] >= 0) mbar_wait(&st.bar_q[s2], (uint32_t)((last_q[s2] >> 1) & 1), WAIT_LIMIT);
     if (loader) {  // copies still in flight land before the CTA leaves
       for (int s2 = 0; s2 < 2; ++s2)
         if (last_ld[s2] >= 0) mbar_wait(&st.bar_ld[s2], (uint32_t)((last_ld[s2] >> 1) & 1), WAIT_LIMIT);
-      if (last_gd >= 0) mbar_wait(&st.bar_gd, (uint32_t)(last_gd & 1), WAIT_LIMIT);
     }
   } else if (!producer && a.ht && (a.nseg == 0 || s == a.nseg - 1)) {
     float4 *dst = reinterpret_cast<float4 *>(a.ht + ((int64_t)state_idx * H + h) * GDN_DK * GDN_DV +
@@ -472,8 +482,21 @@ cudaError_t launch_tc_fwd_ws(const SimtFwdArgs &a, dim3 grid, cudaStream_t st) {
   auto kern = a.use_exp2 ? tc_fwd_ws_kernel<true> : tc_fwd_ws_kernel<false>;
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
   if (e != cudaSuccess) return e;
-  kern<<<grid, NTH, SMEM_BYTES, st>>>(a, maps);
-  return cudaGetLastError();
+  // programmatic dependent launch: the CTAs may start (tensor memory, barriers, h0) while
+  // the UT transform kernel before them in the stream finishes; they wait for it before
+  // their first load
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg;
+  memset(&cfg, 0, sizeof(cfg));
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(NTH);
+  cfg.dynamicSmemBytes = SMEM_BYTES;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, a, maps);
 }
 
 }  // namespace gdn

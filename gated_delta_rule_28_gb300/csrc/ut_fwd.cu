@@ -49,6 +49,9 @@ __global__ void __launch_bounds__(128, 4) ut_kernel(UtArgs a, int64_t items) {
   __shared__ __align__(16) float sGD[4 * GD_BLOCK];     // diagonal-block gates (layout of F_GD)
   __shared__ __align__(16) float sBEG[64];              // beta base^G (column factor of X diag(b e^G))
 
+  // the state kernel launched after this one may be scheduled as SMs free up (it waits for
+  // this grid's completion before it reads anything written here)
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, H = a.H;
   const __nv_bfloat16 *k = static_cast<const __nv_bfloat16 *>(a.k);
   const __nv_bfloat16 *beta = static_cast<const __nv_bfloat16 *>(a.beta);
