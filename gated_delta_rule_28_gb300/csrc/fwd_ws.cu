@@ -61,12 +61,7 @@ constexpr int OFF_VNL = OFF_VN + 8192;        // e^(Gl - G) v_new (MN-major B of
 constexpr int OFF_AQ = OFF_VNL + 8192;        // A_qk per parity: 64 rows (PO's rows 0..63: the 8 KB before)
 constexpr int OFF_SMALL = OFF_AQ + 2 * 8192;
 constexpr int SMALL_BYTES = 6144;
-// gates inside the four diagonal 16x16 blocks of a chunk (the F_GD part of its gate
-// table), per chunk parity
-constexpr int GD_B = GD_BLOCK;
-constexpr int GD_BYTES = 4 * GD_B * 4;
-constexpr int OFF_GD = OFF_SMALL + SMALL_BYTES;
-constexpr int SMEM_BYTES = OFF_GD + 2 * GD_BYTES + 1024;
+constexpr int SMEM_BYTES = OFF_SMALL + SMALL_BYTES + 1024;
 static_assert(SMEM_BYTES <= 232448, "shared memory");
 
 constexpr uint32_t WAIT_LIMIT = 1u << 22;
@@ -184,38 +179,40 @@ __global__ void __launch_bounds__(NTH, 1) tc_fwd_ws_kernel(SimtFwdArgs a, const 
   auto xx_at = [&](int64_t c) { return sb + OFF_XX + (uint32_t)(c & 1) * 16384u; };
   auto v_at = [&](int64_t c) { return sb + OFF_V + (uint32_t)(c & 1) * 8192u; };
 
-  // ---- producer: loads (TMA, issued by one thread: ptid 32, warp 9 lane 0) --------------
+  // ---- producer: loads (TMA, issued by warp 9) ------------------------------------------
+  // Every TMA copy and tcgen05 MMA is issued warp-collectively (one elected lane of a
+  // warp-uniform call, tc.cuh): warp 9 the loads and P1, warp 10 P3, warp 0 the chain's
+  // MMAs and its Q loads.
   // Rows past the run end are loaded as they are (the next run's tokens, or zeros past
   // the tensor): they only meet beta = 0 (zero columns of both X's), a causal mask, or rows
   // of o that are not stored.
   const int ptid = tid - 256;
-  const bool loader = ptid == 32;
-  const bool issuer = ptid == 64;  // producer MMAs: P3 by warp 10 lane 0, P1 by warp 8 lane 0
+  const bool loader = warp == 9;
+  const bool issuer = warp == 10;  // producer MMAs: P3 by warp 10, P1 by warp 9
   int64_t last_ld[2] = {-1, -1};   // loader: newest chunk per barrier
   auto issue_loads = [&](int64_t c) {  // K, the X pair, V and the gate factors of chunk c
     const int s2 = (int)(c & 1);
     const int y = (int)(r0 + c * GDN_CHUNK);
     const int64_t xs = (xbase + c) * H + h;
     uint64_t *bar = &st.bar_ld[s2];
-    mbar_expect_tx(bar, 5 * 8192 + F_ROWS * GDN_CHUNK * 4 + GD_BYTES);
-    tma_load_2d(k_at(c), &maps.k, h * GDN_DK, y, bar);
-    tma_load_2d(k_at(c) + 8192, &maps.k, h * GDN_DK + 64, y, bar);
-    tma_load_2d(xx_at(c), &maps.x, 0, (int)(xs * 2 * GDN_CHUNK), bar);
-    tma_load_2d(xx_at(c) + 8192, &maps.x, 0, (int)(xs * 2 * GDN_CHUNK + GDN_CHUNK), bar);
-    tma_load_2d(v_at(c), &maps.v, h * GDN_DV + col0, y, bar);
-    bulk_load(smem_u32(&st.tab[s2][0][0]), a.ftab + xs * F_TAB, F_ROWS * GDN_CHUNK * 4, bar);
-    bulk_load(sb + OFF_GD + s2 * GD_BYTES, a.ftab + xs * F_TAB + F_GD, GD_BYTES, bar);
+    mbar_expect_tx_w(bar, 5 * 8192 + F_ROWS * GDN_CHUNK * 4);
+    tma_load_2d_w(k_at(c), &maps.k, h * GDN_DK, y, bar);
+    tma_load_2d_w(k_at(c) + 8192, &maps.k, h * GDN_DK + 64, y, bar);
+    tma_load_2d_w(xx_at(c), &maps.x, 0, (int)(xs * 2 * GDN_CHUNK), bar);
+    tma_load_2d_w(xx_at(c) + 8192, &maps.x, 0, (int)(xs * 2 * GDN_CHUNK + GDN_CHUNK), bar);
+    tma_load_2d_w(v_at(c), &maps.v, h * GDN_DV + col0, y, bar);
+    bulk_load_w(smem_u32(&st.tab[s2][0][0]), a.ftab + xs * F_TAB, F_ROWS * GDN_CHUNK * 4, bar);
     last_ld[s2] = c;
   };
-  // Q of chunk c into rows 64..127 of [w; Q] of parity c&1, by the chain's thread 0 (the
+  // Q of chunk c into rows 64..127 of [w; Q] of parity c&1, by the chain's warp 0 (the
   // buffer held chunk c-2, whose P4 it waits for)
   int64_t last_q[2] = {-1, -1};
   auto issue_q = [&](int64_t c) {
     const int s2 = (int)(c & 1);
     const int y = (int)(r0 + c * GDN_CHUNK);
-    mbar_expect_tx(&st.bar_q[s2], 2 * 8192);
-    tma_load_2d(wq_at(c) + 8192, &maps.q, h * GDN_DK, y, &st.bar_q[s2]);
-    tma_load_2d(wq_at(c) + 16384 + 8192, &maps.q, h * GDN_DK + 64, y, &st.bar_q[s2]);
+    mbar_expect_tx_w(&st.bar_q[s2], 2 * 8192);
+    tma_load_2d_w(wq_at(c) + 8192, &maps.q, h * GDN_DK, y, &st.bar_q[s2]);
+    tma_load_2d_w(wq_at(c) + 16384 + 8192, &maps.q, h * GDN_DK + 64, y, &st.bar_q[s2]);
     last_q[s2] = c;
   };
 
@@ -231,11 +228,11 @@ __global__ void __launch_bounds__(NTH, 1) tc_fwd_ws_kernel(SimtFwdArgs a, const 
     if (issuer) {
       // P3: [X diag(b); X diag(b e^G)] [K | V] -> rows 64..127 of the K product = w,
       // rows 0..63 of the V product = u (K and V token-major, read as MN-major B)
-      mma_ops(tmem + T_WW, kmaj(xx_at(pc), 0), mnmaj(k_at(pc), 8192), 64, idesc_bf16(128, 128, false, false, true),
+      mma_ops_w(tmem + T_WW, kmaj(xx_at(pc), 0), mnmaj(k_at(pc), 8192), 64, idesc_bf16(128, 128, false, false, true),
               false);
-      mma_ops(tmem + T_U + 64 * ps, kmaj(xx_at(pc), 0), mnmaj(v_at(pc), 0), 64,
+      mma_ops_w(tmem + T_U + 64 * ps, kmaj(xx_at(pc), 0), mnmaj(v_at(pc), 0), 64,
               idesc_bf16(128, 64, false, false, true), false);
-      mma_commit(&st.bar_p3);
+      mma_commit_w(&st.bar_p3);
     }
     __syncwarp();  // the issuing warp reconverges before any of its lanes polls a barrier
     if (q4 < 2) {
@@ -245,30 +242,41 @@ __global__ void __launch_bounds__(NTH, 1) tc_fwd_ws_kernel(SimtFwdArgs a, const 
         st.EGL[ps][t] = tab[F_EGL][t];
         st.EG[ps][t] = tab[F_EG][t];
       }
-      // gating of Q K^T (rows 0..63 of S) -> A_qk, lower triangle including the diagonal.
-      // Gate factors of this thread's 32 key tokens s, all read from tables (no exponential
-      // here): between 16-token blocks EA[t] EB_{b(t)}[s], inside the diagonal block the UT
-      // kernel's table (in OFF_GD). They do not depend on S, so they are formed while P1 may
-      // still run.
-      if (ptid == 0) {
+      if (warp == 9) {
         // P1: S = Q K^T, once Q has landed (A rows 64..127: the next 64 rows of shared
         // memory, unread output rows)
         wait_par(&st.bar_q[ps], pc >> 1);
-        mma_ops(tmem + T_S, kmaj(wq_at(pc) + 8192, 16384), kmaj(k_at(pc), 8192), 128, idesc_bf16(128, 64), false);
-        mma_commit(&st.bar_p1);
+        mma_ops_w(tmem + T_S, kmaj(wq_at(pc) + 8192, 16384), kmaj(k_at(pc), 8192), 128, idesc_bf16(128, 64), false);
+        mma_commit_w(&st.bar_p1);
       }
-      __syncwarp();  // the issuing warp reconverges before any of its lanes polls a barrier
+      // gating of Q K^T (rows 0..63 of S) -> A_qk, lower triangle including the diagonal.
+      // Gate factors of this thread's 32 key tokens s, formed while P1 runs: between
+      // 16-token blocks from the tables, EA[t] EB_{b(t)}[s] (no exponential); inside the
+      // diagonal block base^(G_t - G_s), 16 exponentials in the two warps whose key tokens
+      // hold their rows' diagonal blocks (8: rows 0..31, keys 0..31; 13: rows 32..63, keys
+      // 32..63).
       float gf[32];
       {
         const int bt = t >> 4;
         const float ea = tab[F_EA][t];
         const float *eb = tab[F_EB1 + (bt > 0 ? bt - 1 : 0)];
-        const float *gd = reinterpret_cast<const float *>(sm + OFF_GD + ps * GD_BYTES) + bt * GD_B + (t & 15);
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
-          const int sj = 32 * hc + j, bs = sj >> 4;
-          const float off = ea * eb[sj], dg = gd[(sj & 15) * 16];
-          gf[j] = bs < bt ? off : (bs == bt ? dg : 0.f);
+          const int sj = 32 * hc + j;
+          gf[j] = (sj >> 4) < bt ? ea * eb[sj] : 0.f;
+        }
+        if (q4 == hc) {
+          const float gt = tab[F_G][t];
+          const int hi = bt & 1, r = t & 15;  // the diagonal block is keys 32 hc + 16 hi + 0..15
+          const float *gs = &tab[F_G][32 * hc + 16 * hi];
+          float e[16];
+#pragma unroll
+          for (int jj = 0; jj < 16; ++jj) e[jj] = jj <= r ? gexp<E2>(gt - gs[jj]) : 0.f;
+#pragma unroll
+          for (int jj = 0; jj < 16; ++jj) {
+            if (hi == 0) gf[jj] = e[jj];
+            else gf[16 + jj] = e[jj];
+          }
         }
       }
       wait_par(&st.bar_p1, pc);
@@ -331,15 +339,15 @@ __global__ void __launch_bounds__(NTH, 1) tc_fwd_ws_kernel(SimtFwdArgs a, const 
       for (int g4 = 0; g4 < 8; ++g4)
         dst[g4] = make_float4(hreg[g4 * 4], hreg[g4 * 4 + 1], hreg[g4 * 4 + 2], hreg[g4 * 4 + 3]);
     }
-    if (tid == 0) {  // P4: [w; Q] h
+    if (warp == 0) {  // P4: [w; Q] h
       fence_after_sync();
-      mma_ops(tmem + T_D4, kmaj(wq_at(c), 16384), mnmaj(sb + OFF_HT, 0), 128,
+      mma_ops_w(tmem + T_D4, kmaj(wq_at(c), 16384), mnmaj(sb + OFF_HT, 0), 128,
               idesc_bf16(128, 64, false, false, true), false);
-      mma_commit(&st.bar_p4);
+      mma_commit_w(&st.bar_p4);
     }
     __syncwarp();  // the issuing warp reconverges before any of its lanes polls a barrier
     wait_par(&st.bar_p4, c);
-    if (tid == 0 && c + 2 < nch) issue_q(c + 2);  // P4 has read Q of chunk c
+    if (warp == 0 && c + 2 < nch) issue_q(c + 2);  // P4 has read Q of chunk c
     if (q4 < 2) {  // v_new = u - w h (token row), and e^(Gl - G) v_new
       const float egl = st.EGL[par][row];
 #pragma unroll
@@ -361,14 +369,14 @@ __global__ void __launch_bounds__(NTH, 1) tc_fwd_ws_kernel(SimtFwdArgs a, const 
     fence_proxy_async();
     fence_before_sync();
     chain_sync();
-    if (tid == 0) {  // P5: K^T (e^(Gl-G) v_new), K read as MN-major A; then the intra-chunk output term
+    if (warp == 0) {  // P5: K^T (e^(Gl-G) v_new), K read as MN-major A; then the intra-chunk output term
       fence_after_sync();
-      mma_ops(tmem + T_P5, mnmaj(k_at(c), 8192), mnmaj(sb + OFF_VNL, 0), 64, idesc_bf16(128, 64, false, true, true),
+      mma_ops_w(tmem + T_P5, mnmaj(k_at(c), 8192), mnmaj(sb + OFF_VNL, 0), 64, idesc_bf16(128, 64, false, true, true),
               false);
-      mma_commit(&st.bar_p5);
-      mma_ops(tmem + T_PO, kmaj(sb + OFF_AQ + par * 8192 - 8192, 0), mnmaj(sb + OFF_VN, 0), 64,
+      mma_commit_w(&st.bar_p5);
+      mma_ops_w(tmem + T_PO, kmaj(sb + OFF_AQ + par * 8192 - 8192, 0), mnmaj(sb + OFF_VN, 0), 64,
               idesc_bf16(128, 64, false, false, true), false);
-      mma_commit(&st.bar_po);
+      mma_commit_w(&st.bar_po);
     }
     __syncwarp();  // the issuing warp reconverges before any of its lanes polls a barrier
     wait_par(&st.bar_p5, c);
@@ -409,7 +417,7 @@ __global__ void __launch_bounds__(NTH, 1) tc_fwd_ws_kernel(SimtFwdArgs a, const 
 
   // ---- prologue --------------------------------------------------------------------------
   if (loader && nch > 0) issue_loads(0);
-  if (tid == 0) {
+  if (warp == 0) {
     if (nch > 0) issue_q(0);
     if (nch > 1) issue_q(1);
   }
@@ -433,16 +441,15 @@ __global__ void __launch_bounds__(NTH, 1) tc_fwd_ws_kernel(SimtFwdArgs a, const 
   }
 
   if (bad) {
-    if (tid == 0) {
-      raise_device_flag(a.dev_flag, kDevTimeout);
-      mma_commit(&st.bar_d0);  // arrives once every MMA this thread issued has finished
-    }
-    if (issuer) mma_commit(&st.bar_d1);
-    if (ptid == 0) mma_commit(&st.bar_d2);
-    if (tid == 0) mbar_wait(&st.bar_d0, 0, WAIT_LIMIT);
+    if (tid == 0) raise_device_flag(a.dev_flag, kDevTimeout);
+    // each issuing warp's elected lane: arrives once every MMA it issued has finished
+    if (warp == 0) mma_commit_w(&st.bar_d0);
+    if (issuer) mma_commit_w(&st.bar_d1);
+    if (warp == 9) mma_commit_w(&st.bar_d2);
+    if (warp == 0) mbar_wait(&st.bar_d0, 0, WAIT_LIMIT);
     if (issuer) mbar_wait(&st.bar_d1, 0, WAIT_LIMIT);
-    if (ptid == 0) mbar_wait(&st.bar_d2, 0, WAIT_LIMIT);
-    if (tid == 0)  // Q copies still in flight land before the CTA leaves
+    if (warp == 9) mbar_wait(&st.bar_d2, 0, WAIT_LIMIT);
+    if (warp == 0)  // Q copies still in flight land before the CTA leaves
       for (int s2 = 0; s2 < 2; ++s2)
         if (last_q[s2] >= 0) mbar_wait(&st.bar_q[s2], (uint32_t)((last_q[s2] >> 1) & 1), WAIT_LIMIT);
     if (loader) {  // copies still in flight land before the CTA leaves

@@ -25,13 +25,11 @@ cudaError_t make_tmap_bf16(TmaMap *map, const void *base, uint64_t cols, uint64_
 //   F_EA   base^(G_t - G_{16 b(t)})         F_EB1 + b - 1  base^(G_{16 b} - G_t) for t < 16 b, else 0
 // so that for tokens t > s in different blocks base^(G_t - G_s) = EA[t] EB_{b(t)}[s], a
 // product of two factors that are both at most 1 for decaying gates.
-// After the rows, the gates inside the four diagonal 16x16 blocks:
-// base^(G_{16b+r} - G_{16b+c}) for r >= c (else 0) at F_GD + b * GD_BLOCK + c * 16 + r (the
-// block stride of 272 floats lets the forward's gating read them without bank conflicts).
 enum GateTabRow { F_G = 0, F_EG, F_EGL, F_BEG, F_BETA, F_EA, F_EB1, F_EB2, F_EB3, F_ROWS };
+constexpr int F_TAB = F_ROWS * 64;  // floats per chunk and head
+// block stride (floats) of a shared-memory table of the gates inside the four diagonal
+// 16x16 blocks; 272 keeps column-wise reads free of bank conflicts
 constexpr int GD_BLOCK = 272;
-constexpr int F_GD = F_ROWS * 64;            // offset of the diagonal-block gates
-constexpr int F_TAB = F_GD + 4 * GD_BLOCK;   // floats per chunk and head
 
 // Arguments of the fp32 SIMT chunk kernel (forward, correction run, segment
 // summary and the backward's state recompute share it).

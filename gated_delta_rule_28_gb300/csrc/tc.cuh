@@ -192,6 +192,43 @@ __device__ __forceinline__ void mma_ops(uint32_t d_tmem, Opnd A, Opnd B, int K, 
 }
 
 // ---------------------------------------------------------------------------
+// Warp-collective issue: called by all 32 lanes of a warp with warp-uniform
+// arguments; one elected lane (the same one every time) issues the operation.
+// Issuing from warp-uniform code keeps the descriptors in uniform registers: a
+// tcgen05.mma issued from a one-thread branch costs tens of cycles of operand
+// moves each, one issued this way about one.
+__device__ __forceinline__ void mma_bf16_w(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                           uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p, e;\n setp.ne.b32 p, %4, 0;\n elect.sync _|e, 0xffffffff;\n"
+      " @e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void mma_commit_w(uint64_t *bar) {
+  asm volatile(
+      "{\n .reg .pred e;\n elect.sync _|e, 0xffffffff;\n"
+      " @e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n}\n" ::"r"(smem_u32(bar))
+      : "memory");
+}
+// mma_ops, warp-collective
+__device__ __forceinline__ void mma_ops_w(uint32_t d_tmem, Opnd A, Opnd B, int K, uint32_t idesc, bool accumulate) {
+  const uint64_t a0 = A.mn ? sdesc_sw128_mn(A.addr, A.step) : sdesc_sw128(A.addr);
+  const uint64_t b0 = B.mn ? sdesc_sw128_mn(B.addr, B.step) : sdesc_sw128(B.addr);
+#pragma unroll
+  for (int ks = 0; ks < K / 16; ++ks) {
+    const uint32_t ao = A.mn ? (uint32_t)ks * 2048u : (uint32_t)(ks >> 2) * A.step + (uint32_t)(ks & 3) * 32u;
+    const uint32_t bo = B.mn ? (uint32_t)ks * 2048u : (uint32_t)(ks >> 2) * B.step + (uint32_t)(ks & 3) * 32u;
+    mma_bf16_w(d_tmem, a0 + (ao >> 4), b0 + (bo >> 4), idesc, (accumulate || ks > 0) ? 1u : 0u);
+  }
+}
+// mma_tiles, warp-collective
+__device__ __forceinline__ void mma_tiles_w(uint32_t d_tmem, uint32_t a_saddr, uint32_t a_kb, uint32_t b_saddr,
+                                            uint32_t b_kb, int K, uint32_t idesc, bool accumulate) {
+  mma_ops_w(d_tmem, kmaj(a_saddr, a_kb), kmaj(b_saddr, b_kb), K, idesc, accumulate);
+}
+
+// ---------------------------------------------------------------------------
 // TMA: tensor tiles and plain bulk copies into shared memory, completing on an
 // mbarrier that the issuing thread armed with the expected byte count
 __device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes) {
@@ -212,6 +249,29 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_
   asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
                "l"(src), "r"(bytes), "r"(smem_u32(bar))
                : "memory");
+}
+
+// TMA, warp-collective (see mma_bf16_w)
+__device__ __forceinline__ void mbar_expect_tx_w(uint64_t *bar, uint32_t bytes) {
+  asm volatile(
+      "{\n .reg .pred e;\n elect.sync _|e, 0xffffffff;\n"
+      " @e mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n}\n" ::"r"(smem_u32(bar)), "r"(bytes)
+      : "memory");
+}
+__device__ __forceinline__ void tma_load_2d_w(uint32_t dst, const void *map, int x, int y, uint64_t *bar) {
+  asm volatile(
+      "{\n .reg .pred e;\n elect.sync _|e, 0xffffffff;\n"
+      " @e cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];\n}\n" ::"r"(
+          dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+__device__ __forceinline__ void bulk_load_w(uint32_t dst, const void *src, uint32_t bytes, uint64_t *bar) {
+  asm volatile(
+      "{\n .reg .pred e;\n elect.sync _|e, 0xffffffff;\n"
+      " @e cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n}\n" ::"r"(dst),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
 }
 
 }  // namespace tc

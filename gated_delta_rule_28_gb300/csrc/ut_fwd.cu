@@ -11,8 +11,7 @@
 // on bf16 mma.sync, the solve in fp32 shared memory) and written in bf16 for the tensor-core
 // state kernel, which then only multiplies by it, with a table of the chunk's
 // per-token gate factors (GateTabRow: G, base^G, base^(G_last - G), beta base^G,
-// beta, the two factors of the gate between 16-token blocks, and the gates inside
-// the diagonal 16x16 blocks).
+// beta, and the two factors of the gate between 16-token blocks).
 // The fp32 X (the A output of the forward) and the cumulative gate are
 // written here when asked for.
 #include <algorithm>
@@ -46,7 +45,6 @@ __global__ void __launch_bounds__(128, 4) ut_kernel(UtArgs a, int64_t items) {
   __shared__ __align__(16) float sG[64];
   __shared__ __align__(16) float sbeta[64];
   __shared__ __align__(16) float sEA[64], sEB[3][64];  // block-factorised gate (rows F_EA, F_EB1..)
-  __shared__ __align__(16) float sGD[4 * GD_BLOCK];     // diagonal-block gates (layout of F_GD)
   __shared__ __align__(16) float sBEG[64];              // beta base^G (column factor of X diag(b e^G))
 
   // the state kernel launched after this one may be scheduled as SMs free up (it waits for
@@ -93,21 +91,37 @@ __global__ void __launch_bounds__(128, 4) ut_kernel(UtArgs a, int64_t items) {
     cp_async_commit();
   };
 
+  // gate and beta of an item into registers, one item ahead (rows past the end: no gate
+  // increment, beta 0)
+  auto load_gb = [&](int64_t it, float &gv, float &bv) {
+    gv = 0.f;
+    bv = 0.f;
+    int64_t rr;
+    int nn;
+    if (tid < 64 && it < items && locate(it, rr, nn) && tid < nn) {
+      const int hh = (int)(it % H);
+      gv = gsrc[(rr + tid) * H + hh];
+      bv = __bfloat162float(beta[(rr + tid) * H + hh]);
+    }
+  };
   int buf = 0;
+  float ng, nb;
   load_keys(blockIdx.x, 0);
+  load_gb(blockIdx.x, ng, nb);
   for (int64_t it = blockIdx.x; it < items; it += gridDim.x, buf ^= 1) {
     int64_t r0 = 0;
     int n = 0;
     const bool ok = locate(it, r0, n);
     const int h = (int)(it % H);
     const int64_t slot = it / H;
-    if (tid < 64) {  // gate and beta; rows past the end: no gate increment, beta 0
-      sg[tid] = ok && tid < n ? gsrc[(r0 + tid) * H + h] : 0.f;
-      sbeta[tid] = ok && tid < n ? __bfloat162float(beta[(r0 + tid) * H + h]) : 0.f;
+    if (tid < 64) {
+      sg[tid] = ng;
+      sbeta[tid] = nb;
     }
     cp_async_wait<0>();
     __syncthreads();
     load_keys(it + gridDim.x, buf ^ 1);
+    load_gb(it + gridDim.x, ng, nb);
     if (!ok) {
       if (tid == 0) raise_device_flag(a.dev_flag, kDevCheck);
       continue;  // uniform: every thread saw the same chunk index
@@ -160,10 +174,6 @@ __global__ void __launch_bounds__(128, 4) ut_kernel(UtArgs a, int64_t items) {
       sEB[bb - 1][s2] = s2 < 16 * bb ? gexp<E2>(sG[16 * bb] - sG[s2]) : 0.f;
     }
     if (tid < 64) sBEG[tid] = sbeta[tid] * gexp<E2>(sG[tid]);
-    for (int e = tid; e < 4 * GD_BLOCK; e += 128) {  // gates inside the diagonal blocks
-      const int bb = e / GD_BLOCK, kk = e - GD_BLOCK * bb, c = kk >> 4, r = kk & 15;
-      sGD[e] = kk < 256 && r >= c ? gexp<E2>(sG[16 * bb + r] - sG[16 * bb + c]) : 0.f;
-    }
     __syncthreads();
     float *LB = reinterpret_cast<float *>(kbuf[buf]);
 #pragma unroll
@@ -188,10 +198,9 @@ __global__ void __launch_bounds__(128, 4) ut_kernel(UtArgs a, int64_t items) {
             const float2 eb = *reinterpret_cast<const float2 *>(&sEB[bi - 1][j]);
             val.x = fa * acc[u][nt][2 * hr] * eb.x;
             val.y = fa * acc[u][nt][2 * hr + 1] * eb.y;
-          } else {  // diagonal block: tabulated gate, strictly lower part
-            const float *gd = sGD + GD_BLOCK * bi + r;
-            val.x = i > j ? bi_[hr] * acc[u][nt][2 * hr] * gd[16 * c] : 0.f;
-            val.y = i > j + 1 ? bi_[hr] * acc[u][nt][2 * hr + 1] * gd[16 * (c + 1)] : 0.f;
+          } else {  // diagonal block: strictly lower part
+            val.x = i > j ? bi_[hr] * acc[u][nt][2 * hr] * gexp<E2>(sG[i] - sG[j]) : 0.f;
+            val.y = i > j + 1 ? bi_[hr] * acc[u][nt][2 * hr + 1] * gexp<E2>(sG[i] - sG[j + 1]) : 0.f;
           }
           *reinterpret_cast<float2 *>(&Lb[bsw(r, c)]) = val;  // c even: c, c+1 adjacent after the swizzle
         }
@@ -248,7 +257,6 @@ __global__ void __launch_bounds__(128, 4) ut_kernel(UtArgs a, int64_t items) {
       tab[F_EB2 * 64 + tid] = sEB[1][tid];
       tab[F_EB3 * 64 + tid] = sEB[2][tid];
     }
-    for (int e = tid; e < 4 * GD_BLOCK; e += 128) a.ftab[(slot * H + h) * F_TAB + F_GD + e] = sGD[e];
     __syncthreads();  // sG, sbeta and the X blocks are rewritten by the next item
   }
   cp_async_wait<0>();
