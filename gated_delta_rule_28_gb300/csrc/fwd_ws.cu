@@ -369,14 +369,15 @@ __global__ void __launch_bounds__(NTH, 1) tc_fwd_ws_kernel(SimtFwdArgs a, const 
     fence_proxy_async();
     fence_before_sync();
     chain_sync();
-    if (warp == 0) {  // P5: K^T (e^(Gl-G) v_new), K read as MN-major A; then the intra-chunk output term
+    if (warp == 0) {  // the intra-chunk output term (the output is the longer path), then
+                      // P5: K^T (e^(Gl-G) v_new), K read as MN-major A
       fence_after_sync();
-      mma_ops_w(tmem + T_P5, mnmaj(k_at(c), 8192), mnmaj(sb + OFF_VNL, 0), 64, idesc_bf16(128, 64, false, true, true),
-              false);
-      mma_commit_w(&st.bar_p5);
       mma_ops_w(tmem + T_PO, kmaj(sb + OFF_AQ + par * 8192 - 8192, 0), mnmaj(sb + OFF_VN, 0), 64,
-              idesc_bf16(128, 64, false, false, true), false);
+                idesc_bf16(128, 64, false, false, true), false);
       mma_commit_w(&st.bar_po);
+      mma_ops_w(tmem + T_P5, mnmaj(k_at(c), 8192), mnmaj(sb + OFF_VNL, 0), 64, idesc_bf16(128, 64, false, true, true),
+                false);
+      mma_commit_w(&st.bar_p5);
     }
     __syncwarp();  // the issuing warp reconverges before any of its lanes polls a barrier
     wait_par(&st.bar_p5, c);
@@ -391,6 +392,7 @@ __global__ void __launch_bounds__(NTH, 1) tc_fwd_ws_kernel(SimtFwdArgs a, const 
         for (int j = 0; j < 16; ++j) hreg[16 * part + j] = fmaf(el, hreg[16 * part + j], p5[j]);
       }
       write_ht();
+      fence_proxy_async();  // h for the next P4 (the output below goes to global memory)
       if (q4 >= 2) {  // o = scale (base^G Q h + A_qk v_new); the whole warp loads (collective)
         wait_par(&st.bar_po, c);
         const float eg = st.EG[par][row - 64];
@@ -411,7 +413,6 @@ __global__ void __launch_bounds__(NTH, 1) tc_fwd_ws_kernel(SimtFwdArgs a, const 
         }
       }
     }
-    fence_proxy_async();
     fence_before_sync();
   };
 
