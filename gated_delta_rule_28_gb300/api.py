@@ -87,6 +87,77 @@ def chunk_gated_delta_rule_fwd(q, k, v, g, beta, *, h0=None, scale=None, use_exp
     return out
 
 
+class HostPipeline:
+    """Forward calls on inputs that live in pinned host memory, pipelined.
+
+    Each ``submit`` enqueues one call: the host-to-device copies of its inputs (spread over
+    ``h2d_streams`` streams, each taking a contiguous share of every tensor), the forward on
+    the compute stream, and the device-to-host copies of o and ht on a third stream. Calls
+    rotate over ``depth`` device buffer sets, so the copies of one call overlap the kernels
+    and copies of its neighbours; a set is refilled only after the kernels that read it and
+    the copies out of it have finished (stream events, no host waits). ``synchronize`` waits
+    for every call submitted so far. BSND layout, bf16 q/k/v/beta, fp32 scalar gate.
+    """
+
+    def __init__(self, Bsz, T, H, K, V, device, *, depth=2, h2d_streams=2, use_exp2=False, scale=None):
+        self.p = B.make_problem(Bsz, T, H, K, V, dtype=B.GDN_DTYPE_BF16, use_exp2=use_exp2,
+                                scale=0.0 if scale is None else scale)
+        self.nws = B.gdn_chunk_fwd_workspace(self.p)
+        self.ws = torch.empty(max(self.nws, 1), device=device, dtype=torch.uint8)
+        bf, f32 = torch.bfloat16, torch.float32
+        self.sets = [dict(q=torch.empty((Bsz, T, H, K), device=device, dtype=bf),
+                          k=torch.empty((Bsz, T, H, K), device=device, dtype=bf),
+                          v=torch.empty((Bsz, T, H, V), device=device, dtype=bf),
+                          g=torch.empty((Bsz, T, H), device=device, dtype=f32),
+                          beta=torch.empty((Bsz, T, H), device=device, dtype=bf),
+                          o=torch.empty((Bsz, T, H, V), device=device, dtype=bf),
+                          ht=torch.empty((Bsz, H, K, V), device=device, dtype=f32)) for _ in range(depth)]
+        self.depth = depth
+        self.s_in = [torch.cuda.Stream(device=device) for _ in range(h2d_streams)]
+        self.s_comp = torch.cuda.Stream(device=device)
+        self.s_out = torch.cuda.Stream(device=device)
+        self.ev_in = [[torch.cuda.Event() for _ in range(h2d_streams)] for _ in range(depth)]
+        self.ev_comp = [torch.cuda.Event() for _ in range(depth)]
+        self.ev_out = [torch.cuda.Event() for _ in range(depth)]
+        self.n = 0
+
+    def streams(self):
+        return self.s_in + [self.s_comp, self.s_out]
+
+    def submit(self, hq, hk, hv, hg, hbeta, ho, hht):
+        i = self.n % self.depth
+        s = self.sets[i]
+        reuse = self.n >= self.depth
+        pairs = [(s["q"], hq), (s["k"], hk), (s["v"], hv), (s["g"], hg), (s["beta"], hbeta)]
+        ns = len(self.s_in)
+        for j, st in enumerate(self.s_in):
+            if reuse:
+                st.wait_event(self.ev_comp[i])  # the kernels that read this set have finished
+            with torch.cuda.stream(st):
+                for dst, src in pairs:
+                    n = dst.numel()
+                    a, b = n * j // ns, n * (j + 1) // ns
+                    dst.view(-1)[a:b].copy_(src.view(-1)[a:b], non_blocking=True)
+            self.ev_in[i][j].record(st)
+        for j in range(ns):
+            self.s_comp.wait_event(self.ev_in[i][j])
+        if reuse:
+            self.s_comp.wait_event(self.ev_out[i])  # the outputs of this set have been copied out
+        B.gdn_chunk_fwd(self.p, s["q"], s["k"], s["v"], s["g"], s["beta"], None, s["o"], s["ht"],
+                        None, None, None, self.ws, self.nws, self.s_comp.cuda_stream)
+        self.ev_comp[i].record(self.s_comp)
+        self.s_out.wait_event(self.ev_comp[i])
+        with torch.cuda.stream(self.s_out):
+            ho.copy_(s["o"], non_blocking=True)
+            hht.copy_(s["ht"], non_blocking=True)
+        self.ev_out[i].record(self.s_out)
+        self.n += 1
+
+    def synchronize(self):
+        for st in self.streams():
+            st.synchronize()
+
+
 def chunk_gated_delta_rule_bwd(q, k, v, g_cumsum, beta, A, dO, *, h0=None, dht=None, scale=None,
                                use_exp2=False, cu_seqlens=None, varlen=None, stream=None):
     """Chunked backward; returns dq, dk, dv, dbeta, dg (raw gate) and dh0."""
