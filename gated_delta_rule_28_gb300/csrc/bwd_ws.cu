@@ -176,7 +176,7 @@ __global__ void __launch_bounds__(NTH, 1) tc_dhu_kernel(BwdArgs a, const __grid_
   // the tensor); the gating and the factor scale (scale base^G) are zeroed there, and
   // beta = 0 removes them from w.
   const int ptid = tid - 256;
-  const bool loader = ptid == 32;
+  const bool loader = warp == 9;  // TMA loads, issued warp-collectively (tc.cuh)
   int64_t last_ld[2] = {-1, -1}, last_do = -1;  // loader: newest order index per barrier
   auto issue_qkx = [&](int64_t m) {  // Q, K, X and the gate table of order index m
     const int64_t c = chunk_of(m);
@@ -186,19 +186,19 @@ __global__ void __launch_bounds__(NTH, 1) tc_dhu_kernel(BwdArgs a, const __grid_
     const int y = (int)(r0 + c * GDN_CHUNK);
     const int64_t xs = (xbase + c) * H + h;
     uint64_t *bar = &st.bar_ld[s2];
-    mbar_expect_tx(bar, 5 * 8192 + F_ROWS * GDN_CHUNK * 4);
-    tma_load_2d(stg, &maps.q, h * GDN_DK, y, bar);  // rows 0..63: Q
-    tma_load_2d(stg + 16384, &maps.q, h * GDN_DK + 64, y, bar);
-    tma_load_2d(stg + 8192, &maps.k, h * GDN_DK, y, bar);  // rows 64..127: K
-    tma_load_2d(stg + 16384 + 8192, &maps.k, h * GDN_DK + 64, y, bar);
-    tma_load_2d(xt, &maps.x, 0, (int)(xs * 2 * GDN_CHUNK + GDN_CHUNK), bar);  // X diag(b e^G)
-    bulk_load(smem_u32(&st.tab[s2][0][0]), a.ftab + xs * F_TAB, F_ROWS * GDN_CHUNK * 4, bar);
+    mbar_expect_tx_w(bar, 5 * 8192 + F_ROWS * GDN_CHUNK * 4);
+    tma_load_2d_w(stg, &maps.q, h * GDN_DK, y, bar);  // rows 0..63: Q
+    tma_load_2d_w(stg + 16384, &maps.q, h * GDN_DK + 64, y, bar);
+    tma_load_2d_w(stg + 8192, &maps.k, h * GDN_DK, y, bar);  // rows 64..127: K
+    tma_load_2d_w(stg + 16384 + 8192, &maps.k, h * GDN_DK + 64, y, bar);
+    tma_load_2d_w(xt, &maps.x, 0, (int)(xs * 2 * GDN_CHUNK + GDN_CHUNK), bar);  // X diag(b e^G)
+    bulk_load_w(smem_u32(&st.tab[s2][0][0]), a.ftab + xs * F_TAB, F_ROWS * GDN_CHUNK * 4, bar);
     last_ld[s2] = m;
   };
   auto issue_do = [&](int64_t m) {  // the CTA's 64 columns of dO
     const int64_t c = chunk_of(m);
-    mbar_expect_tx(&st.bar_do, 8192);
-    tma_load_2d(sb + OFF_DO, &maps.dO, h * GDN_DV + col0, (int)(r0 + c * GDN_CHUNK), &st.bar_do);
+    mbar_expect_tx_w(&st.bar_do, 8192);
+    tma_load_2d_w(sb + OFF_DO, &maps.dO, h * GDN_DV + col0, (int)(r0 + c * GDN_CHUNK), &st.bar_do);
     last_do = m;
   };
 
@@ -210,11 +210,11 @@ __global__ void __launch_bounds__(NTH, 1) tc_dhu_kernel(BwdArgs a, const __grid_
     const int n = chunk_rows(chunk_of(pm));
     if (loader && pm + 1 < nch) issue_qkx(pm + 1);
     wait_par(&st.bar_ld[ps], pm >> 1);  // Q, K, X and factors of this chunk have landed
-    if (ptid == 0) {  // P1: [Q; K] Q^T (rows 64..127 = K Q^T)
-      st.EL[ps] = tab[F_EG][63];
+    if (ptid == 0) st.EL[ps] = tab[F_EG][63];
+    if (warp == 8) {  // P1: [Q; K] Q^T (rows 64..127 = K Q^T), issued warp-collectively
       fence_after_sync();
-      mma_tiles(tmem + T_S + 64 * ps, stg, 16384, stg, 16384, 128, idesc_bf16(128, 64), false);
-      mma_commit(&st.bar_p1);
+      mma_tiles_w(tmem + T_S + 64 * ps, stg, 16384, stg, 16384, 128, idesc_bf16(128, 64), false);
+      mma_commit_w(&st.bar_p1);
     }
     __syncwarp();
     if (ptid < 64) st.seg[ps][ptid] = ptid < n ? scale * tab[F_EG][ptid] : 0.f;
@@ -285,16 +285,16 @@ __global__ void __launch_bounds__(NTH, 1) tc_dhu_kernel(BwdArgs a, const __grid_
     fence_proxy_async();
     fence_before_sync();
     prod_sync();
-    if (ptid == 0) {  // the h-independent products
+    if (warp == 8) {  // the h-independent products
       fence_after_sync();
       const uint32_t xt = sb + (ps ? OFF_X1 : OFF_X0);
       // scale A_qk^T dO  (rows 64..127 of the operand are not used)
-      mma_tiles(tmem + T_I1 + 64 * ps, sb + OFF_AQT, 8192, sb + OFF_DOT, 8192, 64, idesc_bf16(128, 64), false);
+      mma_tiles_w(tmem + T_I1 + 64 * ps, sb + OFF_AQT, 8192, sb + OFF_DOT, 8192, 64, idesc_bf16(128, 64), false);
       // scale Qg^T dO
-      mma_tiles(tmem + T_I2 + 64 * ps, sb + OFF_QGT, 16384, sb + OFF_DOT, 8192, 64, idesc_bf16(128, 64), false);
+      mma_tiles_w(tmem + T_I2 + 64 * ps, sb + OFF_QGT, 16384, sb + OFF_DOT, 8192, 64, idesc_bf16(128, 64), false);
       // w^T = K^T (X diag(beta base^G))^T: the stage's K rows read as an MN-major A
-      mma_ops(tmem + T_WT, mnmaj(stg + 8192, 16384), kmaj(xt, 0), 64, idesc_bf16(128, 64, false, true, false), false);
-      mma_commit(&st.bar_p3);
+      mma_ops_w(tmem + T_WT, mnmaj(stg + 8192, 16384), kmaj(xt, 0), 64, idesc_bf16(128, 64, false, true, false), false);
+      mma_commit_w(&st.bar_p3);
     }
     __syncwarp();
     if (loader && pm + 1 < nch) issue_do(pm + 1);  // dO consumed by the transposes
@@ -358,10 +358,10 @@ __global__ void __launch_bounds__(NTH, 1) tc_dhu_kernel(BwdArgs a, const __grid_
 #pragma unroll
       for (int g4 = 0; g4 < 8; ++g4) dst[g4] = make_float4(dh[4 * g4], dh[4 * g4 + 1], dh[4 * g4 + 2], dh[4 * g4 + 3]);
     }
-    if (tid == 0) {  // D1: dv_new = kgl dh + scale A_qk^T dO
+    if (warp == 0) {  // D1: dv_new = kgl dh + scale A_qk^T dO
       fence_after_sync();
-      mma_tiles(tmem + T_I1 + 64 * cs, sb + OFF_KGL, 8192, sb + OFF_DHT, 8192, 128, idesc_bf16(128, 64), true);
-      mma_commit(&st.bar_d1);
+      mma_tiles_w(tmem + T_I1 + 64 * cs, sb + OFF_KGL, 8192, sb + OFF_DHT, 8192, 128, idesc_bf16(128, 64), true);
+      mma_commit_w(&st.bar_d1);
     }
     __syncwarp();
     wait_par(&st.bar_d1, m);
@@ -386,10 +386,10 @@ __global__ void __launch_bounds__(NTH, 1) tc_dhu_kernel(BwdArgs a, const __grid_
     fence_proxy_async();
     fence_before_sync();
     chain_sync();
-    if (tid == 0) {  // D2: dh increment = scale Qg^T dO - w^T dv_new
+    if (warp == 0) {  // D2: dh increment = scale Qg^T dO - w^T dv_new
       fence_after_sync();
-      mma_tiles(tmem + T_I2 + 64 * cs, sb + OFF_WT, 16384, sb + OFF_DVT, 8192, 64, idesc_bf16(128, 64, true), true);
-      mma_commit(&st.bar_d2);
+      mma_tiles_w(tmem + T_I2 + 64 * cs, sb + OFF_WT, 16384, sb + OFF_DVT, 8192, 64, idesc_bf16(128, 64, true), true);
+      mma_commit_w(&st.bar_d2);
     }
     __syncwarp();
     wait_par(&st.bar_d2, m);
@@ -438,13 +438,12 @@ __global__ void __launch_bounds__(NTH, 1) tc_dhu_kernel(BwdArgs a, const __grid_
   }
 
   if (bad) {
-    if (tid == 0) {
-      raise_device_flag(a.dev_flag, kDevTimeout);
-      mma_commit(&st.bar_x0);  // arrives once every MMA this thread issued has finished
-    }
-    if (tid == 256) mma_commit(&st.bar_x1);
-    if (tid == 0) mbar_wait(&st.bar_x0, 0, WAIT_LIMIT);
-    if (tid == 256) mbar_wait(&st.bar_x1, 0, WAIT_LIMIT);
+    if (tid == 0) raise_device_flag(a.dev_flag, kDevTimeout);
+    // each issuing warp's elected lane: arrives once every MMA it issued has finished
+    if (warp == 0) mma_commit_w(&st.bar_x0);
+    if (warp == 8) mma_commit_w(&st.bar_x1);
+    if (warp == 0) mbar_wait(&st.bar_x0, 0, WAIT_LIMIT);
+    if (warp == 8) mbar_wait(&st.bar_x1, 0, WAIT_LIMIT);
     if (loader) {  // copies still in flight land before the CTA leaves
       for (int s2 = 0; s2 < 2; ++s2)
         if (last_ld[s2] >= 0) mbar_wait(&st.bar_ld[s2], (uint32_t)((last_ld[s2] >> 1) & 1), WAIT_LIMIT);

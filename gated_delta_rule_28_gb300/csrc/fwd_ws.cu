@@ -219,7 +219,7 @@ __global__ void __launch_bounds__(NTH, 1) tc_fwd_ws_kernel(SimtFwdArgs a, const 
   // ---- producer: one chunk -------------------------------------------------------------
   // warps 8, 9, 12, 13 (lane quarters 0, 1): gating of Q K^T; warps 10, 11, 14, 15
   // (quarters 2, 3): the w rows of the P4 operand.
-  auto produce = [&](int64_t pc, int64_t c_chain) {
+  auto produce = [&](int64_t pc) {
     const int ps = (int)(pc & 1);
     const float(&tab)[F_ROWS][64] = st.tab[ps];
     // buffers of chunk pc+1 (they held chunk pc-1, and K chunk pc-2: finished, P4 included)
@@ -431,7 +431,7 @@ __global__ void __launch_bounds__(NTH, 1) tc_fwd_ws_kernel(SimtFwdArgs a, const 
   // round c: the chain runs chunk c while the producer prepares chunk c+1
   for (int64_t c = -1; c < nch; ++c) {
     if (producer) {
-      if (c + 1 < nch) produce(c + 1, c);
+      if (c + 1 < nch) produce(c + 1);
     } else if (c >= 0) {
       chain(c);
     }

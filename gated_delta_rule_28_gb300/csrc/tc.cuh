@@ -131,43 +131,7 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool negate_a = 
          ((b_mn ? 1u : 0u) << 16) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
-__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
-                                         uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
-      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
-__device__ __forceinline__ void mma_commit(uint64_t *bar) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-          smem_u32(bar))
-      : "memory");
-}
-
-// D[M x N] (+)= A[M x K] B[N x K]^T for K a multiple of 64: A and B are
-// consecutive 64-wide K-blocks of swizzled tiles (a_kb / b_kb bytes apart).
-// The descriptor of every K step is the first one plus the step's byte offset
-// in the 14-bit start-address field (addresses stay below 256 KB, so the add
-// never carries out of the field).
-__device__ __forceinline__ void mma_tiles(uint32_t d_tmem, uint32_t a_saddr, uint32_t a_kb,
-                                          uint32_t b_saddr, uint32_t b_kb, int K, uint32_t idesc,
-                                          bool accumulate) {
-  const uint64_t a0 = sdesc_sw128(a_saddr), b0 = sdesc_sw128(b_saddr);
-#pragma unroll
-  for (int kb = 0; kb < K / 64; ++kb) {
-#pragma unroll
-    for (int s = 0; s < 4; ++s) {
-      const uint64_t ad = a0 + ((uint64_t)(kb * a_kb + s * 32) >> 4);
-      const uint64_t bd = b0 + ((uint64_t)(kb * b_kb + s * 32) >> 4);
-      mma_bf16(d_tmem, ad, bd, idesc, (accumulate || kb > 0 || s > 0) ? 1u : 0u);
-    }
-  }
-}
-
-// One operand of mma_ops: a swizzled tile at `addr`. K-major: 64-wide K-blocks `step` bytes
+// One operand of mma_ops_w: a swizzled tile at `addr`. K-major: 64-wide K-blocks `step` bytes
 // apart (a 16-element K step moves 32 bytes inside the block). MN-major: K rows of 128 bytes
 // (a 16-element K step moves 2048 bytes), `step` = bytes to the next 64 along M / N.
 struct Opnd {
@@ -176,20 +140,6 @@ struct Opnd {
 };
 __device__ __forceinline__ Opnd kmaj(uint32_t addr, uint32_t kb) { return Opnd{addr, kb, false}; }
 __device__ __forceinline__ Opnd mnmaj(uint32_t addr, uint32_t lbo) { return Opnd{addr, lbo, true}; }
-
-// D[M x N] (+)= A[M x K] B[N x K]^T for K a multiple of 16, either operand K- or MN-major
-// (the instruction descriptor must say which, idesc_bf16's a_mn / b_mn)
-__device__ __forceinline__ void mma_ops(uint32_t d_tmem, Opnd A, Opnd B, int K, uint32_t idesc,
-                                        bool accumulate) {
-  const uint64_t a0 = A.mn ? sdesc_sw128_mn(A.addr, A.step) : sdesc_sw128(A.addr);
-  const uint64_t b0 = B.mn ? sdesc_sw128_mn(B.addr, B.step) : sdesc_sw128(B.addr);
-#pragma unroll
-  for (int ks = 0; ks < K / 16; ++ks) {
-    const uint32_t ao = A.mn ? (uint32_t)ks * 2048u : (uint32_t)(ks >> 2) * A.step + (uint32_t)(ks & 3) * 32u;
-    const uint32_t bo = B.mn ? (uint32_t)ks * 2048u : (uint32_t)(ks >> 2) * B.step + (uint32_t)(ks & 3) * 32u;
-    mma_bf16(d_tmem, a0 + (ao >> 4), b0 + (bo >> 4), idesc, (accumulate || ks > 0) ? 1u : 0u);
-  }
-}
 
 // ---------------------------------------------------------------------------
 // Warp-collective issue: called by all 32 lanes of a warp with warp-uniform
@@ -211,7 +161,8 @@ __device__ __forceinline__ void mma_commit_w(uint64_t *bar) {
       " @e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n}\n" ::"r"(smem_u32(bar))
       : "memory");
 }
-// mma_ops, warp-collective
+// D[M x N] (+)= A[M x K] B[N x K]^T for K a multiple of 16, either operand K- or MN-major
+// (the instruction descriptor must say which, idesc_bf16's a_mn / b_mn); warp-collective
 __device__ __forceinline__ void mma_ops_w(uint32_t d_tmem, Opnd A, Opnd B, int K, uint32_t idesc, bool accumulate) {
   const uint64_t a0 = A.mn ? sdesc_sw128_mn(A.addr, A.step) : sdesc_sw128(A.addr);
   const uint64_t b0 = B.mn ? sdesc_sw128_mn(B.addr, B.step) : sdesc_sw128(B.addr);
@@ -222,36 +173,16 @@ __device__ __forceinline__ void mma_ops_w(uint32_t d_tmem, Opnd A, Opnd B, int K
     mma_bf16_w(d_tmem, a0 + (ao >> 4), b0 + (bo >> 4), idesc, (accumulate || ks > 0) ? 1u : 0u);
   }
 }
-// mma_tiles, warp-collective
+// both operands K-major: consecutive 64-wide K-blocks a_kb / b_kb bytes apart; warp-collective
 __device__ __forceinline__ void mma_tiles_w(uint32_t d_tmem, uint32_t a_saddr, uint32_t a_kb, uint32_t b_saddr,
                                             uint32_t b_kb, int K, uint32_t idesc, bool accumulate) {
   mma_ops_w(d_tmem, kmaj(a_saddr, a_kb), kmaj(b_saddr, b_kb), K, idesc, accumulate);
 }
 
-// ---------------------------------------------------------------------------
-// TMA: tensor tiles and plain bulk copies into shared memory, completing on an
-// mbarrier that the issuing thread armed with the expected byte count
-__device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
-               : "memory");
-}
-// box of a 2-D tensor map at element coordinates (x = innermost, y); x * 2 bytes
-// must be a multiple of 16 (every caller passes a multiple of 64 elements)
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const void *map, int x, int y, uint64_t *bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
-          dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
-      : "memory");
-}
-// contiguous copy; both addresses 16-byte aligned, bytes a multiple of 16
-__device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes, uint64_t *bar) {
-  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
-               "l"(src), "r"(bytes), "r"(smem_u32(bar))
-               : "memory");
-}
-
-// TMA, warp-collective (see mma_bf16_w)
+// TMA (warp-collective, as above): tensor tiles and plain bulk copies into shared memory,
+// completing on an mbarrier armed with the expected byte count. A tile's x coordinate times
+// 2 bytes must be a multiple of 16 (every caller passes a multiple of 64 elements); a bulk
+// copy wants both addresses 16-byte aligned and a size that is a multiple of 16.
 __device__ __forceinline__ void mbar_expect_tx_w(uint64_t *bar, uint32_t bytes) {
   asm volatile(
       "{\n .reg .pred e;\n elect.sync _|e, 0xffffffff;\n"
