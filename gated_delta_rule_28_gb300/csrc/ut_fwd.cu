@@ -37,8 +37,8 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a
 // Persistent: each CTA walks the (chunk, head) items with a stride of the grid,
 // loading the next item's keys while it works on the current one.
 template <bool E2>
-__global__ void __launch_bounds__(128, 4) ut_kernel(UtArgs a, int64_t items) {
-  __shared__ __align__(1024) uint8_t kbuf[2][16384];  // keys (64 rows x 2 K-blocks, swizzled);
+__global__ void __launch_bounds__(128, 6) ut_kernel(UtArgs a, int64_t items) {
+  __shared__ __align__(1024) uint8_t kbuf[1][16384];  // keys (64 rows x 2 K-blocks, swizzled);
                                                       // the current one then holds L's blocks
   __shared__ __align__(16) float XB[10 * 256], TB[4 * 256];
   __shared__ __align__(16) float sg[64];
@@ -104,11 +104,11 @@ __global__ void __launch_bounds__(128, 4) ut_kernel(UtArgs a, int64_t items) {
       bv = __bfloat162float(beta[(rr + tid) * H + hh]);
     }
   };
-  int buf = 0;
+  const int buf = 0;
   float ng, nb;
-  load_keys(blockIdx.x, 0);
   load_gb(blockIdx.x, ng, nb);
-  for (int64_t it = blockIdx.x; it < items; it += gridDim.x, buf ^= 1) {
+  for (int64_t it = blockIdx.x; it < items; it += gridDim.x) {
+    load_keys(it, buf);
     int64_t r0 = 0;
     int n = 0;
     const bool ok = locate(it, r0, n);
@@ -120,7 +120,6 @@ __global__ void __launch_bounds__(128, 4) ut_kernel(UtArgs a, int64_t items) {
     }
     cp_async_wait<0>();
     __syncthreads();
-    load_keys(it + gridDim.x, buf ^ 1);
     load_gb(it + gridDim.x, ng, nb);
     if (!ok) {
       if (tid == 0) raise_device_flag(a.dev_flag, kDevCheck);
