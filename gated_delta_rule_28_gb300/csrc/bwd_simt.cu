@@ -15,6 +15,8 @@
 //  3. local: per (chunk, head), with the whole value width, the adjoint of the
 //     chunk's UT transform, gates and Gram matrices, giving dq, dk, dv, dbeta
 //     and dg (reverse in-chunk cumulative sum: the gradient of the raw gate).
+#include <type_traits>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -456,6 +458,19 @@ __global__ void __launch_bounds__(NTH, 1) local_kernel(BwdArgs a) {
   zero_acc(aQg);
   zero_acc(aKg);
   zero_acc(aKl);
+  // bf16 inputs: the five value contractions below run on tf32 tensor cores (mma.sync), each
+  // warp owning rows 16 (warp % 4) .. +15 and a quarter-width column block; their fragments
+  // are moved into the thread tiles above after the pass (fp32 inputs keep the FMA path,
+  // whose error bound is tighter than tf32 rounding)
+  constexpr bool TC = !std::is_same<T, float>::value;
+  const int wr0 = 16 * ((tid >> 5) & 3), lane = tid & 31;
+  const int wc128 = 64 * (tid >> 7), wc64 = 32 * (tid >> 7);
+  float fQg[8][4], fKg[8][4], fKl[8][4], fX[4][4], fQk[4][4];
+  zero_acc(fQg);
+  zero_acc(fKg);
+  zero_acc(fKl);
+  zero_acc(fX);
+  zero_acc(fQk);
   for (int vs = 0; vs < GDN_DV; vs += LBV) {
     for (int idx = tid; idx < 128 * LBV; idx += NTH) {
       const int d = idx / LBV, c = idx % LBV;
@@ -521,27 +536,53 @@ __global__ void __launch_bounds__(NTH, 1) local_kernel(BwdArgs a) {
       sDGLh[tid] += acc;
     }
     __syncthreads();
-    // dX += dv_new Z^T ; dA_qk += scale dO v_new^T
+    // dX += dv_new Z^T ; dA_qk += scale dO v_new^T ; dQg += dO h^T ; dKg += dY h^T ;
+    // dkgl += v_new dh^T
     {
-      auto fa = [&](int m, int kk) { return sDDs[m * LVP + kk]; };
-      auto fb = [&](int kk, int nn) { return sZs[nn * LVP + kk]; };
-      mm_acc<64, 64, LBV, 4, 4>(fa, fb, aX, tid);
-      auto fa2 = [&](int m, int kk) { return sDOs[m * LVP + kk]; };
-      auto fb2 = [&](int kk, int nn) { return sDels[nn * LVP + kk]; };
-      mm_acc<64, 64, LBV, 4, 4>(fa2, fb2, aQk, tid);
-    }
-    // dQg += dO h^T ; dKg += dY h^T ; dkgl += v_new dh^T
-    {
+      auto fdd = [&](int m, int kk) { return sDDs[m * LVP + kk]; };
+      auto fz = [&](int kk, int nn) { return sZs[nn * LVP + kk]; };
       auto fo = [&](int m, int kk) { return sDOs[m * LVP + kk]; };
+      auto fdl = [&](int kk, int nn) { return sDels[nn * LVP + kk]; };
       auto fy = [&](int m, int kk) { return sDYs[m * LVP + kk]; };
       auto fd = [&](int m, int kk) { return sDels[m * LVP + kk]; };
       auto fh = [&](int kk, int nn) { return sHs[nn * LVP + kk]; };
       auto fdh = [&](int kk, int nn) { return sDHs[nn * LVP + kk]; };
-      mm_acc<64, 128, LBV, 4, 8>(fo, fh, aQg, tid);
-      mm_acc<64, 128, LBV, 4, 8>(fy, fh, aKg, tid);
-      mm_acc<64, 128, LBV, 4, 8>(fd, fdh, aKl, tid);
+      if constexpr (TC) {
+        mma_tf32_acc<LBV, 4>(fdd, fz, fX, wr0, wc64, lane);
+        mma_tf32_acc<LBV, 4>(fo, fdl, fQk, wr0, wc64, lane);
+        mma_tf32_acc<LBV, 8>(fo, fh, fQg, wr0, wc128, lane);
+        mma_tf32_acc<LBV, 8>(fy, fh, fKg, wr0, wc128, lane);
+        mma_tf32_acc<LBV, 8>(fd, fdh, fKl, wr0, wc128, lane);
+      } else {
+        mm_acc<64, 64, LBV, 4, 4>(fdd, fz, aX, tid);
+        mm_acc<64, 64, LBV, 4, 4>(fo, fdl, aQk, tid);
+        mm_acc<64, 128, LBV, 4, 8>(fo, fh, aQg, tid);
+        mm_acc<64, 128, LBV, 4, 8>(fy, fh, aKg, tid);
+        mm_acc<64, 128, LBV, 4, 8>(fd, fdh, aKl, tid);
+      }
     }
     __syncthreads();
+  }
+
+  if constexpr (TC) {  // tensor-core fragments -> the thread tiles, through the slice region
+    constexpr int LD = GDN_DK + 1;
+    float *st = sSl;  // [64][LD], free after the pass
+    auto to_tiles = [&](auto &frag, auto &tile, int c0, int tm0, int tn0) {
+      mma_frag_store(st, LD, frag, wr0, c0, lane);
+      __syncthreads();
+      constexpr int TMv = sizeof(tile) / sizeof(tile[0]);
+      constexpr int TNv = sizeof(tile[0]) / sizeof(float);
+#pragma unroll
+      for (int x = 0; x < TMv; ++x)
+#pragma unroll
+        for (int y = 0; y < TNv; ++y) tile[x][y] = st[(tm0 + x) * LD + tn0 + y];
+      __syncthreads();
+    };
+    to_tiles(fX, aX, wc64, pm0, pn0);
+    to_tiles(fQk, aQk, wc64, pm0, pn0);
+    to_tiles(fQg, aQg, wc128, gm0, gn0);
+    to_tiles(fKg, aKg, wc128, gm0, gn0);
+    to_tiles(fKl, aKl, wc128, gm0, gn0);
   }
 
   // ---- dL = -X^T dX X^T ; dbeta ; dP ------------------------------------------

@@ -76,6 +76,48 @@ __device__ __forceinline__ void mm_acc(FA fa, FB fb, float (&acc)[TM][TN], int t
   }
 }
 
+// Warp-level tf32 tensor-core product over fp32 shared-memory operands (mma.sync
+// m16n8k8, fp32 accumulation): the warp's 16 x (8 NT) block of an output at rows
+// r0 .. r0+15 and columns c0 .. c0+8NT-1, acc[j] holding the fragment of columns
+// c0+8j .. +7 (thread: rows r0 + lane/4 (+8), columns 2(lane%4) (+1)), accumulated over
+// KD (a multiple of 8) steps of fa(m, kk) fb(kk, n). The operands are rounded to tf32.
+__device__ __forceinline__ uint32_t to_tf32(float x) {
+  uint32_t r;
+  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+  return r;
+}
+template <int KD, int NT, class FA, class FB>
+__device__ __forceinline__ void mma_tf32_acc(FA fa, FB fb, float (&acc)[NT][4], int r0, int c0, int lane) {
+  const int g = lane >> 2, t = lane & 3;
+#pragma unroll
+  for (int k0 = 0; k0 < KD; k0 += 8) {
+    const uint32_t a0 = to_tf32(fa(r0 + g, k0 + t)), a1 = to_tf32(fa(r0 + g + 8, k0 + t));
+    const uint32_t a2 = to_tf32(fa(r0 + g, k0 + t + 4)), a3 = to_tf32(fa(r0 + g + 8, k0 + t + 4));
+#pragma unroll
+    for (int j = 0; j < NT; ++j) {
+      const uint32_t b0 = to_tf32(fb(k0 + t, c0 + 8 * j + g)), b1 = to_tf32(fb(k0 + t + 4, c0 + 8 * j + g));
+      asm volatile(
+          "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+          "{%0,%1,%2,%3};"
+          : "+f"(acc[j][0]), "+f"(acc[j][1]), "+f"(acc[j][2]), "+f"(acc[j][3])
+          : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+    }
+  }
+}
+// store such a fragment block into a row-major shared-memory matrix (row stride ld floats)
+template <int NT>
+__device__ __forceinline__ void mma_frag_store(float *dst, int ld, const float (&acc)[NT][4], int r0, int c0, int lane) {
+  const int g = lane >> 2, t = lane & 3;
+#pragma unroll
+  for (int j = 0; j < NT; ++j) {
+    const int c = c0 + 8 * j + 2 * t;
+    dst[(r0 + g) * ld + c] = acc[j][0];
+    dst[(r0 + g) * ld + c + 1] = acc[j][1];
+    dst[(r0 + g + 8) * ld + c] = acc[j][2];
+    dst[(r0 + g + 8) * ld + c + 1] = acc[j][3];
+  }
+}
+
 template <int M, int N, int TM, int TN>
 __device__ __forceinline__ void tile_origin(int tid, int& m0, int& n0) {
   m0 = (tid / (N / TN)) * TM;
