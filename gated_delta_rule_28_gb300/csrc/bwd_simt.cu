@@ -673,20 +673,39 @@ __global__ void __launch_bounds__(NTH, 1) local_kernel(BwdArgs a) {
     const float *Op = which == 3 ? sQ : sK;
     float t[4][8];
     zero_acc(t);
-    for (int j = 0; j < GDN_CHUNK; ++j) {
+    if constexpr (TC && !PER_KEY) {
+      // the gate is already folded into the 64 x 64 matrix: a plain product, on tf32 tensor
+      // cores, moved into the thread tile through the slice region
+      constexpr int LD = GDN_DK + 1;
+      float *st = sSl;
+      float fr[8][4];
+      zero_acc(fr);
+      auto fm = [&](int m, int kk) { return tr ? Mx[kk * CP + m] : Mx[m * CP + kk]; };
+      auto fop = [&](int kk, int nn) { return Op[kk * KP + nn]; };
+      mma_tf32_acc<GDN_CHUNK, 8>(fm, fop, fr, wr0, wc128, lane);
+      mma_frag_store(st, LD, fr, wr0, wc128, lane);
+      __syncthreads();
 #pragma unroll
-      for (int x = 0; x < 4; ++x) {
-        const int i = gm0 + x;
-        const float m = tr ? Mx[j * CP + i] : Mx[i * CP + j];
-        if (m == 0.f) continue;
+      for (int x = 0; x < 4; ++x)
 #pragma unroll
-        for (int y = 0; y < 8; ++y) {
-          const int d = gn0 + y;
-          float w = m * Op[j * KP + d];
-          if (PER_KEY)
-            w *= tr ? gate_pow(sG[j * KP + d] - sG[i * KP + d], e2)
-                    : gate_pow(sG[i * KP + d] - sG[j * KP + d], e2);
-          t[x][y] += w;
+        for (int y = 0; y < 8; ++y) t[x][y] = st[(gm0 + x) * LD + gn0 + y];
+      __syncthreads();
+    } else {
+      for (int j = 0; j < GDN_CHUNK; ++j) {
+#pragma unroll
+        for (int x = 0; x < 4; ++x) {
+          const int i = gm0 + x;
+          const float m = tr ? Mx[j * CP + i] : Mx[i * CP + j];
+          if (m == 0.f) continue;
+#pragma unroll
+          for (int y = 0; y < 8; ++y) {
+            const int d = gn0 + y;
+            float w = m * Op[j * KP + d];
+            if (PER_KEY)
+              w *= tr ? gate_pow(sG[j * KP + d] - sG[i * KP + d], e2)
+                      : gate_pow(sG[i * KP + d] - sG[j * KP + d], e2);
+            t[x][y] += w;
+          }
         }
       }
     }
