@@ -399,6 +399,14 @@ __global__ void __launch_bounds__(NTH, 1) local_kernel(BwdArgs a) {
     return PER_KEY ? gate_pow(sG[63 * KP + d] - sG[i * KP + d], e2) : sG[128 + i];
   };
 
+  // bf16 inputs: the chunk's dense contractions run on tf32 tensor cores (mma.sync), each warp
+  // owning rows 16 (warp % 4) .. +15 and a quarter-width column block of an output; fp32
+  // inputs keep the FMA path, whose error bound is tighter than tf32 rounding
+  constexpr bool TC = !std::is_same<T, float>::value;
+  const int wr0 = 16 * ((tid >> 5) & 3), lane = tid & 31;
+  const int wc128 = 64 * (tid >> 7), wc64 = 32 * (tid >> 7);
+  const int fg = lane >> 2, ft = lane & 3;  // this thread's fragment row / column pair
+
   // ---- gated Gram matrices ------------------------------------------------
   {
     int m0, n0;
@@ -406,7 +414,39 @@ __global__ void __launch_bounds__(NTH, 1) local_kernel(BwdArgs a) {
     float accP[4][4], accQ[4][4];
     zero_acc(accP);
     zero_acc(accQ);
-    if (n0 <= m0 + 3) {
+    if constexpr (TC && !PER_KEY) {  // K K^T and Q K^T on tensor cores, then gated per element
+      constexpr int LD = GDN_CHUNK + 1;
+      float *st = sSl;  // [64][LD] staging, the slice region is not in use yet
+      float fP[4][4], fQ[4][4];
+      zero_acc(fP);
+      zero_acc(fQ);
+      auto fk = [&](int m, int kk) { return sK[m * KP + kk]; };
+      auto fq = [&](int m, int kk) { return sQ[m * KP + kk]; };
+      auto fkt = [&](int kk, int nn) { return sK[nn * KP + kk]; };
+      mma_tf32_acc<GDN_DK, 4>(fk, fkt, fP, wr0, wc64, lane);
+      mma_tf32_acc<GDN_DK, 4>(fq, fkt, fQ, wr0, wc64, lane);
+      mma_frag_store(st, LD, fP, wr0, wc64, lane);
+      __syncthreads();
+#pragma unroll
+      for (int x = 0; x < 4; ++x)
+#pragma unroll
+        for (int y = 0; y < 4; ++y) accP[x][y] = st[(m0 + x) * LD + n0 + y];
+      __syncthreads();
+      mma_frag_store(st, LD, fQ, wr0, wc64, lane);
+      __syncthreads();
+#pragma unroll
+      for (int x = 0; x < 4; ++x)
+#pragma unroll
+        for (int y = 0; y < 4; ++y) accQ[x][y] = st[(m0 + x) * LD + n0 + y];
+#pragma unroll
+      for (int x = 0; x < 4; ++x)
+#pragma unroll
+        for (int y = 0; y < 4; ++y) {
+          const float gam = n0 + y <= m0 + x ? gate_pow(sG[m0 + x] - sG[n0 + y], e2) : 0.f;
+          accP[x][y] *= gam;
+          accQ[x][y] *= gam;
+        }
+    } else if (n0 <= m0 + 3) {
       if (PER_KEY) {
         for (int d = 0; d < GDN_DK; ++d) {
 #pragma unroll
@@ -458,13 +498,8 @@ __global__ void __launch_bounds__(NTH, 1) local_kernel(BwdArgs a) {
   zero_acc(aQg);
   zero_acc(aKg);
   zero_acc(aKl);
-  // bf16 inputs: the five value contractions below run on tf32 tensor cores (mma.sync), each
-  // warp owning rows 16 (warp % 4) .. +15 and a quarter-width column block; their fragments
-  // are moved into the thread tiles above after the pass (fp32 inputs keep the FMA path,
-  // whose error bound is tighter than tf32 rounding)
-  constexpr bool TC = !std::is_same<T, float>::value;
-  const int wr0 = 16 * ((tid >> 5) & 3), lane = tid & 31;
-  const int wc128 = 64 * (tid >> 7), wc64 = 32 * (tid >> 7);
+  // tensor-core path: the five value contractions below accumulate as fragments, moved into
+  // the thread tiles above after the pass
   float fQg[8][4], fKg[8][4], fKl[8][4], fX[4][4], fQk[4][4];
   zero_acc(fQg);
   zero_acc(fKg);
@@ -492,7 +527,20 @@ __global__ void __launch_bounds__(NTH, 1) local_kernel(BwdArgs a) {
     }
     __syncthreads();
     // Z = beta (V - (K (.) base^G) h) ; also keep V - Y for dbeta
-    if (tid < 64 * LBV / 4) {
+    if constexpr (TC && !PER_KEY) {  // the 64 x 16 product on tensor cores, one tile per warp
+      const int zr0 = 16 * ((tid >> 5) & 3), zc0 = 8 * (tid >> 7);
+      float fz[1][4] = {{0.f, 0.f, 0.f, 0.f}};
+      auto fkg = [&](int m, int kk) { return sK[m * KP + kk] * sG[64 + m]; };
+      auto fhs = [&](int kk, int nn) { return sHs[kk * LVP + nn]; };
+      mma_tf32_acc<GDN_DK, 1>(fkg, fhs, fz, zr0, zc0, lane);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int i = zr0 + fg + 8 * (e >> 1), c = zc0 + 2 * ft + (e & 1);
+        const float r = sVs[i * LVP + c] - fz[0][e];
+        sZs[i * LVP + c] = sBeta[i] * r;
+        sVs[i * LVP + c] = r;  // V - Y
+      }
+    } else if (tid < 64 * LBV / 4) {
       const int i = tid / (LBV / 4), c4 = (tid % (LBV / 4)) * 4;
       float acc[4] = {0.f, 0.f, 0.f, 0.f};
       for (int d = 0; d < GDN_DK; ++d) {
@@ -509,7 +557,30 @@ __global__ void __launch_bounds__(NTH, 1) local_kernel(BwdArgs a) {
     }
     __syncthreads();
     // v_new = X Z ; dZ = X^T dv_new
-    if (tid < 64 * LBV / 4) {
+    if constexpr (TC && !PER_KEY) {  // both 64 x 16 products on tensor cores, one tile per warp
+      const int zr0 = 16 * ((tid >> 5) & 3), zc0 = 8 * (tid >> 7);
+      float fv[1][4] = {{0.f, 0.f, 0.f, 0.f}}, fd[1][4] = {{0.f, 0.f, 0.f, 0.f}};
+      auto fx = [&](int m, int kk) { return sX[m * CP + kk]; };
+      auto fxt = [&](int m, int kk) { return sX[kk * CP + m]; };
+      auto fzs = [&](int kk, int nn) { return sZs[kk * LVP + nn]; };
+      auto fdd = [&](int kk, int nn) { return sDDs[kk * LVP + nn]; };
+      mma_tf32_acc<GDN_CHUNK, 1>(fx, fzs, fv, zr0, zc0, lane);
+      mma_tf32_acc<GDN_CHUNK, 1>(fxt, fdd, fd, zr0, zc0, lane);
+#pragma unroll
+      for (int hr = 0; hr < 2; ++hr) {  // rows zr0 + fg and zr0 + fg + 8
+        const int i = zr0 + fg + 8 * hr;
+        float db = 0.f;
+#pragma unroll
+        for (int cc = 0; cc < 2; ++cc) {
+          const int e = 2 * hr + cc, c = zc0 + 2 * ft + cc;
+          sDels[i * LVP + c] = fv[0][e];
+          db = fmaf(fd[0][e], sVs[i * LVP + c], db);
+          sDYs[i * LVP + c] = -sBeta[i] * fd[0][e];
+          if (i < n) dv[((c0 + i) * H + h) * GDN_DV + vs + c] = from_f32<T>(sBeta[i] * fd[0][e]);
+        }
+        atomicAdd(&sDBeta[i], db);
+      }
+    } else if (tid < 64 * LBV / 4) {
       const int i = tid / (LBV / 4), c4 = (tid % (LBV / 4)) * 4;
       float acc[4] = {0.f, 0.f, 0.f, 0.f}, acc2[4] = {0.f, 0.f, 0.f, 0.f};
       for (int j = 0; j < GDN_CHUNK; ++j) {
