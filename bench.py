@@ -107,11 +107,16 @@ FWD_SOURCES = ("ut_fwd.cu", "fwd_ws.cu", "tile_ops.cuh", "tc.cuh")
 
 
 def fwd_source_sha256():
-    """Digest of the forward kernels' sources (the UT transform and the state kernel)."""
+    """Digest of the forward kernels' code (the UT transform and the state kernel): the
+    sources without // comments and blank lines, so that an edit of comments alone keeps
+    the recorded counters valid while any change of code voids them."""
     import hashlib
+    import re
     d = hashlib.sha256()
     for f in FWD_SOURCES:
-        d.update(open(os.path.join(ROOT, "gated_delta_rule_28_gb300", "csrc", f), "rb").read())
+        text = open(os.path.join(ROOT, "gated_delta_rule_28_gb300", "csrc", f)).read()
+        lines = (re.sub(r"//.*$", "", ln).rstrip() for ln in text.splitlines())
+        d.update("\n".join(ln for ln in lines if ln).encode())
     return d.hexdigest()
 
 

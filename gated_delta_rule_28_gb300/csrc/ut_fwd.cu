@@ -9,8 +9,9 @@
 // X has no dependence on the state, so it is computed here for every chunk
 // in parallel (persistent CTAs of 4 warps walking the (chunk, head) items; K K^T
 // on bf16 mma.sync, the solve in fp32 shared memory) and written in bf16 for the tensor-core
-// state kernel, which then only multiplies by it, with a table of the chunk's
-// per-token gate factors (GateTabRow: G, base^G, base^(G_last - G), beta base^G,
+// state kernel, scaled by its columns as the pair [X diag(beta); X diag(beta base^G)], so
+// that the state kernel only multiplies by it; with a table of the chunk's per-token gate
+// factors (GateTabRow: G, base^G, base^(G_last - G), beta base^G,
 // beta, and the two factors of the gate between 16-token blocks).
 // The fp32 X (the A output of the forward) and the cumulative gate are
 // written here when asked for.
@@ -34,12 +35,12 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-// Persistent: each CTA walks the (chunk, head) items with a stride of the grid,
-// loading the next item's keys while it works on the current one.
+// Persistent: each CTA walks the (chunk, head) items with a stride of the grid (six CTAs per
+// SM: one key buffer each), prefetching the next item's gate and beta into registers.
 template <bool E2>
 __global__ void __launch_bounds__(128, 6) ut_kernel(UtArgs a, int64_t items) {
   __shared__ __align__(1024) uint8_t kbuf[1][16384];  // keys (64 rows x 2 K-blocks, swizzled);
-                                                      // the current one then holds L's blocks
+                                                      // after K K^T it holds L's blocks
   __shared__ __align__(16) float XB[10 * 256], TB[4 * 256];
   __shared__ __align__(16) float sg[64];
   __shared__ __align__(16) float sG[64];
