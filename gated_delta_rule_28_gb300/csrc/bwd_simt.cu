@@ -669,15 +669,22 @@ __global__ void __launch_bounds__(NTH, 1) local_kernel(BwdArgs a) {
     }
   __syncthreads();
   {
-    float acc[4][4];
-    zero_acc(acc);
     auto fa = [&](int m, int kk) { return sDX[m * CP + kk]; };
     auto fb = [&](int kk, int nn) { return sX[nn * CP + kk]; };
-    mm_acc<64, 64, GDN_CHUNK, 4, 4>(fa, fb, acc, tid);  // dX X^T
+    if constexpr (TC) {  // dX X^T on tensor cores, fragments straight into sT1
+      float fr[4][4];
+      zero_acc(fr);
+      mma_tf32_acc<GDN_CHUNK, 4>(fa, fb, fr, wr0, wc64, lane);
+      mma_frag_store(sT1, CP, fr, wr0, wc64, lane);
+    } else {
+      float acc[4][4];
+      zero_acc(acc);
+      mm_acc<64, 64, GDN_CHUNK, 4, 4>(fa, fb, acc, tid);  // dX X^T
 #pragma unroll
-    for (int x = 0; x < 4; ++x)
+      for (int x = 0; x < 4; ++x)
 #pragma unroll
-      for (int y = 0; y < 4; ++y) sT1[(pm0 + x) * CP + pn0 + y] = acc[x][y];
+        for (int y = 0; y < 4; ++y) sT1[(pm0 + x) * CP + pn0 + y] = acc[x][y];
+    }
   }
   __syncthreads();
   {
@@ -685,7 +692,19 @@ __global__ void __launch_bounds__(NTH, 1) local_kernel(BwdArgs a) {
     zero_acc(acc);
     auto fa = [&](int m, int kk) { return sX[kk * CP + m]; };
     auto fb = [&](int kk, int nn) { return sT1[kk * CP + nn]; };
-    mm_acc<64, 64, GDN_CHUNK, 4, 4>(fa, fb, acc, tid);  // X^T (dX X^T)
+    if constexpr (TC) {  // X^T (dX X^T) on tensor cores, into the thread tile through sDX (free)
+      float fr[4][4];
+      zero_acc(fr);
+      mma_tf32_acc<GDN_CHUNK, 4>(fa, fb, fr, wr0, wc64, lane);
+      mma_frag_store(sDX, CP, fr, wr0, wc64, lane);
+      __syncthreads();
+#pragma unroll
+      for (int x = 0; x < 4; ++x)
+#pragma unroll
+        for (int y = 0; y < 4; ++y) acc[x][y] = sDX[(pm0 + x) * CP + pn0 + y];
+    } else {
+      mm_acc<64, 64, GDN_CHUNK, 4, 4>(fa, fb, acc, tid);  // X^T (dX X^T)
+    }
     float rows[4] = {0.f, 0.f, 0.f, 0.f};
     float dPv[4][4];
 #pragma unroll
