@@ -277,15 +277,31 @@ __global__ void __launch_bounds__(NTH) dhu_kernel(BwdArgs a) {
 constexpr int LBV = 16;
 constexpr int LVP = LBV + 1;
 
-template <bool PER_KEY>
+// Row strides (floats) of the local kernel's shared-memory matrices. The FMA path (fp32
+// inputs) pads rows by one float. The tensor-core path (bf16 inputs) reads mma fragments,
+// lane (g, t) at row g and column t (or transposed), so its strides are 4 mod 32: the
+// row-major fragment reads then hit 32 distinct banks, the transposed ones at most two lanes
+// per bank.
+template <typename T>
+struct LocalStrides {
+  static constexpr bool tc = !std::is_same<T, float>::value;
+  static constexpr int kp = tc ? GDN_DK + 4 : GDN_DK + 1;
+  static constexpr int cp = tc ? GDN_CHUNK + 4 : GDN_CHUNK + 1;
+  static constexpr int lvp = tc ? LBV + 4 : LBV + 1;
+};
+
+template <typename T, bool PER_KEY>
 constexpr size_t local_smem_floats() {
   // K, Q, (G), X, P, Aqk, slice buffers, beta, dbeta, EL, dGLh, dGlast, dGrow
-  return 2 * 64 * KP + (PER_KEY ? 64 * KP : 3 * 64) + 3 * 64 * CP +
-         (2 * 128 * LVP + 6 * 64 * LVP) + 64 + 64 + 128 + 128 + 128 + 64;
+  using S = LocalStrides<T>;
+  return 2 * 64 * S::kp + (PER_KEY ? 64 * S::kp : 3 * 64) + 3 * 64 * S::cp +
+         (2 * 128 * S::lvp + 6 * 64 * S::lvp) + 64 + 64 + 128 + 128 + 128 + 64;
 }
 
 template <typename T, bool PER_KEY>
 __global__ void __launch_bounds__(NTH, 1) local_kernel(BwdArgs a) {
+  // this kernel's strides (hide the namespace-scope ones)
+  constexpr int KP = LocalStrides<T>::kp, CP = LocalStrides<T>::cp, LVP = LocalStrides<T>::lvp;
   extern __shared__ float smem[];
   float *sK = smem;
   float *sQ = sK + 64 * KP;
@@ -415,7 +431,7 @@ __global__ void __launch_bounds__(NTH, 1) local_kernel(BwdArgs a) {
     zero_acc(accP);
     zero_acc(accQ);
     if constexpr (TC && !PER_KEY) {  // K K^T and Q K^T on tensor cores, then gated per element
-      constexpr int LD = GDN_CHUNK + 1;
+      constexpr int LD = GDN_CHUNK + 4;
       float *st = sSl;  // [64][LD] staging, the slice region is not in use yet
       float fP[4][4], fQ[4][4];
       zero_acc(fP);
@@ -636,7 +652,7 @@ __global__ void __launch_bounds__(NTH, 1) local_kernel(BwdArgs a) {
   }
 
   if constexpr (TC) {  // tensor-core fragments -> the thread tiles, through the slice region
-    constexpr int LD = GDN_DK + 1;
+    constexpr int LD = GDN_DK + 4;
     float *st = sSl;  // [64][LD], free after the pass
     auto to_tiles = [&](auto &frag, auto &tile, int c0, int tm0, int tn0) {
       mma_frag_store(st, LD, frag, wr0, c0, lane);
@@ -766,7 +782,7 @@ __global__ void __launch_bounds__(NTH, 1) local_kernel(BwdArgs a) {
     if constexpr (TC && !PER_KEY) {
       // the gate is already folded into the 64 x 64 matrix: a plain product, on tf32 tensor
       // cores, moved into the thread tile through the slice region
-      constexpr int LD = GDN_DK + 1;
+      constexpr int LD = GDN_DK + 4;
       float *st = sSl;
       float fr[8][4];
       zero_acc(fr);
@@ -882,7 +898,7 @@ cudaError_t dhu_one(const BwdArgs &a, cudaStream_t st) {
 
 template <typename T, bool PK>
 cudaError_t local_one(const BwdArgs &a, cudaStream_t st) {
-  const size_t bytes = local_smem_floats<PK>() * sizeof(float);
+  const size_t bytes = local_smem_floats<T, PK>() * sizeof(float);
   cudaError_t e = cudaFuncSetAttribute(local_kernel<T, PK>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
   if (e != cudaSuccess) return e;
   const int64_t nch = a.cu ? a.num_chunks : (int64_t)a.B * ((a.T + GDN_CHUNK - 1) / GDN_CHUNK);
