@@ -132,6 +132,24 @@ def _recorded_traffic():
     return None
 
 
+def max_over_ranks(seconds, device=None):
+    """The largest of the ranks' times, on every rank (the whole job ends with the slowest
+    rank); the local time when no process group is initialised. ``device`` is where the
+    reduction runs: the rank's GPU under NCCL, None (host) under gloo."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return float(seconds)
+    t = torch.tensor([float(seconds)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tokens_per_s(world, tokens_per_rank, steps, seconds):
+    """Whole-job throughput: every rank processes its own copy of the workload (weak scaling)."""
+    return world * tokens_per_rank * steps / seconds
+
+
 def _dist():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -324,11 +342,8 @@ def run_ours(args):
     Bd.gdn_device_status(sp)
     elapsed = start.elapsed_time(end) / 1e3
     kern = [a.elapsed_time(b) / 1e3 for a, b in ev]
-    if world > 1:
-        tt = torch.tensor([elapsed], device=dev)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        elapsed = float(tt.item())
-    value = world * tokens * args.steps / elapsed
+    elapsed = max_over_ranks(elapsed, dev)
+    value = job_tokens_per_s(world, tokens, args.steps, elapsed)
     kavg = sum(kern) / len(kern)
 
     # end to end with host buffers: every step copies its inputs in from pinned host memory
@@ -359,11 +374,8 @@ def run_ours(args):
     torch.cuda.synchronize()
     e2e_t = e0.elapsed_time(e1) / 1e3
     Bd.gdn_device_status(pipe.s_comp.cuda_stream)
-    if world > 1:
-        tt = torch.tensor([e2e_t], device=dev)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        e2e_t = float(tt.item())
-    e2e_value = world * tokens * args.steps / e2e_t
+    e2e_t = max_over_ranks(e2e_t, dev)
+    e2e_value = job_tokens_per_s(world, tokens, args.steps, e2e_t)
 
     hbm, tc, src = _peaks()
     alg_bytes = Bsz * T * H * BYTES_PER_TOKEN_HEAD + Bsz * H * STATE_BYTES
