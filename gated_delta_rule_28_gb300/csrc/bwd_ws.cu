@@ -63,6 +63,12 @@ constexpr int SMALL_BYTES = 6144;
 constexpr int GD_B = GD_BLOCK;
 constexpr int OFF_GD = OFF_SMALL + SMALL_BYTES;
 constexpr int SMEM_BYTES = OFF_GD + 4 * GD_B * 4 + 1024;
+// The MN-major K^T operand of w^T (the second stage's K rows: two 64-key groups 16 KB apart, 64
+// token rows) stays below the small state under either assignment of its descriptor's two
+// stride fields (groups 16 KB apart and K rows in 1 KB atoms, or the reverse).
+static_assert(OFF_ST + SZ_STAGE + 8192 + 16384 + 8 * 1024 <= OFF_SMALL &&
+                  OFF_ST + SZ_STAGE + 8192 + 1024 + 7 * 16384 + 1024 <= OFF_SMALL,
+              "MN-major K^T operand extent");
 static_assert(SMEM_BYTES <= 232448, "shared memory");
 
 constexpr uint32_t WAIT_LIMIT = 1u << 22;

@@ -63,6 +63,12 @@ constexpr int OFF_SMALL = OFF_AQ + 2 * 8192;
 constexpr int SMALL_BYTES = 6144;
 constexpr int SMEM_BYTES = OFF_SMALL + SMALL_BYTES + 1024;
 static_assert(SMEM_BYTES <= 232448, "shared memory");
+// The MN-major K operand (two 64-key groups 8 KB apart, 64 token rows) stays below the small
+// state under either assignment of its descriptor's two stride fields: groups 8 KB apart and
+// K rows in 1 KB atoms, or the reverse. The other MN-major operands have one group.
+static_assert(OFF_K + 2 * 16384 + 8192 + 8 * 1024 <= OFF_XX &&
+                  OFF_K + 2 * 16384 + 1024 + 7 * 8192 + 1024 <= OFF_SMALL,
+              "MN-major K operand extent");
 
 constexpr uint32_t WAIT_LIMIT = 1u << 22;
 
