@@ -171,8 +171,8 @@ gdn_status gdn_chunk_bwd(const gdn_problem *p, const void *q, const void *k, con
                          void *dv, float *dg, void *dbeta, float *dh0, void *ws,
                          size_t ws_bytes, void *stream);
 
-/* Backward without a caller workspace (the adapters this library follows have no counterpart; this is
- * a convenience of this library).
+/* Backward without a caller workspace (the adapters this library follows have
+ * no counterpart; this is a convenience of this library).
  * For callers that cannot allocate device memory: runtimes that plan every
  * device buffer at start-up and forbid allocation afterwards, and plugin
  * hosts that hand a library only its input and output buffers. Arguments,
