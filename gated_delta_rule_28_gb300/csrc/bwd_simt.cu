@@ -277,31 +277,34 @@ __global__ void __launch_bounds__(NTH) dhu_kernel(BwdArgs a) {
 constexpr int LBV = 16;
 constexpr int LVP = LBV + 1;
 
-// Row strides (floats) of the local kernel's shared-memory matrices. The FMA path (fp32
-// inputs) pads rows by one float. The tensor-core path (bf16 inputs) reads mma fragments,
-// lane (g, t) at row g and column t (or transposed), so its strides are 4 mod 32: the
-// row-major fragment reads then hit 32 distinct banks, the transposed ones at most two lanes
-// per bank.
-template <typename T>
+// Row strides (floats) of the local kernel's shared-memory matrices, and its value-slice
+// width. The FMA path (fp32 inputs) pads rows by one float. The tensor-core path (bf16
+// inputs) reads mma fragments, lane (g, t) at row g and column t (or transposed), so its
+// strides are 4 mod 32: the row-major fragment reads then hit 32 distinct banks, the
+// transposed ones at most two lanes per bank. With a scalar gate it also takes value slices
+// of 32 columns (half the slice rounds).
+template <typename T, bool PER_KEY>
 struct LocalStrides {
   static constexpr bool tc = !std::is_same<T, float>::value;
   static constexpr int kp = tc ? GDN_DK + 4 : GDN_DK + 1;
   static constexpr int cp = tc ? GDN_CHUNK + 4 : GDN_CHUNK + 1;
-  static constexpr int lvp = tc ? LBV + 4 : LBV + 1;
+  static constexpr int lbv = (tc && !PER_KEY) ? 2 * LBV : LBV;
+  static constexpr int lvp = tc ? lbv + 4 : lbv + 1;
 };
 
 template <typename T, bool PER_KEY>
 constexpr size_t local_smem_floats() {
   // K, Q, (G), X, P, Aqk, slice buffers, beta, dbeta, EL, dGLh, dGlast, dGrow
-  using S = LocalStrides<T>;
+  using S = LocalStrides<T, PER_KEY>;
   return 2 * 64 * S::kp + (PER_KEY ? 64 * S::kp : 3 * 64) + 3 * 64 * S::cp +
          (2 * 128 * S::lvp + 6 * 64 * S::lvp) + 64 + 64 + 128 + 128 + 128 + 64;
 }
 
 template <typename T, bool PER_KEY>
 __global__ void __launch_bounds__(NTH, 1) local_kernel(BwdArgs a) {
-  // this kernel's strides (hide the namespace-scope ones)
-  constexpr int KP = LocalStrides<T>::kp, CP = LocalStrides<T>::cp, LVP = LocalStrides<T>::lvp;
+  // this kernel's strides and slice width (hide the namespace-scope ones)
+  using LS = LocalStrides<T, PER_KEY>;
+  constexpr int KP = LS::kp, CP = LS::cp, LBV = LS::lbv, LVP = LS::lvp;
   extern __shared__ float smem[];
   float *sK = smem;
   float *sQ = sK + 64 * KP;
@@ -543,19 +546,23 @@ __global__ void __launch_bounds__(NTH, 1) local_kernel(BwdArgs a) {
     }
     __syncthreads();
     // Z = beta (V - (K (.) base^G) h) ; also keep V - Y for dbeta
-    if constexpr (TC && !PER_KEY) {  // the 64 x 16 product on tensor cores, one tile per warp
-      const int zr0 = 16 * ((tid >> 5) & 3), zc0 = 8 * (tid >> 7);
-      float fz[1][4] = {{0.f, 0.f, 0.f, 0.f}};
+    if constexpr (TC && !PER_KEY) {  // the 64 x LBV product on tensor cores, LBV/16 tiles per warp
+      constexpr int NZ = LBV / 16;
+      const int zr0 = 16 * ((tid >> 5) & 3), zc0 = (LBV / 2) * (tid >> 7);
+      float fz[NZ][4];
+      zero_acc(fz);
       auto fkg = [&](int m, int kk) { return sK[m * KP + kk] * sG[64 + m]; };
       auto fhs = [&](int kk, int nn) { return sHs[kk * LVP + nn]; };
-      mma_tf32_acc<GDN_DK, 1>(fkg, fhs, fz, zr0, zc0, lane);
+      mma_tf32_acc<GDN_DK, NZ>(fkg, fhs, fz, zr0, zc0, lane);
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int i = zr0 + fg + 8 * (e >> 1), c = zc0 + 2 * ft + (e & 1);
-        const float r = sVs[i * LVP + c] - fz[0][e];
-        sZs[i * LVP + c] = sBeta[i] * r;
-        sVs[i * LVP + c] = r;  // V - Y
-      }
+      for (int j = 0; j < NZ; ++j)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int i = zr0 + fg + 8 * (e >> 1), c = zc0 + 8 * j + 2 * ft + (e & 1);
+          const float r = sVs[i * LVP + c] - fz[j][e];
+          sZs[i * LVP + c] = sBeta[i] * r;
+          sVs[i * LVP + c] = r;  // V - Y
+        }
     } else if (tid < 64 * LBV / 4) {
       const int i = tid / (LBV / 4), c4 = (tid % (LBV / 4)) * 4;
       float acc[4] = {0.f, 0.f, 0.f, 0.f};
@@ -573,27 +580,32 @@ __global__ void __launch_bounds__(NTH, 1) local_kernel(BwdArgs a) {
     }
     __syncthreads();
     // v_new = X Z ; dZ = X^T dv_new
-    if constexpr (TC && !PER_KEY) {  // both 64 x 16 products on tensor cores, one tile per warp
-      const int zr0 = 16 * ((tid >> 5) & 3), zc0 = 8 * (tid >> 7);
-      float fv[1][4] = {{0.f, 0.f, 0.f, 0.f}}, fd[1][4] = {{0.f, 0.f, 0.f, 0.f}};
+    if constexpr (TC && !PER_KEY) {  // both 64 x LBV products on tensor cores, LBV/16 tiles per warp
+      constexpr int NZ = LBV / 16;
+      const int zr0 = 16 * ((tid >> 5) & 3), zc0 = (LBV / 2) * (tid >> 7);
+      float fv[NZ][4], fd[NZ][4];
+      zero_acc(fv);
+      zero_acc(fd);
       auto fx = [&](int m, int kk) { return sX[m * CP + kk]; };
       auto fxt = [&](int m, int kk) { return sX[kk * CP + m]; };
       auto fzs = [&](int kk, int nn) { return sZs[kk * LVP + nn]; };
       auto fdd = [&](int kk, int nn) { return sDDs[kk * LVP + nn]; };
-      mma_tf32_acc<GDN_CHUNK, 1>(fx, fzs, fv, zr0, zc0, lane);
-      mma_tf32_acc<GDN_CHUNK, 1>(fxt, fdd, fd, zr0, zc0, lane);
+      mma_tf32_acc<GDN_CHUNK, NZ>(fx, fzs, fv, zr0, zc0, lane);
+      mma_tf32_acc<GDN_CHUNK, NZ>(fxt, fdd, fd, zr0, zc0, lane);
 #pragma unroll
       for (int hr = 0; hr < 2; ++hr) {  // rows zr0 + fg and zr0 + fg + 8
         const int i = zr0 + fg + 8 * hr;
         float db = 0.f;
 #pragma unroll
-        for (int cc = 0; cc < 2; ++cc) {
-          const int e = 2 * hr + cc, c = zc0 + 2 * ft + cc;
-          sDels[i * LVP + c] = fv[0][e];
-          db = fmaf(fd[0][e], sVs[i * LVP + c], db);
-          sDYs[i * LVP + c] = -sBeta[i] * fd[0][e];
-          if (i < n) dv[((c0 + i) * H + h) * GDN_DV + vs + c] = from_f32<T>(sBeta[i] * fd[0][e]);
-        }
+        for (int j = 0; j < NZ; ++j)
+#pragma unroll
+          for (int cc = 0; cc < 2; ++cc) {
+            const int e = 2 * hr + cc, c = zc0 + 8 * j + 2 * ft + cc;
+            sDels[i * LVP + c] = fv[j][e];
+            db = fmaf(fd[j][e], sVs[i * LVP + c], db);
+            sDYs[i * LVP + c] = -sBeta[i] * fd[j][e];
+            if (i < n) dv[((c0 + i) * H + h) * GDN_DV + vs + c] = from_f32<T>(sBeta[i] * fd[j][e]);
+          }
         atomicAdd(&sDBeta[i], db);
       }
     } else if (tid < 64 * LBV / 4) {
