@@ -31,7 +31,7 @@ GDN_DTYPE_F32, GDN_DTYPE_BF16 = 0, 1
 # every symbol the public header declares
 EXPORTS = ("gdn_last_error", "gdn_device_status", "gdn_prepare_varlen", "gdn_chunk_fwd_workspace",
            "gdn_chunk_fwd", "gdn_chunk_bwd_workspace", "gdn_chunk_bwd", "gdn_chunk_bwd_noalloc",
-           "kda_segment_summary", "kda_segment_merge")
+           "kda_segment_summary", "kda_segment_merge", "gdn_selftest_wait_timeout")
 # bytes of the library's built-in scratch array used by gdn_chunk_bwd_noalloc
 GDN_NOALLOC_SCRATCH_BYTES = 64 * 1024 * 1024
 
@@ -87,6 +87,7 @@ def load():
             lib.gdn_chunk_bwd_noalloc.argtypes = [P] + [vp] * 15 + [vp]
             lib.kda_segment_summary.argtypes = [P, vp, vp, vp, vp, ctypes.c_int32, vp, vp, vp, sz, vp]
             lib.kda_segment_merge.argtypes = [P, vp, vp, ctypes.c_int32, vp, vp, vp, vp]
+            lib.gdn_selftest_wait_timeout.argtypes = [ctypes.c_uint32, vp]
             for name in EXPORTS[1:]:
                 getattr(lib, name).restype = ctypes.c_int
             _lib = lib
@@ -141,6 +142,11 @@ def gdn_device_status(stream=None) -> int:
     """Status of the device-side error flag (synchronises the stream); raises on error."""
     _check(load().gdn_device_status(_stream(stream)))
     return GDN_OK
+
+
+def gdn_selftest_wait_timeout(polls, stream=None):
+    """Launch the bounded-wait self-test (its wait always runs out; see gdn.h)."""
+    _check(load().gdn_selftest_wait_timeout(int(polls), _stream(stream)))
 
 
 def gdn_prepare_varlen(cu_seqlens, total_tokens):

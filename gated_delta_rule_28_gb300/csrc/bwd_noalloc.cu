@@ -9,13 +9,13 @@
 //
 // The array below is a file-scope device variable: every GPU that loads the
 // library holds GDN_NOALLOC_SCRATCH_BYTES of device memory for it until the
-// process exits. In host code its name is only a host-side stand-in, so the
-// device address is looked up with cudaGetSymbolAddress once per device (on
-// the first call made with that device current) and passed to the kernels.
+// process exits. In host code its name is only a host-side stand-in, so every
+// call looks up the array's device address on the current device with
+// cudaGetSymbolAddress and passes that address to the kernels. The lookup is
+// cheap and never cached, so an address can never outlive a device reset.
 #include <cuda_runtime.h>
 
 #include <cstdio>
-#include <mutex>
 
 #include "../../include/gdn.h"
 #include "kernels.h"
@@ -25,10 +25,6 @@ namespace {
 constexpr size_t kScratchBytes = (size_t)GDN_NOALLOC_SCRATCH_BYTES;
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[GDN_NOALLOC_SCRATCH_BYTES];
-
-constexpr int kMaxDevices = 64;
-std::mutex g_setup_mutex;
-void *g_scratch_addr[kMaxDevices];  // device address of the array, per device ordinal
 
 }  // namespace
 
@@ -49,25 +45,13 @@ extern "C" gdn_status gdn_chunk_bwd_noalloc(const gdn_problem *p, const void *q,
              need, kScratchBytes);
     return gdn::set_error(GDN_ERR_WORKSPACE, msg);
   }
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return gdn::set_error(GDN_ERR_CUDA, cudaGetErrorString(e));
-  if (dev < 0 || dev >= kMaxDevices)
-    return gdn::set_error(GDN_ERR_UNSUPPORTED, "gdn_chunk_bwd_noalloc: device ordinal above 63");
+  // device address of the array on the current device, looked up on every call
   void *scratch = nullptr;
-  {
-    std::lock_guard<std::mutex> lock(g_setup_mutex);
-    if (!g_scratch_addr[dev]) {
-      void *addr = nullptr;
-      e = cudaGetSymbolAddress(&addr, g_noalloc_scratch);
-      if (e != cudaSuccess || !addr) {
-        snprintf(msg, sizeof(msg), "gdn_chunk_bwd_noalloc: scratch address lookup failed: %s",
-                 cudaGetErrorString(e));
-        return gdn::set_error(GDN_ERR_CUDA, msg);
-      }
-      g_scratch_addr[dev] = addr;
-    }
-    scratch = g_scratch_addr[dev];
+  const cudaError_t e = cudaGetSymbolAddress(&scratch, g_noalloc_scratch);
+  if (e != cudaSuccess || !scratch) {
+    snprintf(msg, sizeof(msg), "gdn_chunk_bwd_noalloc: scratch address lookup failed: %s",
+             cudaGetErrorString(e));
+    return gdn::set_error(GDN_ERR_CUDA, msg);
   }
   return gdn_chunk_bwd(p, q, k, v, g_cumsum, beta, A, dO, h0, dht, dq, dk, dv, dg, dbeta, dh0,
                        scratch, kScratchBytes, stream);

@@ -227,6 +227,20 @@ gdn_status gdn_device_status(void *stream) {
   return fail(GDN_ERR_DEVICE_CHECK, "a kernel found inconsistent device metadata (code %d)", host);
 }
 
+gdn_status gdn_selftest_wait_timeout(uint32_t polls, void *stream) {
+  if (polls < 1 || polls > GDN_SELFTEST_MAX_POLLS)
+    return fail(GDN_ERR_INVALID_ARGUMENT, "polls must be in [1, %u], got %u", (unsigned)GDN_SELFTEST_MAX_POLLS,
+                polls);
+  int dev;
+  gdn_status st = check_device(&dev);
+  if (st != GDN_OK) return st;
+  int *flag = device_flag_ptr();
+  if (!flag) return fail(GDN_ERR_CUDA, "device flag unavailable");
+  cudaError_t e = gdn::launch_wait_selftest(polls, flag, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "wait self-test launch");
+  return ok();
+}
+
 gdn_status gdn_prepare_varlen(const int32_t *cu, int32_t n_seq_plus_1, int64_t total_tokens,
                               int32_t *chunk_indices, int32_t *num_chunks) {
   if (!cu || !num_chunks) return fail(GDN_ERR_INVALID_ARGUMENT, "cu_seqlens and num_chunks must not be NULL");

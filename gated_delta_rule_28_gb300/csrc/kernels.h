@@ -119,6 +119,10 @@ cudaError_t launch_bwd_local(const BwdArgs &a, bool per_key, bool bf16, cudaStre
 // tcgen05 reverse state recurrence (bf16, scalar gate); needs a.xw / a.ftab
 cudaError_t launch_tc_dhu(const BwdArgs &a, int runs, cudaStream_t st);
 
+// One CTA waits, with the kernels' bounded wait and `polls` polls, on an mbarrier that
+// nothing arrives on, then raises the timeout flag (self-test of the wait path).
+cudaError_t launch_wait_selftest(uint32_t polls, int *flag, cudaStream_t st);
+
 }  // namespace gdn
 
 namespace gdn {

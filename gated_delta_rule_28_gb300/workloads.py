@@ -18,7 +18,7 @@ workload number - 1; draws in the fixed order q, k, v, beta, g, h0, dO):
 5 ``gdn_train_bf16``    bf16 [8, 8192, 16, 128], h0 ~ N(0, 0.1^2) fp32,
                         dO ~ N(0, 1).
 Shared: q, k ~ N(0,1) normalised per token; v ~ N(0,1); beta = sigmoid(N(0,1)).
-Sizes can be overridden (same distributions) for smaller parity cases.
+Sizes (and the gate scale) can be overridden for smaller or harder parity cases.
 """
 from __future__ import annotations
 
@@ -105,8 +105,10 @@ def _sigmoid(x):
 
 
 def make(config: int, *, B=None, T=None, H=None, seed=None, K=128, V=128, dtype=None,
-         with_h0=None, with_dO=None) -> Inputs:
+         with_h0=None, with_dO=None, gscale=None) -> Inputs:
     d = dict(DEFAULTS[config])
+    if gscale is not None:
+        d["gscale"] = gscale
     B = d["B"] if B is None else B
     T = d["T"] if T is None else T
     H = d["H"] if H is None else H

@@ -107,6 +107,19 @@ const char *gdn_last_error(void);
  * Returns GDN_OK, GDN_ERR_DEVICE_CHECK or GDN_ERR_TIMEOUT. */
 gdn_status gdn_device_status(void *stream);
 
+/* Self-test of the bounded device-side waits (a diagnostic; the pages' kernels
+ * have no counterpart). Every wait of the library's tensor-core kernels polls
+ * its barrier a bounded number of times; when the budget runs out the kernel
+ * raises the device flag, finishes or waits out its copies in flight, frees its
+ * tensor memory and returns. This call launches one CTA on `stream` that waits
+ * in that same way, with `polls` polls (1 .. GDN_SELFTEST_MAX_POLLS), on a
+ * barrier that nothing arrives on, so the wait always runs out: afterwards
+ * gdn_device_status() returns GDN_ERR_TIMEOUT (and clears the flag). Nothing
+ * is left in flight and the context stays usable. Returns GDN_OK once the
+ * kernel is launched, GDN_ERR_INVALID_ARGUMENT for a budget out of range. */
+#define GDN_SELFTEST_MAX_POLLS (1u << 20)
+gdn_status gdn_selftest_wait_timeout(uint32_t polls, void *stream);
+
 /* Packed-sequence metadata (host only, no device work).
  * Defined by _packed_offsets / _packed_metadata of the Ascend C adapters
  * ("Diff Coverage" page): offsets must have at least two entries, start at
@@ -183,9 +196,11 @@ gdn_status gdn_chunk_bwd(const gdn_problem *p, const void *q, const void *k, con
  *   - Problems whose backward workspace (gdn_chunk_bwd_workspace) exceeds
  *     GDN_NOALLOC_SCRATCH_BYTES are rejected with GDN_ERR_WORKSPACE and a
  *     message giving both sizes, before any device work.
- *   - The first call on each device looks up the array's device address
- *     (cudaGetSymbolAddress) with that device current; make that first call
- *     before any stream capture.
+ *   - Every call looks up the array's device address on the current device
+ *     (cudaGetSymbolAddress); nothing is cached between calls, so the address
+ *     stays valid across a device reset. The first call on a device also
+ *     loads the library's device code there; make it before any stream
+ *     capture.
  *   - Every call on a device shares the one array and it keeps the last
  *     call's contents; the backward writes every scratch element it reads in
  *     the same call, so no clearing is needed. Calls whose work overlaps on

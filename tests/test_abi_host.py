@@ -119,3 +119,10 @@ def test_backward_workspace_size(lib):
     n = B.gdn_chunk_bwd_workspace(p)
     slots = 2 * 3 * 3  # B * H * ceil(130/64)
     assert n >= 2 * slots * 128 * 128 * 4 + 2 * 130 * 3 * 128 * 4
+
+
+@pytest.mark.parametrize("polls", [0, (1 << 20) + 1])
+def test_wait_selftest_rejects_a_budget_out_of_range(lib, polls):
+    with pytest.raises(B.GdnError) as e:
+        B.gdn_selftest_wait_timeout(polls, 0)
+    assert e.value.status == B.GDN_ERR_INVALID_ARGUMENT

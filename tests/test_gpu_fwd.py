@@ -110,22 +110,29 @@ def test_packed_documents_small():
     assert rel_frob(host(out["A"]), c["A"]) <= TOL["bf16"]
 
 
-def test_in_kernel_l2_norm():
-    """use_qk_l2norm: q, k normalised in-kernel as x / sqrt(sum x^2 + 1e-6)."""
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("per_key", [False, True])
+def test_in_kernel_l2_norm(dtype, per_key):
+    """use_qk_l2norm: q, k normalised in-kernel as x / sqrt(sum x^2 + 1e-6); raw q and k
+    of very different sizes, a ragged last chunk and an initial state."""
     import torch
     from gated_delta_rule_28_gb300 import workloads
-    inp = workloads.make(2, B=1, T=130, H=2, dtype="f32")
+    inp = workloads.make(4 if per_key else 2, B=2, T=130, H=2, dtype=dtype, with_h0=True)
     rng = np.random.default_rng(9)
     qr = (rng.standard_normal(inp.q.shape) * 3).astype(np.float32)
     kr = (rng.standard_normal(inp.k.shape) * 0.5).astype(np.float32)
+    dt = torch.bfloat16 if dtype == "bf16" else torch.float32
+    qd, kd = torch.from_numpy(qr).to("cuda", dt), torch.from_numpy(kr).to("cuda", dt)
+    qr, kr = host(qd), host(kd)  # the values the kernel reads
     nrm = lambda x: x / np.sqrt((x.astype(np.float64) ** 2).sum(-1, keepdims=True) + 1e-6)  # noqa: E731
     d = to_dev(inp)
-    out = _api().chunk_gated_delta_rule_fwd(torch.from_numpy(qr).cuda(), torch.from_numpy(kr).cuda(),
-                                            d["v"], d["g"], d["beta"], use_qk_l2norm=True)
+    out = _api().chunk_gated_delta_rule_fwd(qd, kd, d["v"], d["g"], d["beta"], h0=d["h0"],
+                                            use_exp2=inp.use_exp2, use_qk_l2norm=True)
     _status()
-    o, ht = R.forward(nrm(qr), nrm(kr), inp.v, inp.g, inp.beta)
-    assert rel_frob(host(out["o"]), o) <= TOL["f32"]
-    assert rel_frob(host(out["ht"]), ht) <= TOL["f32"]
+    o, ht = R.forward(nrm(qr), nrm(kr), inp.v, inp.g, inp.beta, inp.h0, per_key=per_key,
+                      use_exp2=inp.use_exp2)
+    assert rel_frob(host(out["o"]), o) <= TOL[dtype]
+    assert rel_frob(host(out["ht"]), ht) <= TOL[dtype]
 
 
 @pytest.mark.parametrize("per_key", [True, False])
@@ -183,17 +190,40 @@ def test_device_metadata_check_flags_bad_offsets():
     B.gdn_device_status()  # cleared
 
 
-def test_full_size_bsnd_workload_sampled_heads():
-    """Workload 2 at full size (B4 T4096 H16) in the benchmark's launch;
-    sampled (batch, head) pairs against the oracle one head at a time."""
+def test_bounded_wait_runs_out_and_reports_timeout():
+    """The kernels' bounded mbarrier wait, on a barrier nothing arrives on, gives up,
+    raises the timeout flag and returns; the context stays usable afterwards."""
+    import torch
+    from gated_delta_rule_28_gb300 import binding as B, workloads
+    B.gdn_device_status()  # start clean
+    B.gdn_selftest_wait_timeout(64)
+    with pytest.raises(B.GdnError) as e:
+        B.gdn_device_status()
+    assert e.value.status == B.GDN_ERR_TIMEOUT
+    B.gdn_device_status()  # read and cleared
+    inp = workloads.make(2, B=1, T=100, H=1)
+    d = to_dev(inp)
+    out = _api().chunk_gated_delta_rule_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"])
+    torch.cuda.synchronize()
+    _status()
+    o, _ = oracle_fwd(inp)
+    assert rel_frob(host(out["o"]), o) <= TOL["bf16"]
+
+
+def test_full_size_bsnd_workload_whole_tensors():
+    """Workload 2 at full size (B4 T4096 H16) in the benchmark's launch: the whole o and
+    ht against the oracle (all 64 (batch, head) pairs, the oracle on every host core)."""
     from gated_delta_rule_28_gb300 import workloads
     inp = workloads.make(2)
     d = to_dev(inp)
     out = _api().chunk_gated_delta_rule_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"])
     _status()
+    o, ht = R.forward(inp.q, inp.k, inp.v, inp.g, inp.beta)
+    assert rel_frob(host(out["o"]), o) <= TOL["bf16"]
+    assert rel_frob(host(out["ht"]), ht) <= TOL["bf16"]
+    # and no (batch, head) pair hides behind the others: each one meets the bound alone
     o_gpu, ht_gpu = host(out["o"]), host(out["ht"])
-    for b, h in [(0, 0), (1, 7), (3, 15)]:
-        sl = lambda x: x[b:b + 1, :, h:h + 1]  # noqa: E731
-        o, ht = R.forward(sl(inp.q), sl(inp.k), sl(inp.v), sl(inp.g), sl(inp.beta))
-        assert rel_frob(o_gpu[b:b + 1, :, h:h + 1], o) <= TOL["bf16"]
-        assert rel_frob(ht_gpu[b, h], ht[0, 0]) <= TOL["bf16"]
+    for b in range(4):
+        for h in range(16):
+            assert rel_frob(o_gpu[b, :, h], o[b, :, h]) <= TOL["bf16"], (b, h)
+            assert rel_frob(ht_gpu[b, h], ht[b, h]) <= TOL["bf16"], (b, h)
