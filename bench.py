@@ -103,6 +103,77 @@ class ClockSampler:
                 "samples": len(use), "samples_in_timed_region": len(inside)}
 
 
+class NvmlClockSampler:
+    """SM clock and clock-event reasons read from NVML (the driver's libnvidia-ml, through
+    ctypes; reads only) every millisecond on a background thread, so that even a timed
+    region of a few milliseconds holds several samples. Same report as ClockSampler."""
+
+    # clock-event reason bits of the NVML API
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, device):
+        import ctypes
+        import threading
+        import torch
+        self.ct = ctypes
+        self.lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if self.lib.nvmlInit_v2() != 0:
+            raise RuntimeError("nvmlInit failed")
+        pr = torch.cuda.get_device_properties(device)
+        bus = f"{pr.pci_domain_id:x}:{pr.pci_bus_id:x}:{pr.pci_device_id:x}.0".encode()
+        self.h = ctypes.c_void_p()
+        if self.lib.nvmlDeviceGetHandleByPciBusId_v2(bus, ctypes.byref(self.h)) != 0:
+            raise RuntimeError("no NVML handle for " + bus.decode())
+        mx = ctypes.c_uint()
+        self.lib.nvmlDeviceGetMaxClockInfo(self.h, 1, ctypes.byref(mx))  # 1: SM clock
+        self.max_mhz = float(mx.value)
+        try:
+            self.reasons_fn = self.lib.nvmlDeviceGetCurrentClocksEventReasons
+        except AttributeError:  # the older name of the same query
+            self.reasons_fn = self.lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        self.samples = []
+        self.t0 = self.t1 = None
+        self.run = False
+        self.thread = threading.Thread(target=self._loop, daemon=True)
+
+    def _read(self):
+        c, r = self.ct.c_uint(), self.ct.c_ulonglong()
+        self.lib.nvmlDeviceGetClockInfo(self.h, 1, self.ct.byref(c))
+        self.reasons_fn(self.h, self.ct.byref(r))
+        return time.perf_counter(), float(c.value), int(r.value)
+
+    def _loop(self):
+        while self.run:
+            self.samples.append(self._read())
+            time.sleep(0.001)
+
+    def start(self):
+        self.run = True
+        self.thread.start()
+
+    def mark(self, which):
+        setattr(self, which, time.perf_counter())
+
+    def stop(self):
+        self.run = False
+        self.thread.join()
+        inside = [s for s in self.samples if self.t0 is not None and self.t0 <= s[0] <= self.t1]
+        use = inside or self.samples
+        sm = [s[1] for s in use]
+        reasons = sorted({name for s in use for bit, name in self.REASONS.items() if s[2] & bit})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": self.max_mhz,
+                "reasons": reasons, "samples": len(use), "samples_in_timed_region": len(inside),
+                "source": "NVML, 1 ms period"}
+
+
+def clock_sampler(device):
+    try:
+        return NvmlClockSampler(device)
+    except Exception:
+        return ClockSampler(device.index)
+
+
 FWD_SOURCES = ("ut_fwd.cu", "fwd_ws.cu", "tile_ops.cuh", "tc.cuh")
 
 
@@ -327,9 +398,9 @@ def run_ours(args):
     stream.synchronize()
     Bd.gdn_device_status(sp)
 
-    sampler = ClockSampler(dev.index)
+    sampler = clock_sampler(dev)
     sampler.start()
-    time.sleep(0.5)
+    time.sleep(0.05)
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(args.steps)]
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)

@@ -36,7 +36,7 @@ class Varlen:
 
 
 def problem_for(q, v, g, *, scale=None, use_exp2=False, varlen: Varlen | None = None,
-                use_qk_l2norm=False, segment_len=0):
+                use_qk_l2norm=False, segment_len=0, use_beta_sigmoid=False):
     packed = varlen is not None
     if packed:
         if q.ndim != 3:
@@ -53,18 +53,20 @@ def problem_for(q, v, g, *, scale=None, use_exp2=False, varlen: Varlen | None = 
         use_exp2=use_exp2, scale=0.0 if scale is None else scale, use_qk_l2norm=use_qk_l2norm,
         cu_seqlens=varlen.cu if packed else None, num_seqs=varlen.num_seqs if packed else 0,
         chunk_indices=varlen.chunk_indices if packed else None,
-        num_chunks=varlen.num_chunks if packed else 0, segment_len=segment_len)
+        num_chunks=varlen.num_chunks if packed else 0, segment_len=segment_len,
+        use_beta_sigmoid=use_beta_sigmoid)
 
 
 def chunk_gated_delta_rule_fwd(q, k, v, g, beta, *, h0=None, scale=None, use_exp2=False,
                                cu_seqlens=None, varlen=None, output_final_state=True,
                                return_g_cumsum=False, return_A=False, return_h_chunks=False,
-                               use_qk_l2norm=False, segment_len=0, stream=None):
+                               use_qk_l2norm=False, use_beta_sigmoid=False, segment_len=0, stream=None):
     """Chunked forward; returns a dict with o and, as requested, ht, g_cumsum, A, h_chunks."""
     if cu_seqlens is not None and varlen is None:
         varlen = Varlen(cu_seqlens, q.shape[0], q.device)
     p = problem_for(q, v, g, scale=scale, use_exp2=use_exp2, varlen=varlen,
-                    use_qk_l2norm=use_qk_l2norm, segment_len=segment_len)
+                    use_qk_l2norm=use_qk_l2norm, segment_len=segment_len,
+                    use_beta_sigmoid=use_beta_sigmoid)
     dev = q.device
     out = {"o": torch.empty_like(v)}
     nstate = varlen.num_seqs if varlen is not None else p.B
@@ -159,11 +161,14 @@ class HostPipeline:
 
 
 def chunk_gated_delta_rule_bwd(q, k, v, g_cumsum, beta, A, dO, *, h0=None, dht=None, scale=None,
-                               use_exp2=False, cu_seqlens=None, varlen=None, stream=None):
-    """Chunked backward; returns dq, dk, dv, dbeta, dg (raw gate) and dh0."""
+                               use_exp2=False, cu_seqlens=None, varlen=None, use_qk_l2norm=False,
+                               use_beta_sigmoid=False, stream=None):
+    """Chunked backward; returns dq, dk, dv, dbeta, dg (raw gate) and dh0. With the input
+    maps on, q, k, beta are the forward's raw inputs and dq, dk, dbeta are w.r.t. them."""
     if cu_seqlens is not None and varlen is None:
         varlen = Varlen(cu_seqlens, q.shape[0], q.device)
-    p = problem_for(q, v, g_cumsum, scale=scale, use_exp2=use_exp2, varlen=varlen)
+    p = problem_for(q, v, g_cumsum, scale=scale, use_exp2=use_exp2, varlen=varlen,
+                    use_qk_l2norm=use_qk_l2norm, use_beta_sigmoid=use_beta_sigmoid)
     nstate = varlen.num_seqs if varlen is not None else p.B
     out = dict(dq=torch.empty_like(q), dk=torch.empty_like(k), dv=torch.empty_like(v),
                dbeta=torch.empty_like(beta), dg=torch.empty_like(g_cumsum),
@@ -175,13 +180,17 @@ def chunk_gated_delta_rule_bwd(q, k, v, g_cumsum, beta, A, dO, *, h0=None, dht=N
     return out
 
 
-def segment_summary(k, v, g, beta, segment_len, *, use_exp2=False, stream=None):
+def segment_summary(k, v, g, beta, segment_len, *, use_exp2=False, use_qk_l2norm=False,
+                    use_beta_sigmoid=False, stream=None):
     """(S_ext [B,H,nseg,K,V], M [B,H,nseg,K,K]) for every segment of ``segment_len`` tokens."""
-    p = problem_for(k, v, g, use_exp2=use_exp2)
+    p = problem_for(k, v, g, use_exp2=use_exp2, use_qk_l2norm=use_qk_l2norm,
+                    use_beta_sigmoid=use_beta_sigmoid)
     nseg = -(-p.T // segment_len)
     S = torch.empty((p.B, p.H, nseg, p.K, p.V), device=k.device, dtype=torch.float32)
     M = torch.empty((p.B, p.H, nseg, p.K, p.K), device=k.device, dtype=torch.float32)
-    B.kda_segment_summary(p, k, v, g, beta, segment_len, S, M, None, 0, stream)
+    nws = B.kda_segment_summary_workspace(p, segment_len)
+    ws = torch.empty(nws, device=k.device, dtype=torch.uint8) if nws else None
+    B.kda_segment_summary(p, k, v, g, beta, segment_len, S, M, ws, nws, stream)
     return S, M
 
 
@@ -196,12 +205,13 @@ def segment_merge(S_ext, M, h0=None, stream=None):
 
 
 def split_forward(q, k, v, g, beta, segment_len, *, h0=None, scale=None, use_exp2=False,
-                  return_h_chunks=False, stream=None):
+                  use_qk_l2norm=False, use_beta_sigmoid=False, return_h_chunks=False, stream=None):
     """Long-sequence forward split across SMs: summaries, merge, corrected run."""
-    S, M = segment_summary(k, v, g, beta, segment_len, use_exp2=use_exp2, stream=stream)
+    maps = dict(use_qk_l2norm=use_qk_l2norm, use_beta_sigmoid=use_beta_sigmoid)
+    S, M = segment_summary(k, v, g, beta, segment_len, use_exp2=use_exp2, stream=stream, **maps)
     S_init, _ = segment_merge(S, M, h0, stream=stream)
     out = chunk_gated_delta_rule_fwd(q, k, v, g, beta, h0=S_init, scale=scale, use_exp2=use_exp2,
                                      segment_len=segment_len, return_h_chunks=return_h_chunks,
-                                     stream=stream)
+                                     stream=stream, **maps)
     out.update(S_ext=S, M=M, S_init=S_init)
     return out

@@ -31,7 +31,8 @@ GDN_DTYPE_F32, GDN_DTYPE_BF16 = 0, 1
 # every symbol the public header declares
 EXPORTS = ("gdn_last_error", "gdn_device_status", "gdn_prepare_varlen", "gdn_chunk_fwd_workspace",
            "gdn_chunk_fwd", "gdn_chunk_bwd_workspace", "gdn_chunk_bwd", "gdn_chunk_bwd_noalloc",
-           "kda_segment_summary", "kda_segment_merge", "gdn_selftest_wait_timeout")
+           "kda_segment_summary_workspace", "kda_segment_summary", "kda_segment_merge",
+           "gdn_selftest_wait_timeout")
 # bytes of the library's built-in scratch array used by gdn_chunk_bwd_noalloc
 GDN_NOALLOC_SCRATCH_BYTES = 64 * 1024 * 1024
 
@@ -51,7 +52,7 @@ class gdn_problem(ctypes.Structure):  # noqa: N801  (C name)
         ("use_qk_l2norm", ctypes.c_int32),
         ("cu_seqlens", ctypes.c_void_p), ("num_seqs", ctypes.c_int32),
         ("chunk_indices", ctypes.c_void_p), ("num_chunks", ctypes.c_int32),
-        ("segment_len", ctypes.c_int32),
+        ("segment_len", ctypes.c_int32), ("use_beta_sigmoid", ctypes.c_int32),
     ]
 
 
@@ -85,6 +86,7 @@ def load():
             lib.gdn_chunk_bwd_workspace.argtypes = [P, ctypes.POINTER(sz)]
             lib.gdn_chunk_bwd.argtypes = [P] + [vp] * 15 + [vp, sz, vp]
             lib.gdn_chunk_bwd_noalloc.argtypes = [P] + [vp] * 15 + [vp]
+            lib.kda_segment_summary_workspace.argtypes = [P, ctypes.c_int32, ctypes.POINTER(sz)]
             lib.kda_segment_summary.argtypes = [P, vp, vp, vp, vp, ctypes.c_int32, vp, vp, vp, sz, vp]
             lib.kda_segment_merge.argtypes = [P, vp, vp, ctypes.c_int32, vp, vp, vp, vp]
             lib.gdn_selftest_wait_timeout.argtypes = [ctypes.c_uint32, vp]
@@ -119,7 +121,7 @@ def _stream(stream):
 def make_problem(B, T, H, K=128, V=128, *, layout=GDN_LAYOUT_BSND, gate_kind=GDN_GATE_SCALAR,
                  dtype=GDN_DTYPE_BF16, use_exp2=False, scale=0.0, chunk_size=64,
                  use_qk_l2norm=False, cu_seqlens=None, num_seqs=0, chunk_indices=None,
-                 num_chunks=0, segment_len=0) -> gdn_problem:
+                 num_chunks=0, segment_len=0, use_beta_sigmoid=False) -> gdn_problem:
     """Fill a ``gdn_problem``; cu_seqlens / chunk_indices are device tensors (or None)."""
     p = gdn_problem()
     p.B, p.T, p.H, p.K, p.V = int(B), int(T), int(H), int(K), int(V)
@@ -131,6 +133,7 @@ def make_problem(B, T, H, K=128, V=128, *, layout=GDN_LAYOUT_BSND, gate_kind=GDN
     p.chunk_indices = None if chunk_indices is None else chunk_indices.data_ptr()
     p.num_chunks = int(num_chunks)
     p.segment_len = int(segment_len)
+    p.use_beta_sigmoid = int(use_beta_sigmoid)
     return p
 
 
@@ -201,6 +204,12 @@ def gdn_chunk_bwd_noalloc(p: gdn_problem, q, k, v, g_cumsum, beta, A, dO, h0, dh
                                         _ptr(beta), _ptr(A), _ptr(dO), _ptr(h0), _ptr(dht),
                                         _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dg), _ptr(dbeta),
                                         _ptr(dh0), _stream(stream)))
+
+
+def kda_segment_summary_workspace(p: gdn_problem, segment_len) -> int:
+    n = ctypes.c_size_t(0)
+    _check(load().kda_segment_summary_workspace(ctypes.byref(p), int(segment_len), ctypes.byref(n)))
+    return n.value
 
 
 def kda_segment_summary(p: gdn_problem, k, v, g, beta, segment_len, S_ext, M, ws=None, ws_bytes=0,

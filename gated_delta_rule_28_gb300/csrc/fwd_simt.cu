@@ -179,20 +179,6 @@ __global__ void __launch_bounds__(NTH) simt_chunk_kernel(SimtFwdArgs a) {
     }
     __syncthreads();
 
-    if (a.l2norm) {  // x / sqrt(sum x^2 + 1e-6), one warp per row
-      const int warp = tid >> 5, lane = tid & 31;
-      for (int i = warp; i < 2 * GDN_CHUNK; i += NTH / 32) {
-        float *row = (i < GDN_CHUNK ? sK : sQ) + (i & 63) * KP;
-        float ss = 0.f;
-        for (int d = lane; d < GDN_DK; d += 32) ss += row[d] * row[d];
-#pragma unroll
-        for (int off = 16; off; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
-        const float r = rsqrtf(ss + 1e-6f);
-        for (int d = lane; d < GDN_DK; d += 32) row[d] *= r;
-      }
-      __syncthreads();
-    }
-
     const bool lead = blockIdx.x == 0 && !summ;
     if (lead && a.g_cumsum) {
       if (PER_KEY) {

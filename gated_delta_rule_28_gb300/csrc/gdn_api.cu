@@ -87,6 +87,8 @@ gdn_status check_problem(const gdn_problem *p, bool allow_segments) {
     return fail(GDN_ERR_INVALID_ARGUMENT, "use_exp2 must be 0 or 1");
   if (p->use_qk_l2norm != 0 && p->use_qk_l2norm != 1)
     return fail(GDN_ERR_INVALID_ARGUMENT, "use_qk_l2norm must be 0 or 1");
+  if (p->use_beta_sigmoid != 0 && p->use_beta_sigmoid != 1)
+    return fail(GDN_ERR_INVALID_ARGUMENT, "use_beta_sigmoid must be 0 or 1");
   if (p->B < 1 || p->H < 1 || p->T < 0)
     return fail(GDN_ERR_INVALID_ARGUMENT, "need B >= 1, H >= 1, T >= 0 (got B=%d H=%d T=%d)", p->B,
                 p->H, p->T);
@@ -140,10 +142,61 @@ float eff_scale(const gdn_problem *p) {
   return p->scale == 0.f ? 1.0f / std::sqrt((float)p->K) : p->scale;
 }
 
-// bf16 inputs with one gate per head run on the tensor-core kernel; fp32
-// inputs, per-key gates and the in-kernel norm run on the fp32 SIMT kernel.
+// bf16 inputs with one gate per head run on the tensor-core kernels; fp32
+// inputs and per-key gates run on the fp32 SIMT kernel. (The input maps run
+// before either, so the choice is made on the mapped problem.)
 bool use_tensor_cores(const gdn_problem *p) {
-  return p->dtype == GDN_DTYPE_BF16 && p->gate_kind == GDN_GATE_SCALAR && !p->use_qk_l2norm;
+  return p->dtype == GDN_DTYPE_BF16 && p->gate_kind == GDN_GATE_SCALAR;
+}
+
+// ---- input maps: L2 norm of q and k, sigmoid of beta ----------------------------------
+bool has_input_maps(const gdn_problem *p) { return p->use_qk_l2norm || p->use_beta_sigmoid; }
+int64_t token_rows(const gdn_problem *p) {
+  return p->layout == GDN_LAYOUT_TND ? (int64_t)p->T : (int64_t)p->B * p->T;
+}
+size_t elt_bytes(const gdn_problem *p) { return p->dtype == GDN_DTYPE_BF16 ? 2 : 4; }
+size_t align256(size_t x);
+// workspace of the mapped inputs: [q_n][k_n] (L2 norm), then [beta_eff] (sigmoid)
+size_t map_part_bytes(const gdn_problem *p) {
+  const size_t rows = (size_t)token_rows(p) * p->H;
+  size_t b = 0;
+  if (p->use_qk_l2norm) b += 2 * align256(rows * GDN_DK * elt_bytes(p));
+  if (p->use_beta_sigmoid) b += align256(rows * elt_bytes(p));
+  return b;
+}
+// the problem the chunk kernels see once the maps have run
+gdn_problem mapped_problem(const gdn_problem *p) {
+  gdn_problem m = *p;
+  m.use_qk_l2norm = 0;
+  m.use_beta_sigmoid = 0;
+  return m;
+}
+// Runs the prologue into `ws` and points q, k, beta at the mapped copies (q may be null).
+cudaError_t run_input_maps(const gdn_problem *p, const void **q, const void **k, const void **beta,
+                           void *ws, cudaStream_t s) {
+  const size_t rows = (size_t)token_rows(p) * p->H;
+  char *w = static_cast<char *>(ws);
+  gdn::InputMapArgs m{};
+  m.q = *q;
+  m.k = *k;
+  m.beta = *beta;
+  m.rows = (int64_t)rows;
+  m.l2norm = p->use_qk_l2norm;
+  m.beta_sigmoid = p->use_beta_sigmoid;
+  if (p->use_qk_l2norm) {
+    m.qn = w;
+    m.kn = w + align256(rows * GDN_DK * elt_bytes(p));
+    w += 2 * align256(rows * GDN_DK * elt_bytes(p));
+  }
+  if (p->use_beta_sigmoid) m.beta_eff = w;
+  cudaError_t e = gdn::launch_input_maps(m, p->dtype == GDN_DTYPE_BF16, false, s);
+  if (e != cudaSuccess) return e;
+  if (p->use_qk_l2norm) {
+    if (*q) *q = m.qn;
+    *k = m.kn;
+  }
+  if (p->use_beta_sigmoid) *beta = m.beta_eff;
+  return cudaSuccess;
 }
 
 int64_t n_chunk_slots(const gdn_problem *p) {
@@ -279,16 +332,19 @@ gdn_status gdn_chunk_fwd_workspace(const gdn_problem *p, size_t *bytes) {
   gdn_status st = check_problem(p, true);
   if (st != GDN_OK) return st;
   if (!bytes) return fail(GDN_ERR_INVALID_ARGUMENT, "bytes must not be NULL");
-  *bytes = x_ws_bytes(p);
+  const gdn_problem m = mapped_problem(p);
+  *bytes = map_part_bytes(p) + x_ws_bytes(&m);
   return ok();
 }
 
-gdn_status gdn_chunk_fwd(const gdn_problem *p, const void *q, const void *k, const void *v,
+gdn_status gdn_chunk_fwd(const gdn_problem *pin, const void *q, const void *k, const void *v,
                          const float *g, const void *beta, const float *h0, void *o, float *ht,
                          float *g_cumsum, float *A, float *h_chunks, void *ws, size_t ws_bytes,
                          void *stream) {
-  gdn_status st = check_problem(p, true);
+  gdn_status st = check_problem(pin, true);
   if (st != GDN_OK) return st;
+  const gdn_problem mp = mapped_problem(pin);
+  const gdn_problem *p = &mp;
   if (p->T > 0) {  // an empty sequence has no token tensors (they may be NULL)
     REQUIRE_PTR(q, "q");
     REQUIRE_PTR(k, "k");
@@ -302,7 +358,8 @@ gdn_status gdn_chunk_fwd(const gdn_problem *p, const void *q, const void *k, con
   OPTIONAL_PTR(g_cumsum, "g_cumsum");
   OPTIONAL_PTR(A, "A");
   OPTIONAL_PTR(h_chunks, "h_chunks");
-  const size_t need = x_ws_bytes(p);
+  const size_t maps = map_part_bytes(pin);
+  const size_t need = maps + x_ws_bytes(p);
   if (need > 0 && (!ws || ws_bytes < need))
     return fail(GDN_ERR_WORKSPACE, "forward workspace needs %zu bytes, got %zu", need,
                 ws ? ws_bytes : (size_t)0);
@@ -312,6 +369,11 @@ gdn_status gdn_chunk_fwd(const gdn_problem *p, const void *q, const void *k, con
   int dev;
   if ((st = check_device(&dev)) != GDN_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (maps > 0 && p->T > 0) {  // normalised q, k and effective beta into the workspace
+    cudaError_t e = run_input_maps(pin, &q, &k, &beta, ws, s);
+    if (e != cudaSuccess) return cuda_fail(e, "input map launch");
+  }
+  ws = static_cast<char *>(ws) + maps;
 
   gdn::SimtFwdArgs a{};
   a.q = q;
@@ -330,7 +392,6 @@ gdn_status gdn_chunk_fwd(const gdn_problem *p, const void *q, const void *k, con
   a.H = p->H;
   a.scale = eff_scale(p);
   a.use_exp2 = p->use_exp2;
-  a.l2norm = p->use_qk_l2norm;
   a.cu = p->layout == GDN_LAYOUT_TND ? p->cu_seqlens : nullptr;
   a.num_seqs = p->num_seqs;
   a.num_chunks = p->num_chunks;
@@ -358,18 +419,21 @@ gdn_status gdn_chunk_bwd_workspace(const gdn_problem *p, size_t *bytes) {
   gdn_status st = check_problem(p, false);
   if (st != GDN_OK) return st;
   if (!bytes) return fail(GDN_ERR_INVALID_ARGUMENT, "bytes must not be NULL");
-  *bytes = bwd_ws_layout(p).total;
+  const gdn_problem m = mapped_problem(p);
+  *bytes = map_part_bytes(p) + bwd_ws_layout(&m).total;
   return ok();
 }
 
-gdn_status gdn_chunk_bwd(const gdn_problem *p, const void *q, const void *k, const void *v,
+gdn_status gdn_chunk_bwd(const gdn_problem *pin, const void *q, const void *k, const void *v,
                          const float *g_cumsum, const void *beta, const float *A, const void *dO,
                          const float *h0, const float *dht, void *dq, void *dk, void *dv, float *dg,
                          void *dbeta, float *dh0, void *ws, size_t ws_bytes, void *stream) {
-  gdn_status st = check_problem(p, false);
+  gdn_status st = check_problem(pin, false);
   if (st != GDN_OK) return st;
-  if (p->use_qk_l2norm)
-    return fail(GDN_ERR_UNSUPPORTED, "the backward takes normalised q and k (use_qk_l2norm = 0)");
+  const gdn_problem mp = mapped_problem(pin);
+  const gdn_problem *p = &mp;
+  const size_t maps = map_part_bytes(pin);
+  const void *q_raw = q, *k_raw = k, *beta_raw = beta;
   if (p->T > 0) {
     REQUIRE_PTR(q, "q");
     REQUIRE_PTR(k, "k");
@@ -388,15 +452,19 @@ gdn_status gdn_chunk_bwd(const gdn_problem *p, const void *q, const void *k, con
   OPTIONAL_PTR(dht, "dht");
   OPTIONAL_PTR(dh0, "dh0");
   const BwdWs L = bwd_ws_layout(p);
-  if (L.total > 0 && (!ws || ws_bytes < L.total))
-    return fail(GDN_ERR_WORKSPACE, "backward workspace needs %zu bytes, got %zu", L.total,
+  if (maps + L.total > 0 && (!ws || ws_bytes < maps + L.total))
+    return fail(GDN_ERR_WORKSPACE, "backward workspace needs %zu bytes, got %zu", maps + L.total,
                 ws ? ws_bytes : (size_t)0);
   if (ws && !aligned16(ws)) return fail(GDN_ERR_INVALID_ARGUMENT, "ws must be 16-byte aligned");
   int dev;
   if ((st = check_device(&dev)) != GDN_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const bool pk = p->gate_kind == GDN_GATE_PER_KEY, bf = p->dtype == GDN_DTYPE_BF16;
-  char *w = static_cast<char *>(ws);
+  if (maps > 0 && p->T > 0) {  // the forward's mapped inputs, recomputed into the workspace
+    cudaError_t e = run_input_maps(pin, &q, &k, &beta, ws, s);
+    if (e != cudaSuccess) return cuda_fail(e, "input map launch");
+  }
+  char *w = static_cast<char *>(ws) + maps;
   float *hch = reinterpret_cast<float *>(w + L.h_chunks);
   float *dhch = reinterpret_cast<float *>(w + L.dh_chunks);
   float *dvn = reinterpret_cast<float *>(w + L.dvnew);
@@ -486,16 +554,41 @@ gdn_status gdn_chunk_bwd(const gdn_problem *p, const void *q, const void *k, con
   if (e != cudaSuccess) return cuda_fail(e, "dhu launch");
   // 3. local gradients
   if ((e = gdn::launch_bwd_local(b, pk, bf, s)) != cudaSuccess) return cuda_fail(e, "local gradient launch");
+  // 4. chain rules of the input maps, in place: gradients w.r.t. the raw q, k and beta
+  if (maps > 0) {
+    gdn::InputMapArgs m{};
+    m.q = q_raw;
+    m.k = k_raw;
+    m.beta = beta_raw;
+    m.dq = dq;
+    m.dk = dk;
+    m.dbeta = dbeta;
+    m.rows = token_rows(p) * p->H;
+    m.l2norm = pin->use_qk_l2norm;
+    m.beta_sigmoid = pin->use_beta_sigmoid;
+    if ((e = gdn::launch_input_maps(m, bf, true, s)) != cudaSuccess) return cuda_fail(e, "input map backward launch");
+  }
   return ok();
 }
 
-gdn_status kda_segment_summary(const gdn_problem *p, const void *k, const void *v, const float *g,
-                               const void *beta, int32_t segment_len, float *S_ext, float *M,
-                               void *ws, size_t ws_bytes, void *stream) {
+gdn_status kda_segment_summary_workspace(const gdn_problem *p, int32_t segment_len, size_t *bytes) {
   gdn_status st = check_problem(p, true);
   if (st != GDN_OK) return st;
-  (void)ws;
-  (void)ws_bytes;
+  if (!bytes) return fail(GDN_ERR_INVALID_ARGUMENT, "bytes must not be NULL");
+  if (segment_len <= 0 || segment_len % GDN_CHUNK != 0)
+    return fail(GDN_ERR_INVALID_ARGUMENT, "segment_len must be a positive multiple of 64, got %d",
+                segment_len);
+  *bytes = map_part_bytes(p);
+  return ok();
+}
+
+gdn_status kda_segment_summary(const gdn_problem *pin, const void *k, const void *v, const float *g,
+                               const void *beta, int32_t segment_len, float *S_ext, float *M,
+                               void *ws, size_t ws_bytes, void *stream) {
+  gdn_status st = check_problem(pin, true);
+  if (st != GDN_OK) return st;
+  const gdn_problem mp = mapped_problem(pin);
+  const gdn_problem *p = &mp;
   if (p->layout != GDN_LAYOUT_BSND)
     return fail(GDN_ERR_UNSUPPORTED, "segment summaries take the BSND layout");
   if (segment_len <= 0 || segment_len % GDN_CHUNK != 0)
@@ -507,9 +600,20 @@ gdn_status kda_segment_summary(const gdn_problem *p, const void *k, const void *
   REQUIRE_PTR(beta, "beta");
   REQUIRE_PTR(S_ext, "S_ext");
   REQUIRE_PTR(M, "M");
+  const size_t maps = map_part_bytes(pin);
+  if (maps > 0 && (!ws || ws_bytes < maps))
+    return fail(GDN_ERR_WORKSPACE, "segment summary workspace needs %zu bytes, got %zu", maps,
+                ws ? ws_bytes : (size_t)0);
+  if (ws && !aligned16(ws)) return fail(GDN_ERR_INVALID_ARGUMENT, "ws must be 16-byte aligned");
   int dev;
   if ((st = check_device(&dev)) != GDN_OK) return st;
   if (p->T == 0) return ok();
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (maps > 0) {  // normalised k and effective beta (q is not needed)
+    const void *qnull = nullptr;
+    cudaError_t e = run_input_maps(pin, &qnull, &k, &beta, ws, s);
+    if (e != cudaSuccess) return cuda_fail(e, "input map launch");
+  }
   gdn::SimtFwdArgs a{};
   a.q = k;  // unused in summary mode
   a.k = k;
@@ -523,15 +627,13 @@ gdn_status kda_segment_summary(const gdn_problem *p, const void *k, const void *
   a.H = p->H;
   a.scale = 1.f;
   a.use_exp2 = p->use_exp2;
-  a.l2norm = p->use_qk_l2norm;
   a.seg_len = segment_len;
   a.nseg = (int)div_up(p->T, segment_len);
   a.summary = 1;
   a.dev_flag = device_flag_ptr();
   const dim3 grid((GDN_DV + GDN_DK) / gdn::simt_fwd_bv(), p->H, p->B * a.nseg);
   cudaError_t e = gdn::launch_simt_fwd(a, p->gate_kind == GDN_GATE_PER_KEY,
-                                       p->dtype == GDN_DTYPE_BF16, grid,
-                                       static_cast<cudaStream_t>(stream));
+                                       p->dtype == GDN_DTYPE_BF16, grid, s);
   if (e != cudaSuccess) return cuda_fail(e, "segment summary launch");
   return ok();
 }

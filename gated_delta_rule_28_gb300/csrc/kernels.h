@@ -46,7 +46,7 @@ struct SimtFwdArgs {
   float *S_ext, *M;  // summary mode outputs
   int B, T, H;
   float scale;
-  int use_exp2, l2norm;
+  int use_exp2;
   const int32_t *cu;  // packed offsets (device) or nullptr
   int num_seqs;
   int num_chunks;     // packed: chunk slots of h_chunks (bounds check)
@@ -118,6 +118,17 @@ cudaError_t launch_bwd_dhu(const BwdArgs &a, bool per_key, bool bf16, cudaStream
 cudaError_t launch_bwd_local(const BwdArgs &a, bool per_key, bool bf16, cudaStream_t st);
 // tcgen05 reverse state recurrence (bf16, scalar gate); needs a.xw / a.ftab
 cudaError_t launch_tc_dhu(const BwdArgs &a, int runs, cudaStream_t st);
+
+// The optional input maps (q, k L2 norm; beta sigmoid) before the chunk kernels, and their
+// chain rules after the backward (in place on dq, dk, dbeta).
+struct InputMapArgs {
+  const void *q, *k, *beta;  // raw inputs (q may be null: maps k only)
+  void *qn, *kn, *beta_eff;  // prologue outputs
+  void *dq, *dk, *dbeta;     // epilogue: gradients w.r.t. the mapped inputs, replaced in place
+  int64_t rows;              // (token, head) rows
+  int l2norm, beta_sigmoid;
+};
+cudaError_t launch_input_maps(const InputMapArgs &a, bool bf16, bool backward, cudaStream_t st);
 
 // One CTA waits, with the kernels' bounded wait and `polls` polls, on an mbarrier that
 // nothing arrives on, then raises the timeout flag (self-test of the wait path).

@@ -70,7 +70,11 @@ enum { GDN_DTYPE_F32 = 0, GDN_DTYPE_BF16 = 1 };
  *   use_exp2      : 0 -> a = exp(g); 1 -> a = 2^g (the KDA stages use base 2).
  *   scale         : output scale; 0 selects K^-1/2 (the adapters' default).
  *   chunk_size    : must be 64 (the fused backends require chunk_size=64).
- *   use_qk_l2norm : normalise q and k in-kernel, x / sqrt(sum x^2 + 1e-6).
+ *   use_qk_l2norm : q and k are raw; a prologue kernel normalises them,
+ *                   x / sqrt(sum x^2 + 1e-6) per (token, head) row, into the
+ *                   workspace before the chunk kernels (the KDA adapter's
+ *                   use_qk_l2norm_in_kernel, epsilon 1e-6). The backward then
+ *                   returns dq, dk w.r.t. the raw q, k.
  *   cu_seqlens    : TND only: device int32 [num_seqs + 1] document offsets,
  *                   validated beforehand with gdn_prepare_varlen.
  *   num_seqs      : TND only: number of documents.
@@ -83,6 +87,9 @@ enum { GDN_DTYPE_F32 = 0, GDN_DTYPE_BF16 = 1 };
  *                   h0 laid out [B, H, nseg, K, V] (the S_init produced by
  *                   kda_segment_merge): the correction run of the segment
  *                   split. ht then receives each batch row's final state.
+ *   use_beta_sigmoid : beta is raw; the prologue maps it to 1 / (1 + exp(-beta))
+ *                   (the KDA adapter's use_beta_sigmoid_in_kernel). The
+ *                   backward then returns dbeta w.r.t. the raw beta.
  */
 typedef struct gdn_problem {
     int32_t B, T, H, K, V;
@@ -98,6 +105,7 @@ typedef struct gdn_problem {
     const int32_t *chunk_indices;
     int32_t num_chunks;
     int32_t segment_len;
+    int32_t use_beta_sigmoid;
 } gdn_problem;
 
 /* Thread-local text of the last failure in this thread ("" after success). */
@@ -176,8 +184,11 @@ gdn_status gdn_chunk_bwd_workspace(const gdn_problem *p, size_t *bytes);
  *                   gate (not its cumulative sum).
  *   dh0           : nullable fp32 [N, H, K, V] gradient of h0.
  *   ws, ws_bytes  : workspace of at least gdn_chunk_bwd_workspace bytes.
- * segment_len must be 0 and use_qk_l2norm must be 0 (the adapters apply
- * the norm outside the native backward). */
+ * segment_len must be 0. With use_qk_l2norm / use_beta_sigmoid the inputs are
+ * the raw q, k, beta of the forward (A and g_cumsum its saved slots), and dq,
+ * dk, dbeta are w.r.t. those raw inputs: the prologue recomputes the mapped
+ * inputs into the workspace and an epilogue kernel applies the chain rules of
+ * the maps to the outputs in place. */
 gdn_status gdn_chunk_bwd(const gdn_problem *p, const void *q, const void *k, const void *v,
                          const float *g_cumsum, const void *beta, const float *A,
                          const void *dO, const float *h0, const float *dht, void *dq, void *dk,
@@ -221,7 +232,10 @@ gdn_status gdn_chunk_bwd_noalloc(const gdn_problem *p, const void *q, const void
  *   k, v, g, beta : device inputs (g_cumsum is computed internally).
  *   S_ext         : device fp32 [B, H, nseg, K, V].
  *   M             : device fp32 [B, H, nseg, K, K].
- * ws may be NULL (no workspace needed). */
+ *   ws, ws_bytes  : workspace of at least kda_segment_summary_workspace bytes
+ *                   (may be NULL when that is 0). */
+gdn_status kda_segment_summary_workspace(const gdn_problem *p, int32_t segment_len,
+                                         size_t *bytes);
 gdn_status kda_segment_summary(const gdn_problem *p, const void *k, const void *v,
                                const float *g, const void *beta, int32_t segment_len,
                                float *S_ext, float *M, void *ws, size_t ws_bytes, void *stream);

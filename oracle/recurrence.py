@@ -11,7 +11,13 @@ Definitions followed (restated in ``gdn_oracle.c``):
     "state_summary.py" kda_split_state_summary_kernel;
   * the segment summary (S_ext, M) and merge S_{s+1} = M_s S_s + S_ext_s of
     apply_kda_state_summary (coverage-diff page) and SANA's
-    _exclusive_prefix_compose.
+    _exclusive_prefix_compose;
+  * the optional in-kernel input maps of the KDA adapter (coverage-diff page,
+    _prepare_kda: use_qk_l2norm_in_kernel with epsilon=1e-6, and
+    use_beta_sigmoid_in_kernel; its backward finalize takes q_rstd / k_rstd and
+    the beta-sigmoid backward helper): q, k <- x / sqrt(sum_d x_d^2 + 1e-6) and
+    beta <- 1 / (1 + exp(-beta)) before the recurrence, and the chain rule of
+    those two maps after its reverse mode.
 """
 from __future__ import annotations
 
@@ -72,6 +78,26 @@ def _load():
     return _lib
 
 
+L2_EPS = 1e-6  # the KDA adapter's epsilon for the in-kernel q/k norm
+
+
+def l2norm(x):
+    """x / sqrt(sum_d x_d^2 + 1e-6) along the last axis, and 1 / sqrt(sum_d x_d^2 + 1e-6)."""
+    x = np.asarray(x, np.float64)
+    rstd = 1.0 / np.sqrt((x * x).sum(-1, keepdims=True) + L2_EPS)
+    return x * rstd, rstd
+
+
+def l2norm_backward(x, dxn):
+    """Gradient w.r.t. x of <x / sqrt(|x|^2 + eps), dxn>: rstd (dxn - xn <xn, dxn>)."""
+    xn, rstd = l2norm(x)
+    return rstd * (dxn - xn * (xn * dxn).sum(-1, keepdims=True))
+
+
+def sigmoid(x):
+    return 1.0 / (1.0 + np.exp(-np.asarray(x, np.float64)))
+
+
 def default_threads() -> int:
     return os.cpu_count() or 1
 
@@ -112,9 +138,15 @@ def _problem(q, v, per_key, use_exp2, scale, cu, n_threads):
 
 
 def forward(q, k, v, g, beta, h0=None, *, scale=None, per_key=False, use_exp2=False,
-            cu=None, n_threads=None, want_o=True, want_ht=True):
-    """Return (o, ht). ``g`` is [.., H] (scalar gate) or [.., H, K] (per key)."""
+            cu=None, n_threads=None, want_o=True, want_ht=True, use_qk_l2norm=False,
+            beta_sigmoid=False):
+    """Return (o, ht). ``g`` is [.., H] (scalar gate) or [.., H, K] (per key).
+    ``use_qk_l2norm`` / ``beta_sigmoid``: q, k and beta are raw and mapped first."""
     q, k, v, g, beta, h0 = map(_f64, (q, k, v, g, beta, h0))
+    if use_qk_l2norm:
+        q, k = l2norm(q)[0], l2norm(k)[0]
+    if beta_sigmoid:
+        beta = sigmoid(beta)
     p, keep, n_state = _problem(q, v, per_key, use_exp2, scale, cu, n_threads)
     o = np.zeros(v.shape, np.float64) if want_o else None
     ht = np.zeros((n_state, p.H, p.K, p.V), np.float64) if want_ht else None
@@ -126,12 +158,18 @@ def forward(q, k, v, g, beta, h0=None, *, scale=None, per_key=False, use_exp2=Fa
 
 
 def backward(q, k, v, g, beta, h0=None, dO=None, dht=None, *, scale=None, per_key=False,
-             use_exp2=False, cu=None, n_threads=None):
+             use_exp2=False, cu=None, n_threads=None, use_qk_l2norm=False, beta_sigmoid=False):
     """Reverse mode of ``forward`` for the loss <o, dO> + <ht, dht>.
 
-    Returns dict(dq, dk, dv, dg, dbeta, dh0); dg is w.r.t. the raw per-token gate.
+    Returns dict(dq, dk, dv, dg, dbeta, dh0); dg is w.r.t. the raw per-token gate; with
+    ``use_qk_l2norm`` / ``beta_sigmoid`` dq, dk and dbeta are w.r.t. the raw inputs.
     """
     q, k, v, g, beta, h0, dO, dht = map(_f64, (q, k, v, g, beta, h0, dO, dht))
+    q_raw, k_raw, beta_raw = q, k, beta
+    if use_qk_l2norm:
+        q, k = l2norm(q)[0], l2norm(k)[0]
+    if beta_sigmoid:
+        beta = sigmoid(beta)
     p, keep, n_state = _problem(q, v, per_key, use_exp2, scale, cu, n_threads)
     out = dict(dq=np.zeros(q.shape), dk=np.zeros(k.shape), dv=np.zeros(v.shape),
                dg=np.zeros(g.shape), dbeta=np.zeros(beta.shape),
@@ -142,6 +180,12 @@ def backward(q, k, v, g, beta, h0=None, dO=None, dht=None, *, scale=None, per_ke
                               _ptr(out["dh0"]))
     assert rc == 0
     del keep
+    if use_qk_l2norm:
+        out["dq"] = l2norm_backward(q_raw, out["dq"])
+        out["dk"] = l2norm_backward(k_raw, out["dk"])
+    if beta_sigmoid:
+        sb = sigmoid(beta_raw)
+        out["dbeta"] = out["dbeta"] * sb * (1.0 - sb)
     return out
 
 

@@ -88,3 +88,31 @@ def test_backward_bf16_final_state_gradient(use_exp2):
     inp.use_exp2 = use_exp2
     dht = np.random.default_rng(7).standard_normal((2, 2, 128, 128)).astype(np.float32)
     _compare(_run(inp, dht), _oracle(inp, dht), TOL["bf16"])
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("per_key", [False, True])
+def test_forward_and_backward_with_input_maps(dtype, per_key):
+    """Raw q, k (normalised by the prologue) and raw beta (sigmoid in the prologue):
+    o, ht and every gradient w.r.t. the raw inputs against the oracle's chain rule."""
+    import torch
+    from gated_delta_rule_28_gb300 import api, binding, workloads
+    inp = workloads.make(4 if per_key else 5, B=2, T=150, H=2, dtype=dtype, with_h0=True, with_dO=True)
+    rng = np.random.default_rng(31)
+    dt = torch.bfloat16 if dtype == "bf16" else torch.float32
+    dev = lambda x: torch.from_numpy(np.ascontiguousarray(x, np.float32)).to("cuda", dt)  # noqa: E731
+    q, k = dev(2.0 * rng.standard_normal(inp.q.shape)), dev(0.3 * rng.standard_normal(inp.k.shape))
+    braw = dev(rng.standard_normal(inp.beta.shape))
+    d = to_dev(inp)
+    kw = dict(use_exp2=inp.use_exp2, use_qk_l2norm=True, use_beta_sigmoid=True)
+    f = api.chunk_gated_delta_rule_fwd(q, k, d["v"], d["g"], braw, h0=d["h0"], return_g_cumsum=True,
+                                       return_A=True, **kw)
+    gr = api.chunk_gated_delta_rule_bwd(q, k, d["v"], f["g_cumsum"], braw, f["A"], d["dO"], h0=d["h0"],
+                                        **kw)
+    binding.gdn_device_status()
+    okw = dict(per_key=inp.per_key, use_exp2=inp.use_exp2, use_qk_l2norm=True, beta_sigmoid=True)
+    o, ht = R.forward(host(q), host(k), inp.v, inp.g, host(braw), inp.h0, **okw)
+    assert rel_frob(host(f["o"]), o) <= TOL[dtype]
+    assert rel_frob(host(f["ht"]), ht) <= TOL[dtype]
+    want = R.backward(host(q), host(k), inp.v, inp.g, host(braw), inp.h0, inp.dO, None, **okw)
+    _compare({n: host(x) for n, x in gr.items()}, want, TOL[dtype])

@@ -170,6 +170,26 @@ def test_segment_summary_merge_and_correction(per_key):
     assert rel_frob(host(out["o"]), host(whole["o"])) <= TOL["bf16"]
 
 
+def test_split_forward_with_input_maps():
+    """Segment summaries, merge and corrected run on raw k (normalised) and raw beta
+    (sigmoid), per-key base-2 gates, against the unsplit oracle on the mapped inputs."""
+    import torch
+    from gated_delta_rule_28_gb300 import workloads
+    inp = workloads.make(4, B=1, T=700, H=2, with_h0=True)
+    rng = np.random.default_rng(33)
+    dev = lambda x: torch.from_numpy(np.ascontiguousarray(x, np.float32)).to("cuda", torch.bfloat16)  # noqa: E731
+    q, k, braw = dev(rng.standard_normal(inp.q.shape)), dev(rng.standard_normal(inp.k.shape)), \
+        dev(rng.standard_normal(inp.beta.shape))
+    d = to_dev(inp)
+    out = _api().split_forward(q, k, d["v"], d["g"], braw, 256, h0=d["h0"], use_exp2=True,
+                               use_qk_l2norm=True, use_beta_sigmoid=True)
+    _status()
+    o, ht = R.forward(host(q), host(k), inp.v, inp.g, host(braw), inp.h0, per_key=True, use_exp2=True,
+                      use_qk_l2norm=True, beta_sigmoid=True)
+    assert rel_frob(host(out["o"]), o) <= TOL["bf16"]
+    assert rel_frob(host(out["ht"]), ht) <= TOL["bf16"]
+
+
 def test_device_metadata_check_flags_bad_offsets():
     """Non-increasing device offsets are skipped and reported, not faulted on."""
     import torch

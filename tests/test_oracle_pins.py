@@ -226,3 +226,52 @@ def test_packed_documents_equal_separate_runs():
                         dO[None, s], None)
         np.testing.assert_allclose(gr["dk"][s], gn["dk"][0], atol=1e-12)
         np.testing.assert_allclose(gr["dh0"][n], gn["dh0"][0], atol=1e-12)
+
+
+@pytest.mark.parametrize("per_key", [False, True])
+def test_input_maps_reverse_mode_matches_central_differences(per_key):
+    """The in-kernel q/k norm and beta sigmoid: the oracle's chain rule through both maps
+    against central differences of its own forward on raw inputs."""
+    rng = np.random.default_rng(13)
+    q, k, v, g, beta, h0 = _rand_case(rng, 1, 11, 2, 6, 3, per_key=per_key)
+    q, k = 3.0 * rng.standard_normal(q.shape), 0.2 * rng.standard_normal(k.shape)  # raw, unnormalised
+    braw = rng.standard_normal(beta.shape)
+    dO = rng.standard_normal(v.shape)
+    kw = dict(per_key=per_key, use_exp2=per_key, use_qk_l2norm=True, beta_sigmoid=True)
+    o, ht = R.forward(q, k, v, g, braw, h0, **kw)
+    dht = rng.standard_normal(ht.shape)
+    grads = R.backward(q, k, v, g, braw, h0, dO, dht, **kw)
+
+    def loss(*a):
+        o, ht = R.forward(*a, **kw)
+        return float((o * dO).sum() + (ht * dht).sum())
+
+    args = [q, k, v, g, braw, h0]
+    for i, name in enumerate(["dq", "dk", "dv", "dg", "dbeta", "dh0"]):
+        d = rng.standard_normal(args[i].shape)
+        eps = 1e-6
+        hi = [x.copy() for x in args]
+        lo = [x.copy() for x in args]
+        hi[i] += eps * d
+        lo[i] -= eps * d
+        fd = (loss(*hi) - loss(*lo)) / (2 * eps)
+        an = float((grads[name] * d).sum())
+        assert abs(fd - an) <= 1e-6 * max(1.0, abs(an)), (name, fd, an)
+
+
+def test_input_maps_fixed_points():
+    """sigmoid(0) = 1/2 exactly; the norm is invariant to scaling its input when
+    sum x^2 >> eps; a row with sum x^2 = eps comes out with squared norm exactly 1/2."""
+    rng = np.random.default_rng(14)
+    q, k, v, g, beta, h0 = _rand_case(rng, 1, 9, 1, 4, 3)
+    o_half, ht_half = R.forward(q, k, v, g, np.full_like(beta, 0.5), h0)
+    o_sig, ht_sig = R.forward(q, k, v, g, np.zeros_like(beta), h0, beta_sigmoid=True)
+    np.testing.assert_array_equal(o_sig, o_half)
+    np.testing.assert_array_equal(ht_sig, ht_half)
+    qr, kr = 5.0 * rng.standard_normal(q.shape), 7.0 * rng.standard_normal(k.shape)
+    o1, _ = R.forward(qr, kr, v, g, beta, h0, use_qk_l2norm=True)
+    o2, _ = R.forward(1e3 * qr, 1e3 * kr, v, g, beta, h0, use_qk_l2norm=True)
+    np.testing.assert_allclose(o1, o2, rtol=1e-6, atol=1e-9)
+    x = np.full((1, 1, 1, 4), math.sqrt(R.L2_EPS / 4))  # sum x^2 = eps
+    xn, _ = R.l2norm(x)
+    assert abs(float((xn * xn).sum()) - 0.5) < 1e-15
