@@ -149,8 +149,69 @@ bool use_tensor_cores(const gdn_problem *p) {
   return p->dtype == GDN_DTYPE_BF16 && p->gate_kind == GDN_GATE_SCALAR;
 }
 
+// bf16 inputs with one gate per key channel run on the per-key tensor-core path (prep
+// kernel + chain kernel over the per-chunk blobs)
+bool use_kda_tc(const gdn_problem *p) {
+  return p->dtype == GDN_DTYPE_BF16 && p->gate_kind == GDN_GATE_PER_KEY;
+}
+int64_t n_chunk_slots(const gdn_problem *p);
+size_t align256(size_t x);
+size_t blob_bytes(const gdn_problem *p) {
+  return align256((size_t)n_chunk_slots(p) * p->H * gdn::kda::BLOB_BYTES);
+}
+// bf16 summaries (either gate kind) run on the tensor-core prep + chain kernels
+size_t summary_blob_bytes(const gdn_problem *p) {
+  return p->dtype == GDN_DTYPE_BF16 ? blob_bytes(p) : 0;
+}
+gdn::KdaPrepArgs kda_prep_args(const gdn_problem *p, const void *q, const void *k, const void *v,
+                               const float *g, const float *g_cum_in, const void *beta, void *blob,
+                               float *g_cumsum, float *A, float scale, int *flag) {
+  gdn::KdaPrepArgs r{};
+  r.q = q;
+  r.k = k;
+  r.v = v;
+  r.beta = beta;
+  r.g = g;
+  r.g_cum_in = g_cum_in;
+  r.blob = static_cast<uint8_t *>(blob);
+  r.g_cumsum = g_cumsum;
+  r.A = A;
+  r.T = p->T;
+  r.H = p->H;
+  r.scale = scale;
+  r.use_exp2 = p->use_exp2;
+  const bool packed = p->layout == GDN_LAYOUT_TND;
+  r.cu = packed ? p->cu_seqlens : nullptr;
+  r.chunk_indices = packed ? p->chunk_indices : nullptr;
+  r.num_seqs = p->num_seqs;
+  r.no_q = q == nullptr;
+  r.scalar_gate = p->gate_kind == GDN_GATE_SCALAR;
+  r.dev_flag = flag;
+  return r;
+}
+gdn::KdaChainArgs kda_chain_args(const gdn::SimtFwdArgs &a, const void *blob) {
+  gdn::KdaChainArgs c{};
+  c.blob = static_cast<const uint8_t *>(blob);
+  c.h0 = a.h0;
+  c.o = static_cast<__nv_bfloat16 *>(a.o);
+  c.ht = a.ht;
+  c.h_chunks = a.h_chunks;
+  c.S_ext = a.S_ext;
+  c.M = a.M;
+  c.B = a.B;
+  c.T = a.T;
+  c.H = a.H;
+  c.cu = a.cu;
+  c.num_seqs = a.num_seqs;
+  c.num_chunks = a.num_chunks;
+  c.seg_len = a.seg_len;
+  c.nseg = a.nseg;
+  c.summary = a.summary;
+  c.dev_flag = a.dev_flag;
+  return c;
+}
+
 // ---- input maps: L2 norm of q and k, sigmoid of beta ----------------------------------
-bool has_input_maps(const gdn_problem *p) { return p->use_qk_l2norm || p->use_beta_sigmoid; }
 int64_t token_rows(const gdn_problem *p) {
   return p->layout == GDN_LAYOUT_TND ? (int64_t)p->T : (int64_t)p->B * p->T;
 }
@@ -211,6 +272,7 @@ size_t x_part_bytes(const gdn_problem *p) {
   return align256((size_t)n_chunk_slots(p) * p->H * 2 * GDN_CHUNK * GDN_CHUNK * 2);
 }
 size_t x_ws_bytes(const gdn_problem *p) {
+  if (use_kda_tc(p)) return blob_bytes(p);
   if (!use_tensor_cores(p)) return 0;
   return x_part_bytes(p) + align256((size_t)n_chunk_slots(p) * p->H * gdn::F_TAB * sizeof(float));
 }
@@ -401,7 +463,11 @@ gdn_status gdn_chunk_fwd(const gdn_problem *pin, const void *q, const void *k, c
   const int runs = a.cu ? p->num_seqs : (a.nseg > 0 ? p->B * a.nseg : p->B);
   if (a.nseg > 0 && p->T == 0) return ok();
   cudaError_t e;
-  if (use_tensor_cores(p)) {
+  if (use_kda_tc(p)) {
+    const gdn::KdaPrepArgs pa = kda_prep_args(p, q, k, v, g, nullptr, beta, ws, g_cumsum, A, a.scale, a.dev_flag);
+    if ((e = gdn::launch_kda_prep(pa, (int)n_chunk_slots(p), s)) != cudaSuccess) return cuda_fail(e, "KDA prep launch");
+    e = gdn::launch_kda_chain(kda_chain_args(a, ws), dim3(2, p->H, runs), s);
+  } else if (use_tensor_cores(p)) {
     const gdn::UtArgs u = ut_args(p, k, g, nullptr, beta, ws, A, g_cumsum, a.dev_flag);
     if ((e = gdn::launch_ut(u, (int)n_chunk_slots(p), s)) != cudaSuccess) return cuda_fail(e, "UT transform launch");
     a.xw = u.xw;
@@ -504,7 +570,12 @@ gdn_status gdn_chunk_bwd(const gdn_problem *pin, const void *q, const void *k, c
   f.A_in = A;
   f.dev_flag = flag;
   cudaError_t e;
-  if (use_tensor_cores(p)) {  // X recomputed from the saved cumulative gate (same values as A)
+  if (use_kda_tc(p)) {  // blobs recomputed from the saved cumulative gate, then the chain
+    const gdn::KdaPrepArgs pa = kda_prep_args(p, q, k, v, nullptr, g_cumsum, beta, xw, nullptr, nullptr,
+                                              f.scale, flag);
+    if ((e = gdn::launch_kda_prep(pa, (int)n_chunk_slots(p), s)) != cudaSuccess) return cuda_fail(e, "KDA prep launch");
+    e = gdn::launch_kda_chain(kda_chain_args(f, xw), dim3(2, p->H, runs), s);
+  } else if (use_tensor_cores(p)) {  // X recomputed from the saved cumulative gate (same values as A)
     const gdn::UtArgs u = ut_args(p, k, nullptr, g_cumsum, beta, xw, nullptr, nullptr, flag);
     if ((e = gdn::launch_ut(u, (int)n_chunk_slots(p), s)) != cudaSuccess) return cuda_fail(e, "UT transform launch");
     f.xw = u.xw;
@@ -578,7 +649,8 @@ gdn_status kda_segment_summary_workspace(const gdn_problem *p, int32_t segment_l
   if (segment_len <= 0 || segment_len % GDN_CHUNK != 0)
     return fail(GDN_ERR_INVALID_ARGUMENT, "segment_len must be a positive multiple of 64, got %d",
                 segment_len);
-  *bytes = map_part_bytes(p);
+  const gdn_problem m = mapped_problem(p);
+  *bytes = map_part_bytes(p) + summary_blob_bytes(&m);
   return ok();
 }
 
@@ -601,8 +673,9 @@ gdn_status kda_segment_summary(const gdn_problem *pin, const void *k, const void
   REQUIRE_PTR(S_ext, "S_ext");
   REQUIRE_PTR(M, "M");
   const size_t maps = map_part_bytes(pin);
-  if (maps > 0 && (!ws || ws_bytes < maps))
-    return fail(GDN_ERR_WORKSPACE, "segment summary workspace needs %zu bytes, got %zu", maps,
+  const size_t need = maps + summary_blob_bytes(p);
+  if (need > 0 && (!ws || ws_bytes < need))
+    return fail(GDN_ERR_WORKSPACE, "segment summary workspace needs %zu bytes, got %zu", need,
                 ws ? ws_bytes : (size_t)0);
   if (ws && !aligned16(ws)) return fail(GDN_ERR_INVALID_ARGUMENT, "ws must be 16-byte aligned");
   int dev;
@@ -631,9 +704,17 @@ gdn_status kda_segment_summary(const gdn_problem *pin, const void *k, const void
   a.nseg = (int)div_up(p->T, segment_len);
   a.summary = 1;
   a.dev_flag = device_flag_ptr();
-  const dim3 grid((GDN_DV + GDN_DK) / gdn::simt_fwd_bv(), p->H, p->B * a.nseg);
-  cudaError_t e = gdn::launch_simt_fwd(a, p->gate_kind == GDN_GATE_PER_KEY,
-                                       p->dtype == GDN_DTYPE_BF16, grid, s);
+  cudaError_t e;
+  if (summary_blob_bytes(p) > 0) {  // bf16: prep (no q) + chain on [V | I] columns
+    void *blob = static_cast<char *>(ws) + maps;
+    const gdn::KdaPrepArgs pa = kda_prep_args(p, nullptr, k, v, g, nullptr, beta, blob, nullptr, nullptr, 1.f,
+                                              a.dev_flag);
+    if ((e = gdn::launch_kda_prep(pa, (int)n_chunk_slots(p), s)) != cudaSuccess) return cuda_fail(e, "KDA prep launch");
+    e = gdn::launch_kda_chain(kda_chain_args(a, blob), dim3(4, p->H, p->B * a.nseg), s);
+  } else {
+    const dim3 grid((GDN_DV + GDN_DK) / gdn::simt_fwd_bv(), p->H, p->B * a.nseg);
+    e = gdn::launch_simt_fwd(a, p->gate_kind == GDN_GATE_PER_KEY, false, grid, s);
+  }
   if (e != cudaSuccess) return cuda_fail(e, "segment summary launch");
   return ok();
 }

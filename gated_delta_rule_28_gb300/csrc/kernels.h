@@ -119,6 +119,54 @@ cudaError_t launch_bwd_local(const BwdArgs &a, bool per_key, bool bf16, cudaStre
 // tcgen05 reverse state recurrence (bf16, scalar gate); needs a.xw / a.ftab
 cudaError_t launch_tc_dhu(const BwdArgs &a, int runs, cudaStream_t st);
 
+// ---- per-key (KDA) tensor-core path ----------------------------------------------------
+// The prep kernel writes, for every (chunk, head), one blob of bf16 tiles already in the
+// 128-byte-swizzled shared-memory layout of the chain kernel's operands, so that the chain
+// kernel fetches each with one bulk copy (G = in-chunk cumulative per-key gate, b the base):
+namespace kda {
+constexpr int BLOB_WQ = 0;      // [w; scale Q b^G] (128 rows x 128 keys, K-major: two K-blocks
+                                //  16 KB apart, each the 64 w rows then the 64 Q rows)
+constexpr int BLOB_KL = 32768;  // K b^(G_last - G): 64 token rows, two 64-key groups 8 KB apart
+constexpr int BLOB_U = 49152;   // u = X diag(beta) V: 64 token rows, two 64-column halves
+constexpr int BLOB_AQ = 65536;  // scale A_qk: 64 x 64, K-major
+constexpr int BLOB_EL = 73728;  // b^(G_last) per key, fp32 [128]
+constexpr int BLOB_BYTES = 74240;
+}  // namespace kda
+
+struct KdaPrepArgs {
+  const void *q, *k, *v, *beta;  // bf16
+  const float *g;                // raw per-key gate [rows, H, K], or
+  const float *g_cum_in;         // the saved cumulative gate (nullable)
+  uint8_t *blob;                 // [slots * H][BLOB_BYTES]
+  float *g_cumsum, *A;           // nullable outputs
+  int T, H;
+  float scale;
+  int use_exp2;
+  const int32_t *cu, *chunk_indices;  // packed documents, or nullptr
+  int num_seqs;
+  int no_q;         // 1: q is not given (segment summary): the Q tile and A_qk are not written
+  int scalar_gate;  // 1: g is one gate per (token, head), the same for every key channel
+  int *dev_flag;
+};
+cudaError_t launch_kda_prep(const KdaPrepArgs &a, int slots, cudaStream_t st);
+
+// Chain kernel over the blobs: the state recurrence and the output (forward, correction
+// run), or the segment summary's [V | I] recurrence (summary = 1: grid x = 4 column slices).
+struct KdaChainArgs {
+  const uint8_t *blob;
+  const float *h0;  // [N,H,K,V]; segment mode [B,H,nseg,K,V]
+  __nv_bfloat16 *o;
+  float *ht, *h_chunks;
+  float *S_ext, *M;  // summary mode outputs
+  int B, T, H;
+  const int32_t *cu;
+  int num_seqs, num_chunks;
+  int seg_len, nseg;
+  int summary;
+  int *dev_flag;
+};
+cudaError_t launch_kda_chain(const KdaChainArgs &a, dim3 grid, cudaStream_t st);
+
 // The optional input maps (q, k L2 norm; beta sigmoid) before the chunk kernels, and their
 // chain rules after the backward (in place on dq, dk, dbeta).
 struct InputMapArgs {

@@ -112,6 +112,31 @@ def test_packed_documents_small():
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 @pytest.mark.parametrize("per_key", [False, True])
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_packed_documents_per_key_gate(dtype):
+    """Per-key base-2 gates on packed documents of 1 to 887 tokens with per-document states:
+    every slot of the forward (the per-key tensor-core path for bf16)."""
+    from gated_delta_rule_28_gb300 import workloads
+    inp = workloads.make(4, B=1, T=1500, H=2, dtype=dtype)
+    q, k, v, beta, g = (x[0] for x in (inp.q, inp.k, inp.v, inp.beta, inp.g))
+    inp.q, inp.k, inp.v, inp.beta, inp.g = q, k, v, beta, g
+    inp.layout = "TND"
+    inp.cu = np.array([0, 1, 64, 129, 613, 1500], np.int32)
+    inp.h0 = np.random.default_rng(8).standard_normal((5, 2, 128, 128)).astype(np.float32) * 0.1
+    d = to_dev(inp)
+    out = _api().chunk_gated_delta_rule_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], h0=d["h0"],
+                                            cu_seqlens=inp.cu, use_exp2=True, return_h_chunks=True,
+                                            return_g_cumsum=True, return_A=True)
+    _status()
+    o, ht = oracle_fwd(inp)
+    c = chunk_ref(inp)
+    assert rel_frob(host(out["o"]), o) <= TOL[dtype]
+    assert rel_frob(host(out["ht"]), ht) <= TOL[dtype]
+    assert rel_frob(host(out["h_chunks"]), c["h_chunks"]) <= TOL[dtype]
+    assert rel_frob(host(out["g_cumsum"]), c["g_cumsum"]) <= 1e-6
+    assert rel_frob(host(out["A"]), c["A"]) <= TOL[dtype]
+
+
 def test_in_kernel_l2_norm(dtype, per_key):
     """use_qk_l2norm: q, k normalised in-kernel as x / sqrt(sum x^2 + 1e-6); raw q and k
     of very different sizes, a ragged last chunk and an initial state."""
