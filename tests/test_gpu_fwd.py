@@ -110,8 +110,6 @@ def test_packed_documents_small():
     assert rel_frob(host(out["A"]), c["A"]) <= TOL["bf16"]
 
 
-@pytest.mark.parametrize("dtype", ["f32", "bf16"])
-@pytest.mark.parametrize("per_key", [False, True])
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
 def test_packed_documents_per_key_gate(dtype):
     """Per-key base-2 gates on packed documents of 1 to 887 tokens with per-document states:
@@ -137,6 +135,8 @@ def test_packed_documents_per_key_gate(dtype):
     assert rel_frob(host(out["A"]), c["A"]) <= TOL[dtype]
 
 
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("per_key", [False, True])
 def test_in_kernel_l2_norm(dtype, per_key):
     """use_qk_l2norm: q, k normalised in-kernel as x / sqrt(sum x^2 + 1e-6); raw q and k
     of very different sizes, a ragged last chunk and an initial state."""
