@@ -297,9 +297,14 @@ def _time_ms(fn, reps, warmup, stream):
     return a.elapsed_time(b) / reps
 
 
-def secondary_rows(dev, hbm_peak):
+ROWS = ("packed_fwd", "kda_split_fwd", "train_fwd_bwd")
+
+
+def secondary_rows(dev, hbm_peak, only=None, reps=None):
     """The other scope rows, each on its own workload at full size (device-generated
-    seeded inputs with the workloads' distributions; timing only, parity is in tests)."""
+    seeded inputs with the workloads' distributions; timing only, parity is in tests).
+    ``only`` restricts the run to one row; ``reps`` overrides the timed repetitions
+    (a profiler capture wants few)."""
     import torch
     from gated_delta_rule_28_gb300 import api, binding as Bd
     g = torch.Generator(device=dev)
@@ -318,41 +323,46 @@ def secondary_rows(dev, hbm_peak):
         gg = -gscale * torch.nn.functional.softplus(torch.randn(gshape, device=dev, generator=g))
         return q, k, v, gg, beta
 
+    want = lambda name: only is None or only == name  # noqa: E731
+    R = (lambda n: n) if reps is None else (lambda n: reps)  # noqa: E731
     with torch.cuda.stream(stream):
-        # packed documents: 32768 tokens, H=32, lengths U[37, 8192]
         from gated_delta_rule_28_gb300 import workloads
-        lens = workloads.doc_lengths(np.random.default_rng(2), 32768)
-        cu = np.concatenate([[0], np.cumsum(lens)])
-        q, k, v, gg, beta = common((32768, 32, 128), (32768, 32), 0.1)
-        vl = api.Varlen(cu, 32768, dev)
-        ms = _time_ms(lambda: api.chunk_gated_delta_rule_fwd(q, k, v, gg, beta, varlen=vl,
-                                                             stream=stream.cuda_stream), 5, 2, stream)
-        byts = 32768 * 32 * BYTES_PER_TOKEN_HEAD + len(lens) * 32 * STATE_BYTES
-        out["packed_fwd"] = {"workload": "gdn_packed_bf16", "ms": ms, "tokens_per_s": 32768 / ms * 1e3,
-                             "hbm_frac": byts / (ms * 1e-3) / 1e9 / hbm_peak, "docs": int(len(lens))}
-        del q, k, v, gg, beta
-        # KDA long context: per-key base-2 gates, 16 segments of 4096 vs unsplit
-        q, k, v, gg, beta = common((1, 65536, 8, 128), (1, 65536, 8, 128), 0.05)
-        ms_split = _time_ms(lambda: api.split_forward(q, k, v, gg, beta, 4096, use_exp2=True,
-                                                      stream=stream.cuda_stream), 2, 1, stream)
-        ms_whole = _time_ms(lambda: api.chunk_gated_delta_rule_fwd(q, k, v, gg, beta, use_exp2=True,
-                                                                   stream=stream.cuda_stream), 1, 1, stream)
-        out["kda_split_fwd"] = {"workload": "kda_long_bf16", "ms_split": ms_split, "ms_unsplit": ms_whole,
-                                "tokens_per_s_split": 65536 / ms_split * 1e3}
-        del q, k, v, gg, beta
-        # training step: forward with saved slots + backward, B8 H16 T8192
-        q, k, v, gg, beta = common((8, 8192, 16, 128), (8, 8192, 16), 0.1)
-        h0 = 0.1 * torch.randn((8, 16, 128, 128), device=dev, generator=g)
-        dO = torch.randn((8, 8192, 16, 128), device=dev, generator=g).to(torch.bfloat16)
-        f = api.chunk_gated_delta_rule_fwd(q, k, v, gg, beta, h0=h0, return_g_cumsum=True,
-                                           return_A=True, stream=stream.cuda_stream)
-        ms_f = _time_ms(lambda: api.chunk_gated_delta_rule_fwd(q, k, v, gg, beta, h0=h0, return_g_cumsum=True,
-                                                               return_A=True, stream=stream.cuda_stream),
-                        2, 1, stream)
-        ms_b = _time_ms(lambda: api.chunk_gated_delta_rule_bwd(q, k, v, f["g_cumsum"], beta, f["A"], dO,
-                                                               h0=h0, stream=stream.cuda_stream), 2, 1, stream)
-        out["train_fwd_bwd"] = {"workload": "gdn_train_bf16", "ms_fwd": ms_f, "ms_bwd": ms_b,
-                                "tokens_per_s": 8 * 8192 / (ms_f + ms_b) * 1e3}
+        if want("packed_fwd"):  # packed documents: 32768 tokens, H=32, lengths U[37, 8192]
+            lens = workloads.doc_lengths(np.random.default_rng(2), 32768)
+            cu = np.concatenate([[0], np.cumsum(lens)])
+            q, k, v, gg, beta = common((32768, 32, 128), (32768, 32), 0.1)
+            vl = api.Varlen(cu, 32768, dev)
+            ms = _time_ms(lambda: api.chunk_gated_delta_rule_fwd(q, k, v, gg, beta, varlen=vl,
+                                                                 stream=stream.cuda_stream), R(5), 2, stream)
+            byts = 32768 * 32 * BYTES_PER_TOKEN_HEAD + len(lens) * 32 * STATE_BYTES
+            out["packed_fwd"] = {"workload": "gdn_packed_bf16", "ms": ms, "tokens_per_s": 32768 / ms * 1e3,
+                                 "hbm_frac": byts / (ms * 1e-3) / 1e9 / hbm_peak, "docs": int(len(lens))}
+            del q, k, v, gg, beta
+        if want("kda_split_fwd"):  # KDA long context: per-key base-2 gates, 16 segments of 4096
+            q, k, v, gg, beta = common((1, 65536, 8, 128), (1, 65536, 8, 128), 0.05)
+            ms_split = _time_ms(lambda: api.split_forward(q, k, v, gg, beta, 4096, use_exp2=True,
+                                                          stream=stream.cuda_stream), R(5), 2, stream)
+            ms_whole = _time_ms(lambda: api.chunk_gated_delta_rule_fwd(q, k, v, gg, beta, use_exp2=True,
+                                                                       stream=stream.cuda_stream), R(5), 2, stream)
+            # algorithmic bytes of the scan: q, k, v, o bf16, per-key g fp32, beta bf16, final state
+            kda_bytes = 65536 * 8 * (4 * 256 + 512 + 2) + 8 * STATE_BYTES
+            out["kda_split_fwd"] = {"workload": "kda_long_bf16", "ms_split": ms_split, "ms_unsplit": ms_whole,
+                                    "tokens_per_s_split": 65536 / ms_split * 1e3,
+                                    "hbm_frac_split": kda_bytes / (ms_split * 1e-3) / 1e9 / hbm_peak}
+            del q, k, v, gg, beta
+        if want("train_fwd_bwd"):  # training step: forward with saved slots + backward, B8 H16 T8192
+            q, k, v, gg, beta = common((8, 8192, 16, 128), (8, 8192, 16), 0.1)
+            h0 = 0.1 * torch.randn((8, 16, 128, 128), device=dev, generator=g)
+            dO = torch.randn((8, 8192, 16, 128), device=dev, generator=g).to(torch.bfloat16)
+            f = api.chunk_gated_delta_rule_fwd(q, k, v, gg, beta, h0=h0, return_g_cumsum=True,
+                                               return_A=True, stream=stream.cuda_stream)
+            ms_f = _time_ms(lambda: api.chunk_gated_delta_rule_fwd(q, k, v, gg, beta, h0=h0, return_g_cumsum=True,
+                                                                   return_A=True, stream=stream.cuda_stream),
+                            R(2), 1, stream)
+            ms_b = _time_ms(lambda: api.chunk_gated_delta_rule_bwd(q, k, v, f["g_cumsum"], beta, f["A"], dO,
+                                                                   h0=h0, stream=stream.cuda_stream), R(2), 1, stream)
+            out["train_fwd_bwd"] = {"workload": "gdn_train_bf16", "ms_fwd": ms_f, "ms_bwd": ms_b,
+                                    "tokens_per_s": 8 * 8192 / (ms_f + ms_b) * 1e3}
     Bd.gdn_device_status(stream.cuda_stream)
     return out
 
@@ -523,11 +533,22 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-rows", action="store_true", help="skip the other scope rows' timings")
+    ap.add_argument("--row", choices=ROWS, help="time only this secondary row and print it (profiling)")
+    ap.add_argument("--reps", type=int, default=None, help="timed repetitions of --row")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":
         return run_reference(args)
+    if args.row:
+        import torch
+        from gated_delta_rule_28_gb300 import build as gbuild
+        gbuild.build()
+        torch.cuda.set_device(0)
+        hbm, _, _ = _peaks()
+        print(json.dumps(secondary_rows(torch.device("cuda", 0), hbm, only=args.row, reps=args.reps)),
+              flush=True)
+        return 0
     return run_ours(args)
 
 
