@@ -300,11 +300,12 @@ def _time_ms(fn, reps, warmup, stream):
 ROWS = ("packed_fwd", "kda_split_fwd", "train_fwd_bwd")
 
 
-def secondary_rows(dev, hbm_peak, only=None, reps=None):
+def secondary_rows(dev, hbm_peak, only=None, reps=None, kda_tokens=65536):
     """The other scope rows, each on its own workload at full size (device-generated
     seeded inputs with the workloads' distributions; timing only, parity is in tests).
     ``only`` restricts the run to one row; ``reps`` overrides the timed repetitions
-    (a profiler capture wants few)."""
+    (a profiler capture wants few); ``kda_tokens`` shrinks the per-key workload for a
+    profiler capture (same distributions and segment length)."""
     import torch
     from gated_delta_rule_28_gb300 import api, binding as Bd
     g = torch.Generator(device=dev)
@@ -339,15 +340,16 @@ def secondary_rows(dev, hbm_peak, only=None, reps=None):
                                  "hbm_frac": byts / (ms * 1e-3) / 1e9 / hbm_peak, "docs": int(len(lens))}
             del q, k, v, gg, beta
         if want("kda_split_fwd"):  # KDA long context: per-key base-2 gates, 16 segments of 4096
-            q, k, v, gg, beta = common((1, 65536, 8, 128), (1, 65536, 8, 128), 0.05)
+            TK = kda_tokens
+            q, k, v, gg, beta = common((1, TK, 8, 128), (1, TK, 8, 128), 0.05)
             ms_split = _time_ms(lambda: api.split_forward(q, k, v, gg, beta, 4096, use_exp2=True,
                                                           stream=stream.cuda_stream), R(5), 2, stream)
             ms_whole = _time_ms(lambda: api.chunk_gated_delta_rule_fwd(q, k, v, gg, beta, use_exp2=True,
                                                                        stream=stream.cuda_stream), R(5), 2, stream)
             # algorithmic bytes of the scan: q, k, v, o bf16, per-key g fp32, beta bf16, final state
-            kda_bytes = 65536 * 8 * (4 * 256 + 512 + 2) + 8 * STATE_BYTES
+            kda_bytes = TK * 8 * (4 * 256 + 512 + 2) + 8 * STATE_BYTES
             out["kda_split_fwd"] = {"workload": "kda_long_bf16", "ms_split": ms_split, "ms_unsplit": ms_whole,
-                                    "tokens_per_s_split": 65536 / ms_split * 1e3,
+                                    "tokens_per_s_split": TK / ms_split * 1e3, "tokens": TK,
                                     "hbm_frac_split": kda_bytes / (ms_split * 1e-3) / 1e9 / hbm_peak}
             del q, k, v, gg, beta
         if want("train_fwd_bwd"):  # training step: forward with saved slots + backward, B8 H16 T8192
@@ -535,6 +537,7 @@ def main():
     ap.add_argument("--no-rows", action="store_true", help="skip the other scope rows' timings")
     ap.add_argument("--row", choices=ROWS, help="time only this secondary row and print it (profiling)")
     ap.add_argument("--reps", type=int, default=None, help="timed repetitions of --row")
+    ap.add_argument("--kda-tokens", type=int, default=65536, help="tokens of the per-key row (profiling)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -546,8 +549,8 @@ def main():
         gbuild.build()
         torch.cuda.set_device(0)
         hbm, _, _ = _peaks()
-        print(json.dumps(secondary_rows(torch.device("cuda", 0), hbm, only=args.row, reps=args.reps)),
-              flush=True)
+        print(json.dumps(secondary_rows(torch.device("cuda", 0), hbm, only=args.row, reps=args.reps,
+                                        kda_tokens=args.kda_tokens)), flush=True)
         return 0
     return run_ours(args)
 
