@@ -238,15 +238,16 @@ __global__ void __launch_bounds__(NTH, 1) kda_chain_kernel(KdaChainArgs a) {
     chain_sync();
     if (warp == 0) {
       fence_after_sync();
+      // P5 first (the state update waits for it): (K b^(Gl-G))^T v_new, the key tile read
+      // as MN-major A; then PO for the output epilogue
+      mma_ops_w(tmem + T_P5, mnmaj(buf + BUF_KL, 8192), mnmaj(sb + OFF_VN, 0), 64,
+                idesc_bf16(128, 64, false, true, true), false);
+      mma_commit_w(&st.bar_p5);
       if (!summ) {  // PO: A_qk v_new (A rows 64..127 = A_qk)
         mma_ops_w(tmem + T_PO, kmaj(buf + BUF_AQ - 8192, 0), mnmaj(sb + OFF_VN, 0), 64,
                   idesc_bf16(128, 64, false, false, true), false);
         mma_commit_w(&st.bar_po);
       }
-      // P5: (K b^(Gl-G))^T v_new, the key tile read as MN-major A
-      mma_ops_w(tmem + T_P5, mnmaj(buf + BUF_KL, 8192), mnmaj(sb + OFF_VN, 0), 64,
-                idesc_bf16(128, 64, false, true, true), false);
-      mma_commit_w(&st.bar_p5);
     }
     __syncwarp();
     wait_par(&st.bar_p5, c);

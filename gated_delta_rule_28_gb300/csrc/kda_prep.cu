@@ -11,19 +11,21 @@
 //   w     = X diag(beta) (K (.) b^G),  u = X diag(beta) V
 //   and the operands K (.) b^(G_last - G), Q (.) b^G, b^(G_last) of the state recurrence.
 //
-// The gated Gram matrices run on bf16 tensor cores (mma.sync) through a
-// factorisation of Gamma by 16-row blocks: for rows i of block bi and the
-// reference row r = 16 bi, (K K^T (.) Gamma)_ij = sum_d (k_id b^(G_id - G_rd))
-// (k_jd b^(G_rd - G_jd)). For j < r (blocks left of the diagonal) both factors
-// are at most 1 for decaying gates, so nothing overflows; inside the diagonal
-// block the column factor grows with the decay over at most 15 tokens. A row
-// block whose factors would leave the range that fp32 and bf16 represent
-// (exponent above 100 in base 2) is computed term by term with one
-// exponential per (i, j, d) instead, exactly for any gate range.
+// The gated Gram matrices run on bf16 tensor cores (mma.sync) through one
+// reference row per chunk (r = 32, the middle): with e_id = b^(G_id - G_rd),
+//   (K K^T (.) Gamma)_ij = sum_d (k_id e_id) (k_jd / e_jd),
+// and the same for Q K^T; K (.) b^G = (K (.) e) Diag(b^(G_r)), so w is formed from
+// the same tile, and K (.) b^(G_last - G) = (K / e) Diag(b^(G_last - G_r)). Every
+// element then costs one exponential and one reciprocal. A chunk in which some
+// |G_id - G_rd| exceeds 100 (in base 2) would leave the range of fp32 and bf16;
+// it is computed term by term instead, with one exponential per (i, j, d) for the
+// Gram matrices and direct exponentials for the factors, exactly for any gate range.
 //
 // The outputs go to one blob per (chunk, head), in the 128-byte-swizzled
 // layout the chain kernel's operands take in shared memory (kernels.h, kda::).
-// Persistent CTAs of 8 warps, two per SM (about 108 KB of shared memory each).
+// Persistent CTAs of 8 warps, two per SM (about 100 KB of shared memory each):
+// every global load of an item (K, Q, V by cp.async, the gate column of each
+// thread) is issued at once, and one CTA's loads overlap the other's compute.
 #include <algorithm>
 
 #include "common.cuh"
@@ -38,25 +40,30 @@ using namespace tile;
 using namespace kda;
 
 constexpr int NTH = 256;
-// shared memory map (bytes from a 1024-aligned base)
-constexpr int OFF_G = 0;                 // G, fp32 [64][128]
-constexpr int OFF_V = OFF_G + 32768;     // V, bf16 K-major swizzled (2 K-blocks of 64 columns)
-constexpr int OFF_KA = OFF_V + 16384;    // K b^(G - G_ref) (Gram A), later K b^G (B of w)
-constexpr int OFF_QA = OFF_KA + 16384;   // Q b^(G - G_ref) (Gram A), later X diag(beta) in bf16
-constexpr int OFF_KB = OFF_QA + 16384;   // K b^(G_ref - G) of the current row block, later X, T
-constexpr int OFF_L = OFF_KB + 16384;    // L in 16x16 fp32 blocks (blk / bsw of tile_ops)
-constexpr int OFF_SMALL = OFF_L + 10240;
-constexpr int SMEM_BYTES = OFF_SMALL + 1024 + 1024;
-static_assert(10240 + 4096 <= 16384, "X and T fit in the Kb region");
+constexpr int REF = 32;   // reference row of the Gram factorisation
+constexpr int GS = 132;   // row stride (floats) of G: 16-byte aligned, rows shift by 4 banks
+// shared memory map (bytes from a 1024-aligned base); swizzled bf16 tiles hold 64 rows as
+// two K-blocks of 64 columns (8 KB apart)
+constexpr int OFF_G = 0;                // G fp32 [64][GS]; once the factors exist: L, X, T
+constexpr int OFF_K = OFF_G + 34816;    // K, then K e (Gram A and B of w), or K b^G (exact)
+constexpr int OFF_Q = OFF_K + 16384;    // Q, then Q e (Gram A), then X diag(beta) in bf16
+constexpr int OFF_V = OFF_Q + 16384;    // V (B of u)
+constexpr int OFF_KB = OFF_V + 16384;   // K / e (Gram B); exact chunks: L while G is in use
+constexpr int OFF_SMALL = OFF_KB + 16384;
+constexpr int SMEM_BYTES = OFF_SMALL + 2048 + 1024;
+constexpr int L_FLOATS = 10 * 256, X_FLOATS = 10 * 256;  // lower 16x16 blocks (blk / bsw)
+static_assert(64 * GS * 4 <= 34816 && (L_FLOATS + X_FLOATS + 4 * 256) * 4 <= 34816, "G region");
 
-// largest exponent (base 2) a factor may take on the tensor-core path
+// largest |exponent| (base 2) a factor may take on the tensor-core path
 constexpr float EXP_LIMIT = 100.f;
 
 struct Small {
   float beta[64];
   float part[128];
-  int flags;  // bit bi: row block bi takes the exact path
+  float eref[128];  // b^(G_r) per key channel
+  float elr[128];   // b^(G_last - G_r) per key channel
 };
+static_assert(sizeof(Small) <= 2048, "small state");
 
 template <bool E2>
 __device__ __forceinline__ float expo_to_base2(float x) { return E2 ? x : x * 1.4426950408889634f; }
@@ -69,14 +76,14 @@ __device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], 
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-// 8 bf16 of a global row (zeros when the row is not valid)
-__device__ __forceinline__ void load8(const __nv_bfloat16 *p, bool valid, float (&x)[8]) {
-  if (valid) {
-    unpack8(*reinterpret_cast<const uint4 *>(p), x);
-  } else {
-#pragma unroll
-    for (int e = 0; e < 8; ++e) x[e] = 0.f;
-  }
+// byte offset of the 8 columns c0 .. c0+7 of `row` in a swizzled 64-row tile
+__device__ __forceinline__ uint32_t tile_off(int row, int c0) {
+  return (uint32_t)((c0 >> 6) * 8192) + chunk_off(row, (c0 & 63) >> 3);
+}
+__device__ __forceinline__ void load_g8(const float *sG, int i, int c0, float (&g)[8]) {
+  const float4 a = *reinterpret_cast<const float4 *>(sG + i * GS + c0);
+  const float4 b = *reinterpret_cast<const float4 *>(sG + i * GS + c0 + 4);
+  g[0] = a.x; g[1] = a.y; g[2] = a.z; g[3] = a.w; g[4] = b.x; g[5] = b.y; g[6] = b.z; g[7] = b.w;
 }
 
 template <bool E2>
@@ -84,7 +91,9 @@ __global__ void __launch_bounds__(NTH, 2) kda_prep_kernel(KdaPrepArgs a, int64_t
   extern __shared__ uint8_t smem_raw[];
   uint8_t *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   float *sG = reinterpret_cast<float *>(sm + OFF_G);
-  float *sL = reinterpret_cast<float *>(sm + OFF_L);
+  float *sL = sG;  // once the factors are formed
+  float *sX = sG + L_FLOATS;
+  float *sT = sX + X_FLOATS;
   Small &sv = *reinterpret_cast<Small *>(sm + OFF_SMALL);
   const uint32_t sb = smem_u32(sm);
 
@@ -95,6 +104,8 @@ __global__ void __launch_bounds__(NTH, 2) kda_prep_kernel(KdaPrepArgs a, int64_t
   const __nv_bfloat16 *beta = static_cast<const __nv_bfloat16 *>(a.beta);
   const int NT = (a.T + GDN_CHUNK - 1) / GDN_CHUNK;
   const float scale = a.scale;
+  const bool has_q = q != nullptr;
+  const int gq = lane >> 2, t4 = lane & 3;
 
   auto locate = [&](int64_t it, int64_t &r0, int &n) -> bool {
     const int64_t slot = it / H;
@@ -120,29 +131,30 @@ __global__ void __launch_bounds__(NTH, 2) kda_prep_kernel(KdaPrepArgs a, int64_t
   for (int64_t it = blockIdx.x; it < items; it += gridDim.x) {
     int64_t r0 = 0;
     int n = 0;
-    const bool ok = locate(it, r0, n);
-    if (!ok) {  // uniform: every thread read the same chunk index
+    if (!locate(it, r0, n)) {  // uniform: every thread read the same chunk index
       if (tid == 0) raise_device_flag(a.dev_flag, kDevCheck);
       continue;
     }
     const int h = (int)(it % H);
     uint8_t *blob = a.blob + (size_t)it * BLOB_BYTES;
-    auto grow = [&](int i) { return ((r0 + i) * H + h) * (int64_t)GDN_DK; };  // row start, 128 wide
+    auto grow = [&](int i) { return ((r0 + i) * H + h) * (int64_t)GDN_DK; };  // token row, 128 wide
 
-    // ---- loads: V by cp.async (zero past the end), the gate column of this thread, beta ----
+    // ---- every load at once: K, Q, V tiles (zero past the end), the gate column, beta ----
     for (int x = tid; x < 1024; x += NTH) {
       const int r = x >> 4, c16 = x & 15;
       const bool valid = r < n;
-      const __nv_bfloat16 *src = v + ((r0 + (valid ? r : 0)) * H + h) * GDN_DV + c16 * 8;
-      cp_async16(sb + OFF_V + (c16 >> 3) * 8192 + chunk_off(r, c16 & 7), src, valid ? 16u : 0u);
+      const int64_t row = (r0 + (valid ? r : 0)) * H + h;
+      const uint32_t o = (c16 >> 3) * 8192 + chunk_off(r, c16 & 7);
+      cp_async16(sb + OFF_K + o, k + row * GDN_DK + c16 * 8, valid ? 16u : 0u);
+      cp_async16(sb + OFF_Q + o, (has_q ? q : k) + row * GDN_DK + c16 * 8, valid && has_q ? 16u : 0u);
+      cp_async16(sb + OFF_V + o, v + row * GDN_DV + c16 * 8, valid ? 16u : 0u);
     }
     cp_async_commit();
     if (tid < 64) sv.beta[tid] = tid < n ? __bfloat162float(beta[(r0 + tid) * H + h]) : 0.f;
-    if (tid == 0) sv.flags = 0;
     const int d = tid & 127, half = tid >> 7;
-    float gcol[32];
     // gate element of row i for this thread's key channel (a scalar gate serves every channel)
     auto gidx = [&](int i) { return a.scalar_gate ? (r0 + i) * H + h : grow(i) + d; };
+    float gcol[32];
     if (a.g_cum_in) {
 #pragma unroll
       for (int j = 0; j < 32; ++j) gcol[j] = a.g_cum_in[gidx(min(32 * half + j, n - 1))];
@@ -160,163 +172,154 @@ __global__ void __launch_bounds__(NTH, 2) kda_prep_kernel(KdaPrepArgs a, int64_t
       for (int j = 0; j < 32; ++j) gcol[j] += base;
     }
 #pragma unroll
-    for (int j = 0; j < 32; ++j) sG[(32 * half + j) * GDN_DK + d] = gcol[j];
+    for (int j = 0; j < 32; ++j) sG[(32 * half + j) * GS + d] = gcol[j];
     if (a.g_cumsum && !a.g_cum_in && (!a.scalar_gate || d == 0)) {
 #pragma unroll
       for (int j = 0; j < 32; ++j)
         if (32 * half + j < n) a.g_cumsum[gidx(32 * half + j)] = gcol[j];
     }
+    if (half == 1) {  // this thread holds rows 32..63 of its channel: G_r and G_last
+      const float gr = gcol[0], gl = gcol[31];
+      sv.eref[d] = gexp<E2>(gr);
+      sv.elr[d] = gexp<E2>(gl - gr);
+      reinterpret_cast<float *>(blob + BLOB_EL)[d] = gexp<E2>(gl);
+    }
     __syncthreads();
-    if (tid < GDN_DK) reinterpret_cast<float *>(blob + BLOB_EL)[tid] = gexp<E2>(sG[63 * GDN_DK + tid]);
-
-    // ---- pass A (8 keys of one row per step): Q b^G, K b^(Gl - G) to the blob; the Gram
-    // A operands K b^(G - G_ref), Q b^(G - G_ref) with G_ref the row block's first row ----
+    // range of the factors around the reference row
+    bool out_of_range = false;
     {
-      int over = 0;
-      for (int x = tid; x < 1024; x += NTH) {
-        const int i = x >> 4, c0 = (x & 15) * 8;
-        float kv[8], qv[8], gv[8], gl[8], gr[8];
-        load8(k + grow(i) + c0, i < n, kv);
-        load8(q ? q + grow(i) + c0 : nullptr, i < n && q, qv);
-        const int r = i & ~15;
+      const float gr = sG[REF * GS + d];
+#pragma unroll
+      for (int j = 0; j < 32; ++j) out_of_range |= fabsf(expo_to_base2<E2>(gcol[j] - gr)) > EXP_LIMIT;
+    }
+    const bool exact = __syncthreads_or(out_of_range);
+    cp_async_wait<0>();
+    __syncthreads();
+
+    if (exact) {  // Gram matrices term by term while K, Q and G are intact: L -> the Kb region
+      float *sLx = reinterpret_cast<float *>(sm + OFF_KB);
+      for (int p = tid; p < 64 * 64; p += NTH) {
+        const int i = p >> 6, j = p & 63;
+        if ((j >> 4) > (i >> 4)) continue;  // blocks right of the diagonal are never read
+        float sk = 0.f, sq = 0.f;
+        if (j <= i && i < n) {
+          for (int c0 = 0; c0 < GDN_DK; c0 += 8) {
+            float ki[8], kj[8], qi[8], gi[8], gj[8];
+            unpack8(*reinterpret_cast<const uint4 *>(sm + OFF_K + tile_off(i, c0)), ki);
+            unpack8(*reinterpret_cast<const uint4 *>(sm + OFF_K + tile_off(j, c0)), kj);
+            unpack8(*reinterpret_cast<const uint4 *>(sm + OFF_Q + tile_off(i, c0)), qi);
+            load_g8(sG, i, c0, gi);
+            load_g8(sG, j, c0, gj);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              const float gam = gexp<E2>(gi[e] - gj[e]);
+              sk = fmaf(ki[e] * kj[e], gam, sk);
+              sq = fmaf(qi[e] * kj[e], gam, sq);
+            }
+          }
+        }
+        sLx[blk(i >> 4, j >> 4) * 256 + bsw(i & 15, j & 15)] = j < i ? sv.beta[i] * sk : 0.f;
+        if (has_q)
+          *reinterpret_cast<__nv_bfloat16 *>(blob + BLOB_AQ + chunk_off(i, j >> 3) + (j & 7) * 2) =
+              __float2bfloat16_rn(j <= i ? scale * sq : 0.f);
+      }
+      __syncthreads();
+    }
+
+    // ---- factors (8 channels of one token row per step) ----
+    for (int x = tid; x < 1024; x += NTH) {
+      const int i = x >> 4, c0 = (x & 15) * 8;
+      const uint32_t to = tile_off(i, c0);
+      float kv[8], qv[8], gv[8], o1[8], o4[8];
+      unpack8(*reinterpret_cast<const uint4 *>(sm + OFF_K + to), kv);
+      unpack8(*reinterpret_cast<const uint4 *>(sm + OFF_Q + to), qv);
+      load_g8(sG, i, c0, gv);
+      if (!exact) {
+        float gr[8], o2[8], o3[8];
+        load_g8(sG, REF, c0, gr);
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
-          gv[e] = sG[i * GDN_DK + c0 + e];
-          gl[e] = sG[63 * GDN_DK + c0 + e];
-          gr[e] = sG[r * GDN_DK + c0 + e];
+          const int c = c0 + e;
+          const float ef = gexp<E2>(gv[e] - gr[e]);
+          const float rf = __frcp_rn(ef);
+          o1[e] = kv[e] * ef;                      // K e      (Gram A; B of w)
+          o2[e] = qv[e] * ef;                      // Q e      (Gram A)
+          o3[e] = kv[e] * rf;                      // K / e    (Gram B)
+          o4[e] = o3[e] * sv.elr[c];               // K b^(Gl - G)
+          qv[e] = scale * o2[e] * sv.eref[c];      // scale Q b^G
         }
-        float o1[8], o2[8], o3[8], o4[8];
+        *reinterpret_cast<uint4 *>(sm + OFF_KB + to) = pack8(o3);
+        *reinterpret_cast<uint4 *>(sm + OFF_Q + to) = pack8(o2);
+      } else {
+        float gl[8];
+        load_g8(sG, 63, c0, gl);
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
           const float eg = gexp<E2>(gv[e]);
-          o1[e] = scale * qv[e] * eg;                 // Q b^G (scaled)
-          o2[e] = kv[e] * gexp<E2>(gl[e] - gv[e]);    // K b^(Gl - G)
-          const float xr = gv[e] - gr[e];
-          over |= fabsf(expo_to_base2<E2>(xr)) > EXP_LIMIT;
-          const float er = gexp<E2>(xr);
-          o3[e] = kv[e] * er;                         // K b^(G - G_ref)
-          o4[e] = qv[e] * er;                         // Q b^(G - G_ref)
+          o1[e] = kv[e] * eg;                      // K b^G (B of w; no column factor)
+          o4[e] = kv[e] * gexp<E2>(gl[e] - gv[e]); // K b^(Gl - G)
+          qv[e] = scale * qv[e] * eg;              // scale Q b^G
         }
-        const uint32_t co = chunk_off(i, (c0 & 63) >> 3);
-        if (!a.no_q) *reinterpret_cast<uint4 *>(blob + BLOB_WQ + (c0 >> 6) * 16384 + 8192 + co) = pack8(o1);
-        *reinterpret_cast<uint4 *>(blob + BLOB_KL + (c0 >> 6) * 8192 + co) = pack8(o2);
-        *reinterpret_cast<uint4 *>(sm + OFF_KA + (c0 >> 6) * 8192 + co) = pack8(o3);
-        *reinterpret_cast<uint4 *>(sm + OFF_QA + (c0 >> 6) * 8192 + co) = pack8(o4);
-        if (over) atomicOr(&sv.flags, 1 << (i >> 4));
-        over = 0;
       }
+      *reinterpret_cast<uint4 *>(sm + OFF_K + to) = pack8(o1);
+      const uint32_t co = chunk_off(i, (c0 & 63) >> 3);
+      *reinterpret_cast<uint4 *>(blob + BLOB_KL + (c0 >> 6) * 8192 + co) = pack8(o4);
+      if (has_q) *reinterpret_cast<uint4 *>(blob + BLOB_WQ + (c0 >> 6) * 16384 + 8192 + co) = pack8(qv);
     }
+    __syncthreads();  // G is dead from here on: its region takes L, X and T
 
-    // ---- gated Gram matrices, one row block at a time ----
-    for (int bi = 0; bi < 4; ++bi) {
-      const int r = 16 * bi, ncol = 16 * bi + 16;
-      // column operand K b^(G_ref - G) for rows j < ncol
-      for (int x = tid; x < ncol * 16; x += NTH) {
-        const int j = x >> 4, c0 = (x & 15) * 8;
-        float kv[8], o[8];
-        load8(k + grow(j) + c0, j < n, kv);
-        int over = 0;
+    if (!exact) {
+      // ---- L and A_qk: the 10 lower 16x16 blocks of each; warp w takes blocks w, w+8, w+16 ----
+      for (int jb = warp; jb < 20; jb += 8) {
+        const int which = jb >= 10, bidx = jb - 10 * which;  // 0: L from K e, 1: A_qk from Q e
+        const int bi = bidx < 1 ? 0 : bidx < 3 ? 1 : bidx < 6 ? 2 : 3;
+        const int bj = bidx - bi * (bi + 1) / 2;
+        if (which && !has_q) continue;
+        const uint32_t abase = sb + (which ? OFF_Q : OFF_K);
+        float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const float xr = sG[r * GDN_DK + c0 + e] - sG[j * GDN_DK + c0 + e];
-          over |= fabsf(expo_to_base2<E2>(xr)) > EXP_LIMIT;
-          o[e] = kv[e] * gexp<E2>(xr);
+        for (int ks = 0; ks < 8; ++ks) {
+          const int c8 = (2 * ks + (lane >> 4)) & 7;
+          uint32_t af[4], bfr[4];
+          ldsm_x4(abase + (ks >> 2) * 8192 + chunk_off(16 * bi + (lane & 15), c8), af);
+          ldsm_x4(sb + OFF_KB + (ks >> 2) * 8192 + chunk_off(16 * bj + (lane & 15), c8), bfr);
+          mma16816(acc[0], af, bfr[0], bfr[2]);
+          mma16816(acc[1], af, bfr[1], bfr[3]);
         }
-        *reinterpret_cast<uint4 *>(sm + OFF_KB + (c0 >> 6) * 8192 + chunk_off(j, (c0 & 63) >> 3)) = pack8(o);
-        if (over) atomicOr(&sv.flags, 1 << bi);
-      }
-      __syncthreads();
-      const bool exact = (sv.flags >> bi) & 1;
-      if (!exact) {
-        // warp 2 bj + which: block (bi, bj) of L (which 0) or of A_qk (which 1)
-        const int which = warp & 1, bj = warp >> 1;
-        if (bj <= bi && !(which == 1 && a.no_q)) {
-          const uint32_t abase = sb + (which ? OFF_QA : OFF_KA);
-          float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll
-          for (int ks = 0; ks < 8; ++ks) {
-            const int c8 = (2 * ks + (lane >> 4)) & 7;
-            uint32_t af[4], bfr[4];
-            ldsm_x4(abase + (ks >> 2) * 8192 + chunk_off(r + (lane & 15), c8), af);
-            ldsm_x4(sb + OFF_KB + (ks >> 2) * 8192 + chunk_off(16 * bj + (lane & 15), c8), bfr);
-            mma16816(acc[0], af, bfr[0], bfr[2]);
-            mma16816(acc[1], af, bfr[1], bfr[3]);
-          }
-          const int gq = lane >> 2, t4 = lane & 3;
+        for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-          for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-            for (int hr = 0; hr < 2; ++hr) {
-              const int rr = gq + 8 * hr, c = nt * 8 + 2 * t4;
-              const int i = r + rr, j = 16 * bj + c;
+          for (int hr = 0; hr < 2; ++hr) {
+            const int rr = gq + 8 * hr, c = nt * 8 + 2 * t4;
+            const int i = 16 * bi + rr, j = 16 * bj + c;
+            if (which == 0) {
+              const float bt = sv.beta[i];
               float2 val;
-              if (which == 0) {
-                const float bt = sv.beta[i];
-                val.x = j < i ? bt * acc[nt][2 * hr] : 0.f;
-                val.y = j + 1 < i ? bt * acc[nt][2 * hr + 1] : 0.f;
-                *reinterpret_cast<float2 *>(&sL[blk(bi, bj) * 256 + bsw(rr, c)]) = val;
-              } else {
-                val.x = j <= i ? scale * acc[nt][2 * hr] : 0.f;
-                val.y = j + 1 <= i ? scale * acc[nt][2 * hr + 1] : 0.f;
-                *reinterpret_cast<uint32_t *>(blob + BLOB_AQ + chunk_off(i, j >> 3) + (j & 7) * 2) =
-                    pack_bf16(val.x, val.y);
-              }
-            }
-        }
-      } else {
-        // exact: one exponential per (i, j, d), rows of block bi against columns j <= i
-        for (int p = tid; p < 16 * ncol; p += NTH) {
-          const int i = r + p / ncol, j = p % ncol;
-          float sk = 0.f, sq = 0.f;
-          if (j <= i && i < n) {
-            for (int c0 = 0; c0 < GDN_DK; c0 += 8) {
-              float ki[8], kj[8], qi[8];
-              load8(k + grow(i) + c0, true, ki);
-              load8(k + grow(j) + c0, true, kj);
-              load8(q ? q + grow(i) + c0 : nullptr, q != nullptr, qi);
-#pragma unroll
-              for (int e = 0; e < 8; ++e) {
-                const float gam = gexp<E2>(sG[i * GDN_DK + c0 + e] - sG[j * GDN_DK + c0 + e]);
-                sk = fmaf(ki[e] * kj[e], gam, sk);
-                sq = fmaf(qi[e] * kj[e], gam, sq);
-              }
+              val.x = j < i ? bt * acc[nt][2 * hr] : 0.f;
+              val.y = j + 1 < i ? bt * acc[nt][2 * hr + 1] : 0.f;
+              *reinterpret_cast<float2 *>(&sL[blk(bi, bj) * 256 + bsw(rr, c)]) = val;
+            } else {
+              *reinterpret_cast<uint32_t *>(blob + BLOB_AQ + chunk_off(i, j >> 3) + (j & 7) * 2) =
+                  pack_bf16(j <= i ? scale * acc[nt][2 * hr] : 0.f, j + 1 <= i ? scale * acc[nt][2 * hr + 1] : 0.f);
             }
           }
-          const int bj = j >> 4;
-          sL[blk(bi, bj) * 256 + bsw(i - r, j & 15)] = j < i ? sv.beta[i] * sk : 0.f;
-          if (!a.no_q) {
-            const float val = j <= i ? scale * sq : 0.f;
-            *reinterpret_cast<__nv_bfloat16 *>(blob + BLOB_AQ + chunk_off(i, j >> 3) + (j & 7) * 2) =
-                __float2bfloat16_rn(val);
-          }
-        }
       }
-      // A_qk right of the diagonal block is zero
-      if (!a.no_q)
-        for (int x = tid; x < 16 * (64 - ncol) / 8; x += NTH) {
-          const int per = (64 - ncol) / 8, i = r + x / per, c8 = ncol / 8 + x % per;
-          *reinterpret_cast<uint4 *>(blob + BLOB_AQ + chunk_off(i, c8)) = make_uint4(0, 0, 0, 0);
-        }
-      __syncthreads();  // the next row block rewrites the column operand
-    }
-
-    // ---- X = (I + L)^-1 (warps 0..3), meanwhile K b^G as the B operand of w (warps 4..7) ----
-    float *sX = reinterpret_cast<float *>(sm + OFF_KB);
-    float *sT = sX + 10 * 256;
-    if (warp < 4) {
-      solve_blocks(sL, sX, sT, tid);
     } else {
-      for (int x = tid - 128; x < 1024; x += 128) {
-        const int i = x >> 4, c0 = (x & 15) * 8;
-        float kv[8], o[8];
-        load8(k + grow(i) + c0, i < n, kv);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) o[e] = kv[e] * gexp<E2>(sG[i * GDN_DK + c0 + e]);
-        *reinterpret_cast<uint4 *>(sm + OFF_KA + (c0 >> 6) * 8192 + chunk_off(i, (c0 & 63) >> 3)) = pack8(o);
-      }
+      const float *sLx = reinterpret_cast<const float *>(sm + OFF_KB);
+      for (int x = tid; x < L_FLOATS; x += NTH) sL[x] = sLx[x];
     }
+    if (has_q)  // A_qk right of each row's diagonal block is zero
+      for (int x = tid; x < 64 * 8; x += NTH) {
+        const int i = x >> 3, c8 = x & 7;
+        if (c8 >= 2 * ((i >> 4) + 1))
+          *reinterpret_cast<uint4 *>(blob + BLOB_AQ + chunk_off(i, c8)) = make_uint4(0, 0, 0, 0);
+      }
     __syncthreads();
-    // X diag(beta) in bf16 (A of w and u); the fp32 X as the A output
+
+    // ---- X = (I + L)^-1 (warps 0..3) ----
+    if (warp < 4) solve_blocks(sL, sX, sT, tid);
+    __syncthreads();
+    // X diag(beta) in bf16 (A of w and u, into the Q tile) and the fp32 X as the A output
     {
       const int i = tid >> 2, cq = (tid & 3) * 16, bi = i >> 4;
       float vals[16];
@@ -338,19 +341,17 @@ __global__ void __launch_bounds__(NTH, 2) kda_prep_kernel(KdaPrepArgs a, int64_t
       }
 #pragma unroll
       for (int c = 0; c < 16; ++c) vals[c] *= sv.beta[cq + c];
-      *reinterpret_cast<uint4 *>(sm + OFF_QA + chunk_off(i, cq >> 3)) = pack8(vals);
-      *reinterpret_cast<uint4 *>(sm + OFF_QA + chunk_off(i, (cq >> 3) + 1)) = pack8(vals + 8);
+      *reinterpret_cast<uint4 *>(sm + OFF_Q + chunk_off(i, cq >> 3)) = pack8(vals);
+      *reinterpret_cast<uint4 *>(sm + OFF_Q + chunk_off(i, (cq >> 3) + 1)) = pack8(vals + 8);
     }
-    cp_async_wait<0>();
     __syncthreads();
 
-    // ---- w = X diag(beta) (K b^G), u = X diag(beta) V: warp -> 16 rows, 64 columns ----
+    // ---- w = X diag(beta) (K e) Diag(b^G_r), u = X diag(beta) V: warp -> 16 rows, 64 columns ----
     {
       const int mt = warp & 3, n0 = (warp >> 2) * 64;
-      const int gq = lane >> 2, t4 = lane & 3;
 #pragma unroll
       for (int which = 0; which < 2; ++which) {
-        const uint32_t bbase = sb + (which ? OFF_V : OFF_KA);
+        const uint32_t bbase = sb + (which ? OFF_V : OFF_K);
         float acc[8][4];
 #pragma unroll
         for (int nt = 0; nt < 8; ++nt)
@@ -359,7 +360,7 @@ __global__ void __launch_bounds__(NTH, 2) kda_prep_kernel(KdaPrepArgs a, int64_t
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks) {
           uint32_t af[4];
-          ldsm_x4(sb + OFF_QA + chunk_off(16 * mt + (lane & 15), (2 * ks + (lane >> 4)) & 7), af);
+          ldsm_x4(sb + OFF_Q + chunk_off(16 * mt + (lane & 15), (2 * ks + (lane >> 4)) & 7), af);
 #pragma unroll
           for (int np = 0; np < 4; ++np) {  // pairs of 8-column tiles
             const int nc = n0 + 16 * np;
@@ -373,18 +374,21 @@ __global__ void __launch_bounds__(NTH, 2) kda_prep_kernel(KdaPrepArgs a, int64_t
         uint8_t *dst = blob + (which ? BLOB_U : BLOB_WQ);
         const uint32_t kstride = which ? 8192u : 16384u;
 #pragma unroll
-        for (int nt = 0; nt < 8; ++nt)
+        for (int nt = 0; nt < 8; ++nt) {
+          const int c = n0 + 8 * nt + 2 * t4;
+          const bool unit = which || exact;
+          const float f0 = unit ? 1.f : sv.eref[c], f1 = unit ? 1.f : sv.eref[c + 1];
 #pragma unroll
           for (int hr = 0; hr < 2; ++hr) {
-            const int i = 16 * mt + gq + 8 * hr, c = n0 + 8 * nt + 2 * t4;
+            const int i = 16 * mt + gq + 8 * hr;
             *reinterpret_cast<uint32_t *>(dst + (c >> 6) * kstride + chunk_off(i, (c & 63) >> 3) + (c & 7) * 2) =
-                pack_bf16(acc[nt][2 * hr], acc[nt][2 * hr + 1]);
+                pack_bf16(acc[nt][2 * hr] * f0, acc[nt][2 * hr + 1] * f1);
           }
+        }
       }
     }
     __syncthreads();  // shared memory is rewritten by the next item
   }
-  cp_async_wait<0>();
 }
 
 }  // namespace

@@ -3,75 +3,120 @@
 // S_init_0 = h0 (or 0), S_init_{s+1} = M_s S_init_s + S_ext_s, all fp32
 // (apply_kda_state_summary on the hyper-parallel "Diff Coverage" page, which
 // keeps the communicated state in fp32 with autocast off; SANA
-// distributed_scan.py _exclusive_prefix_compose). One CTA per (batch row and
-// head, 32 state columns); the K x K transfer of each segment is staged in
-// shared memory and applied with fp32 FMA.
+// distributed_scan.py _exclusive_prefix_compose).
+//
+// The columns of the state are independent, so one CTA owns one (batch row and
+// head, 8 state columns) and walks the segments in order; its 128 threads own
+// one state row each. Per segment the only dependent work is the 128 x 8 x 128
+// product M_s S; the next segment's 64 KB transfer map is copied into the other
+// of two shared-memory buffers (cp.async) while this one is applied. M is kept
+// row-major with the 16-byte chunks of row m XOR-swizzled by m mod 32, so the 16-byte
+// reads of a quarter warp (eight rows, the same columns) hit eight distinct bank groups;
+// the state slice is read by all threads alike (broadcast).
 #include "common.cuh"
 #include "kernels.h"
+#include "tile_ops.cuh"
 
 namespace gdn {
 namespace {
+using namespace tile;
 
-constexpr int BV = 32;
-constexpr int NTH = 256;
-constexpr int MP = GDN_DK + 1;
-constexpr int VP = BV + 1;
+constexpr int BV = 8;      // state columns per CTA
+constexpr int NTH = 128;   // one thread per state row
+constexpr int M_FLOATS = GDN_DK * GDN_DK;
+constexpr size_t SMEM_BYTES = (2 * M_FLOATS + 2 * GDN_DK * BV) * sizeof(float);
+
+// float offset of M[m][4 c4] in the swizzled buffer (c4: 16-byte chunk, 32 per row)
+__device__ __forceinline__ int msw(int m, int c4) { return m * GDN_DK + ((c4 ^ (m & 31)) << 2); }
 
 __global__ void __launch_bounds__(NTH) merge_kernel(MergeArgs a) {
-  extern __shared__ float smem[];
-  float *sM = smem;              // [128][MP]
-  float *sS = sM + GDN_DK * MP;  // [128][VP]
-  const int tid = threadIdx.x;
+  extern __shared__ __align__(16) float smem[];
+  float *sM = smem;                  // two transfer maps
+  float *sS = smem + 2 * M_FLOATS;   // two state slices [128][8]
+  const int m = threadIdx.x;
   const int col0 = blockIdx.x * BV;
   const int64_t bh = blockIdx.y;
   const int64_t KV = (int64_t)GDN_DK * GDN_DV;
+  const uint32_t sMa = static_cast<uint32_t>(__cvta_generic_to_shared(sM));
 
-  for (int idx = tid; idx < GDN_DK * BV; idx += NTH) {
-    const int d = idx / BV, c = idx % BV;
-    sS[d * VP + c] = a.h0 ? a.h0[bh * KV + d * GDN_DV + col0 + c] : 0.f;
+  auto fetch_M = [&](int s) {  // every thread copies one row: 32 chunks of 16 bytes
+    const float *Ms = a.M + (bh * a.nseg + s) * M_FLOATS + (int64_t)m * GDN_DK;
+    const uint32_t dst = sMa + (uint32_t)((s & 1) * M_FLOATS) * 4u;
+#pragma unroll 8
+    for (int c4 = 0; c4 < 32; ++c4) cp_async16(dst + (uint32_t)msw(m, c4) * 4u, Ms + 4 * c4, 16u);
+    cp_async_commit();
+  };
+
+  float cur[BV];
+  {
+    const float *src = a.h0 ? a.h0 + bh * KV + (int64_t)m * GDN_DV + col0 : nullptr;
+#pragma unroll
+    for (int j = 0; j < BV; ++j) cur[j] = src ? src[j] : 0.f;
   }
-  __syncthreads();
-  int m0, n0;
-  tile_origin<128, BV, 4, 4>(tid, m0, n0);
+#pragma unroll
+  for (int j = 0; j < BV; ++j) sS[m * BV + j] = cur[j];
+  if (a.nseg > 0) fetch_M(0);
   for (int s = 0; s < a.nseg; ++s) {
     const int64_t slot = bh * a.nseg + s;
-    for (int idx = tid; idx < GDN_DK * BV; idx += NTH) {
-      const int d = idx / BV, c = idx % BV;
-      a.S_init[slot * KV + d * GDN_DV + col0 + c] = sS[d * VP + c];
+    // this segment's entry state, and its local term
+    float4 *dst = reinterpret_cast<float4 *>(a.S_init + slot * KV + (int64_t)m * GDN_DV + col0);
+    dst[0] = make_float4(cur[0], cur[1], cur[2], cur[3]);
+    dst[1] = make_float4(cur[4], cur[5], cur[6], cur[7]);
+    const float4 *es = reinterpret_cast<const float4 *>(a.S_ext + slot * KV + (int64_t)m * GDN_DV + col0);
+    const float4 e0 = es[0], e1 = es[1];
+    cp_async_wait<0>();  // M_s, the only copy in flight, has landed
+    __syncthreads();     // M_s and the state slice are visible; every read of M_{s-1} is done
+    if (s + 1 < a.nseg) fetch_M(s + 1);  // into the buffer M_{s-1} held, while M_s is applied
+    const float *Mb = sM + (s & 1) * M_FLOATS;
+    const float *Sb = sS + (s & 1) * GDN_DK * BV;
+    float acc[BV];
+#pragma unroll
+    for (int j = 0; j < BV; ++j) acc[j] = 0.f;
+#pragma unroll 4
+    for (int c4 = 0; c4 < 32; ++c4) {
+      const float4 mv = *reinterpret_cast<const float4 *>(Mb + msw(m, c4));
+      const float mk[4] = {mv.x, mv.y, mv.z, mv.w};
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk) {
+        const float4 s0 = *reinterpret_cast<const float4 *>(Sb + (4 * c4 + kk) * BV);
+        const float4 s1 = *reinterpret_cast<const float4 *>(Sb + (4 * c4 + kk) * BV + 4);
+        acc[0] = fmaf(mk[kk], s0.x, acc[0]);
+        acc[1] = fmaf(mk[kk], s0.y, acc[1]);
+        acc[2] = fmaf(mk[kk], s0.z, acc[2]);
+        acc[3] = fmaf(mk[kk], s0.w, acc[3]);
+        acc[4] = fmaf(mk[kk], s1.x, acc[4]);
+        acc[5] = fmaf(mk[kk], s1.y, acc[5]);
+        acc[6] = fmaf(mk[kk], s1.z, acc[6]);
+        acc[7] = fmaf(mk[kk], s1.w, acc[7]);
+      }
     }
-    const float *Ms = a.M + slot * GDN_DK * GDN_DK;
-    for (int idx = tid; idx < GDN_DK * GDN_DK; idx += NTH) sM[(idx >> 7) * MP + (idx & 127)] = Ms[idx];
-    __syncthreads();
-    float acc[4][4];
-    zero_acc(acc);
-    auto fa = [&](int m, int kk) { return sM[m * MP + kk]; };
-    auto fb = [&](int kk, int nn) { return sS[kk * VP + nn]; };
-    mm_acc<128, BV, GDN_DK, 4, 4>(fa, fb, acc, tid);
-    __syncthreads();
-    const float *Es = a.S_ext + slot * KV;
+    cur[0] = acc[0] + e0.x;
+    cur[1] = acc[1] + e0.y;
+    cur[2] = acc[2] + e0.z;
+    cur[3] = acc[3] + e0.w;
+    cur[4] = acc[4] + e1.x;
+    cur[5] = acc[5] + e1.y;
+    cur[6] = acc[6] + e1.z;
+    cur[7] = acc[7] + e1.w;
+    float *Sn = sS + ((s + 1) & 1) * GDN_DK * BV;
 #pragma unroll
-    for (int x = 0; x < 4; ++x)
-#pragma unroll
-      for (int y = 0; y < 4; ++y)
-        sS[(m0 + x) * VP + n0 + y] = acc[x][y] + Es[(m0 + x) * GDN_DV + col0 + n0 + y];
-    __syncthreads();
+    for (int j = 0; j < BV; ++j) Sn[m * BV + j] = cur[j];
   }
   if (a.ht) {
-    for (int idx = tid; idx < GDN_DK * BV; idx += NTH) {
-      const int d = idx / BV, c = idx % BV;
-      a.ht[bh * KV + d * GDN_DV + col0 + c] = sS[d * VP + c];
-    }
+    float4 *dst = reinterpret_cast<float4 *>(a.ht + bh * KV + (int64_t)m * GDN_DV + col0);
+    dst[0] = make_float4(cur[0], cur[1], cur[2], cur[3]);
+    dst[1] = make_float4(cur[4], cur[5], cur[6], cur[7]);
   }
+  cp_async_wait<0>();
 }
 
 }  // namespace
 
 cudaError_t launch_merge(const MergeArgs &a, cudaStream_t st) {
-  const size_t bytes = (size_t)(GDN_DK * MP + GDN_DK * VP) * sizeof(float);
   cudaError_t e = cudaFuncSetAttribute(merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)bytes);
+                                       (int)SMEM_BYTES);
   if (e != cudaSuccess) return e;
-  merge_kernel<<<dim3(GDN_DV / BV, a.BH), NTH, bytes, st>>>(a);
+  merge_kernel<<<dim3(GDN_DV / BV, a.BH), NTH, SMEM_BYTES, st>>>(a);
   return cudaGetLastError();
 }
 
