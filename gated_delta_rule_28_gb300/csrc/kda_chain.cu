@@ -14,7 +14,10 @@
 // document or segment) of one head and 64 state columns; the state lives in fp32
 // registers of the chain warps (thread = key row, 32 columns). The loader warp
 // fetches the next chunk's blob with bulk copies into the other of two buffers
-// while the chain works on the current one.
+// while the chain works on the current one. The output of chunk c is written
+// during step c + 1, by the warps whose tensor-memory lanes hold it (the output
+// rows) while the others form v_new, so it is off the state's critical path:
+// P4 and PO accumulate into two tensor-memory buffers by chunk parity.
 //
 // Summary mode runs the same recurrence for the segment summary (combined mode
 // of kda_split_state_summary_kernel): column slices 0, 1 carry S_ext (from a
@@ -38,10 +41,10 @@ using namespace kda;
 
 constexpr int TBV = 64;
 constexpr int NTH = 288;  // 8 chain warps + the loader
-constexpr uint32_t TMEM_COLS = 256;
-constexpr uint32_t T_D4 = 0;    // P4: rows 0..63 = w h, rows 64..127 = Q b^G h
-constexpr uint32_t T_PO = 64;   // PO: rows 64..127 = A_qk v_new
-constexpr uint32_t T_P5 = 128;  // P5: 128 key rows
+constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t T_D4 = 0;    // 2 x 64, per chunk parity: P4 rows 0..63 = w h, rows 64..127 = Q b^G h
+constexpr uint32_t T_PO = 128;  // 2 x 64, per chunk parity: PO rows 64..127 = A_qk v_new
+constexpr uint32_t T_P5 = 256;  // 64: P5, 128 key rows
 
 // one buffer per chunk parity: the blob's pieces this CTA needs
 constexpr int BUF_WQ = 0;       // [w; Q b^G], K-blocks 16 KB apart
@@ -192,12 +195,32 @@ __global__ void __launch_bounds__(NTH, 1) kda_chain_kernel(KdaChainArgs a) {
     for (int q8 = 0; q8 < 4; ++q8)
       *reinterpret_cast<uint4 *>(sm + OFF_HT + chunk_off(row, 4 * hc + q8)) = pack8(hreg + 8 * q8);
   };
+  // o = Q b^G h + A_qk v_new of chunk c (token row - 64), by the warps of lanes 64..127
+  auto output = [&](int64_t c) {
+    const int par = (int)(c & 1);
+    const int64_t c0 = r0 + c * GDN_CHUNK;
+    const int n = (int)min((int64_t)GDN_CHUNK, r1 - c0);
+    wait_par(&st.bar_po, c);
+    const bool st_row = a.o && row - 64 < n;
+    uint4 *dst = reinterpret_cast<uint4 *>(a.o + ((c0 + (st_row ? row - 64 : 0)) * H + h) * GDN_DV + col0 + 32 * hc);
+#pragma unroll
+    for (int part = 0; part < 2; ++part) {
+      float ov[16], av[16];
+      tmem_ld16(tl + T_D4 + 64 * par + 32 * hc + 16 * part, ov);
+      tmem_ld16(tl + T_PO + 64 * par + 32 * hc + 16 * part, av);
+      tmem_ld_wait();
+#pragma unroll
+      for (int j = 0; j < 16; ++j) ov[j] += av[j];
+      if (st_row) {
+        dst[2 * part] = pack8(ov);
+        dst[2 * part + 1] = pack8(ov + 8);
+      }
+    }
+  };
   auto chain = [&](int64_t c) {
     const int par = (int)(c & 1);
     const uint32_t buf = buf_at(c);
     uint8_t *bufp = sm + (size_t)par * BUF_BYTES;
-    const int64_t c0 = r0 + c * GDN_CHUNK;
-    const int n = (int)min((int64_t)GDN_CHUNK, r1 - c0);
     if (a.h_chunks) {  // entry state of chunk c
       const int64_t slot = a.cu ? (chunk_base + c) * H + h : ((int64_t)b * H + h) * NT + chunk_base + c;
       float4 *dst = reinterpret_cast<float4 *>(a.h_chunks + slot * GDN_DK * GDN_DV + (int64_t)row * GDN_DV +
@@ -208,17 +231,18 @@ __global__ void __launch_bounds__(NTH, 1) kda_chain_kernel(KdaChainArgs a) {
     }
     wait_par(&st.bar_ld[par], c >> 1);
     if (warp == 0) {  // P4: [w; Q b^G] h
-      mma_ops_w(tmem + T_D4, kmaj(buf + BUF_WQ, 16384), mnmaj(sb + OFF_HT, 0), 128,
+      mma_ops_w(tmem + T_D4 + 64 * par, kmaj(buf + BUF_WQ, 16384), mnmaj(sb + OFF_HT, 0), 128,
                 idesc_bf16(128, 64, false, false, true), false);
       mma_commit_w(&st.bar_p4);
     }
     __syncwarp();
+    if (!summ && q4 >= 2 && c > 0) output(c - 1);  // the previous chunk's output, meanwhile
     wait_par(&st.bar_p4, c);
     if (q4 < 2) {  // v_new = u - w h (token row), the whole warp loads tensor memory
 #pragma unroll
       for (int part = 0; part < 2; ++part) {
         float wh[16], u[16];
-        tmem_ld16(tl + T_D4 + 32 * hc + 16 * part, wh);
+        tmem_ld16(tl + T_D4 + 64 * par + 32 * hc + 16 * part, wh);
         tmem_ld_wait();
         if (mcols) {
 #pragma unroll
@@ -239,49 +263,30 @@ __global__ void __launch_bounds__(NTH, 1) kda_chain_kernel(KdaChainArgs a) {
     if (warp == 0) {
       fence_after_sync();
       // P5 first (the state update waits for it): (K b^(Gl-G))^T v_new, the key tile read
-      // as MN-major A; then PO for the output epilogue
+      // as MN-major A; then PO for the output (read during the next step). The commit of
+      // the next P4 also covers this PO, so v_new is not rewritten before PO has read it.
       mma_ops_w(tmem + T_P5, mnmaj(buf + BUF_KL, 8192), mnmaj(sb + OFF_VN, 0), 64,
                 idesc_bf16(128, 64, false, true, true), false);
       mma_commit_w(&st.bar_p5);
       if (!summ) {  // PO: A_qk v_new (A rows 64..127 = A_qk)
-        mma_ops_w(tmem + T_PO, kmaj(buf + BUF_AQ - 8192, 0), mnmaj(sb + OFF_VN, 0), 64,
+        mma_ops_w(tmem + T_PO + 64 * par, kmaj(buf + BUF_AQ - 8192, 0), mnmaj(sb + OFF_VN, 0), 64,
                   idesc_bf16(128, 64, false, false, true), false);
         mma_commit_w(&st.bar_po);
       }
     }
     __syncwarp();
     wait_par(&st.bar_p5, c);
-    {
-      const float el = reinterpret_cast<const float *>(bufp + BUF_EL)[row];
+    const float el = reinterpret_cast<const float *>(bufp + BUF_EL)[row];
 #pragma unroll
-      for (int part = 0; part < 2; ++part) {
-        float p5[16];
-        tmem_ld16(tl + T_P5 + 32 * hc + 16 * part, p5);
-        tmem_ld_wait();
+    for (int part = 0; part < 2; ++part) {
+      float p5[16];
+      tmem_ld16(tl + T_P5 + 32 * hc + 16 * part, p5);
+      tmem_ld_wait();
 #pragma unroll
-        for (int j = 0; j < 16; ++j) hreg[16 * part + j] = fmaf(el, hreg[16 * part + j], p5[j]);
-      }
-      write_ht();
-      fence_proxy_async();
-      if (!summ && q4 >= 2) {  // o = Q b^G h + A_qk v_new (token row - 64)
-        wait_par(&st.bar_po, c);
-        const bool st_row = a.o && row - 64 < n;
-        uint4 *dst = reinterpret_cast<uint4 *>(a.o + ((c0 + (st_row ? row - 64 : 0)) * H + h) * GDN_DV + col0 + 32 * hc);
-#pragma unroll
-        for (int part = 0; part < 2; ++part) {
-          float ov[16], av[16];
-          tmem_ld16(tl + T_D4 + 32 * hc + 16 * part, ov);
-          tmem_ld16(tl + T_PO + 32 * hc + 16 * part, av);
-          tmem_ld_wait();
-#pragma unroll
-          for (int j = 0; j < 16; ++j) ov[j] += av[j];
-          if (st_row) {
-            dst[2 * part] = pack8(ov);
-            dst[2 * part + 1] = pack8(ov + 8);
-          }
-        }
-      }
+      for (int j = 0; j < 16; ++j) hreg[16 * part + j] = fmaf(el, hreg[16 * part + j], p5[j]);
     }
+    write_ht();
+    fence_proxy_async();
     fence_before_sync();
   };
 
@@ -303,6 +308,10 @@ __global__ void __launch_bounds__(NTH, 1) kda_chain_kernel(KdaChainArgs a) {
       break;
     }
   }
+  if (!bad && !summ && nch > 0 && !loader && q4 >= 2) {  // the last chunk's output
+    output(nch - 1);
+  }
+  if (__syncthreads_or(bad)) bad = true;
 
   if (bad) {
     if (tid == 0) raise_device_flag(a.dev_flag, kDevTimeout);

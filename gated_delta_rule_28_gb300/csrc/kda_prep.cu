@@ -57,7 +57,7 @@ static_assert(64 * GS * 4 <= 34816 && (L_FLOATS + X_FLOATS + 4 * 256) * 4 <= 348
 // largest |exponent| (base 2) a factor may take on the tensor-core path
 constexpr float EXP_LIMIT = 100.f;
 
-struct Small {
+struct __align__(16) Small {
   float beta[64];
   float part[128];
   float eref[128];  // b^(G_r) per key channel
@@ -67,6 +67,14 @@ static_assert(sizeof(Small) <= 2048, "small state");
 
 template <bool E2>
 __device__ __forceinline__ float expo_to_base2(float x) { return E2 ? x : x * 1.4426950408889634f; }
+// b^x with one special-function instruction (PTX ex2.approx.ftz: relative error near
+// 2^-22, results below 2^-126 flush to zero) -- ample for factors rounded to bf16
+template <bool E2>
+__device__ __forceinline__ float fexp(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(expo_to_base2<E2>(x)));
+  return y;
+}
 
 __device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
   asm volatile(
@@ -152,15 +160,19 @@ __global__ void __launch_bounds__(NTH, 2) kda_prep_kernel(KdaPrepArgs a, int64_t
     cp_async_commit();
     if (tid < 64) sv.beta[tid] = tid < n ? __bfloat162float(beta[(r0 + tid) * H + h]) : 0.f;
     const int d = tid & 127, half = tid >> 7;
-    // gate element of row i for this thread's key channel (a scalar gate serves every channel)
-    auto gidx = [&](int i) { return a.scalar_gate ? (r0 + i) * H + h : grow(i) + d; };
+    // gate element (row i, this thread's key channel): a scalar gate serves every channel
+    const int64_t gstride = a.scalar_gate ? (int64_t)H : (int64_t)H * GDN_DK;
+    const int64_t g0 = a.scalar_gate ? r0 * H + h : grow(0) + d;
+    auto gidx = [&](int i) { return g0 + i * gstride; };
     float gcol[32];
     if (a.g_cum_in) {
+      const float *gp = a.g_cum_in + g0;
 #pragma unroll
-      for (int j = 0; j < 32; ++j) gcol[j] = a.g_cum_in[gidx(min(32 * half + j, n - 1))];
+      for (int j = 0; j < 32; ++j) gcol[j] = gp[min(32 * half + j, n - 1) * gstride];
     } else {
+      const float *gp = a.g + g0;
 #pragma unroll
-      for (int j = 0; j < 32; ++j) gcol[j] = 32 * half + j < n ? a.g[gidx(32 * half + j)] : 0.f;
+      for (int j = 0; j < 32; ++j) gcol[j] = 32 * half + j < n ? gp[(32 * half + j) * gstride] : 0.f;
 #pragma unroll
       for (int j = 1; j < 32; ++j) gcol[j] += gcol[j - 1];
       if (half == 0) sv.part[d] = gcol[31];
@@ -186,11 +198,16 @@ __global__ void __launch_bounds__(NTH, 2) kda_prep_kernel(KdaPrepArgs a, int64_t
     }
     __syncthreads();
     // range of the factors around the reference row
-    bool out_of_range = false;
+    bool out_of_range;
     {
-      const float gr = sG[REF * GS + d];
+      float lo = gcol[0], hi = gcol[0];
 #pragma unroll
-      for (int j = 0; j < 32; ++j) out_of_range |= fabsf(expo_to_base2<E2>(gcol[j] - gr)) > EXP_LIMIT;
+      for (int j = 1; j < 32; ++j) {
+        lo = fminf(lo, gcol[j]);
+        hi = fmaxf(hi, gcol[j]);
+      }
+      const float gr = sG[REF * GS + d];
+      out_of_range = fmaxf(expo_to_base2<E2>(hi - gr), expo_to_base2<E2>(gr - lo)) > EXP_LIMIT;
     }
     const bool exact = __syncthreads_or(out_of_range);
     cp_async_wait<0>();
@@ -235,18 +252,24 @@ __global__ void __launch_bounds__(NTH, 2) kda_prep_kernel(KdaPrepArgs a, int64_t
       unpack8(*reinterpret_cast<const uint4 *>(sm + OFF_Q + to), qv);
       load_g8(sG, i, c0, gv);
       if (!exact) {
-        float gr[8], o2[8], o3[8];
+        float gr[8], o2[8], o3[8], er[8], el[8];
         load_g8(sG, REF, c0, gr);
+        {
+          const float4 *pe = reinterpret_cast<const float4 *>(sv.eref + c0);
+          const float4 *pl = reinterpret_cast<const float4 *>(sv.elr + c0);
+          const float4 e0 = pe[0], e1 = pe[1], l0 = pl[0], l1 = pl[1];
+          er[0] = e0.x; er[1] = e0.y; er[2] = e0.z; er[3] = e0.w; er[4] = e1.x; er[5] = e1.y; er[6] = e1.z; er[7] = e1.w;
+          el[0] = l0.x; el[1] = l0.y; el[2] = l0.z; el[3] = l0.w; el[4] = l1.x; el[5] = l1.y; el[6] = l1.z; el[7] = l1.w;
+        }
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
-          const int c = c0 + e;
-          const float ef = gexp<E2>(gv[e] - gr[e]);
-          const float rf = __frcp_rn(ef);
+          const float ef = fexp<E2>(gv[e] - gr[e]);
+          const float rf = fexp<E2>(gr[e] - gv[e]);
           o1[e] = kv[e] * ef;                      // K e      (Gram A; B of w)
           o2[e] = qv[e] * ef;                      // Q e      (Gram A)
           o3[e] = kv[e] * rf;                      // K / e    (Gram B)
-          o4[e] = o3[e] * sv.elr[c];               // K b^(Gl - G)
-          qv[e] = scale * o2[e] * sv.eref[c];      // scale Q b^G
+          o4[e] = o3[e] * el[e];                   // K b^(Gl - G)
+          qv[e] = scale * o2[e] * er[e];           // scale Q b^G
         }
         *reinterpret_cast<uint4 *>(sm + OFF_KB + to) = pack8(o3);
         *reinterpret_cast<uint4 *>(sm + OFF_Q + to) = pack8(o2);
