@@ -215,3 +215,39 @@ def segment_merge(S_ext, M, h0=None):
                                    _ptr(S_init), _ptr(ht))
     assert rc == 0
     return S_init, ht
+
+
+def segment_summary_bwd(q, k, v, g, beta, dO, seg_len, *, scale=None, per_key=False, use_exp2=False,
+                        n_threads=None):
+    """Backward segment summary: per segment of ``seg_len`` tokens, the gradient of the
+    segment's entry state from its own outputs alone (the reverse recurrence started from
+    a zero gradient at the segment's exit; "state_summary.py" kda_state_grad_ext_kernel).
+    It does not depend on the state, so it is the segment run's dh0 for any entry state.
+    Returns dS_ext [B, H, nseg, K, V]."""
+    q, k, v, g, beta, dO = map(_f64, (q, k, v, g, beta, dO))
+    B, T, H, K = q.shape
+    nseg = -(-T // seg_len)
+    out = np.zeros((B, H, nseg, K, v.shape[-1]))
+    for s in range(nseg):
+        sl = lambda x: x[:, s * seg_len:(s + 1) * seg_len]  # noqa: E731
+        r = backward(sl(q), sl(k), sl(v), sl(g), sl(beta), None, sl(dO), None, scale=scale,
+                     per_key=per_key, use_exp2=use_exp2, n_threads=n_threads)
+        out[:, :, s] = r["dh0"]
+    return out
+
+
+def segment_merge_bwd(dS_ext, M, dht=None):
+    """Adjoint of the ordered merge: the state gradient flows from the last segment to the
+    first through the transposed transfer maps (SANA distributed_scan.py,
+    _CPAllGatherMerge.backward; the coverage-diff page's state-summary apply helpers):
+        dS_exit[nseg-1] = dht (or 0),  dS_entry[s] = M_s^T dS_exit[s] + dS_ext[s],
+        dS_exit[s-1] = dS_entry[s].
+    Returns (dS_exit [B,H,nseg,K,V]: the gradient at every segment's exit, dh0 = dS_entry[0])."""
+    dS_ext, M, dht = map(_f64, (dS_ext, M, dht))
+    B, H, nseg, K, V = dS_ext.shape
+    dS_exit = np.zeros_like(dS_ext)
+    cur = np.zeros((B, H, K, V)) if dht is None else dht.copy()
+    for s in range(nseg - 1, -1, -1):
+        dS_exit[:, :, s] = cur
+        cur = np.einsum("bhji,bhjv->bhiv", M[:, :, s], cur) + dS_ext[:, :, s]
+    return dS_exit, cur

@@ -275,3 +275,47 @@ def test_input_maps_fixed_points():
     x = np.full((1, 1, 1, 4), math.sqrt(R.L2_EPS / 4))  # sum x^2 = eps
     xn, _ = R.l2norm(x)
     assert abs(float((xn * xn).sum()) - 0.5) < 1e-15
+
+
+@pytest.mark.parametrize("per_key,seg_len", [(False, 5), (True, 7)])
+def test_split_backward_reproduces_unsplit_backward(per_key, seg_len):
+    """Backward segment summaries + the adjoint merge, then every segment's reverse pass
+    seeded with its exit gradient (and its forward with the merged entry state), give the
+    unsplit gradients; the merge's dh0 is the unsplit dh0."""
+    rng = np.random.default_rng(15)
+    q, k, v, g, beta, h0 = _rand_case(rng, 2, 19, 2, 5, 4, per_key=per_key)
+    dO = rng.standard_normal(v.shape)
+    kw = dict(per_key=per_key, use_exp2=per_key)
+    o, ht = R.forward(q, k, v, g, beta, h0, **kw)
+    dht = rng.standard_normal(ht.shape)
+    want = R.backward(q, k, v, g, beta, h0, dO, dht, **kw)
+    S, M = R.segment_summary(k, v, g, beta, seg_len, **kw)
+    S_init, _ = R.segment_merge(S, M, h0)
+    dS_ext = R.segment_summary_bwd(q, k, v, g, beta, dO, seg_len, **kw)
+    dS_exit, dh0 = R.segment_merge_bwd(dS_ext, M, dht)
+    np.testing.assert_allclose(dh0, want["dh0"], rtol=1e-10, atol=1e-12)
+    nseg = S.shape[2]
+    for s in range(nseg):
+        sl = lambda x: x[:, s * seg_len:(s + 1) * seg_len]  # noqa: E731
+        got = R.backward(sl(q), sl(k), sl(v), sl(g), sl(beta), S_init[:, :, s], sl(dO), dS_exit[:, :, s], **kw)
+        for name in ("dq", "dk", "dv", "dg", "dbeta"):
+            np.testing.assert_allclose(got[name], sl(want[name]), rtol=1e-9, atol=1e-11)
+        # the segment's entry gradient is the merge's: M_s^T dS_exit + dS_ext
+        if s > 0:
+            np.testing.assert_allclose(got["dh0"], dS_exit[:, :, s - 1], rtol=1e-9, atol=1e-11)
+
+
+def test_backward_summary_with_no_output_gradient_is_pure_transport():
+    """dO = 0: every backward summary vanishes and dh0 = M_0^T ... M_{n-1}^T dht."""
+    rng = np.random.default_rng(16)
+    q, k, v, g, beta, _ = _rand_case(rng, 1, 12, 1, 4, 3, per_key=True)
+    dO = np.zeros(v.shape)
+    dS_ext = R.segment_summary_bwd(q, k, v, g, beta, dO, 4, per_key=True, use_exp2=True)
+    assert np.abs(dS_ext).max() == 0.0
+    _, M = R.segment_summary(k, v, g, beta, 4, per_key=True, use_exp2=True)
+    dht = rng.standard_normal((1, 1, 4, 3))
+    _, dh0 = R.segment_merge_bwd(dS_ext, M, dht)
+    want = dht[0, 0]
+    for s in range(M.shape[2] - 1, -1, -1):
+        want = M[0, 0, s].T @ want
+    np.testing.assert_allclose(dh0[0, 0], want, rtol=1e-12, atol=1e-14)
