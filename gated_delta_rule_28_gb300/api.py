@@ -162,17 +162,20 @@ class HostPipeline:
 
 def chunk_gated_delta_rule_bwd(q, k, v, g_cumsum, beta, A, dO, *, h0=None, dht=None, scale=None,
                                use_exp2=False, cu_seqlens=None, varlen=None, use_qk_l2norm=False,
-                               use_beta_sigmoid=False, stream=None):
+                               use_beta_sigmoid=False, segment_len=0, stream=None):
     """Chunked backward; returns dq, dk, dv, dbeta, dg (raw gate) and dh0. With the input
     maps on, q, k, beta are the forward's raw inputs and dq, dk, dbeta are w.r.t. them."""
     if cu_seqlens is not None and varlen is None:
         varlen = Varlen(cu_seqlens, q.shape[0], q.device)
     p = problem_for(q, v, g_cumsum, scale=scale, use_exp2=use_exp2, varlen=varlen,
-                    use_qk_l2norm=use_qk_l2norm, use_beta_sigmoid=use_beta_sigmoid)
+                    use_qk_l2norm=use_qk_l2norm, use_beta_sigmoid=use_beta_sigmoid,
+                    segment_len=segment_len)
     nstate = varlen.num_seqs if varlen is not None else p.B
+    sshape = ((p.B, p.H, -(-p.T // segment_len), p.K, p.V) if segment_len
+              else (nstate, p.H, p.K, p.V))
     out = dict(dq=torch.empty_like(q), dk=torch.empty_like(k), dv=torch.empty_like(v),
                dbeta=torch.empty_like(beta), dg=torch.empty_like(g_cumsum),
-               dh0=torch.empty((nstate, p.H, p.K, p.V), device=q.device, dtype=torch.float32))
+               dh0=torch.empty(sshape, device=q.device, dtype=torch.float32))
     nws = B.gdn_chunk_bwd_workspace(p)
     ws = torch.empty(nws, device=q.device, dtype=torch.uint8) if nws else None
     B.gdn_chunk_bwd(p, q, k, v, g_cumsum, beta, A, dO, h0, dht, out["dq"], out["dk"], out["dv"],
@@ -205,13 +208,38 @@ def segment_merge(S_ext, M, h0=None, stream=None):
 
 
 def split_forward(q, k, v, g, beta, segment_len, *, h0=None, scale=None, use_exp2=False,
-                  use_qk_l2norm=False, use_beta_sigmoid=False, return_h_chunks=False, stream=None):
+                  use_qk_l2norm=False, use_beta_sigmoid=False, return_h_chunks=False,
+                  return_g_cumsum=False, return_A=False, stream=None):
     """Long-sequence forward split across SMs: summaries, merge, corrected run."""
     maps = dict(use_qk_l2norm=use_qk_l2norm, use_beta_sigmoid=use_beta_sigmoid)
     S, M = segment_summary(k, v, g, beta, segment_len, use_exp2=use_exp2, stream=stream, **maps)
     S_init, _ = segment_merge(S, M, h0, stream=stream)
     out = chunk_gated_delta_rule_fwd(q, k, v, g, beta, h0=S_init, scale=scale, use_exp2=use_exp2,
                                      segment_len=segment_len, return_h_chunks=return_h_chunks,
+                                     return_g_cumsum=return_g_cumsum, return_A=return_A,
                                      stream=stream, **maps)
     out.update(S_ext=S, M=M, S_init=S_init)
+    return out
+
+
+def split_backward(q, k, v, g_cumsum, beta, A, dO, segment_len, S_init, M, *, dht=None, scale=None,
+                   use_exp2=False, use_qk_l2norm=False, use_beta_sigmoid=False, stream=None):
+    """Backward of ``split_forward``: backward segment summaries (all segments at once), their
+    adjoint merge through M^T, then every segment's backward seeded with its exit gradient.
+    ``S_init`` and ``M`` are the forward split's. Returns the gradients with dh0 [B,H,K,V]."""
+    maps = dict(use_qk_l2norm=use_qk_l2norm, use_beta_sigmoid=use_beta_sigmoid)
+    p = problem_for(q, v, g_cumsum, scale=scale, use_exp2=use_exp2, **maps)
+    nseg = -(-p.T // segment_len)
+    dS_ext = torch.empty((p.B, p.H, nseg, p.K, p.V), device=q.device, dtype=torch.float32)
+    nws = B.kda_segment_summary_bwd_workspace(p, segment_len)
+    ws = torch.empty(max(nws, 1), device=q.device, dtype=torch.uint8)
+    B.kda_segment_summary_bwd(p, q, k, g_cumsum, beta, A, dO, segment_len, dS_ext, ws, nws, stream)
+    dS_exit = torch.empty_like(dS_ext)
+    dh0 = torch.empty((p.B, p.H, p.K, p.V), device=q.device, dtype=torch.float32)
+    mp = B.make_problem(p.B, nseg * 64, p.H, p.K, p.V, dtype=B.GDN_DTYPE_F32)
+    B.kda_segment_merge_bwd(mp, dS_ext, M, nseg, dht, dS_exit, dh0, stream)
+    out = chunk_gated_delta_rule_bwd(q, k, v, g_cumsum, beta, A, dO, h0=S_init, dht=dS_exit,
+                                     scale=scale, use_exp2=use_exp2, segment_len=segment_len,
+                                     stream=stream, **maps)
+    out.update(dh0=dh0, dS_ext=dS_ext, dS_exit=dS_exit)
     return out

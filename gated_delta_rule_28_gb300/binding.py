@@ -32,6 +32,7 @@ GDN_DTYPE_F32, GDN_DTYPE_BF16 = 0, 1
 EXPORTS = ("gdn_last_error", "gdn_device_status", "gdn_prepare_varlen", "gdn_chunk_fwd_workspace",
            "gdn_chunk_fwd", "gdn_chunk_bwd_workspace", "gdn_chunk_bwd", "gdn_chunk_bwd_noalloc",
            "kda_segment_summary_workspace", "kda_segment_summary", "kda_segment_merge",
+           "kda_segment_summary_bwd_workspace", "kda_segment_summary_bwd", "kda_segment_merge_bwd",
            "gdn_selftest_wait_timeout")
 # bytes of the library's built-in scratch array used by gdn_chunk_bwd_noalloc
 GDN_NOALLOC_SCRATCH_BYTES = 64 * 1024 * 1024
@@ -90,6 +91,9 @@ def load():
             lib.kda_segment_summary.argtypes = [P, vp, vp, vp, vp, ctypes.c_int32, vp, vp, vp, sz, vp]
             lib.kda_segment_merge.argtypes = [P, vp, vp, ctypes.c_int32, vp, vp, vp, vp]
             lib.gdn_selftest_wait_timeout.argtypes = [ctypes.c_uint32, vp]
+            lib.kda_segment_summary_bwd_workspace.argtypes = [P, ctypes.c_int32, ctypes.POINTER(sz)]
+            lib.kda_segment_summary_bwd.argtypes = [P] + [vp] * 6 + [ctypes.c_int32, vp, vp, sz, vp]
+            lib.kda_segment_merge_bwd.argtypes = [P, vp, vp, ctypes.c_int32, vp, vp, vp, vp]
             for name in EXPORTS[1:]:
                 getattr(lib, name).restype = ctypes.c_int
             _lib = lib
@@ -217,6 +221,24 @@ def kda_segment_summary(p: gdn_problem, k, v, g, beta, segment_len, S_ext, M, ws
     _check(load().kda_segment_summary(ctypes.byref(p), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
                                       int(segment_len), _ptr(S_ext), _ptr(M), _ptr(ws),
                                       int(ws_bytes), _stream(stream)))
+
+
+def kda_segment_summary_bwd_workspace(p: gdn_problem, segment_len) -> int:
+    n = ctypes.c_size_t(0)
+    _check(load().kda_segment_summary_bwd_workspace(ctypes.byref(p), int(segment_len), ctypes.byref(n)))
+    return n.value
+
+
+def kda_segment_summary_bwd(p: gdn_problem, q, k, g_cumsum, beta, A, dO, segment_len, dS_ext, ws,
+                            ws_bytes, stream=None):
+    _check(load().kda_segment_summary_bwd(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(g_cumsum), _ptr(beta),
+                                          _ptr(A), _ptr(dO), int(segment_len), _ptr(dS_ext), _ptr(ws),
+                                          int(ws_bytes), _stream(stream)))
+
+
+def kda_segment_merge_bwd(p: gdn_problem, dS_ext, M, nseg, dht, dS_exit, dh0=None, stream=None):
+    _check(load().kda_segment_merge_bwd(ctypes.byref(p), _ptr(dS_ext), _ptr(M), int(nseg), _ptr(dht),
+                                        _ptr(dS_exit), _ptr(dh0), _stream(stream)))
 
 
 def kda_segment_merge(p: gdn_problem, S_ext, M, nseg, h0, S_init, ht=None, stream=None):

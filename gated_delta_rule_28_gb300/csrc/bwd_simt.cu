@@ -31,7 +31,7 @@ constexpr int CP = GDN_CHUNK + 1;
 // run / chunk bookkeeping shared by both kernels
 struct Run {
   int64_t r0, r1, chunk_base;
-  int state_idx, b;
+  int state_idx, b, s;
   bool ok;
 };
 
@@ -49,6 +49,13 @@ __device__ Run run_of(const BwdArgs &a, int z) {
     }
     r.state_idx = z;
     r.b = 0;
+  } else if (a.nseg > 0) {  // segment s of batch row b
+    r.b = z / a.nseg;
+    r.s = z % a.nseg;
+    r.r0 = (int64_t)r.b * a.T + (int64_t)r.s * a.seg_len;
+    r.r1 = min(r.r0 + a.seg_len, (int64_t)r.b * a.T + a.T);
+    r.chunk_base = (int64_t)r.s * a.seg_len / GDN_CHUNK;
+    r.state_idx = r.b;
   } else {
     r.b = z;
     r.r0 = (int64_t)z * a.T;
@@ -61,7 +68,13 @@ __device__ Run run_of(const BwdArgs &a, int z) {
 
 __device__ __forceinline__ int64_t chunk_slot(const BwdArgs &a, const Run &r, int64_t ci, int h) {
   const int NT = (a.T + GDN_CHUNK - 1) / GDN_CHUNK;
-  return a.cu ? (r.chunk_base + ci) * a.H + h : ((int64_t)r.b * a.H + h) * NT + ci;
+  return a.cu ? (r.chunk_base + ci) * a.H + h : ((int64_t)r.b * a.H + h) * NT + r.chunk_base + ci;
+}
+
+// element offset of the run's dht / dh0 state: [N, H, K, V], or [B, H, nseg, K, V] for segments
+__device__ __forceinline__ int64_t state_off(const BwdArgs &a, const Run &r, int h) {
+  const int64_t slot = a.nseg > 0 ? ((int64_t)r.b * a.H + h) * a.nseg + r.s : (int64_t)r.state_idx * a.H + h;
+  return slot * GDN_DK * GDN_DV;
 }
 
 // ---------------------------------------------------------------------------
@@ -105,7 +118,7 @@ __global__ void __launch_bounds__(NTH) dhu_kernel(BwdArgs a) {
   const int64_t KV = (int64_t)GDN_DK * GDN_DV;
   for (int idx = tid; idx < 128 * DBV; idx += NTH) {
     const int d = idx / DBV, c = idx % DBV;
-    sDH[d * DVP + c] = a.dht ? a.dht[((int64_t)run.state_idx * H + h) * KV + d * GDN_DV + col0 + c] : 0.f;
+    sDH[d * DVP + c] = a.dht ? a.dht[state_off(a, run, h) + d * GDN_DV + col0 + c] : 0.f;
   }
   __syncthreads();
   const int64_t nchunks = (run.r1 - run.r0 + GDN_CHUNK - 1) / GDN_CHUNK;
@@ -267,7 +280,7 @@ __global__ void __launch_bounds__(NTH) dhu_kernel(BwdArgs a) {
   if (a.dh0) {
     for (int idx = tid; idx < 128 * DBV; idx += NTH) {
       const int d = idx / DBV, c = idx % DBV;
-      a.dh0[((int64_t)run.state_idx * H + h) * KV + d * GDN_DV + col0 + c] = sDH[d * DVP + c];
+      a.dh0[state_off(a, run, h) + d * GDN_DV + col0 + c] = sDH[d * DVP + c];
     }
   }
 }
@@ -903,7 +916,7 @@ cudaError_t dhu_one(const BwdArgs &a, cudaStream_t st) {
   const size_t bytes = dhu_smem_floats<PK>() * sizeof(float);
   cudaError_t e = cudaFuncSetAttribute(dhu_kernel<T, PK>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
   if (e != cudaSuccess) return e;
-  const int runs = a.cu ? a.num_seqs : a.B;
+  const int runs = a.cu ? a.num_seqs : (a.nseg > 0 ? a.B * a.nseg : a.B);
   dhu_kernel<T, PK><<<dim3(GDN_DV / DBV, a.H, runs), NTH, bytes, st>>>(a);
   return cudaGetLastError();
 }

@@ -119,7 +119,7 @@ __global__ void __launch_bounds__(NTH, 1) tc_dhu_kernel(BwdArgs a, const __grid_
 
   // ---- the run: chunk slots as the forward (X workspace: xbase + c; states: slot()) ----
   int64_t r0, r1, chunk_base = 0, xbase;
-  int b = 0;
+  int b = 0, sg = 0;
   const int NT = (a.T + GDN_CHUNK - 1) / GDN_CHUNK;
   if (a.cu) {
     r0 = a.cu[z];
@@ -134,17 +134,26 @@ __global__ void __launch_bounds__(NTH, 1) tc_dhu_kernel(BwdArgs a, const __grid_
       return;
     }
     xbase = chunk_base;
+  } else if (a.nseg > 0) {  // segment sg of batch row b
+    b = z / a.nseg;
+    sg = z % a.nseg;
+    r0 = (int64_t)b * a.T + (int64_t)sg * a.seg_len;
+    r1 = min(r0 + a.seg_len, (int64_t)b * a.T + a.T);
+    chunk_base = (int64_t)sg * a.seg_len / GDN_CHUNK;
+    xbase = (int64_t)b * NT + chunk_base;
   } else {
     b = z;
     r0 = (int64_t)b * a.T;
     r1 = r0 + a.T;
     xbase = (int64_t)b * NT;
   }
-  const int state_idx = z;
+  // dht / dh0 state of the run: [N, H, K, V], or [B, H, nseg, K, V] for segments
+  const int64_t state_off =
+      (a.nseg > 0 ? ((int64_t)b * H + h) * a.nseg + sg : (int64_t)z * H + h) * GDN_DK * GDN_DV;
   const int64_t nch = (r1 - r0 + GDN_CHUNK - 1) / GDN_CHUNK;
   auto chunk_rows = [&](int64_t c) { return (int)min((int64_t)GDN_CHUNK, r1 - (r0 + c * GDN_CHUNK)); };
   auto state_slot = [&](int64_t c) -> int64_t {
-    return a.cu ? (chunk_base + c) * H + h : ((int64_t)b * H + h) * NT + c;
+    return a.cu ? (chunk_base + c) * H + h : ((int64_t)b * H + h) * NT + chunk_base + c;
   };
   // order index m = nch - 1 - c: the reverse loop visits m = 0, 1, ...
   auto chunk_of = [&](int64_t m) { return nch - 1 - m; };
@@ -341,9 +350,7 @@ __global__ void __launch_bounds__(NTH, 1) tc_dhu_kernel(BwdArgs a, const __grid_
   // ---- chain ----------------------------------------------------------------------------
   float dh[32];
   if (!producer) {
-    const float *src = a.dht ? a.dht + ((int64_t)state_idx * H + h) * GDN_DK * GDN_DV + (int64_t)row * GDN_DV +
-                                   col0 + 32 * hc
-                             : nullptr;
+    const float *src = a.dht ? a.dht + state_off + (int64_t)row * GDN_DV + col0 + 32 * hc : nullptr;
 #pragma unroll
     for (int j = 0; j < 32; ++j) dh[j] = src ? src[j] : 0.f;
   }
@@ -456,8 +463,7 @@ __global__ void __launch_bounds__(NTH, 1) tc_dhu_kernel(BwdArgs a, const __grid_
       if (last_do >= 0) mbar_wait(&st.bar_do, (uint32_t)(last_do & 1), WAIT_LIMIT);
     }
   } else if (!producer && a.dh0) {
-    float4 *dst = reinterpret_cast<float4 *>(a.dh0 + ((int64_t)state_idx * H + h) * GDN_DK * GDN_DV +
-                                             (int64_t)row * GDN_DV + col0 + 32 * hc);
+    float4 *dst = reinterpret_cast<float4 *>(a.dh0 + state_off + (int64_t)row * GDN_DV + col0 + 32 * hc);
 #pragma unroll
     for (int g4 = 0; g4 < 8; ++g4) dst[g4] = make_float4(dh[4 * g4], dh[4 * g4 + 1], dh[4 * g4 + 2], dh[4 * g4 + 3]);
   }

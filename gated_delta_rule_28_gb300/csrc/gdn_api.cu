@@ -482,7 +482,7 @@ gdn_status gdn_chunk_fwd(const gdn_problem *pin, const void *q, const void *k, c
 }
 
 gdn_status gdn_chunk_bwd_workspace(const gdn_problem *p, size_t *bytes) {
-  gdn_status st = check_problem(p, false);
+  gdn_status st = check_problem(p, true);
   if (st != GDN_OK) return st;
   if (!bytes) return fail(GDN_ERR_INVALID_ARGUMENT, "bytes must not be NULL");
   const gdn_problem m = mapped_problem(p);
@@ -494,12 +494,15 @@ gdn_status gdn_chunk_bwd(const gdn_problem *pin, const void *q, const void *k, c
                          const float *g_cumsum, const void *beta, const float *A, const void *dO,
                          const float *h0, const float *dht, void *dq, void *dk, void *dv, float *dg,
                          void *dbeta, float *dh0, void *ws, size_t ws_bytes, void *stream) {
-  gdn_status st = check_problem(pin, false);
+  gdn_status st = check_problem(pin, true);
   if (st != GDN_OK) return st;
   const gdn_problem mp = mapped_problem(pin);
   const gdn_problem *p = &mp;
   const size_t maps = map_part_bytes(pin);
   const void *q_raw = q, *k_raw = k, *beta_raw = beta;
+  const int nseg = p->segment_len > 0 ? (int)div_up(p->T, p->segment_len) : 0;
+  if (nseg > 0 && !h0)
+    return fail(GDN_ERR_INVALID_ARGUMENT, "segment_len > 0 needs h0 = S_init [B,H,nseg,K,V]");
   if (p->T > 0) {
     REQUIRE_PTR(q, "q");
     REQUIRE_PTR(k, "k");
@@ -536,11 +539,11 @@ gdn_status gdn_chunk_bwd(const gdn_problem *pin, const void *q, const void *k, c
   float *dvn = reinterpret_cast<float *>(w + L.dvnew);
   void *xw = w + L.xw;
   const bool packed = p->layout == GDN_LAYOUT_TND;
-  const int runs = packed ? p->num_seqs : p->B;
+  const int runs = packed ? p->num_seqs : (nseg > 0 ? p->B * nseg : p->B);
   int *flag = device_flag_ptr();
 
-  if (p->T == 0) {  // nothing but the state: dh0 = dht
-    if (dh0) {
+  if (p->T == 0) {  // nothing but the state: dh0 = dht (no segments at all in segment mode)
+    if (dh0 && nseg == 0 && p->segment_len == 0) {
       const size_t bytes = (size_t)runs * p->H * GDN_DK * GDN_DV * sizeof(float);
       cudaError_t e = dht ? cudaMemcpyAsync(dh0, dht, bytes, cudaMemcpyDeviceToDevice, s)
                           : cudaMemsetAsync(dh0, 0, bytes, s);
@@ -566,6 +569,8 @@ gdn_status gdn_chunk_bwd(const gdn_problem *pin, const void *q, const void *k, c
   f.cu = packed ? p->cu_seqlens : nullptr;
   f.num_seqs = p->num_seqs;
   f.num_chunks = p->num_chunks;
+  f.seg_len = p->segment_len;
+  f.nseg = nseg;
   f.g_cum_in = g_cumsum;
   f.A_in = A;
   f.dev_flag = flag;
@@ -613,6 +618,8 @@ gdn_status gdn_chunk_bwd(const gdn_problem *pin, const void *q, const void *k, c
   b.chunk_indices = packed ? p->chunk_indices : nullptr;
   b.num_seqs = p->num_seqs;
   b.num_chunks = p->num_chunks;
+  b.seg_len = p->segment_len;
+  b.nseg = nseg;
   b.dev_flag = flag;
   // 2. reverse state recurrence
   if (use_tensor_cores(p)) {
@@ -719,6 +726,107 @@ gdn_status kda_segment_summary(const gdn_problem *pin, const void *k, const void
   return ok();
 }
 
+gdn_status kda_segment_summary_bwd_workspace(const gdn_problem *p, int32_t segment_len, size_t *bytes) {
+  if (!p) return fail(GDN_ERR_INVALID_ARGUMENT, "problem is NULL");
+  if (segment_len <= 0 || segment_len % GDN_CHUNK != 0)
+    return fail(GDN_ERR_INVALID_ARGUMENT, "segment_len must be a positive multiple of 64, got %d",
+                segment_len);
+  gdn_problem sp = *p;
+  sp.segment_len = segment_len;
+  return gdn_chunk_bwd_workspace(&sp, bytes);
+}
+
+gdn_status kda_segment_summary_bwd(const gdn_problem *pin, const void *q, const void *k,
+                                   const float *g_cumsum, const void *beta, const float *A,
+                                   const void *dO, int32_t segment_len, float *dS_ext, void *ws,
+                                   size_t ws_bytes, void *stream) {
+  gdn_status st = check_problem(pin, true);
+  if (st != GDN_OK) return st;
+  if (pin->layout != GDN_LAYOUT_BSND)
+    return fail(GDN_ERR_UNSUPPORTED, "segment summaries take the BSND layout");
+  if (segment_len <= 0 || segment_len % GDN_CHUNK != 0)
+    return fail(GDN_ERR_INVALID_ARGUMENT, "segment_len must be a positive multiple of 64, got %d",
+                segment_len);
+  gdn_problem sp = mapped_problem(pin);
+  sp.segment_len = segment_len;
+  const gdn_problem *p = &sp;
+  REQUIRE_PTR(q, "q");
+  REQUIRE_PTR(k, "k");
+  REQUIRE_PTR(g_cumsum, "g_cumsum");
+  REQUIRE_PTR(beta, "beta");
+  REQUIRE_PTR(A, "A");
+  REQUIRE_PTR(dO, "dO");
+  REQUIRE_PTR(dS_ext, "dS_ext");
+  const size_t maps = map_part_bytes(pin);
+  const BwdWs L = bwd_ws_layout(p);
+  if (!ws || ws_bytes < maps + L.total)
+    return fail(GDN_ERR_WORKSPACE, "backward segment summary workspace needs %zu bytes, got %zu",
+                maps + L.total, ws ? ws_bytes : (size_t)0);
+  if (!aligned16(ws)) return fail(GDN_ERR_INVALID_ARGUMENT, "ws must be 16-byte aligned");
+  int dev;
+  if ((st = check_device(&dev)) != GDN_OK) return st;
+  if (p->T == 0) return ok();
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (maps > 0) {  // the forward's mapped q, k and beta
+    cudaError_t e = run_input_maps(pin, &q, &k, &beta, ws, s);
+    if (e != cudaSuccess) return cuda_fail(e, "input map launch");
+  }
+  char *w = static_cast<char *>(ws) + maps;
+  const int nseg = (int)div_up(p->T, segment_len);
+  gdn::BwdArgs b{};
+  b.q = q;
+  b.k = k;
+  b.beta = beta;
+  b.dO = dO;
+  b.g_cumsum = g_cumsum;
+  b.A = A;
+  b.dht = nullptr;  // every segment's reverse pass starts from a zero gradient at its exit
+  b.dh0 = dS_ext;
+  b.dh_chunks = reinterpret_cast<float *>(w + L.dh_chunks);
+  b.dvnew = reinterpret_cast<float *>(w + L.dvnew);
+  b.B = p->B;
+  b.T = p->T;
+  b.H = p->H;
+  b.scale = eff_scale(p);
+  b.use_exp2 = p->use_exp2;
+  b.seg_len = segment_len;
+  b.nseg = nseg;
+  b.dev_flag = device_flag_ptr();
+  cudaError_t e;
+  if (use_tensor_cores(p)) {
+    const gdn::UtArgs u = ut_args(p, k, nullptr, g_cumsum, beta, w + L.xw, nullptr, nullptr, b.dev_flag);
+    if ((e = gdn::launch_ut(u, (int)n_chunk_slots(p), s)) != cudaSuccess) return cuda_fail(e, "UT transform launch");
+    b.xw = u.xw;
+    b.ftab = u.ftab;
+    e = gdn::launch_tc_dhu(b, p->B * nseg, s);
+  } else {
+    e = gdn::launch_bwd_dhu(b, p->gate_kind == GDN_GATE_PER_KEY, p->dtype == GDN_DTYPE_BF16, s);
+  }
+  if (e != cudaSuccess) return cuda_fail(e, "backward segment summary launch");
+  return ok();
+}
+
+gdn_status kda_segment_merge_bwd(const gdn_problem *p, const float *dS_ext, const float *M,
+                                 int32_t nseg, const float *dht, float *dS_exit, float *dh0,
+                                 void *stream) {
+  gdn_status st = check_problem(p, true);
+  if (st != GDN_OK) return st;
+  if (p->layout != GDN_LAYOUT_BSND)
+    return fail(GDN_ERR_UNSUPPORTED, "segment merge takes the BSND layout");
+  if (nseg < 1) return fail(GDN_ERR_INVALID_ARGUMENT, "nseg must be >= 1, got %d", nseg);
+  REQUIRE_PTR(dS_ext, "dS_ext");
+  REQUIRE_PTR(M, "M");
+  REQUIRE_PTR(dS_exit, "dS_exit");
+  OPTIONAL_PTR(dht, "dht");
+  OPTIONAL_PTR(dh0, "dh0");
+  int dev;
+  if ((st = check_device(&dev)) != GDN_OK) return st;
+  gdn::MergeArgs a{dS_ext, M, dht, dS_exit, dh0, p->B * p->H, nseg, 1};
+  cudaError_t e = gdn::launch_merge(a, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "adjoint segment merge launch");
+  return ok();
+}
+
 gdn_status kda_segment_merge(const gdn_problem *p, const float *S_ext, const float *M,
                              int32_t nseg, const float *h0, float *S_init, float *ht,
                              void *stream) {
@@ -734,7 +842,7 @@ gdn_status kda_segment_merge(const gdn_problem *p, const float *S_ext, const flo
   OPTIONAL_PTR(ht, "ht");
   int dev;
   if ((st = check_device(&dev)) != GDN_OK) return st;
-  gdn::MergeArgs a{S_ext, M, h0, S_init, ht, p->B * p->H, nseg};
+  gdn::MergeArgs a{S_ext, M, h0, S_init, ht, p->B * p->H, nseg, 0};
   cudaError_t e = gdn::launch_merge(a, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "segment merge launch");
   return ok();

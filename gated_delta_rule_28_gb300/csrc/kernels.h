@@ -88,10 +88,15 @@ cudaError_t launch_ut(const UtArgs &a, int slots, cudaStream_t st);
 cudaError_t launch_tc_fwd_ws(const SimtFwdArgs &a, dim3 grid, cudaStream_t st);
 int tc_fwd_ws_bv();
 
+// Ordered merge of segment summaries. adjoint = 0: S_init_0 = h0, S_init_{s+1} = M_s S_init_s
+// + S_ext_s, ht the state after the last segment. adjoint = 1 (the backward): the gradient
+// runs from the last segment to the first through M^T: S_init receives every segment's exit
+// gradient (dS_exit_{nseg-1} = h0 = dht), S_ext holds the backward summaries, ht receives dh0.
 struct MergeArgs {
   const float *S_ext, *M, *h0;
   float *S_init, *ht;
   int BH, nseg;
+  int adjoint;
 };
 cudaError_t launch_merge(const MergeArgs &a, cudaStream_t st);
 
@@ -112,6 +117,7 @@ struct BwdArgs {
   const int32_t *cu;
   const int32_t *chunk_indices;
   int num_seqs, num_chunks;
+  int seg_len, nseg;  // segment runs when nseg > 0: dht / dh0 are [B, H, nseg, K, V]
   int *dev_flag;
 };
 cudaError_t launch_bwd_dhu(const BwdArgs &a, bool per_key, bool bf16, cudaStream_t st);

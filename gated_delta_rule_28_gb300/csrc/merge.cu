@@ -3,7 +3,10 @@
 // S_init_0 = h0 (or 0), S_init_{s+1} = M_s S_init_s + S_ext_s, all fp32
 // (apply_kda_state_summary on the hyper-parallel "Diff Coverage" page, which
 // keeps the communicated state in fp32 with autocast off; SANA
-// distributed_scan.py _exclusive_prefix_compose).
+// distributed_scan.py _exclusive_prefix_compose). The adjoint (backward) merge walks the
+// segments from the last to the first with the transposed maps: dS_exit_{nseg-1} = dht,
+// dS_entry_s = M_s^T dS_exit_s + dS_ext_s, dS_exit_{s-1} = dS_entry_s
+// (_CPAllGatherMerge.backward in SANA's distributed_scan.py).
 //
 // The columns of the state are independent, so one CTA owns one (batch row and
 // head, 8 state columns) and walks the segments in order; its 128 threads own
@@ -39,9 +42,12 @@ __global__ void __launch_bounds__(NTH) merge_kernel(MergeArgs a) {
   const int64_t KV = (int64_t)GDN_DK * GDN_DV;
   const uint32_t sMa = static_cast<uint32_t>(__cvta_generic_to_shared(sM));
 
-  auto fetch_M = [&](int s) {  // every thread copies one row: 32 chunks of 16 bytes
-    const float *Ms = a.M + (bh * a.nseg + s) * M_FLOATS + (int64_t)m * GDN_DK;
-    const uint32_t dst = sMa + (uint32_t)((s & 1) * M_FLOATS) * 4u;
+  const bool adj = a.adjoint != 0;
+  // segment visited at step i (forward order, or reverse for the adjoint)
+  auto seg_at = [&](int i) { return adj ? a.nseg - 1 - i : i; };
+  auto fetch_M = [&](int i) {  // every thread copies one row: 32 chunks of 16 bytes
+    const float *Ms = a.M + (bh * a.nseg + seg_at(i)) * M_FLOATS + (int64_t)m * GDN_DK;
+    const uint32_t dst = sMa + (uint32_t)((i & 1) * M_FLOATS) * 4u;
 #pragma unroll 8
     for (int c4 = 0; c4 < 32; ++c4) cp_async16(dst + (uint32_t)msw(m, c4) * 4u, Ms + 4 * c4, 16u);
     cp_async_commit();
@@ -57,7 +63,7 @@ __global__ void __launch_bounds__(NTH) merge_kernel(MergeArgs a) {
   for (int j = 0; j < BV; ++j) sS[m * BV + j] = cur[j];
   if (a.nseg > 0) fetch_M(0);
   for (int s = 0; s < a.nseg; ++s) {
-    const int64_t slot = bh * a.nseg + s;
+    const int64_t slot = bh * a.nseg + seg_at(s);
     // this segment's entry state, and its local term
     float4 *dst = reinterpret_cast<float4 *>(a.S_init + slot * KV + (int64_t)m * GDN_DV + col0);
     dst[0] = make_float4(cur[0], cur[1], cur[2], cur[3]);
@@ -74,8 +80,14 @@ __global__ void __launch_bounds__(NTH) merge_kernel(MergeArgs a) {
     for (int j = 0; j < BV; ++j) acc[j] = 0.f;
 #pragma unroll 4
     for (int c4 = 0; c4 < 32; ++c4) {
-      const float4 mv = *reinterpret_cast<const float4 *>(Mb + msw(m, c4));
-      const float mk[4] = {mv.x, mv.y, mv.z, mv.w};
+      float mk[4];
+      if (!adj) {  // row m of M
+        const float4 mv = *reinterpret_cast<const float4 *>(Mb + msw(m, c4));
+        mk[0] = mv.x; mk[1] = mv.y; mk[2] = mv.z; mk[3] = mv.w;
+      } else {  // row m of M^T: column m of M (a warp reads 32 consecutive columns of one row)
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) mk[kk] = Mb[msw(4 * c4 + kk, m >> 2) + (m & 3)];
+      }
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk) {
         const float4 s0 = *reinterpret_cast<const float4 *>(Sb + (4 * c4 + kk) * BV);

@@ -184,7 +184,11 @@ gdn_status gdn_chunk_bwd_workspace(const gdn_problem *p, size_t *bytes);
  *                   gate (not its cumulative sum).
  *   dh0           : nullable fp32 [N, H, K, V] gradient of h0.
  *   ws, ws_bytes  : workspace of at least gdn_chunk_bwd_workspace bytes.
- * segment_len must be 0. With use_qk_l2norm / use_beta_sigmoid the inputs are
+ * With segment_len > 0 (BSND) this is the corrected backward of the segment
+ * split: h0 is the S_init of every segment [B, H, nseg, K, V] (required), dht
+ * the gradient at every segment's exit [B, H, nseg, K, V] (kda_segment_merge_bwd),
+ * and dh0 receives the gradient at every segment's entry [B, H, nseg, K, V].
+ * With use_qk_l2norm / use_beta_sigmoid the inputs are
  * the raw q, k, beta of the forward (A and g_cumsum its saved slots), and dq,
  * dk, dbeta are w.r.t. those raw inputs: the prologue recomputes the mapped
  * inputs into the workspace and an epilogue kernel applies the chain rules of
@@ -239,6 +243,40 @@ gdn_status kda_segment_summary_workspace(const gdn_problem *p, int32_t segment_l
 gdn_status kda_segment_summary(const gdn_problem *p, const void *k, const void *v,
                                const float *g, const void *beta, int32_t segment_len,
                                float *S_ext, float *M, void *ws, size_t ws_bytes, void *stream);
+
+/* Backward segment summary (state_summary.py kda_state_grad_ext_kernel): for
+ * every batch row b, head h and segment s of segment_len tokens (BSND), the
+ * gradient of the segment's entry state from the segment's own outputs alone,
+ * i.e. the reverse recurrence dv_new = kgl dh + scale A_qk^T dO,
+ * dh <- Diag(b^(G_last)) dh + scale Qg^T dO - w^T dv_new run over the segment
+ * from a zero gradient at its exit. It needs no forward state, so every segment
+ * runs at once. The gradient flows across segments through the forward summary's
+ * transfer maps transposed (kda_segment_merge_bwd).
+ *   q, k, g_cumsum, beta, A, dO : as for gdn_chunk_bwd (v is not needed).
+ *   dS_ext        : device fp32 [B, H, nseg, K, V].
+ *   ws, ws_bytes  : at least kda_segment_summary_bwd_workspace bytes. */
+gdn_status kda_segment_summary_bwd_workspace(const gdn_problem *p, int32_t segment_len,
+                                             size_t *bytes);
+gdn_status kda_segment_summary_bwd(const gdn_problem *p, const void *q, const void *k,
+                                   const float *g_cumsum, const void *beta, const float *A,
+                                   const void *dO, int32_t segment_len, float *dS_ext, void *ws,
+                                   size_t ws_bytes, void *stream);
+
+/* Adjoint of the ordered merge (SANA distributed_scan.py,
+ * _CPAllGatherMerge.backward; the "Diff Coverage" page's state-summary apply
+ * helpers, backward): from the last segment to the first, in fp32,
+ *   dS_exit_{nseg-1} = dht (or 0),  dS_entry_s = M_s^T dS_exit_s + dS_ext_s,
+ *   dS_exit_{s-1} = dS_entry_s.
+ *   dS_ext, M : device fp32 [B, H, nseg, K, V] (kda_segment_summary_bwd) and
+ *               [B, H, nseg, K, K] (kda_segment_summary).
+ *   dht       : nullable device fp32 [B, H, K, V].
+ *   dS_exit   : device fp32 [B, H, nseg, K, V], the gradient at every segment's
+ *               exit (the dht of gdn_chunk_bwd in segment mode).
+ *   dh0       : nullable device fp32 [B, H, K, V], the gradient of the initial
+ *               state (dS_entry_0). */
+gdn_status kda_segment_merge_bwd(const gdn_problem *p, const float *dS_ext, const float *M,
+                                 int32_t nseg, const float *dht, float *dS_exit, float *dh0,
+                                 void *stream);
 
 /* Ordered merge of segment summaries (apply_kda_state_summary on the
  * "Diff Coverage" page; _exclusive_prefix_compose in SANA's
