@@ -310,7 +310,7 @@ constexpr size_t local_smem_floats() {
   // K, Q, (G), X, P, Aqk, slice buffers, beta, dbeta, EL, dGLh, dGlast, dGrow
   using S = LocalStrides<T, PER_KEY>;
   return 2 * 64 * S::kp + (PER_KEY ? 64 * S::kp : 3 * 64) + 3 * 64 * S::cp +
-         (2 * 128 * S::lvp + 6 * 64 * S::lvp) + 64 + 64 + 128 + 128 + 128 + 64;
+         (2 * 128 * S::lvp + 6 * 64 * S::lvp) + 64 + 64 + 128 + 128 + 128 + 64 + 3 * 64 + 8 * 128 + 8;
 }
 
 template <typename T, bool PER_KEY>
@@ -340,6 +340,11 @@ __global__ void __launch_bounds__(NTH, 1) local_kernel(BwdArgs a) {
   float *sDGLh = sEL + 128;   // sum_c dh_{c+1} (.) h per key channel
   float *sDGlast = sDGLh + 128;
   float *sDGrow = sDGlast + 128;
+  // partial sums, each slot with one writer and summed in a fixed order, so that the
+  // gradients do not depend on the order threads arrive in (no shared-memory atomics)
+  float *sDBpart = sDGrow + 64;      // [3][64]: dbeta from the two column halves, and from dL
+  float *sGlPart = sDBpart + 3 * 64;  // [8 warps][128]: dG_last per key channel
+  float *sRowX = sGlPart + 8 * 128;   // [4 warps]: the G_last term of the scalar gate
 
   const int tid = threadIdx.x, H = a.H, h = blockIdx.y;
   const int64_t zc = blockIdx.x;
@@ -404,6 +409,7 @@ __global__ void __launch_bounds__(NTH, 1) local_kernel(BwdArgs a) {
     sBeta[tid] = tid < n ? to_f32(beta[(c0 + tid) * H + h]) : 0.f;
     sDBeta[tid] = 0.f;
     sDGrow[tid] = 0.f;
+    sDBpart[tid] = sDBpart[64 + tid] = sDBpart[128 + tid] = 0.f;
     if (!PER_KEY) sG[tid] = a.g_cumsum[(c0 + min(tid, n - 1)) * H + h];
   }
   if (tid < 128) {
@@ -619,7 +625,10 @@ __global__ void __launch_bounds__(NTH, 1) local_kernel(BwdArgs a) {
             sDYs[i * LVP + c] = -sBeta[i] * fd[j][e];
             if (i < n) dv[((c0 + i) * H + h) * GDN_DV + vs + c] = from_f32<T>(sBeta[i] * fd[j][e]);
           }
-        atomicAdd(&sDBeta[i], db);
+        // the row's four lanes, then one writer per (column half, row)
+        db += __shfl_xor_sync(0xffffffffu, db, 1);
+        db += __shfl_xor_sync(0xffffffffu, db, 2);
+        if (ft == 0) sDBpart[64 * (tid >> 7) + i] += db;
       }
     } else if (tid < 64 * LBV / 4) {
       const int i = tid / (LBV / 4), c4 = (tid % (LBV / 4)) * 4;
@@ -640,7 +649,10 @@ __global__ void __launch_bounds__(NTH, 1) local_kernel(BwdArgs a) {
         sDYs[i * LVP + c4 + y] = -sBeta[i] * acc2[y];
         if (i < n) dv[((c0 + i) * H + h) * GDN_DV + vs + c4 + y] = from_f32<T>(sBeta[i] * acc2[y]);
       }
-      atomicAdd(&sDBeta[i], db);
+      // the row's LBV/4 consecutive lanes, then one writer per row
+#pragma unroll
+      for (int off = 1; off < LBV / 4; off <<= 1) db += __shfl_xor_sync(0xffffffffu, db, off);
+      if (c4 == 0) sDBpart[i] += db;
     }
     if (tid < GDN_DK) {
       float acc = 0.f;
@@ -757,8 +769,13 @@ __global__ void __launch_bounds__(NTH, 1) local_kernel(BwdArgs a) {
         rows[x] = fmaf(dL, sP[i * CP + j], rows[x]);
         dPv[x][y] = sBeta[i] * dL;
       }
+    // the 16 lanes of a row block (consecutive threads), then one writer per row
 #pragma unroll
-    for (int x = 0; x < 4; ++x) atomicAdd(&sDBeta[pm0 + x], rows[x]);
+    for (int x = 0; x < 4; ++x) {
+#pragma unroll
+      for (int off = 1; off < 16; off <<= 1) rows[x] += __shfl_xor_sync(0xffffffffu, rows[x], off);
+      if ((tid & 15) == 0) sDBpart[128 + pm0 + x] = rows[x];
+    }
     __syncthreads();  // every read of sP (the gated Gram) is done
 #pragma unroll
     for (int x = 0; x < 4; ++x)
@@ -795,8 +812,12 @@ __global__ void __launch_bounds__(NTH, 1) local_kernel(BwdArgs a) {
       rdG[x][y] = lnb * (dQg * qq * eg + aKg[x][y] * kk * eg - aKl[x][y] * kk * egl);
       colGl[y] = fmaf(aKl[x][y] * kk, egl, colGl[y]);
     }
+  // threads t and t + 16 of a warp share the columns, then one slot per (warp, column)
 #pragma unroll
-  for (int y = 0; y < 8; ++y) atomicAdd(&sDGlast[gn0 + y], colGl[y]);
+  for (int y = 0; y < 8; ++y) {
+    colGl[y] += __shfl_xor_sync(0xffffffffu, colGl[y], 16);
+    if (lane < 16) sGlPart[(tid >> 5) * 128 + gn0 + y] = colGl[y];
+  }
   // Gram adjoints, one at a time: (dP K), (dP^T K), (dAqk K), (dAqk^T Q), with Gamma
   for (int which = 0; which < 4; ++which) {
     const float *Mx = which < 2 ? sP : sAqk;
@@ -872,7 +893,15 @@ __global__ void __launch_bounds__(NTH, 1) local_kernel(BwdArgs a) {
       dk[off] = from_f32<T>(rdk[x][y]);
     }
   }
-  __syncthreads();  // sDGlast complete; sQ free for the gate gradient
+  __syncthreads();  // the dG_last slots are complete; sQ is free for the gate gradient
+  if (tid < GDN_DK) {
+    float acc = 0.f;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) acc += sGlPart[w * 128 + tid];
+    sDGlast[tid] = acc;
+  }
+  if (tid < 64) sDBeta[tid] = sDBpart[tid] + sDBpart[64 + tid] + sDBpart[128 + tid];
+  __syncthreads();
   // ---- gate gradient: add G_last terms, reverse cumulative sum ---------------
   if (PER_KEY) {
     float *sDG = sQ;
@@ -891,19 +920,28 @@ __global__ void __launch_bounds__(NTH, 1) local_kernel(BwdArgs a) {
       }
     }
   } else {
+    // the 16 lanes of a row block, then one writer per row
 #pragma unroll
     for (int x = 0; x < 4; ++x) {
-      float s = 0.f;
+      float sr = 0.f;
 #pragma unroll
-      for (int y = 0; y < 8; ++y) s += rdG[x][y];
-      atomicAdd(&sDGrow[gm0 + x], s);
+      for (int y = 0; y < 8; ++y) sr += rdG[x][y];
+#pragma unroll
+      for (int off = 1; off < 16; off <<= 1) sr += __shfl_xor_sync(0xffffffffu, sr, off);
+      if ((tid & 15) == 0) sDGrow[gm0 + x] = sr;
     }
-    if (tid < GDN_DK) atomicAdd(&sDGrow[n - 1], lnb * (sDGlast[tid] + sEL[tid] * sDGLh[tid]));
+    if (tid < GDN_DK) {  // the G_last term, summed over the key channels warp by warp
+      float xg = lnb * (sDGlast[tid] + sEL[tid] * sDGLh[tid]);
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) xg += __shfl_xor_sync(0xffffffffu, xg, off);
+      if (lane == 0) sRowX[tid >> 5] = xg;
+    }
     __syncthreads();
     if (tid == 0) {
       float run = 0.f;
+      const float extra = sRowX[0] + sRowX[1] + sRowX[2] + sRowX[3];
       for (int i = n - 1; i >= 0; --i) {
-        run += sDGrow[i];
+        run += sDGrow[i] + (i == n - 1 ? extra : 0.f);
         a.dg[(c0 + i) * H + h] = run;
       }
     }

@@ -116,3 +116,22 @@ def test_forward_and_backward_with_input_maps(dtype, per_key):
     assert rel_frob(host(f["ht"]), ht) <= TOL[dtype]
     want = R.backward(host(q), host(k), inp.v, inp.g, host(braw), inp.h0, inp.dO, None, **okw)
     _compare({n: host(x) for n, x in gr.items()}, want, TOL[dtype])
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("per_key", [False, True])
+def test_backward_is_bit_reproducible(dtype, per_key):
+    """No reduction of the backward depends on thread arrival order: two runs on the same
+    inputs give identical bits in every gradient."""
+    import torch
+    from gated_delta_rule_28_gb300 import api, binding, workloads
+    inp = workloads.make(4 if per_key else 5, B=2, T=200, H=2, dtype=dtype, with_h0=True, with_dO=True)
+    d = to_dev(inp)
+    kw = dict(use_exp2=inp.use_exp2)
+    f = api.chunk_gated_delta_rule_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], h0=d["h0"],
+                                       return_g_cumsum=True, return_A=True, **kw)
+    runs = [api.chunk_gated_delta_rule_bwd(d["q"], d["k"], d["v"], f["g_cumsum"], d["beta"], f["A"],
+                                           d["dO"], h0=d["h0"], **kw) for _ in range(2)]
+    binding.gdn_device_status()
+    for name in runs[0]:
+        assert torch.equal(runs[0][name], runs[1][name]), name

@@ -12,7 +12,6 @@ import numpy as np
 import pytest
 
 from tests.conftest import cuda_available
-from tests.helpers import host, rel_frob
 
 pytestmark = pytest.mark.gpu
 
@@ -46,22 +45,10 @@ def _args(d, o):
             o["dq"], o["dk"], o["dv"], o["dg"], o["dbeta"], o["dh0"])
 
 
-def _bf16_ulps(a, b):
-    """Largest distance, in representable bf16 steps, between two bf16 tensors of one sign pattern."""
-    import torch
-    ia = a.contiguous().view(torch.int16).to(torch.int32)
-    ib = b.contiguous().view(torch.int16).to(torch.int32)
-    same_sign = ((ia < 0) == (ib < 0)) | (ia == ib)
-    assert bool(same_sign.all())
-    return int((ia - ib).abs().max().item()) if ia.numel() else 0
-
-
 def test_backward_without_allocation_matches_workspace_backward():
-    """Same kernels, same inputs: dq, dk, dv and dh0 must be bit-identical. dg and dbeta
-    sum partial products with shared-memory atomics whose order may change between runs,
-    so they may differ by the rounding of that sum only: 1e-6 relative for dg (fp32) and
-    at most one bf16 step per element for dbeta. A stale or aliased scratch word moves
-    results far more than either bound."""
+    """Same kernels, same inputs, and no step of the backward depends on the order in
+    which threads arrive (no atomics): every output must be bit-identical. A stale or
+    aliased word of the built-in scratch would show up as a difference."""
     if not cuda_available():
         pytest.skip("no CUDA device")
     import torch
@@ -77,10 +64,8 @@ def test_backward_without_allocation_matches_workspace_backward():
         got = _outputs(d)
         B.gdn_chunk_bwd_noalloc(p, *_args(d, got))
         B.gdn_device_status()
-        for name in ("dq", "dk", "dv", "dh0"):
+        for name in ref:
             assert torch.equal(got[name], ref[name]), (seed, name)
-        assert rel_frob(host(got["dg"]), host(ref["dg"])) <= 1e-6, seed
-        assert _bf16_ulps(got["dbeta"], ref["dbeta"]) <= 1, seed
 
 
 def test_backward_without_allocation_rejects_oversized_problems():
