@@ -300,12 +300,13 @@ def _time_ms(fn, reps, warmup, stream):
 ROWS = ("packed_fwd", "kda_split_fwd", "train_fwd_bwd")
 
 
-def secondary_rows(dev, hbm_peak, only=None, reps=None, kda_tokens=65536):
+def secondary_rows(dev, hbm_peak, only=None, reps=None, kda_tokens=65536, train_tokens=8192):
     """The other scope rows, each on its own workload at full size (device-generated
     seeded inputs with the workloads' distributions; timing only, parity is in tests).
     ``only`` restricts the run to one row; ``reps`` overrides the timed repetitions
     (a profiler capture wants few); ``kda_tokens`` shrinks the per-key workload for a
-    profiler capture (same distributions and segment length)."""
+    profiler capture (same distributions and segment length), ``train_tokens`` the training
+    workload's tokens per batch row."""
     import torch
     from gated_delta_rule_28_gb300 import api, binding as Bd
     g = torch.Generator(device=dev)
@@ -353,9 +354,10 @@ def secondary_rows(dev, hbm_peak, only=None, reps=None, kda_tokens=65536):
                                     "hbm_frac_split": kda_bytes / (ms_split * 1e-3) / 1e9 / hbm_peak}
             del q, k, v, gg, beta
         if want("train_fwd_bwd"):  # training step: forward with saved slots + backward, B8 H16 T8192
-            q, k, v, gg, beta = common((8, 8192, 16, 128), (8, 8192, 16), 0.1)
+            TT = train_tokens
+            q, k, v, gg, beta = common((8, TT, 16, 128), (8, TT, 16), 0.1)
             h0 = 0.1 * torch.randn((8, 16, 128, 128), device=dev, generator=g)
-            dO = torch.randn((8, 8192, 16, 128), device=dev, generator=g).to(torch.bfloat16)
+            dO = torch.randn((8, TT, 16, 128), device=dev, generator=g).to(torch.bfloat16)
             f = api.chunk_gated_delta_rule_fwd(q, k, v, gg, beta, h0=h0, return_g_cumsum=True,
                                                return_A=True, stream=stream.cuda_stream)
             ms_f = _time_ms(lambda: api.chunk_gated_delta_rule_fwd(q, k, v, gg, beta, h0=h0, return_g_cumsum=True,
@@ -364,7 +366,7 @@ def secondary_rows(dev, hbm_peak, only=None, reps=None, kda_tokens=65536):
             ms_b = _time_ms(lambda: api.chunk_gated_delta_rule_bwd(q, k, v, f["g_cumsum"], beta, f["A"], dO,
                                                                    h0=h0, stream=stream.cuda_stream), R(2), 1, stream)
             out["train_fwd_bwd"] = {"workload": "gdn_train_bf16", "ms_fwd": ms_f, "ms_bwd": ms_b,
-                                    "tokens_per_s": 8 * 8192 / (ms_f + ms_b) * 1e3}
+                                    "tokens_per_s": 8 * TT / (ms_f + ms_b) * 1e3, "tokens": TT}
     Bd.gdn_device_status(stream.cuda_stream)
     return out
 
@@ -538,6 +540,7 @@ def main():
     ap.add_argument("--row", choices=ROWS, help="time only this secondary row and print it (profiling)")
     ap.add_argument("--reps", type=int, default=None, help="timed repetitions of --row")
     ap.add_argument("--kda-tokens", type=int, default=65536, help="tokens of the per-key row (profiling)")
+    ap.add_argument("--train-tokens", type=int, default=8192, help="tokens per batch row of the training row")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -550,7 +553,8 @@ def main():
         torch.cuda.set_device(0)
         hbm, _, _ = _peaks()
         print(json.dumps(secondary_rows(torch.device("cuda", 0), hbm, only=args.row, reps=args.reps,
-                                        kda_tokens=args.kda_tokens)), flush=True)
+                                        kda_tokens=args.kda_tokens, train_tokens=args.train_tokens)),
+              flush=True)
         return 0
     return run_ours(args)
 
