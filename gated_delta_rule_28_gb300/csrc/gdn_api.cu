@@ -631,7 +631,8 @@ gdn_status gdn_chunk_bwd(const gdn_problem *pin, const void *q, const void *k, c
   }
   if (e != cudaSuccess) return cuda_fail(e, "dhu launch");
   // 3. local gradients
-  if ((e = gdn::launch_bwd_local(b, pk, bf, s)) != cudaSuccess) return cuda_fail(e, "local gradient launch");
+  e = use_tensor_cores(p) ? gdn::launch_bwd_local_tc(b, s) : gdn::launch_bwd_local(b, pk, bf, s);
+  if (e != cudaSuccess) return cuda_fail(e, "local gradient launch");
   // 4. chain rules of the input maps, in place: gradients w.r.t. the raw q, k and beta
   if (maps > 0) {
     gdn::InputMapArgs m{};

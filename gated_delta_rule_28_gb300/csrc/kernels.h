@@ -122,6 +122,8 @@ struct BwdArgs {
 };
 cudaError_t launch_bwd_dhu(const BwdArgs &a, bool per_key, bool bf16, cudaStream_t st);
 cudaError_t launch_bwd_local(const BwdArgs &a, bool per_key, bool bf16, cudaStream_t st);
+// local gradients on bf16 tensor cores (mma.sync), bf16 inputs with a scalar gate
+cudaError_t launch_bwd_local_tc(const BwdArgs &a, cudaStream_t st);
 // tcgen05 reverse state recurrence (bf16, scalar gate); needs a.xw / a.ftab
 cudaError_t launch_tc_dhu(const BwdArgs &a, int runs, cudaStream_t st);
 
