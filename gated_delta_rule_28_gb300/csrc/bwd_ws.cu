@@ -365,7 +365,11 @@ __global__ void __launch_bounds__(NTH, 1) tc_dhu_kernel(BwdArgs a, const __grid_
     const int64_t c = chunk_of(m);
     const int64_t c0 = r0 + c * GDN_CHUNK;
     const int n = chunk_rows(c);
-    {  // gradient of this chunk's exit state
+    if (a.dh_tiles) {  // gradient of this chunk's exit state, as a bf16 tile (key `row`)
+      uint8_t *tb = reinterpret_cast<uint8_t *>(a.dh_tiles + state_slot(c) * STATE_TILE) + (col0 >> 6) * 16384;
+#pragma unroll
+      for (int q8 = 0; q8 < 4; ++q8) *reinterpret_cast<uint4 *>(tb + chunk_off(row, 4 * hc + q8)) = pack8(dh + 8 * q8);
+    } else {  // fp32
       float4 *dst = reinterpret_cast<float4 *>(a.dh_chunks + state_slot(c) * GDN_DK * GDN_DV +
                                                (int64_t)row * GDN_DV + col0 + 32 * hc);
 #pragma unroll
@@ -383,11 +387,16 @@ __global__ void __launch_bounds__(NTH, 1) tc_dhu_kernel(BwdArgs a, const __grid_
       const bool valid = row < n;
       float4 *gdst = reinterpret_cast<float4 *>(a.dvnew + ((c0 + (valid ? row : 0)) * H + h) * GDN_DV + col0 + 32 * hc);
 #pragma unroll
+      uint8_t *dvt = a.dv_tiles ? reinterpret_cast<uint8_t *>(a.dv_tiles + state_slot(c) * DV_TILE) + (col0 >> 6) * 8192
+                                : nullptr;
       for (int part = 0; part < 2; ++part) {
         float dv[16];
         tmem_ld16(tl + T_I1 + 64 * cs + 32 * hc + 16 * part, dv);
         tmem_ld_wait();
-        if (valid) {
+        if (dvt) {  // bf16 tile (rows past the end hold values the local kernel never uses)
+          *reinterpret_cast<uint4 *>(dvt + chunk_off(row, 4 * hc + 2 * part)) = pack8(dv);
+          *reinterpret_cast<uint4 *>(dvt + chunk_off(row, 4 * hc + 2 * part + 1)) = pack8(dv + 8);
+        } else if (valid) {
 #pragma unroll
           for (int g4 = 0; g4 < 4; ++g4)
             gdst[4 * part + g4] = make_float4(dv[4 * g4], dv[4 * g4 + 1], dv[4 * g4 + 2], dv[4 * g4 + 3]);

@@ -337,13 +337,21 @@ __global__ void __launch_bounds__(NTH, 1) tc_fwd_ws_kernel(SimtFwdArgs a, const 
     const int par = (int)(c & 1);
     const int64_t c0 = r0 + c * GDN_CHUNK;
     const int n = chunk_rows(c);
-    if (a.h_chunks) {  // entry state of chunk c
+    if (a.h_chunks || a.h_tiles) {  // entry state of chunk c
       const int64_t slot = a.cu ? (chunk_base + c) * H + h : ((int64_t)b * H + h) * NT + chunk_base + c;
-      float4 *dst = reinterpret_cast<float4 *>(a.h_chunks + slot * GDN_DK * GDN_DV + (int64_t)row * GDN_DV +
-                                               col0 + 32 * hc);
+      if (a.h_chunks) {
+        float4 *dst = reinterpret_cast<float4 *>(a.h_chunks + slot * GDN_DK * GDN_DV + (int64_t)row * GDN_DV +
+                                                 col0 + 32 * hc);
 #pragma unroll
-      for (int g4 = 0; g4 < 8; ++g4)
-        dst[g4] = make_float4(hreg[g4 * 4], hreg[g4 * 4 + 1], hreg[g4 * 4 + 2], hreg[g4 * 4 + 3]);
+        for (int g4 = 0; g4 < 8; ++g4)
+          dst[g4] = make_float4(hreg[g4 * 4], hreg[g4 * 4 + 1], hreg[g4 * 4 + 2], hreg[g4 * 4 + 3]);
+      }
+      if (a.h_tiles) {  // key `row`, values col0 + 32 hc .. +31: four 16-byte chunks of the tile
+        uint8_t *tb = reinterpret_cast<uint8_t *>(a.h_tiles + slot * STATE_TILE) + (col0 >> 6) * 16384;
+#pragma unroll
+        for (int q8 = 0; q8 < 4; ++q8)
+          *reinterpret_cast<uint4 *>(tb + chunk_off(row, 4 * hc + q8)) = pack8(hreg + 8 * q8);
+      }
     }
     if (warp == 0) {  // P4: [w; Q] h
       fence_after_sync();

@@ -303,15 +303,20 @@ struct BwdWs {
   size_t h_chunks, dh_chunks, dvnew, xw, total;
 };
 
+// Backward workspace: entry states, exit-state gradients, dv_new, then the forward's. The bf16
+// scalar-gate path keeps the first three as bf16 tiles in its local kernel's layout (32 KB, 32 KB
+// and 16 KB per chunk and head); the other paths as fp32 arrays.
 BwdWs bwd_ws_layout(const gdn_problem *p) {
-  const size_t KV = (size_t)GDN_DK * GDN_DV * sizeof(float);
   BwdWs w{};
   const size_t slots = (size_t)n_chunk_slots(p) * p->H;
   const size_t rows = (size_t)p->B * p->T;
+  const bool tiles = use_tensor_cores(p);
+  const size_t state = tiles ? (size_t)gdn::STATE_TILE * 2 : (size_t)GDN_DK * GDN_DV * sizeof(float);
+  const size_t dv = tiles ? slots * gdn::DV_TILE * 2 : rows * p->H * GDN_DV * sizeof(float);
   w.h_chunks = 0;
-  w.dh_chunks = align256(slots * KV);
-  w.dvnew = w.dh_chunks + align256(slots * KV);
-  w.xw = w.dvnew + align256(rows * p->H * GDN_DV * sizeof(float));
+  w.dh_chunks = align256(slots * state);
+  w.dvnew = w.dh_chunks + align256(slots * state);
+  w.xw = w.dvnew + align256(dv);
   w.total = w.xw + x_ws_bytes(p);
   return w;
 }
@@ -553,6 +558,7 @@ gdn_status gdn_chunk_bwd(const gdn_problem *pin, const void *q, const void *k, c
   }
 
   // 1. entry state of every chunk, from the saved cumulative gate and A
+  const bool tiles = use_tensor_cores(p);
   gdn::SimtFwdArgs f{};
   f.q = q;
   f.k = k;
@@ -560,7 +566,8 @@ gdn_status gdn_chunk_bwd(const gdn_problem *pin, const void *q, const void *k, c
   f.g = g_cumsum;
   f.beta = beta;
   f.h0 = h0;
-  f.h_chunks = hch;
+  f.h_chunks = tiles ? nullptr : hch;
+  f.h_tiles = tiles ? reinterpret_cast<__nv_bfloat16 *>(hch) : nullptr;
   f.B = p->B;
   f.T = p->T;
   f.H = p->H;
@@ -609,6 +616,11 @@ gdn_status gdn_chunk_bwd(const gdn_problem *pin, const void *q, const void *k, c
   b.h_chunks = hch;
   b.dh_chunks = dhch;
   b.dvnew = dvn;
+  if (tiles) {
+    b.h_tiles = reinterpret_cast<const __nv_bfloat16 *>(hch);
+    b.dh_tiles = reinterpret_cast<__nv_bfloat16 *>(dhch);
+    b.dv_tiles = reinterpret_cast<__nv_bfloat16 *>(dvn);
+  }
   b.B = p->B;
   b.T = p->T;
   b.H = p->H;
@@ -785,6 +797,10 @@ gdn_status kda_segment_summary_bwd(const gdn_problem *pin, const void *q, const 
   b.dh0 = dS_ext;
   b.dh_chunks = reinterpret_cast<float *>(w + L.dh_chunks);
   b.dvnew = reinterpret_cast<float *>(w + L.dvnew);
+  if (use_tensor_cores(p)) {  // the workspace holds bf16 tiles on this path
+    b.dh_tiles = reinterpret_cast<__nv_bfloat16 *>(w + L.dh_chunks);
+    b.dv_tiles = reinterpret_cast<__nv_bfloat16 *>(w + L.dvnew);
+  }
   b.B = p->B;
   b.T = p->T;
   b.H = p->H;

@@ -56,8 +56,15 @@ struct SimtFwdArgs {
   const float *A_in;      // nullable: read X = (I + L)^-1 instead of solving
   const __nv_bfloat16 *xw;  // tensor-core path: [X diag(b); X diag(b e^G)] of every chunk, [slots, H, 128, 64] bf16
   const float *ftab;        // tensor-core path: gate factor table of every chunk, [slots, H, F_TAB]
+  // nullable: the entry state of every chunk in bf16, as the backward's local kernel reads it:
+  // per (chunk slot, head) a [128 keys x 128 values] tile of two 64-column K-blocks (16 KB
+  // each, 128-byte rows swizzled by key), slots as h_chunks
+  __nv_bfloat16 *h_tiles;
   int *dev_flag;
 };
+// elements of one state tile (h_tiles, dh_tiles) and of one dv_new tile (dv_tiles)
+constexpr int STATE_TILE = 128 * 128;
+constexpr int DV_TILE = 64 * 128;
 
 cudaError_t launch_simt_fwd(const SimtFwdArgs &a, bool per_key, bool bf16, dim3 grid,
                             cudaStream_t st);
@@ -118,6 +125,11 @@ struct BwdArgs {
   const int32_t *chunk_indices;
   int num_seqs, num_chunks;
   int seg_len, nseg;  // segment runs when nseg > 0: dht / dh0 are [B, H, nseg, K, V]
+  // bf16 tensor-core backward: the states, exit-state gradients and dv_new as bf16 tiles in
+  // the local kernel's shared-memory layout (per chunk slot and head: h and dh [128 x 128] as two
+  // 64-column K-blocks, dv_new [64 tokens x 128] likewise), replacing h_chunks, dh_chunks, dvnew
+  const __nv_bfloat16 *h_tiles;
+  __nv_bfloat16 *dh_tiles, *dv_tiles;
   int *dev_flag;
 };
 cudaError_t launch_bwd_dhu(const BwdArgs &a, bool per_key, bool bf16, cudaStream_t st);

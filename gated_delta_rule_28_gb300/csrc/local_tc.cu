@@ -2,7 +2,8 @@
 //
 // One CTA of 8 warps per (chunk, head) computes dq, dk, dv, dbeta and dg of its chunk from
 // the chunk's inputs, its entry state h, the gradient dh of its exit state and the gradient
-// dN of v_new (the reverse recurrence's outputs) -- the finalize stage of the backward
+// dN of v_new (the recompute's and the reverse recurrence's outputs, bf16 tiles in this
+// kernel's shared-memory layout, fetched with cp.async) -- the finalize stage of the backward
 // (the KDA adapter's chunk_kda_bwd_finalize on the "Diff Coverage" page; the GDN adapter's
 // chunk_gated_delta_rule_bwd contract). With gamma_i = b^(G_i), lambda_i = b^(G_last - G_i),
 // Gamma_ij = b^(G_i - G_j) and X = (I + L)^-1 (the forward's A slot):
@@ -180,12 +181,10 @@ __global__ void __launch_bounds__(NTH, 1) local_tc_kernel(BwdArgs a) {
     n = min(GDN_CHUNK, a.T - cc * GDN_CHUNK);
     slot = ((int64_t)b * H + h) * NT + cc;
   }
-  const int64_t KV = (int64_t)GDN_DK * GDN_DV;
-  const float *hc = a.h_chunks + slot * KV;
-  const float *dhc = a.dh_chunks + slot * KV;
   auto row_of = [&](int i) { return (c0 + i) * H + h; };
 
-  // ---- loads: K, Q, V, dO by cp.async (zero past the end); h, dh, dN, X converted ---------
+  // ---- loads, all by cp.async: K, Q, V, dO (zero past the end) and the bf16 tiles of h, dh
+  // and dN written by the recompute and the reverse recurrence (already in this layout) ------
   for (int x = tid; x < 1024; x += NTH) {
     const int r = x >> 4, c16 = x & 15;
     const bool valid = r < n;
@@ -196,6 +195,16 @@ __global__ void __launch_bounds__(NTH, 1) local_tc_kernel(BwdArgs a) {
     cp_async16(toff(tW, r, c16), v + off, sz);
     cp_async16(toff(tDO, r, c16), dO + off, sz);
   }
+  {
+    const uint8_t *gh = reinterpret_cast<const uint8_t *>(a.h_tiles + slot * STATE_TILE);
+    const uint8_t *gdh = reinterpret_cast<const uint8_t *>(a.dh_tiles + slot * STATE_TILE);
+    const uint8_t *gdn = reinterpret_cast<const uint8_t *>(a.dv_tiles + slot * DV_TILE);
+    for (int x = tid; x < 2048; x += NTH) {  // 32 KB each
+      cp_async16(sb + O_H + 16 * x, gh + 16 * x, 16u);
+      cp_async16(sb + O_DH + 16 * x, gdh + 16 * x, 16u);
+    }
+    for (int x = tid; x < 1024; x += NTH) cp_async16(sb + O_DN + 16 * x, gdn + 16 * x, 16u);  // 16 KB
+  }
   cp_async_commit();
   if (tid < 64) {
     const int i = tid;
@@ -203,32 +212,6 @@ __global__ void __launch_bounds__(NTH, 1) local_tc_kernel(BwdArgs a) {
     sv.G[i] = G;
     sv.beta[i] = i < n ? __bfloat162float(beta[row_of(i)]) : 0.f;
     sv.gam[i] = gexp<E2>(G);
-  }
-  // h and dh (fp32, 128 x 128) -> bf16 tiles; <dh, h> for the gradient of the last gate
-  float hdh = 0.f;
-#pragma unroll 2
-  for (int x = tid; x < 128 * 16; x += NTH) {  // one row, 8 values per step
-    const int r = x >> 4, c16 = x & 15;
-    const float4 *ph = reinterpret_cast<const float4 *>(hc + r * GDN_DV + c16 * 8);
-    const float4 *pd = reinterpret_cast<const float4 *>(dhc + r * GDN_DV + c16 * 8);
-    const float4 h0 = ph[0], h1 = ph[1], d0 = pd[0], d1 = pd[1];
-    const float hv[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
-    const float dv8[8] = {d0.x, d0.y, d0.z, d0.w, d1.x, d1.y, d1.z, d1.w};
-#pragma unroll
-    for (int e = 0; e < 8; ++e) hdh = fmaf(hv[e], dv8[e], hdh);
-    *reinterpret_cast<uint4 *>(sm + (toff(tH, r, c16) - sb)) = pack8(hv);
-    *reinterpret_cast<uint4 *>(sm + (toff(tDH, r, c16) - sb)) = pack8(dv8);
-  }
-  // dN (fp32 [rows, H, V]) -> bf16 tile
-  for (int x = tid; x < 64 * 16; x += NTH) {
-    const int r = x >> 4, c16 = x & 15;
-    float dn[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    if (r < n) {
-      const float4 *p = reinterpret_cast<const float4 *>(a.dvnew + row_of(r) * GDN_DV + c16 * 8);
-      const float4 u0 = p[0], u1 = p[1];
-      dn[0] = u0.x; dn[1] = u0.y; dn[2] = u0.z; dn[3] = u0.w; dn[4] = u1.x; dn[5] = u1.y; dn[6] = u1.z; dn[7] = u1.w;
-    }
-    *reinterpret_cast<uint4 *>(sm + (toff(tDN, r, c16) - sb)) = pack8(dn);
   }
   __syncthreads();  // beta and the gate of every row are in place
   if (tid < 64) sv.lam[tid] = gexp<E2>(sv.G[63] - sv.G[tid]);
@@ -245,12 +228,28 @@ __global__ void __launch_bounds__(NTH, 1) local_tc_kernel(BwdArgs a) {
     *reinterpret_cast<uint4 *>(sm + (toff(tX, r, c8) - sb)) = pack8(xv);
     *reinterpret_cast<uint4 *>(sm + (toff(tXB, r, c8) - sb)) = pack8(xb);
   }
-  {  // <dh, h> over the CTA: lanes, then one slot per warp
+  cp_async_wait<0>();
+  __syncthreads();
+  // rows of dN past the chunk's end are zero (the tile holds whatever the reverse recurrence
+  // computed there); <dh, h> over the whole state for the gradient of the last gate
+  if (n < 64)
+    for (int x = tid; x < (64 - n) * 16; x += NTH) {
+      const int r = n + x / 16, c16 = x % 16;
+      *reinterpret_cast<uint4 *>(sm + (toff(tDN, r, c16) - sb)) = make_uint4(0, 0, 0, 0);
+    }
+  {
+    float hdh = 0.f;
+    for (int x = tid; x < 2048; x += NTH) {  // the same swizzle in both tiles: element-wise
+      float hv[8], dv8[8];
+      unpack8(*reinterpret_cast<const uint4 *>(sm + O_H + 16 * x), hv);
+      unpack8(*reinterpret_cast<const uint4 *>(sm + O_DH + 16 * x), dv8);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) hdh = fmaf(hv[e], dv8[e], hdh);
+    }
 #pragma unroll
     for (int off = 16; off; off >>= 1) hdh += __shfl_xor_sync(0xffffffffu, hdh, off);
     if (lane == 0) sv.gl[warp] = hdh;
   }
-  cp_async_wait<0>();
   __syncthreads();
 
   // warp tile of the 64 x 128 products: rows m0 .. +15, columns n0 .. +63

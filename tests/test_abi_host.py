@@ -115,10 +115,15 @@ def test_null_and_misaligned_pointers_are_rejected_before_launch(lib):
 
 
 def test_backward_workspace_size(lib):
-    p = B.make_problem(2, 130, 3)
-    n = B.gdn_chunk_bwd_workspace(p)
     slots = 2 * 3 * 3  # B * H * ceil(130/64)
-    assert n >= 2 * slots * 128 * 128 * 4 + 2 * 130 * 3 * 128 * 4
+    # fp32: entry states and exit-state gradients (fp32 [K, V] per chunk and head), dv_new per token
+    p = B.make_problem(2, 130, 3, dtype=B.GDN_DTYPE_F32)
+    assert B.gdn_chunk_bwd_workspace(p) >= 2 * slots * 128 * 128 * 4 + 2 * 130 * 3 * 128 * 4
+    # bf16 scalar gate: the same as bf16 tiles (K x V per chunk and head, 64 x V for dv_new), then
+    # the forward's X pair (128 x 64 bf16) and gate table (9 x 64 fp32) per chunk and head
+    p = B.make_problem(2, 130, 3)
+    assert B.gdn_chunk_bwd_workspace(p) >= (2 * slots * 128 * 128 * 2 + slots * 64 * 128 * 2
+                                            + slots * 128 * 64 * 2 + slots * 9 * 64 * 4)
 
 
 @pytest.mark.parametrize("polls", [0, (1 << 20) + 1])
