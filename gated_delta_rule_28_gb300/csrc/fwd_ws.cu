@@ -1,5 +1,6 @@
-// Tensor-core (tcgen05) chunk forward for bf16 inputs, scalar gate (sm_103a),
-// state recurrence overlapped with the preparation of the next chunk.
+// Tensor-core (tcgen05) chunk forward for bf16 inputs, scalar gate (sm_103a):
+// the state recurrence, with the preparation of the next chunk and the output
+// of the current one interleaved on the tensor pipe.
 //
 // One CTA (512 threads) owns one independent run (batch row, packed document
 // or segment) of one head and 64 of the 128 state columns; the UT transform
@@ -7,24 +8,35 @@
 // as the pair [X diag(b); X diag(b e^G)] in bf16. Per chunk (GDN Ascend C adapter
 // forward, chunk_fwd_h and the output step):
 //
-//   producer warps 8..15, chunk c+1 (no dependence on the state):
 //     P1   S = Q K^T                           -> A_qk = lower-incl(Q K^T (.) Gamma)
 //     P3   [X diag(b); X diag(b e^G)] [K | V]  -> w = X diag(b e^G) K,  u = X diag(b) V
-//          w rows of the operand [w; Q] of P4 (Q is loaded into it)
-//   chain warps 0..7, chunk c (the state h lives in their registers, fp32):
 //     P4   [w; Q] h                            -> v_new = u - w h,  Q h
 //     P5   K^T (e^(G_last - G) v_new)          -> h <- e^(G_last) h + P5
 //     PO   A_qk v_new                          -> o = scale (e^G (Q h) + A_qk v_new)
 //
-// The two warp groups meet once per chunk (a CTA barrier); every buffer one group
-// writes while the other reads is double-buffered by chunk parity (K, read by P5 one
-// round later, by three).
-// Loads are TMA copies (tensor tiles with the 128-byte swizzle, and bulk copies
-// of the chunk's gate factors) completing on mbarriers. No operand is
-// transposed: the token-major tiles (K, V, v_new, h by key) enter the MMAs as
-// MN-major operands, and every row the threads write is a run of 16-byte stores.
-// Every mbarrier wait is bounded; a wait that runs out sets the device flag and
-// the CTA drains its MMAs, frees its tensor memory and leaves.
+// Only P4 -> v_new -> P5 -> h is a dependence chain from one chunk to the next;
+// the tensor pipe runs one MMA group at a time, so one warp issues every MMA in
+// the order P4(c), P3(c+1), P5(c), PO(c), P1(c+1): the next chunk's preparation
+// fills the pipe while the chain converts v_new and h, and the output term runs
+// while the chain waits for its next state. The warps are split by role and meet
+// only on mbarriers (no CTA barrier per chunk):
+//   warps 0..7   the state h in fp32 registers (thread = key row, 32 columns):
+//                v_new (lane quarters 0, 1: token rows), Q h and the output
+//                (quarters 2, 3), the update of h and its bf16 copy
+//   warps 8, 9, 12, 13   the gating of Q K^T into A_qk
+//   warp 10      the MMAs and the tensor copies of K, the X pair, V and the gate table
+//   warps 11, 14, 15     w from tensor memory into the rows of the P4 operand [w; Q]
+// The issuer waits on five barriers per chunk: "ready for P4" (h, w and the read of
+// the previous Q h), the loads of chunk c+1, v_new, "ready for PO" (A_qk and the read of
+// the previous output term) and Q of chunk c+1. Buffers are double- or triple-buffered so
+// that every wait is for the event it names and no mbarrier runs two phases ahead of a
+// thread that waits on it.
+// Loads are TMA copies (tensor tiles with the 128-byte swizzle, and bulk copies of
+// the gate table). No operand is transposed: the token-major tiles (K, V, v_new, h
+// by key) enter the MMAs as MN-major operands. Every mbarrier wait is bounded; a
+// wait that runs out raises the CTA's abort word, the others give up within a few
+// hundred polls, and the CTA drains its MMAs and copies, frees its tensor memory
+// and leaves with the device flag set.
 #include <string.h>
 
 #include "common.cuh"
@@ -38,7 +50,7 @@ using namespace tc;
 using namespace tile;
 
 constexpr int TBV = 64;   // state columns per CTA
-constexpr int NTH = 512;  // threads per CTA: 256 chain + 256 producer
+constexpr int NTH = 512;  // 8 chain warps + 8 preparation warps
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t T_S = 0;     // 64: P1 (rows 0..63 = Q K^T)
 constexpr uint32_t T_PO = 64;   // 64: PO (rows 64..127 = A_qk v_new)
@@ -52,20 +64,22 @@ constexpr uint32_t T_P5 = 448;  // 64: P5
 // are. P1 and PO use 128-row A operands whose rows 64..127 (P1) or 0..63 (PO) are not
 // needed: they read whatever follows (precedes) the tile, and land in unread rows of D.
 constexpr int OFF_WQ = 0;                     // [w; Q] per chunk parity: 2 K-blocks x 128 rows
-constexpr int OFF_K = OFF_WQ + 2 * 32768;     // K, three chunks in flight: 2 K-blocks x 64 rows
+constexpr int OFF_K = OFF_WQ + 2 * 32768;     // K per chunk mod 3: 2 K-blocks x 64 rows
 constexpr int OFF_XX = OFF_K + 3 * 16384;     // [X diag(b); X diag(b e^G)] per parity: 128 rows
 constexpr int OFF_V = OFF_XX + 2 * 16384;     // V slice per parity: 64 rows
 constexpr int OFF_HT = OFF_V + 2 * 8192;      // h: 128 key rows (MN-major B of P4)
 constexpr int OFF_VN = OFF_HT + 16384;        // v_new: 64 token rows (MN-major B of PO)
 constexpr int OFF_VNL = OFF_VN + 8192;        // e^(Gl - G) v_new (MN-major B of P5)
 constexpr int OFF_AQ = OFF_VNL + 8192;        // A_qk per parity: 64 rows (PO's rows 0..63: the 8 KB before)
-constexpr int OFF_SMALL = OFF_AQ + 2 * 8192;
-constexpr int SMALL_BYTES = 6144;
+constexpr int OFF_TAB = OFF_AQ + 2 * 8192;    // gate table per chunk mod 3 (F_TAB floats)
+constexpr int OFF_SMALL = OFF_TAB + 3 * F_TAB * 4;
+constexpr int SMALL_BYTES = 512;
 constexpr int SMEM_BYTES = OFF_SMALL + SMALL_BYTES + 1024;
 static_assert(SMEM_BYTES <= 232448, "shared memory");
-// The MN-major K operand (two 64-key groups 8 KB apart, 64 token rows) stays below the small
-// state under either assignment of its descriptor's two stride fields: groups 8 KB apart and
-// K rows in 1 KB atoms, or the reverse. The other MN-major operands have one group.
+static_assert((F_TAB * 4) % 16 == 0 && OFF_TAB % 16 == 0, "bulk copy alignment");
+// The MN-major K operand (two 64-key groups 8 KB apart, 64 token rows) stays inside shared
+// memory under either assignment of its descriptor's two stride fields: groups 8 KB apart
+// and K rows in 1 KB atoms, or the reverse. The other MN-major operands have one group.
 static_assert(OFF_K + 2 * 16384 + 8192 + 8 * 1024 <= OFF_XX &&
                   OFF_K + 2 * 16384 + 1024 + 7 * 8192 + 1024 <= OFF_SMALL,
               "MN-major K operand extent");
@@ -73,23 +87,33 @@ static_assert(OFF_K + 2 * 16384 + 8192 + 8 * 1024 <= OFF_XX &&
 constexpr uint32_t WAIT_LIMIT = 1u << 22;
 
 struct WsState {
-  alignas(16) float tab[2][F_ROWS][64];  // refilled with chunk c+2 while the chain runs chunk c
-  float EGL[2][64];                 // base^(G_last - G) per chunk parity, for the chain
-  float EG[2][64];                  // base^G per chunk parity, for the chain
-  float EL[2];                      // base^(G_last) per chunk parity, for the chain
-  uint64_t bar_p1, bar_p3, bar_p4, bar_p5, bar_po, bar_d0, bar_d1, bar_d2;
-  uint64_t bar_ld[2];  // TMA loads per chunk parity: K, the X pair, V, gate factors
-  uint64_t bar_q[2];   // TMA loads per chunk parity: Q (issued once P4 has read the buffer)
+  // MMA completions (tcgen05.commit by the issuing warp)
+  uint64_t p1, p3, p4, p5, po, d0;
+  // hand-offs to the issuer: ready for P4(c) = h(c) (8 chain warps) + w(c) (3) + Q h of
+  // c-1 read (4 output warps); v_new(c) (4); ready for PO(c) = A_qk(c) (4 gating warps) +
+  // output of c-1 read (4 output warps)
+  uint64_t rdy4, vn, rdyo;
+  uint64_t ld[3];  // TMA loads per chunk mod 3: K, the X pair, V and the gate table
+  uint64_t q[2];   // TMA loads per chunk parity: Q (issued once P4 has read the buffer)
   uint32_t tmem;
+  int abort;       // raised by a wait that ran out; the other waits then give up
 };
 static_assert(sizeof(WsState) <= SMALL_BYTES, "small state");
-
-__device__ __forceinline__ void chain_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
 
 // TMA maps: q, k, v over [rows, H*128]; the X pair over [slots*H*128, 64]; 64 x 64 boxes
 struct FwdMaps {
   TmaMap q, k, v, x;
 };
+
+// Polls until the phase of `parity` has completed; false once `limit` polls ran out or
+// (checked every 256 polls) the CTA's abort word is set.
+__device__ __forceinline__ bool poll(uint64_t *bar, uint32_t parity, const volatile int *abort) {
+  for (uint32_t i = 0; i < WAIT_LIMIT; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 255u) == 255u && *abort) return false;
+  }
+  return false;
+}
 
 template <bool E2>
 __global__ void __launch_bounds__(NTH, 1) tc_fwd_ws_kernel(SimtFwdArgs a, const __grid_constant__ FwdMaps maps) {
@@ -101,7 +125,7 @@ __global__ void __launch_bounds__(NTH, 1) tc_fwd_ws_kernel(SimtFwdArgs a, const 
   const uint32_t sb = smem_u32(sm);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const bool producer = warp >= 8;
+  const bool chain_warp = warp < 8;
   const int q4 = warp & 3;         // tensor-memory lane quarter of this warp
   const int hc = (warp >> 2) & 1;  // column half (32 of 64) inside the warp group
   const int row = q4 * 32 + lane;  // tensor-memory lane = matrix row
@@ -145,8 +169,8 @@ __global__ void __launch_bounds__(NTH, 1) tc_fwd_ws_kernel(SimtFwdArgs a, const 
     state_idx = b;
     xbase = (int64_t)b * NT;
   }
-  const int64_t nch = (r1 - r0 + GDN_CHUNK - 1) / GDN_CHUNK;
-  auto chunk_rows = [&](int64_t c) { return (int)min((int64_t)GDN_CHUNK, r1 - (r0 + c * GDN_CHUNK)); };
+  const int nch = (int)((r1 - r0 + GDN_CHUNK - 1) / GDN_CHUNK);
+  auto chunk_rows = [&](int c) { return (int)min((int64_t)GDN_CHUNK, r1 - (r0 + (int64_t)c * GDN_CHUNK)); };
 
   // ---- tensor memory, barriers -----------------------------------------------------
   if (warp == 0) {
@@ -154,18 +178,19 @@ __global__ void __launch_bounds__(NTH, 1) tc_fwd_ws_kernel(SimtFwdArgs a, const 
     tmem_relinquish();
   }
   if (tid == 0) {
-    mbar_init(&st.bar_p1, 1);
-    mbar_init(&st.bar_p3, 1);
-    mbar_init(&st.bar_p4, 1);
-    mbar_init(&st.bar_p5, 1);
-    mbar_init(&st.bar_po, 1);
-    mbar_init(&st.bar_d0, 1);
-    mbar_init(&st.bar_d1, 1);
-    mbar_init(&st.bar_d2, 1);
-    mbar_init(&st.bar_q[0], 1);
-    mbar_init(&st.bar_q[1], 1);
-    mbar_init(&st.bar_ld[0], 1);
-    mbar_init(&st.bar_ld[1], 1);
+    mbar_init(&st.p1, 1);
+    mbar_init(&st.p3, 1);
+    mbar_init(&st.p4, 1);
+    mbar_init(&st.p5, 1);
+    mbar_init(&st.po, 1);
+    mbar_init(&st.d0, 1);
+    mbar_init(&st.rdy4, 15);
+    mbar_init(&st.vn, 4);
+    mbar_init(&st.rdyo, 8);
+    for (int i = 0; i < 3; ++i) mbar_init(&st.ld[i], 1);
+    mbar_init(&st.q[0], 1);
+    mbar_init(&st.q[1], 1);
+    st.abort = 0;
     mbar_fence_init();
   }
   fence_before_sync();
@@ -175,92 +200,153 @@ __global__ void __launch_bounds__(NTH, 1) tc_fwd_ws_kernel(SimtFwdArgs a, const 
   asm volatile("griddepcontrol.wait;" ::: "memory");
   const uint32_t tmem = st.tmem;
   const uint32_t tl = tmem + ((uint32_t)(q4 * 32) << 16);  // this warp's lane quarter
+  volatile int *abort_word = &st.abort;
   bool bad = false;
-  auto wait_par = [&](uint64_t *bar, int64_t phase) {
-    if (!mbar_wait(bar, (uint32_t)(phase & 1), WAIT_LIMIT)) bad = true;
+  // warp-uniform bounded wait for the completion of phase `phase` (its parity)
+  auto wt = [&](uint64_t *bar, int phase) -> bool {
+    bool ok = poll(bar, (uint32_t)(phase & 1), abort_word);
+    ok = __all_sync(0xffffffffu, ok);
+    if (!ok) {
+      bad = true;
+      *abort_word = 1;
+    }
     fence_after_sync();
+    return ok;
   };
-  auto wq_at = [&](int64_t c) { return sb + OFF_WQ + (uint32_t)(c & 1) * 32768u; };
-  auto k_at = [&](int64_t c) { return sb + OFF_K + (uint32_t)(c % 3) * 16384u; };
-  auto xx_at = [&](int64_t c) { return sb + OFF_XX + (uint32_t)(c & 1) * 16384u; };
-  auto v_at = [&](int64_t c) { return sb + OFF_V + (uint32_t)(c & 1) * 8192u; };
+  // one arrival per warp, after the warp's shared-memory writes (made visible to the tensor
+  // core) and tensor-memory reads
+  auto arrive_w = [&](uint64_t *bar) {
+    fence_proxy_async();
+    fence_before_sync();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar);
+  };
+  auto wq_at = [&](int c) { return sb + OFF_WQ + (uint32_t)(c & 1) * 32768u; };
+  auto k_at = [&](int c) { return sb + OFF_K + (uint32_t)(c % 3) * 16384u; };
+  auto xx_at = [&](int c) { return sb + OFF_XX + (uint32_t)(c & 1) * 16384u; };
+  auto v_at = [&](int c) { return sb + OFF_V + (uint32_t)(c & 1) * 8192u; };
+  auto tab_at = [&](int c) { return reinterpret_cast<const float(*)[64]>(sm + OFF_TAB + (c % 3) * (F_TAB * 4)); };
 
-  // ---- producer: loads (TMA, issued by warp 9) ------------------------------------------
-  // Every TMA copy and tcgen05 MMA is issued warp-collectively (one elected lane of a
-  // warp-uniform call, tc.cuh): warp 9 the loads and P1, warp 10 P3, warp 0 the chain's
-  // MMAs and its Q loads.
-  // Rows past the run end are loaded as they are (the next run's tokens, or zeros past
-  // the tensor): they only meet beta = 0 (zero columns of both X's), a causal mask, or rows
-  // of o that are not stored.
-  const int ptid = tid - 256;
-  const bool loader = warp == 9;
-  const bool issuer = warp == 10;  // producer MMAs: P3 by warp 10, P1 by warp 9
-  int64_t last_ld[2] = {-1, -1};   // loader: newest chunk per barrier
-  auto issue_loads = [&](int64_t c) {  // K, the X pair, V and the gate factors of chunk c
-    const int s2 = (int)(c & 1);
-    const int y = (int)(r0 + c * GDN_CHUNK);
-    const int64_t xs = (xbase + c) * H + h;
-    uint64_t *bar = &st.bar_ld[s2];
-    mbar_expect_tx_w(bar, 5 * 8192 + F_ROWS * GDN_CHUNK * 4);
-    tma_load_2d_w(k_at(c), &maps.k, h * GDN_DK, y, bar);
-    tma_load_2d_w(k_at(c) + 8192, &maps.k, h * GDN_DK + 64, y, bar);
-    tma_load_2d_w(xx_at(c), &maps.x, 0, (int)(xs * 2 * GDN_CHUNK), bar);
-    tma_load_2d_w(xx_at(c) + 8192, &maps.x, 0, (int)(xs * 2 * GDN_CHUNK + GDN_CHUNK), bar);
-    tma_load_2d_w(v_at(c), &maps.v, h * GDN_DV + col0, y, bar);
-    bulk_load_w(smem_u32(&st.tab[s2][0][0]), a.ftab + xs * F_TAB, F_ROWS * GDN_CHUNK * 4, bar);
-    last_ld[s2] = c;
-  };
-  // Q of chunk c into rows 64..127 of [w; Q] of parity c&1, by the chain's warp 0 (the
-  // buffer held chunk c-2, whose P4 it waits for)
-  int64_t last_q[2] = {-1, -1};
-  auto issue_q = [&](int64_t c) {
-    const int s2 = (int)(c & 1);
-    const int y = (int)(r0 + c * GDN_CHUNK);
-    mbar_expect_tx_w(&st.bar_q[s2], 2 * 8192);
-    tma_load_2d_w(wq_at(c) + 8192, &maps.q, h * GDN_DK, y, &st.bar_q[s2]);
-    tma_load_2d_w(wq_at(c) + 16384 + 8192, &maps.q, h * GDN_DK + 64, y, &st.bar_q[s2]);
+  int last_ld[3] = {-1, -1, -1};  // issuer: newest chunk loaded per buffer
+  int last_q[2] = {-1, -1};       // chain warp 0: newest Q load per parity
+  float hreg[32];                     // chain warps: the state (key `row`, 32 columns)
+  // Q of chunk c into rows 64..127 of [w; Q] of parity c&1, by chain warp 0 once P4 of
+  // chunk c-2 (the last reader of the buffer) has completed
+  auto issue_q = [&](int c) {
+    const int s2 = c & 1;
+    const int y = (int)(r0 + (int64_t)c * GDN_CHUNK);
+    mbar_expect_tx_w(&st.q[s2], 2 * 8192);
+    tma_load_2d_w(wq_at(c) + 8192, &maps.q, h * GDN_DK, y, &st.q[s2]);
+    tma_load_2d_w(wq_at(c) + 16384 + 8192, &maps.q, h * GDN_DK + 64, y, &st.q[s2]);
     last_q[s2] = c;
   };
 
-  // ---- producer: one chunk -------------------------------------------------------------
-  // warps 8, 9, 12, 13 (lane quarters 0, 1): gating of Q K^T; warps 10, 11, 14, 15
-  // (quarters 2, 3): the w rows of the P4 operand.
-  auto produce = [&](int64_t pc) {
-    const int ps = (int)(pc & 1);
-    const float(&tab)[F_ROWS][64] = st.tab[ps];
-    // buffers of chunk pc+1 (they held chunk pc-1, and K chunk pc-2: finished, P4 included)
-    if (loader && pc + 1 < nch) issue_loads(pc + 1);
-    wait_par(&st.bar_ld[ps], pc >> 1);  // K, X's, V and factors of chunk pc have landed
-    if (issuer) {
-      // P3: [X diag(b); X diag(b e^G)] [K | V] -> rows 64..127 of the K product = w,
-      // rows 0..63 of the V product = u (K and V token-major, read as MN-major B)
-      mma_ops_w(tmem + T_WW, kmaj(xx_at(pc), 0), mnmaj(k_at(pc), 8192), 64, idesc_bf16(128, 128, false, false, true),
-              false);
-      mma_ops_w(tmem + T_U + 64 * ps, kmaj(xx_at(pc), 0), mnmaj(v_at(pc), 0), 64,
-              idesc_bf16(128, 64, false, false, true), false);
-      mma_commit_w(&st.bar_p3);
+  if (warp == 10) {
+    // ---- MMA issue and loads -------------------------------------------------------------
+    // Every TMA copy and tcgen05 MMA is issued warp-collectively (one elected lane of a
+    // warp-uniform call, tc.cuh). Rows past the run end are loaded as they are (the next
+    // run's tokens, or zeros past the tensor): they only meet beta = 0 (zero columns of
+    // both X's), a causal mask, or rows of o that are not stored.
+    auto issue_loads = [&](int c) {  // K, the X pair, V and the gate table of chunk c
+      const int sl = c % 3;
+      const int y = (int)(r0 + (int64_t)c * GDN_CHUNK);
+      const int64_t xs = (xbase + c) * H + h;
+      uint64_t *bar = &st.ld[sl];
+      mbar_expect_tx_w(bar, 5 * 8192 + F_TAB * 4);
+      tma_load_2d_w(k_at(c), &maps.k, h * GDN_DK, y, bar);
+      tma_load_2d_w(k_at(c) + 8192, &maps.k, h * GDN_DK + 64, y, bar);
+      tma_load_2d_w(xx_at(c), &maps.x, 0, (int)(xs * 2 * GDN_CHUNK), bar);
+      tma_load_2d_w(xx_at(c) + 8192, &maps.x, 0, (int)(xs * 2 * GDN_CHUNK + GDN_CHUNK), bar);
+      tma_load_2d_w(v_at(c), &maps.v, h * GDN_DV + col0, y, bar);
+      bulk_load_w(sb + OFF_TAB + (uint32_t)sl * (F_TAB * 4), a.ftab + xs * F_TAB, F_TAB * 4, bar);
+      last_ld[sl] = c;
+    };
+    // P3: [X diag(b); X diag(b e^G)] [K | V] -> rows 64..127 of the K product = w, rows
+    // 0..63 of the V product = u (K and V token-major, read as MN-major B)
+    auto p3 = [&](int c) {
+      mma_ops_w(tmem + T_WW, kmaj(xx_at(c), 0), mnmaj(k_at(c), 8192), 64, idesc_bf16(128, 128, false, false, true),
+                false);
+      mma_ops_w(tmem + T_U + 64 * (uint32_t)(c & 1), kmaj(xx_at(c), 0), mnmaj(v_at(c), 0), 64,
+                idesc_bf16(128, 64, false, false, true), false);
+      mma_commit_w(&st.p3);
+    };
+    // P1: S = Q K^T (A rows 64..127: the next 64 rows of shared memory, unread output rows)
+    auto p1 = [&](int c) {
+      mma_ops_w(tmem + T_S, kmaj(wq_at(c) + 8192, 16384), kmaj(k_at(c), 8192), 128, idesc_bf16(128, 64), false);
+      mma_commit_w(&st.p1);
+    };
+    do {
+      if (nch > 0) issue_loads(0);
+      if (nch > 1) issue_loads(1);
+      if (nch == 0) break;
+      if (!wt(&st.ld[0], 0)) break;
+      p3(0);
+      if (!wt(&st.q[0], 0)) break;
+      p1(0);
+      for (int c = 0; c < nch; ++c) {
+        const int par = c & 1;
+        // P4(c): h(c), w(c) written, Q h of c-1 read; Q(c) landed (waited for P1(c))
+        if (!wt(&st.rdy4, c)) break;
+        mma_ops_w(tmem + T_D4, kmaj(wq_at(c), 16384), mnmaj(sb + OFF_HT, 0), 128,
+                  idesc_bf16(128, 64, false, false, true), false);
+        mma_commit_w(&st.p4);
+        // loads of chunk c+2: its X / V buffers held chunk c (P3(c) came before P5(c-1), done
+        // before h(c)); its K buffer and gate table chunk c-1 (P5(c-1) done; every warp read
+        // its factors of c-1 before h(c) or A_qk(c-1))
+        if (c + 2 < nch) issue_loads(c + 2);
+        // P3(c+1): its loads landed; w(c) and u(c-1) have left tensor memory
+        if (c + 1 < nch) {
+          if (!wt(&st.ld[(c + 1) % 3], ((c + 1) / 3) & 1)) break;
+          p3(c + 1);
+        }
+        // P5(c): K^T (e^(Gl-G) v_new), K read as MN-major A
+        if (!wt(&st.vn, c)) break;
+        mma_ops_w(tmem + T_P5, mnmaj(k_at(c), 8192), mnmaj(sb + OFF_VNL, 0), 64, idesc_bf16(128, 64, false, true, true),
+                  false);
+        mma_commit_w(&st.p5);
+        // PO(c): A_qk(c) written; the output of c-1 has read its accumulator
+        if (!wt(&st.rdyo, c)) break;
+        mma_ops_w(tmem + T_PO, kmaj(sb + OFF_AQ + par * 8192 - 8192, 0), mnmaj(sb + OFF_VN, 0), 64,
+                  idesc_bf16(128, 64, false, false, true), false);
+        mma_commit_w(&st.po);
+        // P1(c+1): Q(c+1) landed; A_qk(c) has left tensor memory
+        if (c + 1 < nch) {
+          if (!wt(&st.q[(c + 1) & 1], (c + 1) >> 1)) break;
+          p1(c + 1);
+        }
+      }
+    } while (false);
+  } else if (warp == 11 || warp == 14 || warp == 15) {
+    // ---- w rows of the P4 operand -----------------------------------------------------------
+    // rows 0..63 of [w; Q] of chunk c = P3 rows 64..127: warp 14 rows 64..95, all 128 keys;
+    // warps 11, 15 rows 96..127, keys 0..63 / 64..127
+    const int kb0 = warp == 15 ? 1 : 0, kb1 = warp == 14 ? 2 : kb0 + 1;
+    for (int c = 0; c < nch; ++c) {
+      if (!wt(&st.p3, c)) break;
+      uint8_t *wq = sm + OFF_WQ + (c & 1) * 32768;
+      for (int kb = kb0; kb < kb1; ++kb) {
+#pragma unroll
+        for (int part = 0; part < 4; ++part) {
+          float sv[16];
+          tmem_ld16(tl + T_WW + 64 * kb + 16 * part, sv);
+          tmem_ld_wait();
+          *reinterpret_cast<uint4 *>(wq + kb * 16384 + chunk_off(row - 64, 2 * part)) = pack8(sv);
+          *reinterpret_cast<uint4 *>(wq + kb * 16384 + chunk_off(row - 64, 2 * part + 1)) = pack8(sv + 8);
+        }
+      }
+      arrive_w(&st.rdy4);
     }
-    __syncwarp();  // the issuing warp reconverges before any of its lanes polls a barrier
-    if (q4 < 2) {
-      const int t = row;
-      if (ptid == 0) st.EL[ps] = tab[F_EG][63];
-      if (hc == 0) {
-        st.EGL[ps][t] = tab[F_EGL][t];
-        st.EG[ps][t] = tab[F_EG][t];
-      }
-      if (warp == 9) {
-        // P1: S = Q K^T, once Q has landed (A rows 64..127: the next 64 rows of shared
-        // memory, unread output rows)
-        wait_par(&st.bar_q[ps], pc >> 1);
-        mma_ops_w(tmem + T_S, kmaj(wq_at(pc) + 8192, 16384), kmaj(k_at(pc), 8192), 128, idesc_bf16(128, 64), false);
-        mma_commit_w(&st.bar_p1);
-      }
-      // gating of Q K^T (rows 0..63 of S) -> A_qk, lower triangle including the diagonal.
-      // Gate factors of this thread's 32 key tokens s, formed while P1 runs: between
-      // 16-token blocks from the tables, EA[t] EB_{b(t)}[s] (no exponential); inside the
-      // diagonal block base^(G_t - G_s), 16 exponentials in the two warps whose key tokens
-      // hold their rows' diagonal blocks (8: rows 0..31, keys 0..31; 13: rows 32..63, keys
-      // 32..63).
+  } else if (!chain_warp) {
+    // ---- gating of Q K^T (rows 0..63 of S) -> A_qk, lower triangle with the diagonal ----------
+    // Gate factors of this thread's 32 key tokens s, formed before P1 completes: between
+    // 16-token blocks from the tables, EA[t] EB_{b(t)}[s] (no exponential); inside the
+    // diagonal block base^(G_t - G_s), 16 exponentials in the two warps whose key tokens
+    // hold their rows' diagonal blocks (8: rows 0..31, keys 0..31; 13: rows 32..63, keys
+    // 32..63).
+    const int t = row;
+    for (int c = 0; c < nch; ++c) {
+      if (!wt(&st.ld[c % 3], (c / 3) & 1)) break;
+      const float(*tab)[64] = tab_at(c);
       float gf[32];
       {
         const int bt = t >> 4;
@@ -285,39 +371,20 @@ __global__ void __launch_bounds__(NTH, 1) tc_fwd_ws_kernel(SimtFwdArgs a, const 
           }
         }
       }
-      wait_par(&st.bar_p1, pc);
-      {
-        float sv[32];
-        tmem_ld16(tl + T_S + 32 * hc, *reinterpret_cast<float(*)[16]>(sv));
-        tmem_ld16(tl + T_S + 32 * hc + 16, *reinterpret_cast<float(*)[16]>(sv + 16));
-        tmem_ld_wait();
+      if (!wt(&st.p1, c)) break;
+      float sv[32];
+      tmem_ld16(tl + T_S + 32 * hc, *reinterpret_cast<float(*)[16]>(sv));
+      tmem_ld16(tl + T_S + 32 * hc + 16, *reinterpret_cast<float(*)[16]>(sv + 16));
+      tmem_ld_wait();
 #pragma unroll
-        for (int j = 0; j < 32; ++j) sv[j] *= gf[j];
-        uint8_t *dst = sm + OFF_AQ + ps * 8192;
+      for (int j = 0; j < 32; ++j) sv[j] *= gf[j];
+      uint8_t *dst = sm + OFF_AQ + (c & 1) * 8192;
 #pragma unroll
-        for (int q8 = 0; q8 < 4; ++q8)
-          *reinterpret_cast<uint4 *>(dst + chunk_off(t, 4 * hc + q8)) = pack8(sv + 8 * q8);
-      }
-    } else {
-      // rows 0..63 of the P4 operand [w; Q] of chunk pc (keys 64*hc .. +64), once P3 is done
-      uint8_t *wq = sm + OFF_WQ + ps * 32768 + hc * 16384;
-      wait_par(&st.bar_p3, pc);
-#pragma unroll
-      for (int part = 0; part < 4; ++part) {
-        float sv[16];
-        tmem_ld16(tl + T_WW + 64 * hc + 16 * part, sv);
-        tmem_ld_wait();
-        *reinterpret_cast<uint4 *>(wq + chunk_off(row - 64, 2 * part)) = pack8(sv);
-        *reinterpret_cast<uint4 *>(wq + chunk_off(row - 64, 2 * part + 1)) = pack8(sv + 8);
-      }
+      for (int q8 = 0; q8 < 4; ++q8) *reinterpret_cast<uint4 *>(dst + chunk_off(t, 4 * hc + q8)) = pack8(sv + 8 * q8);
+      arrive_w(&st.rdyo);
     }
-    fence_proxy_async();
-    fence_before_sync();
-  };
-
-  // ---- chain: state and one chunk ----------------------------------------------------------
-  float hreg[32];
-  if (!producer) {
+  } else {
+    // ---- chain: the state, v_new, Q h, the output ------------------------------------------------
     const float *src = nullptr;
     if (a.h0) {
       const int64_t slot = a.nseg > 0 ? (((int64_t)b * H + h) * a.nseg + s) : ((int64_t)state_idx * H + h);
@@ -325,153 +392,135 @@ __global__ void __launch_bounds__(NTH, 1) tc_fwd_ws_kernel(SimtFwdArgs a, const 
     }
 #pragma unroll
     for (int j = 0; j < 32; ++j) hreg[j] = src ? src[j] : 0.f;
-  }
-  // h in bf16 (MN-major B operand of P4): this thread's key `row`, columns 32*hc .. +32
-  auto write_ht = [&]() {
-    uint8_t *hrow = sm + OFF_HT;
+    // h in bf16 (MN-major B operand of P4): this thread's key `row`, columns 32*hc .. +32
+    auto write_ht = [&]() {
+      uint8_t *hrow = sm + OFF_HT;
 #pragma unroll
-    for (int q8 = 0; q8 < 4; ++q8)
-      *reinterpret_cast<uint4 *>(hrow + chunk_off(row, 4 * hc + q8)) = pack8(hreg + 8 * q8);
-  };
-  auto chain = [&](int64_t c) {
-    const int par = (int)(c & 1);
-    const int64_t c0 = r0 + c * GDN_CHUNK;
-    const int n = chunk_rows(c);
-    if (a.h_chunks || a.h_tiles) {  // entry state of chunk c
-      const int64_t slot = a.cu ? (chunk_base + c) * H + h : ((int64_t)b * H + h) * NT + chunk_base + c;
-      if (a.h_chunks) {
-        float4 *dst = reinterpret_cast<float4 *>(a.h_chunks + slot * GDN_DK * GDN_DV + (int64_t)row * GDN_DV +
-                                                 col0 + 32 * hc);
-#pragma unroll
-        for (int g4 = 0; g4 < 8; ++g4)
-          dst[g4] = make_float4(hreg[g4 * 4], hreg[g4 * 4 + 1], hreg[g4 * 4 + 2], hreg[g4 * 4 + 3]);
-      }
-      if (a.h_tiles) {  // key `row`, values col0 + 32 hc .. +31: four 16-byte chunks of the tile
-        uint8_t *tb = reinterpret_cast<uint8_t *>(a.h_tiles + slot * STATE_TILE) + (col0 >> 6) * 16384;
-#pragma unroll
-        for (int q8 = 0; q8 < 4; ++q8)
-          *reinterpret_cast<uint4 *>(tb + chunk_off(row, 4 * hc + q8)) = pack8(hreg + 8 * q8);
-      }
+      for (int q8 = 0; q8 < 4; ++q8)
+        *reinterpret_cast<uint4 *>(hrow + chunk_off(row, 4 * hc + q8)) = pack8(hreg + 8 * q8);
+    };
+    if (warp == 0) {
+      if (nch > 0) issue_q(0);
+      if (nch > 1) issue_q(1);
     }
-    if (warp == 0) {  // P4: [w; Q] h
-      fence_after_sync();
-      mma_ops_w(tmem + T_D4, kmaj(wq_at(c), 16384), mnmaj(sb + OFF_HT, 0), 128,
-              idesc_bf16(128, 64, false, false, true), false);
-      mma_commit_w(&st.bar_p4);
+    write_ht();
+    arrive_w(&st.rdy4);  // h(0)
+    if (q4 >= 2) {       // no Q h and no output before chunk 0
+      arrive_w(&st.rdy4);
+      arrive_w(&st.rdyo);
     }
-    __syncwarp();  // the issuing warp reconverges before any of its lanes polls a barrier
-    wait_par(&st.bar_p4, c);
-    if (warp == 0 && c + 2 < nch) issue_q(c + 2);  // P4 has read Q of chunk c
-    if (q4 < 2) {  // v_new = u - w h (token row), and e^(Gl - G) v_new
-      const float egl = st.EGL[par][row];
+    for (int c = 0; c < nch; ++c) {
+      const int par = c & 1;
+      const int64_t c0 = r0 + (int64_t)c * GDN_CHUNK;
+      const int n = chunk_rows(c);
+      if (a.h_chunks || a.h_tiles) {  // entry state of chunk c
+        const int64_t slot = a.cu ? (chunk_base + c) * H + h : ((int64_t)b * H + h) * NT + chunk_base + c;
+        if (a.h_chunks) {
+          float4 *dst = reinterpret_cast<float4 *>(a.h_chunks + slot * GDN_DK * GDN_DV + (int64_t)row * GDN_DV +
+                                                   col0 + 32 * hc);
 #pragma unroll
-      for (int part = 0; part < 2; ++part) {
-        float wh[16], u[16];
-        tmem_ld16(tl + T_D4 + 32 * hc + 16 * part, wh);
-        tmem_ld16(tl + T_U + 64 * par + 32 * hc + 16 * part, u);
-        tmem_ld_wait();
+          for (int g4 = 0; g4 < 8; ++g4)
+            dst[g4] = make_float4(hreg[g4 * 4], hreg[g4 * 4 + 1], hreg[g4 * 4 + 2], hreg[g4 * 4 + 3]);
+        }
+        if (a.h_tiles) {  // key `row`, values col0 + 32 hc .. +31: four 16-byte chunks of the tile
+          uint8_t *tb = reinterpret_cast<uint8_t *>(a.h_tiles + slot * STATE_TILE) + (col0 >> 6) * 16384;
 #pragma unroll
-        for (int j = 0; j < 16; ++j) u[j] -= wh[j];
-        *reinterpret_cast<uint4 *>(sm + OFF_VN + chunk_off(row, 4 * hc + 2 * part)) = pack8(u);
-        *reinterpret_cast<uint4 *>(sm + OFF_VN + chunk_off(row, 4 * hc + 2 * part + 1)) = pack8(u + 8);
-#pragma unroll
-        for (int j = 0; j < 16; ++j) u[j] *= egl;
-        *reinterpret_cast<uint4 *>(sm + OFF_VNL + chunk_off(row, 4 * hc + 2 * part)) = pack8(u);
-        *reinterpret_cast<uint4 *>(sm + OFF_VNL + chunk_off(row, 4 * hc + 2 * part + 1)) = pack8(u + 8);
+          for (int q8 = 0; q8 < 4; ++q8)
+            *reinterpret_cast<uint4 *>(tb + chunk_off(row, 4 * hc + q8)) = pack8(hreg + 8 * q8);
+        }
       }
-    }
-    fence_proxy_async();
-    fence_before_sync();
-    chain_sync();
-    if (warp == 0) {  // the intra-chunk output term (the output is the longer path), then
-                      // P5: K^T (e^(Gl-G) v_new), K read as MN-major A
-      fence_after_sync();
-      mma_ops_w(tmem + T_PO, kmaj(sb + OFF_AQ + par * 8192 - 8192, 0), mnmaj(sb + OFF_VN, 0), 64,
-                idesc_bf16(128, 64, false, false, true), false);
-      mma_commit_w(&st.bar_po);
-      mma_ops_w(tmem + T_P5, mnmaj(k_at(c), 8192), mnmaj(sb + OFF_VNL, 0), 64, idesc_bf16(128, 64, false, true, true),
-                false);
-      mma_commit_w(&st.bar_p5);
-    }
-    __syncwarp();  // the issuing warp reconverges before any of its lanes polls a barrier
-    wait_par(&st.bar_p5, c);
-    {
-      const float el = st.EL[par];
+      // this thread's gate factors of chunk c, read before h(c+1) is handed over (after which
+      // the table's buffer may be refilled)
+      if (!wt(&st.ld[c % 3], (c / 3) & 1)) break;
+      const float(*tab)[64] = tab_at(c);
+      const float el = tab[F_EG][63];
+      const float egl = tab[F_EGL][row & 63];
+      const float eg = tab[F_EG][row & 63];
+      if (!wt(&st.p4, c)) break;
+      if (warp == 0 && c + 2 < nch) issue_q(c + 2);  // P4 has read Q of chunk c
+      uint32_t qe[16];  // output rows: base^G Q h in bf16 pairs
+      if (q4 < 2) {  // v_new = u - w h (token row), and e^(Gl - G) v_new
 #pragma unroll
-      for (int part = 0; part < 2; ++part) {
-        float p5[16];
-        tmem_ld16(tl + T_P5 + 32 * hc + 16 * part, p5);
-        tmem_ld_wait();
+        for (int part = 0; part < 2; ++part) {
+          float wh[16], u[16];
+          tmem_ld16(tl + T_D4 + 32 * hc + 16 * part, wh);
+          tmem_ld16(tl + T_U + 64 * par + 32 * hc + 16 * part, u);
+          tmem_ld_wait();
 #pragma unroll
-        for (int j = 0; j < 16; ++j) hreg[16 * part + j] = fmaf(el, hreg[16 * part + j], p5[j]);
+          for (int j = 0; j < 16; ++j) u[j] -= wh[j];
+          *reinterpret_cast<uint4 *>(sm + OFF_VN + chunk_off(row, 4 * hc + 2 * part)) = pack8(u);
+          *reinterpret_cast<uint4 *>(sm + OFF_VN + chunk_off(row, 4 * hc + 2 * part + 1)) = pack8(u + 8);
+#pragma unroll
+          for (int j = 0; j < 16; ++j) u[j] *= egl;
+          *reinterpret_cast<uint4 *>(sm + OFF_VNL + chunk_off(row, 4 * hc + 2 * part)) = pack8(u);
+          *reinterpret_cast<uint4 *>(sm + OFF_VNL + chunk_off(row, 4 * hc + 2 * part + 1)) = pack8(u + 8);
+        }
+        arrive_w(&st.vn);
+      } else {  // base^G Q h (rows 64..127 of P4), kept for the output
+#pragma unroll
+        for (int part = 0; part < 2; ++part) {
+          float qv[16];
+          tmem_ld16(tl + T_D4 + 32 * hc + 16 * part, qv);
+          tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const __nv_bfloat162 b2 = __floats2bfloat162_rn(eg * qv[2 * j], eg * qv[2 * j + 1]);
+            qe[8 * part + j] = *reinterpret_cast<const uint32_t *>(&b2);
+          }
+        }
+        arrive_w(&st.rdy4);
       }
-      write_ht();
-      fence_proxy_async();  // h for the next P4 (the output below goes to global memory)
-      if (q4 >= 2) {  // o = scale (base^G Q h + A_qk v_new); the whole warp loads (collective)
-        wait_par(&st.bar_po, c);
-        const float eg = st.EG[par][row - 64];
+      if (!wt(&st.p5, c)) break;
+      {
+#pragma unroll
+        for (int part = 0; part < 2; ++part) {
+          float p5[16];
+          tmem_ld16(tl + T_P5 + 32 * hc + 16 * part, p5);
+          tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 16; ++j) hreg[16 * part + j] = fmaf(el, hreg[16 * part + j], p5[j]);
+        }
+        write_ht();
+        arrive_w(&st.rdy4);
+      }
+      if (q4 >= 2) {  // o = scale (base^G Q h + A_qk v_new)
+        if (!wt(&st.po, c)) break;
         const bool st_row = o && row - 64 < n;
         uint4 *dst = reinterpret_cast<uint4 *>(o + ((c0 + (st_row ? row - 64 : 0)) * H + h) * GDN_DV + col0 + 32 * hc);
 #pragma unroll
         for (int part = 0; part < 2; ++part) {
-          float ov[16], av[16];
-          tmem_ld16(tl + T_D4 + 32 * hc + 16 * part, ov);
+          float av[16];
           tmem_ld16(tl + T_PO + 32 * hc + 16 * part, av);
           tmem_ld_wait();
 #pragma unroll
-          for (int j = 0; j < 16; ++j) ov[j] = scale * fmaf(eg, ov[j], av[j]);
+          for (int j = 0; j < 8; ++j) {
+            const float2 q2 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&qe[8 * part + j]));
+            av[2 * j] = scale * (q2.x + av[2 * j]);
+            av[2 * j + 1] = scale * (q2.y + av[2 * j + 1]);
+          }
           if (st_row) {
-            dst[2 * part] = pack8(ov);
-            dst[2 * part + 1] = pack8(ov + 8);
+            dst[2 * part] = pack8(av);
+            dst[2 * part + 1] = pack8(av + 8);
           }
         }
+        arrive_w(&st.rdyo);
       }
     }
-    fence_before_sync();
-  };
-
-  // ---- prologue --------------------------------------------------------------------------
-  if (loader && nch > 0) issue_loads(0);
-  if (warp == 0) {
-    if (nch > 0) issue_q(0);
-    if (nch > 1) issue_q(1);
   }
-  if (!producer) {
-    write_ht();
-    fence_proxy_async();
-  }
-  __syncthreads();
 
-  // round c: the chain runs chunk c while the producer prepares chunk c+1
-  for (int64_t c = -1; c < nch; ++c) {
-    if (producer) {
-      if (c + 1 < nch) produce(c + 1);
-    } else if (c >= 0) {
-      chain(c);
+  if (__syncthreads_or(bad)) {
+    if (warp == 10) {
+      // the elected lane arrives once every MMA it issued has finished; copies in flight land
+      mma_commit_w(&st.d0);
+      mbar_wait(&st.d0, 0, WAIT_LIMIT);
+      for (int sl = 0; sl < 3; ++sl)
+        if (last_ld[sl] >= 0) mbar_wait(&st.ld[sl], (uint32_t)((last_ld[sl] / 3) & 1), WAIT_LIMIT);
     }
-    if (__syncthreads_or(bad)) {
-      bad = true;
-      break;
-    }
-  }
-
-  if (bad) {
-    if (tid == 0) raise_device_flag(a.dev_flag, kDevTimeout);
-    // each issuing warp's elected lane: arrives once every MMA it issued has finished
-    if (warp == 0) mma_commit_w(&st.bar_d0);
-    if (issuer) mma_commit_w(&st.bar_d1);
-    if (warp == 9) mma_commit_w(&st.bar_d2);
-    if (warp == 0) mbar_wait(&st.bar_d0, 0, WAIT_LIMIT);
-    if (issuer) mbar_wait(&st.bar_d1, 0, WAIT_LIMIT);
-    if (warp == 9) mbar_wait(&st.bar_d2, 0, WAIT_LIMIT);
     if (warp == 0)  // Q copies still in flight land before the CTA leaves
       for (int s2 = 0; s2 < 2; ++s2)
-        if (last_q[s2] >= 0) mbar_wait(&st.bar_q[s2], (uint32_t)((last_q[s2] >> 1) & 1), WAIT_LIMIT);
-    if (loader) {  // copies still in flight land before the CTA leaves
-      for (int s2 = 0; s2 < 2; ++s2)
-        if (last_ld[s2] >= 0) mbar_wait(&st.bar_ld[s2], (uint32_t)((last_ld[s2] >> 1) & 1), WAIT_LIMIT);
-    }
-  } else if (!producer && a.ht && (a.nseg == 0 || s == a.nseg - 1)) {
+        if (last_q[s2] >= 0) mbar_wait(&st.q[s2], (uint32_t)((last_q[s2] >> 1) & 1), WAIT_LIMIT);
+    if (tid == 0) raise_device_flag(a.dev_flag, kDevTimeout);
+  } else if (chain_warp && a.ht && (a.nseg == 0 || s == a.nseg - 1)) {
     float4 *dst = reinterpret_cast<float4 *>(a.ht + ((int64_t)state_idx * H + h) * GDN_DK * GDN_DV +
                                              (int64_t)row * GDN_DV + col0 + 32 * hc);
 #pragma unroll

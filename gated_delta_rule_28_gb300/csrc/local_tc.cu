@@ -67,6 +67,10 @@ __device__ __forceinline__ uint32_t toff(Tl t, int row, int c8) {
 __device__ __forceinline__ float ldt(const uint8_t *sm, uint32_t sb, Tl t, int row, int col) {
   return __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(sm + (toff(t, row, col >> 3) - sb) + (col & 7) * 2));
 }
+// columns col, col + 1 (col even: the same 16-byte chunk) of `row`
+__device__ __forceinline__ float2 ldt2(const uint8_t *sm, uint32_t sb, Tl t, int row, int col) {
+  return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(sm + (toff(t, row, col >> 3) - sb) + (col & 7) * 2));
+}
 
 __device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
   asm volatile(
@@ -260,6 +264,7 @@ __global__ void __launch_bounds__(NTH, 1) local_tc_kernel(BwdArgs a) {
   // per-row partial sums (rows m0 + g, m0 + g + 8): dbeta, dG, and the G_last terms
   float pb[2] = {0.f, 0.f}, pg[2] = {0.f, 0.f}, plast = 0.f;
   auto tile_val = [&](Tl T, int r, int c) { return ldt(sm, sb, T, r, c); };
+  auto tile_val2 = [&](Tl T, int r, int c) { return ldt2(sm, sb, T, r, c); };
 
   // ---- 1. W = V - diag(gamma) K h (in place of V) ----------------------------------------
   {
@@ -287,8 +292,9 @@ __global__ void __launch_bounds__(NTH, 1) local_tc_kernel(BwdArgs a) {
 #pragma unroll
       for (int hr = 0; hr < 2; ++hr) {
         const int r = m0 + g + 8 * hr, c = n0 + 8 * j + 2 * t4;
-        pb[hr] = fmaf(acc[j][2 * hr], tile_val(tW, r, c), pb[hr]);
-        pb[hr] = fmaf(acc[j][2 * hr + 1], tile_val(tW, r, c + 1), pb[hr]);
+        const float2 w2 = tile_val2(tW, r, c);
+        pb[hr] = fmaf(acc[j][2 * hr], w2.x, pb[hr]);
+        pb[hr] = fmaf(acc[j][2 * hr + 1], w2.y, pb[hr]);
         if (r < n) {
           const float bt = sv.beta[r];
           *reinterpret_cast<uint32_t *>(dv + row_of(r) * GDN_DV + c) = pack_bf16(bt * acc[j][2 * hr], bt * acc[j][2 * hr + 1]);
@@ -336,11 +342,12 @@ __global__ void __launch_bounds__(NTH, 1) local_tc_kernel(BwdArgs a) {
       for (int hr = 0; hr < 2; ++hr) {
         const int r = m0 + g + 8 * hr, c = n0 + 8 * j + 2 * t4;
         const float gm = sv.gam[r];
+        const float2 q2 = tile_val2(tQ, r, c);
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
           const float d = scale * acc[j][2 * hr + e];
           dqa[j][2 * hr + e] = gm * d;
-          pg[hr] = fmaf(lnb * gm * d, tile_val(tQ, r, c + e), pg[hr]);
+          pg[hr] = fmaf(lnb * gm * d, e ? q2.y : q2.x, pg[hr]);
         }
       }
   }
@@ -355,11 +362,12 @@ __global__ void __launch_bounds__(NTH, 1) local_tc_kernel(BwdArgs a) {
       for (int hr = 0; hr < 2; ++hr) {
         const int r = m0 + g + 8 * hr, c = n0 + 8 * j + 2 * t4;
         const float la = sv.lam[r];
+        const float2 k2 = tile_val2(tK, r, c);
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
           const float d = la * acc[j][2 * hr + e];
           dka[j][2 * hr + e] = d;
-          const float w = lnb * d * tile_val(tK, r, c + e);
+          const float w = lnb * d * (e ? k2.y : k2.x);
           pg[hr] -= w;
           plast += w;
         }
@@ -376,11 +384,12 @@ __global__ void __launch_bounds__(NTH, 1) local_tc_kernel(BwdArgs a) {
       for (int hr = 0; hr < 2; ++hr) {
         const int r = m0 + g + 8 * hr, c = n0 + 8 * j + 2 * t4;
         const float gm = sv.gam[r];
+        const float2 k2 = tile_val2(tK, r, c);
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
           const float d = gm * acc[j][2 * hr + e];
           dka[j][2 * hr + e] += d;
-          pg[hr] = fmaf(lnb * d, tile_val(tK, r, c + e), pg[hr]);
+          pg[hr] = fmaf(lnb * d, e ? k2.y : k2.x, pg[hr]);
         }
       }
   }
@@ -432,15 +441,16 @@ __global__ void __launch_bounds__(NTH, 1) local_tc_kernel(BwdArgs a) {
 #pragma unroll
         for (int hr = 0; hr < 2; ++hr) {
           const int r = m0 + g + 8 * hr, c = n0 + 8 * j + 2 * t4;
+          const float2 o2 = tile_val2(which == 2 ? tQ : tK, r, c);
 #pragma unroll
           for (int e = 0; e < 2; ++e) {
             const float d = acc[j][2 * hr + e];
+            const float w = lnb * d * (e ? o2.y : o2.x);
             if (which == 2) {
               dqa[j][2 * hr + e] += d;
-              pg[hr] = fmaf(lnb * d, tile_val(tQ, r, c + e), pg[hr]);
+              pg[hr] += w;
             } else {
               dka[j][2 * hr + e] += d;
-              const float w = lnb * d * tile_val(tK, r, c + e);
               pg[hr] += (which == 0) ? w : -w;
             }
           }
