@@ -264,15 +264,15 @@ __global__ void __launch_bounds__(NTH, 1) tc_fwd_ws_kernel(SimtFwdArgs a, const 
     // P3: [X diag(b); X diag(b e^G)] [K | V] -> rows 64..127 of the K product = w, rows
     // 0..63 of the V product = u (K and V token-major, read as MN-major B)
     auto p3 = [&](int c) {
-      mma_ops_w(tmem + T_WW, kmaj(xx_at(c), 0), mnmaj(k_at(c), 8192), 64, idesc_bf16(128, 128, false, false, true),
+      mma_grp_w(tmem + T_WW, kmaj(xx_at(c), 0), mnmaj(k_at(c), 8192), 64, idesc_bf16(128, 128, false, false, true),
                 false);
-      mma_ops_w(tmem + T_U + 64 * (uint32_t)(c & 1), kmaj(xx_at(c), 0), mnmaj(v_at(c), 0), 64,
+      mma_grp_w(tmem + T_U + 64 * (uint32_t)(c & 1), kmaj(xx_at(c), 0), mnmaj(v_at(c), 0), 64,
                 idesc_bf16(128, 64, false, false, true), false);
       mma_commit_w(&st.p3);
     };
     // P1: S = Q K^T (A rows 64..127: the next 64 rows of shared memory, unread output rows)
     auto p1 = [&](int c) {
-      mma_ops_w(tmem + T_S, kmaj(wq_at(c) + 8192, 16384), kmaj(k_at(c), 8192), 128, idesc_bf16(128, 64), false);
+      mma_grp_w(tmem + T_S, kmaj(wq_at(c) + 8192, 16384), kmaj(k_at(c), 8192), 128, idesc_bf16(128, 64), false);
       mma_commit_w(&st.p1);
     };
     do {
@@ -287,7 +287,7 @@ __global__ void __launch_bounds__(NTH, 1) tc_fwd_ws_kernel(SimtFwdArgs a, const 
         const int par = c & 1;
         // P4(c): h(c), w(c) written, Q h of c-1 read; Q(c) landed (waited for P1(c))
         if (!wt(&st.rdy4, c)) break;
-        mma_ops_w(tmem + T_D4, kmaj(wq_at(c), 16384), mnmaj(sb + OFF_HT, 0), 128,
+        mma_grp_w(tmem + T_D4, kmaj(wq_at(c), 16384), mnmaj(sb + OFF_HT, 0), 128,
                   idesc_bf16(128, 64, false, false, true), false);
         mma_commit_w(&st.p4);
         // loads of chunk c+2: its X / V buffers held chunk c (P3(c) came before P5(c-1), done
@@ -301,12 +301,12 @@ __global__ void __launch_bounds__(NTH, 1) tc_fwd_ws_kernel(SimtFwdArgs a, const 
         }
         // P5(c): K^T (e^(Gl-G) v_new), K read as MN-major A
         if (!wt(&st.vn, c)) break;
-        mma_ops_w(tmem + T_P5, mnmaj(k_at(c), 8192), mnmaj(sb + OFF_VNL, 0), 64, idesc_bf16(128, 64, false, true, true),
+        mma_grp_w(tmem + T_P5, mnmaj(k_at(c), 8192), mnmaj(sb + OFF_VNL, 0), 64, idesc_bf16(128, 64, false, true, true),
                   false);
         mma_commit_w(&st.p5);
         // PO(c): A_qk(c) written; the output of c-1 has read its accumulator
         if (!wt(&st.rdyo, c)) break;
-        mma_ops_w(tmem + T_PO, kmaj(sb + OFF_AQ + par * 8192 - 8192, 0), mnmaj(sb + OFF_VN, 0), 64,
+        mma_grp_w(tmem + T_PO, kmaj(sb + OFF_AQ + par * 8192 - 8192, 0), mnmaj(sb + OFF_VN, 0), 64,
                   idesc_bf16(128, 64, false, false, true), false);
         mma_commit_w(&st.po);
         // P1(c+1): Q(c+1) landed; A_qk(c) has left tensor memory

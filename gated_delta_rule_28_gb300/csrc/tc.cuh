@@ -173,6 +173,50 @@ __device__ __forceinline__ void mma_ops_w(uint32_t d_tmem, Opnd A, Opnd B, int K
     mma_bf16_w(d_tmem, a0 + (ao >> 4), b0 + (bo >> 4), idesc, (accumulate || ks > 0) ? 1u : 0u);
   }
 }
+// Four MMAs of one K=64 block in one asm statement, one elect. The operand descriptors
+// are formed inside from their low words (start address >> 4 and the leading byte
+// offset, sdesc_sw128 / sdesc_sw128_mn) and the common high word (1 KB stride between
+// 8-row atoms, version, 128-byte swizzle); A advances by AO, B by BO (16-byte units) per
+// 16-element K step (K-major: 2, MN-major: 128).
+constexpr uint32_t SDESC_HI = (1024u >> 4) | (1u << 14) | (2u << 29);
+template <int AO, int BO>
+__device__ __forceinline__ void mma4_w(uint32_t d_tmem, uint32_t alo, uint32_t blo, uint32_t idesc,
+                                       uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p, q, e;\n .reg .b32 x, y;\n .reg .b64 a, b;\n"
+      " setp.ne.b32 p, %4, 0;\n setp.eq.u32 q, 0, 0;\n elect.sync _|e, 0xffffffff;\n"
+      " mov.b64 a, {%1, %11};\n mov.b64 b, {%2, %11};\n"
+      " @e tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, p;\n"
+      " add.u32 x, %1, %5;\n add.u32 y, %2, %8;\n mov.b64 a, {x, %11};\n mov.b64 b, {y, %11};\n"
+      " @e tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, q;\n"
+      " add.u32 x, %1, %6;\n add.u32 y, %2, %9;\n mov.b64 a, {x, %11};\n mov.b64 b, {y, %11};\n"
+      " @e tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, q;\n"
+      " add.u32 x, %1, %7;\n add.u32 y, %2, %10;\n mov.b64 a, {x, %11};\n mov.b64 b, {y, %11};\n"
+      " @e tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, q;\n}\n" ::"r"(d_tmem),
+      "r"(alo), "r"(blo), "r"(idesc), "r"(accumulate), "n"(AO), "n"(2 * AO), "n"(3 * AO), "n"(BO), "n"(2 * BO),
+      "n"(3 * BO), "n"(SDESC_HI)
+      : "memory");
+}
+// low descriptor word of an operand (sdesc_sw128 / sdesc_sw128_mn)
+__device__ __forceinline__ uint32_t sdesc_lo(Opnd X) {
+  return ((X.addr & 0x3FFFFu) >> 4) | ((X.mn ? ((X.step >> 4) & 0x3FFFu) : 1u) << 16);
+}
+// D (+)= A B^T over K (a multiple of 64) in groups of four MMAs; operands as mma_ops_w
+__device__ __forceinline__ void mma_grp_w(uint32_t d_tmem, Opnd A, Opnd B, int K, uint32_t idesc, bool accumulate) {
+  const uint32_t a0 = sdesc_lo(A), b0 = sdesc_lo(B);
+#pragma unroll
+  for (int g = 0; g < K / 64; ++g) {
+    // K block g: K-major operands move to the next 64-wide block (`step` bytes), MN-major
+    // ones by 4 x 2048 bytes
+    const uint32_t ag = a0 + ((A.mn ? (uint32_t)g * 8192u : (uint32_t)g * A.step) >> 4);
+    const uint32_t bg = b0 + ((B.mn ? (uint32_t)g * 8192u : (uint32_t)g * B.step) >> 4);
+    const uint32_t acc = (accumulate || g > 0) ? 1u : 0u;
+    if (A.mn && B.mn) mma4_w<128, 128>(d_tmem, ag, bg, idesc, acc);
+    else if (A.mn) mma4_w<128, 2>(d_tmem, ag, bg, idesc, acc);
+    else if (B.mn) mma4_w<2, 128>(d_tmem, ag, bg, idesc, acc);
+    else mma4_w<2, 2>(d_tmem, ag, bg, idesc, acc);
+  }
+}
 // both operands K-major: consecutive 64-wide K-blocks a_kb / b_kb bytes apart; warp-collective
 __device__ __forceinline__ void mma_tiles_w(uint32_t d_tmem, uint32_t a_saddr, uint32_t a_kb, uint32_t b_saddr,
                                             uint32_t b_kb, int K, uint32_t idesc, bool accumulate) {
