@@ -162,8 +162,9 @@ __device__ __forceinline__ void mma_commit_w(uint64_t *bar) {
       : "memory");
 }
 // D[M x N] (+)= A[M x K] B[N x K]^T for K a multiple of 16, either operand K- or MN-major
-// (the instruction descriptor must say which, idesc_bf16's a_mn / b_mn); warp-collective
-__device__ __forceinline__ void mma_ops_w(uint32_t d_tmem, Opnd A, Opnd B, int K, uint32_t idesc, bool accumulate) {
+// (the instruction descriptor must say which, idesc_bf16's a_mn / b_mn); warp-collective;
+// one MMA per call (K a multiple of 64 goes through mma_grp_w, below)
+__device__ __forceinline__ void mma_ops1_w(uint32_t d_tmem, Opnd A, Opnd B, int K, uint32_t idesc, bool accumulate) {
   const uint64_t a0 = A.mn ? sdesc_sw128_mn(A.addr, A.step) : sdesc_sw128(A.addr);
   const uint64_t b0 = B.mn ? sdesc_sw128_mn(B.addr, B.step) : sdesc_sw128(B.addr);
 #pragma unroll
@@ -216,6 +217,12 @@ __device__ __forceinline__ void mma_grp_w(uint32_t d_tmem, Opnd A, Opnd B, int K
     else if (B.mn) mma4_w<2, 128>(d_tmem, ag, bg, idesc, acc);
     else mma4_w<2, 2>(d_tmem, ag, bg, idesc, acc);
   }
+}
+// D (+)= A B^T: groups of four MMAs when K is a multiple of 64 (smaller code), else one
+// MMA per K step
+__device__ __forceinline__ void mma_ops_w(uint32_t d_tmem, Opnd A, Opnd B, int K, uint32_t idesc, bool accumulate) {
+  if (K % 64 == 0) mma_grp_w(d_tmem, A, B, K, idesc, accumulate);
+  else mma_ops1_w(d_tmem, A, B, K, idesc, accumulate);
 }
 // both operands K-major: consecutive 64-wide K-blocks a_kb / b_kb bytes apart; warp-collective
 __device__ __forceinline__ void mma_tiles_w(uint32_t d_tmem, uint32_t a_saddr, uint32_t a_kb, uint32_t b_saddr,
