@@ -11,7 +11,10 @@ Contents
 ``chunk_form``  fp64 numpy statement of the 64-token chunk algorithm that
                 defines the intermediate outputs (cumulative gate, A, w, u,
                 v_new, per-chunk entry states) and its reverse mode.
+``frame_scan``  fp64 numpy statement of the dense per-token transition scan (right-
+                multiply KV and left-multiply Z states, truncation, the
+                segment-split correction).
 ``brute``       exact rational (``fractions.Fraction``) unrolled-product form
                 of the recurrence for tiny inputs; the pin for ``recurrence``.
 """
-from . import brute, chunk_form, recurrence  # noqa: F401
+from . import brute, chunk_form, frame_scan, recurrence  # noqa: F401
