@@ -297,16 +297,18 @@ def _time_ms(fn, reps, warmup, stream):
     return a.elapsed_time(b) / reps
 
 
-ROWS = ("packed_fwd", "kda_split_fwd", "train_fwd_bwd")
+ROWS = ("packed_fwd", "kda_split_fwd", "train_fwd_bwd", "frame_scan")
 
 
-def secondary_rows(dev, hbm_peak, only=None, reps=None, kda_tokens=65536, train_tokens=8192):
+def secondary_rows(dev, hbm_peak, only=None, reps=None, kda_tokens=65536, train_tokens=8192,
+                   frame_positions=4096):
     """The other scope rows, each on its own workload at full size (device-generated
     seeded inputs with the workloads' distributions; timing only, parity is in tests).
     ``only`` restricts the run to one row; ``reps`` overrides the timed repetitions
     (a profiler capture wants few); ``kda_tokens`` shrinks the per-key workload for a
     profiler capture (same distributions and segment length), ``train_tokens`` the training
-    workload's tokens per batch row."""
+    workload's tokens per batch row, ``frame_positions`` the transition scan's positions per
+    sequence."""
     import torch
     from gated_delta_rule_28_gb300 import api, binding as Bd
     g = torch.Generator(device=dev)
@@ -367,6 +369,33 @@ def secondary_rows(dev, hbm_peak, only=None, reps=None, kda_tokens=65536, train_
                                                                    h0=h0, stream=stream.cuda_stream), R(2), 1, stream)
             out["train_fwd_bwd"] = {"workload": "gdn_train_bf16", "ms_fwd": ms_f, "ms_bwd": ms_b,
                                     "tokens_per_s": 8 * TT / (ms_f + ms_b) * 1e3, "tokens": TT}
+            del q, k, v, gg, beta, h0, dO, f
+        if want("frame_scan"):  # dense per-token transition scan: 16 sequences x 4096 positions, D = 64
+            BH, TF, D = 16, frame_positions, 64
+            eye = torch.eye(D, device=dev)
+
+            def trans():
+                return 0.9 * eye + (0.05 / D ** 0.5) * torch.randn((BH, TF, D, D), device=dev, generator=g)
+
+            W_kv = trans()
+            U_kv = torch.randn((BH, TF, D, D), device=dev, generator=g) / D ** 0.5
+            W_z = trans()
+            u_z = torch.randn((BH, TF, D), device=dev, generator=g) / D ** 0.5
+            S0 = torch.randn((BH, D, D), device=dev, generator=g)
+            s0 = torch.randn((BH, D), device=dev, generator=g)
+            # algorithmic bytes: W_kv, U_kv, W_z, u_z in and every position's two states out
+            fbytes = BH * TF * (4 * D * D + 2 * D) * 4
+            sweep = {}
+            for seg in (128, 256, 512, 0):
+                sweep[seg] = _time_ms(lambda: api.frame_scan(W_kv, U_kv, W_z, u_z, S0_kv=S0, s0_z=s0,
+                                                             segment_len=seg, stream=stream.cuda_stream),
+                                      R(3), 1, stream)
+            ms = sweep[256]
+            out["frame_scan"] = {"workload": "frame_scan_f32", "BH": BH, "T": TF, "D": D, "segment_len": 256,
+                                 "ms": ms, "positions_per_s": BH * TF / ms * 1e3,
+                                 "hbm_frac": fbytes / (ms * 1e-3) / 1e9 / hbm_peak,
+                                 "ms_by_segment_len": {str(k2): v2 for k2, v2 in sweep.items()}}
+            del W_kv, U_kv, W_z, u_z
     Bd.gdn_device_status(stream.cuda_stream)
     return out
 
@@ -541,6 +570,8 @@ def main():
     ap.add_argument("--reps", type=int, default=None, help="timed repetitions of --row")
     ap.add_argument("--kda-tokens", type=int, default=65536, help="tokens of the per-key row (profiling)")
     ap.add_argument("--train-tokens", type=int, default=8192, help="tokens per batch row of the training row")
+    ap.add_argument("--frame-positions", type=int, default=4096,
+                    help="positions per sequence of the transition-scan row (profiling)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -553,7 +584,8 @@ def main():
         torch.cuda.set_device(0)
         hbm, _, _ = _peaks()
         print(json.dumps(secondary_rows(torch.device("cuda", 0), hbm, only=args.row, reps=args.reps,
-                                        kda_tokens=args.kda_tokens, train_tokens=args.train_tokens)),
+                                        kda_tokens=args.kda_tokens, train_tokens=args.train_tokens,
+                                        frame_positions=args.frame_positions)),
               flush=True)
         return 0
     return run_ours(args)

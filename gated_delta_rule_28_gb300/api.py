@@ -243,3 +243,22 @@ def split_backward(q, k, v, g_cumsum, beta, A, dO, segment_len, S_init, M, *, dh
                                      stream=stream, **maps)
     out.update(dh0=dh0, dS_ext=dS_ext, dS_exit=dS_exit)
     return out
+
+
+def frame_scan(W_kv, U_kv, W_z, u_z, *, S0_kv=None, s0_z=None, active=0, segment_len=0, stream=None):
+    """Dense per-token transition scan (SANA's cp_frame_gdn_scan and its local scan) through
+    ``frame_scan_fwd``: S_kv[t] = S_kv[t-1] @ W_kv[t] + U_kv[t], s_z[t] = W_z[t] @ s_z[t-1] + u_z[t],
+    fp32 [BH, T, D, D] / [BH, T, D] on the device; ``active`` is truncate_to_active (0: off);
+    ``segment_len`` > 0 splits each sequence over the SMs. Returns (S_kv_all, s_z_all,
+    S_kv_last, s_z_last)."""
+    BH, T, D, _ = W_kv.shape
+    p = B.make_frame_problem(BH, T, D, active=active, segment_len=segment_len)
+    S_all = torch.empty_like(U_kv)
+    z_all = torch.empty_like(u_z)
+    S_last = torch.empty((BH, D, D), device=W_kv.device, dtype=torch.float32)
+    z_last = torch.empty((BH, D), device=W_kv.device, dtype=torch.float32)
+    nbytes = B.frame_scan_workspace(p)
+    ws = torch.empty(max(nbytes, 16), device=W_kv.device, dtype=torch.uint8) if nbytes else None
+    B.frame_scan_fwd(p, W_kv, U_kv, W_z, u_z, S0_kv, s0_z, S_all, z_all, S_last, z_last,
+                     ws, nbytes, stream)
+    return S_all, z_all, S_last, z_last

@@ -33,7 +33,7 @@ EXPORTS = ("gdn_last_error", "gdn_device_status", "gdn_prepare_varlen", "gdn_chu
            "gdn_chunk_fwd", "gdn_chunk_bwd_workspace", "gdn_chunk_bwd", "gdn_chunk_bwd_noalloc",
            "kda_segment_summary_workspace", "kda_segment_summary", "kda_segment_merge",
            "kda_segment_summary_bwd_workspace", "kda_segment_summary_bwd", "kda_segment_merge_bwd",
-           "gdn_selftest_wait_timeout")
+           "gdn_selftest_wait_timeout", "frame_scan_workspace", "frame_scan_fwd")
 # bytes of the library's built-in scratch array used by gdn_chunk_bwd_noalloc
 GDN_NOALLOC_SCRATCH_BYTES = 64 * 1024 * 1024
 
@@ -55,6 +55,11 @@ class gdn_problem(ctypes.Structure):  # noqa: N801  (C name)
         ("chunk_indices", ctypes.c_void_p), ("num_chunks", ctypes.c_int32),
         ("segment_len", ctypes.c_int32), ("use_beta_sigmoid", ctypes.c_int32),
     ]
+
+
+class frame_scan_problem(ctypes.Structure):  # noqa: N801  (C name)
+    _fields_ = [("BH", ctypes.c_int32), ("T", ctypes.c_int32), ("D", ctypes.c_int32),
+                ("active", ctypes.c_int32), ("segment_len", ctypes.c_int32)]
 
 
 _lock = threading.Lock()
@@ -94,6 +99,9 @@ def load():
             lib.kda_segment_summary_bwd_workspace.argtypes = [P, ctypes.c_int32, ctypes.POINTER(sz)]
             lib.kda_segment_summary_bwd.argtypes = [P] + [vp] * 6 + [ctypes.c_int32, vp, vp, sz, vp]
             lib.kda_segment_merge_bwd.argtypes = [P, vp, vp, ctypes.c_int32, vp, vp, vp, vp]
+            FP = ctypes.POINTER(frame_scan_problem)
+            lib.frame_scan_workspace.argtypes = [FP, ctypes.POINTER(sz)]
+            lib.frame_scan_fwd.argtypes = [FP] + [vp] * 10 + [vp, sz, vp]
             for name in EXPORTS[1:]:
                 getattr(lib, name).restype = ctypes.c_int
             _lib = lib
@@ -244,3 +252,21 @@ def kda_segment_merge_bwd(p: gdn_problem, dS_ext, M, nseg, dht, dS_exit, dh0=Non
 def kda_segment_merge(p: gdn_problem, S_ext, M, nseg, h0, S_init, ht=None, stream=None):
     _check(load().kda_segment_merge(ctypes.byref(p), _ptr(S_ext), _ptr(M), int(nseg), _ptr(h0),
                                     _ptr(S_init), _ptr(ht), _stream(stream)))
+
+
+def make_frame_problem(BH, T, D, *, active=0, segment_len=0) -> frame_scan_problem:
+    return frame_scan_problem(int(BH), int(T), int(D), int(active), int(segment_len))
+
+
+def frame_scan_workspace(p: frame_scan_problem) -> int:
+    n = ctypes.c_size_t(0)
+    _check(load().frame_scan_workspace(ctypes.byref(p), ctypes.byref(n)))
+    return n.value
+
+
+def frame_scan_fwd(p: frame_scan_problem, W_kv, U_kv, W_z, u_z, S0_kv, s0_z, S_kv_all, s_z_all,
+                   S_kv_last=None, s_z_last=None, ws=None, ws_bytes=0, stream=None):
+    _check(load().frame_scan_fwd(ctypes.byref(p), _ptr(W_kv), _ptr(U_kv), _ptr(W_z), _ptr(u_z),
+                                 _ptr(S0_kv), _ptr(s0_z), _ptr(S_kv_all), _ptr(s_z_all),
+                                 _ptr(S_kv_last), _ptr(s_z_last), _ptr(ws), int(ws_bytes),
+                                 _stream(stream)))

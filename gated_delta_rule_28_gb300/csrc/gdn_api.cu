@@ -865,6 +865,94 @@ gdn_status kda_segment_merge(const gdn_problem *p, const float *S_ext, const flo
   return ok();
 }
 
+namespace {
+gdn_status check_frame(const frame_scan_problem *p, int *nseg) {
+  if (!p) return fail(GDN_ERR_INVALID_ARGUMENT, "problem is NULL");
+  if (p->BH < 1 || p->T < 1)
+    return fail(GDN_ERR_INVALID_ARGUMENT, "need BH >= 1 and T >= 1 (got BH=%d T=%d)", p->BH, p->T);
+  if (p->D != 32 && p->D != 64) return fail(GDN_ERR_UNSUPPORTED, "D must be 32 or 64, got %d", p->D);
+  if (p->active < 0 || p->active > p->T)
+    return fail(GDN_ERR_INVALID_ARGUMENT, "active must be 0 or in [1, T=%d], got %d", p->T, p->active);
+  if (p->segment_len < 0)
+    return fail(GDN_ERR_INVALID_ARGUMENT, "segment_len must be >= 0, got %d", p->segment_len);
+  if ((int64_t)p->BH * p->T * p->D * p->D >= (int64_t)1 << 40)
+    return fail(GDN_ERR_INVALID_ARGUMENT, "problem too large");
+  *nseg = p->segment_len > 0 ? (int)(((int64_t)p->T + p->segment_len - 1) / p->segment_len) : 1;
+  if ((int64_t)*nseg > 65535) return fail(GDN_ERR_INVALID_ARGUMENT, "more than 65535 segments");
+  return GDN_OK;
+}
+size_t frame_ws_bytes(const frame_scan_problem *p, int nseg) {
+  if (nseg <= 1) return 0;
+  return (size_t)p->BH * nseg * (4 * (size_t)p->D * p->D + 2 * (size_t)p->D) * sizeof(float);
+}
+}  // namespace
+
+gdn_status frame_scan_workspace(const frame_scan_problem *p, size_t *bytes) {
+  int nseg = 1;
+  gdn_status st = check_frame(p, &nseg);
+  if (st != GDN_OK) return st;
+  if (!bytes) return fail(GDN_ERR_INVALID_ARGUMENT, "bytes must not be NULL");
+  *bytes = frame_ws_bytes(p, nseg);
+  return ok();
+}
+
+gdn_status frame_scan_fwd(const frame_scan_problem *p, const float *W_kv, const float *U_kv,
+                          const float *W_z, const float *u_z, const float *S0_kv,
+                          const float *s0_z, float *S_kv_all, float *s_z_all, float *S_kv_last,
+                          float *s_z_last, void *ws, size_t ws_bytes, void *stream) {
+  int nseg = 1;
+  gdn_status st = check_frame(p, &nseg);
+  if (st != GDN_OK) return st;
+  REQUIRE_PTR(W_kv, "W_kv");
+  REQUIRE_PTR(U_kv, "U_kv");
+  REQUIRE_PTR(W_z, "W_z");
+  REQUIRE_PTR(u_z, "u_z");
+  REQUIRE_PTR(S_kv_all, "S_kv_all");
+  REQUIRE_PTR(s_z_all, "s_z_all");
+  OPTIONAL_PTR(S0_kv, "S0_kv");
+  OPTIONAL_PTR(s0_z, "s0_z");
+  OPTIONAL_PTR(S_kv_last, "S_kv_last");
+  OPTIONAL_PTR(s_z_last, "s_z_last");
+  const size_t need = frame_ws_bytes(p, nseg);
+  if (need > 0 && (!ws || ws_bytes < need))
+    return fail(GDN_ERR_WORKSPACE, "frame scan workspace needs %zu bytes, got %zu", need, ws_bytes);
+  if (need > 0) OPTIONAL_PTR(ws, "workspace");
+  int dev;
+  if ((st = check_device(&dev)) != GDN_OK) return st;
+  gdn::FrameScanArgs a;
+  memset(&a, 0, sizeof(a));
+  a.W_kv = W_kv;
+  a.U_kv = U_kv;
+  a.W_z = W_z;
+  a.u_z = u_z;
+  a.S0 = S0_kv;
+  a.z0 = s0_z;
+  a.S_all = S_kv_all;
+  a.z_all = s_z_all;
+  a.S_last = S_kv_last;
+  a.z_last = s_z_last;
+  a.BH = p->BH;
+  a.D = p->D;
+  a.active = p->active;
+  a.nseg = nseg;
+  a.T = p->T;
+  a.seg_len = nseg > 1 ? p->segment_len : p->T;
+  a.dev_flag = device_flag_ptr();
+  if (nseg > 1) {
+    float *w = static_cast<float *>(ws);
+    const size_t DD = (size_t)p->BH * nseg * p->D * p->D, Dn = (size_t)p->BH * nseg * p->D;
+    a.h_kv = w;
+    a.M_kv = w + DD;
+    a.M_z = w + 2 * DD;
+    a.S_init = w + 3 * DD;
+    a.h_z = w + 4 * DD;
+    a.z_init = w + 4 * DD + Dn;
+  }
+  cudaError_t e = gdn::launch_frame_scan(a, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "frame scan launch");
+  return ok();
+}
+
 }  // extern "C"
 
 namespace gdn {

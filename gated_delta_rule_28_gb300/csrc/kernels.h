@@ -107,6 +107,21 @@ struct MergeArgs {
 };
 cudaError_t launch_merge(const MergeArgs &a, cudaStream_t st);
 
+// Dense per-token transition scan (frame_scan.cu). Inputs [BH, T, D, D] (u_z [BH, T, D]);
+// nseg = 1: one pass per sequence from S0 / z0; nseg > 1: summary, merge and seeded scan
+// over segments of seg_len positions, with h_kv, M_kv, M_z, S_init [BH, nseg, D, D] and
+// h_z, z_init [BH, nseg, D] in the workspace.
+struct FrameScanArgs {
+  const float *W_kv, *U_kv, *W_z, *u_z;
+  const float *S0, *z0;                 // nullable initial states
+  float *S_all, *z_all, *S_last, *z_last;
+  float *h_kv, *M_kv, *h_z, *M_z, *S_init, *z_init;
+  int BH, D, active, nseg;
+  int64_t T, seg_len;
+  int *dev_flag;
+};
+cudaError_t launch_frame_scan(const FrameScanArgs &a, cudaStream_t st);
+
 // Backward: reverse state recurrence (dhu) and local gradients.
 struct BwdArgs {
   const void *q, *k, *v, *beta, *dO;

@@ -19,6 +19,13 @@ workload number - 1; draws in the fixed order q, k, v, beta, g, h0, dO):
                         dO ~ N(0, 1).
 Shared: q, k ~ N(0,1) normalised per token; v ~ N(0,1); beta = sigmoid(N(0,1)).
 Sizes (and the gate scale) can be overridden for smaller or harder parity cases.
+
+``frame_scan_f32`` (``make_frame``): the dense per-token transition scan of SANA's
+distributed_scan page, fp32, BH = 16 sequences of T = 4096 positions, D = 64. The page fixes
+no sizes and no value law; the recipe is contracting transitions W = 0.9 I + 0.05 N(0,1)/sqrt(D)
+(spectral norm about 1, so the states stay bounded over thousands of positions) for both
+states, inputs U_kv, u_z ~ N(0, 1/D), initial states ~ N(0, 1); seed 5, draws in the order
+W_kv, U_kv, W_z, u_z, S0_kv, s0_z.
 """
 from __future__ import annotations
 
@@ -138,3 +145,41 @@ def make(config: int, *, B=None, T=None, H=None, seed=None, K=128, V=128, dtype=
     return Inputs(name=NAMES[config], layout=d["layout"], dtype=dtype, per_key=d["per_key"],
                   use_exp2=d["use_exp2"], q=q, k=k, v=v, g=g, beta=beta, h0=h0, dO=dO, cu=cu,
                   seg_len=d.get("seg_len", 0), meta=dict(config=config, seed=seed))
+
+
+FRAME_DEFAULTS = dict(BH=16, T=4096, D=64, seed=5)
+
+
+@dataclass
+class FrameInputs:
+    """Inputs of the dense per-token transition scan, float32."""
+    W_kv: np.ndarray  # [BH, T, D, D]
+    U_kv: np.ndarray  # [BH, T, D, D]
+    W_z: np.ndarray   # [BH, T, D, D]
+    u_z: np.ndarray   # [BH, T, D]
+    S0_kv: np.ndarray  # [BH, D, D]
+    s0_z: np.ndarray   # [BH, D]
+
+
+def make_frame(*, BH=None, T=None, D=None, seed=None) -> FrameInputs:
+    d = dict(FRAME_DEFAULTS)
+    for k, v in (("BH", BH), ("T", T), ("D", D), ("seed", seed)):
+        if v is not None:
+            d[k] = v
+    BH, T, D = d["BH"], d["T"], d["D"]
+    rng = np.random.default_rng(d["seed"])
+    eye = np.eye(D, dtype=np.float32)
+
+    def trans():
+        w = rng.standard_normal((BH, T, D, D), dtype=np.float32)
+        w *= np.float32(0.05 / np.sqrt(D))
+        w += np.float32(0.9) * eye
+        return w
+
+    W_kv = trans()
+    U_kv = rng.standard_normal((BH, T, D, D), dtype=np.float32) * np.float32(1.0 / np.sqrt(D))
+    W_z = trans()
+    u_z = rng.standard_normal((BH, T, D), dtype=np.float32) * np.float32(1.0 / np.sqrt(D))
+    S0 = rng.standard_normal((BH, D, D), dtype=np.float32)
+    s0 = rng.standard_normal((BH, D), dtype=np.float32)
+    return FrameInputs(W_kv, U_kv, W_z, u_z, S0, s0)

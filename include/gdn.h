@@ -291,6 +291,56 @@ gdn_status kda_segment_merge(const gdn_problem *p, const float *S_ext, const flo
                              int32_t nseg, const float *h0, float *S_init, float *ht,
                              void *stream);
 
+/* ---------------------------------------------------------------------------
+ * Dense per-token transition scan (SANA, distributed_scan.py page:
+ * cp_frame_gdn_scan and its local scan). For each of BH independent sequences of
+ * T positions, with D x D transitions, in fp32:
+ *   KV state, right multiply:  S_kv[t] = S_kv[t-1] W_kv[t] + U_kv[t]
+ *   Z state, left multiply:    s_z[t]  = W_z[t] s_z[t-1] + u_z[t]
+ * from S_kv[-1] = S0_kv (or 0) and s_z[-1] = s0_z (or 0). With active > 0 (the
+ * page's truncate_to_active), positions t >= active leave both states unchanged
+ * (the page sets W = I and U = 0 there): their outputs repeat the state of
+ * position active-1, which is also the terminal state.
+ * With segment_len > 0 a sequence runs as ceil(T / segment_len) segments on
+ * different SMs: each segment's final state from zero and transition product
+ * (M_kv = W_kv[a] ... W_kv[b-1], M_z = W_z[b-1] ... W_z[a]), their ordered
+ * composition into every segment's entry state (S_init_{j+1} = S_init_j M_kv_j
+ * + h_kv_j, s_init_{j+1} = M_z_j s_init_j + h_z_j, the page's exclusive prefix
+ * composition), then every segment from its entry state: the page's context-
+ * parallel scan, with its ranks as the SMs of one GPU.
+ *   BH, T, D     : sequences, positions, state width (D = 32 or 64).
+ *   active       : 0 (every position) or 1 <= active <= T.
+ *   segment_len  : 0 (one pass per sequence) or >= 1.                         */
+typedef struct frame_scan_problem {
+    int32_t BH;
+    int32_t T;
+    int32_t D;
+    int32_t active;
+    int32_t segment_len;
+} frame_scan_problem;
+
+/* Workspace bytes of frame_scan_fwd: 0 for one pass, else
+ * BH * nseg * (4 D^2 + 2 D) * 4 (the segments' summaries and entry states). */
+gdn_status frame_scan_workspace(const frame_scan_problem *p, size_t *bytes);
+
+/*   W_kv, U_kv, W_z : device fp32 [BH, T, D, D], row-major D x D per position.
+ *   u_z             : device fp32 [BH, T, D].
+ *   S0_kv, s0_z     : nullable device fp32 [BH, D, D], [BH, D] initial states.
+ *   S_kv_all, s_z_all : device fp32 [BH, T, D, D], [BH, T, D]: every position's
+ *                   state (outputs).
+ *   S_kv_last, s_z_last : nullable device fp32 [BH, D, D], [BH, D]: the
+ *                   terminal states (position active-1, or T-1).
+ *   workspace       : device, frame_scan_workspace() bytes (may be NULL when 0).
+ * Errors: GDN_ERR_INVALID_ARGUMENT (shapes, null or unaligned pointers, active
+ * or segment_len out of range), GDN_ERR_UNSUPPORTED (D not 32 or 64),
+ * GDN_ERR_WORKSPACE, GDN_ERR_CUDA. A bounded wait that runs out raises the
+ * device flag (GDN_ERR_TIMEOUT from gdn_device_status). */
+gdn_status frame_scan_fwd(const frame_scan_problem *p, const float *W_kv, const float *U_kv,
+                          const float *W_z, const float *u_z, const float *S0_kv,
+                          const float *s0_z, float *S_kv_all, float *s_z_all, float *S_kv_last,
+                          float *s_z_last, void *workspace, size_t workspace_bytes,
+                          void *stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -131,3 +131,30 @@ def test_wait_selftest_rejects_a_budget_out_of_range(lib, polls):
     with pytest.raises(B.GdnError) as e:
         B.gdn_selftest_wait_timeout(polls, 0)
     assert e.value.status == B.GDN_ERR_INVALID_ARGUMENT
+
+
+def test_frame_scan_contract_checks(lib):
+    # validation runs before any device work: fake aligned addresses are never touched
+    fake = 4096
+    p = B.make_frame_problem(2, 64, 64, segment_len=8)
+    need = B.frame_scan_workspace(p)
+    assert need == 2 * 8 * (4 * 64 * 64 + 2 * 64) * 4
+    assert B.frame_scan_workspace(B.make_frame_problem(2, 64, 64)) == 0
+    assert B.frame_scan_workspace(B.make_frame_problem(2, 64, 32, segment_len=64)) == 0
+    cases = [
+        (B.make_frame_problem(1, 4, 48), [fake] * 4, B.GDN_ERR_UNSUPPORTED),
+        (B.make_frame_problem(1, 4, 64, active=5), [fake] * 4, B.GDN_ERR_INVALID_ARGUMENT),
+        (B.make_frame_problem(1, 4, 64, active=-1), [fake] * 4, B.GDN_ERR_INVALID_ARGUMENT),
+        (B.make_frame_problem(0, 4, 64), [fake] * 4, B.GDN_ERR_INVALID_ARGUMENT),
+        (B.make_frame_problem(1, 4, 64, segment_len=-2), [fake] * 4, B.GDN_ERR_INVALID_ARGUMENT),
+        (B.make_frame_problem(1, 4, 64), [fake, None, fake, fake], B.GDN_ERR_INVALID_ARGUMENT),
+        (B.make_frame_problem(1, 4, 64), [fake, fake + 4, fake, fake], B.GDN_ERR_INVALID_ARGUMENT),
+    ]
+    for prob, (w, u, wz, uz), status in cases:
+        with pytest.raises(B.GdnError) as e:
+            B.frame_scan_fwd(prob, w, u, wz, uz, None, None, fake, fake, stream=0)
+        assert e.value.status == status
+    with pytest.raises(B.GdnError) as e:
+        B.frame_scan_fwd(p, fake, fake, fake, fake, None, None, fake, fake, ws=fake, ws_bytes=need - 16,
+                         stream=0)
+    assert e.value.status == B.GDN_ERR_WORKSPACE
