@@ -390,8 +390,8 @@ def secondary_rows(dev, hbm_peak, only=None, reps=None, kda_tokens=65536, train_
                 sweep[seg] = _time_ms(lambda: api.frame_scan(W_kv, U_kv, W_z, u_z, S0_kv=S0, s0_z=s0,
                                                              segment_len=seg, stream=stream.cuda_stream),
                                       R(3), 1, stream)
-            ms = sweep[256]
-            out["frame_scan"] = {"workload": "frame_scan_f32", "BH": BH, "T": TF, "D": D, "segment_len": 256,
+            ms = sweep[0]
+            out["frame_scan"] = {"workload": "frame_scan_f32", "BH": BH, "T": TF, "D": D, "segment_len": 0,
                                  "ms": ms, "positions_per_s": BH * TF / ms * 1e3,
                                  "hbm_frac": fbytes / (ms * 1e-3) / 1e9 / hbm_peak,
                                  "ms_by_segment_len": {str(k2): v2 for k2, v2 in sweep.items()}}

@@ -320,6 +320,218 @@ __global__ void __launch_bounds__(FS_NTH, 1) frame_merge_kernel(FrameScanArgs a)
   }
 }
 
+// ---- one pass with the KV rows split over CTAs -----------------------------------------------
+// The rows of the KV state are independent (S[t][i, :] = S[t-1][i, :] W_kv[t] + U_kv[t][i, :]),
+// so R rows of one sequence (or segment) go to one CTA, and D / R such CTAs walk the same
+// positions, each reading the whole W_kv[t] (L2 serves the repeats). In a CTA of 256 threads,
+// KQ = 256 / D groups split the contraction over k (thread = one column of one group, its R
+// rows in registers); the groups' partial sums meet in shared memory, where all threads add
+// them, two outputs each. The Z state takes a CTA of its own.
+template <int D, int R, int STAGES>
+__device__ __forceinline__ void frame_kv_rows(const FrameScanArgs &a) {
+  constexpr int STG = D * D + R * D;  // floats of one stage: W_kv[t], U_kv[t] rows r0 .. r0+R-1
+  constexpr int KQ = FS_NTH / D, KL = D / KQ;  // contraction groups, k per group
+  constexpr int OPT = R * D / FS_NTH;          // outputs per thread in the sum
+  static_assert(OPT >= 1 && OPT * FS_NTH == R * D, "whole outputs per thread");
+  extern __shared__ __align__(16) float smf[];
+  float *pos = smf;
+  float *St = pos + STAGES * STG;  // 2 x [D][R]: St[k][r] = S[r0 + r][k]
+  float *Part = St + 2 * D * R;    // [KQ][R][D] partial sums
+  uint64_t *bar = reinterpret_cast<uint64_t *>(Part + KQ * R * D);
+  const int tid = threadIdx.x, warp = tid >> 5;
+  const int j = tid % D, kq = tid / D;
+  const int r0 = blockIdx.x * R, seg = blockIdx.y, bh = blockIdx.z;
+  const int64_t T = a.T;
+  const int64_t t0 = (int64_t)seg * a.seg_len, t1 = min(t0 + a.seg_len, T);
+  const int64_t tact = a.active > 0 ? min(t1, (int64_t)a.active) : t1;
+  const int64_t slot = (int64_t)bh * a.nseg + seg;
+  if (tid == 0) {
+    for (int s = 0; s < STAGES; ++s) mbar_init(&bar[s], 1);
+    mbar_fence_init();
+  }
+  const float *S_in = a.S_init ? a.S_init + slot * D * D : a.S0 ? a.S0 + (int64_t)bh * D * D : nullptr;
+  for (int e = tid; e < R * D; e += FS_NTH) {
+    const int r = e / D, c = e % D;
+    St[c * R + r] = S_in ? S_in[(r0 + r) * D + c] : 0.f;
+  }
+  __syncthreads();
+  const float *gW = a.W_kv + (int64_t)bh * T * D * D, *gU = a.U_kv + (int64_t)bh * T * D * D;
+  int64_t last_issued = -1;
+  auto issue = [&](int64_t t) {  // warp 0
+    const int s = (int)((t - t0) % STAGES);
+    float *dst = pos + s * STG;
+    mbar_expect_tx_w(&bar[s], STG * 4);
+    bulk_load_w(smem_u32(dst), gW + t * D * D, D * D * 4, &bar[s]);
+    bulk_load_w(smem_u32(dst + D * D), gU + t * D * D + r0 * D, R * D * 4, &bar[s]);
+    last_issued = t;
+  };
+  if (warp == 0)
+    for (int s = 0; s < STAGES && t0 + s < tact; ++s) issue(t0 + s);
+  int cur = 0;
+  bool bad = false;
+  float *gS = a.S_all + (int64_t)bh * T * D * D;
+  for (int64_t t = t0; t < t1; ++t) {
+    float *Sn = St + (cur ^ 1) * D * R;
+    const float *Sc = St + cur * D * R;
+    if (t < tact) {
+      const int s = (int)((t - t0) % STAGES);
+      if (!mbar_wait(&bar[s], (uint32_t)(((t - t0) / STAGES) & 1), FS_WAIT_LIMIT)) bad = true;
+      const float *W = pos + s * STG, *U = W + D * D;
+      float acc[R];
+#pragma unroll
+      for (int r = 0; r < R; ++r) acc[r] = kq == 0 ? U[r * D + j] : 0.f;
+#pragma unroll
+      for (int kk = 0; kk < KL; ++kk) {
+        const int k = kq * KL + kk;
+        const float w = W[k * D + j];
+        float sk[R];
+#pragma unroll
+        for (int q = 0; q < R / 4; ++q) Vec<4>::ld(Sc + k * R + 4 * q, sk + 4 * q);
+#pragma unroll
+        for (int r = 0; r < R; ++r) acc[r] = fmaf(sk[r], w, acc[r]);
+      }
+#pragma unroll
+      for (int r = 0; r < R; ++r) Part[(kq * R + r) * D + j] = acc[r];
+      __syncthreads();
+#pragma unroll
+      for (int o = 0; o < OPT; ++o) {
+        const int e = tid + o * FS_NTH, r = e / D, c = e % D;
+        float v = 0.f;
+#pragma unroll
+        for (int g = 0; g < KQ; ++g) v += Part[(g * R + r) * D + c];
+        Sn[c * R + r] = v;
+        gS[t * D * D + (r0 + r) * D + c] = v;
+      }
+      cur ^= 1;
+    } else {
+#pragma unroll
+      for (int o = 0; o < OPT; ++o) {
+        const int e = tid + o * FS_NTH, r = e / D, c = e % D;
+        gS[t * D * D + (r0 + r) * D + c] = Sc[c * R + r];
+      }
+    }
+    if (__syncthreads_or(bad)) {
+      bad = true;
+      break;
+    }
+    if (warp == 0 && t + STAGES < tact) issue(t + STAGES);
+  }
+  if (bad) {
+    if (warp == 0 && last_issued >= 0)
+      for (int64_t t = max(t0, last_issued - STAGES + 1); t <= last_issued; ++t)
+        mbar_wait(&bar[(t - t0) % STAGES], (uint32_t)(((t - t0) / STAGES) & 1), FS_WAIT_LIMIT);
+    if (tid == 0) raise_device_flag(a.dev_flag, kDevTimeout);
+    return;
+  }
+  if (seg == a.nseg - 1 && a.S_last)
+    for (int e = tid; e < R * D; e += FS_NTH) {
+      const int r = e / D, c = e % D;
+      a.S_last[(int64_t)bh * D * D + (r0 + r) * D + c] = St[cur * D * R + c * R + r];
+    }
+}
+
+// The Z state of one sequence (or segment): s[t] = W_z[t] s[t-1] + u_z[t], 256 threads; in each
+// of D / 16 passes a warp takes two rows, 16 lanes per row, one float4 of the row per lane
+// (a warp reads 512 contiguous bytes: no bank conflict), and sums with shuffles.
+template <int D, int STAGES>
+__device__ __forceinline__ void frame_z(const FrameScanArgs &a) {
+  constexpr int STG = D * D + D;  // W_z[t], u_z[t]
+  constexpr int LPR = D / 4;      // lanes per row: one float4 each
+  constexpr int RPP = FS_NTH / LPR;  // rows per pass
+  extern __shared__ __align__(16) float smf[];
+  float *pos = smf;
+  float *zs = pos + STAGES * STG;  // 2 x [D]
+  uint64_t *bar = reinterpret_cast<uint64_t *>(zs + 2 * D);
+  const int tid = threadIdx.x, warp = tid >> 5;
+  const int seg = blockIdx.y, bh = blockIdx.z;
+  const int64_t T = a.T;
+  const int64_t t0 = (int64_t)seg * a.seg_len, t1 = min(t0 + a.seg_len, T);
+  const int64_t tact = a.active > 0 ? min(t1, (int64_t)a.active) : t1;
+  const int64_t slot = (int64_t)bh * a.nseg + seg;
+  if (tid == 0) {
+    for (int s = 0; s < STAGES; ++s) mbar_init(&bar[s], 1);
+    mbar_fence_init();
+  }
+  const float *z_in = a.z_init ? a.z_init + slot * D : a.z0 ? a.z0 + (int64_t)bh * D : nullptr;
+  if (tid < D) zs[tid] = z_in ? z_in[tid] : 0.f;
+  __syncthreads();
+  const float *gW = a.W_z + (int64_t)bh * T * D * D, *gu = a.u_z + (int64_t)bh * T * D;
+  int64_t last_issued = -1;
+  auto issue = [&](int64_t t) {
+    const int s = (int)((t - t0) % STAGES);
+    float *dst = pos + s * STG;
+    mbar_expect_tx_w(&bar[s], STG * 4);
+    bulk_load_w(smem_u32(dst), gW + t * D * D, D * D * 4, &bar[s]);
+    bulk_load_w(smem_u32(dst + D * D), gu + t * D, D * 4, &bar[s]);
+    last_issued = t;
+  };
+  if (warp == 0)
+    for (int s = 0; s < STAGES && t0 + s < tact; ++s) issue(t0 + s);
+  int cur = 0;
+  bool bad = false;
+  float *gz = a.z_all + (int64_t)bh * T * D;
+  const int lr = tid / LPR, q = tid % LPR;  // row within the pass, float4 index within the row
+  for (int64_t t = t0; t < t1; ++t) {
+    if (t < tact) {
+      const int s = (int)((t - t0) % STAGES);
+      if (!mbar_wait(&bar[s], (uint32_t)(((t - t0) / STAGES) & 1), FS_WAIT_LIMIT)) bad = true;
+      const float *W = pos + s * STG, *u = W + D * D;
+      float zq[4];
+      Vec<4>::ld(zs + cur * D + 4 * q, zq);
+#pragma unroll
+      for (int p = 0; p < D / RPP; ++p) {
+        const int row = p * RPP + lr;
+        float w[4];
+        Vec<4>::ld(W + row * D + 4 * q, w);
+        float sum = w[0] * zq[0];
+        sum = fmaf(w[1], zq[1], sum);
+        sum = fmaf(w[2], zq[2], sum);
+        sum = fmaf(w[3], zq[3], sum);
+#pragma unroll
+        for (int off = LPR / 2; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+        if (q == 0) zs[(cur ^ 1) * D + row] = sum + u[row];
+      }
+      cur ^= 1;
+    }
+    if (__syncthreads_or(bad)) {
+      bad = true;
+      break;
+    }
+    if (tid < D) gz[t * D + tid] = zs[cur * D + tid];
+    if (warp == 0 && t + STAGES < tact) issue(t + STAGES);
+  }
+  if (bad) {
+    if (warp == 0 && last_issued >= 0)
+      for (int64_t t = max(t0, last_issued - STAGES + 1); t <= last_issued; ++t)
+        mbar_wait(&bar[(t - t0) % STAGES], (uint32_t)(((t - t0) / STAGES) & 1), FS_WAIT_LIMIT);
+    if (tid == 0) raise_device_flag(a.dev_flag, kDevTimeout);
+    return;
+  }
+  if (seg == a.nseg - 1 && a.z_last && tid < D) a.z_last[(int64_t)bh * D + tid] = zs[cur * D + tid];
+}
+
+// One grid for both states: blocks 0 .. D/R-1 of every sequence (or segment) take KV rows,
+// block D/R its Z state, so that the two run side by side.
+template <int D, int R, int KS, int ZS>
+__global__ void __launch_bounds__(FS_NTH, 1) frame_rows_kernel(FrameScanArgs a) {
+  if (blockIdx.x < D / R) frame_kv_rows<D, R, KS>(a);
+  else frame_z<D, ZS>(a);
+}
+
+template <int D>
+cudaError_t launch_rows(const FrameScanArgs &a, cudaStream_t st) {
+  constexpr int R = 8, KS = 4, ZS = 4;
+  constexpr int ksmem = 4 * (KS * (D * D + R * D) + 2 * D * R + (FS_NTH / D) * R * D) + 8 * KS;
+  constexpr int zsmem = 4 * (ZS * (D * D + D) + 2 * D) + 8 * ZS;
+  constexpr int smem = ksmem > zsmem ? ksmem : zsmem;
+  static_assert(smem <= 232448, "shared memory");
+  auto kern = frame_rows_kernel<D, R, KS, ZS>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  kern<<<dim3(D / R + 1, a.nseg, a.BH), FS_NTH, smem, st>>>(a);
+  return cudaGetLastError();
+}
+
 template <int D, bool SUMMARY, int STAGES>
 cudaError_t launch_scan(const FrameScanArgs &a, dim3 grid, cudaStream_t st) {
   constexpr int smem = fs_smem_bytes<D, SUMMARY, STAGES>();
@@ -345,7 +557,7 @@ cudaError_t launch_all(const FrameScanArgs &a0, cudaStream_t st) {
     a.S_init = nullptr;
     a.z_init = nullptr;
   }
-  return launch_scan<D, false, 3>(a, dim3(a.nseg, a.BH), st);
+  return launch_rows<D>(a, st);
 }
 
 }  // namespace

@@ -868,8 +868,8 @@ gdn_status kda_segment_merge(const gdn_problem *p, const float *S_ext, const flo
 namespace {
 gdn_status check_frame(const frame_scan_problem *p, int *nseg) {
   if (!p) return fail(GDN_ERR_INVALID_ARGUMENT, "problem is NULL");
-  if (p->BH < 1 || p->T < 1)
-    return fail(GDN_ERR_INVALID_ARGUMENT, "need BH >= 1 and T >= 1 (got BH=%d T=%d)", p->BH, p->T);
+  if (p->BH < 1 || p->T < 1 || p->BH > 65535)
+    return fail(GDN_ERR_INVALID_ARGUMENT, "need 1 <= BH <= 65535 and T >= 1 (got BH=%d T=%d)", p->BH, p->T);
   if (p->D != 32 && p->D != 64) return fail(GDN_ERR_UNSUPPORTED, "D must be 32 or 64, got %d", p->D);
   if (p->active < 0 || p->active > p->T)
     return fail(GDN_ERR_INVALID_ARGUMENT, "active must be 0 or in [1, T=%d], got %d", p->T, p->active);

@@ -308,7 +308,8 @@ gdn_status kda_segment_merge(const gdn_problem *p, const float *S_ext, const flo
  * + h_kv_j, s_init_{j+1} = M_z_j s_init_j + h_z_j, the page's exclusive prefix
  * composition), then every segment from its entry state: the page's context-
  * parallel scan, with its ranks as the SMs of one GPU.
- *   BH, T, D     : sequences, positions, state width (D = 32 or 64).
+ *   BH, T, D     : sequences (at most 65535), positions, state width (D = 32
+ *                  or 64).
  *   active       : 0 (every position) or 1 <= active <= T.
  *   segment_len  : 0 (one pass per sequence) or >= 1.                         */
 typedef struct frame_scan_problem {
