@@ -297,7 +297,7 @@ def _time_ms(fn, reps, warmup, stream):
     return a.elapsed_time(b) / reps
 
 
-ROWS = ("packed_fwd", "kda_split_fwd", "train_fwd_bwd", "frame_scan")
+ROWS = ("packed_fwd", "kda_split_fwd", "train_fwd_bwd", "frame_scan", "aux_paths")
 
 
 def secondary_rows(dev, hbm_peak, only=None, reps=None, kda_tokens=65536, train_tokens=8192,
@@ -396,6 +396,37 @@ def secondary_rows(dev, hbm_peak, only=None, reps=None, kda_tokens=65536, train_
                                  "hbm_frac": fbytes / (ms * 1e-3) / 1e9 / hbm_peak,
                                  "ms_by_segment_len": {str(k2): v2 for k2, v2 in sweep.items()}}
             del W_kv, U_kv, W_z, u_z
+        if only == "aux_paths":  # the other kernels, for their profiles (not part of the default run)
+            aux = {}
+            # fp32 scalar gate: the FMA forward and backward kernels
+            q, k, v, gg, beta = common((2, 2048, 8, 128), (2, 2048, 8), 0.1)
+            q, k, v, beta = q.float(), k.float(), v.float(), beta.float()
+            dO = torch.randn((2, 2048, 8, 128), device=dev, generator=g)
+            f = api.chunk_gated_delta_rule_fwd(q, k, v, gg, beta, return_g_cumsum=True, return_A=True,
+                                               stream=stream.cuda_stream)
+            aux["f32_fwd_ms"] = _time_ms(lambda: api.chunk_gated_delta_rule_fwd(
+                q, k, v, gg, beta, stream=stream.cuda_stream), R(3), 1, stream)
+            aux["f32_bwd_ms"] = _time_ms(lambda: api.chunk_gated_delta_rule_bwd(
+                q, k, v, f["g_cumsum"], beta, f["A"], dO, stream=stream.cuda_stream), R(3), 1, stream)
+            # bf16 per-key gate backward (recompute on the per-key kernels, FMA reverse recurrence
+            # and local gradients)
+            q, k, v, gg, beta = common((1, 4096, 8, 128), (1, 4096, 8, 128), 0.05)
+            dO = torch.randn((1, 4096, 8, 128), device=dev, generator=g).to(torch.bfloat16)
+            f = api.chunk_gated_delta_rule_fwd(q, k, v, gg, beta, use_exp2=True, return_g_cumsum=True,
+                                               return_A=True, stream=stream.cuda_stream)
+            aux["kda_bwd_ms"] = _time_ms(lambda: api.chunk_gated_delta_rule_bwd(
+                q, k, v, f["g_cumsum"], beta, f["A"], dO, use_exp2=True, stream=stream.cuda_stream),
+                R(3), 1, stream)
+            # bf16 scalar gate with the in-kernel input maps (L2 norm of q, k; beta sigmoid)
+            q, k, v, gg, beta = common((1, 4096, 16, 128), (1, 4096, 16), 0.1)
+            dO = torch.randn((1, 4096, 16, 128), device=dev, generator=g).to(torch.bfloat16)
+            kw = dict(use_qk_l2norm=True, use_beta_sigmoid=True, stream=stream.cuda_stream)
+            f = api.chunk_gated_delta_rule_fwd(q, k, v, gg, beta, return_g_cumsum=True, return_A=True, **kw)
+            aux["maps_fwd_ms"] = _time_ms(lambda: api.chunk_gated_delta_rule_fwd(q, k, v, gg, beta, **kw),
+                                          R(3), 1, stream)
+            aux["maps_bwd_ms"] = _time_ms(lambda: api.chunk_gated_delta_rule_bwd(
+                q, k, v, f["g_cumsum"], beta, f["A"], dO, **kw), R(3), 1, stream)
+            out["aux_paths"] = aux
     Bd.gdn_device_status(stream.cuda_stream)
     return out
 
