@@ -638,6 +638,9 @@ gdn_status gdn_chunk_bwd(const gdn_problem *pin, const void *q, const void *k, c
     b.xw = f.xw;
     b.ftab = f.ftab;
     e = gdn::launch_tc_dhu(b, runs, s);
+  } else if (use_kda_tc(p)) {
+    b.blob = static_cast<const uint8_t *>(xw);
+    e = gdn::launch_kda_dhu(b, runs, s);
   } else {
     e = gdn::launch_bwd_dhu(b, pk, bf, s);
   }

@@ -145,6 +145,8 @@ struct BwdArgs {
   // 64-column K-blocks, dv_new [64 tokens x 128] likewise), replacing h_chunks, dh_chunks, dvnew
   const __nv_bfloat16 *h_tiles;
   __nv_bfloat16 *dh_tiles, *dv_tiles;
+  // bf16 per-key backward: the prep kernel's blobs of every chunk (kda:: layout)
+  const uint8_t *blob;
   int *dev_flag;
 };
 cudaError_t launch_bwd_dhu(const BwdArgs &a, bool per_key, bool bf16, cudaStream_t st);
@@ -153,6 +155,8 @@ cudaError_t launch_bwd_local(const BwdArgs &a, bool per_key, bool bf16, cudaStre
 cudaError_t launch_bwd_local_tc(const BwdArgs &a, cudaStream_t st);
 // tcgen05 reverse state recurrence (bf16, scalar gate); needs a.xw / a.ftab
 cudaError_t launch_tc_dhu(const BwdArgs &a, int runs, cudaStream_t st);
+// tcgen05 reverse state recurrence (bf16, per-key gate) over the prep blobs; needs a.blob
+cudaError_t launch_kda_dhu(const BwdArgs &a, int runs, cudaStream_t st);
 
 // ---- per-key (KDA) tensor-core path ----------------------------------------------------
 // The prep kernel writes, for every (chunk, head), one blob of bf16 tiles already in the
