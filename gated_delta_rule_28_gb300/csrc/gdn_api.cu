@@ -819,6 +819,12 @@ gdn_status kda_segment_summary_bwd(const gdn_problem *pin, const void *q, const 
     b.xw = u.xw;
     b.ftab = u.ftab;
     e = gdn::launch_tc_dhu(b, p->B * nseg, s);
+  } else if (use_kda_tc(p)) {  // the prep's blobs (no v: the reverse recurrence does not read u)
+    const gdn::KdaPrepArgs pa = kda_prep_args(p, q, k, nullptr, nullptr, g_cumsum, beta, w + L.xw, nullptr, nullptr,
+                                              b.scale, b.dev_flag);
+    if ((e = gdn::launch_kda_prep(pa, (int)n_chunk_slots(p), s)) != cudaSuccess) return cuda_fail(e, "KDA prep launch");
+    b.blob = reinterpret_cast<const uint8_t *>(w + L.xw);
+    e = gdn::launch_kda_dhu(b, p->B * nseg, s);
   } else {
     e = gdn::launch_bwd_dhu(b, p->gate_kind == GDN_GATE_PER_KEY, p->dtype == GDN_DTYPE_BF16, s);
   }

@@ -155,7 +155,7 @@ __global__ void __launch_bounds__(NTH, 2) kda_prep_kernel(KdaPrepArgs a, int64_t
       const uint32_t o = (c16 >> 3) * 8192 + chunk_off(r, c16 & 7);
       cp_async16(sb + OFF_K + o, k + row * GDN_DK + c16 * 8, valid ? 16u : 0u);
       cp_async16(sb + OFF_Q + o, (has_q ? q : k) + row * GDN_DK + c16 * 8, valid && has_q ? 16u : 0u);
-      cp_async16(sb + OFF_V + o, v + row * GDN_DV + c16 * 8, valid ? 16u : 0u);
+      cp_async16(sb + OFF_V + o, (v ? v : k) + row * GDN_DV + c16 * 8, valid && v ? 16u : 0u);  // no v: u = 0
     }
     cp_async_commit();
     if (tid < 64) sv.beta[tid] = tid < n ? __bfloat162float(beta[(r0 + tid) * H + h]) : 0.f;
