@@ -445,83 +445,105 @@ __global__ void __launch_bounds__(NTH, 1) local_kernel(BwdArgs a) {
   const int wc128 = 64 * (tid >> 7), wc64 = 32 * (tid >> 7);
   const int fg = lane >> 2, ft = lane & 3;  // this thread's fragment row / column pair
 
-  // ---- gated Gram matrices ------------------------------------------------
+  // per-key gate on the tensor-core path: with one reference row r per chunk and
+  // e_id = b^(G_id - G_rd), every gated product is a plain product of pre-scaled operands,
+  //   sum_j M_ij x_jd b^(G_id - G_jd) = e_id sum_j M_ij (x_jd / e_jd),
+  // valid while every |G_id - G_rd| stays within 100 in base 2 (the factors stay inside the
+  // fp32 range); a chunk beyond that takes the term-by-term loops, exact for any gate range
+  constexpr int REFR = 32;
+  const float l2b = e2 ? 1.f : 1.4426950408889634f;
+  bool fast = false;
+  if constexpr (TC && PER_KEY) {
+    const int d = tid & 127, r0 = 32 * (tid >> 7);
+    const float gr = sG[REFR * KP + d];
+    float span = 0.f;
+    for (int i = r0; i < r0 + 32; ++i) span = fmaxf(span, fabsf(sG[i * KP + d] - gr));
+    fast = !__syncthreads_or(!(span * l2b <= 100.f));
+  }
+  // b^x with one special-function instruction (PTX ex2.approx.ftz, relative error near 2^-22)
+  auto bx = [&](float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x * l2b));
+    return y;
+  };
+  auto EP = [&](int i, int d) { return bx(sG[i * KP + d] - sG[REFR * KP + d]); };
+  auto EM = [&](int i, int d) { return bx(sG[REFR * KP + d] - sG[i * KP + d]); };
+
+  // ---- gated Gram matrix P = strictly-lower(K K^T (.) Gamma) ----------------------
+  // (the gated Q K^T of the forward is not needed: dA_qk is formed from dO and v_new)
   {
     int m0, n0;
     tile_origin<64, 64, 4, 4>(tid, m0, n0);
-    float accP[4][4], accQ[4][4];
+    float accP[4][4];
     zero_acc(accP);
-    zero_acc(accQ);
-    if constexpr (TC && !PER_KEY) {  // K K^T and Q K^T on tensor cores, then gated per element
+    bool in_tiles = true;
+    if constexpr (TC && !PER_KEY) {  // K K^T on tensor cores, then gated per element
       constexpr int LD = GDN_CHUNK + 4;
       float *st = sSl;  // [64][LD] staging, the slice region is not in use yet
-      float fP[4][4], fQ[4][4];
+      float fP[4][4];
       zero_acc(fP);
-      zero_acc(fQ);
       auto fk = [&](int m, int kk) { return sK[m * KP + kk]; };
-      auto fq = [&](int m, int kk) { return sQ[m * KP + kk]; };
       auto fkt = [&](int kk, int nn) { return sK[nn * KP + kk]; };
       mma_tf32_acc<GDN_DK, 4>(fk, fkt, fP, wr0, wc64, lane);
-      mma_tf32_acc<GDN_DK, 4>(fq, fkt, fQ, wr0, wc64, lane);
       mma_frag_store(st, LD, fP, wr0, wc64, lane);
       __syncthreads();
 #pragma unroll
       for (int x = 0; x < 4; ++x)
 #pragma unroll
-        for (int y = 0; y < 4; ++y) accP[x][y] = st[(m0 + x) * LD + n0 + y];
-      __syncthreads();
-      mma_frag_store(st, LD, fQ, wr0, wc64, lane);
-      __syncthreads();
+        for (int y = 0; y < 4; ++y) {
+          const float gam = n0 + y <= m0 + x ? gate_pow(sG[m0 + x] - sG[n0 + y], e2) : 0.f;
+          accP[x][y] = st[(m0 + x) * LD + n0 + y] * gam;
+        }
+    } else {
+      if constexpr (TC && PER_KEY) {
+        if (fast) {  // (K (.) e)(K / e)^T on tensor cores, fragments straight into sP
+          float fP[4][4];
+          zero_acc(fP);
+          auto fa = [&](int m, int kk) { return sK[m * KP + kk] * EP(m, kk); };
+          auto fb = [&](int kk, int nn) { return sK[nn * KP + kk] * EM(nn, kk); };
+          mma_tf32_acc<GDN_DK, 4>(fa, fb, fP, wr0, wc64, lane);
 #pragma unroll
-      for (int x = 0; x < 4; ++x)
+          for (int j = 0; j < 4; ++j)
 #pragma unroll
-        for (int y = 0; y < 4; ++y) accQ[x][y] = st[(m0 + x) * LD + n0 + y];
+            for (int e = 0; e < 4; ++e) {
+              const int i = wr0 + fg + 8 * (e >> 1), c = wc64 + 8 * j + 2 * ft + (e & 1);
+              sP[i * CP + c] = c < i ? fP[j][e] : 0.f;
+            }
+          in_tiles = false;
+        }
+      }
+      if (in_tiles && n0 <= m0 + 3) {
+        if (PER_KEY) {
+          for (int d = 0; d < GDN_DK; ++d) {
+#pragma unroll
+            for (int x = 0; x < 4; ++x)
+#pragma unroll
+              for (int y = 0; y < 4; ++y) {
+                if (n0 + y > m0 + x) continue;
+                const float gam = gate_pow(sG[(m0 + x) * KP + d] - sG[(n0 + y) * KP + d], e2);
+                accP[x][y] = fmaf(sK[(m0 + x) * KP + d] * sK[(n0 + y) * KP + d], gam, accP[x][y]);
+              }
+          }
+        } else {
+          auto fk = [&](int m, int kk) { return sK[m * KP + kk]; };
+          auto fkt = [&](int kk, int nn) { return sK[nn * KP + kk]; };
+          mm_acc<64, 64, GDN_DK, 4, 4>(fk, fkt, accP, tid);
+#pragma unroll
+          for (int x = 0; x < 4; ++x)
+#pragma unroll
+            for (int y = 0; y < 4; ++y) accP[x][y] *= gate_pow(sG[m0 + x] - sG[n0 + y], e2);
+        }
+      }
+    }
+    if (in_tiles) {
 #pragma unroll
       for (int x = 0; x < 4; ++x)
 #pragma unroll
         for (int y = 0; y < 4; ++y) {
-          const float gam = n0 + y <= m0 + x ? gate_pow(sG[m0 + x] - sG[n0 + y], e2) : 0.f;
-          accP[x][y] *= gam;
-          accQ[x][y] *= gam;
+          const int i = m0 + x, j = n0 + y;
+          sP[i * CP + j] = j < i ? accP[x][y] : 0.f;
         }
-    } else if (n0 <= m0 + 3) {
-      if (PER_KEY) {
-        for (int d = 0; d < GDN_DK; ++d) {
-#pragma unroll
-          for (int x = 0; x < 4; ++x)
-#pragma unroll
-            for (int y = 0; y < 4; ++y) {
-              if (n0 + y > m0 + x) continue;
-              const float gam = gate_pow(sG[(m0 + x) * KP + d] - sG[(n0 + y) * KP + d], e2);
-              const float kj = sK[(n0 + y) * KP + d];
-              accP[x][y] = fmaf(sK[(m0 + x) * KP + d] * kj, gam, accP[x][y]);
-              accQ[x][y] = fmaf(sQ[(m0 + x) * KP + d] * kj, gam, accQ[x][y]);
-            }
-        }
-      } else {
-        auto fk = [&](int m, int kk) { return sK[m * KP + kk]; };
-        auto fq = [&](int m, int kk) { return sQ[m * KP + kk]; };
-        auto fkt = [&](int kk, int nn) { return sK[nn * KP + kk]; };
-        mm_acc<64, 64, GDN_DK, 4, 4>(fk, fkt, accP, tid);
-        mm_acc<64, 64, GDN_DK, 4, 4>(fq, fkt, accQ, tid);
-#pragma unroll
-        for (int x = 0; x < 4; ++x)
-#pragma unroll
-          for (int y = 0; y < 4; ++y) {
-            const float gam = gate_pow(sG[m0 + x] - sG[n0 + y], e2);
-            accP[x][y] *= gam;
-            accQ[x][y] *= gam;
-          }
-      }
     }
-#pragma unroll
-    for (int x = 0; x < 4; ++x)
-#pragma unroll
-      for (int y = 0; y < 4; ++y) {
-        const int i = m0 + x, j = n0 + y;
-        sP[i * CP + j] = j < i ? accP[x][y] : 0.f;
-        sAqk[i * CP + j] = j <= i ? accQ[x][y] : 0.f;
-      }
   }
   __syncthreads();
 
@@ -565,12 +587,12 @@ __global__ void __launch_bounds__(NTH, 1) local_kernel(BwdArgs a) {
     }
     __syncthreads();
     // Z = beta (V - (K (.) base^G) h) ; also keep V - Y for dbeta
-    if constexpr (TC && !PER_KEY) {  // the 64 x LBV product on tensor cores, LBV/16 tiles per warp
+    if constexpr (TC) {  // the 64 x LBV product on tensor cores, LBV/16 tiles per warp
       constexpr int NZ = LBV / 16;
       const int zr0 = 16 * ((tid >> 5) & 3), zc0 = (LBV / 2) * (tid >> 7);
       float fz[NZ][4];
       zero_acc(fz);
-      auto fkg = [&](int m, int kk) { return sK[m * KP + kk] * sG[64 + m]; };
+      auto fkg = [&](int m, int kk) { return sK[m * KP + kk] * (PER_KEY ? bx(sG[m * KP + kk]) : sG[64 + m]); };
       auto fhs = [&](int kk, int nn) { return sHs[kk * LVP + nn]; };
       mma_tf32_acc<GDN_DK, NZ>(fkg, fhs, fz, zr0, zc0, lane);
 #pragma unroll
@@ -599,7 +621,7 @@ __global__ void __launch_bounds__(NTH, 1) local_kernel(BwdArgs a) {
     }
     __syncthreads();
     // v_new = X Z ; dZ = X^T dv_new
-    if constexpr (TC && !PER_KEY) {  // both 64 x LBV products on tensor cores, LBV/16 tiles per warp
+    if constexpr (TC) {  // both 64 x LBV products on tensor cores, LBV/16 tiles per warp
       constexpr int NZ = LBV / 16;
       const int zr0 = 16 * ((tid >> 5) & 3), zc0 = (LBV / 2) * (tid >> 7);
       float fv[NZ][4], fd[NZ][4];
@@ -825,24 +847,8 @@ __global__ void __launch_bounds__(NTH, 1) local_kernel(BwdArgs a) {
     const float *Op = which == 3 ? sQ : sK;
     float t[4][8];
     zero_acc(t);
-    if constexpr (TC && !PER_KEY) {
-      // the gate is already folded into the 64 x 64 matrix: a plain product, on tf32 tensor
-      // cores, moved into the thread tile through the slice region
-      constexpr int LD = GDN_DK + 4;
-      float *st = sSl;
-      float fr[8][4];
-      zero_acc(fr);
-      auto fm = [&](int m, int kk) { return tr ? Mx[kk * CP + m] : Mx[m * CP + kk]; };
-      auto fop = [&](int kk, int nn) { return Op[kk * KP + nn]; };
-      mma_tf32_acc<GDN_CHUNK, 8>(fm, fop, fr, wr0, wc128, lane);
-      mma_frag_store(st, LD, fr, wr0, wc128, lane);
-      __syncthreads();
-#pragma unroll
-      for (int x = 0; x < 4; ++x)
-#pragma unroll
-        for (int y = 0; y < 8; ++y) t[x][y] = st[(gm0 + x) * LD + gn0 + y];
-      __syncthreads();
-    } else {
+    // term by term, one gate factor per (i, j, d): exact for any gate range
+    auto by_terms = [&]() {
       for (int j = 0; j < GDN_CHUNK; ++j) {
 #pragma unroll
         for (int x = 0; x < 4; ++x) {
@@ -860,6 +866,49 @@ __global__ void __launch_bounds__(NTH, 1) local_kernel(BwdArgs a) {
           }
         }
       }
+    };
+    if constexpr (TC && !PER_KEY) {
+      // the gate is already folded into the 64 x 64 matrix: a plain product, on tf32 tensor
+      // cores, moved into the thread tile through the slice region
+      constexpr int LD = GDN_DK + 4;
+      float *st = sSl;
+      float fr[8][4];
+      zero_acc(fr);
+      auto fm = [&](int m, int kk) { return tr ? Mx[kk * CP + m] : Mx[m * CP + kk]; };
+      auto fop = [&](int kk, int nn) { return Op[kk * KP + nn]; };
+      mma_tf32_acc<GDN_CHUNK, 8>(fm, fop, fr, wr0, wc128, lane);
+      mma_frag_store(st, LD, fr, wr0, wc128, lane);
+      __syncthreads();
+#pragma unroll
+      for (int x = 0; x < 4; ++x)
+#pragma unroll
+        for (int y = 0; y < 8; ++y) t[x][y] = st[(gm0 + x) * LD + gn0 + y];
+      __syncthreads();
+    } else if constexpr (TC && PER_KEY) {
+      if (fast) {
+        // (M or M^T)(Op (.) e^-+1) on tf32 tensor cores, then the row factor e^+-1 of (i, d)
+        constexpr int LD = GDN_DK + 4;
+        float *st = sSl;
+        float fr[8][4];
+        zero_acc(fr);
+        auto fm = [&](int m, int kk) { return tr ? Mx[kk * CP + m] : Mx[m * CP + kk]; };
+        auto fop = [&](int kk, int nn) { return Op[kk * KP + nn] * (tr ? EP(kk, nn) : EM(kk, nn)); };
+        mma_tf32_acc<GDN_CHUNK, 8>(fm, fop, fr, wr0, wc128, lane);
+        mma_frag_store(st, LD, fr, wr0, wc128, lane);
+        __syncthreads();
+#pragma unroll
+        for (int x = 0; x < 4; ++x)
+#pragma unroll
+          for (int y = 0; y < 8; ++y) {
+            const int i = gm0 + x, d = gn0 + y;
+            t[x][y] = st[i * LD + d] * (tr ? EM(i, d) : EP(i, d));
+          }
+        __syncthreads();
+      } else {
+        by_terms();
+      }
+    } else {
+      by_terms();
     }
 #pragma unroll
     for (int x = 0; x < 4; ++x)
