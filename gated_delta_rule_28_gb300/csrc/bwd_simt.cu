@@ -286,6 +286,22 @@ __global__ void __launch_bounds__(NTH) dhu_kernel(BwdArgs a) {
 }
 
 // ---------------------------------------------------------------------------
+// 16-byte global loads (every operand row and the slices within it start on 16 bytes):
+// 8 bf16 or 4 fp32 values per load. The local kernel issues all of a phase's loads before
+// its first shared-memory store, so that one memory round trip covers the phase.
+__device__ __forceinline__ uint4 ld16(const void *p) { return __ldg(reinterpret_cast<const uint4 *>(p)); }
+template <typename T>
+__device__ __forceinline__ float lane16(const uint4 &u, int e) {
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+  if constexpr (std::is_same<T, float>::value) {
+    return __uint_as_float(w[e]);
+  } else {
+    const uint32_t x = w[e >> 1];
+    return __uint_as_float((e & 1) ? (x & 0xffff0000u) : (x << 16));
+  }
+}
+
+// ---------------------------------------------------------------------------
 // local gradients, one CTA per (chunk, head), the value width in 8 slices
 constexpr int LBV = 16;
 constexpr int LVP = LBV + 1;
@@ -387,30 +403,70 @@ __global__ void __launch_bounds__(NTH, 1) local_kernel(BwdArgs a) {
   const float *hc = a.h_chunks + slot * KV;
   const float *dhc = a.dh_chunks + slot * KV;
 
-  // ---- chunk operands ----------------------------------------------------
-  for (int idx = tid; idx < 64 * GDN_DK; idx += NTH) {
-    const int i = idx >> 7, d = idx & 127;
-    float kv = 0.f, qv = 0.f, gv = 0.f;
-    if (i < n) {
-      const int64_t off = ((c0 + i) * H + h) * GDN_DK + d;
-      kv = to_f32(k[off]);
-      qv = to_f32(q[off]);
-      if (PER_KEY) gv = a.g_cumsum[off];
+  // ---- chunk operands (16-byte loads, all issued before the first store) ---------
+  float bet = 0.f, gsc = 0.f;  // beta and (scalar gate) the cumulative gate of token tid
+  {
+    constexpr int EV = 16 / sizeof(T);               // q, k values per load
+    constexpr int NV = 64 * GDN_DK / EV / NTH;        // loads per thread and operand
+    constexpr int NG = PER_KEY ? 64 * GDN_DK / 4 / NTH : 1;
+    uint4 kr[NV], qr[NV], gr[NG], xr[64 * GDN_CHUNK / 4 / NTH];
+    const uint4 z4 = make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+    for (int r = 0; r < NV; ++r) {
+      const int idx = tid + r * NTH, i = idx / (GDN_DK / EV), d0 = idx % (GDN_DK / EV) * EV;
+      const int64_t off = ((c0 + i) * H + h) * GDN_DK + d0;
+      kr[r] = i < n ? ld16(k + off) : z4;
+      qr[r] = i < n ? ld16(q + off) : z4;
     }
-    sK[i * KP + d] = kv;
-    sQ[i * KP + d] = qv;
-    if (PER_KEY) sG[i * KP + d] = gv;
-  }
-  for (int idx = tid; idx < 64 * 64; idx += NTH) {
-    const int i = idx >> 6, j = idx & 63;
-    sX[i * CP + j] = (i < n && j < n) ? a.A[((c0 + i) * H + h) * GDN_CHUNK + j] : (i == j ? 1.f : 0.f);
+    if (PER_KEY) {
+#pragma unroll
+      for (int r = 0; r < NG; ++r) {
+        const int idx = tid + r * NTH, i = idx / (GDN_DK / 4), d0 = idx % (GDN_DK / 4) * 4;
+        gr[r] = i < n ? ld16(a.g_cumsum + ((c0 + i) * H + h) * GDN_DK + d0) : z4;
+      }
+    }
+#pragma unroll
+    for (int r = 0; r < 64 * GDN_CHUNK / 4 / NTH; ++r) {
+      const int idx = tid + r * NTH, i = idx / (GDN_CHUNK / 4), j0 = idx % (GDN_CHUNK / 4) * 4;
+      xr[r] = i < n ? ld16(a.A + ((c0 + i) * H + h) * GDN_CHUNK + j0) : z4;
+    }
+    if (tid < 64) {
+      if (tid < n) bet = to_f32(beta[(c0 + tid) * H + h]);
+      if (!PER_KEY) gsc = a.g_cumsum[(c0 + min(tid, n - 1)) * H + h];
+    }
+#pragma unroll
+    for (int r = 0; r < NV; ++r) {
+      const int idx = tid + r * NTH, i = idx / (GDN_DK / EV), d0 = idx % (GDN_DK / EV) * EV;
+#pragma unroll
+      for (int e = 0; e < EV; ++e) {
+        sK[i * KP + d0 + e] = lane16<T>(kr[r], e);
+        sQ[i * KP + d0 + e] = lane16<T>(qr[r], e);
+      }
+    }
+    if (PER_KEY) {
+#pragma unroll
+      for (int r = 0; r < NG; ++r) {
+        const int idx = tid + r * NTH, i = idx / (GDN_DK / 4), d0 = idx % (GDN_DK / 4) * 4;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) sG[i * KP + d0 + e] = lane16<float>(gr[r], e);
+      }
+    }
+#pragma unroll
+    for (int r = 0; r < 64 * GDN_CHUNK / 4 / NTH; ++r) {
+      const int idx = tid + r * NTH, i = idx / (GDN_CHUNK / 4), j0 = idx % (GDN_CHUNK / 4) * 4;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int j = j0 + e;
+        sX[i * CP + j] = (i < n && j < n) ? lane16<float>(xr[r], e) : (i == j ? 1.f : 0.f);
+      }
+    }
   }
   if (tid < 64) {
-    sBeta[tid] = tid < n ? to_f32(beta[(c0 + tid) * H + h]) : 0.f;
+    sBeta[tid] = bet;
     sDBeta[tid] = 0.f;
     sDGrow[tid] = 0.f;
     sDBpart[tid] = sDBpart[64 + tid] = sDBpart[128 + tid] = 0.f;
-    if (!PER_KEY) sG[tid] = a.g_cumsum[(c0 + min(tid, n - 1)) * H + h];
+    if (!PER_KEY) sG[tid] = gsc;
   }
   if (tid < 128) {
     sDGLh[tid] = 0.f;
@@ -567,23 +623,62 @@ __global__ void __launch_bounds__(NTH, 1) local_kernel(BwdArgs a) {
   zero_acc(fX);
   zero_acc(fQk);
   for (int vs = 0; vs < GDN_DV; vs += LBV) {
-    for (int idx = tid; idx < 128 * LBV; idx += NTH) {
-      const int d = idx / LBV, c = idx % LBV;
-      sHs[d * LVP + c] = hc[d * GDN_DV + vs + c];
-      sDHs[d * LVP + c] = dhc[d * GDN_DV + vs + c];
-    }
-    for (int idx = tid; idx < 64 * LBV; idx += NTH) {
-      const int i = idx / LBV, c = idx % LBV;
-      float vv = 0.f, dov = 0.f, ddv = 0.f;
-      if (i < n) {
-        const int64_t off = ((c0 + i) * H + h) * GDN_DV + vs + c;
-        vv = to_f32(v[off]);
-        dov = to_f32(dO[off]);
-        ddv = a.dvnew[off];
+    {  // the slice: h, dh (128 x LBV), v, dO, dv_new (64 x LBV), 16-byte loads issued together
+      constexpr int EV = 16 / sizeof(T);
+      constexpr int NH = 128 * LBV / 4, NVv = 64 * LBV / EV, ND = 64 * LBV / 4;
+      constexpr int RH = (NH + NTH - 1) / NTH, RV = (NVv + NTH - 1) / NTH, RD = (ND + NTH - 1) / NTH;
+      uint4 hr[RH], dhr[RH], vr[RV], dor[RV], ddr[RD];
+      const uint4 z4 = make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+      for (int r = 0; r < RH; ++r) {
+        const int idx = tid + r * NTH, d = idx / (LBV / 4), cc = idx % (LBV / 4) * 4;
+        if (idx < NH) {
+          hr[r] = ld16(hc + d * GDN_DV + vs + cc);
+          dhr[r] = ld16(dhc + d * GDN_DV + vs + cc);
+        }
       }
-      sVs[i * LVP + c] = vv;
-      sDOs[i * LVP + c] = dov;
-      sDDs[i * LVP + c] = ddv;
+#pragma unroll
+      for (int r = 0; r < RV; ++r) {
+        const int idx = tid + r * NTH, i = idx / (LBV / EV), cc = idx % (LBV / EV) * EV;
+        const int64_t off = ((c0 + i) * H + h) * GDN_DV + vs + cc;
+        vr[r] = (idx < NVv && i < n) ? ld16(v + off) : z4;
+        dor[r] = (idx < NVv && i < n) ? ld16(dO + off) : z4;
+      }
+#pragma unroll
+      for (int r = 0; r < RD; ++r) {
+        const int idx = tid + r * NTH, i = idx / (LBV / 4), cc = idx % (LBV / 4) * 4;
+        ddr[r] = (idx < ND && i < n) ? ld16(a.dvnew + ((c0 + i) * H + h) * GDN_DV + vs + cc) : z4;
+      }
+#pragma unroll
+      for (int r = 0; r < RH; ++r) {
+        const int idx = tid + r * NTH, d = idx / (LBV / 4), cc = idx % (LBV / 4) * 4;
+        if (idx < NH) {
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            sHs[d * LVP + cc + e] = lane16<float>(hr[r], e);
+            sDHs[d * LVP + cc + e] = lane16<float>(dhr[r], e);
+          }
+        }
+      }
+#pragma unroll
+      for (int r = 0; r < RV; ++r) {
+        const int idx = tid + r * NTH, i = idx / (LBV / EV), cc = idx % (LBV / EV) * EV;
+        if (idx < NVv) {
+#pragma unroll
+          for (int e = 0; e < EV; ++e) {
+            sVs[i * LVP + cc + e] = lane16<T>(vr[r], e);
+            sDOs[i * LVP + cc + e] = lane16<T>(dor[r], e);
+          }
+        }
+      }
+#pragma unroll
+      for (int r = 0; r < RD; ++r) {
+        const int idx = tid + r * NTH, i = idx / (LBV / 4), cc = idx % (LBV / 4) * 4;
+        if (idx < ND) {
+#pragma unroll
+          for (int e = 0; e < 4; ++e) sDDs[i * LVP + cc + e] = lane16<float>(ddr[r], e);
+        }
+      }
     }
     __syncthreads();
     // Z = beta (V - (K (.) base^G) h) ; also keep V - Y for dbeta
