@@ -16,6 +16,7 @@
 // The fp32 X (the A output of the forward) and the cumulative gate are
 // written here when asked for.
 #include <algorithm>
+#include <climits>
 
 #include "common.cuh"
 #include "kernels.h"
@@ -57,35 +58,43 @@ __global__ void __launch_bounds__(128, 6) ut_kernel(UtArgs a, int64_t items) {
   const float *gsrc = a.g_cum_in ? a.g_cum_in : a.g;
   const int NT = (a.T + GDN_CHUNK - 1) / GDN_CHUNK;
 
-  // rows [r0, r0 + n) of item it = slot * H + h; false for a corrupt packed chunk index
-  auto locate = [&](int64_t it, int64_t &r0, int &n) -> bool {
-    const int64_t slot = it / H;
+  // Item it = slot * H + h covers rows [r0, r0 + n) of head h. Each item is located once,
+  // one iteration ahead, in 32-bit arithmetic (the launch checks that items < 2^31).
+  struct Loc {
+    int64_t r0, slot;
+    int n, h;
+    bool live, ok;  // live: it < items; ok: a valid chunk (a corrupt packed index is not)
+  };
+  auto locate = [&](int64_t it) -> Loc {
+    Loc L{0, 0, 0, 0, it < items, false};
+    if (!L.live) return L;
+    const uint32_t u = (uint32_t)it, slot = u / (uint32_t)H;
+    L.slot = slot;
+    L.h = (int)(u - slot * (uint32_t)H);
     int64_t r1;
     if (a.cu) {
       const int seq = a.chunk_indices[2 * slot], cc = a.chunk_indices[2 * slot + 1];
-      if (!(seq >= 0 && seq < a.num_seqs && cc >= 0)) return false;
-      r0 = (int64_t)a.cu[seq] + (int64_t)cc * GDN_CHUNK;
+      if (!(seq >= 0 && seq < a.num_seqs && cc >= 0)) return L;
+      L.r0 = (int64_t)a.cu[seq] + (int64_t)cc * GDN_CHUNK;
       r1 = a.cu[seq + 1];
-      if (!(r0 >= 0 && r0 < r1 && r1 <= a.T)) return false;
+      if (!(L.r0 >= 0 && L.r0 < r1 && r1 <= a.T)) return L;
     } else {
-      const int64_t b = slot / NT, c = slot % NT;
-      r0 = b * a.T + c * GDN_CHUNK;
-      r1 = b * a.T + a.T;
+      const uint32_t b = slot / (uint32_t)NT, c = slot - b * (uint32_t)NT;
+      L.r0 = (int64_t)b * a.T + (int64_t)c * GDN_CHUNK;
+      r1 = (int64_t)b * a.T + a.T;
     }
-    n = (int)min((int64_t)GDN_CHUNK, r1 - r0);
-    return true;
+    L.n = (int)min((int64_t)GDN_CHUNK, r1 - L.r0);
+    L.ok = true;
+    return L;
   };
-  auto load_keys = [&](int64_t it, int buf) {  // zero past the chunk end
-    int64_t r0;
-    int n;
-    if (it < items && locate(it, r0, n)) {
-      const int h = (int)(it % H);
+  auto load_keys = [&](const Loc &L, int buf) {  // zero past the chunk end
+    if (L.live && L.ok) {
       const uint32_t kt = smem_u32(kbuf[buf]);
 #pragma unroll
       for (int x = tid; x < 1024; x += 128) {
         const int r = x >> 4, f16 = x & 15;
-        const bool valid = r < n;
-        const __nv_bfloat16 *src = k + ((r0 + (valid ? r : 0)) * H + h) * GDN_DK + f16 * 8;
+        const bool valid = r < L.n;
+        const __nv_bfloat16 *src = k + ((L.r0 + (valid ? r : 0)) * H + L.h) * GDN_DK + f16 * 8;
         cp_async16(kt + (f16 >> 3) * 8192 + chunk_off(r, f16 & 7), src, valid ? 16u : 0u);
       }
     }
@@ -94,34 +103,32 @@ __global__ void __launch_bounds__(128, 6) ut_kernel(UtArgs a, int64_t items) {
 
   // gate and beta of an item into registers, one item ahead (rows past the end: no gate
   // increment, beta 0)
-  auto load_gb = [&](int64_t it, float &gv, float &bv) {
+  auto load_gb = [&](const Loc &L, float &gv, float &bv) {
     gv = 0.f;
     bv = 0.f;
-    int64_t rr;
-    int nn;
-    if (tid < 64 && it < items && locate(it, rr, nn) && tid < nn) {
-      const int hh = (int)(it % H);
-      gv = gsrc[(rr + tid) * H + hh];
-      bv = __bfloat162float(beta[(rr + tid) * H + hh]);
+    if (tid < 64 && L.live && L.ok && tid < L.n) {
+      gv = gsrc[(L.r0 + tid) * H + L.h];
+      bv = __bfloat162float(beta[(L.r0 + tid) * H + L.h]);
     }
   };
   const int buf = 0;
   float ng, nb;
-  load_gb(blockIdx.x, ng, nb);
+  Loc cur = locate(blockIdx.x);
+  load_gb(cur, ng, nb);
   for (int64_t it = blockIdx.x; it < items; it += gridDim.x) {
-    load_keys(it, buf);
-    int64_t r0 = 0;
-    int n = 0;
-    const bool ok = locate(it, r0, n);
-    const int h = (int)(it % H);
-    const int64_t slot = it / H;
+    load_keys(cur, buf);
+    const Loc nxt = locate(it + gridDim.x);  // while the keys arrive
+    const bool ok = cur.ok;
+    const int64_t r0 = cur.r0, slot = cur.slot;
+    const int n = cur.n, h = cur.h;
     if (tid < 64) {
       sg[tid] = ng;
       sbeta[tid] = nb;
     }
     cp_async_wait<0>();
     __syncthreads();
-    load_gb(it + gridDim.x, ng, nb);
+    load_gb(nxt, ng, nb);
+    cur = nxt;
     if (!ok) {
       if (tid == 0) raise_device_flag(a.dev_flag, kDevCheck);
       continue;  // uniform: every thread saw the same chunk index
@@ -273,6 +280,7 @@ cudaError_t launch_ut(const UtArgs &a, int slots, cudaStream_t st) {
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 128, 0);
   if (e != cudaSuccess) return e;
+  if (items > INT32_MAX) return cudaErrorInvalidValue;  // the kernel locates items in 32 bits
   const int64_t grid = std::min<int64_t>(items, (int64_t)std::max(1, sms * std::max(1, per_sm)));
   kern<<<(unsigned)grid, 128, 0, st>>>(a, items);
   return cudaGetLastError();
