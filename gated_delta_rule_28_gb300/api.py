@@ -210,8 +210,31 @@ def segment_merge(S_ext, M, h0=None, stream=None):
 def split_forward(q, k, v, g, beta, segment_len, *, h0=None, scale=None, use_exp2=False,
                   use_qk_l2norm=False, use_beta_sigmoid=False, return_h_chunks=False,
                   return_g_cumsum=False, return_A=False, stream=None):
-    """Long-sequence forward split across SMs: summaries, merge, corrected run."""
+    """Long-sequence forward split across SMs: summaries, merge, corrected run (bf16 with a
+    per-key gate: one ``gdn_chunk_fwd_split`` call, whose chunk preparation serves both passes)."""
     maps = dict(use_qk_l2norm=use_qk_l2norm, use_beta_sigmoid=use_beta_sigmoid)
+    p = problem_for(q, v, g, scale=scale, use_exp2=use_exp2, **maps)
+    if p.dtype == B.GDN_DTYPE_BF16 and p.gate_kind == B.GDN_GATE_PER_KEY:
+        dev = q.device
+        nseg = -(-p.T // segment_len)
+        out = {"o": torch.empty_like(v),
+               "ht": torch.empty((p.B, p.H, p.K, p.V), device=dev, dtype=torch.float32),
+               "S_ext": torch.empty((p.B, p.H, nseg, p.K, p.V), device=dev, dtype=torch.float32),
+               "M": torch.empty((p.B, p.H, nseg, p.K, p.K), device=dev, dtype=torch.float32)}
+        out["S_init"] = torch.empty_like(out["S_ext"])
+        if return_g_cumsum:
+            out["g_cumsum"] = torch.empty_like(g, dtype=torch.float32)
+        if return_A:
+            out["A"] = torch.empty(q.shape[:-1] + (64,), device=dev, dtype=torch.float32)
+        if return_h_chunks:
+            out["h_chunks"] = torch.empty((p.B, p.H, -(-p.T // 64), p.K, p.V), device=dev,
+                                          dtype=torch.float32)
+        nws = B.gdn_chunk_fwd_split_workspace(p, segment_len)
+        ws = torch.empty(nws, device=dev, dtype=torch.uint8) if nws else None
+        B.gdn_chunk_fwd_split(p, q, k, v, g, beta, h0, segment_len, out["o"], out["ht"], out["S_ext"],
+                              out["M"], out["S_init"], out.get("g_cumsum"), out.get("A"),
+                              out.get("h_chunks"), ws, nws, stream)
+        return out
     S, M = segment_summary(k, v, g, beta, segment_len, use_exp2=use_exp2, stream=stream, **maps)
     S_init, _ = segment_merge(S, M, h0, stream=stream)
     out = chunk_gated_delta_rule_fwd(q, k, v, g, beta, h0=S_init, scale=scale, use_exp2=use_exp2,

@@ -33,7 +33,8 @@ EXPORTS = ("gdn_last_error", "gdn_device_status", "gdn_prepare_varlen", "gdn_chu
            "gdn_chunk_fwd", "gdn_chunk_bwd_workspace", "gdn_chunk_bwd", "gdn_chunk_bwd_noalloc",
            "kda_segment_summary_workspace", "kda_segment_summary", "kda_segment_merge",
            "kda_segment_summary_bwd_workspace", "kda_segment_summary_bwd", "kda_segment_merge_bwd",
-           "gdn_selftest_wait_timeout", "frame_scan_workspace", "frame_scan_fwd")
+           "gdn_selftest_wait_timeout", "frame_scan_workspace", "frame_scan_fwd",
+           "gdn_chunk_fwd_split_workspace", "gdn_chunk_fwd_split")
 # bytes of the library's built-in scratch array used by gdn_chunk_bwd_noalloc
 GDN_NOALLOC_SCRATCH_BYTES = 64 * 1024 * 1024
 
@@ -99,6 +100,8 @@ def load():
             lib.kda_segment_summary_bwd_workspace.argtypes = [P, ctypes.c_int32, ctypes.POINTER(sz)]
             lib.kda_segment_summary_bwd.argtypes = [P] + [vp] * 6 + [ctypes.c_int32, vp, vp, sz, vp]
             lib.kda_segment_merge_bwd.argtypes = [P, vp, vp, ctypes.c_int32, vp, vp, vp, vp]
+            lib.gdn_chunk_fwd_split_workspace.argtypes = [P, ctypes.c_int32, ctypes.POINTER(sz)]
+            lib.gdn_chunk_fwd_split.argtypes = [P] + [vp] * 6 + [ctypes.c_int32] + [vp] * 8 + [vp, sz, vp]
             FP = ctypes.POINTER(frame_scan_problem)
             lib.frame_scan_workspace.argtypes = [FP, ctypes.POINTER(sz)]
             lib.frame_scan_fwd.argtypes = [FP] + [vp] * 10 + [vp, sz, vp]
@@ -228,6 +231,20 @@ def kda_segment_summary(p: gdn_problem, k, v, g, beta, segment_len, S_ext, M, ws
                         stream=None):
     _check(load().kda_segment_summary(ctypes.byref(p), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
                                       int(segment_len), _ptr(S_ext), _ptr(M), _ptr(ws),
+                                      int(ws_bytes), _stream(stream)))
+
+
+def gdn_chunk_fwd_split_workspace(p: gdn_problem, segment_len) -> int:
+    n = ctypes.c_size_t(0)
+    _check(load().gdn_chunk_fwd_split_workspace(ctypes.byref(p), int(segment_len), ctypes.byref(n)))
+    return n.value
+
+
+def gdn_chunk_fwd_split(p: gdn_problem, q, k, v, g, beta, h0, segment_len, o, ht, S_ext, M, S_init,
+                        g_cumsum=None, A=None, h_chunks=None, ws=None, ws_bytes=0, stream=None):
+    _check(load().gdn_chunk_fwd_split(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
+                                      _ptr(h0), int(segment_len), _ptr(o), _ptr(ht), _ptr(S_ext), _ptr(M),
+                                      _ptr(S_init), _ptr(g_cumsum), _ptr(A), _ptr(h_chunks), _ptr(ws),
                                       int(ws_bytes), _stream(stream)))
 
 

@@ -875,6 +875,114 @@ gdn_status kda_segment_merge(const gdn_problem *p, const float *S_ext, const flo
 }
 
 namespace {
+// the problem of a one-call split forward: `p` with its segment length, checked
+gdn_status split_problem(const gdn_problem *p, int32_t segment_len, gdn_problem *sp) {
+  if (!p) return fail(GDN_ERR_INVALID_ARGUMENT, "problem is NULL");
+  if (segment_len <= 0 || segment_len % GDN_CHUNK != 0)
+    return fail(GDN_ERR_INVALID_ARGUMENT, "segment_len must be a positive multiple of 64, got %d",
+                segment_len);
+  *sp = *p;
+  sp->segment_len = segment_len;
+  gdn_status st = check_problem(sp, true);
+  if (st != GDN_OK) return st;
+  const gdn_problem m = mapped_problem(sp);
+  if (m.layout != GDN_LAYOUT_BSND || !use_kda_tc(&m))
+    return fail(GDN_ERR_UNSUPPORTED,
+                "the one-call split forward takes bf16 inputs with a per-key gate in the BSND layout");
+  return GDN_OK;
+}
+}  // namespace
+
+gdn_status gdn_chunk_fwd_split_workspace(const gdn_problem *p, int32_t segment_len, size_t *bytes) {
+  gdn_problem sp;
+  gdn_status st = split_problem(p, segment_len, &sp);
+  if (st != GDN_OK) return st;
+  if (!bytes) return fail(GDN_ERR_INVALID_ARGUMENT, "bytes must not be NULL");
+  const gdn_problem m = mapped_problem(&sp);
+  *bytes = map_part_bytes(&sp) + blob_bytes(&m);
+  return ok();
+}
+
+gdn_status gdn_chunk_fwd_split(const gdn_problem *pin, const void *q, const void *k, const void *v,
+                               const float *g, const void *beta, const float *h0, int32_t segment_len,
+                               void *o, float *ht, float *S_ext, float *M, float *S_init,
+                               float *g_cumsum, float *A, float *h_chunks, void *ws, size_t ws_bytes,
+                               void *stream) {
+  gdn_problem sp;
+  gdn_status st = split_problem(pin, segment_len, &sp);
+  if (st != GDN_OK) return st;
+  const gdn_problem mp = mapped_problem(&sp);
+  const gdn_problem *p = &mp;
+  if (p->T > 0) {
+    REQUIRE_PTR(q, "q");
+    REQUIRE_PTR(k, "k");
+    REQUIRE_PTR(v, "v");
+    REQUIRE_PTR(g, "g");
+    REQUIRE_PTR(beta, "beta");
+    REQUIRE_PTR(o, "o");
+  }
+  REQUIRE_PTR(S_ext, "S_ext");
+  REQUIRE_PTR(M, "M");
+  REQUIRE_PTR(S_init, "S_init");
+  OPTIONAL_PTR(h0, "h0");
+  OPTIONAL_PTR(ht, "ht");
+  OPTIONAL_PTR(g_cumsum, "g_cumsum");
+  OPTIONAL_PTR(A, "A");
+  OPTIONAL_PTR(h_chunks, "h_chunks");
+  const size_t maps = map_part_bytes(&sp);
+  const size_t need = maps + blob_bytes(p);
+  if (need > 0 && (!ws || ws_bytes < need))
+    return fail(GDN_ERR_WORKSPACE, "split forward workspace needs %zu bytes, got %zu", need,
+                ws ? ws_bytes : (size_t)0);
+  if (ws && !aligned16(ws)) return fail(GDN_ERR_INVALID_ARGUMENT, "ws must be 16-byte aligned");
+  int dev;
+  if ((st = check_device(&dev)) != GDN_OK) return st;
+  if (p->T == 0) return ok();
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (maps > 0) {
+    cudaError_t e = run_input_maps(&sp, &q, &k, &beta, ws, s);
+    if (e != cudaSuccess) return cuda_fail(e, "input map launch");
+  }
+  void *blob = static_cast<char *>(ws) + maps;
+  const int nseg = (int)div_up(p->T, segment_len);
+  int *flag = device_flag_ptr();
+  // 1. every chunk's operands, once for both passes (the summary reads w, u and the decays;
+  //    the corrected run also the query-side operands)
+  const gdn::KdaPrepArgs pa = kda_prep_args(p, q, k, v, g, nullptr, beta, blob, g_cumsum, A, eff_scale(p), flag);
+  cudaError_t e = gdn::launch_kda_prep(pa, (int)n_chunk_slots(p), s);
+  if (e != cudaSuccess) return cuda_fail(e, "KDA prep launch");
+  // 2. segment summaries on [V | I] columns, as kda_segment_summary
+  gdn::SimtFwdArgs a{};
+  a.B = p->B;
+  a.T = p->T;
+  a.H = p->H;
+  a.scale = eff_scale(p);
+  a.use_exp2 = p->use_exp2;
+  a.seg_len = segment_len;
+  a.nseg = nseg;
+  a.dev_flag = flag;
+  a.S_ext = S_ext;
+  a.M = M;
+  a.summary = 1;
+  if ((e = gdn::launch_kda_chain(kda_chain_args(a, blob), dim3(4, p->H, p->B * nseg), s)) != cudaSuccess)
+    return cuda_fail(e, "segment summary launch");
+  // 3. ordered merge from h0, as kda_segment_merge (the final state comes from step 4)
+  gdn::MergeArgs ma{S_ext, M, h0, S_init, nullptr, p->B * p->H, nseg, 0};
+  if ((e = gdn::launch_merge(ma, s)) != cudaSuccess) return cuda_fail(e, "segment merge launch");
+  // 4. every segment from its merged entry state, as gdn_chunk_fwd with segment_len
+  a.S_ext = nullptr;
+  a.M = nullptr;
+  a.summary = 0;
+  a.h0 = S_init;
+  a.o = o;
+  a.ht = ht;
+  a.h_chunks = h_chunks;
+  if ((e = gdn::launch_kda_chain(kda_chain_args(a, blob), dim3(2, p->H, p->B * nseg), s)) != cudaSuccess)
+    return cuda_fail(e, "chunk forward launch");
+  return ok();
+}
+
+namespace {
 gdn_status check_frame(const frame_scan_problem *p, int *nseg) {
   if (!p) return fail(GDN_ERR_INVALID_ARGUMENT, "problem is NULL");
   if (p->BH < 1 || p->T < 1 || p->BH > 65535)

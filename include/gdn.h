@@ -291,6 +291,32 @@ gdn_status kda_segment_merge(const gdn_problem *p, const float *S_ext, const flo
                              int32_t nseg, const float *h0, float *S_init, float *ht,
                              void *stream);
 
+/* The whole split forward in one call, for bf16 inputs with a per-key gate in
+ * the BSND layout: the segment summaries (as kda_segment_summary), their ordered
+ * merge from h0 (as kda_segment_merge) and the corrected run of every segment from
+ * its merged entry state (as gdn_chunk_fwd with segment_len) -- the split of the
+ * long-context forward over the SMs on the state_summary.py and "Diff Coverage"
+ * pages (kda_split_state_summary_kernel, apply_kda_state_summary, the KDA state
+ * CP's forward). The chunk preparation (gated Gram matrices, the UT solve, w, u and
+ * the scaled operands) runs once and serves both passes, where the three calls run
+ * it twice; every output equals theirs bit for bit. All pointers device.
+ *   q, k, v, g, beta, o, g_cumsum, A, h_chunks : as for gdn_chunk_fwd
+ *                   (h_chunks in the BSND layout; g_cumsum, A, h_chunks nullable).
+ *   h0            : nullable fp32 [B, H, K, V], the state before the first segment.
+ *   segment_len   : a positive multiple of 64 (the last segment may be shorter).
+ *   ht            : nullable fp32 [B, H, K, V], the state after the last segment.
+ *   S_ext, M      : fp32 [B, H, nseg, K, V] and [B, H, nseg, K, K], the summaries.
+ *   S_init        : fp32 [B, H, nseg, K, V], the entry state of every segment.
+ *   ws, ws_bytes  : at least gdn_chunk_fwd_split_workspace bytes.
+ * Other dtypes, gate kinds and layouts return GDN_ERR_UNSUPPORTED (use the three
+ * calls); p->segment_len is ignored (the argument sets it). */
+gdn_status gdn_chunk_fwd_split_workspace(const gdn_problem *p, int32_t segment_len, size_t *bytes);
+gdn_status gdn_chunk_fwd_split(const gdn_problem *p, const void *q, const void *k, const void *v,
+                               const float *g, const void *beta, const float *h0,
+                               int32_t segment_len, void *o, float *ht, float *S_ext, float *M,
+                               float *S_init, float *g_cumsum, float *A, float *h_chunks, void *ws,
+                               size_t ws_bytes, void *stream);
+
 /* ---------------------------------------------------------------------------
  * Dense per-token transition scan (SANA, distributed_scan.py page:
  * cp_frame_gdn_scan and its local scan). For each of BH independent sequences of

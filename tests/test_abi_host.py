@@ -158,3 +158,31 @@ def test_frame_scan_contract_checks(lib):
         B.frame_scan_fwd(p, fake, fake, fake, fake, None, None, fake, fake, ws=fake, ws_bytes=need - 16,
                          stream=0)
     assert e.value.status == B.GDN_ERR_WORKSPACE
+
+
+def test_one_call_split_forward_contract_checks(lib):
+    # bf16 inputs with a per-key gate, BSND: the workspace is the preparation's blobs
+    fake = 4096
+    pk = dict(gate_kind=B.GDN_GATE_PER_KEY, use_exp2=True)
+    p = B.make_problem(2, 1000, 3, **pk)
+    need = B.gdn_chunk_fwd_split_workspace(p, 256)
+    assert need >= 2 * 16 * 3 * 64 * 128 * 2 * 4  # per chunk and head: w, u and the scaled operands
+    assert need == B.gdn_chunk_fwd_split_workspace(p, 512)  # one blob per chunk, whatever the split
+    for prob, seg, status in [
+        (B.make_problem(2, 1000, 3), 256, B.GDN_ERR_UNSUPPORTED),  # scalar gate
+        (B.make_problem(2, 1000, 3, dtype=B.GDN_DTYPE_F32, **pk), 256, B.GDN_ERR_UNSUPPORTED),
+        (p, 100, B.GDN_ERR_INVALID_ARGUMENT),
+        (p, 0, B.GDN_ERR_INVALID_ARGUMENT),
+    ]:
+        with pytest.raises(B.GdnError) as e:
+            B.gdn_chunk_fwd_split_workspace(prob, seg)
+        assert e.value.status == status
+    # pointers and the workspace are checked before any device work
+    a = [fake] * 5
+    with pytest.raises(B.GdnError) as e:
+        B.gdn_chunk_fwd_split(p, *a, None, 256, fake, None, fake, None, fake, ws=fake, ws_bytes=need, stream=0)
+    assert e.value.status == B.GDN_ERR_INVALID_ARGUMENT and "M must not be NULL" in str(e.value)
+    with pytest.raises(B.GdnError) as e:
+        B.gdn_chunk_fwd_split(p, *a, None, 256, fake, None, fake, fake, fake, ws=fake, ws_bytes=need - 16,
+                              stream=0)
+    assert e.value.status == B.GDN_ERR_WORKSPACE

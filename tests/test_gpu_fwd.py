@@ -195,6 +195,28 @@ def test_segment_summary_merge_and_correction(per_key):
     assert rel_frob(host(out["o"]), host(whole["o"])) <= TOL["bf16"]
 
 
+def test_one_call_split_forward_equals_the_three_calls():
+    """gdn_chunk_fwd_split (bf16, per-key gate) runs the chunk preparation once for both passes;
+    kda_segment_summary, kda_segment_merge and gdn_chunk_fwd with segment_len run the same
+    kernels on the same operands, so every output agrees bit for bit (ragged last segment,
+    initial state, every optional slot)."""
+    import torch
+    from gated_delta_rule_28_gb300 import workloads
+    inp = workloads.make(4, B=2, T=1000, H=2, with_h0=True)
+    d = to_dev(inp)
+    api = _api()
+    kw = dict(use_exp2=True, return_h_chunks=True, return_g_cumsum=True, return_A=True)
+    one = api.split_forward(d["q"], d["k"], d["v"], d["g"], d["beta"], 256, h0=d["h0"], **kw)
+    S, M = api.segment_summary(d["k"], d["v"], d["g"], d["beta"], 256, use_exp2=True)
+    S_init, _ = api.segment_merge(S, M, d["h0"])
+    three = api.chunk_gated_delta_rule_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], h0=S_init,
+                                           segment_len=256, **kw)
+    _status()
+    three.update(S_ext=S, M=M, S_init=S_init)
+    for name in ("o", "ht", "g_cumsum", "A", "h_chunks", "S_ext", "M", "S_init"):
+        assert torch.equal(one[name], three[name]), name
+
+
 def test_split_forward_with_input_maps():
     """Segment summaries, merge and corrected run on raw k (normalised) and raw beta
     (sigmoid), per-key base-2 gates, against the unsplit oracle on the mapped inputs."""
