@@ -304,28 +304,31 @@ __device__ __forceinline__ float lane16(const uint4 &u, int e) {
 // ---------------------------------------------------------------------------
 // local gradients, one CTA per (chunk, head), the value width in 8 slices
 constexpr int LBV = 16;
-constexpr int LVP = LBV + 1;
 
 // Row strides (floats) of the local kernel's shared-memory matrices, and its value-slice
 // width. The FMA path (fp32 inputs) pads rows by one float. The tensor-core path (bf16
-// inputs) reads mma fragments, lane (g, t) at row g and column t (or transposed), so its
-// strides are 4 mod 32: the row-major fragment reads then hit 32 distinct banks, the
-// transposed ones at most two lanes per bank. With a scalar gate it also takes value slices
-// of 32 columns (half the slice rounds).
+// inputs, per-key gate; a scalar gate with bf16 inputs runs on local_tc) reads mma
+// fragments, lane (g, t) at row g and column t (or transposed), so its strides are 4 mod 32:
+// the row-major fragment reads then hit 32 distinct banks, the transposed ones at most two
+// lanes per bank. It also keeps a region of xtra floats after A_qk's, so that A_qk's region
+// with it, and it with X's, each hold one 64 x 128 operand tile while A_qk's or X's
+// contents are not in use.
 template <typename T, bool PER_KEY>
 struct LocalStrides {
   static constexpr bool tc = !std::is_same<T, float>::value;
+  static_assert(!tc || PER_KEY, "bf16 inputs with a scalar gate run on local_tc");
   static constexpr int kp = tc ? GDN_DK + 4 : GDN_DK + 1;
   static constexpr int cp = tc ? GDN_CHUNK + 4 : GDN_CHUNK + 1;
-  static constexpr int lbv = (tc && !PER_KEY) ? 2 * LBV : LBV;
+  static constexpr int lbv = LBV;
   static constexpr int lvp = tc ? lbv + 4 : lbv + 1;
+  static constexpr int xtra = tc ? 64 * kp - 64 * cp + 128 : 0;
 };
 
 template <typename T, bool PER_KEY>
 constexpr size_t local_smem_floats() {
-  // K, Q, (G), X, P, Aqk, slice buffers, beta, dbeta, EL, dGLh, dGlast, dGrow
+  // K, Q, (G), P, Aqk, (extra), X, slice buffers, beta, dbeta, EL, dGLh, dGlast, dGrow, ...
   using S = LocalStrides<T, PER_KEY>;
-  return 2 * 64 * S::kp + (PER_KEY ? 64 * S::kp : 3 * 64) + 3 * 64 * S::cp +
+  return 2 * 64 * S::kp + (PER_KEY ? 64 * S::kp : 3 * 64) + 3 * 64 * S::cp + S::xtra +
          (2 * 128 * S::lvp + 6 * 64 * S::lvp) + 64 + 64 + 128 + 128 + 128 + 64 + 3 * 64 + 8 * 128 + 8;
 }
 
@@ -338,10 +341,14 @@ __global__ void __launch_bounds__(NTH, 1) local_kernel(BwdArgs a) {
   float *sK = smem;
   float *sQ = sK + 64 * KP;
   float *sG = sQ + 64 * KP;  // cumulative gate (scalar gate: + e^G, e^(Gl-G))
-  float *sX = sG + (PER_KEY ? 64 * KP : 3 * 64);
-  float *sP = sX + 64 * CP;     // gated K K^T (strict lower), later dP (.) Gamma
-  float *sAqk = sP + 64 * CP;   // gated Q K^T (lower incl), later dA_qk (.) Gamma
-  float *sSl = sAqk + 64 * CP;  // slice region
+  float *sP = sG + (PER_KEY ? 64 * KP : 3 * 64);  // gated K K^T (strict lower), later dP (.) Gamma
+  float *sAqk = sP + 64 * CP;   // dA_qk (.) Gamma (after the value pass)
+  float *sX = sAqk + 64 * CP + LS::xtra;
+  float *sSl = sX + 64 * CP;    // slice region
+  // tensor-core path: 64 x 128 operand tiles over A_qk's region and the extra floats (the
+  // Gram's right operand, then K (.) b^G during the value pass), and over the extra floats
+  // and X's region (the Gram adjoints' right operands, once X is no longer read)
+  float *sWideA = sAqk, *sWideB = sAqk + 64 * CP;
   float *sHs = sSl;                  // [128][LVP] h slice
   float *sDHs = sHs + 128 * LVP;     // [128][LVP] dh_{c+1} slice
   float *sVs = sDHs + 128 * LVP;     // [64][LVP]
@@ -504,8 +511,9 @@ __global__ void __launch_bounds__(NTH, 1) local_kernel(BwdArgs a) {
   // per-key gate on the tensor-core path: with one reference row r per chunk and
   // e_id = b^(G_id - G_rd), every gated product is a plain product of pre-scaled operands,
   //   sum_j M_ij x_jd b^(G_id - G_jd) = e_id sum_j M_ij (x_jd / e_jd),
-  // valid while every |G_id - G_rd| stays within 100 in base 2 (the factors stay inside the
-  // fp32 range); a chunk beyond that takes the term-by-term loops, exact for any gate range
+  // each scaled operand formed once in shared memory; valid while every |G_id - G_rd| stays
+  // within 100 in base 2 (the factors stay inside the fp32 range); a chunk beyond that takes
+  // the term-by-term loops, exact for any gate range
   constexpr int REFR = 32;
   const float l2b = e2 ? 1.f : 1.4426950408889634f;
   bool fast = false;
@@ -522,8 +530,6 @@ __global__ void __launch_bounds__(NTH, 1) local_kernel(BwdArgs a) {
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x * l2b));
     return y;
   };
-  auto EP = [&](int i, int d) { return bx(sG[i * KP + d] - sG[REFR * KP + d]); };
-  auto EM = [&](int i, int d) { return bx(sG[REFR * KP + d] - sG[i * KP + d]); };
 
   // ---- gated Gram matrix P = strictly-lower(K K^T (.) Gamma) ----------------------
   // (the gated Q K^T of the forward is not needed: dA_qk is formed from dO and v_new)
@@ -533,30 +539,21 @@ __global__ void __launch_bounds__(NTH, 1) local_kernel(BwdArgs a) {
     float accP[4][4];
     zero_acc(accP);
     bool in_tiles = true;
-    if constexpr (TC && !PER_KEY) {  // K K^T on tensor cores, then gated per element
-      constexpr int LD = GDN_CHUNK + 4;
-      float *st = sSl;  // [64][LD] staging, the slice region is not in use yet
-      float fP[4][4];
-      zero_acc(fP);
-      auto fk = [&](int m, int kk) { return sK[m * KP + kk]; };
-      auto fkt = [&](int kk, int nn) { return sK[nn * KP + kk]; };
-      mma_tf32_acc<GDN_DK, 4>(fk, fkt, fP, wr0, wc64, lane);
-      mma_frag_store(st, LD, fP, wr0, wc64, lane);
-      __syncthreads();
-#pragma unroll
-      for (int x = 0; x < 4; ++x)
-#pragma unroll
-        for (int y = 0; y < 4; ++y) {
-          const float gam = n0 + y <= m0 + x ? gate_pow(sG[m0 + x] - sG[n0 + y], e2) : 0.f;
-          accP[x][y] = st[(m0 + x) * LD + n0 + y] * gam;
-        }
-    } else {
-      if constexpr (TC && PER_KEY) {
+    {
+      if constexpr (TC) {
         if (fast) {  // (K (.) e)(K / e)^T on tensor cores, fragments straight into sP
+          float *tA = sSl, *tB = sWideA;  // [64][KP] each: K (.) e and K / e
+          for (int idx = tid; idx < 64 * GDN_DK; idx += NTH) {
+            const int i = idx >> 7, d = idx & 127;
+            const float kv = sK[i * KP + d], x = sG[i * KP + d] - sG[REFR * KP + d];
+            tA[i * KP + d] = kv * bx(x);
+            tB[i * KP + d] = kv * bx(-x);
+          }
+          __syncthreads();
           float fP[4][4];
           zero_acc(fP);
-          auto fa = [&](int m, int kk) { return sK[m * KP + kk] * EP(m, kk); };
-          auto fb = [&](int kk, int nn) { return sK[nn * KP + kk] * EM(nn, kk); };
+          auto fa = [&](int m, int kk) { return tA[m * KP + kk]; };
+          auto fb = [&](int kk, int nn) { return tB[nn * KP + kk]; };
           mma_tf32_acc<GDN_DK, 4>(fa, fb, fP, wr0, wc64, lane);
 #pragma unroll
           for (int j = 0; j < 4; ++j)
@@ -602,6 +599,13 @@ __global__ void __launch_bounds__(NTH, 1) local_kernel(BwdArgs a) {
     }
   }
   __syncthreads();
+  if constexpr (TC) {  // K (.) b^G, the left operand of the value pass's state product
+    for (int idx = tid; idx < 64 * GDN_DK; idx += NTH) {
+      const int i = idx >> 7, d = idx & 127;
+      sWideA[i * KP + d] = sK[i * KP + d] * bx(sG[i * KP + d]);
+    }
+    // (the first slice's barrier orders these stores before the product reads them)
+  }
 
   // ---- pass over value slices: accumulate the value contractions -----------
   // register tiles: 64x64 (4x4 per thread) and 64x128 (4x8 per thread)
@@ -687,7 +691,7 @@ __global__ void __launch_bounds__(NTH, 1) local_kernel(BwdArgs a) {
       const int zr0 = 16 * ((tid >> 5) & 3), zc0 = (LBV / 2) * (tid >> 7);
       float fz[NZ][4];
       zero_acc(fz);
-      auto fkg = [&](int m, int kk) { return sK[m * KP + kk] * (PER_KEY ? bx(sG[m * KP + kk]) : sG[64 + m]); };
+      auto fkg = [&](int m, int kk) { return sWideA[m * KP + kk]; };
       auto fhs = [&](int kk, int nn) { return sHs[kk * LVP + nn]; };
       mma_tf32_acc<GDN_DK, NZ>(fkg, fhs, fz, zr0, zc0, lane);
 #pragma unroll
@@ -921,7 +925,8 @@ __global__ void __launch_bounds__(NTH, 1) local_kernel(BwdArgs a) {
 #pragma unroll
     for (int y = 0; y < 8; ++y) {
       const int i = gm0 + x, d = gn0 + y;
-      const float eg = EG(i, d), egl = EGL(i, d);
+      const float eg = TC ? bx(sG[i * KP + d]) : EG(i, d);
+      const float egl = TC ? bx(sG[63 * KP + d] - sG[i * KP + d]) : EGL(i, d);
       const float kk = sK[i * KP + d], qq = sQ[i * KP + d];
       const float dQg = a.scale * aQg[x][y];
       rdq[x][y] = dQg * eg;
@@ -935,8 +940,11 @@ __global__ void __launch_bounds__(NTH, 1) local_kernel(BwdArgs a) {
     colGl[y] += __shfl_xor_sync(0xffffffffu, colGl[y], 16);
     if (lane < 16) sGlPart[(tid >> 5) * 128 + gn0 + y] = colGl[y];
   }
-  // Gram adjoints, one at a time: (dP K), (dP^T K), (dAqk K), (dAqk^T Q), with Gamma
-  for (int which = 0; which < 4; ++which) {
+  // Gram adjoints, one at a time: (dP K), (dAqk K), (dP^T K), (dAqk^T Q), with Gamma (in
+  // this order the tensor-core path forms its right operands K / e, K (.) e, Q (.) e once each)
+#pragma unroll 1
+  for (int step = 0; step < 4; ++step) {
+    const int which = step == 1 ? 2 : step == 2 ? 1 : step;
     const float *Mx = which < 2 ? sP : sAqk;
     const bool tr = which == 1 || which == 3;  // use M^T
     const float *Op = which == 3 ? sQ : sK;
@@ -962,32 +970,24 @@ __global__ void __launch_bounds__(NTH, 1) local_kernel(BwdArgs a) {
         }
       }
     };
-    if constexpr (TC && !PER_KEY) {
-      // the gate is already folded into the 64 x 64 matrix: a plain product, on tf32 tensor
-      // cores, moved into the thread tile through the slice region
-      constexpr int LD = GDN_DK + 4;
-      float *st = sSl;
-      float fr[8][4];
-      zero_acc(fr);
-      auto fm = [&](int m, int kk) { return tr ? Mx[kk * CP + m] : Mx[m * CP + kk]; };
-      auto fop = [&](int kk, int nn) { return Op[kk * KP + nn]; };
-      mma_tf32_acc<GDN_CHUNK, 8>(fm, fop, fr, wr0, wc128, lane);
-      mma_frag_store(st, LD, fr, wr0, wc128, lane);
-      __syncthreads();
-#pragma unroll
-      for (int x = 0; x < 4; ++x)
-#pragma unroll
-        for (int y = 0; y < 8; ++y) t[x][y] = st[(gm0 + x) * LD + gn0 + y];
-      __syncthreads();
-    } else if constexpr (TC && PER_KEY) {
+    if constexpr (TC) {
       if (fast) {
         // (M or M^T)(Op (.) e^-+1) on tf32 tensor cores, then the row factor e^+-1 of (i, d)
         constexpr int LD = GDN_DK + 4;
         float *st = sSl;
+        float *tB = sWideB;  // [64][KP], the right operand (X's region is free by now)
+        if (step != 1) {
+          for (int idx = tid; idx < 64 * GDN_DK; idx += NTH) {
+            const int j = idx >> 7, d = idx & 127;
+            const float x = sG[j * KP + d] - sG[REFR * KP + d];
+            tB[j * KP + d] = Op[j * KP + d] * bx(tr ? x : -x);
+          }
+          __syncthreads();
+        }
         float fr[8][4];
         zero_acc(fr);
         auto fm = [&](int m, int kk) { return tr ? Mx[kk * CP + m] : Mx[m * CP + kk]; };
-        auto fop = [&](int kk, int nn) { return Op[kk * KP + nn] * (tr ? EP(kk, nn) : EM(kk, nn)); };
+        auto fop = [&](int kk, int nn) { return tB[kk * KP + nn]; };
         mma_tf32_acc<GDN_CHUNK, 8>(fm, fop, fr, wr0, wc128, lane);
         mma_frag_store(st, LD, fr, wr0, wc128, lane);
         __syncthreads();
@@ -996,7 +996,8 @@ __global__ void __launch_bounds__(NTH, 1) local_kernel(BwdArgs a) {
 #pragma unroll
           for (int y = 0; y < 8; ++y) {
             const int i = gm0 + x, d = gn0 + y;
-            t[x][y] = st[i * LD + d] * (tr ? EM(i, d) : EP(i, d));
+            const float xi = sG[i * KP + d] - sG[REFR * KP + d];
+            t[x][y] = st[i * LD + d] * bx(tr ? -xi : xi);
           }
         __syncthreads();
       } else {
@@ -1122,7 +1123,10 @@ cudaError_t launch_bwd_dhu(const BwdArgs &a, bool per_key, bool bf16, cudaStream
 }
 
 cudaError_t launch_bwd_local(const BwdArgs &a, bool per_key, bool bf16, cudaStream_t st) {
-  if (bf16) return per_key ? local_one<__nv_bfloat16, true>(a, st) : local_one<__nv_bfloat16, false>(a, st);
+  if (bf16) {  // a scalar gate with bf16 inputs runs on local_tc (launch_bwd_local_tc)
+    if (!per_key) return cudaErrorNotSupported;
+    return local_one<__nv_bfloat16, true>(a, st);
+  }
   return per_key ? local_one<float, true>(a, st) : local_one<float, false>(a, st);
 }
 
