@@ -13,7 +13,7 @@
 //
 // One CTA (512 threads) owns one run of one head and 64 of the 128 value
 // columns; dh lives in fp32 registers of the chain warps 0..7, which run
-//   D1   [kgl; -] dh^T-operand  accumulated onto  scale A_qk^T dO   -> dv_new
+//   D1   [kgl; -] dh            accumulated onto  scale A_qk^T dO   -> dv_new
 //   D2   -w^T dv_new            accumulated onto  scale Qg^T dO     -> dh update
 // while the producer warps 8..15 prepare the previous chunk: A_qk^T (from
 // [Q; K] Q^T and the gate), the three h-independent products scale A_qk^T dO,
@@ -54,8 +54,8 @@ constexpr int OFF_AQT = OFF_DOT + 8192;       // A_qk^T rows 0..63 (rows 64..127
 constexpr int OFF_QGT = OFF_AQT + 8192;       // (scale base^G Q)^T   128 rows
 constexpr int OFF_KGL = OFF_QGT + 16384;      // kgl, 2 K-blocks of 64 rows
 constexpr int OFF_WT = OFF_KGL + 16384;       // w^T, 128 rows
-constexpr int OFF_DHT = OFF_WT + 16384;       // dh^T, 2 K-blocks x 64 rows
-constexpr int OFF_DVT = OFF_DHT + 16384;      // dv_new^T, 64 rows
+constexpr int OFF_DHT = OFF_WT + 16384;       // dh: 128 key rows (MN-major B of D1)
+constexpr int OFF_DVT = OFF_DHT + 16384;      // dv_new: 64 token rows (MN-major B of D2)
 constexpr int OFF_SMALL = OFF_DVT + 8192;
 constexpr int SMALL_BYTES = 6144;
 // gates of the four diagonal 16x16 blocks, gdn[b][x][y] = base^(G_{16b+x} - G_{16b+y}) for
@@ -85,13 +85,6 @@ static_assert(sizeof(BwState) <= SMALL_BYTES, "small state");
 
 __device__ __forceinline__ void chain_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
 __device__ __forceinline__ void prod_sync() { asm volatile("bar.sync 2, 256;" ::: "memory"); }
-__device__ __forceinline__ void sts_u16(uint32_t addr, uint16_t v) {
-  asm volatile("st.shared.u16 [%0], %1;" ::"r"(addr), "h"(v) : "memory");
-}
-__device__ __forceinline__ uint16_t bf16_bits(float x) {
-  const __nv_bfloat16 b = __float2bfloat16_rn(x);
-  return *reinterpret_cast<const uint16_t *>(&b);
-}
 
 // TMA maps: q, k, dO over [rows, H*128] and X over [slots*H*64, 64], 64 x 64 boxes
 struct BwdMaps {
@@ -354,11 +347,10 @@ __global__ void __launch_bounds__(NTH, 1) tc_dhu_kernel(BwdArgs a, const __grid_
 #pragma unroll
     for (int j = 0; j < 32; ++j) dh[j] = src ? src[j] : 0.f;
   }
-  auto write_dht = [&]() {  // dh^T (B operand of D1): key `row`, columns 32*hc .. +32
-    const uint32_t hbase = sb + OFF_DHT + (row >> 6) * 8192 + (row & 7) * 2;
-    const int kc = (row & 63) >> 3;
+  auto write_dht = [&]() {  // dh (MN-major B operand of D1): key `row`, columns 32*hc .. +32
 #pragma unroll
-    for (int j = 0; j < 32; ++j) sts_u16(hbase + chunk_off(32 * hc + j, kc), bf16_bits(dh[j]));
+    for (int q8 = 0; q8 < 4; ++q8)
+      *reinterpret_cast<uint4 *>(sm + OFF_DHT + chunk_off(row, 4 * hc + q8)) = pack8(dh + 8 * q8);
   };
   auto chain = [&](int64_t m) {
     const int cs = (int)(m & 1);
@@ -377,13 +369,13 @@ __global__ void __launch_bounds__(NTH, 1) tc_dhu_kernel(BwdArgs a, const __grid_
     }
     if (warp == 0) {  // D1: dv_new = kgl dh + scale A_qk^T dO
       fence_after_sync();
-      mma_tiles_w(tmem + T_I1 + 64 * cs, sb + OFF_KGL, 8192, sb + OFF_DHT, 8192, 128, idesc_bf16(128, 64), true);
+      mma_ops_w(tmem + T_I1 + 64 * cs, kmaj(sb + OFF_KGL, 8192), mnmaj(sb + OFF_DHT, 0), 128,
+                idesc_bf16(128, 64, false, false, true), true);
       mma_commit_w(&st.bar_d1);
     }
     __syncwarp();
     wait_par(&st.bar_d1, m);
-    if (q4 < 2) {  // dv_new rows: fp32 to the workspace, bf16 into dv_new^T
-      const uint32_t base = sb + OFF_DVT + (row & 7) * 2;
+    if (q4 < 2) {  // dv_new rows: fp32 to the workspace, bf16 into D2's operand
       const bool valid = row < n;
       float4 *gdst = reinterpret_cast<float4 *>(a.dvnew + ((c0 + (valid ? row : 0)) * H + h) * GDN_DV + col0 + 32 * hc);
 #pragma unroll
@@ -401,8 +393,8 @@ __global__ void __launch_bounds__(NTH, 1) tc_dhu_kernel(BwdArgs a, const __grid_
           for (int g4 = 0; g4 < 4; ++g4)
             gdst[4 * part + g4] = make_float4(dv[4 * g4], dv[4 * g4 + 1], dv[4 * g4 + 2], dv[4 * g4 + 3]);
         }
-#pragma unroll
-        for (int j = 0; j < 16; ++j) sts_u16(base + chunk_off(32 * hc + 16 * part + j, row >> 3), bf16_bits(dv[j]));
+        *reinterpret_cast<uint4 *>(sm + OFF_DVT + chunk_off(row, 4 * hc + 2 * part)) = pack8(dv);
+        *reinterpret_cast<uint4 *>(sm + OFF_DVT + chunk_off(row, 4 * hc + 2 * part + 1)) = pack8(dv + 8);
       }
     }
     fence_proxy_async();
@@ -410,27 +402,23 @@ __global__ void __launch_bounds__(NTH, 1) tc_dhu_kernel(BwdArgs a, const __grid_
     chain_sync();
     if (warp == 0) {  // D2: dh increment = scale Qg^T dO - w^T dv_new
       fence_after_sync();
-      mma_tiles_w(tmem + T_I2 + 64 * cs, sb + OFF_WT, 16384, sb + OFF_DVT, 8192, 64, idesc_bf16(128, 64, true), true);
+      mma_ops_w(tmem + T_I2 + 64 * cs, kmaj(sb + OFF_WT, 16384), mnmaj(sb + OFF_DVT, 0), 64,
+                idesc_bf16(128, 64, true, false, true), true);
       mma_commit_w(&st.bar_d2);
     }
     __syncwarp();
     wait_par(&st.bar_d2, m);
     {
       const float el = st.EL[cs];
-      const uint32_t hbase = sb + OFF_DHT + (row >> 6) * 8192 + (row & 7) * 2;
-      const int kc = (row & 63) >> 3;
 #pragma unroll
       for (int part = 0; part < 2; ++part) {
         float inc[16];
         tmem_ld16(tl + T_I2 + 64 * cs + 32 * hc + 16 * part, inc);
         tmem_ld_wait();
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          float &d = dh[16 * part + j];
-          d = fmaf(el, d, inc[j]);
-          sts_u16(hbase + chunk_off(32 * hc + 16 * part + j, kc), bf16_bits(d));
-        }
+        for (int j = 0; j < 16; ++j) dh[16 * part + j] = fmaf(el, dh[16 * part + j], inc[j]);
       }
+      write_dht();
     }
     fence_proxy_async();
     fence_before_sync();
