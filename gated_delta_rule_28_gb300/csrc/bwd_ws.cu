@@ -17,8 +17,8 @@
 //   D2   -w^T dv_new            accumulated onto  scale Qg^T dO     -> dh update
 // while the producer warps 8..15 prepare the previous chunk: A_qk^T (from
 // [Q; K] Q^T and the gate), the three h-independent products scale A_qk^T dO,
-// scale Qg^T dO and w^T (= K^T (X diag(beta base^G))^T, the stage's K read as an
-// MN-major operand), and the operands kgl and w^T. X diag(beta base^G) and the
+// scale Qg^T dO = Q^T (diag(scale base^G) dO) and w^T (= K^T (X diag(beta base^G))^T),
+// with Q, K and dO read in place as MN-major operands, and the operands kgl and w^T. X diag(beta base^G) and the
 // per-token gate factors come from the UT transform kernel.
 // Loads are TMA copies completing on mbarriers.
 // It writes dh of every chunk (the exit-state gradient) and dv_new in fp32
@@ -48,11 +48,11 @@ constexpr int SZ_STAGE = 32768;               // [Q; K]: 2 K-blocks x 128 rows
 constexpr int OFF_ST = 0;                     // 2 stages
 constexpr int OFF_X0 = OFF_ST + 2 * SZ_STAGE; // X diag(beta base^G) of even-order chunks (64 rows)
 constexpr int OFF_X1 = OFF_X0 + 8192;
-constexpr int OFF_DO = OFF_X1 + 8192;         // dO slice, natural (64 rows, one buffer)
-constexpr int OFF_DOT = OFF_DO + 8192;        // dO^T (64 value rows)
-constexpr int OFF_AQT = OFF_DOT + 8192;       // A_qk^T rows 0..63 (rows 64..127 of the operand: QGT)
-constexpr int OFF_QGT = OFF_AQT + 8192;       // (scale base^G Q)^T   128 rows
-constexpr int OFF_KGL = OFF_QGT + 16384;      // kgl, 2 K-blocks of 64 rows
+constexpr int OFF_DO = OFF_X1 + 8192;         // dO slice per order parity: 64 token rows (MN-major B)
+constexpr int OFF_DOS = OFF_DO + 2 * 8192;    // diag(scale base^G) dO: 64 token rows (MN-major B)
+constexpr int OFF_AQT = OFF_DOS + 8192;       // A_qk^T rows 0..63 (rows 64..127 of the operand: kgl's,
+                                              // whose output rows are not read)
+constexpr int OFF_KGL = OFF_AQT + 8192;       // kgl, 2 K-blocks of 64 rows
 constexpr int OFF_WT = OFF_KGL + 16384;       // w^T, 128 rows
 constexpr int OFF_DHT = OFF_WT + 16384;       // dh: 128 key rows (MN-major B of D1)
 constexpr int OFF_DVT = OFF_DHT + 16384;      // dv_new: 64 token rows (MN-major B of D2)
@@ -78,7 +78,7 @@ struct BwState {
   float seg[2][64];                 // scale base^G
   float EL[2];
   uint64_t bar_p1, bar_p3, bar_d1, bar_d2, bar_x0, bar_x1;
-  uint64_t bar_ld[2], bar_do;  // TMA loads: order parity (Q, K, X, factors) and dO
+  uint64_t bar_ld[2], bar_do[2];  // TMA loads per order parity: Q, K, X, factors; dO
   uint32_t tmem;
 };
 static_assert(sizeof(BwState) <= SMALL_BYTES, "small state");
@@ -106,9 +106,6 @@ __global__ void __launch_bounds__(NTH, 1) tc_dhu_kernel(BwdArgs a, const __grid_
   const int H = a.H, h = blockIdx.y, z = blockIdx.z;
   const int col0 = blockIdx.x * TBV;
   const float scale = a.scale;
-  const __nv_bfloat16 *q = static_cast<const __nv_bfloat16 *>(a.q);
-  const __nv_bfloat16 *k = static_cast<const __nv_bfloat16 *>(a.k);
-  const __nv_bfloat16 *dO = static_cast<const __nv_bfloat16 *>(a.dO);
 
   // ---- the run: chunk slots as the forward (X workspace: xbase + c; states: slot()) ----
   int64_t r0, r1, chunk_base = 0, xbase;
@@ -165,7 +162,8 @@ __global__ void __launch_bounds__(NTH, 1) tc_dhu_kernel(BwdArgs a, const __grid_
     mbar_init(&st.bar_x1, 1);
     mbar_init(&st.bar_ld[0], 1);
     mbar_init(&st.bar_ld[1], 1);
-    mbar_init(&st.bar_do, 1);
+    mbar_init(&st.bar_do[0], 1);
+    mbar_init(&st.bar_do[1], 1);
     mbar_fence_init();
   }
   fence_before_sync();
@@ -185,7 +183,7 @@ __global__ void __launch_bounds__(NTH, 1) tc_dhu_kernel(BwdArgs a, const __grid_
   // beta = 0 removes them from w.
   const int ptid = tid - 256;
   const bool loader = warp == 9;  // TMA loads, issued warp-collectively (tc.cuh)
-  int64_t last_ld[2] = {-1, -1}, last_do = -1;  // loader: newest order index per barrier
+  int64_t last_ld[2] = {-1, -1}, last_do[2] = {-1, -1};  // loader: newest order index per barrier
   auto issue_qkx = [&](int64_t m) {  // Q, K, X and the gate table of order index m
     const int64_t c = chunk_of(m);
     const int s2 = (int)(m & 1);
@@ -205,9 +203,10 @@ __global__ void __launch_bounds__(NTH, 1) tc_dhu_kernel(BwdArgs a, const __grid_
   };
   auto issue_do = [&](int64_t m) {  // the CTA's 64 columns of dO
     const int64_t c = chunk_of(m);
-    mbar_expect_tx_w(&st.bar_do, 8192);
-    tma_load_2d_w(sb + OFF_DO, &maps.dO, h * GDN_DV + col0, (int)(r0 + c * GDN_CHUNK), &st.bar_do);
-    last_do = m;
+    const int s2 = (int)(m & 1);
+    mbar_expect_tx_w(&st.bar_do[s2], 8192);
+    tma_load_2d_w(sb + OFF_DO + s2 * 8192, &maps.dO, h * GDN_DV + col0, (int)(r0 + c * GDN_CHUNK), &st.bar_do[s2]);
+    last_do[s2] = m;
   };
 
   // ---- producer: one chunk (order index pm) ------------------------------------------------
@@ -216,7 +215,10 @@ __global__ void __launch_bounds__(NTH, 1) tc_dhu_kernel(BwdArgs a, const __grid_
     const uint32_t stg = sb + OFF_ST + ps * SZ_STAGE;
     const float(&tab)[F_ROWS][64] = st.tab[ps];
     const int n = chunk_rows(chunk_of(pm));
-    if (loader && pm + 1 < nch) issue_qkx(pm + 1);
+    if (loader && pm + 1 < nch) {  // the other buffers were last read by chunk pm - 1's products
+      issue_qkx(pm + 1);
+      issue_do(pm + 1);
+    }
     wait_par(&st.bar_ld[ps], pm >> 1);  // Q, K, X and factors of this chunk have landed
     if (ptid == 0) st.EL[ps] = tab[F_EG][63];
     if (warp == 8) {  // P1: [Q; K] Q^T (rows 64..127 = K Q^T), issued warp-collectively
@@ -235,33 +237,23 @@ __global__ void __launch_bounds__(NTH, 1) tc_dhu_kernel(BwdArgs a, const __grid_
         gdn[b * GD_B + x * 16 + y] = x >= y ? v : 0.f;
       }
     }
-    // transposes: Q -> (scale base^G Q)^T; dO -> dO^T
+    // diag(scale base^G) dO (zero past the chunk end): the right operand of Qg^T dO
+    wait_par(&st.bar_do[ps], pm >> 1);  // dO of this chunk
     {
-      const int pw = warp - 8;
-      uint32_t xq[4][4], xd[2][4];
+      const int r = ptid >> 2;
+      const uint8_t *src = sm + OFF_DO + ps * 8192;
+      const float f = st.seg[ps][r];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int jb = pw + 8 * i, rb = jb >> 3, fb = jb & 7;
-        trans16_load(stg + (fb >> 2) * 16384, rb * 16, (fb & 3) * 2, lane, xq[i]);
-      }
-      wait_par(&st.bar_do, pm);  // dO of this chunk
+      for (int q2 = 0; q2 < 2; ++q2) {
+        const int c16 = 2 * (ptid & 3) + q2;
+        float x[8];
+        unpack8(*reinterpret_cast<const uint4 *>(src + chunk_off(r, c16)), x);
 #pragma unroll
-      for (int i = 0; i < 2; ++i) {
-        const int t = pw + 8 * i, rb = t >> 2, cb = t & 3;
-        trans16_load(sb + OFF_DO, rb * 16, cb * 2, lane, xd[i]);
-      }
-#pragma unroll
-      for (int i = 0; i < 2; ++i) {
-        const int t = pw + 8 * i, rb = t >> 2, cb = t & 3;
-        trans16_store(sb + OFF_DOT, cb * 16, rb * 16, xd[i], nullptr, lane);
-      }
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int jb = pw + 8 * i, rb = jb >> 3, fb = jb & 7;
-        trans16_store(sb + OFF_QGT, fb * 16, rb * 16, xq[i], st.seg[ps], lane);
+        for (int e = 0; e < 8; ++e) x[e] *= f;
+        *reinterpret_cast<uint4 *>(sm + OFF_DOS + chunk_off(r, c16)) = pack8(x);
       }
     }
-    prod_sync();  // dO consumed (the next chunk's is loaded after the product issue)
+    prod_sync();  // the gate table is complete
     // gating of K Q^T (rows 64..127 of S): A_qk^T[s][t] = scale (k_s . q_t) base^(G_t - G_s),
     // s <= t < n; gate factors from tables as in the forward, formed while P1 may still run.
     float gf[32];
@@ -296,16 +288,17 @@ __global__ void __launch_bounds__(NTH, 1) tc_dhu_kernel(BwdArgs a, const __grid_
     if (warp == 8) {  // the h-independent products
       fence_after_sync();
       const uint32_t xt = sb + (ps ? OFF_X1 : OFF_X0);
-      // scale A_qk^T dO  (rows 64..127 of the operand are not used)
-      mma_tiles_w(tmem + T_I1 + 64 * ps, sb + OFF_AQT, 8192, sb + OFF_DOT, 8192, 64, idesc_bf16(128, 64), false);
-      // scale Qg^T dO
-      mma_tiles_w(tmem + T_I2 + 64 * ps, sb + OFF_QGT, 16384, sb + OFF_DOT, 8192, 64, idesc_bf16(128, 64), false);
+      // scale A_qk^T dO  (rows 64..127 of the operand are not used); dO read as an MN-major B
+      mma_ops_w(tmem + T_I1 + 64 * ps, kmaj(sb + OFF_AQT, 8192), mnmaj(sb + OFF_DO + ps * 8192, 0), 64,
+                idesc_bf16(128, 64, false, false, true), false);
+      // scale Qg^T dO = Q^T (diag(scale base^G) dO): the stage's Q rows read as an MN-major A
+      mma_ops_w(tmem + T_I2 + 64 * ps, mnmaj(stg, 16384), mnmaj(sb + OFF_DOS, 0), 64,
+                idesc_bf16(128, 64, false, true, true), false);
       // w^T = K^T (X diag(beta base^G))^T: the stage's K rows read as an MN-major A
       mma_ops_w(tmem + T_WT, mnmaj(stg + 8192, 16384), kmaj(xt, 0), 64, idesc_bf16(128, 64, false, true, false), false);
       mma_commit_w(&st.bar_p3);
     }
     __syncwarp();
-    if (loader && pm + 1 < nch) issue_do(pm + 1);  // dO consumed by the transposes
     // kgl rows (K rows scaled by base^(G_last - G)) once the chain's D1 has read the previous ones
     if (m_chain >= 0) wait_par(&st.bar_d1, m_chain);
     if (q4 >= 2) {
@@ -378,9 +371,9 @@ __global__ void __launch_bounds__(NTH, 1) tc_dhu_kernel(BwdArgs a, const __grid_
     if (q4 < 2) {  // dv_new rows: fp32 to the workspace, bf16 into D2's operand
       const bool valid = row < n;
       float4 *gdst = reinterpret_cast<float4 *>(a.dvnew + ((c0 + (valid ? row : 0)) * H + h) * GDN_DV + col0 + 32 * hc);
-#pragma unroll
       uint8_t *dvt = a.dv_tiles ? reinterpret_cast<uint8_t *>(a.dv_tiles + state_slot(c) * DV_TILE) + (col0 >> 6) * 8192
                                 : nullptr;
+#pragma unroll
       for (int part = 0; part < 2; ++part) {
         float dv[16];
         tmem_ld16(tl + T_I1 + 64 * cs + 32 * hc + 16 * part, dv);
@@ -457,7 +450,8 @@ __global__ void __launch_bounds__(NTH, 1) tc_dhu_kernel(BwdArgs a, const __grid_
     if (loader) {  // copies still in flight land before the CTA leaves
       for (int s2 = 0; s2 < 2; ++s2)
         if (last_ld[s2] >= 0) mbar_wait(&st.bar_ld[s2], (uint32_t)((last_ld[s2] >> 1) & 1), WAIT_LIMIT);
-      if (last_do >= 0) mbar_wait(&st.bar_do, (uint32_t)(last_do & 1), WAIT_LIMIT);
+      for (int s2 = 0; s2 < 2; ++s2)
+        if (last_do[s2] >= 0) mbar_wait(&st.bar_do[s2], (uint32_t)((last_do[s2] >> 1) & 1), WAIT_LIMIT);
     }
   } else if (!producer && a.dh0) {
     float4 *dst = reinterpret_cast<float4 *>(a.dh0 + state_off + (int64_t)row * GDN_DV + col0 + 32 * hc);
