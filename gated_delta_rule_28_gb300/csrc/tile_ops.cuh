@@ -60,54 +60,6 @@ __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
                : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
                : "r"(addr));
 }
-__device__ __forceinline__ void stsm_x4(uint32_t addr, const uint32_t (&r)[4]) {
-  asm volatile("stmatrix.sync.aligned.m8n8.x4.shared.b16 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(r[0]),
-               "r"(r[1]), "r"(r[2]), "r"(r[3])
-               : "memory");
-}
-
-// Transposes one 16x16 bf16 block with one warp: source rows s0..s0+15 and
-// columns 8*c0 .. 8*c0+15 of a swizzled tile (`src` is the
-// address of the K-block holding those columns) become rows d0..d0+15 of the
-// destination, columns s0..s0+15 (inside the destination K-block given), each
-// element multiplied by fac[source row] when fac is given.
-struct TransJob {
-  uint32_t src;       // address of the source tile's K-block holding chunk c0
-  int s0, c0;         // first source row; first source chunk (even, within the K-block)
-  uint32_t dst;       // address of the destination tile's K-block holding column s0
-  int d0;             // first destination row
-};
-// The two halves of a transpose, so that a warp can issue the shared-memory
-// loads of several blocks before their stores: load the 16x16 block at source
-// rows s0.. and chunks c0, c0+1 of `src`; store it (scaled by fac[source row]
-// when fac is given) as rows d0..d0+15 of `dst`, columns s0..s0+15.
-__device__ __forceinline__ void trans16_load(uint32_t src, int s0, int c0, int lane, uint32_t (&x)[4]) {
-  const int m = lane >> 3, r = lane & 7;
-  ldsm_x4_trans(src + chunk_off(s0 + r + 8 * (m & 1), c0 + (m >> 1)), x);
-}
-__device__ __forceinline__ void trans16_store(uint32_t dst, int d0, int s0, const uint32_t (&x)[4],
-                                              const float *fac, int lane) {
-  const int m = lane >> 3, r = lane & 7;
-  uint32_t y[4];
-  // register i of this thread holds destination (row lane/4, columns 2(lane%4), +1) of
-  // matrix i, i.e. source rows s0 + 8*(i&1) + 2(lane%4) + {0, 1}
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    if (fac) {
-      const int srow = s0 + 8 * (i & 1) + 2 * (lane & 3);
-      const float2 t = unpack_bf16(x[i]);
-      y[i] = pack_bf16(t.x * fac[srow], t.y * fac[srow + 1]);
-    } else {
-      y[i] = x[i];
-    }
-  }
-  stsm_x4(dst + chunk_off(d0 + r + 8 * (m >> 1), ((s0 & 63) >> 3) + (m & 1)), y);
-}
-__device__ __forceinline__ void trans16(const TransJob &j, const float *fac, int lane) {
-  uint32_t x[4];
-  trans16_load(j.src, j.s0, j.c0, lane, x);
-  trans16_store(j.dst, j.d0, j.s0, x, fac, lane);
-}
 
 // --- blocked 64x64 fp32 matrices for the solve ------------------------------------------
 __device__ __forceinline__ int blk(int bi, int bj) { return bi * (bi + 1) / 2 + bj; }
