@@ -108,6 +108,7 @@ struct FwdMaps {
 // Polls until the phase of `parity` has completed; false once `limit` polls ran out or
 // (checked every 256 polls) the CTA's abort word is set.
 __device__ __forceinline__ bool poll(uint64_t *bar, uint32_t parity, const volatile int *abort) {
+#pragma unroll 1
   for (uint32_t i = 0; i < WAIT_LIMIT; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((i & 255u) == 255u && *abort) return false;
