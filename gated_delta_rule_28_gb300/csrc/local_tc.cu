@@ -187,8 +187,23 @@ __global__ void __launch_bounds__(NTH, 1) local_tc_kernel(BwdArgs a) {
   }
   auto row_of = [&](int i) { return (c0 + i) * H + h; };
 
-  // ---- loads, all by cp.async: K, Q, V, dO (zero past the end) and the bf16 tiles of h, dh
-  // and dN written by the recompute and the reverse recurrence (already in this layout) ------
+  // ---- loads: the gate, beta and X (rows past the end: identity) into registers first, so
+  // that they do not queue behind the tiles; then K, Q, V, dO (zero past the end) and the bf16
+  // tiles of h, dh and dN written by the recompute and the reverse recurrence (already in this
+  // layout), all by cp.async ---------------------------------------------------------------
+  float G_t = 0.f, beta_t = 0.f;
+  if (tid < 64) {
+    G_t = a.g_cumsum[row_of(min(tid, n - 1))];
+    if (tid < n) beta_t = __bfloat162float(beta[row_of(tid)]);
+  }
+  float4 xr[2][2];  // X row x >> 3, columns 8 (x & 7) .. +7, for x = tid, tid + 256
+#pragma unroll
+  for (int u = 0; u < 2; ++u) {
+    const int x = tid + u * NTH, r = x >> 3, c8 = x & 7;
+    const float4 *src = reinterpret_cast<const float4 *>(a.A + row_of(r < n ? r : 0) * GDN_CHUNK + 8 * c8);
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) xr[u][hh] = r < n ? __ldg(src + hh) : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
   for (int x = tid; x < 1024; x += NTH) {
     const int r = x >> 4, c16 = x & 15;
     const bool valid = r < n;
@@ -211,22 +226,23 @@ __global__ void __launch_bounds__(NTH, 1) local_tc_kernel(BwdArgs a) {
   }
   cp_async_commit();
   if (tid < 64) {
-    const int i = tid;
-    const float G = a.g_cumsum[row_of(min(i, n - 1))];
-    sv.G[i] = G;
-    sv.beta[i] = i < n ? __bfloat162float(beta[row_of(i)]) : 0.f;
-    sv.gam[i] = gexp<E2>(G);
+    sv.G[tid] = G_t;
+    sv.beta[tid] = beta_t;
+    sv.gam[tid] = gexp<E2>(G_t);
   }
   __syncthreads();  // beta and the gate of every row are in place
   if (tid < 64) sv.lam[tid] = gexp<E2>(sv.G[63] - sv.G[tid]);
   // X (rows i, columns j; identity outside the chunk) and X diag(beta)
-  for (int x = tid; x < 64 * 8; x += NTH) {
-    const int r = x >> 3, c8 = x & 7;
+#pragma unroll
+  for (int u = 0; u < 2; ++u) {
+    const int x = tid + u * NTH, r = x >> 3, c8 = x & 7;
+    const float raw[8] = {xr[u][0].x, xr[u][0].y, xr[u][0].z, xr[u][0].w,
+                          xr[u][1].x, xr[u][1].y, xr[u][1].z, xr[u][1].w};
     float xv[8], xb[8];
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
       const int j = 8 * c8 + e;
-      xv[e] = (r < n && j < n) ? a.A[row_of(r) * GDN_CHUNK + j] : (r == j ? 1.f : 0.f);
+      xv[e] = (r < n && j < n) ? raw[e] : (r == j ? 1.f : 0.f);
       xb[e] = xv[e] * sv.beta[j];
     }
     *reinterpret_cast<uint4 *>(sm + (toff(tX, r, c8) - sb)) = pack8(xv);
@@ -495,16 +511,25 @@ __global__ void __launch_bounds__(NTH, 1) local_tc_kernel(BwdArgs a) {
   if (lane == 0) sv.gl[warp] = plast;
   if (tid < 64 && tid < n) dbeta[row_of(tid)] = __float2bfloat16_rn(dbeta_row);
   __syncthreads();
-  if (tid == 0) {
+  if (warp == 0) {  // the reverse cumulative sum over the chunk's rows, two rows per lane
     float extra = 0.f;
 #pragma unroll
     for (int w = 0; w < 8; ++w) extra += sv.gl[w];
     extra += lnb * gexp<E2>(sv.G[63]) * hdh_all;
-    float run = 0.f;
-    for (int i = n - 1; i >= 0; --i) {
-      run += sv.part[0][i] + sv.part[1][i] + (i == n - 1 ? extra : 0.f);
-      a.dg[row_of(i)] = run;
+    const int i0 = 2 * lane, i1 = i0 + 1;
+    const float x0 = i0 < n ? sv.part[0][i0] + sv.part[1][i0] + (i0 == n - 1 ? extra : 0.f) : 0.f;
+    const float x1 = i1 < n ? sv.part[0][i1] + sv.part[1][i1] + (i1 == n - 1 ? extra : 0.f) : 0.f;
+    float incl = x0 + x1;  // then: the sum over the rows of this lane and every later lane
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const float y = __shfl_down_sync(0xffffffffu, incl, off);
+      if (lane + off < 32) incl += y;
     }
+    float later = __shfl_down_sync(0xffffffffu, incl, 1);
+    if (lane == 31) later = 0.f;
+    const float run1 = x1 + later;
+    if (i1 < n) a.dg[row_of(i1)] = run1;
+    if (i0 < n) a.dg[row_of(i0)] = x0 + run1;
   }
 }
 
