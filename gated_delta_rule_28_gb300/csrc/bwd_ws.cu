@@ -350,10 +350,12 @@ __global__ void __launch_bounds__(NTH, 1) tc_dhu_kernel(BwdArgs a, const __grid_
     const int64_t c = chunk_of(m);
     const int64_t c0 = r0 + c * GDN_CHUNK;
     const int n = chunk_rows(c);
-    if (a.dh_tiles) {  // gradient of this chunk's exit state, as a bf16 tile (key `row`)
-      uint8_t *tb = reinterpret_cast<uint8_t *>(a.dh_tiles + state_slot(c) * STATE_TILE) + (col0 >> 6) * 16384;
-#pragma unroll
-      for (int q8 = 0; q8 < 4; ++q8) *reinterpret_cast<uint4 *>(tb + chunk_off(row, 4 * hc + q8)) = pack8(dh + 8 * q8);
+    uint8_t *dvt = a.dv_tiles ? reinterpret_cast<uint8_t *>(a.dv_tiles + state_slot(c) * DV_TILE) + (col0 >> 6) * 8192
+                              : nullptr;
+    if (a.dh_tiles) {  // gradient of this chunk's exit state: D1's dh operand is that bf16 tile
+      if (warp == 0)
+        bulk_store_w(reinterpret_cast<uint8_t *>(a.dh_tiles + state_slot(c) * STATE_TILE) + (col0 >> 6) * 16384,
+                     sb + OFF_DHT, 16384);
     } else {  // fp32
       float4 *dst = reinterpret_cast<float4 *>(a.dh_chunks + state_slot(c) * GDN_DK * GDN_DV +
                                                (int64_t)row * GDN_DV + col0 + 32 * hc);
@@ -371,17 +373,12 @@ __global__ void __launch_bounds__(NTH, 1) tc_dhu_kernel(BwdArgs a, const __grid_
     if (q4 < 2) {  // dv_new rows: fp32 to the workspace, bf16 into D2's operand
       const bool valid = row < n;
       float4 *gdst = reinterpret_cast<float4 *>(a.dvnew + ((c0 + (valid ? row : 0)) * H + h) * GDN_DV + col0 + 32 * hc);
-      uint8_t *dvt = a.dv_tiles ? reinterpret_cast<uint8_t *>(a.dv_tiles + state_slot(c) * DV_TILE) + (col0 >> 6) * 8192
-                                : nullptr;
 #pragma unroll
       for (int part = 0; part < 2; ++part) {
         float dv[16];
         tmem_ld16(tl + T_I1 + 64 * cs + 32 * hc + 16 * part, dv);
         tmem_ld_wait();
-        if (dvt) {  // bf16 tile (rows past the end hold values the local kernel never uses)
-          *reinterpret_cast<uint4 *>(dvt + chunk_off(row, 4 * hc + 2 * part)) = pack8(dv);
-          *reinterpret_cast<uint4 *>(dvt + chunk_off(row, 4 * hc + 2 * part + 1)) = pack8(dv + 8);
-        } else if (valid) {
+        if (!dvt && valid) {  // (the bf16 tile is D2's operand, stored below as it stands)
 #pragma unroll
           for (int g4 = 0; g4 < 4; ++g4)
             gdst[4 * part + g4] = make_float4(dv[4 * g4], dv[4 * g4 + 1], dv[4 * g4 + 2], dv[4 * g4 + 3]);
@@ -392,9 +389,12 @@ __global__ void __launch_bounds__(NTH, 1) tc_dhu_kernel(BwdArgs a, const __grid_
     }
     fence_proxy_async();
     fence_before_sync();
+    if (warp == 0 && a.dh_tiles) bulk_store_wait_read_w();  // the dh tile is rewritten below
     chain_sync();
     if (warp == 0) {  // D2: dh increment = scale Qg^T dO - w^T dv_new
       fence_after_sync();
+      if (dvt)  // dv_new as a bf16 tile (rows past the end hold values the local kernel never uses)
+        bulk_store_w(dvt, sb + OFF_DVT, 8192);
       mma_ops_w(tmem + T_I2 + 64 * cs, kmaj(sb + OFF_WT, 16384), mnmaj(sb + OFF_DVT, 0), 64,
                 idesc_bf16(128, 64, true, false, true), true);
       mma_commit_w(&st.bar_d2);
@@ -413,6 +413,7 @@ __global__ void __launch_bounds__(NTH, 1) tc_dhu_kernel(BwdArgs a, const __grid_
       }
       write_dht();
     }
+    if (warp == 0 && dvt) bulk_store_wait_read_w();  // the dv_new tile is rewritten next round
     fence_proxy_async();
     fence_before_sync();
   };
@@ -458,6 +459,7 @@ __global__ void __launch_bounds__(NTH, 1) tc_dhu_kernel(BwdArgs a, const __grid_
 #pragma unroll
     for (int g4 = 0; g4 < 8; ++g4) dst[g4] = make_float4(dh[4 * g4], dh[4 * g4 + 1], dh[4 * g4 + 2], dh[4 * g4 + 3]);
   }
+  if (warp == 0) bulk_store_wait_w();  // the tiles' bulk stores have completed
   fence_before_sync();
   __syncthreads();
   if (warp == 0) tmem_dealloc(tmem, TMEM_COLS);

@@ -257,5 +257,28 @@ __device__ __forceinline__ void bulk_load_w(uint32_t dst, const void *src, uint3
       : "memory");
 }
 
+// Bulk stores shared -> global (warp-collective, the same elected lane each time, so that
+// the one thread that commits a group also waits for it): both addresses 16-byte aligned and
+// a size that is a multiple of 16.
+__device__ __forceinline__ void bulk_store_w(void *dst, uint32_t src, uint32_t bytes) {
+  asm volatile(
+      "{\n .reg .pred e;\n elect.sync _|e, 0xffffffff;\n"
+      " @e cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;\n"
+      " @e cp.async.bulk.commit_group;\n}\n" ::"l"(reinterpret_cast<uint64_t>(dst)),
+      "r"(src), "r"(bytes)
+      : "memory");
+}
+// the source of every committed bulk store has been read (it may be rewritten)
+__device__ __forceinline__ void bulk_store_wait_read_w() {
+  asm volatile(
+      "{\n .reg .pred e;\n elect.sync _|e, 0xffffffff;\n @e cp.async.bulk.wait_group.read 0;\n}\n" ::
+          : "memory");
+}
+// every committed bulk store has completed
+__device__ __forceinline__ void bulk_store_wait_w() {
+  asm volatile("{\n .reg .pred e;\n elect.sync _|e, 0xffffffff;\n @e cp.async.bulk.wait_group 0;\n}\n" ::
+                   : "memory");
+}
+
 }  // namespace tc
 }  // namespace gdn
