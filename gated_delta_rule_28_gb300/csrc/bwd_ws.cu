@@ -16,9 +16,10 @@
 //   D1   [kgl; -] dh            accumulated onto  scale A_qk^T dO   -> dv_new
 //   D2   -w^T dv_new            accumulated onto  scale Qg^T dO     -> dh update
 // while the producer warps 8..15 prepare the previous chunk: A_qk^T (from
-// [Q; K] Q^T and the gate), the three h-independent products scale A_qk^T dO,
+// [Q; K] Q^T and the gate) and the three h-independent products scale A_qk^T dO,
 // scale Qg^T dO = Q^T (diag(scale base^G) dO) and w^T (= K^T (X diag(beta base^G))^T),
-// with Q, K and dO read in place as MN-major operands, and the operands kgl and w^T. X diag(beta base^G) and the
+// with Q, K and dO read in place as MN-major operands. The chain warps form that chunk's
+// operands kgl and w^T (from tensor memory) in the parts of their round where they would wait. X diag(beta base^G) and the
 // per-token gate factors come from the UT transform kernel.
 // Loads are TMA copies completing on mbarriers.
 // It writes dh of every chunk (the exit-state gradient) and dv_new in fp32
@@ -210,7 +211,7 @@ __global__ void __launch_bounds__(NTH, 1) tc_dhu_kernel(BwdArgs a, const __grid_
   };
 
   // ---- producer: one chunk (order index pm) ------------------------------------------------
-  auto produce = [&](int64_t pm, int64_t m_chain) {
+  auto produce = [&](int64_t pm) {
     const int ps = (int)(pm & 1);
     const uint32_t stg = sb + OFF_ST + ps * SZ_STAGE;
     const float(&tab)[F_ROWS][64] = st.tab[ps];
@@ -299,41 +300,43 @@ __global__ void __launch_bounds__(NTH, 1) tc_dhu_kernel(BwdArgs a, const __grid_
       mma_commit_w(&st.bar_p3);
     }
     __syncwarp();
-    // kgl rows (K rows scaled by base^(G_last - G)) once the chain's D1 has read the previous ones
-    if (m_chain >= 0) wait_par(&st.bar_d1, m_chain);
-    if (q4 >= 2) {
-      const int t = row - 64;
-      const float egl = tab[F_EGL][t];
-      const uint8_t *krow = sm + OFF_ST + ps * SZ_STAGE + hc * 16384;
-      uint8_t *dst = sm + OFF_KGL + hc * 8192;
-#pragma unroll
-      for (int c8 = 0; c8 < 8; ++c8) {
-        float f[8];
-        unpack8(*reinterpret_cast<const uint4 *>(krow + chunk_off(row, c8)), f);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) f[e] *= egl;
-        *reinterpret_cast<uint4 *>(dst + chunk_off(t, c8)) = pack8(f);
-      }
-    }
-    // w^T rows (keys) once the products are done and the chain's D2 has read the previous ones
-    wait_par(&st.bar_p3, pm);
-    if (m_chain >= 0) wait_par(&st.bar_d2, m_chain);
-    {
-      uint8_t *dst = sm + OFF_WT;
-#pragma unroll
-      for (int part = 0; part < 2; ++part) {
-        float sv[16];
-        tmem_ld16(tl + T_WT + 32 * hc + 16 * part, sv);
-        tmem_ld_wait();
-        *reinterpret_cast<uint4 *>(dst + chunk_off(row, 4 * hc + 2 * part)) = pack8(sv);
-        *reinterpret_cast<uint4 *>(dst + chunk_off(row, 4 * hc + 2 * part + 1)) = pack8(sv + 8);
-      }
-    }
     fence_proxy_async();
     fence_before_sync();
   };
 
   // ---- chain ----------------------------------------------------------------------------
+  // the operands of chunk pm's D1 and D2 that come from the producer's work, written by the
+  // chain warps while the chain of chunk pm - 1 waits or idles (the producer bounds a round):
+  // kgl rows (K rows scaled by base^(G_last - G); the lanes of tokens 64..127 of the stage) and
+  // w^T rows (keys, from tensor memory once the producer's products are done)
+  auto write_kgl = [&](int64_t pm) {  // warps of lanes 64..127 only
+    const int ps = (int)(pm & 1);
+    wait_par(&st.bar_ld[ps], pm >> 1);
+    const int t = row - 64;
+    const float egl = st.tab[ps][F_EGL][t];
+    const uint8_t *krow = sm + OFF_ST + ps * SZ_STAGE + hc * 16384;
+    uint8_t *dst = sm + OFF_KGL + hc * 8192;
+#pragma unroll
+    for (int c8 = 0; c8 < 8; ++c8) {
+      float f[8];
+      unpack8(*reinterpret_cast<const uint4 *>(krow + chunk_off(row, c8)), f);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) f[e] *= egl;
+      *reinterpret_cast<uint4 *>(dst + chunk_off(t, c8)) = pack8(f);
+    }
+  };
+  auto write_wt = [&](int64_t pm) {
+    wait_par(&st.bar_p3, pm);
+    uint8_t *dst = sm + OFF_WT;
+#pragma unroll
+    for (int part = 0; part < 2; ++part) {
+      float sv[16];
+      tmem_ld16(tl + T_WT + 32 * hc + 16 * part, sv);
+      tmem_ld_wait();
+      *reinterpret_cast<uint4 *>(dst + chunk_off(row, 4 * hc + 2 * part)) = pack8(sv);
+      *reinterpret_cast<uint4 *>(dst + chunk_off(row, 4 * hc + 2 * part + 1)) = pack8(sv + 8);
+    }
+  };
   float dh[32];
   if (!producer) {
     const float *src = a.dht ? a.dht + state_off + (int64_t)row * GDN_DV + col0 + 32 * hc : nullptr;
@@ -386,6 +389,8 @@ __global__ void __launch_bounds__(NTH, 1) tc_dhu_kernel(BwdArgs a, const __grid_
         *reinterpret_cast<uint4 *>(sm + OFF_DVT + chunk_off(row, 4 * hc + 2 * part)) = pack8(dv);
         *reinterpret_cast<uint4 *>(sm + OFF_DVT + chunk_off(row, 4 * hc + 2 * part + 1)) = pack8(dv + 8);
       }
+    } else if (m + 1 < nch) {  // D1 has read kgl: the next chunk's, meanwhile
+      write_kgl(m + 1);
     }
     fence_proxy_async();
     fence_before_sync();
@@ -413,6 +418,7 @@ __global__ void __launch_bounds__(NTH, 1) tc_dhu_kernel(BwdArgs a, const __grid_
       }
       write_dht();
     }
+    if (m + 1 < nch) write_wt(m + 1);  // D2 has read w^T: the next chunk's
     if (warp == 0 && dvt) bulk_store_wait_read_w();  // the dv_new tile is rewritten next round
     fence_proxy_async();
     fence_before_sync();
@@ -431,9 +437,14 @@ __global__ void __launch_bounds__(NTH, 1) tc_dhu_kernel(BwdArgs a, const __grid_
   // round m: the chain runs order index m while the producer prepares m+1
   for (int64_t m = -1; m < nch; ++m) {
     if (producer) {
-      if (m + 1 < nch) produce(m + 1, m);
+      if (m + 1 < nch) produce(m + 1);
     } else if (m >= 0) {
       chain(m);
+    } else if (nch > 0) {  // chunk 0's kgl and w^T
+      if (q4 >= 2) write_kgl(0);
+      write_wt(0);
+      fence_proxy_async();
+      fence_before_sync();
     }
     if (__syncthreads_or(bad)) {
       bad = true;
