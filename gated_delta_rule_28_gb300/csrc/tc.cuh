@@ -268,6 +268,16 @@ __device__ __forceinline__ void bulk_store_w(void *dst, uint32_t src, uint32_t b
       "r"(src), "r"(bytes)
       : "memory");
 }
+// a tensor tile shared -> global (its box from the map; the 128-byte-swizzled layout in shared
+// memory), committed as a bulk group of the elected lane, as bulk_store_w
+__device__ __forceinline__ void tma_store_2d_w(const void *map, int x, int y, uint32_t src) {
+  asm volatile(
+      "{\n .reg .pred e;\n elect.sync _|e, 0xffffffff;\n"
+      " @e cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];\n"
+      " @e cp.async.bulk.commit_group;\n}\n" ::"l"(reinterpret_cast<uint64_t>(map)),
+      "r"(x), "r"(y), "r"(src)
+      : "memory");
+}
 // the source of every committed bulk store has been read (it may be rewritten)
 __device__ __forceinline__ void bulk_store_wait_read_w() {
   asm volatile(

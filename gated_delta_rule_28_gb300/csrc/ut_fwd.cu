@@ -38,8 +38,13 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a
 
 // Persistent: each CTA walks the (chunk, head) items with a stride of the grid (six CTAs per
 // SM: one key buffer each), prefetching the next item's gate and beta into registers.
+// TMA map over the X pairs: [slots * H * 128 rows][64] bf16, 64 x 64 boxes
+struct UtMaps {
+  TmaMap x;
+};
+
 template <bool E2>
-__global__ void __launch_bounds__(128, 6) ut_kernel(UtArgs a, int64_t items) {
+__global__ void __launch_bounds__(128, 6) ut_kernel(UtArgs a, int64_t items, const __grid_constant__ UtMaps maps) {
   __shared__ __align__(1024) uint8_t kbuf[1][16384];  // keys (64 rows x 2 K-blocks, swizzled);
                                                       // after K K^T it holds L's blocks
   __shared__ __align__(16) float XB[10 * 256], TB[4 * 256];
@@ -238,17 +243,27 @@ __global__ void __launch_bounds__(128, 6) ut_kernel(UtArgs a, int64_t items) {
 #pragma unroll
         for (int q = 0; q < 8; ++q) Ad[q] = make_float4(vals[4 * q], vals[4 * q + 1], vals[4 * q + 2], vals[4 * q + 3]);
       }
-      // the pair [X diag(beta); X diag(beta base^G)] in bf16, 128 rows per chunk and head
-      __nv_bfloat16 *xrow = a.xw + ((slot * H + h) * 2 * GDN_CHUNK + row) * GDN_CHUNK + 32 * half;
+      // the pair [X diag(beta); X diag(beta base^G)] in bf16, 128 rows per chunk and head, staged
+      // in the key buffer (free after the solve) as two 64-row boxes in the 128-byte-swizzled
+      // layout, then written by two TMA stores
+      uint8_t *stage = kbuf[buf];
       float sc[32];
 #pragma unroll
       for (int j = 0; j < 32; ++j) sc[j] = vals[j] * sbeta[32 * half + j];
 #pragma unroll
-      for (int q = 0; q < 4; ++q) reinterpret_cast<uint4 *>(xrow)[q] = pack8(sc + 8 * q);
+      for (int q = 0; q < 4; ++q) *reinterpret_cast<uint4 *>(stage + chunk_off(row, 4 * half + q)) = pack8(sc + 8 * q);
 #pragma unroll
       for (int j = 0; j < 32; ++j) sc[j] = vals[j] * sBEG[32 * half + j];
 #pragma unroll
-      for (int q = 0; q < 4; ++q) reinterpret_cast<uint4 *>(xrow + GDN_CHUNK * GDN_CHUNK)[q] = pack8(sc + 8 * q);
+      for (int q = 0; q < 4; ++q)
+        *reinterpret_cast<uint4 *>(stage + 8192 + chunk_off(row, 4 * half + q)) = pack8(sc + 8 * q);
+    }
+    fence_proxy_async();  // the staged pair, to the TMA unit
+    __syncthreads();
+    if (warp == 0) {
+      const int y = (int)((slot * H + h) * 2 * GDN_CHUNK);
+      tma_store_2d_w(&maps.x, 0, y, smem_u32(kbuf[buf]));
+      tma_store_2d_w(&maps.x, 0, y + GDN_CHUNK, smem_u32(kbuf[buf]) + 8192);
     }
     if (a.g_cumsum && !a.g_cum_in && tid < n) a.g_cumsum[(r0 + tid) * H + h] = sG[tid];
     if (tid < 64) {  // per-token gate factors for the state kernels (rows of GateTabRow)
@@ -264,9 +279,11 @@ __global__ void __launch_bounds__(128, 6) ut_kernel(UtArgs a, int64_t items) {
       tab[F_EB2 * 64 + tid] = sEB[1][tid];
       tab[F_EB3 * 64 + tid] = sEB[2][tid];
     }
+    if (warp == 0) bulk_store_wait_read_w();  // the key buffer takes the next item's keys
     __syncthreads();  // sG, sbeta and the X blocks are rewritten by the next item
   }
   cp_async_wait<0>();
+  if (warp == 0) bulk_store_wait_w();  // the X pairs have reached global memory
 }
 
 }  // namespace
@@ -280,9 +297,13 @@ cudaError_t launch_ut(const UtArgs &a, int slots, cudaStream_t st) {
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 128, 0);
   if (e != cudaSuccess) return e;
-  if (items > INT32_MAX) return cudaErrorInvalidValue;  // the kernel locates items in 32 bits
+  // the kernel locates items in 32 bits, and the X pairs' TMA rows are 32-bit coordinates
+  if (items > INT32_MAX / (2 * GDN_CHUNK)) return cudaErrorInvalidValue;
+  UtMaps maps;
+  e = make_tmap_bf16(&maps.x, a.xw, GDN_CHUNK, (uint64_t)items * 2 * GDN_CHUNK, GDN_CHUNK * 2);
+  if (e != cudaSuccess) return e;
   const int64_t grid = std::min<int64_t>(items, (int64_t)std::max(1, sms * std::max(1, per_sm)));
-  kern<<<(unsigned)grid, 128, 0, st>>>(a, items);
+  kern<<<(unsigned)grid, 128, 0, st>>>(a, items, maps);
   return cudaGetLastError();
 }
 
