@@ -52,7 +52,9 @@ constexpr int OFF_KB = OFF_V + 16384;   // K / e (Gram B); exact chunks: L while
 constexpr int OFF_SMALL = OFF_KB + 16384;
 constexpr int SMEM_BYTES = OFF_SMALL + 2048 + 1024;
 constexpr int L_FLOATS = 10 * 256, X_FLOATS = 10 * 256;  // lower 16x16 blocks (blk / bsw)
-static_assert(64 * GS * 4 <= 34816 && (L_FLOATS + X_FLOATS + 4 * 256) * 4 <= 34816, "G region");
+constexpr int OFF_AQS = OFF_G + 24576;  // A_qk staged for its bulk copy, after L, X and T
+static_assert(64 * GS * 4 <= 34816 && (L_FLOATS + X_FLOATS + 4 * 256) * 4 <= 24576 && 24576 + 8192 <= 34816,
+              "G region: G; then L, X, T and the staged A_qk; then the staged u");
 
 // largest |exponent| (base 2) a factor may take on the tensor-core path
 constexpr float EXP_LIMIT = 100.f;
@@ -321,8 +323,8 @@ __global__ void __launch_bounds__(NTH, 2) kda_prep_kernel(KdaPrepArgs a, int64_t
               val.x = j < i ? bt * acc[nt][2 * hr] : 0.f;
               val.y = j + 1 < i ? bt * acc[nt][2 * hr + 1] : 0.f;
               *reinterpret_cast<float2 *>(&sL[blk(bi, bj) * 256 + bsw(rr, c)]) = val;
-            } else {
-              *reinterpret_cast<uint32_t *>(blob + BLOB_AQ + chunk_off(i, j >> 3) + (j & 7) * 2) =
+            } else {  // A_qk staged in G's free tail, copied out below
+              *reinterpret_cast<uint32_t *>(sm + OFF_AQS + chunk_off(i, j >> 3) + (j & 7) * 2) =
                   pack_bf16(j <= i ? scale * acc[nt][2 * hr] : 0.f, j + 1 <= i ? scale * acc[nt][2 * hr + 1] : 0.f);
             }
           }
@@ -331,13 +333,16 @@ __global__ void __launch_bounds__(NTH, 2) kda_prep_kernel(KdaPrepArgs a, int64_t
       const float *sLx = reinterpret_cast<const float *>(sm + OFF_KB);
       for (int x = tid; x < L_FLOATS; x += NTH) sL[x] = sLx[x];
     }
-    if (has_q)  // A_qk right of each row's diagonal block is zero
+    if (has_q) {  // A_qk right of each row's diagonal block is zero
+      uint8_t *aq = exact ? blob + BLOB_AQ : sm + OFF_AQS;
       for (int x = tid; x < 64 * 8; x += NTH) {
         const int i = x >> 3, c8 = x & 7;
-        if (c8 >= 2 * ((i >> 4) + 1))
-          *reinterpret_cast<uint4 *>(blob + BLOB_AQ + chunk_off(i, c8)) = make_uint4(0, 0, 0, 0);
+        if (c8 >= 2 * ((i >> 4) + 1)) *reinterpret_cast<uint4 *>(aq + chunk_off(i, c8)) = make_uint4(0, 0, 0, 0);
       }
+    }
+    fence_proxy_async();  // the staged A_qk, to the bulk copy
     __syncthreads();
+    if (warp == 0 && has_q && !exact) bulk_store_w(blob + BLOB_AQ, sb + OFF_AQS, 8192);
 
     // ---- X = (I + L)^-1 (warps 0..3) ----
     if (warp < 4) solve_blocks(sL, sX, sT, tid);
@@ -394,8 +399,10 @@ __global__ void __launch_bounds__(NTH, 2) kda_prep_kernel(KdaPrepArgs a, int64_t
             mma16816(acc[2 * np + 1], af, x[2], x[3]);
           }
         }
-        uint8_t *dst = blob + (which ? BLOB_U : BLOB_WQ);
-        const uint32_t kstride = which ? 8192u : 16384u;
+        // staged as two 64-column blocks of 64 rows: u in G's region (L, X and T are dead), w in
+        // K / e's (the Gram's right operand), copied out below
+        uint8_t *dst = sm + (which ? OFF_G : OFF_KB);
+        const uint32_t kstride = 8192u;
 #pragma unroll
         for (int nt = 0; nt < 8; ++nt) {
           const int c = n0 + 8 * nt + 2 * t4;
@@ -410,8 +417,17 @@ __global__ void __launch_bounds__(NTH, 2) kda_prep_kernel(KdaPrepArgs a, int64_t
         }
       }
     }
+    fence_proxy_async();  // the staged w and u, to the bulk copies
+    __syncthreads();
+    if (warp == 0) {
+      bulk_store_w(blob + BLOB_WQ, sb + OFF_KB, 8192);  // w: rows 0..63 of each 128-row K-block
+      bulk_store_w(blob + BLOB_WQ + 16384, sb + OFF_KB + 8192, 8192);
+      bulk_store_w(blob + BLOB_U, sb + OFF_G, 16384);
+      bulk_store_wait_read_w();
+    }
     __syncthreads();  // shared memory is rewritten by the next item
   }
+  if (warp == 0) bulk_store_wait_w();  // the blobs have reached global memory
 }
 
 }  // namespace
