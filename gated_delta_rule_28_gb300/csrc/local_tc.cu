@@ -22,6 +22,8 @@
 // tiles through ldmatrix (transposed where the product needs it); dq and dk accumulate in
 // registers over the phases; per-row reductions go through warp shuffles and one-writer
 // slots summed in a fixed order, so the result does not depend on thread timing.
+#include <climits>
+
 #include "common.cuh"
 #include "kernels.h"
 #include "tc.cuh"
@@ -53,7 +55,13 @@ struct __align__(16) Small {
   float G[64], gam[64], lam[64], beta[64];
   float part[6][64];   // per-row partial sums, one writer each: [column half][row] x 3
   float gl[8];         // per-warp partials of the G_last terms
+  uint64_t ldbar;      // the chunk's tile copies
 };
+// TMA maps over q, k, v, dO ([token rows][H * 128] bf16, 64 x 64 boxes)
+struct LocalMaps {
+  TmaMap q, k, v, dO;
+};
+constexpr uint32_t WAIT_LIMIT = 1u << 22;
 static_assert(sizeof(Small) <= 4096, "small state");
 
 struct Tl {
@@ -136,7 +144,7 @@ __device__ __forceinline__ float quad_sum(float v) {
 }
 
 template <bool E2>
-__global__ void __launch_bounds__(NTH, 1) local_tc_kernel(BwdArgs a) {
+__global__ void __launch_bounds__(NTH, 1) local_tc_kernel(BwdArgs a, const __grid_constant__ LocalMaps maps) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   Small &sv = *reinterpret_cast<Small *>(sm + O_SMALL);
@@ -150,11 +158,7 @@ __global__ void __launch_bounds__(NTH, 1) local_tc_kernel(BwdArgs a) {
   const int64_t zc = blockIdx.x;
   const float lnb = E2 ? 0.69314718055994530942f : 1.f;
   const float scale = a.scale;
-  const __nv_bfloat16 *q = static_cast<const __nv_bfloat16 *>(a.q);
-  const __nv_bfloat16 *k = static_cast<const __nv_bfloat16 *>(a.k);
-  const __nv_bfloat16 *v = static_cast<const __nv_bfloat16 *>(a.v);
   const __nv_bfloat16 *beta = static_cast<const __nv_bfloat16 *>(a.beta);
-  const __nv_bfloat16 *dO = static_cast<const __nv_bfloat16 *>(a.dO);
   __nv_bfloat16 *dq = static_cast<__nv_bfloat16 *>(a.dq);
   __nv_bfloat16 *dk = static_cast<__nv_bfloat16 *>(a.dk);
   __nv_bfloat16 *dv = static_cast<__nv_bfloat16 *>(a.dv);
@@ -187,6 +191,11 @@ __global__ void __launch_bounds__(NTH, 1) local_tc_kernel(BwdArgs a) {
   }
   auto row_of = [&](int i) { return (c0 + i) * H + h; };
 
+  if (tid == 0) {
+    mbar_init(&sv.ldbar, 1);
+    mbar_fence_init();
+  }
+  __syncthreads();
   // ---- loads: the gate, beta and X (rows past the end: identity) into registers first, so
   // that they do not queue behind the tiles; then K, Q, V, dO (zero past the end) and the bf16
   // tiles of h, dh and dN written by the recompute and the reverse recurrence (already in this
@@ -204,27 +213,24 @@ __global__ void __launch_bounds__(NTH, 1) local_tc_kernel(BwdArgs a) {
 #pragma unroll
     for (int hh = 0; hh < 2; ++hh) xr[u][hh] = r < n ? __ldg(src + hh) : make_float4(0.f, 0.f, 0.f, 0.f);
   }
-  for (int x = tid; x < 1024; x += NTH) {
-    const int r = x >> 4, c16 = x & 15;
-    const bool valid = r < n;
-    const int64_t off = row_of(valid ? r : 0) * GDN_DK + c16 * 8;
-    const uint32_t sz = valid ? 16u : 0u;
-    cp_async16(toff(tK, r, c16), k + off, sz);
-    cp_async16(toff(tQ, r, c16), q + off, sz);
-    cp_async16(toff(tW, r, c16), v + off, sz);
-    cp_async16(toff(tDO, r, c16), dO + off, sz);
+  // the tiles: q, k, v, dO as two 64 x 64 TMA boxes each (rows past the chunk's end hold the
+  // tensor's next rows, zeroed below), h, dh and dN (already in this layout) as bulk copies
+  if (warp == 0) {
+    uint64_t *bar = &sv.ldbar;
+    const int y = (int)c0, x0 = h * GDN_DK;
+    mbar_expect_tx_w(bar, 4 * 16384 + 2 * 32768 + 16384);
+    tma_load_2d_w(sb + O_K, &maps.k, x0, y, bar);
+    tma_load_2d_w(sb + O_K + 8192, &maps.k, x0 + 64, y, bar);
+    tma_load_2d_w(sb + O_Q, &maps.q, x0, y, bar);
+    tma_load_2d_w(sb + O_Q + 8192, &maps.q, x0 + 64, y, bar);
+    tma_load_2d_w(sb + O_W, &maps.v, x0, y, bar);
+    tma_load_2d_w(sb + O_W + 8192, &maps.v, x0 + 64, y, bar);
+    tma_load_2d_w(sb + O_DO, &maps.dO, x0, y, bar);
+    tma_load_2d_w(sb + O_DO + 8192, &maps.dO, x0 + 64, y, bar);
+    bulk_load_w(sb + O_H, a.h_tiles + slot * STATE_TILE, 32768, bar);
+    bulk_load_w(sb + O_DH, a.dh_tiles + slot * STATE_TILE, 32768, bar);
+    bulk_load_w(sb + O_DN, a.dv_tiles + slot * DV_TILE, 16384, bar);
   }
-  {
-    const uint8_t *gh = reinterpret_cast<const uint8_t *>(a.h_tiles + slot * STATE_TILE);
-    const uint8_t *gdh = reinterpret_cast<const uint8_t *>(a.dh_tiles + slot * STATE_TILE);
-    const uint8_t *gdn = reinterpret_cast<const uint8_t *>(a.dv_tiles + slot * DV_TILE);
-    for (int x = tid; x < 2048; x += NTH) {  // 32 KB each
-      cp_async16(sb + O_H + 16 * x, gh + 16 * x, 16u);
-      cp_async16(sb + O_DH + 16 * x, gdh + 16 * x, 16u);
-    }
-    for (int x = tid; x < 1024; x += NTH) cp_async16(sb + O_DN + 16 * x, gdn + 16 * x, 16u);  // 16 KB
-  }
-  cp_async_commit();
   if (tid < 64) {
     sv.G[tid] = G_t;
     sv.beta[tid] = beta_t;
@@ -248,14 +254,24 @@ __global__ void __launch_bounds__(NTH, 1) local_tc_kernel(BwdArgs a) {
     *reinterpret_cast<uint4 *>(sm + (toff(tX, r, c8) - sb)) = pack8(xv);
     *reinterpret_cast<uint4 *>(sm + (toff(tXB, r, c8) - sb)) = pack8(xb);
   }
-  cp_async_wait<0>();
-  __syncthreads();
-  // rows of dN past the chunk's end are zero (the tile holds whatever the reverse recurrence
-  // computed there); <dh, h> over the whole state for the gradient of the last gate
+  const bool late = !mbar_wait(&sv.ldbar, 0, WAIT_LIMIT);
+  if (__syncthreads_or(late)) {  // the tiles did not arrive: report, let the copies land, leave
+    if (tid == 0) raise_device_flag(a.dev_flag, kDevTimeout);
+    mbar_wait(&sv.ldbar, 0, WAIT_LIMIT);
+    return;
+  }
+  // rows past the chunk's end are zero in K, Q, V, dO (the boxes hold the tensor's next rows)
+  // and dN (the tile holds whatever the reverse recurrence computed there); <dh, h> over the
+  // whole state for the gradient of the last gate
   if (n < 64)
     for (int x = tid; x < (64 - n) * 16; x += NTH) {
       const int r = n + x / 16, c16 = x % 16;
-      *reinterpret_cast<uint4 *>(sm + (toff(tDN, r, c16) - sb)) = make_uint4(0, 0, 0, 0);
+      const uint4 z = make_uint4(0, 0, 0, 0);
+      *reinterpret_cast<uint4 *>(sm + (toff(tK, r, c16) - sb)) = z;
+      *reinterpret_cast<uint4 *>(sm + (toff(tQ, r, c16) - sb)) = z;
+      *reinterpret_cast<uint4 *>(sm + (toff(tW, r, c16) - sb)) = z;
+      *reinterpret_cast<uint4 *>(sm + (toff(tDO, r, c16) - sb)) = z;
+      *reinterpret_cast<uint4 *>(sm + (toff(tDN, r, c16) - sb)) = z;
     }
   {
     float hdh = 0.f;
@@ -541,7 +557,16 @@ cudaError_t launch_bwd_local_tc(const BwdArgs &a, cudaStream_t st) {
   if (e != cudaSuccess) return e;
   const int64_t nch = a.cu ? a.num_chunks : (int64_t)a.B * ((a.T + GDN_CHUNK - 1) / GDN_CHUNK);
   if (nch == 0) return cudaSuccess;
-  kern<<<dim3((unsigned)nch, a.H), NTH, SMEM_BYTES, st>>>(a);
+  const uint64_t rows = a.cu ? (uint64_t)a.T : (uint64_t)a.B * a.T;  // token rows (32-bit TMA rows)
+  if (rows > (uint64_t)INT32_MAX) return cudaErrorInvalidValue;
+  const uint64_t pitch = (uint64_t)a.H * GDN_DK * 2;
+  LocalMaps maps;
+  e = make_tmap_bf16(&maps.q, a.q, (uint64_t)a.H * GDN_DK, rows, pitch);
+  if (e == cudaSuccess) e = make_tmap_bf16(&maps.k, a.k, (uint64_t)a.H * GDN_DK, rows, pitch);
+  if (e == cudaSuccess) e = make_tmap_bf16(&maps.v, a.v, (uint64_t)a.H * GDN_DV, rows, (uint64_t)a.H * GDN_DV * 2);
+  if (e == cudaSuccess) e = make_tmap_bf16(&maps.dO, a.dO, (uint64_t)a.H * GDN_DV, rows, (uint64_t)a.H * GDN_DV * 2);
+  if (e != cudaSuccess) return e;
+  kern<<<dim3((unsigned)nch, a.H), NTH, SMEM_BYTES, st>>>(a, maps);
   return cudaGetLastError();
 }
 
