@@ -22,8 +22,10 @@
 // operands kgl and w^T (from tensor memory) in the parts of their round where they would wait. X diag(beta base^G) and the
 // per-token gate factors come from the UT transform kernel.
 // Loads are TMA copies completing on mbarriers.
-// It writes dh of every chunk (the exit-state gradient) and dv_new in fp32
-// for the local-gradient kernel, and dh of the first chunk's entry as dh0.
+// It writes dh of every chunk (the exit-state gradient) and dv_new for the
+// local-gradient kernel -- bf16 tiles in that kernel's layout, bulk-copied from
+// the MMA operand tiles (fp32 rows when no tiles are asked for) -- and dh of the
+// first chunk's entry as dh0.
 // Every mbarrier wait is bounded; a wait that runs out sets the device flag
 // and the CTA drains its MMAs, frees its tensor memory and leaves.
 #include "common.cuh"

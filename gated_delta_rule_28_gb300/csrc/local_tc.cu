@@ -3,7 +3,7 @@
 // One CTA of 8 warps per (chunk, head) computes dq, dk, dv, dbeta and dg of its chunk from
 // the chunk's inputs, its entry state h, the gradient dh of its exit state and the gradient
 // dN of v_new (the recompute's and the reverse recurrence's outputs, bf16 tiles in this
-// kernel's shared-memory layout, fetched with cp.async) -- the finalize stage of the backward
+// kernel's shared-memory layout, fetched with bulk copies) -- the finalize stage of the backward
 // (the KDA adapter's chunk_kda_bwd_finalize on the "Diff Coverage" page; the GDN adapter's
 // chunk_gated_delta_rule_bwd contract). With gamma_i = b^(G_i), lambda_i = b^(G_last - G_i),
 // Gamma_ij = b^(G_i - G_j) and X = (I + L)^-1 (the forward's A slot):
@@ -197,9 +197,7 @@ __global__ void __launch_bounds__(NTH, 1) local_tc_kernel(BwdArgs a, const __gri
   }
   __syncthreads();
   // ---- loads: the gate, beta and X (rows past the end: identity) into registers first, so
-  // that they do not queue behind the tiles; then K, Q, V, dO (zero past the end) and the bf16
-  // tiles of h, dh and dN written by the recompute and the reverse recurrence (already in this
-  // layout), all by cp.async ---------------------------------------------------------------
+  // that they do not queue behind the tiles; then the tiles (below) ----------------------------
   float G_t = 0.f, beta_t = 0.f;
   if (tid < 64) {
     G_t = a.g_cumsum[row_of(min(tid, n - 1))];
