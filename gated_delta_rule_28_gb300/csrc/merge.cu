@@ -11,8 +11,9 @@
 // The columns of the state are independent, so one CTA owns one (batch row and
 // head, 8 state columns) and walks the segments in order; its 128 threads own
 // one state row each. Per segment the only dependent work is the 128 x 8 x 128
-// product M_s S; the next segment's 64 KB transfer map is copied into the other
-// of two shared-memory buffers (cp.async) while this one is applied. M is kept
+// product M_s S; the transfer maps (64 KB each) are copied two segments ahead into
+// three shared-memory buffers (cp.async) while the current one is applied, and the
+// local terms one segment ahead into registers. M is kept
 // row-major with the 16-byte chunks of row m XOR-swizzled by m mod 32, so the 16-byte
 // reads of a quarter warp (eight rows, the same columns) hit eight distinct bank groups;
 // the state slice is read by all threads alike (broadcast).
@@ -27,15 +28,16 @@ using namespace tile;
 constexpr int BV = 8;      // state columns per CTA
 constexpr int NTH = 128;   // one thread per state row
 constexpr int M_FLOATS = GDN_DK * GDN_DK;
-constexpr size_t SMEM_BYTES = (2 * M_FLOATS + 2 * GDN_DK * BV) * sizeof(float);
+constexpr int MSTAGES = 3;  // transfer-map buffers
+constexpr size_t SMEM_BYTES = (MSTAGES * M_FLOATS + 2 * GDN_DK * BV) * sizeof(float);
 
 // float offset of M[m][4 c4] in the swizzled buffer (c4: 16-byte chunk, 32 per row)
 __device__ __forceinline__ int msw(int m, int c4) { return m * GDN_DK + ((c4 ^ (m & 31)) << 2); }
 
 __global__ void __launch_bounds__(NTH) merge_kernel(MergeArgs a) {
   extern __shared__ __align__(16) float smem[];
-  float *sM = smem;                  // two transfer maps
-  float *sS = smem + 2 * M_FLOATS;   // two state slices [128][8]
+  float *sM = smem;                        // MSTAGES transfer maps
+  float *sS = smem + MSTAGES * M_FLOATS;   // two state slices [128][8]
   const int m = threadIdx.x;
   const int col0 = blockIdx.x * BV;
   const int64_t bh = blockIdx.y;
@@ -47,7 +49,7 @@ __global__ void __launch_bounds__(NTH) merge_kernel(MergeArgs a) {
   auto seg_at = [&](int i) { return adj ? a.nseg - 1 - i : i; };
   auto fetch_M = [&](int i) {  // every thread copies one row: 32 chunks of 16 bytes
     const float *Ms = a.M + (bh * a.nseg + seg_at(i)) * M_FLOATS + (int64_t)m * GDN_DK;
-    const uint32_t dst = sMa + (uint32_t)((i & 1) * M_FLOATS) * 4u;
+    const uint32_t dst = sMa + (uint32_t)((i % MSTAGES) * M_FLOATS) * 4u;
 #pragma unroll 8
     for (int c4 = 0; c4 < 32; ++c4) cp_async16(dst + (uint32_t)msw(m, c4) * 4u, Ms + 4 * c4, 16u);
     cp_async_commit();
@@ -61,19 +63,33 @@ __global__ void __launch_bounds__(NTH) merge_kernel(MergeArgs a) {
   }
 #pragma unroll
   for (int j = 0; j < BV; ++j) sS[m * BV + j] = cur[j];
-  if (a.nseg > 0) fetch_M(0);
+  // the local term of the segment visited at step i (row m, this CTA's columns)
+  auto ext_at = [&](int i, float4 &e0, float4 &e1) {
+    const float4 *es = reinterpret_cast<const float4 *>(
+        a.S_ext + (bh * a.nseg + seg_at(i)) * KV + (int64_t)m * GDN_DV + col0);
+    e0 = es[0];
+    e1 = es[1];
+  };
+  float4 e0 = make_float4(0.f, 0.f, 0.f, 0.f), e1 = e0;
+  if (a.nseg > 0) {
+    fetch_M(0);
+    ext_at(0, e0, e1);
+  }
+  if (a.nseg > 1) fetch_M(1);
   for (int s = 0; s < a.nseg; ++s) {
     const int64_t slot = bh * a.nseg + seg_at(s);
-    // this segment's entry state, and its local term
+    // this segment's entry state; the next segment's local term, meanwhile
     float4 *dst = reinterpret_cast<float4 *>(a.S_init + slot * KV + (int64_t)m * GDN_DV + col0);
     dst[0] = make_float4(cur[0], cur[1], cur[2], cur[3]);
     dst[1] = make_float4(cur[4], cur[5], cur[6], cur[7]);
-    const float4 *es = reinterpret_cast<const float4 *>(a.S_ext + slot * KV + (int64_t)m * GDN_DV + col0);
-    const float4 e0 = es[0], e1 = es[1];
-    cp_async_wait<0>();  // M_s, the only copy in flight, has landed
-    __syncthreads();     // M_s and the state slice are visible; every read of M_{s-1} is done
-    if (s + 1 < a.nseg) fetch_M(s + 1);  // into the buffer M_{s-1} held, while M_s is applied
-    const float *Mb = sM + (s & 1) * M_FLOATS;
+    float4 n0 = e0, n1 = e1;
+    if (s + 1 < a.nseg) ext_at(s + 1, n0, n1);
+    // M_s has landed (M_{s+1} may still be in flight)
+    if (s + 1 < a.nseg) cp_async_wait<1>();
+    else cp_async_wait<0>();
+    __syncthreads();  // M_s and the state slice are visible; every read of M_{s-1} is done
+    if (s + 2 < a.nseg) fetch_M(s + 2);  // into the buffer M_{s-1} held
+    const float *Mb = sM + (s % MSTAGES) * M_FLOATS;
     const float *Sb = sS + (s & 1) * GDN_DK * BV;
     float acc[BV];
 #pragma unroll
@@ -110,6 +126,8 @@ __global__ void __launch_bounds__(NTH) merge_kernel(MergeArgs a) {
     cur[5] = acc[5] + e1.y;
     cur[6] = acc[6] + e1.z;
     cur[7] = acc[7] + e1.w;
+    e0 = n0;
+    e1 = n1;
     float *Sn = sS + ((s + 1) & 1) * GDN_DK * BV;
 #pragma unroll
     for (int j = 0; j < BV; ++j) Sn[m * BV + j] = cur[j];
