@@ -847,7 +847,7 @@ gdn_status kda_segment_merge_bwd(const gdn_problem *p, const float *dS_ext, cons
   OPTIONAL_PTR(dh0, "dh0");
   int dev;
   if ((st = check_device(&dev)) != GDN_OK) return st;
-  gdn::MergeArgs a{dS_ext, M, dht, dS_exit, dh0, p->B * p->H, nseg, 1};
+  gdn::MergeArgs a{dS_ext, M, dht, dS_exit, dh0, p->B * p->H, nseg, 1, device_flag_ptr()};
   cudaError_t e = gdn::launch_merge(a, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "adjoint segment merge launch");
   return ok();
@@ -868,7 +868,7 @@ gdn_status kda_segment_merge(const gdn_problem *p, const float *S_ext, const flo
   OPTIONAL_PTR(ht, "ht");
   int dev;
   if ((st = check_device(&dev)) != GDN_OK) return st;
-  gdn::MergeArgs a{S_ext, M, h0, S_init, ht, p->B * p->H, nseg, 0};
+  gdn::MergeArgs a{S_ext, M, h0, S_init, ht, p->B * p->H, nseg, 0, device_flag_ptr()};
   cudaError_t e = gdn::launch_merge(a, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "segment merge launch");
   return ok();
@@ -967,7 +967,7 @@ gdn_status gdn_chunk_fwd_split(const gdn_problem *pin, const void *q, const void
   if ((e = gdn::launch_kda_chain(kda_chain_args(a, blob), dim3(4, p->H, p->B * nseg), s)) != cudaSuccess)
     return cuda_fail(e, "segment summary launch");
   // 3. ordered merge from h0, as kda_segment_merge (the final state comes from step 4)
-  gdn::MergeArgs ma{S_ext, M, h0, S_init, nullptr, p->B * p->H, nseg, 0};
+  gdn::MergeArgs ma{S_ext, M, h0, S_init, nullptr, p->B * p->H, nseg, 0, flag};
   if ((e = gdn::launch_merge(ma, s)) != cudaSuccess) return cuda_fail(e, "segment merge launch");
   // 4. every segment from its merged entry state, as gdn_chunk_fwd with segment_len
   a.S_ext = nullptr;

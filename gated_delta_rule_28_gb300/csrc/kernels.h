@@ -17,6 +17,9 @@ struct alignas(64) TmaMap {
 // Map over a row-major bf16 matrix [rows][cols] (row pitch row_bytes) read in
 // 64 x 64 boxes with the 128-byte swizzle; zero fill outside the matrix.
 cudaError_t make_tmap_bf16(TmaMap *map, const void *base, uint64_t cols, uint64_t rows, uint64_t row_bytes);
+// Map over a row-major fp32 matrix [rows][128] read in 32-column x 128-row boxes with the
+// 128-byte swizzle (16-byte chunk c of row r at chunk c ^ (r mod 8) of the row's 128 bytes)
+cudaError_t make_tmap_f32_32x128(TmaMap *map, const void *base, uint64_t rows);
 
 // Rows of the per-chunk gate factor table written by the UT transform kernel
 // (64 floats each, one per token t of the chunk, b(t) = t / 16 its 16-token block):
@@ -104,6 +107,7 @@ struct MergeArgs {
   float *S_init, *ht;
   int BH, nseg;
   int adjoint;
+  int *dev_flag;
 };
 cudaError_t launch_merge(const MergeArgs &a, cudaStream_t st);
 

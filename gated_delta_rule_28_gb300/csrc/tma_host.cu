@@ -46,4 +46,19 @@ cudaError_t make_tmap_bf16(TmaMap *map, const void *base, uint64_t cols, uint64_
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+cudaError_t make_tmap_f32_32x128(TmaMap *map, const void *base, uint64_t rows) {
+  auto fn = encoder();
+  if (!fn) return cudaErrorNotSupported;
+  if (!base || (reinterpret_cast<uintptr_t>(base) & 15u) || rows < 128) return cudaErrorInvalidValue;
+  const cuuint64_t dims[2] = {128, rows};
+  const cuuint64_t strides[1] = {128 * sizeof(float)};
+  const cuuint32_t box[2] = {32, 128};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = fn(reinterpret_cast<CUtensorMap *>(map), CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2,
+                        const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 }  // namespace gdn
