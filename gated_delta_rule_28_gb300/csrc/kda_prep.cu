@@ -27,6 +27,7 @@
 // every global load of an item (K, Q, V by cp.async, the gate column of each
 // thread) is issued at once, and one CTA's loads overlap the other's compute.
 #include <algorithm>
+#include <climits>
 
 #include "common.cuh"
 #include "kernels.h"
@@ -60,6 +61,8 @@ static_assert(64 * GS * 4 <= 34816 && (L_FLOATS + X_FLOATS + 4 * 256) * 4 <= 245
 constexpr float EXP_LIMIT = 100.f;
 
 struct __align__(16) Small {
+  uint64_t ldbar;  // the item's tile copies
+  uint64_t pad;
   float beta[64];
   float part[128];
   float eref[128];  // b^(G_r) per key channel
@@ -96,8 +99,15 @@ __device__ __forceinline__ void load_g8(const float *sG, int i, int c0, float (&
   g[0] = a.x; g[1] = a.y; g[2] = a.z; g[3] = a.w; g[4] = b.x; g[5] = b.y; g[6] = b.z; g[7] = b.w;
 }
 
+// TMA maps over k, q, v ([token rows][H * 128] bf16, 64 x 64 boxes); q and v only when given
+struct PrepMaps {
+  TmaMap k, q, v;
+};
+constexpr uint32_t WAIT_LIMIT = 1u << 22;
+
 template <bool E2>
-__global__ void __launch_bounds__(NTH, 2) kda_prep_kernel(KdaPrepArgs a, int64_t items) {
+__global__ void __launch_bounds__(NTH, 2) kda_prep_kernel(KdaPrepArgs a, int64_t items,
+                                                          const __grid_constant__ PrepMaps maps) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   float *sG = reinterpret_cast<float *>(sm + OFF_G);
@@ -108,13 +118,11 @@ __global__ void __launch_bounds__(NTH, 2) kda_prep_kernel(KdaPrepArgs a, int64_t
   const uint32_t sb = smem_u32(sm);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, H = a.H;
-  const __nv_bfloat16 *q = static_cast<const __nv_bfloat16 *>(a.q);
-  const __nv_bfloat16 *k = static_cast<const __nv_bfloat16 *>(a.k);
-  const __nv_bfloat16 *v = static_cast<const __nv_bfloat16 *>(a.v);
+  const void *v = a.v;
   const __nv_bfloat16 *beta = static_cast<const __nv_bfloat16 *>(a.beta);
   const int NT = (a.T + GDN_CHUNK - 1) / GDN_CHUNK;
   const float scale = a.scale;
-  const bool has_q = q != nullptr;
+  const bool has_q = a.q != nullptr;
   const int gq = lane >> 2, t4 = lane & 3;
 
   auto locate = [&](int64_t it, int64_t &r0, int &n) -> bool {
@@ -138,6 +146,14 @@ __global__ void __launch_bounds__(NTH, 2) kda_prep_kernel(KdaPrepArgs a, int64_t
   // the chain kernel launched after this one may be scheduled as SMs free up (it waits for
   // this grid's completion before it reads a blob)
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  uint32_t ldphase = 0;
+  if (tid == 0) {
+    mbar_init(&sv.ldbar, 1);
+    mbar_fence_init();
+  }
+  if (!v)  // no v: the V tile is zero for every item (u = 0)
+    for (int x = tid; x < 1024; x += NTH) *reinterpret_cast<uint4 *>(sm + OFF_V + 16 * x) = make_uint4(0, 0, 0, 0);
+  __syncthreads();
   for (int64_t it = blockIdx.x; it < items; it += gridDim.x) {
     int64_t r0 = 0;
     int n = 0;
@@ -149,17 +165,22 @@ __global__ void __launch_bounds__(NTH, 2) kda_prep_kernel(KdaPrepArgs a, int64_t
     uint8_t *blob = a.blob + (size_t)it * BLOB_BYTES;
     auto grow = [&](int i) { return ((r0 + i) * H + h) * (int64_t)GDN_DK; };  // token row, 128 wide
 
-    // ---- every load at once: K, Q, V tiles (zero past the end), the gate column, beta ----
-    for (int x = tid; x < 1024; x += NTH) {
-      const int r = x >> 4, c16 = x & 15;
-      const bool valid = r < n;
-      const int64_t row = (r0 + (valid ? r : 0)) * H + h;
-      const uint32_t o = (c16 >> 3) * 8192 + chunk_off(r, c16 & 7);
-      cp_async16(sb + OFF_K + o, k + row * GDN_DK + c16 * 8, valid ? 16u : 0u);
-      cp_async16(sb + OFF_Q + o, (has_q ? q : k) + row * GDN_DK + c16 * 8, valid && has_q ? 16u : 0u);
-      cp_async16(sb + OFF_V + o, (v ? v : k) + row * GDN_DV + c16 * 8, valid && v ? 16u : 0u);  // no v: u = 0
+    // ---- every load at once: K, Q, V tiles (two 64 x 64 TMA boxes each; rows past the end
+    // hold the tensor's next rows and are zeroed below), the gate column, beta ----
+    if (warp == 0) {
+      const int y = (int)r0, x0 = h * GDN_DK;
+      mbar_expect_tx_w(&sv.ldbar, 16384u * (1u + (has_q ? 1u : 0u) + (v ? 1u : 0u)));
+      tma_load_2d_w(sb + OFF_K, &maps.k, x0, y, &sv.ldbar);
+      tma_load_2d_w(sb + OFF_K + 8192, &maps.k, x0 + 64, y, &sv.ldbar);
+      if (has_q) {
+        tma_load_2d_w(sb + OFF_Q, &maps.q, x0, y, &sv.ldbar);
+        tma_load_2d_w(sb + OFF_Q + 8192, &maps.q, x0 + 64, y, &sv.ldbar);
+      }
+      if (v) {  // (no v: the V tile stays zero, u = 0)
+        tma_load_2d_w(sb + OFF_V, &maps.v, x0, y, &sv.ldbar);
+        tma_load_2d_w(sb + OFF_V + 8192, &maps.v, x0 + 64, y, &sv.ldbar);
+      }
     }
-    cp_async_commit();
     if (tid < 64) sv.beta[tid] = tid < n ? __bfloat162float(beta[(r0 + tid) * H + h]) : 0.f;
     const int d = tid & 127, half = tid >> 7;
     // gate element (row i, this thread's key channel): a scalar gate serves every channel
@@ -212,8 +233,24 @@ __global__ void __launch_bounds__(NTH, 2) kda_prep_kernel(KdaPrepArgs a, int64_t
       out_of_range = fmaxf(expo_to_base2<E2>(hi - gr), expo_to_base2<E2>(gr - lo)) > EXP_LIMIT;
     }
     const bool exact = __syncthreads_or(out_of_range);
-    cp_async_wait<0>();
-    __syncthreads();
+    const bool late = !mbar_wait(&sv.ldbar, ldphase, WAIT_LIMIT);
+    ldphase ^= 1u;
+    if (__syncthreads_or(late)) {  // the tiles did not arrive: report, let the copies land, stop
+      if (tid == 0) raise_device_flag(a.dev_flag, kDevTimeout);
+      mbar_wait(&sv.ldbar, ldphase ^ 1u, WAIT_LIMIT);
+      break;
+    }
+    if (n < 64) {  // rows past the chunk's end: zero K, Q, V
+      for (int x = tid; x < (64 - n) * 16; x += NTH) {
+        const int r = n + x / 16, c16 = x % 16;
+        const uint32_t o = (c16 >> 3) * 8192 + chunk_off(r, c16 & 7);
+        const uint4 z = make_uint4(0, 0, 0, 0);
+        *reinterpret_cast<uint4 *>(sm + OFF_K + o) = z;
+        *reinterpret_cast<uint4 *>(sm + OFF_Q + o) = z;
+        *reinterpret_cast<uint4 *>(sm + OFF_V + o) = z;
+      }
+      __syncthreads();
+    }
 
     if (exact) {  // Gram matrices term by term while K, Q and G are intact: L -> the Kb region
       float *sLx = reinterpret_cast<float *>(sm + OFF_KB);
@@ -425,6 +462,7 @@ __global__ void __launch_bounds__(NTH, 2) kda_prep_kernel(KdaPrepArgs a, int64_t
       bulk_store_w(blob + BLOB_U, sb + OFF_G, 16384);
       bulk_store_wait_read_w();
     }
+    fence_proxy_async();  // this item's reads of K, Q, V, before the next item's copies
     __syncthreads();  // shared memory is rewritten by the next item
   }
   if (warp == 0) bulk_store_wait_w();  // the blobs have reached global memory
@@ -443,8 +481,17 @@ cudaError_t launch_kda_prep(const KdaPrepArgs &a, int slots, cudaStream_t st) {
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, NTH, SMEM_BYTES);
   if (e != cudaSuccess) return e;
+  const int NT = (a.T + GDN_CHUNK - 1) / GDN_CHUNK;
+  const uint64_t rows = a.cu ? (uint64_t)a.T : (uint64_t)(slots / NT) * a.T;  // token rows
+  if (rows > (uint64_t)INT32_MAX) return cudaErrorInvalidValue;  // 32-bit TMA rows
+  const uint64_t pitch = (uint64_t)a.H * GDN_DK * 2;
+  PrepMaps maps{};
+  e = make_tmap_bf16(&maps.k, a.k, (uint64_t)a.H * GDN_DK, rows, pitch);
+  if (e == cudaSuccess && a.q) e = make_tmap_bf16(&maps.q, a.q, (uint64_t)a.H * GDN_DK, rows, pitch);
+  if (e == cudaSuccess && a.v) e = make_tmap_bf16(&maps.v, a.v, (uint64_t)a.H * GDN_DV, rows, (uint64_t)a.H * GDN_DV * 2);
+  if (e != cudaSuccess) return e;
   const int64_t grid = std::min<int64_t>(items, (int64_t)std::max(1, sms * std::max(1, per_sm)));
-  kern<<<(unsigned)grid, NTH, SMEM_BYTES, st>>>(a, items);
+  kern<<<(unsigned)grid, NTH, SMEM_BYTES, st>>>(a, items, maps);
   return cudaGetLastError();
 }
 
