@@ -587,9 +587,9 @@ gdn_status gdn_chunk_bwd(const gdn_problem *pin, const void *q, const void *k, c
                                               f.scale, flag);
     if ((e = gdn::launch_kda_prep(pa, (int)n_chunk_slots(p), s)) != cudaSuccess) return cuda_fail(e, "KDA prep launch");
     e = gdn::launch_kda_chain(kda_chain_args(f, xw), dim3(2, p->H, runs), s);
-  } else if (use_tensor_cores(p)) {  // X recomputed from the saved cumulative gate (same values as A)
+  } else if (use_tensor_cores(p)) {  // the X pair and gate tables from the saved A and cumulative gate
     const gdn::UtArgs u = ut_args(p, k, nullptr, g_cumsum, beta, xw, nullptr, nullptr, flag);
-    if ((e = gdn::launch_ut(u, (int)n_chunk_slots(p), s)) != cudaSuccess) return cuda_fail(e, "UT transform launch");
+    if ((e = gdn::launch_ut_pair(u, A, (int)n_chunk_slots(p), s)) != cudaSuccess) return cuda_fail(e, "X pair launch");
     f.xw = u.xw;
     f.ftab = u.ftab;
     e = gdn::launch_tc_fwd_ws(f, dim3(GDN_DV / gdn::tc_fwd_ws_bv(), p->H, runs), s);
@@ -815,7 +815,7 @@ gdn_status kda_segment_summary_bwd(const gdn_problem *pin, const void *q, const 
   cudaError_t e;
   if (use_tensor_cores(p)) {
     const gdn::UtArgs u = ut_args(p, k, nullptr, g_cumsum, beta, w + L.xw, nullptr, nullptr, b.dev_flag);
-    if ((e = gdn::launch_ut(u, (int)n_chunk_slots(p), s)) != cudaSuccess) return cuda_fail(e, "UT transform launch");
+    if ((e = gdn::launch_ut_pair(u, A, (int)n_chunk_slots(p), s)) != cudaSuccess) return cuda_fail(e, "X pair launch");
     b.xw = u.xw;
     b.ftab = u.ftab;
     e = gdn::launch_tc_dhu(b, p->B * nseg, s);

@@ -92,6 +92,9 @@ struct UtArgs {
   int *dev_flag;
 };
 cudaError_t launch_ut(const UtArgs &a, int slots, cudaStream_t st);
+// The same X pair and gate tables from a saved X (the forward's A slot, fp32 [rows, H, 64]) and
+// the saved cumulative gate (a.g_cum_in): the backward's recompute, without a second solve
+cudaError_t launch_ut_pair(const UtArgs &a, const float *A, int slots, cudaStream_t st);
 
 // tcgen05 chunk forward with the state recurrence overlapped with the next
 // chunk's preparation; reads X from a.xw (launch_ut first)

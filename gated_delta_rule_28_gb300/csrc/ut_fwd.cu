@@ -286,7 +286,92 @@ __global__ void __launch_bounds__(128, 6) ut_kernel(UtArgs a, int64_t items, con
   if (warp == 0) bulk_store_wait_w();  // the X pairs have reached global memory
 }
 
+// The backward's X pair and gate tables from the forward's A slot (X, fp32) instead of a
+// second UT transform: the same values the UT kernel forms, bit for bit (X rows past the
+// chunk's end are identity rows there, so those pair rows are zero). One CTA per item.
+template <bool E2>
+__global__ void __launch_bounds__(256) ut_pair_kernel(UtArgs a, const float *__restrict__ A) {
+  __shared__ __align__(16) float sG[64], sbeta[64], sBEG[64], sEA[64], sEB[3][64];
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  const int tid = threadIdx.x, H = a.H;
+  const __nv_bfloat16 *beta = static_cast<const __nv_bfloat16 *>(a.beta);
+  const uint32_t u = blockIdx.x, slot = u / (uint32_t)H;
+  const int h = (int)(u - slot * (uint32_t)H);
+  int64_t r0, r1;
+  if (a.cu) {
+    const int seq = a.chunk_indices[2 * slot], cc = a.chunk_indices[2 * slot + 1];
+    const bool ok = seq >= 0 && seq < a.num_seqs && cc >= 0 && (r0 = (int64_t)a.cu[seq] + (int64_t)cc * GDN_CHUNK,
+                                                                r1 = a.cu[seq + 1], r0 >= 0 && r0 < r1 && r1 <= a.T);
+    if (!ok) {
+      if (tid == 0) raise_device_flag(a.dev_flag, kDevCheck);
+      return;
+    }
+  } else {
+    const int NT = (a.T + GDN_CHUNK - 1) / GDN_CHUNK;
+    const uint32_t b = slot / (uint32_t)NT, c = slot - b * (uint32_t)NT;
+    r0 = (int64_t)b * a.T + (int64_t)c * GDN_CHUNK;
+    r1 = (int64_t)b * a.T + a.T;
+  }
+  const int n = (int)min((int64_t)GDN_CHUNK, r1 - r0);
+  if (tid < 64) {
+    sG[tid] = a.g_cum_in[(r0 + min(tid, n - 1)) * H + h];
+    sbeta[tid] = tid < n ? __bfloat162float(beta[(r0 + tid) * H + h]) : 0.f;
+  }
+  __syncthreads();
+  if (tid < 64) {
+    sEA[tid] = gexp<E2>(sG[tid] - sG[tid & ~15]);
+    sBEG[tid] = sbeta[tid] * gexp<E2>(sG[tid]);
+  }
+  if (tid < 192) {
+    const int bb = 1 + (tid >> 6), s2 = tid & 63;
+    sEB[bb - 1][s2] = s2 < 16 * bb ? gexp<E2>(sG[16 * bb] - sG[s2]) : 0.f;
+  }
+  __syncthreads();
+  // pair rows r and r + 32 (and 64 + those), columns 8 c .. 8 c + 7: 128-byte rows per 8 lanes
+  const int r = tid >> 3, c = tid & 7;
+  __nv_bfloat16 *xw = a.xw + (int64_t)u * 2 * GDN_CHUNK * GDN_CHUNK;
+#pragma unroll
+  for (int rr = r; rr < 64; rr += 32) {
+    float x[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    if (rr < n) {
+      const float4 *src = reinterpret_cast<const float4 *>(A + ((r0 + rr) * H + h) * GDN_CHUNK + 8 * c);
+      const float4 x0 = __ldg(src), x1 = __ldg(src + 1);
+      x[0] = x0.x; x[1] = x0.y; x[2] = x0.z; x[3] = x0.w; x[4] = x1.x; x[5] = x1.y; x[6] = x1.z; x[7] = x1.w;
+    }
+    float s0[8], s1[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      s0[e] = x[e] * sbeta[8 * c + e];
+      s1[e] = x[e] * sBEG[8 * c + e];
+    }
+    *reinterpret_cast<uint4 *>(xw + rr * GDN_CHUNK + 8 * c) = pack8(s0);
+    *reinterpret_cast<uint4 *>(xw + (GDN_CHUNK + rr) * GDN_CHUNK + 8 * c) = pack8(s1);
+  }
+  if (tid < 64) {  // the gate table, as the UT kernel writes it
+    float *tab = a.ftab + (int64_t)u * F_TAB;
+    const float G = sG[tid], eg = gexp<E2>(G), bt = sbeta[tid];
+    tab[F_G * 64 + tid] = G;
+    tab[F_EG * 64 + tid] = eg;
+    tab[F_EGL * 64 + tid] = gexp<E2>(sG[63] - G);
+    tab[F_BEG * 64 + tid] = bt * eg;
+    tab[F_BETA * 64 + tid] = bt;
+    tab[F_EA * 64 + tid] = sEA[tid];
+    tab[F_EB1 * 64 + tid] = sEB[0][tid];
+    tab[F_EB2 * 64 + tid] = sEB[1][tid];
+    tab[F_EB3 * 64 + tid] = sEB[2][tid];
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_ut_pair(const UtArgs &a, const float *A, int slots, cudaStream_t st) {
+  if (slots <= 0) return cudaSuccess;
+  const int64_t items = (int64_t)slots * a.H;
+  if (items > INT32_MAX || !a.g_cum_in) return cudaErrorInvalidValue;
+  auto kern = a.use_exp2 ? ut_pair_kernel<true> : ut_pair_kernel<false>;
+  kern<<<(unsigned)items, 256, 0, st>>>(a, A);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_ut(const UtArgs &a, int slots, cudaStream_t st) {
   if (slots <= 0) return cudaSuccess;
