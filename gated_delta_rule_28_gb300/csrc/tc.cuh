@@ -203,10 +203,12 @@ __device__ __forceinline__ void mma4_w(uint32_t d_tmem, uint32_t alo, uint32_t b
 __device__ __forceinline__ uint32_t sdesc_lo(Opnd X) {
   return ((X.addr & 0x3FFFFu) >> 4) | ((X.mn ? ((X.step >> 4) & 0x3FFFu) : 1u) << 16);
 }
-// D (+)= A B^T over K (a multiple of 64) in groups of four MMAs; operands as mma_ops_w
+// D (+)= A B^T over K (a multiple of 64) in groups of four MMAs; operands as mma_ops_w. The
+// loop over the groups stays rolled: one copy of the issue code per call site (the issuing
+// warps' loops run from the instruction cache, and this is most of their code)
 __device__ __forceinline__ void mma_grp_w(uint32_t d_tmem, Opnd A, Opnd B, int K, uint32_t idesc, bool accumulate) {
   const uint32_t a0 = sdesc_lo(A), b0 = sdesc_lo(B);
-#pragma unroll
+#pragma unroll 1
   for (int g = 0; g < K / 64; ++g) {
     // K block g: K-major operands move to the next 64-wide block (`step` bytes), MN-major
     // ones by 4 x 2048 bytes
