@@ -36,23 +36,28 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-// Persistent: each CTA walks the (chunk, head) items with a stride of the grid (six CTAs per
-// SM: one key buffer each), prefetching the next item's gate and beta into registers.
+// Persistent: each CTA walks the (chunk, head) items with a stride of the grid (eight CTAs per
+// SM: one key buffer each, 27 KB of shared memory), prefetching the next item's gate and beta
+// into registers.
 // TMA map over the X pairs: [slots * H * 128 rows][64] bf16, 64 x 64 boxes
 struct UtMaps {
   TmaMap x;
 };
 
 template <bool E2>
-__global__ void __launch_bounds__(128, 6) ut_kernel(UtArgs a, int64_t items, const __grid_constant__ UtMaps maps) {
+__global__ void __launch_bounds__(128, 8) ut_kernel(UtArgs a, int64_t items, const __grid_constant__ UtMaps maps) {
   __shared__ __align__(1024) uint8_t kbuf[1][16384];  // keys (64 rows x 2 K-blocks, swizzled);
                                                       // after K K^T it holds L's blocks
-  __shared__ __align__(16) float XB[10 * 256], TB[4 * 256];
+  __shared__ __align__(16) float XB[10 * 256];
+  // the solve's scratch: the last 6 KB of the key buffer, which L (10 blocks, 10 KB) leaves free
+  float *TB = reinterpret_cast<float *>(kbuf[0] + 10 * 256 * 4);
   __shared__ __align__(16) float sg[64];
   __shared__ __align__(16) float sG[64];
   __shared__ __align__(16) float sbeta[64];
-  __shared__ __align__(16) float sEA[64], sEB[3][64];  // block-factorised gate (rows F_EA, F_EB1..)
   __shared__ __align__(16) float sBEG[64];              // beta base^G (column factor of X diag(b e^G))
+  // the block-factorised gate (rows F_EA, F_EB1..) while L is formed, in the solve's scratch
+  float *sEA = TB;
+  float(*sEB)[64] = reinterpret_cast<float(*)[64]>(TB + 64);
 
   // the state kernel launched after this one may be scheduled as SMs free up (it waits for
   // this grid's completion before it reads anything written here)
@@ -274,10 +279,9 @@ __global__ void __launch_bounds__(128, 6) ut_kernel(UtArgs a, int64_t items, con
       tab[F_EGL * 64 + tid] = gexp<E2>(sG[63] - G);
       tab[F_BEG * 64 + tid] = bt * eg;
       tab[F_BETA * 64 + tid] = bt;
-      tab[F_EA * 64 + tid] = sEA[tid];
-      tab[F_EB1 * 64 + tid] = sEB[0][tid];
-      tab[F_EB2 * 64 + tid] = sEB[1][tid];
-      tab[F_EB3 * 64 + tid] = sEB[2][tid];
+      tab[F_EA * 64 + tid] = gexp<E2>(G - sG[tid & ~15]);  // recomputed: the solve reused their space
+#pragma unroll
+      for (int bb = 1; bb <= 3; ++bb) tab[(F_EB1 + bb - 1) * 64 + tid] = tid < 16 * bb ? gexp<E2>(sG[16 * bb] - G) : 0.f;
     }
     if (warp == 0) bulk_store_wait_read_w();  // the key buffer takes the next item's keys
     __syncthreads();  // sG, sbeta and the X blocks are rewritten by the next item
