@@ -317,6 +317,17 @@ __global__ void __launch_bounds__(256) ut_pair_kernel(UtArgs a, const float *__r
     r1 = (int64_t)b * a.T + a.T;
   }
   const int n = (int)min((int64_t)GDN_CHUNK, r1 - r0);
+  // this thread's X values (rows r and r + 32, columns 8 c .. 8 c + 7), issued before the gate
+  // and beta loads so that the two wait together
+  const int r = tid >> 3, c = tid & 7;
+  float4 xv[2][2];
+#pragma unroll
+  for (int k2 = 0; k2 < 2; ++k2) {
+    const int rr = r + 32 * k2;
+    const float4 *src = reinterpret_cast<const float4 *>(A + ((r0 + min(rr, n - 1)) * H + h) * GDN_CHUNK + 8 * c);
+    xv[k2][0] = rr < n ? __ldg(src) : make_float4(0.f, 0.f, 0.f, 0.f);
+    xv[k2][1] = rr < n ? __ldg(src + 1) : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
   if (tid < 64) {
     sG[tid] = a.g_cum_in[(r0 + min(tid, n - 1)) * H + h];
     sbeta[tid] = tid < n ? __bfloat162float(beta[(r0 + tid) * H + h]) : 0.f;
@@ -332,16 +343,12 @@ __global__ void __launch_bounds__(256) ut_pair_kernel(UtArgs a, const float *__r
   }
   __syncthreads();
   // pair rows r and r + 32 (and 64 + those), columns 8 c .. 8 c + 7: 128-byte rows per 8 lanes
-  const int r = tid >> 3, c = tid & 7;
   __nv_bfloat16 *xw = a.xw + (int64_t)u * 2 * GDN_CHUNK * GDN_CHUNK;
 #pragma unroll
-  for (int rr = r; rr < 64; rr += 32) {
-    float x[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    if (rr < n) {
-      const float4 *src = reinterpret_cast<const float4 *>(A + ((r0 + rr) * H + h) * GDN_CHUNK + 8 * c);
-      const float4 x0 = __ldg(src), x1 = __ldg(src + 1);
-      x[0] = x0.x; x[1] = x0.y; x[2] = x0.z; x[3] = x0.w; x[4] = x1.x; x[5] = x1.y; x[6] = x1.z; x[7] = x1.w;
-    }
+  for (int k2 = 0; k2 < 2; ++k2) {
+    const int rr = r + 32 * k2;
+    const float x[8] = {xv[k2][0].x, xv[k2][0].y, xv[k2][0].z, xv[k2][0].w,
+                        xv[k2][1].x, xv[k2][1].y, xv[k2][1].z, xv[k2][1].w};
     float s0[8], s1[8];
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
