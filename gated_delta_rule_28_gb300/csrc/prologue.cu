@@ -12,8 +12,9 @@
 //
 // Memory-bound elementwise work: half a warp per row, each lane eight consecutive
 // elements (one 16-byte bf16 or two 16-byte fp32 vectors), the row sum by shuffles
-// inside the half warp; a warp takes eight rows per pass and issues all of their
-// loads before the first sum, so that 128 bytes per lane (bf16) are in flight;
+// inside the half warp; a warp takes eight rows per pass (four in the backward's
+// map, which reads two tensors per row) and issues all of their loads before the
+// first sum, so that 64 bytes per lane (bf16) are in flight;
 // grid-stride over the passes with a grid of whole waves of the SMs. The norm is
 // computed in fp32 from the stored inputs (the backward recomputes it from the raw
 // rows rather than reading a saved rstd).
@@ -27,7 +28,8 @@ namespace {
 
 constexpr int PRO_THREADS = 256;
 constexpr float L2_EPS = 1e-6f;
-constexpr int RPW = 8;  // rows per warp and pass: two half warps x 4
+constexpr int RPW = 8;      // rows per warp and pass: two half warps x 4
+constexpr int RPW_BWD = 4;  // the same for the backward's map (two inputs per row: fewer registers)
 
 // eight consecutive elements of a row (16-byte aligned: rows are 128 elements)
 template <typename T>
@@ -128,12 +130,12 @@ __global__ void __launch_bounds__(PRO_THREADS) epilogue_bwd_kernel(InputMapArgs 
   T *dq = static_cast<T *>(a.dq), *dk = static_cast<T *>(a.dk);
   if (a.l2norm) {
     const int64_t nrows = 2 * a.rows;
-    for (int64_t b = w0; b * RPW < nrows; b += warps) {
-      float x[4][8], d[4][8];
-      bool on[4];
+    for (int64_t b = w0; b * RPW_BWD < nrows; b += warps) {
+      float x[RPW_BWD / 2][8], d[RPW_BWD / 2][8];
+      bool on[RPW_BWD / 2];
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {  // every load of the pass first
-        const int64_t r = b * RPW + 2 * u + half;
+      for (int u = 0; u < RPW_BWD / 2; ++u) {  // every load of the pass first
+        const int64_t r = b * RPW_BWD + 2 * u + half;
         const bool isq = r < a.rows;
         on[u] = r < nrows;  // (half-warp uniform)
         if (on[u]) {
@@ -143,7 +145,7 @@ __global__ void __launch_bounds__(PRO_THREADS) epilogue_bwd_kernel(InputMapArgs 
         }
       }
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
+      for (int u = 0; u < RPW_BWD / 2; ++u) {
         float ss = 0.f;
 #pragma unroll
         for (int i = 0; i < 8; ++i) ss = on[u] ? fmaf(x[u][i], x[u][i], ss) : 0.f;
@@ -155,7 +157,7 @@ __global__ void __launch_bounds__(PRO_THREADS) epilogue_bwd_kernel(InputMapArgs 
         for (int i = 0; i < 8; ++i) dt = on[u] ? fmaf(x[u][i], d[u][i], dt) : 0.f;
         const float dot = half_sum(dt);
         if (on[u]) {
-          const int64_t r = b * RPW + 2 * u + half;
+          const int64_t r = b * RPW_BWD + 2 * u + half;
           const bool isq = r < a.rows;
 #pragma unroll
           for (int i = 0; i < 8; ++i) d[u][i] = rstd * (d[u][i] - x[u][i] * dot);
@@ -183,7 +185,8 @@ cudaError_t launch_pair(const InputMapArgs &a, bool bwd, cudaStream_t st) {
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
   // eight resident CTAs of 8 warps per SM, capped by the work (eight rows per warp and pass)
-  const int64_t passes = (2 * a.rows + RPW - 1) / RPW;
+  const int rpw = bwd ? RPW_BWD : RPW;
+  const int64_t passes = (2 * a.rows + rpw - 1) / rpw;
   const int64_t need = (passes + PRO_THREADS / 32 - 1) / (PRO_THREADS / 32);
   const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(need, (int64_t)sms * 8));
   if (bwd)
