@@ -175,9 +175,10 @@ gdn_status gdn_chunk_bwd_workspace(const gdn_problem *p, size_t *bytes);
  * g_cumsum, beta and A, the output gradient and scale; first five result
  * slots dq, dk, dv, dbeta, dg). All pointers device.
  *   q, k, v, beta : forward inputs.
- *   g_cumsum, A   : the forward's saved slots (fp32). The state recompute and
- *                   the local gradients take X from A (no second solve), so A
- *                   must be the forward's own, for the same k, beta, g.
+ *   g_cumsum, A   : the forward's saved slots (fp32). The local gradients, and
+ *                   the state recompute of a scalar gate, take X from A (no
+ *                   second solve), so A must be the forward's own, for the
+ *                   same k, beta and g.
  *   dO            : output gradient, layout of v.
  *   h0            : nullable fp32 [N, H, K, V] initial state of the forward.
  *   dht           : nullable fp32 [N, H, K, V] gradient of the final state.
